@@ -1,0 +1,170 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) chunked Gated DeltaNet training path.
+ *
+ * The operation (one value head h, one document, state reset to zero at the
+ * document start, q/k head j = h / (HV/H)):
+ *
+ *     S_t = a_t S_{t-1} + beta_t k^_t (v_t - a_t S_{t-1}^T k^_t)^T,   a_t = exp(g_t)
+ *     o_t = scale * S_t^T q^_t
+ *
+ * with q^, k^ the L2-normalised q, k (x / sqrt(x.x + 1e-6)) when l2norm != 0,
+ * else q, k as given; S is a dk x dv matrix kept in FP32.  This is the gated
+ * delta rule that the flashinfer Cake GDN training pages run: "packed GDN
+ * layers" over variable-length documents with head dim 128, BF16 q/k/v and
+ * output gradient, FP32 g and beta, grouped heads (H query/key heads, HV value
+ * heads), optional in-kernel q/k L2 norm, chunk states every 64 tokens
+ * ("feat(cake_gdn_kcp): ... Cake GDN chunked autograd backend - #8172" page,
+ * its #8181 section; "#8542" page, the opening description and the save-set
+ * table).  The backward returns the gradients of sum(o * dO) with respect to
+ * q, k, v, g and beta.
+ *
+ * Conventions (all entry points):
+ *   - Sizes: dk = dv = 128, HV % H == 0, T = cu_seqlens[N], chunk = 64.
+ *   - Layouts, all contiguous and token-major:
+ *       q, k, dq, dk      [T][H][128]   BF16
+ *       v, dO, o, dv      [T][HV][128]  BF16
+ *       g, beta, dg, dbeta [T][HV]      FP32
+ *       cu_seqlens        [N+1]         int32, 0 = cu[0] <= cu[1] <= ... <= cu[N] = T
+ *     Device pointers must be 16-byte aligned.
+ *   - cu_seqlens is passed twice: the host copy drives planning (chunk counts,
+ *     segment plan, buffer sizes) and the device copy drives the kernels.  The
+ *     two must hold the same values.
+ *   - Ownership: the caller allocates and owns every buffer (inputs, outputs,
+ *     `saved`, `workspace`).  The library allocates no device memory, keeps no
+ *     per-call global state, and launches everything asynchronously on
+ *     `stream` in stream order; it never synchronises the host except in
+ *     gdn_device_status().  Calls on different streams must use different
+ *     workspaces.
+ *   - Errors are returned, never thrown.  Host-side checks (null pointers,
+ *     sizes, cu_seqlens, alignment, buffer sizes) return before any launch.
+ *     Conditions only the device can see (a saved buffer whose header does
+ *     not match the call, a bounded wait that ran out) are written to an
+ *     error word in the workspace; later kernels of the same call then skip
+ *     their work, and gdn_device_status() reports the word.
+ *   - Results are bitwise reproducible run to run for a fixed problem and plan
+ *     (every reduction has a fixed order).
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t */
+
+typedef struct {
+    int64_t T;        /* total packed tokens (= cu_seqlens[N]) */
+    int32_t N;        /* number of documents (>= 1; empty documents allowed) */
+    int32_t H;        /* query/key heads */
+    int32_t HV;       /* value heads, a multiple of H */
+    int32_t dk;       /* must be 128 */
+    int32_t dv;       /* must be 128 */
+    float scale;      /* output scale (typically dk^-0.5) */
+    int32_t l2norm;   /* non-zero: L2-normalise q and k inside the kernels */
+    int32_t segments; /* 0: the planner chooses the segment split;
+                         > 0: split the longest document into `segments`
+                         segments (see gdn_plan_segment_chunks()) */
+} gdn_problem;
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,        /* null pointer, bad size, bad cu_seqlens, misalignment */
+    GDN_ERR_UNSUPPORTED = 2,        /* dk or dv != 128, HV % H != 0 */
+    GDN_ERR_WORKSPACE_TOO_SMALL = 3,/* ws_bytes below the gdn_saved_bytes() figure */
+    GDN_ERR_SAVED_MISMATCH = 4,     /* device-side: `saved` was not written by a forward of this problem */
+    GDN_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed */
+    GDN_ERR_TIMEOUT = 6,            /* device-side: a bounded wait ran out */
+    GDN_ERR_DEVICE = 7              /* device-side: any other kernel-detected fault */
+} gdn_status;
+
+/*
+ * Byte sizes of the caller-owned buffers for this problem.
+ *   saved_bytes      the set gdn_fwd() writes for gdn_bwd(): a 4 KiB header,
+ *                    the BF16 state entering every 64-token chunk of every
+ *                    value head (32 KiB per chunk and value head; the pages'
+ *                    "h tape" of states every 64 tokens), and, where a
+ *                    document is split into P > 1 segments, the FP32 segment
+ *                    transfer plane M_seg (P x HV x 64 KiB per document) that
+ *                    the backward's merges read ("#8542" page: the full saved
+ *                    set keeps M_seg at P > 1).
+ *   workspace_bytes  scratch for one gdn_fwd / gdn_bwd / gdn_ckpt_fwd_bwd call.
+ * Returns GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED on a bad problem.
+ */
+gdn_status gdn_saved_bytes(const gdn_problem *prob, const int32_t *cu_seqlens_host,
+                           size_t *saved_bytes, size_t *workspace_bytes);
+
+/*
+ * Forward.  Writes o.  If `saved` is non-null it also writes the saved set
+ * (header + state tape [+ M_seg]) that gdn_bwd() consumes; with saved == NULL
+ * no state is stored (the forward of a checkpointed step).
+ */
+gdn_status gdn_fwd(const gdn_problem *prob, const void *q, const void *k, const void *v,
+                   const float *g, const float *beta, const int32_t *cu_seqlens_dev,
+                   const int32_t *cu_seqlens_host, void *o, void *saved, void *workspace,
+                   size_t ws_bytes, struct CUstream_st *stream);
+
+/*
+ * Backward.  Given dO and the saved set of a gdn_fwd() of the same problem and
+ * inputs, writes dq, dk, dv (BF16) and dg, dbeta (FP32).  Every output element
+ * is written (no accumulation into the caller's buffers).  A saved set whose
+ * header does not match the problem sets GDN_ERR_SAVED_MISMATCH on the device
+ * (see gdn_device_status) and leaves the gradients unwritten.
+ */
+gdn_status gdn_bwd(const gdn_problem *prob, const void *q, const void *k, const void *v,
+                   const float *g, const float *beta, const int32_t *cu_seqlens_dev,
+                   const int32_t *cu_seqlens_host, const void *dO, const void *saved,
+                   void *dq, void *dk, void *dv, float *dg, float *dbeta, void *workspace,
+                   size_t ws_bytes, struct CUstream_st *stream);
+
+/*
+ * Activation-checkpointed step: a forward that keeps no states and writes o,
+ * then a forward that writes the saved set into `saved_scratch` (saved_bytes
+ * large), then the backward.  This is the pages' "ckpt" operation, two
+ * forwards plus one backward.  With o == NULL the first forward, which would
+ * produce nothing, is skipped.
+ */
+gdn_status gdn_ckpt_fwd_bwd(const gdn_problem *prob, const void *q, const void *k,
+                            const void *v, const float *g, const float *beta,
+                            const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host,
+                            const void *dO, void *o, void *dq, void *dk, void *dv, float *dg,
+                            float *dbeta, void *saved_scratch, void *workspace,
+                            size_t ws_bytes, struct CUstream_st *stream);
+
+/* Static description of a status code. */
+const char *gdn_status_string(gdn_status s);
+
+/*
+ * Synchronises `stream`, then returns the device-side error word of the last
+ * call that used `workspace` (GDN_OK if none), or GDN_ERR_CUDA if the stream
+ * reports a CUDA error.
+ */
+gdn_status gdn_device_status(void *workspace, struct CUstream_st *stream);
+
+/*
+ * Introspection for tests and tools: byte offsets, into the workspace, of the
+ * chunk tables every call builds from cu_seqlens (int32 arrays:
+ * offsets[0] -> chunk_offsets[N+1], the index of each document's first chunk;
+ * offsets[1] -> chunk_doc[NC]; offsets[2] -> chunk_tok0[NC], first token of
+ * each chunk; offsets[3] -> chunk_len[NC], 1..64 tokens), and NC.
+ */
+gdn_status gdn_chunk_table_offsets(const gdn_problem *prob, const int32_t *cu_seqlens_host,
+                                   size_t offsets[4], int32_t *num_chunks);
+
+/*
+ * The segment length (in 64-token chunks) the planner uses for this problem:
+ * documents longer than this are split into ceil(chunks / seg) segments whose
+ * transfer operators are composed by a merge kernel (the intra-GPU segment
+ * split).  With prob->segments > 0 the answer is ceil(max_doc_chunks /
+ * prob->segments), i.e. the longest document gets `segments` segments.
+ * Returns 0 on an invalid problem.
+ */
+int32_t gdn_plan_segment_chunks(const gdn_problem *prob, const int32_t *cu_seqlens_host);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_H_ */

@@ -1,0 +1,183 @@
+"""Python binding of libgdn, the sm_103a chunked Gated DeltaNet training path.
+
+The functions below carry the C ABI's names (include/gdn.h) and only marshal
+arguments: torch tensors become device pointers, host arrays become host
+pointers, a non-OK status raises GDNError.  Every step of the path runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback, and importing
+this package fails if the compiled library is missing (build it with
+``python -m linear_attention_gdn_gb300.build`` or ``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+LIB_PATH = _build.LIB
+STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_WORKSPACE_TOO_SMALL",
+          4: "GDN_ERR_SAVED_MISMATCH", 5: "GDN_ERR_CUDA", 6: "GDN_ERR_TIMEOUT", 7: "GDN_ERR_DEVICE"}
+EXPORTS = ("gdn_saved_bytes", "gdn_fwd", "gdn_bwd", "gdn_ckpt_fwd_bwd", "gdn_status_string",
+           "gdn_device_status", "gdn_plan_segment_chunks", "gdn_chunk_table_offsets")
+
+
+class GDNError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({gdn_status_string(status)})")
+
+
+class gdn_problem(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("N", ctypes.c_int32), ("H", ctypes.c_int32), ("HV", ctypes.c_int32),
+                ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("l2norm", ctypes.c_int32), ("segments", ctypes.c_int32)]
+
+
+def problem(T, N, H, HV, scale=128 ** -0.5, l2norm=True, segments=0, dk=128, dv=128) -> gdn_problem:
+    return gdn_problem(int(T), int(N), int(H), int(HV), int(dk), int(dv), float(scale), int(bool(l2norm)),
+                       int(segments))
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libgdn.so not built ({LIB_PATH}); run linear_attention_gdn_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, sz, i32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(ctypes.c_int32)
+    pp = ctypes.POINTER(gdn_problem)
+    L.gdn_saved_bytes.argtypes = [pp, i32p, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    L.gdn_fwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, sz, vp]
+    L.gdn_bwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.gdn_ckpt_fwd_bwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.gdn_status_string.argtypes = [ctypes.c_int]
+    L.gdn_status_string.restype = ctypes.c_char_p
+    L.gdn_device_status.argtypes = [vp, vp]
+    L.gdn_plan_segment_chunks.argtypes = [pp, i32p]
+    L.gdn_plan_segment_chunks.restype = ctypes.c_int32
+    L.gdn_chunk_table_offsets.argtypes = [pp, i32p, ctypes.POINTER(sz), i32p]
+    for name in ("gdn_saved_bytes", "gdn_fwd", "gdn_bwd", "gdn_ckpt_fwd_bwd", "gdn_device_status",
+                 "gdn_chunk_table_offsets"):
+        getattr(L, name).restype = ctypes.c_int
+    return L
+
+
+class _Lazy:
+    """The library handle, loaded on first use (importing the package must not
+    require the library, so that the build step can import it)."""
+    _h = None
+
+    def __getattr__(self, name):
+        if _Lazy._h is None:
+            _Lazy._h = _load()
+        return getattr(_Lazy._h, name)
+
+
+lib = _Lazy()
+
+
+def load():
+    """Load libgdn.so now and check that it exports every ABI symbol."""
+    for name in EXPORTS:
+        getattr(lib, name)
+    return lib
+
+
+def _ptr(x):
+    """Device/host address of a tensor or array; None -> NULL."""
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return ctypes.c_void_p(x.data_ptr())
+    if isinstance(x, np.ndarray):
+        return ctypes.c_void_p(x.ctypes.data)
+    return ctypes.c_void_p(int(x))
+
+
+def _cu_host(cu):
+    a = np.ascontiguousarray(np.asarray(cu, dtype=np.int32))
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(st, where):
+    if st != 0:
+        raise GDNError(st, where)
+
+
+def gdn_status_string(status: int) -> str:
+    return lib.gdn_status_string(int(status)).decode()
+
+
+def gdn_saved_bytes(prob: gdn_problem, cu_seqlens_host):
+    cu, cup = _cu_host(cu_seqlens_host)
+    s, w = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(lib.gdn_saved_bytes(ctypes.byref(prob), cup, ctypes.byref(s), ctypes.byref(w)), "gdn_saved_bytes")
+    return s.value, w.value
+
+
+def gdn_plan_segment_chunks(prob: gdn_problem, cu_seqlens_host) -> int:
+    cu, cup = _cu_host(cu_seqlens_host)
+    return int(lib.gdn_plan_segment_chunks(ctypes.byref(prob), cup))
+
+
+def gdn_chunk_table_offsets(prob: gdn_problem, cu_seqlens_host):
+    cu, cup = _cu_host(cu_seqlens_host)
+    offs = (ctypes.c_size_t * 4)()
+    nc = ctypes.c_int32(0)
+    _check(lib.gdn_chunk_table_offsets(ctypes.byref(prob), cup, offs, ctypes.byref(nc)), "gdn_chunk_table_offsets")
+    return list(offs), nc.value
+
+
+def gdn_fwd(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, o, saved, workspace, ws_bytes=None,
+            stream=None):
+    cu, cup = _cu_host(cu_seqlens_host)
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
+    _check(lib.gdn_fwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                       ctypes.cast(_ptr(cu_seqlens_dev), ctypes.POINTER(ctypes.c_int32)), cup, _ptr(o),
+                       _ptr(saved), _ptr(workspace), ws_bytes, _stream(stream)), "gdn_fwd")
+
+
+def gdn_bwd(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, dO, saved, dq, dk, dv, dg, dbeta,
+            workspace, ws_bytes=None, stream=None):
+    cu, cup = _cu_host(cu_seqlens_host)
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
+    _check(lib.gdn_bwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                       ctypes.cast(_ptr(cu_seqlens_dev), ctypes.POINTER(ctypes.c_int32)), cup, _ptr(dO),
+                       _ptr(saved), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(workspace),
+                       ws_bytes, _stream(stream)), "gdn_bwd")
+
+
+def gdn_ckpt_fwd_bwd(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, dO, o, dq, dk, dv, dg, dbeta,
+                     saved_scratch, workspace, ws_bytes=None, stream=None):
+    cu, cup = _cu_host(cu_seqlens_host)
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
+    _check(lib.gdn_ckpt_fwd_bwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                ctypes.cast(_ptr(cu_seqlens_dev), ctypes.POINTER(ctypes.c_int32)), cup, _ptr(dO),
+                                _ptr(o), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(saved_scratch),
+                                _ptr(workspace), ws_bytes, _stream(stream)), "gdn_ckpt_fwd_bwd")
+
+
+def gdn_device_status(workspace, stream=None) -> int:
+    return int(lib.gdn_device_status(_ptr(workspace), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# allocation helpers (torch owns the memory; the library allocates nothing)
+# ---------------------------------------------------------------------------
+class Buffers:
+    """Caller-side saved set and workspace for one problem, allocated with torch."""
+
+    def __init__(self, prob: gdn_problem, cu_seqlens_host, device="cuda", fill=None):
+        import torch
+        self.saved_bytes, self.ws_bytes = gdn_saved_bytes(prob, cu_seqlens_host)
+        mk = (lambda n: torch.full((max(n, 1024),), fill, dtype=torch.uint8, device=device)) if fill is not None \
+            else (lambda n: torch.empty((max(n, 1024),), dtype=torch.uint8, device=device))
+        self.saved = mk(self.saved_bytes)
+        self.workspace = mk(self.ws_bytes)

@@ -1,0 +1,134 @@
+// gdn_internal.h -- layouts and kernel argument blocks shared by the host
+// layer (gdn_api.cu) and the kernels.  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr int CHUNK = 64;   // tokens per chunk
+
+// ---- per (chunk, value head) block written by the prep kernel ----
+// T' = T diag(beta gamma rk), T'' = T diag(beta), Aqk = tril(Q^ K^T . Gamma),
+// T = (I + A)^-1 (backward only), all BF16 SwTile(64 x 64); then scalars.
+constexpr int CB_TP = 0;
+constexpr int CB_TPP = 8192;
+constexpr int CB_AQK = 16384;
+constexpr int CB_T = 24576;
+constexpr int CB_SCAL = 32768;   // float sc[64], kd[64], gL, (int) L
+constexpr int CB_SCAL_BYTES = 1024;
+constexpr int CB_BYTES = 33792;
+constexpr int TILE64_BYTES = 8192;
+
+// one saved state: BF16 S^T (dv rows x dk cols) as SwTile(128 x 128)
+constexpr int STATE_BYTES = 32768;
+constexpr int STATE_F32 = 128 * 128;   // an FP32 S^T, row-major [dv][dk]
+constexpr int SAVED_HEADER = 4096;
+
+// saved-set header (first bytes of `saved`)
+struct SavedHeader {
+  uint32_t magic, version;
+  int64_t T;
+  int32_t N, H, HV, dk, dv, l2norm;
+  int32_t NC, NSEG, nsplit, seg_len;
+  uint32_t scale_bits, cu_hash;
+};
+constexpr uint32_t SAVED_MAGIC = 0x4744'4e31u;   // "GDN1"
+constexpr uint32_t SAVED_VERSION = 1;
+
+// ---- device tables built by the table kernel ----
+struct Tables {
+  int* chunk_offsets;  // [N+1]
+  int* chunk_doc;      // [NC]
+  int* chunk_tok0;     // [NC]
+  int* chunk_len;      // [NC]
+  int* seg_offsets;    // [N+1]  segments per document, prefix sum
+  int* split_offsets;  // [N+1]  split segments (transfer walks) per document, prefix sum
+  int* seg_doc;        // [NSEG]
+  int* seg_c0;         // [NSEG] first chunk (global index)
+  int* seg_c1;         // [NSEG] one past the last chunk
+  int* seg_idx;        // [NSEG] index of the segment within its document
+  int* seg_split;      // [NSEG] index in the split list, or -1
+  int* split_seg;      // [nsplit] segments that get transfer walks (p < P-1 of split docs)
+  int* sdoc_first;     // [nsdoc+1] first split index of each split document
+};
+
+struct TableArgs {
+  const int* cu;
+  int N, NC, NSEG, nsplit, nsdoc;
+  int seg_len, split_min;   // a document of n chunks is split iff n > split_min
+  Tables t;
+  int* err;
+  SavedHeader hdr;          // written into `saved` when it is non-null
+  uint8_t* saved;
+};
+
+struct PrepArgs {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const float* g;
+  const float* beta;
+  const int* chunk_tok0;
+  const int* chunk_len;
+  uint8_t* cb;        // [NC][HV][CB_BYTES]
+  int H, HV, G, l2norm, write_T;
+  float scale;
+  int* err;
+};
+
+struct ScanArgs {
+  CUtensorMap tq, tk, tv;
+  const uint8_t* cb;
+  const int* chunk_tok0;
+  const int* chunk_len;
+  const int* seg_c0;
+  const int* seg_c1;
+  const int* seg_idx;
+  const int* seg_split;
+  const int* split_seg;
+  int H, HV, G, nsplit, walk;   // walk = 0: full walks over all segments; 1: B and M walks
+  float scale;
+  uint8_t* tape;              // [NC][HV][STATE_BYTES] or null
+  __nv_bfloat16* o;           // [T][HV][128] or null
+  const float* s_init;        // [nsplit][HV][STATE_F32]: start of the segment after split segment i
+  float* bend;                // [nsplit][HV][STATE_F32]
+  float* mend;                // [nsplit][HV][STATE_F32]
+  int* err;
+};
+
+struct MergeArgs {
+  const int* sdoc_first;
+  const float* bend;
+  const float* mend;
+  float* s_init;
+  int HV;
+  int* err;
+};
+
+// host-side plan of one call (sizes, segment plan, buffer offsets)
+struct Plan {
+  int64_t T;
+  int N, H, HV, G;
+  int NC, NSEG, nsplit, nsdoc, seg_len, split_min, max_doc_chunks;
+  uint32_t cu_hash;
+  // workspace offsets (bytes)
+  size_t o_tables[14];
+  size_t o_cb, o_bend, o_sinit, o_mend_ws;
+  size_t o_dtape, o_dbend, o_dsinit;   // backward
+  size_t ws_fwd, ws_bwd;
+  // saved offsets
+  size_t s_tape, s_mseg, saved_bytes;
+};
+
+inline Tables tables_at(const Plan& P, uint8_t* ws) {
+  Tables t;
+  int** f[13] = {&t.chunk_offsets, &t.seg_offsets, &t.split_offsets, &t.chunk_doc, &t.chunk_tok0,
+                 &t.chunk_len,     &t.seg_doc,     &t.seg_c0,        &t.seg_c1,    &t.seg_idx,
+                 &t.seg_split,     &t.split_seg,   &t.sdoc_first};
+  for (int i = 0; i < 13; ++i) *f[i] = reinterpret_cast<int*>(ws + P.o_tables[i]);
+  return t;
+}
+
+}  // namespace gdn

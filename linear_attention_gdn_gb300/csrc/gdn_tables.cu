@@ -1,0 +1,144 @@
+// gdn_tables.cu -- the varlen chunk-index builder.
+//
+// From cu_seqlens it builds, bit-exactly, the chunk tables every other kernel
+// indexes (chunks of 64 tokens restart at each document start; the last chunk
+// of a document holds len mod 64 tokens or a full chunk) and the segment plan
+// of the intra-GPU split: a document of n > split_min chunks is cut into
+// ceil(n / seg_len) segments of seg_len chunks (the last one shorter).  The
+// flashinfer Cake GDN pages keep four chunk tables plus a segment table built
+// from cu_seqlens ("feat(cake_gdn_kcp) ... #8172" page, commit note on the
+// backend's fifth table); their contents are not printed, so these tables are
+// this library's own definition.
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+
+namespace gdn {
+
+// Block-wide exclusive scan of 4 counters (1024 threads).
+__device__ __forceinline__ void block_scan4(int v[4], int excl[4], int total[4]) {
+  __shared__ int warp_sums[32][4];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    int x = v[m];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    incl[m] = x;
+    if (lane == 31) warp_sums[warp][m] = x;
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      int x = warp_sums[lane][m];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      warp_sums[lane][m] = x;   // inclusive over warps
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    int before = warp ? warp_sums[warp - 1][m] : 0;
+    excl[m] = before + incl[m] - v[m];
+    total[m] = warp_sums[31][m];
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(1024) tables_scan_kernel(TableArgs a) {
+  int carry[4] = {0, 0, 0, 0};   // chunks, segments, split segments, split documents
+  for (int base = 0; base < a.N; base += 1024) {
+    const int d = base + (int)threadIdx.x;
+    int v[4] = {0, 0, 0, 0};
+    if (d < a.N) {
+      const int len = a.cu[d + 1] - a.cu[d];
+      const int n = (len + CH - 1) / CH;
+      const int P = n > a.split_min ? (n + a.seg_len - 1) / a.seg_len : (n > 0 ? 1 : 0);
+      v[0] = n;
+      v[1] = P;
+      v[2] = P > 1 ? P - 1 : 0;
+      v[3] = P > 1 ? 1 : 0;
+    }
+    int excl[4], total[4];
+    block_scan4(v, excl, total);
+    if (d < a.N) {
+      a.t.chunk_offsets[d] = carry[0] + excl[0];
+      a.t.seg_offsets[d] = carry[1] + excl[1];
+      a.t.split_offsets[d] = carry[2] + excl[2];
+      if (v[3] && carry[3] + excl[3] <= a.nsdoc) a.t.sdoc_first[carry[3] + excl[3]] = carry[2] + excl[2];
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) carry[m] += total[m];
+  }
+  if (threadIdx.x == 0) {
+    a.t.chunk_offsets[a.N] = carry[0];
+    a.t.seg_offsets[a.N] = carry[1];
+    a.t.split_offsets[a.N] = carry[2];
+    if (carry[3] <= a.nsdoc) a.t.sdoc_first[carry[3]] = carry[2];
+    // the host planned from its copy of cu_seqlens; a device copy that
+    // disagrees is reported instead of indexing out of bounds
+    if (carry[0] != a.NC || carry[1] != a.NSEG || carry[2] != a.nsplit || carry[3] != a.nsdoc)
+      atomicCAS(a.err, 0, 1 /* GDN_ERR_INVALID_ARG */);
+    if (a.saved) *reinterpret_cast<SavedHeader*>(a.saved) = a.hdr;
+  }
+}
+
+// largest d in [0, n) with off[d] <= x  (off non-decreasing, off[0] <= x)
+__device__ __forceinline__ int find_owner(const int* off, int n, int x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(256) tables_fill_kernel(TableArgs a) {
+  if (*(volatile int*)a.err) return;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < a.NC) {
+    const int d = find_owner(a.t.chunk_offsets, a.N, i);
+    const int t0 = a.cu[d] + (i - a.t.chunk_offsets[d]) * CH;
+    a.t.chunk_doc[i] = d;
+    a.t.chunk_tok0[i] = t0;
+    a.t.chunk_len[i] = min(CH, a.cu[d + 1] - t0);
+  }
+  if (i < a.NSEG) {
+    const int d = find_owner(a.t.seg_offsets, a.N, i);
+    const int p = i - a.t.seg_offsets[d];
+    const int P = a.t.seg_offsets[d + 1] - a.t.seg_offsets[d];
+    const int cd0 = a.t.chunk_offsets[d], cd1 = a.t.chunk_offsets[d + 1];
+    int c0 = cd0, c1 = cd1;
+    if (P > 1) {
+      c0 = cd0 + p * a.seg_len;
+      c1 = min(c0 + a.seg_len, cd1);
+    }
+    a.t.seg_doc[i] = d;
+    a.t.seg_c0[i] = c0;
+    a.t.seg_c1[i] = c1;
+    a.t.seg_idx[i] = p;
+    int sp = -1;
+    if (P > 1 && p < P - 1) {
+      sp = a.t.split_offsets[d] + p;
+      a.t.split_seg[sp] = i;
+    }
+    a.t.seg_split[i] = sp;
+  }
+}
+
+void launch_tables(const TableArgs& a, cudaStream_t s) {
+  tables_scan_kernel<<<1, 1024, 0, s>>>(a);
+  const int n = a.NC > a.NSEG ? a.NC : a.NSEG;
+  if (n > 0) tables_fill_kernel<<<(n + 255) / 256, 256, 0, s>>>(a);
+}
+
+}  // namespace gdn

@@ -1,0 +1,89 @@
+"""Host-side logic of the C ABI, without a GPU: the library loads and exports
+every symbol include/gdn.h declares, byte queries follow the documented
+layout, and invalid problems / arguments are refused before any launch."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import linear_attention_gdn_gb300 as gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:gdn_status|const char \*|int32_t)\s*\**\s*(gdn_\w+)\s*\(", src, re.M)))
+
+
+def test_exports_every_declared_symbol():
+    gdn.load()
+    syms = declared_symbols()
+    assert len(syms) >= 8, syms
+    for s in syms:
+        assert hasattr(gdn.lib, s), s
+        assert s in gdn.EXPORTS
+
+
+def test_status_strings():
+    for code in range(8):
+        assert gdn.gdn_status_string(code)
+    assert gdn.gdn_status_string(99) == "unknown status"
+
+
+def test_saved_and_workspace_bytes():
+    p = gdn.problem(320, 2, 2, 4)
+    saved, ws = gdn.gdn_saved_bytes(p, [0, 128, 320])
+    # header + 5 chunks x 4 v-heads x 32 KiB BF16 states, no segment split
+    assert saved == 4096 + 5 * 4 * 32768
+    assert ws > 5 * 4 * 33792
+    p = gdn.problem(64 * 40, 1, 1, 2, segments=4)
+    saved, _ = gdn.gdn_saved_bytes(p, [0, 64 * 40])
+    assert gdn.gdn_plan_segment_chunks(p, [0, 64 * 40]) == 10
+    # 4 segments -> 3 transfer operators per v-head in FP32
+    assert saved == 4096 + 40 * 2 * 32768 + 3 * 2 * 128 * 128 * 4
+
+
+@pytest.mark.parametrize("cu,T,N,H,HV,dk,code", [
+    ([0, 10, 5], 5, 2, 1, 1, 128, 1),      # decreasing cu_seqlens
+    ([1, 10], 9, 1, 1, 1, 128, 1),         # cu[0] != 0
+    ([0, 10], 11, 1, 1, 1, 128, 1),        # cu[N] != T
+    ([0, 10], 10, 1, 2, 3, 128, 2),        # HV not a multiple of H
+    ([0, 10], 10, 1, 1, 1, 64, 2),         # dk != 128
+])
+def test_invalid_problems_refused(cu, T, N, H, HV, dk, code):
+    p = gdn.problem(T, N, H, HV, dk=dk)
+    cu_a = np.array(cu, dtype=np.int32)
+    s, w = ctypes.c_size_t(), ctypes.c_size_t()
+    st = gdn.lib.gdn_saved_bytes(ctypes.byref(p), cu_a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                 ctypes.byref(s), ctypes.byref(w))
+    assert st == code
+
+
+def test_invalid_arguments_refused_before_launch():
+    """Null, misaligned or undersized buffers return INVALID_ARG /
+    WORKSPACE_TOO_SMALL from host checks (fake device addresses are never
+    dereferenced)."""
+    p = gdn.problem(320, 2, 2, 4)
+    cu = np.array([0, 128, 320], dtype=np.int32)
+    cup = cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    saved, ws = gdn.gdn_saved_bytes(p, cu)
+    A = 1 << 20   # a fake, aligned address
+    args = lambda q=A, o=A, sv=A, wsp=A, wsb=ws: (ctypes.byref(p), ctypes.c_void_p(q), ctypes.c_void_p(A),
+                                                  ctypes.c_void_p(A), ctypes.c_void_p(A), ctypes.c_void_p(A),
+                                                  ctypes.cast(ctypes.c_void_p(A), ctypes.POINTER(ctypes.c_int32)),
+                                                  cup, ctypes.c_void_p(o) if o else None,
+                                                  ctypes.c_void_p(sv) if sv else None,
+                                                  ctypes.c_void_p(wsp) if wsp else None, wsb, None)
+    assert gdn.lib.gdn_fwd(*args(q=A + 2)) == 1          # misaligned q
+    assert gdn.lib.gdn_fwd(*args(o=0, sv=0)) == 1         # nothing to write
+    assert gdn.lib.gdn_fwd(*args(wsp=0)) == 1             # no workspace
+    assert gdn.lib.gdn_fwd(*args(wsb=100)) == 3           # workspace too small
+    bw = lambda sv, wsb: gdn.lib.gdn_bwd(ctypes.byref(p), *[ctypes.c_void_p(A)] * 5,
+                                          ctypes.cast(ctypes.c_void_p(A), ctypes.POINTER(ctypes.c_int32)), cup,
+                                          ctypes.c_void_p(A), ctypes.c_void_p(sv) if sv else None,
+                                          *[ctypes.c_void_p(A)] * 5, ctypes.c_void_p(A), wsb, None)
+    assert bw(0, ws) == 1                                 # backward needs the saved set
+    assert bw(A, 10) == 3
