@@ -1,12 +1,1029 @@
-// gdn_bwd.cu -- backward kernels (placeholder until they land)
+// gdn_bwd.cu -- backward of the chunked GDN form.
+//
+// Per chunk (local positions r, S = state entering, dS' = gradient of the
+// state leaving the chunk, P = scale), reversing the forward equations
+//   V_new = U - W S,  O = P (diag(gamma) Q^ S + Aqk V_new),
+//   S' = gamma_L S + Kd^T V_new:
+//   dV_new = P Aqk^T dO + Kd dS'
+//   dS     = gamma_L dS' + P (diag(gamma) Q^)^T dO - W^T dV_new      (reverse scan)
+// and the chunk-local gradients (dq^, dk^, dv, dbeta, dG -> dg) from the
+// UT / WY relations W = T diag(beta gamma) K^, U = T diag(beta) V,
+// T = (I + A)^-1 (dA = -T^T dT T^T on the strict lower triangle).  These are
+// the adjoint walk and the dA / dv and fused-gradient programs of the
+// flashinfer Cake GDN pages ("feat(cake_gdn_kcp) ... #8172" page, commit
+// notes on the K2 walk, kcp_dav and the fused-gradient program; "#8542" page:
+// the backward's merges read the M_seg plane of the forward).
+//
+// Kernels:
+//   bwd_scan_kernel   reverse dS walk per (segment, value head); writes the
+//                     BF16 dS' tape (gradient leaving each chunk), or, in the
+//                     split's zero-start mode, the adjoint at a segment start
+//   merge_bwd_kernel  dS_end(p) = dS_end(p+1) M_{p+1} + B'_{p+1} over segments
+//   grad_kernel       per (chunk, q/k head): everything chunk-local, summing
+//                     dq^, dk^ over the group's value heads, then the L2-norm
+//                     backward
+#include "gdn.h"
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
-#include "gdn.h"
+
 namespace gdn {
-void setup_bwd_attrs() {}
-gdn_status run_bwd(const Plan&, const gdn_problem&, const void*, const void*, const void*, const float*,
-                   const float*, const int32_t*, const void*, const void*, void*, void*, void*, float*, float*,
-                   uint8_t*, cudaStream_t) {
-  return GDN_ERR_UNSUPPORTED;
+
+bool make_tmap(CUtensorMap* m, const void* base, int64_t T, int heads);
+gdn_status run_tables(const Plan& P, const gdn_problem* p, const int32_t* cu_dev, uint8_t* ws, void* saved,
+                      cudaStream_t s);
+gdn_status run_prep(const Plan& P, const gdn_problem* p, const void* q, const void* k, const float* g,
+                    const float* beta, uint8_t* ws, int write_T, cudaStream_t s);
+
+struct BScanArgs {
+  CUtensorMap tq, tk, tdo;
+  const uint8_t* cb;
+  const int* chunk_tok0;
+  const int* seg_c0;
+  const int* seg_c1;
+  const int* seg_split;
+  const int* split_seg;
+  int HV, G, nsplit, walk;
+  float scale;
+  uint8_t* dtape;        // [NC][HV][STATE_BYTES]
+  const float* ds_init;  // [nsplit][HV][STATE_F32]: adjoint at the end of split segment i
+  float* dbend;          // [nsplit][HV][STATE_F32]
+  int* err;
+};
+
+struct GradArgs {
+  CUtensorMap tq, tk, tv, tdo;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const float* g;
+  const float* beta;
+  const uint8_t* cb;
+  const uint8_t* tape;    // saved S^T per chunk
+  const uint8_t* dtape;   // dS'^T per chunk
+  const int* chunk_tok0;
+  const int* chunk_len;
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float* dg;
+  float* dbeta;
+  int H, HV, G, l2norm;
+  float scale;
+  int* err;
+};
+
+struct MergeBwdArgs {
+  const int* sdoc_first;
+  const float* dbend;
+  const float* mend;
+  float* ds_init;
+  int HV;
+  int* err;
+};
+
+struct CheckArgs {
+  const uint8_t* saved;
+  SavedHeader expect;
+  int* err;
+};
+
+// ===========================================================================
+// reverse dS scan
+// ===========================================================================
+constexpr int BS_K = 0, BS_Q = 16384, BS_DO = 32768, BS_TP = 49152, BS_AQK = 57344, BS_SCAL = 65536;
+constexpr int BS_STAGE = 66560;
+constexpr int BS_DS = 2 * BS_STAGE;           // BF16 dS'^T tile
+constexpr int BS_W = BS_DS + STATE_BYTES;     // -W^T tile, SwTile(128 x 64)
+constexpr int BS_SMEM = BS_W + 16384;
+constexpr int BS_SMEM_ALLOC = BS_SMEM + 1024;
+constexpr int BT_DW = 0, BT_DX = 64, BT_DY = 128, BT_DS = 192, BT_ADV = 320, BT_ADO = 352;
+
+__device__ __forceinline__ void store_row128(uint8_t* dst, int row, const float* S) {
+#pragma unroll
+  for (int c8 = 0; c8 < 16; ++c8) {
+    uint4 w;
+    w.x = pack_bf16(S[c8 * 8 + 0], S[c8 * 8 + 1]);
+    w.y = pack_bf16(S[c8 * 8 + 2], S[c8 * 8 + 3]);
+    w.z = pack_bf16(S[c8 * 8 + 4], S[c8 * 8 + 5]);
+    w.w = pack_bf16(S[c8 * 8 + 6], S[c8 * 8 + 7]);
+    *reinterpret_cast<uint4*>(dst + sw_chunk(row, c8, 128)) = w;
+  }
 }
+
+__device__ __forceinline__ float ld_bf16(const uint8_t* tile, int r, int c, int R) {
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + sw_off(r, c, R)));
+}
+
+__global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant__ BScanArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t full_bar[2], mma_bar;
+  __shared__ uint32_t tslot;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (*(volatile int*)a.err) return;
+
+  int seg, hv, split = -1;
+  if (!a.walk) {
+    seg = blockIdx.x / a.HV;
+    hv = blockIdx.x % a.HV;
+  } else {  // zero-start reverse walk of the segment after split point `split`
+    split = blockIdx.x / a.HV;
+    hv = blockIdx.x % a.HV;
+    seg = a.split_seg[split] + 1;
+  }
+  const int kh = hv / a.G;
+  const int c0 = a.seg_c0[seg], nch = a.seg_c1[seg] - c0;
+
+  float dS[128];
+  {
+    const float* src = nullptr;
+    if (!a.walk && a.seg_split[seg] >= 0)
+      src = a.ds_init + ((size_t)a.seg_split[seg] * a.HV + hv) * STATE_F32 + (size_t)tid * 128;
+#pragma unroll
+    for (int jj = 0; jj < 128; ++jj) dS[jj] = src ? src[jj] : 0.f;
+  }
+  uint8_t* ds_tile = sm + BS_DS;
+  store_row128(ds_tile, tid, dS);
+
+  if (warp == 0) tmem_alloc(&tslot, 512);
+  if (tid == 0) {
+    mbar_init(&full_bar[0], 1);
+    mbar_init(&full_bar[1], 1);
+    mbar_init(&mma_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;");
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tslot;
+
+  // iteration `it` processes chunk c0 + nch - 1 - it
+  auto issue = [&](int it) {
+    const int ci = c0 + nch - 1 - it;
+    uint8_t* st = sm + (it & 1) * BS_STAGE;
+    uint64_t* bar = &full_bar[it & 1];
+    const int t0 = a.chunk_tok0[ci];
+    const uint8_t* cbp = a.cb + ((size_t)ci * a.HV + hv) * CB_BYTES;
+    mbar_expect_tx(bar, (uint32_t)BS_STAGE);
+    tma_load_3d(st + BS_K, &a.tk, 0, kh, t0, bar);
+    tma_load_3d(st + BS_K + 8192, &a.tk, 64, kh, t0, bar);
+    tma_load_3d(st + BS_Q, &a.tq, 0, kh, t0, bar);
+    tma_load_3d(st + BS_Q + 8192, &a.tq, 64, kh, t0, bar);
+    tma_load_3d(st + BS_DO, &a.tdo, 0, hv, t0, bar);
+    tma_load_3d(st + BS_DO + 8192, &a.tdo, 64, hv, t0, bar);
+    bulk_load(st + BS_TP, cbp + CB_TP, TILE64_BYTES, bar);
+    bulk_load(st + BS_AQK, cbp + CB_AQK, TILE64_BYTES, bar);
+    bulk_load(st + BS_SCAL, cbp + CB_SCAL, CB_SCAL_BYTES, bar);
+  };
+  if (tid == 0) {
+    if (nch > 0) issue(0);
+    if (nch > 1) issue(1);
+  }
+  uint32_t mph = 0;
+  bool ok = true;
+  const uint32_t sm_ds = smem_u32(ds_tile), sm_w = smem_u32(sm + BS_W);
+  for (int it = 0; it < nch && ok; ++it) {
+    const int ci = c0 + nch - 1 - it;
+    uint8_t* st = sm + (it & 1) * BS_STAGE;
+    const uint32_t a_k = smem_u32(st + BS_K), a_q = smem_u32(st + BS_Q), a_do = smem_u32(st + BS_DO);
+    const uint32_t a_tp = smem_u32(st + BS_TP), a_aqk = smem_u32(st + BS_AQK);
+    const float* scal = reinterpret_cast<const float*>(st + BS_SCAL);
+    ok = __syncthreads_and(mbar_wait(&full_bar[it & 1], (it >> 1) & 1, a.err));
+    if (!ok) break;
+    const int L = reinterpret_cast<const int*>(scal)[129];
+    if (L < CH) {
+      for (int idx = tid; idx < (CH - L) * 48; idx += 128) {
+        const int t = idx / 48, rem = idx % 48, tile = rem / 16, c8 = rem % 16;
+        const int off = tile == 0 ? BS_K : (tile == 1 ? BS_Q : BS_DO);
+        *reinterpret_cast<uint4*>(st + off + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      fence_async_smem();
+      __syncthreads();
+    }
+    if (!a.walk) store_row128(a.dtape + ((size_t)ci * a.HV + hv) * STATE_BYTES, tid, dS);
+    tc_fence_after();
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ss(tb + BT_DW, desc_mn(a_k, 64, ks), desc_k(a_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ss(tb + BT_DX, desc_mn(a_do, 64, ks), desc_mn(a_aqk, 64, ks), idesc(128, 64, 1, 1), ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ss(tb + BT_DY, desc_k(sm_ds, 128, ks), desc_k(a_k, 64, ks), idesc(128, 64, 0, 0), ks > 0);
+      mma_commit(&mma_bar);
+    }
+    {  // (P gamma_r rq_r dO[r][tid]) -> TMEM A operand, while the MMAs run
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t p8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int r = q * 16 + 2 * e;
+          p8[e] = pack_bf16(scal[r] * ld_bf16(st + BS_DO, r, tid, 64), scal[r + 1] * ld_bf16(st + BS_DO, r + 1, tid, 64));
+        }
+        tmem_st8(taddr(tb, warp * 32, BT_ADO + q * 8), p8);
+      }
+    }
+    ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
+    mph ^= 1;
+    if (!ok) break;
+    tc_fence_after();
+    {
+      float w[64];
+      tmem_ld32(taddr(tb, warp * 32, BT_DW), w);
+      tmem_ld32(taddr(tb, warp * 32, BT_DW + 32), w + 32);
+      uint8_t* wt = sm + BS_W;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        uint4 v;
+        v.x = pack_bf16(-w[c8 * 8 + 0], -w[c8 * 8 + 1]);
+        v.y = pack_bf16(-w[c8 * 8 + 2], -w[c8 * 8 + 3]);
+        v.z = pack_bf16(-w[c8 * 8 + 4], -w[c8 * 8 + 5]);
+        v.w = pack_bf16(-w[c8 * 8 + 6], -w[c8 * 8 + 7]);
+        *reinterpret_cast<uint4*>(wt + sw_chunk(tid, c8, 128)) = v;
+      }
+      const float* kd = scal + 64;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float x[32], y[32];
+        tmem_ld32(taddr(tb, warp * 32, BT_DX + h * 32), x);
+        tmem_ld32(taddr(tb, warp * 32, BT_DY + h * 32), y);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint32_t p8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int j = q * 16 + 2 * e, r = h * 32 + j;
+            p8[e] = pack_bf16(fmaf(a.scale, x[j], kd[r] * y[j]), fmaf(a.scale, x[j + 1], kd[r + 1] * y[j + 1]));
+          }
+          tmem_st8(taddr(tb, warp * 32, BT_ADV + h * 16 + q * 8), p8);
+        }
+      }
+      tmem_wait_st();
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ts(tb + BT_DS, tb + BT_ADV + ks * 8, desc_k(sm_w, 128, ks), idesc(128, 128, 0, 0), ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ts(tb + BT_DS, tb + BT_ADO + ks * 8, desc_mn(a_q, 64, ks), idesc(128, 128, 0, 1), 1u);
+      mma_commit(&mma_bar);
+    }
+    ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
+    mph ^= 1;
+    if (!ok) break;
+    tc_fence_after();
+    {
+      const float gL = scal[128];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        float x[32];
+        tmem_ld32(taddr(tb, warp * 32, BT_DS + h * 32), x);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) dS[h * 32 + e] = fmaf(gL, dS[h * 32 + e], x[e]);
+      }
+      store_row128(ds_tile, tid, dS);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && it + 2 < nch) issue(it + 2);
+  }
+  if (ok && a.walk) {
+    float* dst = a.dbend + ((size_t)split * a.HV + hv) * STATE_F32 + (size_t)tid * 128;
+#pragma unroll
+    for (int jj = 0; jj < 128; jj += 4)
+      *reinterpret_cast<float4*>(dst + jj) = make_float4(dS[jj], dS[jj + 1], dS[jj + 2], dS[jj + 3]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+// dS^T_end(i) = dS^T_end(i+1) M + B'^T(i), walking the split segments of one
+// document backwards; M = M_{p+1}, stored transposed (mend[i] = M_{p+1}^T).
+__global__ void __launch_bounds__(256) merge_bwd_kernel(MergeBwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  float* Sp = reinterpret_cast<float*>(smem_raw);   // [128][129]
+  float* Mt = Sp + 128 * 129;                       // Mt[kk][c] = M[kk][c] = mend[c][kk]
+  if (*(volatile int*)a.err) return;
+  const int sd = blockIdx.x, hv = blockIdx.y, tid = threadIdx.x;
+  const int f0 = a.sdoc_first[sd], f1 = a.sdoc_first[sd + 1];
+  const size_t stride = (size_t)a.HV * STATE_F32;
+  for (int i = tid; i < STATE_F32; i += 256) {
+    const float b = a.dbend[(size_t)(f1 - 1) * stride + (size_t)hv * STATE_F32 + i];
+    Sp[(i >> 7) * 129 + (i & 127)] = b;
+    a.ds_init[(size_t)(f1 - 1) * stride + (size_t)hv * STATE_F32 + i] = b;
+  }
+  __syncthreads();
+  const int r0 = (tid >> 4) * 8, cc0 = (tid & 15) * 8;
+  for (int p = f1 - 2; p >= f0; --p) {
+    const float* M = a.mend + (size_t)p * stride + (size_t)hv * STATE_F32;
+    const float* B = a.dbend + (size_t)p * stride + (size_t)hv * STATE_F32;
+    for (int i = tid; i < STATE_F32; i += 256) Mt[(i & 127) * 129 + (i >> 7)] = M[i];
+    __syncthreads();
+    float acc[8][8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x)
+#pragma unroll
+      for (int y = 0; y < 8; ++y) acc[x][y] = 0.f;
+    for (int kk = 0; kk < 128; ++kk) {
+      float sa[8], mb[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) sa[x] = Sp[(r0 + x) * 129 + kk];
+#pragma unroll
+      for (int y = 0; y < 8; ++y) mb[y] = Mt[kk * 129 + cc0 + y];
+#pragma unroll
+      for (int x = 0; x < 8; ++x)
+#pragma unroll
+        for (int y = 0; y < 8; ++y) acc[x][y] = fmaf(sa[x], mb[y], acc[x][y]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int x = 0; x < 8; ++x)
+#pragma unroll
+      for (int y = 0; y < 8; ++y) {
+        const int i = (r0 + x) * 128 + cc0 + y;
+        const float v = acc[x][y] + B[i];
+        Sp[(r0 + x) * 129 + cc0 + y] = v;
+        a.ds_init[(size_t)p * stride + (size_t)hv * STATE_F32 + i] = v;
+      }
+    __syncthreads();
+  }
+}
+
+__global__ void check_saved_kernel(CheckArgs a) {
+  const SavedHeader* h = reinterpret_cast<const SavedHeader*>(a.saved);
+  const SavedHeader& e = a.expect;
+  if (h->magic != e.magic || h->version != e.version || h->T != e.T || h->N != e.N || h->H != e.H ||
+      h->HV != e.HV || h->dk != e.dk || h->dv != e.dv || h->l2norm != e.l2norm || h->NC != e.NC ||
+      h->NSEG != e.NSEG || h->nsplit != e.nsplit || h->seg_len != e.seg_len || h->scale_bits != e.scale_bits ||
+      h->cu_hash != e.cu_hash)
+    atomicCAS(a.err, 0, ST_SAVED_MISMATCH);
+}
+
+// ===========================================================================
+// chunk gradients
+// ===========================================================================
+constexpr int GK_Q = 0, GK_K = 16384, GK_V = 32768, GK_DO = 49152, GK_S = 65536, GK_DS = 98304,
+              GK_T = 131072, GK_SCAL = 139264;
+constexpr int GK_WD = 140288, GK_DV = 156672, GK_VN = 173056, GK_TP = 189440, GK_TPP = 197632, GK_AQ = 205824;
+constexpr int GK_SMEM = 214016;
+constexpr int GK_SMEM_ALLOC = GK_SMEM + 1024;
+constexpr int GK_DT = GK_TP, GK_R1 = GK_TPP;                                   // free after M1
+constexpr int GK_H1 = GK_S, GK_H2 = GK_S + 8192, GK_F1 = GK_S + 16384, GK_F2 = GK_S + 24576;  // after M3
+constexpr int GK_C = GK_DS;                   // FP32 [64][64] of dAqk.Aqk + dA.A, after M3
+constexpr int GK_PART = GK_AQ;                // FP32 partial column sums [6][4][64], after M1
+constexpr int GT_KK = 0, GT_QK = 64, GT_S0 = 128, GT_S1 = 192, GT_S2 = 256, GT_S3 = 320, GT_S4 = 384, GT_S5 = 448;
+constexpr uint32_t GK_VH_BYTES = 2 * 16384 + 2 * STATE_BYTES + TILE64_BYTES + CB_SCAL_BYTES;
+
+// sum over the 32 lanes of a warp of column `lane` of v[32] (fixed order)
+__device__ __forceinline__ float colsum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int kq = 0; kq < o; ++kq) {
+      const float mine = up ? v[kq + o] : v[kq];
+      const float other = up ? v[kq] : v[kq + o];
+      v[kq] = mine + __shfl_xor_sync(0xffffffffu, other, o);
+    }
+  }
+  return v[0];
+}
+
+__device__ __forceinline__ void store_chunk8(uint8_t* tile, int r, int c8, int R, const float* x) {
+  uint4 w;
+  w.x = pack_bf16(x[0], x[1]);
+  w.y = pack_bf16(x[2], x[3]);
+  w.z = pack_bf16(x[4], x[5]);
+  w.w = pack_bf16(x[6], x[7]);
+  *reinterpret_cast<uint4*>(tile + sw_chunk(r, c8, R)) = w;
+}
+
+__global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ GradArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t ld_bar, mma_bar;
+  __shared__ uint32_t tslot;
+  __shared__ float rq[CH], rk[CH], Gs[CH], bs[CH], gs[CH];
+  __shared__ float rowB[2][CH], sdot[8];
+  const int c = blockIdx.x, j = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wg = tid >> 7, w4 = warp & 3;
+  const int row = w4 * 32 + lane;          // TMEM lane / M = 128 row of this thread
+  const int cb0 = wg * 32;                 // first of this thread's 32 columns
+  const int r64 = w4 * 16 + lane;          // M = 64 row (valid for lane < 16)
+  if (*(volatile int*)a.err) return;
+  const int tok0 = a.chunk_tok0[c], L = a.chunk_len[c];
+
+  if (warp == 0) tmem_alloc(&tslot, 512);
+  if (tid == 0) {
+    mbar_init(&ld_bar, 1);
+    mbar_init(&mma_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;");
+  }
+  __syncthreads();
+  const uint32_t tb = tslot;
+  auto issue_vhead = [&](int hv, bool with_qk) {
+    const uint8_t* cbp = a.cb + ((size_t)c * a.HV + hv) * CB_BYTES;
+    mbar_expect_tx(&ld_bar, GK_VH_BYTES + (with_qk ? 32768u : 0u));
+    if (with_qk) {
+      tma_load_3d(sm + GK_Q, &a.tq, 0, j, tok0, &ld_bar);
+      tma_load_3d(sm + GK_Q + 8192, &a.tq, 64, j, tok0, &ld_bar);
+      tma_load_3d(sm + GK_K, &a.tk, 0, j, tok0, &ld_bar);
+      tma_load_3d(sm + GK_K + 8192, &a.tk, 64, j, tok0, &ld_bar);
+    }
+    tma_load_3d(sm + GK_V, &a.tv, 0, hv, tok0, &ld_bar);
+    tma_load_3d(sm + GK_V + 8192, &a.tv, 64, hv, tok0, &ld_bar);
+    tma_load_3d(sm + GK_DO, &a.tdo, 0, hv, tok0, &ld_bar);
+    tma_load_3d(sm + GK_DO + 8192, &a.tdo, 64, hv, tok0, &ld_bar);
+    bulk_load(sm + GK_S, a.tape + ((size_t)c * a.HV + hv) * STATE_BYTES, STATE_BYTES, &ld_bar);
+    bulk_load(sm + GK_DS, a.dtape + ((size_t)c * a.HV + hv) * STATE_BYTES, STATE_BYTES, &ld_bar);
+    bulk_load(sm + GK_T, cbp + CB_T, TILE64_BYTES, &ld_bar);
+    bulk_load(sm + GK_SCAL, cbp + CB_SCAL, CB_SCAL_BYTES, &ld_bar);
+  };
+  if (tid == 0) issue_vhead(j * a.G, true);
+
+  uint32_t lph = 0, mph = 0;
+  bool ok = true;
+  auto mma_sync_wait = [&]() -> bool {
+    bool r = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
+    mph ^= 1;
+    tc_fence_after();
+    return r;
+  };
+  auto handoff = [&]() {   // generic smem/TMEM writes -> visible to the next MMAs
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  };
+  const uint32_t s_q = smem_u32(sm + GK_Q), s_k = smem_u32(sm + GK_K), s_v = smem_u32(sm + GK_V),
+                 s_do = smem_u32(sm + GK_DO), s_s = smem_u32(sm + GK_S), s_ds = smem_u32(sm + GK_DS),
+                 s_t = smem_u32(sm + GK_T), s_wd = smem_u32(sm + GK_WD), s_dv = smem_u32(sm + GK_DV),
+                 s_vn = smem_u32(sm + GK_VN), s_tp = smem_u32(sm + GK_TP), s_tpp = smem_u32(sm + GK_TPP),
+                 s_aq = smem_u32(sm + GK_AQ), s_dt = smem_u32(sm + GK_DT), s_r1 = smem_u32(sm + GK_R1),
+                 s_h1 = smem_u32(sm + GK_H1), s_h2 = smem_u32(sm + GK_H2), s_f1 = smem_u32(sm + GK_F1),
+                 s_f2 = smem_u32(sm + GK_F2);
+  const float* scal = reinterpret_cast<const float*>(sm + GK_SCAL);
+  float* Cm = reinterpret_cast<float*>(sm + GK_C);
+  float* part = reinterpret_cast<float*>(sm + GK_PART);
+  auto tld32 = [&](int col, float* out) { tmem_ld32(taddr(tb, w4 * 32, col + cb0), out); };
+
+  float dq_acc[32], dk_acc[32];   // dq^T, dk^T [row][cb0 + e], summed over the group
+#pragma unroll
+  for (int e = 0; e < 32; ++e) dq_acc[e] = dk_acc[e] = 0.f;
+
+  for (int h = 0; h < a.G && ok; ++h) {
+    const int hv = j * a.G + h;
+    ok = __syncthreads_and(mbar_wait(&ld_bar, lph, a.err));
+    lph ^= 1;
+    if (!ok) break;
+    if (L < CH) {  // zero rows past the document end in the token tiles
+      const int ntile = h == 0 ? 4 : 2;
+      for (int idx = tid; idx < (CH - L) * 16 * ntile; idx += 256) {
+        const int t = idx / (16 * ntile), rem = idx % (16 * ntile), tile = rem / 16, c8 = rem % 16;
+        const int off = tile == 0 ? GK_V : tile == 1 ? GK_DO : tile == 2 ? GK_Q : GK_K;
+        *reinterpret_cast<uint4*>(sm + off + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    if (h == 0 && tid < 128) {   // L2 norms of the q/k rows
+      const uint8_t* tile = sm + (tid < 64 ? GK_K : GK_Q);
+      const int r = tid & 63;
+      float ss = 0.f;
+      for (int cc = 0; cc < D; ++cc) {
+        const float x = r < L ? ld_bf16(tile, r, cc, 64) : 0.f;
+        ss = fmaf(x, x, ss);
+      }
+      const float rn = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+      if (tid < 64) rk[r] = rn;
+      else rq[r] = rn;
+    }
+    if (warp == 0) {  // gates of this value head
+      const int r0 = 2 * lane, r1 = r0 + 1;
+      float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+      if (r0 < L) {
+        g0 = a.g[(size_t)(tok0 + r0) * a.HV + hv];
+        b0 = a.beta[(size_t)(tok0 + r0) * a.HV + hv];
+      }
+      if (r1 < L) {
+        g1 = a.g[(size_t)(tok0 + r1) * a.HV + hv];
+        b1 = a.beta[(size_t)(tok0 + r1) * a.HV + hv];
+      }
+      float s = g0 + g1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += y;
+      }
+      const float ex = s - (g0 + g1);
+      Gs[r0] = ex + g0;
+      Gs[r1] = ex + g0 + g1;
+      bs[r0] = b0;
+      bs[r1] = b1;
+      gs[r0] = r0 < L ? expf(ex + g0) : 0.f;
+      gs[r1] = r1 < L ? expf(ex + g0 + g1) : 0.f;
+    }
+    __syncthreads();
+    const float GL = Gs[L - 1], gL = scal[128];
+    if (h == 0) {  // KK^T and QK^T (M = 64), kept in TMEM for the whole group
+      handoff();
+      if (tid == 0) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_ss(tb + GT_KK, desc_k(s_k, 64, ks), desc_k(s_k, 64, ks), idesc(64, 64, 0, 0), ks > 0);
+          mma_ss(tb + GT_QK, desc_k(s_q, 64, ks), desc_k(s_k, 64, ks), idesc(64, 64, 0, 0), ks > 0);
+        }
+        mma_commit(&mma_bar);
+      }
+      if (!(ok = mma_sync_wait())) break;
+    }
+    // ---- T' = T diag(beta gamma rk), T'' = T diag(beta), Aqk tile
+    for (int idx = tid; idx < 64 * 8; idx += 256) {
+      const int r = idx >> 3, c8 = idx & 7;
+      const uint4 raw = *reinterpret_cast<const uint4*>(sm + GK_T + sw_chunk(r, c8, 64));
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      float tp[8], tpp[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h2[e]);
+        const int c0 = c8 * 8 + 2 * e;
+        tpp[2 * e] = f.x * bs[c0];
+        tpp[2 * e + 1] = f.y * bs[c0 + 1];
+        tp[2 * e] = tpp[2 * e] * gs[c0] * rk[c0];
+        tp[2 * e + 1] = tpp[2 * e + 1] * gs[c0 + 1] * rk[c0 + 1];
+      }
+      store_chunk8(sm + GK_TP, r, c8, 64, tp);
+      store_chunk8(sm + GK_TPP, r, c8, 64, tpp);
+    }
+    {
+      float qk[32];
+      tld32(GT_QK, qk);
+      if (lane < 16) {
+        const int r = r64;
+        const float Gr = Gs[r], qr = rq[r];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int cc = cb0 + q4 * 8 + e;
+            x[e] = (cc <= r && r < L) ? qr * rk[cc] * expf(Gr - Gs[cc]) * qk[q4 * 8 + e] : 0.f;
+          }
+          store_chunk8(sm + GK_AQ, r, (cb0 >> 3) + q4, 64, x);
+        }
+      }
+    }
+    handoff();
+    // ---- M1: W^T, U^T, dO^T Aqk, dS'^T K^T
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        mma_ss(tb + GT_S0, desc_mn(s_k, 64, ks), desc_k(s_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+        mma_ss(tb + GT_S1, desc_mn(s_v, 64, ks), desc_k(s_tpp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+        mma_ss(tb + GT_S2, desc_mn(s_do, 64, ks), desc_mn(s_aq, 64, ks), idesc(128, 64, 1, 1), ks > 0);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ss(tb + GT_S3, desc_k(s_ds, 128, ks), desc_k(s_k, 64, ks), idesc(128, 64, 0, 0), ks > 0);
+      mma_commit(&mma_bar);
+    }
+    if (!(ok = mma_sync_wait())) break;
+    {  // H1: -W^T -> WD; dV_new^T = P dO^T Aqk + kd (dS'^T K^T) -> dV
+      float w[32], x[32], y[32];
+      tld32(GT_S0, w);
+      tld32(GT_S2, x);
+      tld32(GT_S3, y);
+      const float* kd = scal + 64;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float nw[8], dvn[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int jj = q4 * 8 + e;
+          nw[e] = -w[jj];
+          dvn[e] = fmaf(a.scale, x[jj], kd[cb0 + jj] * y[jj]);
+        }
+        store_chunk8(sm + GK_WD, row, (cb0 >> 3) + q4, 128, nw);
+        store_chunk8(sm + GK_DV, row, (cb0 >> 3) + q4, 128, dvn);
+      }
+    }
+    handoff();
+    // ---- M2: V_new^T, S dV_new^T, dV_new^T T, S dO^T
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        mma_ss(tb + GT_S1, desc_k(s_s, 128, ks), desc_mn(s_wd, 128, ks), idesc(128, 64, 0, 1), 1u);
+        mma_ss(tb + GT_S0, desc_mn(s_s, 128, ks), desc_mn(s_dv, 128, ks), idesc(128, 64, 1, 1), ks > 0);
+        mma_ss(tb + GT_S3, desc_mn(s_s, 128, ks), desc_k(s_do, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ss(tb + GT_S2, desc_k(s_dv, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
+      mma_commit(&mma_bar);
+    }
+    if (!(ok = mma_sync_wait())) break;
+    {  // H2
+      float x[32], cb[32], cg[32];
+      tld32(GT_S1, x);   // V_new^T row (dv)
+      {
+        float t8[8];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t8[e] = x[q4 * 8 + e];
+          store_chunk8(sm + GK_VN, row, (cb0 >> 3) + q4, 128, t8);
+        }
+      }
+      tld32(GT_S0, x);   // (S dV_new^T) row (dk) -> dW^T = -(.)
+      {
+        float t8[8];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t8[e] = -x[q4 * 8 + e];
+          store_chunk8(sm + GK_WD, row, (cb0 >> 3) + q4, 128, t8);
+        }
+      }
+      tld32(GT_S2, x);   // X^T = dV_new^T T, row = dv index
+      __nv_bfloat16* dvp = a.dv + ((size_t)tok0 * a.HV + hv) * D + row;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int cc = cb0 + e;
+        if (cc < L) dvp[(size_t)cc * a.HV * D] = __float2bfloat16_rn(bs[cc] * x[e]);
+        cb[e] = ld_bf16(sm + GK_V, cc, row, 64) * x[e];
+      }
+      tld32(GT_S3, x);   // S dO^T, row = dk index
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int cc = cb0 + e;
+        const float pg = a.scale * gs[cc];
+        dq_acc[e] = fmaf(pg, x[e], dq_acc[e]);
+        cg[e] = pg * rq[cc] * ld_bf16(sm + GK_Q, cc, row, 64) * x[e];
+      }
+      // <S, dS'> over this thread's half of the row
+      float sd = 0.f;
+      for (int cc = wg * 64; cc < wg * 64 + 64; ++cc)
+        sd = fmaf(ld_bf16(sm + GK_S, row, cc, 128), ld_bf16(sm + GK_DS, row, cc, 128), sd);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
+      if (lane == 0) sdot[warp] = sd;
+      const float sb = colsum32(cb, lane);
+      const float sg = colsum32(cg, lane);
+      part[(0 * 4 + w4) * 64 + cb0 + lane] = sb;
+      part[(1 * 4 + w4) * 64 + cb0 + lane] = sg;
+    }
+    handoff();
+    // ---- M3: dKd^T, dO V_new^T, Y^T = dW^T T, dV_new V^T, dW K^T
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        mma_ss(tb + GT_S4, desc_mn(s_ds, 128, ks), desc_mn(s_vn, 128, ks), idesc(128, 64, 1, 1), ks > 0);
+        mma_ss(tb + GT_S5, desc_k(s_do, 64, ks), desc_mn(s_vn, 128, ks), idesc(64, 64, 0, 1), ks > 0);
+        mma_ss(tb + GT_S2, desc_mn(s_dv, 128, ks), desc_k(s_v, 64, ks), idesc(64, 64, 1, 0), ks > 0);
+        mma_ss(tb + GT_S3, desc_mn(s_wd, 128, ks), desc_k(s_k, 64, ks), idesc(64, 64, 1, 0), ks > 0);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ss(tb + GT_S0, desc_k(s_wd, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
+      mma_commit(&mma_bar);
+    }
+    if (!(ok = mma_sync_wait())) break;
+    {  // H3
+      float x[32], cz[32], cy[32];
+      tld32(GT_S4, x);   // dKd^T, row = dk index
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int cc = cb0 + e;
+        const float dec = cc < L ? expf(GL - Gs[cc]) : 0.f;
+        dk_acc[e] = fmaf(dec, x[e], dk_acc[e]);
+        cz[e] = rk[cc] * ld_bf16(sm + GK_K, cc, row, 64) * x[e];
+      }
+      tld32(GT_S0, x);   // Y^T = dW^T T
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int cc = cb0 + e;
+        dk_acc[e] = fmaf(bs[cc] * gs[cc], x[e], dk_acc[e]);
+        cy[e] = rk[cc] * ld_bf16(sm + GK_K, cc, row, 64) * x[e];
+      }
+      const float sz = colsum32(cz, lane);
+      const float sy = colsum32(cy, lane);
+      part[(2 * 4 + w4) * 64 + cb0 + lane] = sz;
+      part[(3 * 4 + w4) * 64 + cb0 + lane] = sy;
+      // M = 64 results: rows r64 (lanes < 16)
+      float daq[32], qk[32], t1[32], t2[32];
+      tld32(GT_S5, daq);
+      tld32(GT_QK, qk);
+      tld32(GT_S2, t1);
+      tld32(GT_S3, t2);
+      if (lane < 16) {
+        const int r = r64;
+        const float Gr = Gs[r];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float h1[8], h2[8], dt[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int jj = q4 * 8 + e, cc = cb0 + jj;
+            const bool live = cc <= r && r < L;
+            const float gam = live ? expf(Gr - Gs[cc]) : 0.f;
+            const float dA = live ? a.scale * daq[jj] : 0.f;
+            Cm[r * 64 + cc] = dA * gam * rq[r] * rk[cc] * qk[jj];
+            h1[e] = rk[cc] * gam * dA;
+            h2[e] = rq[r] * gam * dA;
+            dt[e] = bs[cc] * fmaf(gs[cc] * rk[cc], t2[jj], t1[jj]);
+          }
+          store_chunk8(sm + GK_H1, r, (cb0 >> 3) + q4, 64, h1);
+          store_chunk8(sm + GK_H2, r, (cb0 >> 3) + q4, 64, h2);
+          store_chunk8(sm + GK_DT, r, (cb0 >> 3) + q4, 64, dt);
+        }
+      }
+    }
+    handoff();
+    // ---- M4: R1 = dT T^T, K^T H1 (-> dq^), Q^T H2 (-> dk^)
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        mma_ss(tb + GT_S1, desc_k(s_dt, 64, ks), desc_k(s_t, 64, ks), idesc(64, 64, 0, 0), ks > 0);
+        mma_ss(tb + GT_S4, desc_mn(s_k, 64, ks), desc_k(s_h1, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+        mma_ss(tb + GT_S5, desc_mn(s_q, 64, ks), desc_mn(s_h2, 64, ks), idesc(128, 64, 1, 1), ks > 0);
+      }
+      mma_commit(&mma_bar);
+    }
+    if (!(ok = mma_sync_wait())) break;
+    {  // H4
+      float x[32];
+      tld32(GT_S4, x);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dq_acc[e] += x[e];
+      tld32(GT_S5, x);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dk_acc[e] += x[e];
+      tld32(GT_S1, x);
+      if (lane < 16) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) store_chunk8(sm + GK_R1, r64, (cb0 >> 3) + q4, 64, x + q4 * 8);
+      }
+    }
+    handoff();
+    // ---- M5: T^T R1 (= -dA)
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ss(tb + GT_S0, desc_mn(s_t, 64, ks), desc_mn(s_r1, 64, ks), idesc(64, 64, 1, 1), ks > 0);
+      mma_commit(&mma_bar);
+    }
+    if (!(ok = mma_sync_wait())) break;
+    {  // H5: dA rows -> dbeta row terms, C, F1, F2
+      float x[32], kk[32];
+      tld32(GT_S0, x);
+      tld32(GT_KK, kk);
+      if (lane < 16) {
+        const int r = r64;
+        const float Gr = Gs[r], br = bs[r];
+        float rb = 0.f;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float f1[8], f2[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int jj = q4 * 8 + e, cc = cb0 + jj;
+            const bool live = cc < r && r < L;
+            const float gam = live ? expf(Gr - Gs[cc]) : 0.f;
+            const float dA = live ? -x[jj] : 0.f;
+            const float base = dA * gam * rk[r] * rk[cc] * kk[jj];   // dA . (A / beta_r)
+            rb += base;
+            Cm[r * 64 + cc] += br * base;
+            const float E = dA * br * gam;
+            f1[e] = rk[cc] * E;
+            f2[e] = rk[r] * E;
+          }
+          store_chunk8(sm + GK_F1, r, (cb0 >> 3) + q4, 64, f1);
+          store_chunk8(sm + GK_F2, r, (cb0 >> 3) + q4, 64, f2);
+        }
+        rowB[wg][r] = rb;
+      }
+    }
+    handoff();
+    // ---- M6: K^T F1 + K^T F2 (-> dk^)
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ss(tb + GT_S2, desc_mn(s_k, 64, ks), desc_k(s_f1, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ss(tb + GT_S2, desc_mn(s_k, 64, ks), desc_mn(s_f2, 64, ks), idesc(128, 64, 1, 1), 1u);
+      mma_commit(&mma_bar);
+    }
+    if (!(ok = mma_sync_wait())) break;
+    {
+      float x[32];
+      tld32(GT_S2, x);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dk_acc[e] += x[e];
+    }
+    __syncthreads();
+    // ---- per-token totals: dbeta, dG -> dg (threads 0..63, token r)
+    if (tid < 64) {
+      const int r = tid;
+      float sb = 0.f, sg = 0.f, sz = 0.f, sy = 0.f, rowc = 0.f, colc = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        sb += part[(0 * 4 + w) * 64 + r];
+        sg += part[(1 * 4 + w) * 64 + r];
+        sz += part[(2 * 4 + w) * 64 + r];
+        sy += part[(3 * 4 + w) * 64 + r];
+      }
+      for (int cc = 0; cc < 64; ++cc) {
+        rowc += Cm[r * 64 + cc];
+        colc += Cm[cc * 64 + r];
+      }
+      const float dec = r < L ? expf(GL - Gs[r]) : 0.f;
+      const float z = dec * sz;
+      float dG = sg - z + bs[r] * gs[r] * sy + rowc - colc;
+      const float db = sb + gs[r] * sy + rowB[0][r] + rowB[1][r];
+      // chunk-end terms: gamma_L <S, dS'> and sum_c z_c
+      float zs = z;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
+      __shared__ float zpart[2];
+      if (lane == 0) zpart[warp] = zs;
+      named_bar(1, 64);
+      if (r == L - 1) {
+        float sd = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) sd += sdot[w];
+        dG += gL * sd + zpart[0] + zpart[1];
+      }
+      if (r >= L) dG = 0.f;
+      // dg_r = sum_{i >= r} dG_i (reverse inclusive scan over 64 tokens)
+      __shared__ float dgs[64];
+      dgs[r] = dG;
+      named_bar(1, 64);
+      float acc = 0.f;
+      for (int i = 63; i >= r; --i) acc += dgs[i];
+      if (r < L) {
+        a.dg[(size_t)(tok0 + r) * a.HV + hv] = acc;
+        a.dbeta[(size_t)(tok0 + r) * a.HV + hv] = db;
+      }
+      named_bar(1, 64);
+    }
+    __syncthreads();
+    if (tid == 0 && h + 1 < a.G) issue_vhead(hv + 1, false);
+  }
+
+  // ---- L2-norm backward of the group sums, then dq, dk
+  if (ok) {
+    float pq[32], pk[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int cc = cb0 + e;
+      pq[e] = ld_bf16(sm + GK_Q, cc, row, 64) * dq_acc[e];
+      pk[e] = ld_bf16(sm + GK_K, cc, row, 64) * dk_acc[e];
+    }
+    const float sq = colsum32(pq, lane), sk = colsum32(pk, lane);
+    part[(4 * 4 + w4) * 64 + cb0 + lane] = sq;
+    part[(5 * 4 + w4) * 64 + cb0 + lane] = sk;
+    __syncthreads();
+    __nv_bfloat16* dqp = a.dq + ((size_t)tok0 * a.H + j) * D + row;
+    __nv_bfloat16* dkp = a.dk + ((size_t)tok0 * a.H + j) * D + row;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int cc = cb0 + e;
+      if (cc >= L) continue;
+      float outq = dq_acc[e], outk = dk_acc[e];
+      if (a.l2norm) {
+        float xq = 0.f, xk = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          xq += part[(4 * 4 + w) * 64 + cc];
+          xk += part[(5 * 4 + w) * 64 + cc];
+        }
+        const float nq = rq[cc], nk = rk[cc];
+        outq = nq * dq_acc[e] - ld_bf16(sm + GK_Q, cc, row, 64) * xq * nq * nq * nq;
+        outk = nk * dk_acc[e] - ld_bf16(sm + GK_K, cc, row, 64) * xk * nk * nk * nk;
+      }
+      dqp[(size_t)cc * a.H * D] = __float2bfloat16_rn(outq);
+      dkp[(size_t)cc * a.H * D] = __float2bfloat16_rn(outk);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+// ===========================================================================
+// host side
+// ===========================================================================
+void setup_bwd_attrs() {
+  cudaFuncSetAttribute(bwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BS_SMEM_ALLOC);
+  cudaFuncSetAttribute(grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GK_SMEM_ALLOC);
+  cudaFuncSetAttribute(merge_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 128 * 129 * 4);
+}
+
+gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const void* k, const void* v,
+                   const float* g, const float* beta, const int32_t* cu_dev, const void* dO, const void* saved,
+                   void* dq, void* dk, void* dv, float* dg, float* dbeta, uint8_t* ws, cudaStream_t s) {
+  gdn_status st = run_tables(P, &pr, cu_dev, ws, nullptr, s);
+  if (st != GDN_OK) return st;
+  {
+    CheckArgs ca;
+    ca.saved = static_cast<const uint8_t*>(saved);
+    SavedHeader h;
+    memset(&h, 0, sizeof(h));
+    h.magic = SAVED_MAGIC;
+    h.version = SAVED_VERSION;
+    h.T = P.T;
+    h.N = P.N;
+    h.H = P.H;
+    h.HV = P.HV;
+    h.dk = pr.dk;
+    h.dv = pr.dv;
+    h.l2norm = pr.l2norm ? 1 : 0;
+    h.NC = P.NC;
+    h.NSEG = P.NSEG;
+    h.nsplit = P.nsplit;
+    h.seg_len = P.seg_len;
+    memcpy(&h.scale_bits, &pr.scale, 4);
+    h.cu_hash = P.cu_hash;
+    ca.expect = h;
+    ca.err = reinterpret_cast<int*>(ws);
+    check_saved_kernel<<<1, 1, 0, s>>>(ca);
+  }
+  if (P.NC == 0) return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  st = run_prep(P, &pr, q, k, g, beta, ws, 1, s);
+  if (st != GDN_OK) return st;
+  Tables t = tables_at(P, ws);
+  const uint8_t* sv = static_cast<const uint8_t*>(saved);
+  BScanArgs ba;
+  memset(&ba, 0, sizeof(ba));
+  if (!make_tmap(&ba.tq, q, P.T, P.H) || !make_tmap(&ba.tk, k, P.T, P.H) || !make_tmap(&ba.tdo, dO, P.T, P.HV))
+    return GDN_ERR_CUDA;
+  ba.cb = ws + P.o_cb;
+  ba.chunk_tok0 = t.chunk_tok0;
+  ba.seg_c0 = t.seg_c0;
+  ba.seg_c1 = t.seg_c1;
+  ba.seg_split = t.seg_split;
+  ba.split_seg = t.split_seg;
+  ba.HV = P.HV;
+  ba.G = P.G;
+  ba.nsplit = P.nsplit;
+  ba.scale = pr.scale;
+  ba.dtape = ws + P.o_dtape;
+  ba.ds_init = reinterpret_cast<const float*>(ws + P.o_dsinit);
+  ba.dbend = reinterpret_cast<float*>(ws + P.o_dbend);
+  ba.err = reinterpret_cast<int*>(ws);
+  if (P.nsplit > 0) {
+    ba.walk = 1;
+    bwd_scan_kernel<<<P.nsplit * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
+    MergeBwdArgs ma;
+    ma.sdoc_first = t.sdoc_first;
+    ma.dbend = ba.dbend;
+    ma.mend = reinterpret_cast<const float*>(sv + P.s_mseg);
+    ma.ds_init = reinterpret_cast<float*>(ws + P.o_dsinit);
+    ma.HV = P.HV;
+    ma.err = ba.err;
+    merge_bwd_kernel<<<dim3(P.nsdoc, P.HV), 256, 2 * 128 * 129 * 4, s>>>(ma);
+  }
+  ba.walk = 0;
+  bwd_scan_kernel<<<P.NSEG * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
+
+  GradArgs ga;
+  memset(&ga, 0, sizeof(ga));
+  ga.tq = ba.tq;
+  ga.tk = ba.tk;
+  ga.tdo = ba.tdo;
+  if (!make_tmap(&ga.tv, v, P.T, P.HV)) return GDN_ERR_CUDA;
+  ga.q = static_cast<const __nv_bfloat16*>(q);
+  ga.k = static_cast<const __nv_bfloat16*>(k);
+  ga.g = g;
+  ga.beta = beta;
+  ga.cb = ws + P.o_cb;
+  ga.tape = sv + P.s_tape;
+  ga.dtape = ws + P.o_dtape;
+  ga.chunk_tok0 = t.chunk_tok0;
+  ga.chunk_len = t.chunk_len;
+  ga.dq = static_cast<__nv_bfloat16*>(dq);
+  ga.dk = static_cast<__nv_bfloat16*>(dk);
+  ga.dv = static_cast<__nv_bfloat16*>(dv);
+  ga.dg = dg;
+  ga.dbeta = dbeta;
+  ga.H = P.H;
+  ga.HV = P.HV;
+  ga.G = P.G;
+  ga.l2norm = pr.l2norm ? 1 : 0;
+  ga.scale = pr.scale;
+  ga.err = reinterpret_cast<int*>(ws);
+  grad_kernel<<<dim3(P.NC, P.H), 256, GK_SMEM_ALLOC, s>>>(ga);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 }  // namespace gdn

@@ -19,8 +19,9 @@
 // M_seg and the merges that read them):
 //   full (walk = 0)  every segment, from its true start state; writes o, tape
 //   B    (walk = 1)  segment from a zero state; writes its end state B_p^T
-//   M    (walk = 2)  segment with U = 0 from S^T = I; its end state is
-//                    M_p^T, the transfer of the segment (S_end = M_p S_start + B_p)
+//   M    (walk = 2)  the segment after a split point, with U = 0 from S^T = I;
+//                    its end state is M^T, the transfer of that segment
+//                    (S_end = M S_start + B)
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 
@@ -68,7 +69,9 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
     const int bb = blockIdx.x % half;
     split = bb / a.HV;
     hv = bb % a.HV;
-    seg = a.split_seg[split];
+    // B walks run on split segment p, M walks on segment p + 1: the merges
+    // use M_1 .. M_{P-1} (M_0 only ever multiplies the zero start state)
+    seg = a.split_seg[split] + (mode == 2 ? 1 : 0);
   }
   const int kh = hv / a.G;
   const int c0 = a.seg_c0[seg], nch = a.seg_c1[seg] - c0;
@@ -282,7 +285,8 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
 }
 
 // S^T_{p+1} = S^T_p M_p^T + B_p^T, S_0 = 0, for the split segments of one
-// document and value head; s_init[i] = start state of the segment after split i.
+// document and value head; s_init[i] = start state of the segment after split
+// i, bend[i] = B of split segment i, mend[i] = M^T of the segment after it.
 __global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   float* Sp = reinterpret_cast<float*>(smem_raw);          // [128][129]
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
   __syncthreads();
   const int r0 = (tid >> 4) * 8, cc0 = (tid & 15) * 8;
   for (int p = f0 + 1; p < f1; ++p) {
-    const float* M = a.mend + (size_t)p * stride + (size_t)hv * STATE_F32;
+    const float* M = a.mend + (size_t)(p - 1) * stride + (size_t)hv * STATE_F32;
     const float* B = a.bend + (size_t)p * stride + (size_t)hv * STATE_F32;
     for (int i = tid; i < STATE_F32; i += 256) Mt[(i >> 7) * 129 + (i & 127)] = M[i];
     __syncthreads();
