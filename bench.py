@@ -1,0 +1,442 @@
+"""Benchmark of the GB300 chunked Gated DeltaNet training step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 2] [--op fwd+bwd|fwd|ckpt]
+
+A step is one pass of the whole hot path over one batch: gdn_fwd (writing the
+saved states) + gdn_bwd on the packed 4-document workload of 262,144 tokens
+with H = 16 q/k heads, HV = 48 value heads, head dim 128 (the pages' "shape
+A").  Inputs are seeded synthetic tensors already resident in HBM; they are
+far larger than L2 (no flush needed).  Prints one JSON line.
+
+Multi-GPU: the path has no exchange step, so N GPUs run N independent
+replicas (one process per GPU under torchrun); value = all tokens processed /
+the slowest rank's time.
+
+--impl reference times the FP64 CPU oracle (the only other implementation
+there is) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN fwd+bwd Mtokens/s on 1 GB300 (H16/HV48, d=128); % BF16 tensor-core peak"
+UNIT = "Mtokens/s"
+D = 128
+C = 64
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work per kernel launch: the dense tile products the chunked
+# method needs (KK^T, QK^T once per q/k head; the O(C^3) inverse not counted)
+# ---------------------------------------------------------------------------
+def chunk_lens(w):
+    out = []
+    for n in w.doc_lens:
+        out += [C] * (n // C) + ([n % C] if n % C else [])
+    return out
+
+
+def kernel_flops(name, w):
+    """FLOPs of one launch of `name` on workload w (real chunk lengths)."""
+    Ls = chunk_lens(w)
+    HV, H = w.HV, w.H
+    if name == "fwd_scan_kernel":        # W, U, Aqk V_new (C^2 d) + W S, S Q, Kd^T V_new (C d^2)
+        return sum(HV * (3 * 2 * L * L * D + 3 * 2 * L * D * D) for L in Ls)
+    if name == "bwd_scan_kernel":        # W, dO^T Aqk (C^2 d) + dS' K^T, dV W, dO' Q (C d^2)
+        return sum(HV * (2 * 2 * L * L * D + 3 * 2 * L * D * D) for L in Ls)
+    if name == "grad_kernel":            # 5 C d^2, 12 C^2 d, 2 C^3 per v-head; KK^T, QK^T per q/k head
+        return sum(HV * (5 * 2 * L * D * D + 12 * 2 * L * L * D + 2 * 2 * L ** 3) + H * 2 * 2 * L * L * D
+                   for L in Ls)
+    if name == "prep_kernel":            # KK^T, QK^T per q/k head
+        return sum(H * 2 * 2 * L * L * D for L in Ls)
+    return 0
+
+
+def kernel_bytes(name, w):
+    """Algorithmic HBM bytes of one launch (each input read once, each output written once)."""
+    T, H, HV, NC = w.T, w.H, w.HV, w.num_chunks
+    cb_fwd = 3 * 8192 + 1024
+    if name == "prep_kernel":
+        return T * H * D * 2 * 2 + T * HV * 8 + NC * HV * cb_fwd
+    if name == "fwd_scan_kernel":
+        return T * H * D * 2 * 2 + T * HV * D * 2 * 2 + NC * HV * (cb_fwd + 32768)
+    if name == "bwd_scan_kernel":
+        return T * H * D * 2 * 2 + T * HV * D * 2 + NC * HV * (2 * 8192 + 1024 + 32768)
+    if name == "grad_kernel":
+        return (T * H * D * 2 * 2 * 2 + T * HV * D * 2 * 3 + T * HV * 8 * 2
+                + NC * HV * (8192 + 1024 + 2 * 32768))
+    return 0
+
+
+def step_flops(w, op):
+    Ls = chunk_lens(w)
+    f_fwd = sum(w.HV * (6 * L * D * D + 6 * L * L * D) + w.H * 4 * L * L * D for L in Ls)
+    f_bwd = sum(w.HV * (14 * L * D * D + 24 * L * L * D) + w.H * 4 * L * L * D for L in Ls)
+    return {"fwd": f_fwd, "fwd+bwd": f_fwd + f_bwd, "ckpt": 2 * f_fwd + f_bwd}[op]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        m = json.load(open(p))
+        return {"hbm_gbs": m["hbm_gbs"], "bf16_tflops": m["bf16_tflops"],
+                "bf16_tflops_sustained": m.get("bf16_tflops_sustained", m["bf16_tflops"]), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+def source_hash():
+    h = hashlib.sha256()
+    cs = os.path.join(ROOT, "linear_attention_gdn_gb300", "csrc")
+    for f in sorted(os.listdir(cs)):
+        h.update(open(os.path.join(cs, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    m = json.load(open(p))
+    if m.get("source_hash") != source_hash():
+        return None
+    k = m.get("kernels", {}).get(kernel)
+    return None if k is None else k.get("dram_bytes_per_launch_full")
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu):
+        self.gpu = gpu
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi"] + (["-i", str(self.gpu)] if self.gpu else []) +
+                                         [f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import linear_attention_gdn_gb300 as gdn
+    from linear_attention_gdn_gb300 import inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = inputs.workload(args.workload)
+    x = inputs.generate(w, dev)
+    cu_dev = torch.from_numpy(w.cu_seqlens).to(dev)
+    prob = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm, w.segments)
+    buf = gdn.Buffers(prob, w.cu_seqlens, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    o = torch.empty((w.T, w.HV, D), dtype=torch.bfloat16, device=dev)
+    dq, dk = torch.empty_like(x["q"]), torch.empty_like(x["k"])
+    dv = torch.empty_like(x["v"])
+    dg, db = torch.empty_like(x["g"]), torch.empty_like(x["beta"])
+
+    def step(op, xx=x):
+        if op in ("fwd", "fwd+bwd"):
+            gdn.gdn_fwd(prob, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_dev, w.cu_seqlens, o,
+                        buf.saved, buf.workspace, stream=stream)
+        if op == "fwd+bwd":
+            gdn.gdn_bwd(prob, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_dev, w.cu_seqlens, xx["dO"],
+                        buf.saved, dq, dk, dv, dg, db, buf.workspace, stream=stream)
+        if op == "ckpt":
+            gdn.gdn_ckpt_fwd_bwd(prob, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_dev, w.cu_seqlens,
+                                 xx["dO"], o, dq, dk, dv, dg, db, buf.saved, buf.workspace, stream=stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def allmax(v):
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([v], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return t.item()
+        return v
+
+    def timed(op, K, W):
+        for _ in range(W):
+            step(op)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            step(op)
+        e1.record(stream)
+        barrier()
+        return allmax(e0.elapsed_time(e1) / K)
+
+    op = args.op
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    gdn.gdn_profile_read_all()                      # reset the launch counters
+    with ClockSampler(uuid) as clk:
+        ms = timed(op, args.steps, args.warmup)
+    launches = gdn.gdn_profile_read_all()
+    st = gdn.gdn_device_status(buf.workspace, stream)
+    assert st == 0, gdn.gdn_status_string(st)
+    n_launch = sum(v["launches"] for v in launches.values())
+    n_launch = int(round(n_launch * args.steps / (args.steps + args.warmup)))
+
+    # per-kernel device times over a second timed pass with launch events
+    gdn.gdn_profile_enable(1)
+    timed(op, args.steps, 1)
+    gdn.gdn_profile_enable(0)
+    kstats = gdn.gdn_profile_read_all()
+
+    extra = {}
+    if not args.quick:
+        for other in ("fwd", "ckpt"):
+            if other != op:
+                t_o = timed(other, max(3, args.steps // 2), 2)
+                extra[other] = {"ms": round(t_o, 4), "Mtokens_per_s": round(world * w.T / t_o / 1e3, 3),
+                                "TFLOP_per_s": round(world * step_flops(w, other) / t_o / 1e9, 1)}
+
+    # end to end through the C ABI with pinned host buffers: every step copies
+    # its inputs in and all of its outputs back
+    e2e = None
+    if not args.no_e2e:
+        names_in = ("q", "k", "v", "g", "beta", "dO")
+        h_in = {n: x[n].to("cpu").pin_memory() for n in names_in}
+        outs = (o, dq, dk, dv, dg, db) if op != "fwd" else (o,)
+        h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        d_in = {n: torch.empty_like(x[n]) for n in names_in}
+        h_cu = torch.from_numpy(w.cu_seqlens).pin_memory()
+        bi = sum(t.numel() * t.element_size() for t in h_in.values()) + w.cu_seqlens.nbytes
+        bo = sum(t.numel() * t.element_size() for t in h_out)
+
+        def e2e_step():
+            cu_dev.copy_(h_cu, non_blocking=True)
+            for n in names_in:
+                d_in[n].copy_(h_in[n], non_blocking=True)
+            step(op, d_in)
+            for hb, dbuf in zip(h_out, outs):
+                hb.copy_(dbuf, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        ke = max(2, min(args.steps, 5))
+        t0 = time.perf_counter()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        ms_e2e = allmax(max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3) / ke)
+        e2e = {"value": round(world * w.T / ms_e2e / 1e3, 3), "unit": UNIT, "h2d_bytes_per_step": int(bi),
+               "d2h_bytes_per_step": int(bo), "ms_per_step": round(ms_e2e, 3)}
+
+    if rank != 0:
+        return None
+    pk = peaks()
+    kt = {k: v for k, v in kstats.items() if v["timed_launches"] > 0}
+    top = max(kt, key=lambda k: kt[k]["total_ms"])
+    per_launch_ms = kt[top]["total_ms"] / kt[top]["timed_launches"]
+    fl = kernel_flops(top, w)
+    if fl > 0:
+        achieved = fl / (per_launch_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops_sustained"], 4)}
+        note = f"{pk['src']} sustained BF16 (the kernel is timed inside a multi-ms step)"
+    else:
+        by = kernel_bytes(top, w)
+        achieved = by / (per_launch_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 4)}
+        note = f"{pk['src']} HBM copy bandwidth"
+    roof.update({"traffic": ncu_traffic(top), "kernel": top, "peak_note": note,
+                 "launch_ms": round(per_launch_ms, 4), "algorithmic_flops_per_launch": fl,
+                 "algorithmic_bytes_per_launch": kernel_bytes(top, w),
+                 "achieved_hbm_gbs": round(kernel_bytes(top, w) / (per_launch_ms * 1e-3) / 1e9, 1)})
+    tot = sum(u["total_ms"] for u in kt.values())
+    kernels = {}
+    for k, v in kt.items():
+        f, b = kernel_flops(k, w), kernel_bytes(k, w)
+        kernels[k] = {"launches_per_step": round(v["launches"] / args.steps, 2),
+                      "ms_per_step": round(v["total_ms"] / args.steps, 4), "share": round(v["total_ms"] / tot, 4),
+                      "TFLOP_per_s": round(f * v["timed_launches"] / v["total_ms"] / 1e9, 1) if f else None,
+                      "GB_per_s": round(b * v["timed_launches"] / v["total_ms"] / 1e6, 1) if b else None}
+    tflops = world * step_flops(w, op) / ms / 1e9
+    in_gb = sum(x[n].numel() * x[n].element_size() for n in ("q", "k", "v", "g", "beta", "dO")) / 1e9
+    return {
+        "metric": METRIC, "value": round(world * w.T / ms / 1e3, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.T, "docs": w.doc_lens, "H": w.H, "HV": w.HV, "dk": D,
+                   "dv": D, "chunk": C, "l2norm": w.l2norm, "op": op,
+                   "l2_flush": f"none needed: {in_gb:.1f} GB of inputs per step exceed the 129 MB L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tflops": round(tflops, 1), "tensor_frac_of_step": round(tflops / pk["bf16_tflops_sustained"], 4),
+        "roofline": roof, "kernels": kernels, "gpu_launches": n_launch, "clocks": clk.summary(),
+        "e2e": e2e, "ops": extra,
+    }
+
+
+# ---------------------------------------------------------------------------
+# the FP64 CPU oracle on a bounded sample of the same workload
+# ---------------------------------------------------------------------------
+def oracle_sample(w, tokens_per_unit, units, threads):
+    """Run `units` q/k-head-group jobs of the oracle, fwd+bwd, each over a
+    `tokens_per_unit`-token document (an exact sub-problem with the workload's
+    head counts and distributions), in parallel.  Returns (seconds, rate in
+    Mtokens/s of the full HV-head problem)."""
+    from linear_attention_gdn_gb300 import inputs
+    from oracle import ref
+
+    small = inputs.custom([tokens_per_unit], w.H, w.HV, w.l2norm, w.g_lo, w.g_hi, seed=w.seed)
+    x = inputs.generate(small, "cpu")
+    G = w.HV // w.H
+    us = [ref.Unit(0, u % w.H, 0, tokens_per_unit, 0, tokens_per_unit) for u in range(units)]
+    t0 = time.perf_counter()
+    ref.run(x, w.H, w.HV, l2norm=w.l2norm, scale=w.scale, units=us, threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, units * tokens_per_unit * G / w.HV / dt / 1e6
+
+
+def cpu_count():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    from linear_attention_gdn_gb300 import inputs
+    w = inputs.workload(args.workload)
+    threads = cpu_count()
+    tpu = 1024
+    res = []
+    for i in range(args.warmup + args.steps):
+        dt, rate = oracle_sample(w, tpu, threads, threads)
+        if i >= args.warmup:
+            res.append((dt, rate))
+    dt = statistics.median(t[0] for t in res)
+    rate = statistics.median(t[1] for t in res)
+    sample = (f"{threads} q/k-head groups x {tpu}-token document (3 value heads each), fwd+bwd, per step; "
+              f"rate scaled to all {w.HV} value heads")
+    return {"impl": "reference", "metric": METRIC, "value": round(rate, 6), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "op": "fwd+bwd", "sample": sample},
+            "cpu_baseline": {"value": round(rate, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(rate, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--op", default="fwd+bwd", choices=("fwd", "fwd+bwd", "ckpt"))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--quick", action="store_true", help="skip the extra fwd / ckpt timings")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args), allow_nan=False), flush=True)
+        return
+    args.warmup = max(args.warmup, 3)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    out = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu:
+            from linear_attention_gdn_gb300 import inputs
+            w = inputs.workload(args.workload)
+            threads = cpu_count()
+            dt, rate = oracle_sample(w, 8192, threads, threads)
+            out["cpu_baseline"] = {"value": round(rate, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+                                   "sample": f"{threads} q/k-head groups x 8192-token document, fwd+bwd, "
+                                             f"{dt:.1f} s; rate scaled to all {w.HV} value heads"}
+        print(json.dumps(out, allow_nan=False), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -155,6 +155,25 @@ gdn_status gdn_chunk_table_offsets(const gdn_problem *prob, const int32_t *cu_se
                                    size_t offsets[4], int32_t *num_chunks);
 
 /*
+ * Optional per-kernel timing, for benchmarks and tools.  The library counts
+ * every kernel it launches; while profiling is enabled it also records a CUDA
+ * event pair on the launching stream around each launch.  gdn_profile_read()
+ * synchronises on the recorded events, fills up to max_entries records (one
+ * per kernel that launched since the last read: its name, the number of
+ * launches, how many of them were timed, and their summed device time in ms),
+ * resets the counters and returns the number of kernels with launches.  The
+ * bookkeeping is process-wide and thread-safe.
+ */
+typedef struct {
+    const char *name;
+    long long launches;
+    long long timed_launches;
+    double total_ms;
+} gdn_kernel_stat;
+void gdn_profile_enable(int on);
+int gdn_profile_read(gdn_kernel_stat *out, int max_entries);
+
+/*
  * The segment length (in 64-token chunks) the planner uses for this problem:
  * documents longer than this are split into ceil(chunks / seg) segments whose
  * transfer operators are composed by a merge kernel (the intra-GPU segment

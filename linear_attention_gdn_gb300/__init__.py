@@ -20,13 +20,19 @@ LIB_PATH = _build.LIB
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_WORKSPACE_TOO_SMALL",
           4: "GDN_ERR_SAVED_MISMATCH", 5: "GDN_ERR_CUDA", 6: "GDN_ERR_TIMEOUT", 7: "GDN_ERR_DEVICE"}
 EXPORTS = ("gdn_saved_bytes", "gdn_fwd", "gdn_bwd", "gdn_ckpt_fwd_bwd", "gdn_status_string",
-           "gdn_device_status", "gdn_plan_segment_chunks", "gdn_chunk_table_offsets")
+           "gdn_device_status", "gdn_plan_segment_chunks", "gdn_chunk_table_offsets", "gdn_profile_enable",
+           "gdn_profile_read")
 
 
 class GDNError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         super().__init__(f"{where}: {STATUS.get(status, status)} ({gdn_status_string(status)})")
+
+
+class gdn_kernel_stat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_longlong), ("timed_launches", ctypes.c_longlong),
+                ("total_ms", ctypes.c_double)]
 
 
 class gdn_problem(ctypes.Structure):
@@ -56,6 +62,10 @@ def _load():
     L.gdn_plan_segment_chunks.argtypes = [pp, i32p]
     L.gdn_plan_segment_chunks.restype = ctypes.c_int32
     L.gdn_chunk_table_offsets.argtypes = [pp, i32p, ctypes.POINTER(sz), i32p]
+    L.gdn_profile_enable.argtypes = [ctypes.c_int]
+    L.gdn_profile_enable.restype = None
+    L.gdn_profile_read.argtypes = [ctypes.POINTER(gdn_kernel_stat), ctypes.c_int]
+    L.gdn_profile_read.restype = ctypes.c_int
     for name in ("gdn_saved_bytes", "gdn_fwd", "gdn_bwd", "gdn_ckpt_fwd_bwd", "gdn_device_status",
                  "gdn_chunk_table_offsets"):
         getattr(L, name).restype = ctypes.c_int
@@ -162,6 +172,22 @@ def gdn_ckpt_fwd_bwd(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, dO
                                 ctypes.cast(_ptr(cu_seqlens_dev), ctypes.POINTER(ctypes.c_int32)), cup, _ptr(dO),
                                 _ptr(o), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(saved_scratch),
                                 _ptr(workspace), ws_bytes, _stream(stream)), "gdn_ckpt_fwd_bwd")
+
+
+def gdn_profile_enable(on: int) -> None:
+    lib.gdn_profile_enable(int(on))
+
+
+def gdn_profile_read(out, max_entries: int) -> int:
+    return int(lib.gdn_profile_read(out, int(max_entries)))
+
+
+def gdn_profile_read_all() -> dict:
+    """{kernel name: {launches, timed_launches, total_ms}} since the last read."""
+    arr = (gdn_kernel_stat * 32)()
+    n = gdn_profile_read(arr, 32)
+    return {arr[i].name.decode(): {"launches": arr[i].launches, "timed_launches": arr[i].timed_launches,
+                                   "total_ms": arr[i].total_ms} for i in range(min(n, 32))}
 
 
 def gdn_device_status(workspace, stream=None) -> int:

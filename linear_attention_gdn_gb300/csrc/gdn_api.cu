@@ -12,6 +12,7 @@
 
 #include "gdn.h"
 #include "gdn_internal.h"
+#include "gdn_prof.h"
 
 namespace gdn {
 void launch_tables(const TableArgs& a, cudaStream_t s);
@@ -20,6 +21,7 @@ void launch_fwd_scan(const ScanArgs& a, int nchains, cudaStream_t s);
 void launch_merge(const MergeArgs& a, int nsdoc, cudaStream_t s);
 void setup_fwd_scan_attrs();
 void setup_bwd_attrs();
+void setup_prep_attrs();
 gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const void* k, const void* v,
                    const float* g, const float* beta, const int32_t* cu_dev, const void* dO, const void* saved,
                    void* dq, void* dk, void* dv, float* dg, float* dbeta, uint8_t* ws, cudaStream_t s);
@@ -217,9 +219,57 @@ static bool device_setup() {
   if (!done[dev]) {
     setup_fwd_scan_attrs();
     setup_bwd_attrs();
+    setup_prep_attrs();
     done[dev] = true;
   }
   return true;
+}
+
+
+// ---------------------------------------------------------------------------
+// launch counters and optional per-kernel event timing
+// ---------------------------------------------------------------------------
+static const char* const kKernelNames[K_NUM] = {
+    "tables_scan_kernel", "tables_fill_kernel", "prep_kernel",    "fwd_scan_kernel(walk)",
+    "merge_kernel",       "fwd_scan_kernel",    "check_saved_kernel", "bwd_scan_kernel(walk)",
+    "merge_bwd_kernel",   "bwd_scan_kernel",    "grad_kernel"};
+struct ProfRec {
+  int id;
+  cudaEvent_t e0, e1;
+};
+static std::mutex g_prof_mu;
+static bool g_prof_on = false;
+static long long g_launches[K_NUM] = {};
+static std::vector<ProfRec> g_recs;
+static std::vector<cudaEvent_t> g_pool;
+static cudaEvent_t g_open[K_NUM] = {};
+
+static cudaEvent_t pool_get() {
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+void prof_begin(int id, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_launches[id] += 1;
+  if (!g_prof_on) return;
+  cudaEvent_t e = pool_get();
+  cudaEventRecord(e, s);
+  g_open[id] = e;
+}
+void prof_end(int id, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on || !g_open[id]) return;
+  cudaEvent_t e = pool_get();
+  cudaEventRecord(e, s);
+  g_recs.push_back({id, g_open[id], e});
+  g_open[id] = nullptr;
 }
 
 static bool aligned16(const void* p) { return p && ((uintptr_t)p & 15) == 0; }
@@ -424,6 +474,41 @@ gdn_status gdn_chunk_table_offsets(const gdn_problem* prob, const int32_t* cu_ho
   offsets[3] = P.o_tables[5];   // chunk_len
   *num_chunks = P.NC;
   return GDN_OK;
+}
+
+
+void gdn_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = on != 0;
+}
+
+int gdn_profile_read(gdn_kernel_stat* out, int max_entries) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  double ms[K_NUM] = {};
+  long long timed[K_NUM] = {};
+  for (const ProfRec& r : g_recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.e1) == cudaSuccess && cudaEventElapsedTime(&t, r.e0, r.e1) == cudaSuccess) {
+      ms[r.id] += t;
+      timed[r.id] += 1;
+    }
+    g_pool.push_back(r.e0);
+    g_pool.push_back(r.e1);
+  }
+  g_recs.clear();
+  int n = 0;
+  for (int i = 0; i < K_NUM; ++i) {
+    if (g_launches[i] == 0) continue;
+    if (out && n < max_entries) {
+      out[n].name = kKernelNames[i];
+      out[n].launches = g_launches[i];
+      out[n].timed_launches = timed[i];
+      out[n].total_ms = ms[i];
+    }
+    ++n;
+    g_launches[i] = 0;
+  }
+  return n;
 }
 
 gdn_status gdn_device_status(void* workspace, struct CUstream_st* stream) {

@@ -25,6 +25,7 @@
 #include "gdn.h"
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_prof.h"
 
 namespace gdn {
 
@@ -956,7 +957,9 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
     h.cu_hash = P.cu_hash;
     ca.expect = h;
     ca.err = reinterpret_cast<int*>(ws);
+    prof_begin(K_CHECK_SAVED, s);
     check_saved_kernel<<<1, 1, 0, s>>>(ca);
+    prof_end(K_CHECK_SAVED, s);
   }
   if (P.NC == 0) return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
   st = run_prep(P, &pr, q, k, g, beta, ws, 1, s);
@@ -983,7 +986,9 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
   ba.err = reinterpret_cast<int*>(ws);
   if (P.nsplit > 0) {
     ba.walk = 1;
+    prof_begin(K_BWD_WALK, s);
     bwd_scan_kernel<<<P.nsplit * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
+    prof_end(K_BWD_WALK, s);
     MergeBwdArgs ma;
     ma.sdoc_first = t.sdoc_first;
     ma.dbend = ba.dbend;
@@ -991,10 +996,14 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
     ma.ds_init = reinterpret_cast<float*>(ws + P.o_dsinit);
     ma.HV = P.HV;
     ma.err = ba.err;
+    prof_begin(K_BWD_MERGE, s);
     merge_bwd_kernel<<<dim3(P.nsdoc, P.HV), 256, 2 * 128 * 129 * 4, s>>>(ma);
+    prof_end(K_BWD_MERGE, s);
   }
   ba.walk = 0;
+  prof_begin(K_BWD_SCAN, s);
   bwd_scan_kernel<<<P.NSEG * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
+  prof_end(K_BWD_SCAN, s);
 
   GradArgs ga;
   memset(&ga, 0, sizeof(ga));
@@ -1022,7 +1031,9 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
   ga.l2norm = pr.l2norm ? 1 : 0;
   ga.scale = pr.scale;
   ga.err = reinterpret_cast<int*>(ws);
+  prof_begin(K_GRAD, s);
   grad_kernel<<<dim3(P.NC, P.H), 256, GK_SMEM_ALLOC, s>>>(ga);
+  prof_end(K_GRAD, s);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

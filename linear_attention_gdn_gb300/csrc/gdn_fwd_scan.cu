@@ -24,6 +24,7 @@
 //                    (S_end = M S_start + B)
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_prof.h"
 
 namespace gdn {
 
@@ -339,10 +340,17 @@ __global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
 }
 
 void launch_fwd_scan(const ScanArgs& a, int nchains, cudaStream_t s) {
-  if (nchains > 0) fwd_scan_kernel<<<nchains, 128, SC_SMEM_ALLOC, s>>>(a);
+  if (nchains <= 0) return;
+  const int id = a.walk ? K_FWD_WALK : K_FWD_SCAN;
+  prof_begin(id, s);
+  fwd_scan_kernel<<<nchains, 128, SC_SMEM_ALLOC, s>>>(a);
+  prof_end(id, s);
 }
 void launch_merge(const MergeArgs& a, int nsdoc, cudaStream_t s) {
-  if (nsdoc > 0) merge_kernel<<<dim3(nsdoc, a.HV), 256, 2 * 128 * 129 * 4, s>>>(a);
+  if (nsdoc <= 0) return;
+  prof_begin(K_FWD_MERGE, s);
+  merge_kernel<<<dim3(nsdoc, a.HV), 256, 2 * 128 * 129 * 4, s>>>(a);
+  prof_end(K_FWD_MERGE, s);
 }
 void setup_fwd_scan_attrs() {
   cudaFuncSetAttribute(fwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_SMEM_ALLOC);

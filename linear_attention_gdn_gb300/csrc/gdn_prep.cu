@@ -20,6 +20,7 @@
 // (M = 64) on the padded 64 x 64 operands.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_prof.h"
 
 namespace gdn {
 
@@ -327,13 +328,14 @@ __global__ void __launch_bounds__(128, 2) prep_kernel(PrepArgs a) {
   if (warp == 0) tmem_dealloc(tb, 128);
 }
 
+void setup_prep_attrs() {
+  cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM_ALLOC);
+}
 void launch_prep(const PrepArgs& a, int NC, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM_ALLOC);
-    attr = true;
-  }
-  if (NC > 0) prep_kernel<<<dim3(NC, a.H), 128, PREP_SMEM_ALLOC, s>>>(a);
+  if (NC <= 0) return;
+  prof_begin(K_PREP, s);
+  prep_kernel<<<dim3(NC, a.H), 128, PREP_SMEM_ALLOC, s>>>(a);
+  prof_end(K_PREP, s);
 }
 
 }  // namespace gdn

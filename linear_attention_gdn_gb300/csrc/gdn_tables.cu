@@ -11,6 +11,7 @@
 // this library's own definition.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_prof.h"
 
 namespace gdn {
 
@@ -136,9 +137,15 @@ __global__ void __launch_bounds__(256) tables_fill_kernel(TableArgs a) {
 }
 
 void launch_tables(const TableArgs& a, cudaStream_t s) {
+  prof_begin(K_TABLES_SCAN, s);
   tables_scan_kernel<<<1, 1024, 0, s>>>(a);
+  prof_end(K_TABLES_SCAN, s);
   const int n = a.NC > a.NSEG ? a.NC : a.NSEG;
-  if (n > 0) tables_fill_kernel<<<(n + 255) / 256, 256, 0, s>>>(a);
+  if (n > 0) {
+    prof_begin(K_TABLES_FILL, s);
+    tables_fill_kernel<<<(n + 255) / 256, 256, 0, s>>>(a);
+    prof_end(K_TABLES_FILL, s);
+  }
 }
 
 }  // namespace gdn
