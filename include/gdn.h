@@ -155,6 +155,38 @@ gdn_status gdn_chunk_table_offsets(const gdn_problem *prob, const int32_t *cu_se
                                    size_t offsets[4], int32_t *num_chunks);
 
 /*
+ * Forward for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this entry point; it exists for hosts that give a library
+ * only its inputs and outputs (plugin-style runtimes without a workspace
+ * query, or latency-bound paths that may not call cudaMalloc because it
+ * synchronises the device).
+ *
+ * It computes exactly what gdn_fwd(prob, ..., o, saved = NULL, ...) computes,
+ * with the workspace taken from a fixed array of GDN_FWD_NOALLOC_SCRATCH_BYTES
+ * (64 MiB) that the library keeps in device memory on every GPU where it is
+ * loaded, until the process exits.  Inputs and `o` are the caller's, as for
+ * gdn_fwd; no saved set is written (use gdn_fwd for training).
+ *   - A problem whose forward workspace exceeds 64 MiB is refused with
+ *     GDN_ERR_WORKSPACE_TOO_SMALL before any launch (at HV = 48 that is about
+ *     40 chunks of 64 tokens; see gdn_saved_bytes for the general size).
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array and the array keeps the last call's
+ *     contents; the forward rewrites everything it reads.  Calls that overlap
+ *     on the GPU (different streams, or different host threads) race on the
+ *     array and must be serialised by the caller.
+ *   - Device-side conditions (a bounded wait that ran out) are recorded in the
+ *     array, which the caller cannot address, so this entry point reports only
+ *     host-side statuses.
+ * No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+#define GDN_FWD_NOALLOC_SCRATCH_BYTES (64u << 20)
+gdn_status gdn_fwd_noalloc(const gdn_problem *prob, const void *q, const void *k, const void *v,
+                           const float *g, const float *beta, const int32_t *cu_seqlens_dev,
+                           const int32_t *cu_seqlens_host, void *o, struct CUstream_st *stream);
+
+/*
  * Optional per-kernel timing, for benchmarks and tools.  The library counts
  * every kernel it launches; while profiling is enabled it also records a CUDA
  * event pair on the launching stream around each launch.  gdn_profile_read()

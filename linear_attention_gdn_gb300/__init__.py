@@ -21,7 +21,7 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "G
           4: "GDN_ERR_SAVED_MISMATCH", 5: "GDN_ERR_CUDA", 6: "GDN_ERR_TIMEOUT", 7: "GDN_ERR_DEVICE"}
 EXPORTS = ("gdn_saved_bytes", "gdn_fwd", "gdn_bwd", "gdn_ckpt_fwd_bwd", "gdn_status_string",
            "gdn_device_status", "gdn_plan_segment_chunks", "gdn_chunk_table_offsets", "gdn_profile_enable",
-           "gdn_profile_read")
+           "gdn_profile_read", "gdn_fwd_noalloc")
 
 
 class GDNError(RuntimeError):
@@ -62,6 +62,8 @@ def _load():
     L.gdn_plan_segment_chunks.argtypes = [pp, i32p]
     L.gdn_plan_segment_chunks.restype = ctypes.c_int32
     L.gdn_chunk_table_offsets.argtypes = [pp, i32p, ctypes.POINTER(sz), i32p]
+    L.gdn_fwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, i32p, i32p, vp, vp]
+    L.gdn_fwd_noalloc.restype = ctypes.c_int
     L.gdn_profile_enable.argtypes = [ctypes.c_int]
     L.gdn_profile_enable.restype = None
     L.gdn_profile_read.argtypes = [ctypes.POINTER(gdn_kernel_stat), ctypes.c_int]
@@ -152,6 +154,15 @@ def gdn_fwd(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, o, saved, w
     _check(lib.gdn_fwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                        ctypes.cast(_ptr(cu_seqlens_dev), ctypes.POINTER(ctypes.c_int32)), cup, _ptr(o),
                        _ptr(saved), _ptr(workspace), ws_bytes, _stream(stream)), "gdn_fwd")
+
+
+def gdn_fwd_noalloc(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, o, stream=None):
+    """gdn_fwd without a caller workspace or saved set (the library's fixed
+    64 MiB device array serves as the workspace); see include/gdn.h."""
+    cu, cup = _cu_host(cu_seqlens_host)
+    _check(lib.gdn_fwd_noalloc(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                               ctypes.cast(_ptr(cu_seqlens_dev), ctypes.POINTER(ctypes.c_int32)), cup, _ptr(o),
+                               _stream(stream)), "gdn_fwd_noalloc")
 
 
 def gdn_bwd(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, dO, saved, dq, dk, dv, dg, dbeta,
