@@ -365,6 +365,7 @@ static gdn_status run_fwd(const Plan& P, const gdn_problem* p, const void* q, co
   sa.walk = 0;
   sa.tape = saved ? static_cast<uint8_t*>(saved) + P.s_tape : nullptr;
   sa.o = static_cast<__nv_bfloat16*>(o);
+  if (o && !make_tmap(&sa.to, o, P.T, P.HV)) return GDN_ERR_CUDA;
   launch_fwd_scan(sa, P.NSEG * P.HV, s);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

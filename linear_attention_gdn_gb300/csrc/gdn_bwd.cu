@@ -29,6 +29,8 @@
 
 namespace gdn {
 
+constexpr float kLog2e = 1.4426950408889634f;
+
 bool make_tmap(CUtensorMap* m, const void* base, int64_t T, int heads);
 gdn_status run_tables(const Plan& P, const gdn_problem* p, const int32_t* cu_dev, uint8_t* ws, void* saved,
                       cudaStream_t s);
@@ -201,9 +203,13 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
       fence_async_smem();
       __syncthreads();
     }
-    if (!a.walk) store_row128(a.dtape + ((size_t)ci * a.HV + hv) * STATE_BYTES, tid, dS);
     tc_fence_after();
     if (tid == 0) {
+      // the dS'^T tile (written and fenced last iteration) is this chunk's tape entry
+      if (!a.walk) {
+        bulk_store(a.dtape + ((size_t)ci * a.HV + hv) * STATE_BYTES, ds_tile, STATE_BYTES);
+        bulk_commit();
+      }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_ss(tb + BT_DW, desc_mn(a_k, 64, ks), desc_k(a_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
@@ -276,6 +282,7 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
       for (int ks = 0; ks < 4; ++ks)
         mma_ts(tb + BT_DS, tb + BT_ADO + ks * 8, desc_mn(a_q, 64, ks), idesc(128, 128, 0, 1), 1u);
       mma_commit(&mma_bar);
+      bulk_wait_read();   // the tape copy has read the dS'^T tile rewritten below
     }
     ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
     mph ^= 1;
@@ -297,6 +304,7 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
     __syncthreads();
     if (tid == 0 && it + 2 < nch) issue(it + 2);
   }
+  if (tid == 0) bulk_wait_all();
   if (ok && a.walk) {
     float* dst = a.dbend + ((size_t)split * a.HV + hv) * STATE_F32 + (size_t)tid * 128;
 #pragma unroll
@@ -380,15 +388,20 @@ constexpr int GK_SMEM = 214016;
 constexpr int GK_SMEM_ALLOC = GK_SMEM + 1024;
 constexpr int GK_DT = GK_TP, GK_R1 = GK_TPP;                                   // free after M1
 constexpr int GK_H1 = GK_S, GK_H2 = GK_S + 8192, GK_F1 = GK_S + 16384, GK_F2 = GK_S + 24576;  // after M3
-constexpr int GK_C = GK_DS;                   // FP32 [64][64] of dAqk.Aqk + dA.A, after M3
+constexpr int GK_C = GK_DS;                   // FP32 [64][65] of dAqk.Aqk + dA.A, after M3
+constexpr int GK_CLD = 65;                    // padded row pitch of C (no bank conflicts)
 constexpr int GK_PART = GK_AQ;                // FP32 partial column sums [6][4][64], after M1
 constexpr int GT_KK = 0, GT_QK = 64, GT_S0 = 128, GT_S1 = 192, GT_S2 = 256, GT_S3 = 320, GT_S4 = 384, GT_S5 = 448;
 constexpr uint32_t GK_VH_BYTES = 2 * 16384 + 2 * STATE_BYTES + TILE64_BYTES + CB_SCAL_BYTES;
 
-// sum over the 32 lanes of a warp of column `lane` of v[32] (fixed order)
-__device__ __forceinline__ float colsum32(float (&v)[32], int lane) {
+constexpr int GK_NWG = 4;                    // warpgroups; each takes GK_CW of the 64 token columns
+constexpr int GK_CW = 64 / GK_NWG;
+constexpr int GK_THREADS = 128 * GK_NWG;
+
+// sum over the 32 lanes of a warp of column `lane & 15` of v[16] (fixed order)
+__device__ __forceinline__ float colsum16(float (&v)[16], int lane) {
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
+  for (int o = 8; o >= 1; o >>= 1) {
     const bool up = (lane & o) != 0;
 #pragma unroll
     for (int kq = 0; kq < o; ++kq) {
@@ -397,7 +410,7 @@ __device__ __forceinline__ float colsum32(float (&v)[32], int lane) {
       v[kq] = mine + __shfl_xor_sync(0xffffffffu, other, o);
     }
   }
-  return v[0];
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
 __device__ __forceinline__ void store_chunk8(uint8_t* tile, int r, int c8, int R, const float* x) {
@@ -409,18 +422,18 @@ __device__ __forceinline__ void store_chunk8(uint8_t* tile, int r, int c8, int R
   *reinterpret_cast<uint4*>(tile + sw_chunk(r, c8, R)) = w;
 }
 
-__global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ GradArgs a) {
+__global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_constant__ GradArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t ld_bar, mma_bar;
   __shared__ uint32_t tslot;
   __shared__ float rq[CH], rk[CH], Gs[CH], bs[CH], gs[CH];
-  __shared__ float rowB[2][CH], sdot[8];
+  __shared__ float rowB[GK_NWG][CH], sdot[GK_THREADS / 32], cdiff[CH];
   const int c = blockIdx.x, j = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wg = tid >> 7, w4 = warp & 3;
   const int row = w4 * 32 + lane;          // TMEM lane / M = 128 row of this thread
-  const int cb0 = wg * 32;                 // first of this thread's 32 columns
+  const int cb0 = wg * GK_CW;              // first of this thread's GK_CW columns
   const int r64 = w4 * 16 + lane;          // M = 64 row (valid for lane < 16)
   if (*(volatile int*)a.err) return;
   const int tok0 = a.chunk_tok0[c], L = a.chunk_len[c];
@@ -477,11 +490,11 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Gr
   const float* scal = reinterpret_cast<const float*>(sm + GK_SCAL);
   float* Cm = reinterpret_cast<float*>(sm + GK_C);
   float* part = reinterpret_cast<float*>(sm + GK_PART);
-  auto tld32 = [&](int col, float* out) { tmem_ld32(taddr(tb, w4 * 32, col + cb0), out); };
+  auto tld = [&](int col, float* out) { tmem_ld16(taddr(tb, w4 * 32, col + cb0), out); };
 
-  float dq_acc[32], dk_acc[32];   // dq^T, dk^T [row][cb0 + e], summed over the group
+  float dq_acc[GK_CW], dk_acc[GK_CW];   // dq^T, dk^T [row][cb0 + e], summed over the group
 #pragma unroll
-  for (int e = 0; e < 32; ++e) dq_acc[e] = dk_acc[e] = 0.f;
+  for (int e = 0; e < GK_CW; ++e) dq_acc[e] = dk_acc[e] = 0.f;
 
   for (int h = 0; h < a.G && ok; ++h) {
     const int hv = j * a.G + h;
@@ -490,7 +503,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Gr
     if (!ok) break;
     if (L < CH) {  // zero rows past the document end in the token tiles
       const int ntile = h == 0 ? 4 : 2;
-      for (int idx = tid; idx < (CH - L) * 16 * ntile; idx += 256) {
+      for (int idx = tid; idx < (CH - L) * 16 * ntile; idx += GK_THREADS) {
         const int t = idx / (16 * ntile), rem = idx % (16 * ntile), tile = rem / 16, c8 = rem % 16;
         const int off = tile == 0 ? GK_V : tile == 1 ? GK_DO : tile == 2 ? GK_Q : GK_K;
         *reinterpret_cast<uint4*>(sm + off + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
@@ -500,9 +513,18 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Gr
       const uint8_t* tile = sm + (tid < 64 ? GK_K : GK_Q);
       const int r = tid & 63;
       float ss = 0.f;
-      for (int cc = 0; cc < D; ++cc) {
-        const float x = r < L ? ld_bf16(tile, r, cc, 64) : 0.f;
-        ss = fmaf(x, x, ss);
+      if (r < L) {   // same summation order as the prep kernel's norms
+#pragma unroll
+        for (int c8 = 0; c8 < 16; ++c8) {
+          const uint4 val = *reinterpret_cast<const uint4*>(tile + sw_chunk(r, c8, 64));
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&val);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(h2[e]);
+            ss = fmaf(f.x, f.x, ss);
+            ss = fmaf(f.y, f.y, ss);
+          }
+        }
       }
       const float rn = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
       if (tid < 64) rk[r] = rn;
@@ -526,12 +548,13 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Gr
         if (lane >= o) s += y;
       }
       const float ex = s - (g0 + g1);
-      Gs[r0] = ex + g0;
-      Gs[r1] = ex + g0 + g1;
+      // cumulative gate in log2 units (the prep kernel's convention)
+      Gs[r0] = (ex + g0) * kLog2e;
+      Gs[r1] = (ex + g0 + g1) * kLog2e;
       bs[r0] = b0;
       bs[r1] = b1;
-      gs[r0] = r0 < L ? expf(ex + g0) : 0.f;
-      gs[r1] = r1 < L ? expf(ex + g0 + g1) : 0.f;
+      gs[r0] = r0 < L ? exp2f(Gs[r0]) : 0.f;
+      gs[r1] = r1 < L ? exp2f(Gs[r1]) : 0.f;
     }
     __syncthreads();
     const float GL = Gs[L - 1], gL = scal[128];
@@ -548,7 +571,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Gr
       if (!(ok = mma_sync_wait())) break;
     }
     // ---- T' = T diag(beta gamma rk), T'' = T diag(beta), Aqk tile
-    for (int idx = tid; idx < 64 * 8; idx += 256) {
+    for (int idx = tid; idx < 64 * 8; idx += GK_THREADS) {
       const int r = idx >> 3, c8 = idx & 7;
       const uint4 raw = *reinterpret_cast<const uint4*>(sm + GK_T + sw_chunk(r, c8, 64));
       const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
@@ -566,18 +589,18 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Gr
       store_chunk8(sm + GK_TPP, r, c8, 64, tpp);
     }
     {
-      float qk[32];
-      tld32(GT_QK, qk);
+      float qk[GK_CW];
+      tld(GT_QK, qk);
       if (lane < 16) {
         const int r = r64;
         const float Gr = Gs[r], qr = rq[r];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
           float x[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int cc = cb0 + q4 * 8 + e;
-            x[e] = (cc <= r && r < L) ? qr * rk[cc] * expf(Gr - Gs[cc]) * qk[q4 * 8 + e] : 0.f;
+            x[e] = (cc <= r && r < L) ? qr * rk[cc] * exp2f(Gr - Gs[cc]) * qk[q4 * 8 + e] : 0.f;
           }
           store_chunk8(sm + GK_AQ, r, (cb0 >> 3) + q4, 64, x);
         }
@@ -599,13 +622,13 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Gr
     }
     if (!(ok = mma_sync_wait())) break;
     {  // H1: -W^T -> WD; dV_new^T = P dO^T Aqk + kd (dS'^T K^T) -> dV
-      float w[32], x[32], y[32];
-      tld32(GT_S0, w);
-      tld32(GT_S2, x);
-      tld32(GT_S3, y);
+      float w[GK_CW], x[GK_CW], y[GK_CW];
+      tld(GT_S0, w);
+      tld(GT_S2, x);
+      tld(GT_S3, y);
       const float* kd = scal + 64;
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
         float nw[8], dvn[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -633,38 +656,38 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Gr
     }
     if (!(ok = mma_sync_wait())) break;
     {  // H2
-      float x[32], cb[32], cg[32];
-      tld32(GT_S1, x);   // V_new^T row (dv)
+      float x[GK_CW], cb[GK_CW], cg[GK_CW];
+      tld(GT_S1, x);   // V_new^T row (dv)
       {
         float t8[8];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) t8[e] = x[q4 * 8 + e];
           store_chunk8(sm + GK_VN, row, (cb0 >> 3) + q4, 128, t8);
         }
       }
-      tld32(GT_S0, x);   // (S dV_new^T) row (dk) -> dW^T = -(.)
+      tld(GT_S0, x);   // (S dV_new^T) row (dk) -> dW^T = -(.)
       {
         float t8[8];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) t8[e] = -x[q4 * 8 + e];
           store_chunk8(sm + GK_WD, row, (cb0 >> 3) + q4, 128, t8);
         }
       }
-      tld32(GT_S2, x);   // X^T = dV_new^T T, row = dv index
+      tld(GT_S2, x);   // X^T = dV_new^T T, row = dv index
       __nv_bfloat16* dvp = a.dv + ((size_t)tok0 * a.HV + hv) * D + row;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < GK_CW; ++e) {
         const int cc = cb0 + e;
         if (cc < L) dvp[(size_t)cc * a.HV * D] = __float2bfloat16_rn(bs[cc] * x[e]);
         cb[e] = ld_bf16(sm + GK_V, cc, row, 64) * x[e];
       }
-      tld32(GT_S3, x);   // S dO^T, row = dk index
+      tld(GT_S3, x);   // S dO^T, row = dk index
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < GK_CW; ++e) {
         const int cc = cb0 + e;
         const float pg = a.scale * gs[cc];
         dq_acc[e] = fmaf(pg, x[e], dq_acc[e]);
@@ -672,15 +695,28 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Gr
       }
       // <S, dS'> over this thread's half of the row
       float sd = 0.f;
-      for (int cc = wg * 64; cc < wg * 64 + 64; ++cc)
-        sd = fmaf(ld_bf16(sm + GK_S, row, cc, 128), ld_bf16(sm + GK_DS, row, cc, 128), sd);
+#pragma unroll
+      for (int c8 = wg * (16 / GK_NWG); c8 < (wg + 1) * (16 / GK_NWG); ++c8) {   // 16-byte chunks in swizzle order
+        const uint4 sa = *reinterpret_cast<const uint4*>(sm + GK_S + sw_chunk(row, c8, 128));
+        const uint4 sb = *reinterpret_cast<const uint4*>(sm + GK_DS + sw_chunk(row, c8, 128));
+        const __nv_bfloat162* ha = reinterpret_cast<const __nv_bfloat162*>(&sa);
+        const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&sb);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 fa = __bfloat1622float2(ha[e]), fb = __bfloat1622float2(hb[e]);
+          sd = fmaf(fa.x, fb.x, sd);
+          sd = fmaf(fa.y, fb.y, sd);
+        }
+      }
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
       if (lane == 0) sdot[warp] = sd;
-      const float sb = colsum32(cb, lane);
-      const float sg = colsum32(cg, lane);
-      part[(0 * 4 + w4) * 64 + cb0 + lane] = sb;
-      part[(1 * 4 + w4) * 64 + cb0 + lane] = sg;
+      const float sb = colsum16(cb, lane);
+      const float sg = colsum16(cg, lane);
+      if (lane < GK_CW) {
+        part[(0 * 4 + w4) * 64 + cb0 + lane] = sb;
+        part[(1 * 4 + w4) * 64 + cb0 + lane] = sg;
+      }
     }
     handoff();
     // ---- M3: dKd^T, dO V_new^T, Y^T = dW^T T, dV_new V^T, dW K^T
@@ -699,45 +735,47 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Gr
     }
     if (!(ok = mma_sync_wait())) break;
     {  // H3
-      float x[32], cz[32], cy[32];
-      tld32(GT_S4, x);   // dKd^T, row = dk index
+      float x[GK_CW], cz[GK_CW], cy[GK_CW];
+      tld(GT_S4, x);   // dKd^T, row = dk index
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < GK_CW; ++e) {
         const int cc = cb0 + e;
-        const float dec = cc < L ? expf(GL - Gs[cc]) : 0.f;
+        const float dec = cc < L ? exp2f(GL - Gs[cc]) : 0.f;
         dk_acc[e] = fmaf(dec, x[e], dk_acc[e]);
         cz[e] = rk[cc] * ld_bf16(sm + GK_K, cc, row, 64) * x[e];
       }
-      tld32(GT_S0, x);   // Y^T = dW^T T
+      tld(GT_S0, x);   // Y^T = dW^T T
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < GK_CW; ++e) {
         const int cc = cb0 + e;
         dk_acc[e] = fmaf(bs[cc] * gs[cc], x[e], dk_acc[e]);
         cy[e] = rk[cc] * ld_bf16(sm + GK_K, cc, row, 64) * x[e];
       }
-      const float sz = colsum32(cz, lane);
-      const float sy = colsum32(cy, lane);
-      part[(2 * 4 + w4) * 64 + cb0 + lane] = sz;
-      part[(3 * 4 + w4) * 64 + cb0 + lane] = sy;
+      const float sz = colsum16(cz, lane);
+      const float sy = colsum16(cy, lane);
+      if (lane < GK_CW) {
+        part[(2 * 4 + w4) * 64 + cb0 + lane] = sz;
+        part[(3 * 4 + w4) * 64 + cb0 + lane] = sy;
+      }
       // M = 64 results: rows r64 (lanes < 16)
-      float daq[32], qk[32], t1[32], t2[32];
-      tld32(GT_S5, daq);
-      tld32(GT_QK, qk);
-      tld32(GT_S2, t1);
-      tld32(GT_S3, t2);
+      float daq[GK_CW], qk[GK_CW], t1[GK_CW], t2[GK_CW];
+      tld(GT_S5, daq);
+      tld(GT_QK, qk);
+      tld(GT_S2, t1);
+      tld(GT_S3, t2);
       if (lane < 16) {
         const int r = r64;
         const float Gr = Gs[r];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
           float h1[8], h2[8], dt[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int jj = q4 * 8 + e, cc = cb0 + jj;
             const bool live = cc <= r && r < L;
-            const float gam = live ? expf(Gr - Gs[cc]) : 0.f;
+            const float gam = live ? exp2f(Gr - Gs[cc]) : 0.f;
             const float dA = live ? a.scale * daq[jj] : 0.f;
-            Cm[r * 64 + cc] = dA * gam * rq[r] * rk[cc] * qk[jj];
+            Cm[r * GK_CLD + cc] = dA * gam * rq[r] * rk[cc] * qk[jj];
             h1[e] = rk[cc] * gam * dA;
             h2[e] = rq[r] * gam * dA;
             dt[e] = bs[cc] * fmaf(gs[cc] * rk[cc], t2[jj], t1[jj]);
@@ -761,17 +799,17 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Gr
     }
     if (!(ok = mma_sync_wait())) break;
     {  // H4
-      float x[32];
-      tld32(GT_S4, x);
+      float x[GK_CW];
+      tld(GT_S4, x);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) dq_acc[e] += x[e];
-      tld32(GT_S5, x);
+      for (int e = 0; e < GK_CW; ++e) dq_acc[e] += x[e];
+      tld(GT_S5, x);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) dk_acc[e] += x[e];
-      tld32(GT_S1, x);
+      for (int e = 0; e < GK_CW; ++e) dk_acc[e] += x[e];
+      tld(GT_S1, x);
       if (lane < 16) {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) store_chunk8(sm + GK_R1, r64, (cb0 >> 3) + q4, 64, x + q4 * 8);
+        for (int q4 = 0; q4 < GK_CW / 8; ++q4) store_chunk8(sm + GK_R1, r64, (cb0 >> 3) + q4, 64, x + q4 * 8);
       }
     }
     handoff();
@@ -784,25 +822,25 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Gr
     }
     if (!(ok = mma_sync_wait())) break;
     {  // H5: dA rows -> dbeta row terms, C, F1, F2
-      float x[32], kk[32];
-      tld32(GT_S0, x);
-      tld32(GT_KK, kk);
+      float x[GK_CW], kk[GK_CW];
+      tld(GT_S0, x);
+      tld(GT_KK, kk);
       if (lane < 16) {
         const int r = r64;
         const float Gr = Gs[r], br = bs[r];
         float rb = 0.f;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
           float f1[8], f2[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int jj = q4 * 8 + e, cc = cb0 + jj;
             const bool live = cc < r && r < L;
-            const float gam = live ? expf(Gr - Gs[cc]) : 0.f;
+            const float gam = live ? exp2f(Gr - Gs[cc]) : 0.f;
             const float dA = live ? -x[jj] : 0.f;
             const float base = dA * gam * rk[r] * rk[cc] * kk[jj];   // dA . (A / beta_r)
             rb += base;
-            Cm[r * 64 + cc] += br * base;
+            Cm[r * GK_CLD + cc] += br * base;
             const float E = dA * br * gam;
             f1[e] = rk[cc] * E;
             f2[e] = rk[r] * E;
@@ -826,16 +864,26 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Gr
     }
     if (!(ok = mma_sync_wait())) break;
     {
-      float x[32];
-      tld32(GT_S2, x);
+      float x[GK_CW];
+      tld(GT_S2, x);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) dk_acc[e] += x[e];
+      for (int e = 0; e < GK_CW; ++e) dk_acc[e] += x[e];
     }
     __syncthreads();
-    // ---- per-token totals: dbeta, dG -> dg (threads 0..63, token r)
-    if (tid < 64) {
+    // ---- per-token totals: dbeta, dG -> dg
+    if (tid < 4 * CH) {   // row sum - column sum of C, 4 threads per token
+      const int r = tid >> 2, qq = tid & 3;
+      float d = 0.f;
+#pragma unroll
+      for (int cc = qq * 16; cc < qq * 16 + 16; ++cc) d += Cm[r * GK_CLD + cc] - Cm[cc * GK_CLD + r];
+      d += __shfl_xor_sync(0xffffffffu, d, 1);
+      d += __shfl_xor_sync(0xffffffffu, d, 2);
+      if (qq == 0) cdiff[r] = d;
+    }
+    __syncthreads();
+    if (tid < CH) {
       const int r = tid;
-      float sb = 0.f, sg = 0.f, sz = 0.f, sy = 0.f, rowc = 0.f, colc = 0.f;
+      float sb = 0.f, sg = 0.f, sz = 0.f, sy = 0.f;
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         sb += part[(0 * 4 + w) * 64 + r];
@@ -843,39 +891,40 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Gr
         sz += part[(2 * 4 + w) * 64 + r];
         sy += part[(3 * 4 + w) * 64 + r];
       }
-      for (int cc = 0; cc < 64; ++cc) {
-        rowc += Cm[r * 64 + cc];
-        colc += Cm[cc * 64 + r];
-      }
-      const float dec = r < L ? expf(GL - Gs[r]) : 0.f;
+      const float dec = r < L ? exp2f(GL - Gs[r]) : 0.f;
       const float z = dec * sz;
-      float dG = sg - z + bs[r] * gs[r] * sy + rowc - colc;
-      const float db = sb + gs[r] * sy + rowB[0][r] + rowB[1][r];
+      float dG = sg - z + bs[r] * gs[r] * sy + cdiff[r];
+      float db = sb + gs[r] * sy;
+#pragma unroll
+      for (int w = 0; w < GK_NWG; ++w) db += rowB[w][r];
       // chunk-end terms: gamma_L <S, dS'> and sum_c z_c
       float zs = z;
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
-      __shared__ float zpart[2];
+      __shared__ float zpart[2], wtot[2];
       if (lane == 0) zpart[warp] = zs;
       named_bar(1, 64);
       if (r == L - 1) {
         float sd = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) sd += sdot[w];
+        for (int w = 0; w < GK_THREADS / 32; ++w) sd += sdot[w];
         dG += gL * sd + zpart[0] + zpart[1];
       }
       if (r >= L) dG = 0.f;
-      // dg_r = sum_{i >= r} dG_i (reverse inclusive scan over 64 tokens)
-      __shared__ float dgs[64];
-      dgs[r] = dG;
+      // dg_r = sum_{i >= r} dG_i: reverse scan within each warp, then add the later warp's total
+      float acc = dG;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_down_sync(0xffffffffu, acc, o);
+        if (lane + o < 32) acc += y;
+      }
+      if (lane == 0) wtot[warp] = acc;
       named_bar(1, 64);
-      float acc = 0.f;
-      for (int i = 63; i >= r; --i) acc += dgs[i];
+      if (warp == 0) acc += wtot[1];
       if (r < L) {
         a.dg[(size_t)(tok0 + r) * a.HV + hv] = acc;
         a.dbeta[(size_t)(tok0 + r) * a.HV + hv] = db;
       }
-      named_bar(1, 64);
     }
     __syncthreads();
     if (tid == 0 && h + 1 < a.G) issue_vhead(hv + 1, false);
@@ -883,21 +932,23 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Gr
 
   // ---- L2-norm backward of the group sums, then dq, dk
   if (ok) {
-    float pq[32], pk[32];
+    float pq[GK_CW], pk[GK_CW];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
+    for (int e = 0; e < GK_CW; ++e) {
       const int cc = cb0 + e;
       pq[e] = ld_bf16(sm + GK_Q, cc, row, 64) * dq_acc[e];
       pk[e] = ld_bf16(sm + GK_K, cc, row, 64) * dk_acc[e];
     }
-    const float sq = colsum32(pq, lane), sk = colsum32(pk, lane);
-    part[(4 * 4 + w4) * 64 + cb0 + lane] = sq;
-    part[(5 * 4 + w4) * 64 + cb0 + lane] = sk;
+    const float sq = colsum16(pq, lane), sk = colsum16(pk, lane);
+    if (lane < GK_CW) {
+      part[(4 * 4 + w4) * 64 + cb0 + lane] = sq;
+      part[(5 * 4 + w4) * 64 + cb0 + lane] = sk;
+    }
     __syncthreads();
     __nv_bfloat16* dqp = a.dq + ((size_t)tok0 * a.H + j) * D + row;
     __nv_bfloat16* dkp = a.dk + ((size_t)tok0 * a.H + j) * D + row;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
+    for (int e = 0; e < GK_CW; ++e) {
       const int cc = cb0 + e;
       if (cc >= L) continue;
       float outq = dq_acc[e], outk = dk_acc[e];
@@ -1032,7 +1083,7 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
   ga.scale = pr.scale;
   ga.err = reinterpret_cast<int*>(ws);
   prof_begin(K_GRAD, s);
-  grad_kernel<<<dim3(P.NC, P.H), 256, GK_SMEM_ALLOC, s>>>(ga);
+  grad_kernel<<<dim3(P.NC, P.H), GK_THREADS, GK_SMEM_ALLOC, s>>>(ga);
   prof_end(K_GRAD, s);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

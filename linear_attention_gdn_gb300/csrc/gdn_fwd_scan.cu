@@ -33,7 +33,8 @@ constexpr int SC_K = 0, SC_Q = 16384, SC_V = 32768, SC_TP = 49152, SC_TPP = 5734
 constexpr int SC_STAGE = 74752;
 constexpr int SC_S = 2 * SC_STAGE;          // BF16 S^T tile, SwTile(128 x 128)
 constexpr int SC_W = SC_S + STATE_BYTES;    // -W^T tile, SwTile(128 x 64)
-constexpr int SC_SMEM = SC_W + 16384;
+constexpr int SC_O = SC_W + 16384;         // BF16 output staging tile [64 tok][128], SwTile(64 x 128)
+constexpr int SC_SMEM = SC_O + 16384;
 constexpr int SC_SMEM_ALLOC = SC_SMEM + 1024;
 
 // TMEM columns
@@ -236,6 +237,7 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
           mma_ts(tb + TM_O2, tb + TM_AVN + ks * 8, desc_k(a_aqk, 64, ks), idesc(128, 64, 0, 0), ks > 0);
       }
       mma_commit(&mma_bar);
+      bulk_wait_read();   // the last chunk's tape / output stores have read the tiles rewritten below
     }
     ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
     mph ^= 1;
@@ -250,13 +252,10 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 32; ++e) S[h * 32 + e] = fmaf(gL, S[h * 32 + e], ds[e]);
       }
-      store_state_row(s_tile, tid, S);
-      if (mode == 0 && a.tape && n + 1 < nch)
-        store_state_row(a.tape + ((size_t)(c0 + n + 1) * a.HV + hv) * STATE_BYTES, tid, S);
+      store_state_row(s_tile, tid, S);   // also the saved state entering the next chunk (bulk copy below)
     }
-    if (with_o) {  // o[t0 + r][hv][tid] = sc_r (S^T Q^T)[tid][r] + scale (V_new^T Aqk^T)[tid][r]
-      const int t0 = a.chunk_tok0[c0 + n];
-      __nv_bfloat16* orow = a.o + (size_t)t0 * a.HV * D + (size_t)hv * D + tid;
+    uint8_t* o_stage = sm + SC_O;
+    if (with_o) {  // O^T row tid -> staging tile [token][feature]: o = sc_r (S^T Q^T) + scale (V_new^T Aqk^T)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float x1[32], x2[32];
@@ -265,15 +264,34 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int r = h * 32 + e;
-          if (r < L) orow[(size_t)r * a.HV * D] = __float2bfloat16_rn(fmaf(scal[r], x1[e], a.scale * x2[e]));
+          *reinterpret_cast<__nv_bfloat16*>(o_stage + sw_off(r, tid, 64)) =
+              __float2bfloat16_rn(fmaf(scal[r], x1[e], a.scale * x2[e]));
         }
       }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && n + 2 < nch) issue(n + 2);
+    const int t0 = a.chunk_tok0[c0 + n];
+    if (with_o && L < CH) {  // ragged last chunk: only its own rows (the next rows are another document's)
+      for (int idx = tid; idx < L * 16; idx += 128) {
+        const int r = idx >> 4, c8 = idx & 15;
+        *reinterpret_cast<uint4*>(a.o + ((size_t)(t0 + r) * a.HV + hv) * D + c8 * 8) =
+            *reinterpret_cast<const uint4*>(o_stage + sw_chunk(r, c8, 64));
+      }
+    }
+    if (tid == 0) {  // asynchronous stores of the saved state and the output tile
+      if (mode == 0 && a.tape && n + 1 < nch)
+        bulk_store(a.tape + ((size_t)(c0 + n + 1) * a.HV + hv) * STATE_BYTES, s_tile, STATE_BYTES);
+      if (with_o && L == CH) {
+        tma_store_3d(&a.to, o_stage, 0, hv, t0);
+        tma_store_3d(&a.to, o_stage + 8192, 64, hv, t0);
+      }
+      bulk_commit();
+      if (n + 2 < nch) issue(n + 2);
+    }
   }
+  if (tid == 0) bulk_wait_all();
   if (ok && mode != 0) {
     float* dst = (mode == 1 ? a.bend : a.mend) + ((size_t)split * a.HV + hv) * STATE_F32 + (size_t)tid * 128;
 #pragma unroll

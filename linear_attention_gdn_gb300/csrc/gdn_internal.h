@@ -79,7 +79,7 @@ struct PrepArgs {
 };
 
 struct ScanArgs {
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const uint8_t* cb;
   const int* chunk_tok0;
   const int* chunk_len;

@@ -24,8 +24,10 @@
 
 namespace gdn {
 
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr int PREP_GR = 3;                            // value heads per round
-constexpr int PREP_BLK = 32 * 33;                     // padded 32 x 32 FP32 block
+constexpr int PREP_BLK = 32 * 33 + 1;                 // padded 32 x 32 FP32 block (odd stride: the
+                                                      // blocks' same elements fall in different banks)
 constexpr int PREP_TILES = 0;                         // Lm, Dm, Xt tiles (3 x 8 KB)
 constexpr int PREP_AD = 3 * TILE64_BYTES;             // diagonal blocks of A
 constexpr int PREP_TD = PREP_AD + PREP_GR * 2 * PREP_BLK * 4;   // their inverses
@@ -136,8 +138,9 @@ __global__ void __launch_bounds__(128, 2) prep_kernel(PrepArgs a) {
         if (lane >= o) s += y;
       }
       const float ex = s - (g0 + g1);
-      Gs[warp][r0] = ex + g0;
-      Gs[warp][r1] = ex + g0 + g1;
+      // cumulative gate in log2 units: every exponential below is exp2f of a difference
+      Gs[warp][r0] = (ex + g0) * kLog2e;
+      Gs[warp][r1] = (ex + g0 + g1) * kLog2e;
       bs[warp][r0] = b0;
       bs[warp][r1] = b1;
     }
@@ -157,7 +160,7 @@ __global__ void __launch_bounds__(128, 2) prep_kernel(PrepArgs a) {
         float* A2 = A21s + hh * PREP_BLK;
 #pragma unroll
         for (int jj = 0; jj < 64; ++jj) {
-          const float val = (jj < r && r < L) ? br * rk[jj] * expf(Gr - Gh[jj]) * kq[jj] : 0.f;
+          const float val = (jj < r && r < L) ? br * rk[jj] * exp2f(Gr - Gh[jj]) * kq[jj] : 0.f;
           if (r < 32) {
             if (jj < 32) A0[r * 33 + jj] = val;
           } else if (jj >= 32) {
@@ -168,10 +171,10 @@ __global__ void __launch_bounds__(128, 2) prep_kernel(PrepArgs a) {
         }
         float* sc = reinterpret_cast<float*>(cbp + CB_SCAL);
         const float GL = Gh[L - 1];
-        sc[r] = r < L ? a.scale * expf(Gr) * rq[r] : 0.f;
-        sc[64 + r] = r < L ? expf(GL - Gr) * rk[r] : 0.f;
+        sc[r] = r < L ? a.scale * exp2f(Gr) * rq[r] : 0.f;
+        sc[64 + r] = r < L ? exp2f(GL - Gr) * rk[r] : 0.f;
         if (r == 0) {
-          sc[128] = expf(GL);
+          sc[128] = exp2f(GL);
           reinterpret_cast<int*>(sc)[129] = L;
         }
       } else {
@@ -183,8 +186,8 @@ __global__ void __launch_bounds__(128, 2) prep_kernel(PrepArgs a) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int j0 = c8 * 8 + 2 * e, j1 = j0 + 1;
-            const float v0 = (j0 <= r && r < L) ? qr * rk[j0] * expf(Gr - Gh[j0]) * kq[j0] : 0.f;
-            const float v1 = (j1 <= r && r < L) ? qr * rk[j1] * expf(Gr - Gh[j1]) * kq[j1] : 0.f;
+            const float v0 = (j0 <= r && r < L) ? qr * rk[j0] * exp2f(Gr - Gh[j0]) * kq[j0] : 0.f;
+            const float v1 = (j1 <= r && r < L) ? qr * rk[j1] * exp2f(Gr - Gh[j1]) * kq[j1] : 0.f;
             w[e] = pack_bf16(v0, v1);
           }
           *reinterpret_cast<uint4*>(cbp + CB_AQK + sw_chunk(r, c8, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(128, 2) prep_kernel(PrepArgs a) {
                 const int cc = c8 * 8 + 2 * e + u;
                 tv[u] = dval(r, cc) - ((r >= 32 && cc < 32) ? y[cc] : 0.f);
                 tpp[u] = tv[u] * bh[cc];
-                tp[u] = tpp[u] * expf(Gh[cc]) * rk[cc];
+                tp[u] = tpp[u] * exp2f(Gh[cc]) * rk[cc];
               }
               wt[e] = pack_bf16(tv[0], tv[1]);
               wpp[e] = pack_bf16(tpp[0], tpp[1]);
