@@ -427,7 +427,8 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t ld_bar, mma_bar;
   __shared__ uint32_t tslot;
-  __shared__ float rq[CH], rk[CH], Gs[CH], bs[CH], gs[CH];
+  __shared__ float rq[CH], rk[CH], Gs[CH], bs[CH], gs[CH], decs[CH], eGr[CH], eGi[CH];
+  __shared__ int gsafe;
   __shared__ float rowB[GK_NWG][CH], sdot[GK_THREADS / 32], cdiff[CH];
   const int c = blockIdx.x, j = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -555,9 +556,25 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       bs[r1] = b1;
       gs[r0] = r0 < L ? exp2f(Gs[r0]) : 0.f;
       gs[r1] = r1 < L ? exp2f(Gs[r1]) : 0.f;
+      // per-token gate factors: e^{G_r - G_j} = eGr[r] eGi[j] when the chunk's range is FP32-safe
+      const float G0v = Gs[r0], G1v = Gs[r1];
+      const float Gfirst = __shfl_sync(0xffffffffu, G0v, 0);
+      const float Glast = __shfl_sync(0xffffffffu, G1v, 31);
+      const bool sf = (Gfirst - Glast) < 100.f;
+      eGr[r0] = exp2f(G0v - Gfirst);
+      eGr[r1] = exp2f(G1v - Gfirst);
+      eGi[r0] = sf ? exp2f(Gfirst - G0v) : 0.f;
+      eGi[r1] = sf ? exp2f(Gfirst - G1v) : 0.f;
+      decs[r0] = r0 < L ? exp2f(Glast - G0v) : 0.f;
+      decs[r1] = r1 < L ? exp2f(Glast - G1v) : 0.f;
+      if (lane == 0) gsafe = sf;
     }
     __syncthreads();
-    const float GL = Gs[L - 1], gL = scal[128];
+    const bool sfac = gsafe;
+    auto gamma_rc = [&](int r, int cc) -> float {   // e^{G_r - G_c}, c <= r
+      return sfac ? eGr[r] * eGi[cc] : exp2f(Gs[r] - Gs[cc]);
+    };
+    const float gL = scal[128];
     if (h == 0) {  // KK^T and QK^T (M = 64), kept in TMEM for the whole group
       handoff();
       if (tid == 0) {
@@ -593,14 +610,14 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       tld(GT_QK, qk);
       if (lane < 16) {
         const int r = r64;
-        const float Gr = Gs[r], qr = rq[r];
+        const float qr = rq[r];
 #pragma unroll
         for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
           float x[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int cc = cb0 + q4 * 8 + e;
-            x[e] = (cc <= r && r < L) ? qr * rk[cc] * exp2f(Gr - Gs[cc]) * qk[q4 * 8 + e] : 0.f;
+            x[e] = (cc <= r && r < L) ? qr * rk[cc] * gamma_rc(r, cc) * qk[q4 * 8 + e] : 0.f;
           }
           store_chunk8(sm + GK_AQ, r, (cb0 >> 3) + q4, 64, x);
         }
@@ -740,7 +757,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
 #pragma unroll
       for (int e = 0; e < GK_CW; ++e) {
         const int cc = cb0 + e;
-        const float dec = cc < L ? exp2f(GL - Gs[cc]) : 0.f;
+        const float dec = decs[cc];
         dk_acc[e] = fmaf(dec, x[e], dk_acc[e]);
         cz[e] = rk[cc] * ld_bf16(sm + GK_K, cc, row, 64) * x[e];
       }
@@ -765,7 +782,6 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       tld(GT_S3, t2);
       if (lane < 16) {
         const int r = r64;
-        const float Gr = Gs[r];
 #pragma unroll
         for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
           float h1[8], h2[8], dt[8];
@@ -773,7 +789,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
           for (int e = 0; e < 8; ++e) {
             const int jj = q4 * 8 + e, cc = cb0 + jj;
             const bool live = cc <= r && r < L;
-            const float gam = live ? exp2f(Gr - Gs[cc]) : 0.f;
+            const float gam = live ? gamma_rc(r, cc) : 0.f;
             const float dA = live ? a.scale * daq[jj] : 0.f;
             Cm[r * GK_CLD + cc] = dA * gam * rq[r] * rk[cc] * qk[jj];
             h1[e] = rk[cc] * gam * dA;
@@ -827,7 +843,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       tld(GT_KK, kk);
       if (lane < 16) {
         const int r = r64;
-        const float Gr = Gs[r], br = bs[r];
+        const float br = bs[r];
         float rb = 0.f;
 #pragma unroll
         for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
@@ -836,7 +852,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
           for (int e = 0; e < 8; ++e) {
             const int jj = q4 * 8 + e, cc = cb0 + jj;
             const bool live = cc < r && r < L;
-            const float gam = live ? exp2f(Gr - Gs[cc]) : 0.f;
+            const float gam = live ? gamma_rc(r, cc) : 0.f;
             const float dA = live ? -x[jj] : 0.f;
             const float base = dA * gam * rk[r] * rk[cc] * kk[jj];   // dA . (A / beta_r)
             rb += base;
@@ -891,7 +907,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         sz += part[(2 * 4 + w) * 64 + r];
         sy += part[(3 * 4 + w) * 64 + r];
       }
-      const float dec = r < L ? exp2f(GL - Gs[r]) : 0.f;
+      const float dec = decs[r];
       const float z = dec * sz;
       float dG = sg - z + bs[r] * gs[r] * sy + cdiff[r];
       float db = sb + gs[r] * sy;
