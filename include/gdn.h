@@ -88,9 +88,12 @@ typedef enum {
  *                    value head (32 KiB per chunk and value head; the pages'
  *                    "h tape" of states every 64 tokens), and, where a
  *                    document is split into P > 1 segments, the FP32 segment
- *                    transfer plane M_seg (P x HV x 64 KiB per document) that
- *                    the backward's merges read ("#8542" page: the full saved
- *                    set keeps M_seg at P > 1).
+ *                    transfer plane M_seg ((P-1) x HV x 64 KiB per document)
+ *                    that the backward's merges read ("#8542" page: the full
+ *                    saved set keeps M_seg at P > 1), and the per-chunk UT
+ *                    blocks (T = (I + A)^-1 with its scaled forms and the gated
+ *                    Aqk rows, 33 KiB per chunk and value head) so that the
+ *                    backward does not recompute them.
  *   workspace_bytes  scratch for one gdn_fwd / gdn_bwd / gdn_ckpt_fwd_bwd call.
  * Returns GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED on a bad problem.
  */

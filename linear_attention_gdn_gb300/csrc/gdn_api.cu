@@ -153,7 +153,8 @@ static gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
   // saved set
   P->s_tape = SAVED_HEADER;
   P->s_mseg = P->s_tape + (size_t)NC * P->HV * STATE_BYTES;
-  P->saved_bytes = P->s_mseg + st_f32;
+  P->s_cb = align_up(P->s_mseg + st_f32, 1024);
+  P->saved_bytes = P->s_cb + (size_t)NC * P->HV * CB_BYTES;
   return GDN_OK;
 }
 
@@ -298,7 +299,7 @@ gdn_status run_tables(const Plan& P, const gdn_problem* p, const int32_t* cu_dev
 }
 
 gdn_status run_prep(const Plan& P, const gdn_problem* p, const void* q, const void* k, const float* g,
-                    const float* beta, uint8_t* ws, int write_T, cudaStream_t s) {
+                    const float* beta, uint8_t* ws, uint8_t* cb, int write_T, cudaStream_t s) {
   Tables t = tables_at(P, ws);
   PrepArgs pa;
   pa.q = static_cast<const __nv_bfloat16*>(q);
@@ -307,7 +308,7 @@ gdn_status run_prep(const Plan& P, const gdn_problem* p, const void* q, const vo
   pa.beta = beta;
   pa.chunk_tok0 = t.chunk_tok0;
   pa.chunk_len = t.chunk_len;
-  pa.cb = ws + P.o_cb;
+  pa.cb = cb;
   pa.H = P.H;
   pa.HV = P.HV;
   pa.G = P.G;
@@ -325,14 +326,16 @@ static gdn_status run_fwd(const Plan& P, const gdn_problem* p, const void* q, co
   gdn_status st = run_tables(P, p, cu_dev, ws, saved, s);
   if (st != GDN_OK) return st;
   if (P.NC == 0) return GDN_OK;
-  st = run_prep(P, p, q, k, g, beta, ws, 0, s);
+  // with a saved set, the per-chunk UT blocks (with T) go into it for the backward
+  uint8_t* cb = saved ? static_cast<uint8_t*>(saved) + P.s_cb : ws + P.o_cb;
+  st = run_prep(P, p, q, k, g, beta, ws, cb, saved ? 1 : 0, s);
   if (st != GDN_OK) return st;
   Tables t = tables_at(P, ws);
   ScanArgs sa;
   memset(&sa, 0, sizeof(sa));
   if (!make_tmap(&sa.tq, q, P.T, P.H) || !make_tmap(&sa.tk, k, P.T, P.H) || !make_tmap(&sa.tv, v, P.T, P.HV))
     return GDN_ERR_CUDA;
-  sa.cb = ws + P.o_cb;
+  sa.cb = cb;
   sa.chunk_tok0 = t.chunk_tok0;
   sa.chunk_len = t.chunk_len;
   sa.seg_c0 = t.seg_c0;

@@ -35,7 +35,7 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t T, int heads);
 gdn_status run_tables(const Plan& P, const gdn_problem* p, const int32_t* cu_dev, uint8_t* ws, void* saved,
                       cudaStream_t s);
 gdn_status run_prep(const Plan& P, const gdn_problem* p, const void* q, const void* k, const float* g,
-                    const float* beta, uint8_t* ws, int write_T, cudaStream_t s);
+                    const float* beta, uint8_t* ws, uint8_t* cb, int write_T, cudaStream_t s);
 
 struct BScanArgs {
   CUtensorMap tq, tk, tdo;
@@ -392,7 +392,6 @@ constexpr int GK_C = GK_DS;                   // FP32 [64][65] of dAqk.Aqk + dA.
 constexpr int GK_CLD = 65;                    // padded row pitch of C (no bank conflicts)
 constexpr int GK_PART = GK_AQ;                // FP32 partial column sums [6][4][64], after M1
 constexpr int GT_KK = 0, GT_QK = 64, GT_S0 = 128, GT_S1 = 192, GT_S2 = 256, GT_S3 = 320, GT_S4 = 384, GT_S5 = 448;
-constexpr uint32_t GK_VH_BYTES = 2 * 16384 + 2 * STATE_BYTES + TILE64_BYTES + CB_SCAL_BYTES;
 
 constexpr int GK_NWG = 4;                    // warpgroups; each takes GK_CW of the 64 token columns
 constexpr int GK_CW = 64 / GK_NWG;
@@ -425,7 +424,8 @@ __device__ __forceinline__ void store_chunk8(uint8_t* tile, int r, int c8, int R
 __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_constant__ GradArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t ld_bar, mma_bar;
+  __shared__ uint64_t bar_qk, bar_vd, bar_t, bar_s, bar_ds, mma_bar;
+  __shared__ float gall[8][CH], ball[8][CH];   // the group's gates, prefetched (first 8 value heads)
   __shared__ uint32_t tslot;
   __shared__ float rq[CH], rk[CH], Gs[CH], bs[CH], gs[CH], decs[CH], eGr[CH], eGi[CH];
   __shared__ int gsafe;
@@ -441,33 +441,58 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
 
   if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {
-    mbar_init(&ld_bar, 1);
+    mbar_init(&bar_qk, 1);
+    mbar_init(&bar_vd, 1);
+    mbar_init(&bar_t, 1);
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_ds, 1);
     mbar_init(&mma_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   __syncthreads();
   const uint32_t tb = tslot;
-  auto issue_vhead = [&](int hv, bool with_qk) {
-    const uint8_t* cbp = a.cb + ((size_t)c * a.HV + hv) * CB_BYTES;
-    mbar_expect_tx(&ld_bar, GK_VH_BYTES + (with_qk ? 32768u : 0u));
-    if (with_qk) {
-      tma_load_3d(sm + GK_Q, &a.tq, 0, j, tok0, &ld_bar);
-      tma_load_3d(sm + GK_Q + 8192, &a.tq, 64, j, tok0, &ld_bar);
-      tma_load_3d(sm + GK_K, &a.tk, 0, j, tok0, &ld_bar);
-      tma_load_3d(sm + GK_K + 8192, &a.tk, 64, j, tok0, &ld_bar);
-    }
-    tma_load_3d(sm + GK_V, &a.tv, 0, hv, tok0, &ld_bar);
-    tma_load_3d(sm + GK_V + 8192, &a.tv, 64, hv, tok0, &ld_bar);
-    tma_load_3d(sm + GK_DO, &a.tdo, 0, hv, tok0, &ld_bar);
-    tma_load_3d(sm + GK_DO + 8192, &a.tdo, 64, hv, tok0, &ld_bar);
-    bulk_load(sm + GK_S, a.tape + ((size_t)c * a.HV + hv) * STATE_BYTES, STATE_BYTES, &ld_bar);
-    bulk_load(sm + GK_DS, a.dtape + ((size_t)c * a.HV + hv) * STATE_BYTES, STATE_BYTES, &ld_bar);
-    bulk_load(sm + GK_T, cbp + CB_T, TILE64_BYTES, &ld_bar);
-    bulk_load(sm + GK_SCAL, cbp + CB_SCAL, CB_SCAL_BYTES, &ld_bar);
+  // Each value head's inputs land on four barriers, requested as soon as the
+  // buffer they overwrite is dead in the previous value head.
+  auto issue_vd = [&](int hv) {   // V, dO tiles
+    mbar_expect_tx(&bar_vd, 32768u);
+    tma_load_3d(sm + GK_V, &a.tv, 0, hv, tok0, &bar_vd);
+    tma_load_3d(sm + GK_V + 8192, &a.tv, 64, hv, tok0, &bar_vd);
+    tma_load_3d(sm + GK_DO, &a.tdo, 0, hv, tok0, &bar_vd);
+    tma_load_3d(sm + GK_DO + 8192, &a.tdo, 64, hv, tok0, &bar_vd);
   };
-  if (tid == 0) issue_vhead(j * a.G, true);
+  auto issue_t = [&](int hv) {
+    mbar_expect_tx(&bar_t, (uint32_t)TILE64_BYTES);
+    bulk_load(sm + GK_T, a.cb + ((size_t)c * a.HV + hv) * CB_BYTES + CB_T, TILE64_BYTES, &bar_t);
+  };
+  auto issue_s = [&](int hv) {
+    mbar_expect_tx(&bar_s, (uint32_t)STATE_BYTES);
+    bulk_load(sm + GK_S, a.tape + ((size_t)c * a.HV + hv) * STATE_BYTES, STATE_BYTES, &bar_s);
+  };
+  auto issue_ds = [&](int hv) {   // dS' tile and the chunk scalars
+    mbar_expect_tx(&bar_ds, (uint32_t)(STATE_BYTES + CB_SCAL_BYTES));
+    bulk_load(sm + GK_DS, a.dtape + ((size_t)c * a.HV + hv) * STATE_BYTES, STATE_BYTES, &bar_ds);
+    bulk_load(sm + GK_SCAL, a.cb + ((size_t)c * a.HV + hv) * CB_BYTES + CB_SCAL, CB_SCAL_BYTES, &bar_ds);
+  };
+  if (tid == 0) {
+    mbar_expect_tx(&bar_qk, 32768u);
+    tma_load_3d(sm + GK_Q, &a.tq, 0, j, tok0, &bar_qk);
+    tma_load_3d(sm + GK_Q + 8192, &a.tq, 64, j, tok0, &bar_qk);
+    tma_load_3d(sm + GK_K, &a.tk, 0, j, tok0, &bar_qk);
+    tma_load_3d(sm + GK_K + 8192, &a.tk, 64, j, tok0, &bar_qk);
+    issue_vd(j * a.G);
+    issue_t(j * a.G);
+    issue_s(j * a.G);
+    issue_ds(j * a.G);
+  }
+  for (int i = tid; i < min(a.G, 8) * CH; i += GK_THREADS) {   // gates of the group
+    const int hh = i / CH, r = i % CH;
+    const size_t gi = (size_t)(tok0 + r) * a.HV + j * a.G + hh;
+    gall[hh][r] = r < L ? a.g[gi] : 0.f;
+    ball[hh][r] = r < L ? a.beta[gi] : 0.f;
+  }
+  __syncthreads();
 
-  uint32_t lph = 0, mph = 0;
+  uint32_t mph = 0;
   bool ok = true;
   auto mma_sync_wait = [&]() -> bool {
     bool r = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
@@ -492,6 +517,15 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
   float* Cm = reinterpret_cast<float*>(sm + GK_C);
   float* part = reinterpret_cast<float*>(sm + GK_PART);
   auto tld = [&](int col, float* out) { tmem_ld16(taddr(tb, w4 * 32, col + cb0), out); };
+  // issue several TMEM loads, then wait once
+  auto tld2 = [&](int c0_, float* o0, int c1_, float* o1) {
+    uint32_t r0[16], r1[16];
+    tmem_ld16_async(taddr(tb, w4 * 32, c0_ + cb0), r0);
+    tmem_ld16_async(taddr(tb, w4 * 32, c1_ + cb0), r1);
+    tmem_wait_ld();
+    as_float16(r0, o0);
+    as_float16(r1, o1);
+  };
 
   float dq_acc[GK_CW], dk_acc[GK_CW];   // dq^T, dk^T [row][cb0 + e], summed over the group
 #pragma unroll
@@ -499,16 +533,10 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
 
   for (int h = 0; h < a.G && ok; ++h) {
     const int hv = j * a.G + h;
-    ok = __syncthreads_and(mbar_wait(&ld_bar, lph, a.err));
-    lph ^= 1;
-    if (!ok) break;
-    if (L < CH) {  // zero rows past the document end in the token tiles
-      const int ntile = h == 0 ? 4 : 2;
-      for (int idx = tid; idx < (CH - L) * 16 * ntile; idx += GK_THREADS) {
-        const int t = idx / (16 * ntile), rem = idx % (16 * ntile), tile = rem / 16, c8 = rem % 16;
-        const int off = tile == 0 ? GK_V : tile == 1 ? GK_DO : tile == 2 ? GK_Q : GK_K;
-        *reinterpret_cast<uint4*>(sm + off + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
-      }
+    const uint32_t vph = h & 1;   // phase of the per-value-head barriers
+    if (h == 0) {
+      ok = __syncthreads_and(mbar_wait(&bar_qk, 0, a.err));
+      if (!ok) break;
     }
     if (h == 0 && tid < 128) {   // L2 norms of the q/k rows
       const uint8_t* tile = sm + (tid < 64 ? GK_K : GK_Q);
@@ -534,13 +562,20 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     if (warp == 0) {  // gates of this value head
       const int r0 = 2 * lane, r1 = r0 + 1;
       float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-      if (r0 < L) {
-        g0 = a.g[(size_t)(tok0 + r0) * a.HV + hv];
-        b0 = a.beta[(size_t)(tok0 + r0) * a.HV + hv];
-      }
-      if (r1 < L) {
-        g1 = a.g[(size_t)(tok0 + r1) * a.HV + hv];
-        b1 = a.beta[(size_t)(tok0 + r1) * a.HV + hv];
+      if (h < 8) {
+        g0 = gall[h][r0];
+        g1 = gall[h][r1];
+        b0 = ball[h][r0];
+        b1 = ball[h][r1];
+      } else {
+        if (r0 < L) {
+          g0 = a.g[(size_t)(tok0 + r0) * a.HV + hv];
+          b0 = a.beta[(size_t)(tok0 + r0) * a.HV + hv];
+        }
+        if (r1 < L) {
+          g1 = a.g[(size_t)(tok0 + r1) * a.HV + hv];
+          b1 = a.beta[(size_t)(tok0 + r1) * a.HV + hv];
+        }
       }
       float s = g0 + g1;
 #pragma unroll
@@ -574,7 +609,6 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     auto gamma_rc = [&](int r, int cc) -> float {   // e^{G_r - G_c}, c <= r
       return sfac ? eGr[r] * eGi[cc] : exp2f(Gs[r] - Gs[cc]);
     };
-    const float gL = scal[128];
     if (h == 0) {  // KK^T and QK^T (M = 64), kept in TMEM for the whole group
       handoff();
       if (tid == 0) {
@@ -587,6 +621,8 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       }
       if (!(ok = mma_sync_wait())) break;
     }
+    ok = __syncthreads_and(mbar_wait(&bar_t, vph, a.err));
+    if (!ok) break;
     // ---- T' = T diag(beta gamma rk), T'' = T diag(beta), Aqk tile
     for (int idx = tid; idx < 64 * 8; idx += GK_THREADS) {
       const int r = idx >> 3, c8 = idx & 7;
@@ -623,6 +659,17 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         }
       }
     }
+    ok = __syncthreads_and(mbar_wait(&bar_vd, vph, a.err) & mbar_wait(&bar_ds, vph, a.err));
+    if (!ok) break;
+    if (L < CH) {  // zero rows past the document end in the V, dO tiles (Q, K at the first head)
+      const int ntile = h == 0 ? 4 : 2;
+      for (int idx = tid; idx < (CH - L) * 16 * ntile; idx += GK_THREADS) {
+        const int t = idx / (16 * ntile), rem = idx % (16 * ntile), tile = rem / 16, c8 = rem % 16;
+        const int off = tile == 0 ? GK_V : tile == 1 ? GK_DO : tile == 2 ? GK_Q : GK_K;
+        *reinterpret_cast<uint4*>(sm + off + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    const float gL = scal[128];
     handoff();
     // ---- M1: W^T, U^T, dO^T Aqk, dS'^T K^T
     if (tid == 0) {
@@ -640,9 +687,16 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     if (!(ok = mma_sync_wait())) break;
     {  // H1: -W^T -> WD; dV_new^T = P dO^T Aqk + kd (dS'^T K^T) -> dV
       float w[GK_CW], x[GK_CW], y[GK_CW];
-      tld(GT_S0, w);
-      tld(GT_S2, x);
-      tld(GT_S3, y);
+      {
+        uint32_t r0[16], r1[16], r2[16];
+        tmem_ld16_async(taddr(tb, w4 * 32, GT_S0 + cb0), r0);
+        tmem_ld16_async(taddr(tb, w4 * 32, GT_S2 + cb0), r1);
+        tmem_ld16_async(taddr(tb, w4 * 32, GT_S3 + cb0), r2);
+        tmem_wait_ld();
+        as_float16(r0, w);
+        as_float16(r1, x);
+        as_float16(r2, y);
+      }
       const float* kd = scal + 64;
 #pragma unroll
       for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
@@ -657,6 +711,8 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         store_chunk8(sm + GK_DV, row, (cb0 >> 3) + q4, 128, dvn);
       }
     }
+    ok = __syncthreads_and(mbar_wait(&bar_s, vph, a.err));
+    if (!ok) break;
     handoff();
     // ---- M2: V_new^T, S dV_new^T, dV_new^T T, S dO^T
     if (tid == 0) {
@@ -673,8 +729,8 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     }
     if (!(ok = mma_sync_wait())) break;
     {  // H2
-      float x[GK_CW], cb[GK_CW], cg[GK_CW];
-      tld(GT_S1, x);   // V_new^T row (dv)
+      float x[GK_CW], x2[GK_CW], cb[GK_CW], cg[GK_CW];
+      tld2(GT_S1, x, GT_S0, x2);   // V_new^T row (dv); S dV_new^T row (dk)
       {
         float t8[8];
 #pragma unroll
@@ -684,17 +740,16 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
           store_chunk8(sm + GK_VN, row, (cb0 >> 3) + q4, 128, t8);
         }
       }
-      tld(GT_S0, x);   // (S dV_new^T) row (dk) -> dW^T = -(.)
-      {
+      {  // dW^T = -(S dV_new^T)
         float t8[8];
 #pragma unroll
         for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) t8[e] = -x[q4 * 8 + e];
+          for (int e = 0; e < 8; ++e) t8[e] = -x2[q4 * 8 + e];
           store_chunk8(sm + GK_WD, row, (cb0 >> 3) + q4, 128, t8);
         }
       }
-      tld(GT_S2, x);   // X^T = dV_new^T T, row = dv index
+      tld2(GT_S2, x, GT_S3, x2);   // X^T = dV_new^T T (row = dv index); S dO^T (row = dk index)
       __nv_bfloat16* dvp = a.dv + ((size_t)tok0 * a.HV + hv) * D + row;
 #pragma unroll
       for (int e = 0; e < GK_CW; ++e) {
@@ -702,13 +757,12 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         if (cc < L) dvp[(size_t)cc * a.HV * D] = __float2bfloat16_rn(bs[cc] * x[e]);
         cb[e] = ld_bf16(sm + GK_V, cc, row, 64) * x[e];
       }
-      tld(GT_S3, x);   // S dO^T, row = dk index
 #pragma unroll
       for (int e = 0; e < GK_CW; ++e) {
         const int cc = cb0 + e;
         const float pg = a.scale * gs[cc];
-        dq_acc[e] = fmaf(pg, x[e], dq_acc[e]);
-        cg[e] = pg * rq[cc] * ld_bf16(sm + GK_Q, cc, row, 64) * x[e];
+        dq_acc[e] = fmaf(pg, x2[e], dq_acc[e]);
+        cg[e] = pg * rq[cc] * ld_bf16(sm + GK_Q, cc, row, 64) * x2[e];
       }
       // <S, dS'> over this thread's half of the row
       float sd = 0.f;
@@ -751,9 +805,10 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       mma_commit(&mma_bar);
     }
     if (!(ok = mma_sync_wait())) break;
+    if (tid == 0 && h + 1 < a.G) issue_vd(hv + 1);   // V, dO are dead from here on
     {  // H3
-      float x[GK_CW], cz[GK_CW], cy[GK_CW];
-      tld(GT_S4, x);   // dKd^T, row = dk index
+      float x[GK_CW], cz[GK_CW], cy[GK_CW], yv[GK_CW];
+      tld2(GT_S4, x, GT_S0, yv);   // dKd^T and Y^T = dW^T T, rows = dk index
 #pragma unroll
       for (int e = 0; e < GK_CW; ++e) {
         const int cc = cb0 + e;
@@ -761,12 +816,11 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         dk_acc[e] = fmaf(dec, x[e], dk_acc[e]);
         cz[e] = rk[cc] * ld_bf16(sm + GK_K, cc, row, 64) * x[e];
       }
-      tld(GT_S0, x);   // Y^T = dW^T T
 #pragma unroll
       for (int e = 0; e < GK_CW; ++e) {
         const int cc = cb0 + e;
-        dk_acc[e] = fmaf(bs[cc] * gs[cc], x[e], dk_acc[e]);
-        cy[e] = rk[cc] * ld_bf16(sm + GK_K, cc, row, 64) * x[e];
+        dk_acc[e] = fmaf(bs[cc] * gs[cc], yv[e], dk_acc[e]);
+        cy[e] = rk[cc] * ld_bf16(sm + GK_K, cc, row, 64) * yv[e];
       }
       const float sz = colsum16(cz, lane);
       const float sy = colsum16(cy, lane);
@@ -776,10 +830,8 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       }
       // M = 64 results: rows r64 (lanes < 16)
       float daq[GK_CW], qk[GK_CW], t1[GK_CW], t2[GK_CW];
-      tld(GT_S5, daq);
-      tld(GT_QK, qk);
-      tld(GT_S2, t1);
-      tld(GT_S3, t2);
+      tld2(GT_S5, daq, GT_QK, qk);
+      tld2(GT_S2, t1, GT_S3, t2);
       if (lane < 16) {
         const int r = r64;
 #pragma unroll
@@ -815,13 +867,13 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     }
     if (!(ok = mma_sync_wait())) break;
     {  // H4
-      float x[GK_CW];
-      tld(GT_S4, x);
+      float x[GK_CW], x2[GK_CW];
+      tld2(GT_S4, x, GT_S5, x2);
 #pragma unroll
-      for (int e = 0; e < GK_CW; ++e) dq_acc[e] += x[e];
-      tld(GT_S5, x);
-#pragma unroll
-      for (int e = 0; e < GK_CW; ++e) dk_acc[e] += x[e];
+      for (int e = 0; e < GK_CW; ++e) {
+        dq_acc[e] += x[e];
+        dk_acc[e] += x2[e];
+      }
       tld(GT_S1, x);
       if (lane < 16) {
 #pragma unroll
@@ -837,10 +889,10 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       mma_commit(&mma_bar);
     }
     if (!(ok = mma_sync_wait())) break;
+    if (tid == 0 && h + 1 < a.G) issue_t(hv + 1);    // T is dead from here on
     {  // H5: dA rows -> dbeta row terms, C, F1, F2
       float x[GK_CW], kk[GK_CW];
-      tld(GT_S0, x);
-      tld(GT_KK, kk);
+      tld2(GT_S0, x, GT_KK, kk);
       if (lane < 16) {
         const int r = r64;
         const float br = bs[r];
@@ -879,6 +931,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       mma_commit(&mma_bar);
     }
     if (!(ok = mma_sync_wait())) break;
+    if (tid == 0 && h + 1 < a.G) issue_s(hv + 1);    // the S region (H1, H2, F1, F2) is dead
     {
       float x[GK_CW];
       tld(GT_S2, x);
@@ -943,7 +996,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       }
     }
     __syncthreads();
-    if (tid == 0 && h + 1 < a.G) issue_vhead(hv + 1, false);
+    if (tid == 0 && h + 1 < a.G) issue_ds(hv + 1);   // C, partial sums and scalars are dead
   }
 
   // ---- L2-norm backward of the group sums, then dq, dk
@@ -1029,15 +1082,14 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
     prof_end(K_CHECK_SAVED, s);
   }
   if (P.NC == 0) return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
-  st = run_prep(P, &pr, q, k, g, beta, ws, 1, s);
-  if (st != GDN_OK) return st;
+  // the per-chunk UT blocks come from the saved set (written by the forward)
   Tables t = tables_at(P, ws);
   const uint8_t* sv = static_cast<const uint8_t*>(saved);
   BScanArgs ba;
   memset(&ba, 0, sizeof(ba));
   if (!make_tmap(&ba.tq, q, P.T, P.H) || !make_tmap(&ba.tk, k, P.T, P.H) || !make_tmap(&ba.tdo, dO, P.T, P.HV))
     return GDN_ERR_CUDA;
-  ba.cb = ws + P.o_cb;
+  ba.cb = sv + P.s_cb;
   ba.chunk_tok0 = t.chunk_tok0;
   ba.seg_c0 = t.seg_c0;
   ba.seg_c1 = t.seg_c1;
@@ -1082,7 +1134,7 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
   ga.k = static_cast<const __nv_bfloat16*>(k);
   ga.g = g;
   ga.beta = beta;
-  ga.cb = ws + P.o_cb;
+  ga.cb = sv + P.s_cb;
   ga.tape = sv + P.s_tape;
   ga.dtape = ws + P.o_dtape;
   ga.chunk_tok0 = t.chunk_tok0;

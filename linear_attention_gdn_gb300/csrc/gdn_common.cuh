@@ -113,6 +113,13 @@ __device__ __forceinline__ uint32_t taddr(uint32_t base, int lane, int col) {
         "=r"(r[14]), "=r"(r[15])                                                                    \
       : "r"(addr))
 
+// start loading 16 consecutive FP32 columns of this thread's lane (complete with tmem_wait_ld)
+__device__ __forceinline__ void tmem_ld16_async(uint32_t addr, uint32_t (&r)[16]) { GDN_TMEM_LD16(addr, r); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void as_float16(const uint32_t (&r)[16], float* out) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) out[j] = __uint_as_float(r[j]);
+}
 // load 16 consecutive FP32 columns of this thread's lane
 __device__ __forceinline__ void tmem_ld16(uint32_t addr, float* out) {
   uint32_t r[16];

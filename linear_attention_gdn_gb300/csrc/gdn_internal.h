@@ -36,7 +36,7 @@ struct SavedHeader {
   uint32_t scale_bits, cu_hash;
 };
 constexpr uint32_t SAVED_MAGIC = 0x4744'4e31u;   // "GDN1"
-constexpr uint32_t SAVED_VERSION = 1;
+constexpr uint32_t SAVED_VERSION = 2;
 
 // ---- device tables built by the table kernel ----
 struct Tables {
@@ -119,7 +119,7 @@ struct Plan {
   size_t o_dtape, o_dbend, o_dsinit;   // backward
   size_t ws_fwd, ws_bwd;
   // saved offsets
-  size_t s_tape, s_mseg, saved_bytes;
+  size_t s_tape, s_mseg, s_cb, saved_bytes;
 };
 
 inline Tables tables_at(const Plan& P, uint8_t* ws) {
