@@ -33,12 +33,13 @@ constexpr int SC_K = 0, SC_Q = 16384, SC_V = 32768, SC_TP = 49152, SC_TPP = 5734
 constexpr int SC_STAGE = 74752;
 constexpr int SC_S = 2 * SC_STAGE;          // BF16 S^T tile, SwTile(128 x 128)
 constexpr int SC_W = SC_S + STATE_BYTES;    // -W^T tile, SwTile(128 x 64)
-constexpr int SC_O = SC_W + 16384;         // BF16 output staging tile [64 tok][128], SwTile(64 x 128)
-constexpr int SC_SMEM = SC_O + 16384;
+constexpr int SC_O = SC_W + 16384;          // BF16 output staging tile [64 tok][128], SwTile(64 x 128)
+constexpr int SC_SIDE = SC_O + 16384;       // per-token output scales of the last two chunks (+ their L)
+constexpr int SC_SMEM = SC_SIDE + 2 * 272;
 constexpr int SC_SMEM_ALLOC = SC_SMEM + 1024;
 
-// TMEM columns
-constexpr int TM_D1 = 0, TM_DW = 64, TM_DS = 128, TM_O1 = 256, TM_O2 = 320, TM_AVS = 384, TM_AVN = 416;
+// TMEM columns: D1 double-buffered (U^T, then V_new^T, of chunks n and n+1)
+constexpr int TM_D1 = 0, TM_DW = 128, TM_DS = 192, TM_O1 = 320, TM_O2 = 384, TM_AVS = 448, TM_AVN = 480;
 
 __device__ __forceinline__ void store_state_row(uint8_t* dst, int row, const float* S) {
 #pragma unroll
@@ -52,10 +53,15 @@ __device__ __forceinline__ void store_state_row(uint8_t* dst, int row, const flo
   }
 }
 
+// The chain of one chunk is MMA1 (V_new^T = U^T - S^T W^T) -> V_new hop ->
+// MMA2 (dS^T = (V_new^T diag(kd)) K, with the output products) -> S hop.
+// Work that does not feed the chain runs in the shadow of its MMAs:
+// W^T / U^T of chunk n+1 are issued right after MMA1(n) and their hop overlaps
+// MMA2(n); the output epilogue of chunk n-1 overlaps MMA1(n).
 __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant__ ScanArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t full_bar[2], mma_bar;
+  __shared__ uint64_t full_bar[2], bar_m1, bar_w, bar_m2;
   __shared__ uint32_t tslot;
   const int tid = threadIdx.x, warp = tid >> 5;
   if (*(volatile int*)a.err) return;
@@ -99,7 +105,9 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
   if (tid == 0) {
     mbar_init(&full_bar[0], 1);
     mbar_init(&full_bar[1], 1);
-    mbar_init(&mma_bar, 1);
+    mbar_init(&bar_m1, 1);
+    mbar_init(&bar_w, 1);
+    mbar_init(&bar_m2, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   fence_async_smem();
@@ -133,19 +141,18 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
     if (nch > 1) issue(1);
   }
 
-  uint32_t mph = 0;
+  uint32_t ph_m1 = 0, ph_w = 0, ph_m2 = 0;
   bool ok = true;
   const uint32_t sm_s = smem_u32(s_tile), sm_w = smem_u32(sm + SC_W);
-  for (int n = 0; n < nch && ok; ++n) {
+  float* side = reinterpret_cast<float*>(sm + SC_SIDE);   // [2][68]: sc[64], L
+
+  // wait for chunk n's tiles; zero the rows past a document end (they hold the next document)
+  auto land = [&](int n) -> bool {
     uint8_t* st = sm + (n & 1) * SC_STAGE;
-    const uint32_t a_k = smem_u32(st + SC_K), a_q = smem_u32(st + SC_Q), a_v = smem_u32(st + SC_V);
-    const uint32_t a_tp = smem_u32(st + SC_TP), a_tpp = smem_u32(st + SC_TPP), a_aqk = smem_u32(st + SC_AQK);
-    const float* scal = reinterpret_cast<const float*>(st + SC_SCAL);
-    ok = __syncthreads_and(mbar_wait(&full_bar[n & 1], (n >> 1) & 1, a.err));
-    if (!ok) break;
-    const int L = reinterpret_cast<const int*>(scal)[129];
-    if (L < CH) {  // rows past the document end hold the next document's tokens: zero them
-      for (int idx = tid; idx < (CH - L) * 2 * 8 * 3; idx += 128) {
+    if (!__syncthreads_and(mbar_wait(&full_bar[n & 1], (n >> 1) & 1, a.err))) return false;
+    const int L = reinterpret_cast<const int*>(st + SC_SCAL)[129];
+    if (L < CH) {
+      for (int idx = tid; idx < (CH - L) * 48; idx += 128) {
         const int t = idx / 48, rem = idx % 48, tile = rem / 16, c8 = rem % 16;
         const int off = tile == 0 ? SC_K : (tile == 1 ? SC_Q : SC_V);
         *reinterpret_cast<uint4*>(st + off + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
@@ -153,62 +160,119 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
       fence_async_smem();
       __syncthreads();
     }
-    // ---- W^T, U^T (into D1), S^T Q^T
+    return true;
+  };
+  // W^T of chunk n -> DW, U^T -> D1[n & 1]
+  auto issue_wu = [&](int n) {
+    uint8_t* st = sm + (n & 1) * SC_STAGE;
+    const uint32_t a_k = smem_u32(st + SC_K), a_v = smem_u32(st + SC_V);
+    const uint32_t a_tp = smem_u32(st + SC_TP), a_tpp = smem_u32(st + SC_TPP);
     tc_fence_after();
-    if (tid == 0) {
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma_ss_w(tb + TM_DW, desc_mn(a_k, 64, ks), desc_k(a_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+    if (with_u) {
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tb + TM_DW, desc_mn(a_k, 64, ks), desc_k(a_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
-      if (with_u) {
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ss(tb + TM_D1, desc_mn(a_v, 64, ks), desc_k(a_tpp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
-      }
-      if (with_o) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ss(tb + TM_O1, desc_k(sm_s, 128, ks), desc_k(a_q, 64, ks), idesc(128, 64, 0, 0), ks > 0);
-      }
-      mma_commit(&mma_bar);
+        mma_ss_w(tb + TM_D1 + (n & 1) * 64, desc_mn(a_v, 64, ks), desc_k(a_tpp, 64, ks), idesc(128, 64, 1, 0),
+               ks > 0);
     }
-    ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
-    mph ^= 1;
-    if (!ok) break;
-    tc_fence_after();
-    {  // -W^T -> shared (row tid = dk index), MN-major B operand of the next MMA
-      float w[64];
-      tmem_ld32(taddr(tb, warp * 32, TM_DW), w);
-      tmem_ld32(taddr(tb, warp * 32, TM_DW + 32), w + 32);
-      uint8_t* wt = sm + SC_W;
+    mma_commit_w(&bar_w);
+  };
+  // -W^T -> shared (row tid = dk index), the MN-major B operand of MMA1
+  auto hop_w = [&]() {
+    float w[64];
+    tmem_ld32(taddr(tb, warp * 32, TM_DW), w);
+    tmem_ld32(taddr(tb, warp * 32, TM_DW + 32), w + 32);
+    uint8_t* wt = sm + SC_W;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        uint4 v;
-        v.x = pack_bf16(-w[c8 * 8 + 0], -w[c8 * 8 + 1]);
-        v.y = pack_bf16(-w[c8 * 8 + 2], -w[c8 * 8 + 3]);
-        v.z = pack_bf16(-w[c8 * 8 + 4], -w[c8 * 8 + 5]);
-        v.w = pack_bf16(-w[c8 * 8 + 6], -w[c8 * 8 + 7]);
-        *reinterpret_cast<uint4*>(wt + sw_chunk(tid, c8, 128)) = v;
+    for (int c8 = 0; c8 < 8; ++c8) {
+      uint4 v;
+      v.x = pack_bf16(-w[c8 * 8 + 0], -w[c8 * 8 + 1]);
+      v.y = pack_bf16(-w[c8 * 8 + 2], -w[c8 * 8 + 3]);
+      v.z = pack_bf16(-w[c8 * 8 + 4], -w[c8 * 8 + 5]);
+      v.w = pack_bf16(-w[c8 * 8 + 6], -w[c8 * 8 + 7]);
+      *reinterpret_cast<uint4*>(wt + sw_chunk(tid, c8, 128)) = v;
+    }
+    fence_async_smem();
+  };
+  // output of chunk n from O1, O2 (TMEM) with the saved per-token scales
+  uint8_t* o_stage = sm + SC_O;
+  auto output = [&](int n) {
+    const float* sc = side + (n & 1) * 68;
+    const int L = reinterpret_cast<const int*>(sc)[64];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float x1[32], x2[32];
+      tmem_ld32(taddr(tb, warp * 32, TM_O1 + h * 32), x1);
+      tmem_ld32(taddr(tb, warp * 32, TM_O2 + h * 32), x2);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int r = h * 32 + e;
+        *reinterpret_cast<__nv_bfloat16*>(o_stage + sw_off(r, tid, 64)) =
+            __float2bfloat16_rn(fmaf(sc[r], x1[e], a.scale * x2[e]));
       }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
+    const int t0 = a.chunk_tok0[c0 + n];
+    if (L < CH) {  // ragged last chunk: only its own rows (the next rows are another document's)
+      for (int idx = tid; idx < L * 16; idx += 128) {
+        const int r = idx >> 4, c8 = idx & 15;
+        *reinterpret_cast<uint4*>(a.o + ((size_t)(t0 + r) * a.HV + hv) * D + c8 * 8) =
+            *reinterpret_cast<const uint4*>(o_stage + sw_chunk(r, c8, 64));
+      }
+    } else if (tid == 0) {
+      tma_store_3d(&a.to, o_stage, 0, hv, t0);
+      tma_store_3d(&a.to, o_stage + 8192, 64, hv, t0);
+      bulk_commit();
+    }
+  };
+
+  // ---- prologue: W^T, U^T of chunk 0 and its -W^T tile
+  if (nch > 0) {
+    ok = land(0);
+    if (ok && warp == 0) issue_wu(0);
+    ok = ok && __syncthreads_and(mbar_wait(&bar_w, ph_w, a.err));
+    ph_w ^= 1;
     tc_fence_after();
-    if (tid == 0) {  // V_new^T = U^T - S^T W^T
+    if (ok) hop_w();
+    tc_fence_before();
+    __syncthreads();
+  }
+  for (int n = 0; n < nch && ok; ++n) {
+    uint8_t* st = sm + (n & 1) * SC_STAGE;
+    const uint32_t a_k = smem_u32(st + SC_K), a_q = smem_u32(st + SC_Q), a_aqk = smem_u32(st + SC_AQK);
+    const float* scal = reinterpret_cast<const float*>(st + SC_SCAL);
+    const uint32_t d1 = tb + TM_D1 + (n & 1) * 64;
+    // ---- MMA1: V_new^T = U^T - S^T W^T (into D1[n & 1])
+    if (warp == 0) {
+      tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        mma_ss(tb + TM_D1, desc_k(sm_s, 128, ks), desc_mn(sm_w, 128, ks), idesc(128, 64, 0, 1),
-               (with_u || ks > 0) ? 1u : 0u);
-      mma_commit(&mma_bar);
+        mma_ss_w(d1, desc_k(sm_s, 128, ks), desc_mn(sm_w, 128, ks), idesc(128, 64, 0, 1),
+                 (with_u || ks > 0) ? 1u : 0u);
+      mma_commit_w(&bar_m1);
     }
-    ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
-    mph ^= 1;
+    // ---- in its shadow: the output of chunk n - 1, then W^T / U^T of chunk n + 1
+    if (with_o && n > 0) {
+      tc_fence_after();
+      output(n - 1);
+    }
+    const bool next = n + 1 < nch;
+    if (next) {
+      if (!(ok = land(n + 1))) break;
+      if (warp == 0) issue_wu(n + 1);
+    }
+    ok = __syncthreads_and(mbar_wait(&bar_m1, ph_m1, a.err));
+    ph_m1 ^= 1;
     if (!ok) break;
     tc_fence_after();
     {  // V_new^T row tid -> TMEM A operands: scaled by kd (state update), plain (output)
       float vn[64];
-      tmem_ld32(taddr(tb, warp * 32, TM_D1), vn);
-      tmem_ld32(taddr(tb, warp * 32, TM_D1 + 32), vn + 32);
+      tmem_ld32(taddr(tb, warp * 32, d1 - tb), vn);
+      tmem_ld32(taddr(tb, warp * 32, d1 - tb + 32), vn + 32);
       const float* kd = scal + 64;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -222,25 +286,42 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
         tmem_st8(taddr(tb, warp * 32, TM_AVS + q * 8), ps);
         if (with_o) tmem_st8(taddr(tb, warp * 32, TM_AVN + q * 8), pn);
       }
+      if (with_o) {  // this chunk's output scales outlive its stage buffer
+        float* sd = side + (n & 1) * 68;
+        if (tid < 64) sd[tid] = scal[tid];
+        if (tid == 64) reinterpret_cast<int*>(sd)[64] = reinterpret_cast<const int*>(scal)[129];
+      }
       tmem_wait_st();
     }
     tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
+    // ---- MMA2: dS^T = (V_new^T diag(kd)) K; O2 = V_new^T Aqk^T; O1 = S^T Q^T
+    if (warp == 0) {
+      tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_ts(tb + TM_DS, tb + TM_AVS + ks * 8, desc_mn(a_k, 64, ks), idesc(128, 128, 0, 1), ks > 0);
+        mma_ts_w(tb + TM_DS, tb + TM_AVS + ks * 8, desc_mn(a_k, 64, ks), idesc(128, 128, 0, 1), ks > 0);
       if (with_o) {
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          mma_ts(tb + TM_O2, tb + TM_AVN + ks * 8, desc_k(a_aqk, 64, ks), idesc(128, 64, 0, 0), ks > 0);
+          mma_ts_w(tb + TM_O2, tb + TM_AVN + ks * 8, desc_k(a_aqk, 64, ks), idesc(128, 64, 0, 0), ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ss_w(tb + TM_O1, desc_k(sm_s, 128, ks), desc_k(a_q, 64, ks), idesc(128, 64, 0, 0), ks > 0);
       }
-      mma_commit(&mma_bar);
-      bulk_wait_read();   // the last chunk's tape / output stores have read the tiles rewritten below
+      mma_commit_w(&bar_m2);
+      if (tid == 0) bulk_wait_read();   // earlier tape / output stores have read the tiles rewritten below
     }
-    ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
-    mph ^= 1;
+    // ---- in its shadow: the -W^T tile of chunk n + 1
+    if (next) {
+      ok = __syncthreads_and(mbar_wait(&bar_w, ph_w, a.err));
+      ph_w ^= 1;
+      if (!ok) break;
+      tc_fence_after();
+      hop_w();
+    }
+    ok = __syncthreads_and(mbar_wait(&bar_m2, ph_m2, a.err));
+    ph_m2 ^= 1;
     if (!ok) break;
     tc_fence_after();
     {  // S^T <- gamma_L S^T + dS^T
@@ -252,46 +333,24 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 32; ++e) S[h * 32 + e] = fmaf(gL, S[h * 32 + e], ds[e]);
       }
-      store_state_row(s_tile, tid, S);   // also the saved state entering the next chunk (bulk copy below)
-    }
-    uint8_t* o_stage = sm + SC_O;
-    if (with_o) {  // O^T row tid -> staging tile [token][feature]: o = sc_r (S^T Q^T) + scale (V_new^T Aqk^T)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float x1[32], x2[32];
-        tmem_ld32(taddr(tb, warp * 32, TM_O1 + h * 32), x1);
-        tmem_ld32(taddr(tb, warp * 32, TM_O2 + h * 32), x2);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int r = h * 32 + e;
-          *reinterpret_cast<__nv_bfloat16*>(o_stage + sw_off(r, tid, 64)) =
-              __float2bfloat16_rn(fmaf(scal[r], x1[e], a.scale * x2[e]));
-        }
-      }
+      store_state_row(s_tile, tid, S);   // also the saved state entering the next chunk
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    const int t0 = a.chunk_tok0[c0 + n];
-    if (with_o && L < CH) {  // ragged last chunk: only its own rows (the next rows are another document's)
-      for (int idx = tid; idx < L * 16; idx += 128) {
-        const int r = idx >> 4, c8 = idx & 15;
-        *reinterpret_cast<uint4*>(a.o + ((size_t)(t0 + r) * a.HV + hv) * D + c8 * 8) =
-            *reinterpret_cast<const uint4*>(o_stage + sw_chunk(r, c8, 64));
-      }
-    }
-    if (tid == 0) {  // asynchronous stores of the saved state and the output tile
-      if (mode == 0 && a.tape && n + 1 < nch)
+    if (tid == 0) {
+      if (mode == 0 && a.tape && next) {
         bulk_store(a.tape + ((size_t)(c0 + n + 1) * a.HV + hv) * STATE_BYTES, s_tile, STATE_BYTES);
-      if (with_o && L == CH) {
-        tma_store_3d(&a.to, o_stage, 0, hv, t0);
-        tma_store_3d(&a.to, o_stage + 8192, 64, hv, t0);
+        bulk_commit();
       }
-      bulk_commit();
-      if (n + 2 < nch) issue(n + 2);
+      if (n + 2 < nch) issue(n + 2);   // chunk n's stage is dead: its scales are in `side`
     }
   }
-  if (tid == 0) bulk_wait_all();
+  if (ok && with_o && nch > 0) {
+    tc_fence_after();
+    output(nch - 1);
+  }
+  if (tid == 0) bulk_wait_read();
   if (ok && mode != 0) {
     float* dst = (mode == 1 ? a.bend : a.mend) + ((size_t)split * a.HV + hv) * STATE_F32 + (size_t)tid * 128;
 #pragma unroll
