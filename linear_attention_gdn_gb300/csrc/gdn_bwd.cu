@@ -388,7 +388,7 @@ constexpr int GK_SMEM = 214016;
 constexpr int GK_SMEM_ALLOC = GK_SMEM + 1024;
 constexpr int GK_DT = GK_TP, GK_R1 = GK_TPP;                                   // free after M1
 constexpr int GK_H1 = GK_S, GK_H2 = GK_S + 8192, GK_F1 = GK_S + 16384, GK_F2 = GK_S + 24576;  // after M3
-constexpr int GK_C = GK_DS;                   // FP32 [64][65] of dAqk.Aqk + dA.A, after M3
+constexpr int GK_C = GK_DV;                   // FP32 [64][65] of dAqk.Aqk + dA.A, after M3 (dV, VN dead)
 constexpr int GK_CLD = 65;                    // padded row pitch of C (no bank conflicts)
 constexpr int GK_PART = GK_AQ;                // FP32 partial column sums [6][4][64], after M1
 constexpr int GT_KK = 0, GT_QK = 64, GT_S0 = 128, GT_S1 = 192, GT_S2 = 256, GT_S3 = 320, GT_S4 = 384, GT_S5 = 448;
@@ -805,7 +805,10 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       mma_commit(&mma_bar);
     }
     if (!(ok = mma_sync_wait())) break;
-    if (tid == 0 && h + 1 < a.G) issue_vd(hv + 1);   // V, dO are dead from here on
+    if (tid == 0 && h + 1 < a.G) {   // V, dO, dS' and the scalars are dead from here on
+      issue_vd(hv + 1);
+      issue_ds(hv + 1);
+    }
     {  // H3
       float x[GK_CW], cz[GK_CW], cy[GK_CW], yv[GK_CW];
       tld2(GT_S4, x, GT_S0, yv);   // dKd^T and Y^T = dW^T T, rows = dk index
@@ -996,7 +999,6 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       }
     }
     __syncthreads();
-    if (tid == 0 && h + 1 < a.G) issue_ds(hv + 1);   // C, partial sums and scalars are dead
   }
 
   // ---- L2-norm backward of the group sums, then dq, dk
