@@ -92,7 +92,9 @@ typedef enum {
  *                    that the backward's merges read ("#8542" page: the full
  *                    saved set keeps M_seg at P > 1), and the per-chunk UT
  *                    blocks (T = (I + A)^-1 with its scaled forms and the gated
- *                    Aqk rows, 33 KiB per chunk and value head) so that the
+ *                    Aqk rows, 33 KiB per chunk and value head) and the BF16
+ *                    V_new^T = (U - W S)^T of every chunk (16 KiB per chunk
+ *                    and value head; the pages' v_new rows), so that the
  *                    backward does not recompute them.
  *   workspace_bytes  scratch for one gdn_fwd / gdn_bwd / gdn_ckpt_fwd_bwd call.
  * Returns GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED on a bad problem.

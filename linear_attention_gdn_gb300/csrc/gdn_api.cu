@@ -145,6 +145,8 @@ static gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
   P->ws_fwd = off;
   P->o_dtape = off;
   off += (size_t)NC * P->HV * STATE_BYTES;
+  P->o_dvn = off;
+  off += (size_t)NC * P->HV * VN_BYTES;
   P->o_dbend = off;
   off += st_f32;
   P->o_dsinit = off;
@@ -154,7 +156,8 @@ static gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
   P->s_tape = SAVED_HEADER;
   P->s_mseg = P->s_tape + (size_t)NC * P->HV * STATE_BYTES;
   P->s_cb = align_up(P->s_mseg + st_f32, 1024);
-  P->saved_bytes = P->s_cb + (size_t)NC * P->HV * CB_BYTES;
+  P->s_vn = P->s_cb + (size_t)NC * P->HV * CB_BYTES;
+  P->saved_bytes = P->s_vn + (size_t)NC * P->HV * VN_BYTES;
   return GDN_OK;
 }
 
@@ -367,6 +370,7 @@ static gdn_status run_fwd(const Plan& P, const gdn_problem* p, const void* q, co
   }
   sa.walk = 0;
   sa.tape = saved ? static_cast<uint8_t*>(saved) + P.s_tape : nullptr;
+  sa.vn = saved ? static_cast<uint8_t*>(saved) + P.s_vn : nullptr;
   sa.o = static_cast<__nv_bfloat16*>(o);
   if (o && !make_tmap(&sa.to, o, P.T, P.HV)) return GDN_ERR_CUDA;
   launch_fwd_scan(sa, P.NSEG * P.HV, s);

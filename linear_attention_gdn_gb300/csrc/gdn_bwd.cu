@@ -48,6 +48,7 @@ struct BScanArgs {
   int HV, G, nsplit, walk;
   float scale;
   uint8_t* dtape;        // [NC][HV][STATE_BYTES]
+  uint8_t* dvn;          // [NC][HV][VN_BYTES] dV_new^T tiles (full walks)
   const float* ds_init;  // [nsplit][HV][STATE_F32]: adjoint at the end of split segment i
   float* dbend;          // [nsplit][HV][STATE_F32]
   int* err;
@@ -62,6 +63,8 @@ struct GradArgs {
   const uint8_t* cb;
   const uint8_t* tape;    // saved S^T per chunk
   const uint8_t* dtape;   // dS'^T per chunk
+  const uint8_t* vn;      // V_new^T per chunk (saved by the forward)
+  const uint8_t* dvn;     // dV_new^T per chunk (written by the adjoint walk)
   const int* chunk_tok0;
   const int* chunk_len;
   __nv_bfloat16* dq;
@@ -96,7 +99,8 @@ constexpr int BS_K = 0, BS_Q = 16384, BS_DO = 32768, BS_TP = 49152, BS_AQK = 573
 constexpr int BS_STAGE = 66560;
 constexpr int BS_DS = 2 * BS_STAGE;           // BF16 dS'^T tile
 constexpr int BS_W = BS_DS + STATE_BYTES;     // -W^T tile, SwTile(128 x 64)
-constexpr int BS_SMEM = BS_W + 16384;
+constexpr int BS_DV = BS_W + 16384;           // dV_new^T staging, SwTile(128 x 64)
+constexpr int BS_SMEM = BS_DV + VN_BYTES;
 constexpr int BS_SMEM_ALLOC = BS_SMEM + 1024;
 constexpr int BT_DW = 0, BT_DX = 64, BT_DY = 128, BT_DS = 192, BT_ADV = 320, BT_ADO = 352;
 
@@ -266,6 +270,12 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
             p8[e] = pack_bf16(fmaf(a.scale, x[j], kd[r] * y[j]), fmaf(a.scale, x[j + 1], kd[r + 1] * y[j + 1]));
           }
           tmem_st8(taddr(tb, warp * 32, BT_ADV + h * 16 + q * 8), p8);
+          if (!a.walk) {
+            uint8_t* dvt = sm + BS_DV;
+            const int c8 = h * 4 + q * 2;
+            *reinterpret_cast<uint4*>(dvt + sw_chunk(tid, c8, 128)) = make_uint4(p8[0], p8[1], p8[2], p8[3]);
+            *reinterpret_cast<uint4*>(dvt + sw_chunk(tid, c8 + 1, 128)) = make_uint4(p8[4], p8[5], p8[6], p8[7]);
+          }
         }
       }
       tmem_wait_st();
@@ -275,6 +285,10 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
     __syncthreads();
     tc_fence_after();
     if (tid == 0) {
+      if (!a.walk) {   // this chunk's dV_new^T for the gradient kernel
+        bulk_store(a.dvn + ((size_t)ci * a.HV + hv) * VN_BYTES, sm + BS_DV, VN_BYTES);
+        bulk_commit();
+      }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_ts(tb + BT_DS, tb + BT_ADV + ks * 8, desc_k(sm_w, 128, ks), idesc(128, 128, 0, 0), ks > 0);
@@ -282,7 +296,7 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
       for (int ks = 0; ks < 4; ++ks)
         mma_ts(tb + BT_DS, tb + BT_ADO + ks * 8, desc_mn(a_q, 64, ks), idesc(128, 128, 0, 1), 1u);
       mma_commit(&mma_bar);
-      bulk_wait_read();   // the tape copy has read the dS'^T tile rewritten below
+      bulk_wait_read();   // the tape copies have read the dS'^T and dV_new^T tiles rewritten next
     }
     ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
     mph ^= 1;
@@ -381,17 +395,19 @@ __global__ void check_saved_kernel(CheckArgs a) {
 // ===========================================================================
 // chunk gradients
 // ===========================================================================
-constexpr int GK_Q = 0, GK_K = 16384, GK_V = 32768, GK_DO = 49152, GK_S = 65536, GK_DS = 98304,
-              GK_T = 131072, GK_SCAL = 139264;
-constexpr int GK_WD = 140288, GK_DV = 156672, GK_VN = 173056, GK_TP = 189440, GK_TPP = 197632, GK_AQ = 205824;
-constexpr int GK_SMEM = 214016;
+// Shared memory of the chunk-gradient kernel (bytes; tiles 1024-aligned).
+constexpr int GK_Q = 0, GK_K = 16384, GK_KQ = 32768, GK_V = 50176, GK_DO = 66560, GK_DV = 82944,
+              GK_VN = 99328, GK_S = 115712, GK_DS = 148480, GK_T = 181248, GK_SCAL = 189440, GK_WD = 190464;
+constexpr int GK_SMEM = 206848;
 constexpr int GK_SMEM_ALLOC = GK_SMEM + 1024;
-constexpr int GK_DT = GK_TP, GK_R1 = GK_TPP;                                   // free after M1
-constexpr int GK_H1 = GK_S, GK_H2 = GK_S + 8192, GK_F1 = GK_S + 16384, GK_F2 = GK_S + 24576;  // after M3
-constexpr int GK_C = GK_DV;                   // FP32 [64][65] of dAqk.Aqk + dA.A, after M3 (dV, VN dead)
-constexpr int GK_CLD = 65;                    // padded row pitch of C (no bank conflicts)
-constexpr int GK_PART = GK_AQ;                // FP32 partial column sums [6][4][64], after M1
-constexpr int GT_KK = 0, GT_QK = 64, GT_S0 = 128, GT_S1 = 192, GT_S2 = 256, GT_S3 = 320, GT_S4 = 384, GT_S5 = 448;
+constexpr int GK_KQLD = 68;   // row pitch (floats) of the FP32 [QK^T lower | KK^T upper] table
+static_assert(GK_KQ + 64 * GK_KQLD * 4 <= GK_V, "KQ table");
+// regions reused once their first contents are dead
+constexpr int GK_H1 = GK_DO, GK_H2 = GK_DO + 8192;   // after MA (dO dead)
+constexpr int GK_DT = GK_DV, GK_R1 = GK_DV + 8192;   // after MA (dV_new dead)
+constexpr int GK_F1 = GK_WD, GK_F2 = GK_WD + 8192;   // after MB (dW dead)
+// TMEM columns: dq^T, dk^T accumulators of the group, then six 64-column results
+constexpr int GT_DQ = 0, GT_DK = 64, GT_A0 = 128, GT_A1 = 192, GT_A2 = 256, GT_A3 = 320, GT_A4 = 384, GT_A5 = 448;
 
 constexpr int GK_NWG = 4;                    // warpgroups; each takes GK_CW of the 64 token columns
 constexpr int GK_CW = 64 / GK_NWG;
@@ -421,15 +437,31 @@ __device__ __forceinline__ void store_chunk8(uint8_t* tile, int r, int c8, int R
   *reinterpret_cast<uint4*>(tile + sw_chunk(r, c8, R)) = w;
 }
 
+// One CTA per (chunk, q/k head); its value heads one after another.  Every
+// operand of the first MMA group of a value head comes from memory: S and
+// dS' from the two tapes, V_new^T from the forward, dV_new^T from the
+// adjoint walk, V, dO, and T from the saved UT block.  Per value head:
+//   MA  S dV_new^T (= -dW^T), S dO^T, X^T = dV_new^T T, dKd^T = dS' V_new^T,
+//       dO V_new^T (-> dAqk), dV_new V^T                       (44 MMAs)
+//   MB  dW K^T, Y^T = dW^T T
+//   M4  R1 = dT T^T, K^T H1 (+= dq^T), Q^T H2 (+= dk^T)
+//   M5  T^T R1 (= -dA)
+//   M6  K^T F1 + K^T F2 (+= dk^T)
+// Each CUDA-core pass first writes what the next group reads, hands off, and
+// does its side work (dv, column-scaled dq / dk terms, per-token partial
+// sums) while that group runs.  The next value head's loads are requested as
+// soon as the buffers they land in are dead.
 __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_constant__ GradArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t bar_qk, bar_vd, bar_t, bar_s, bar_ds, mma_bar;
+  __shared__ uint64_t bar_qk, bar_vn, bar_sv, bar_do, bar_dt, mma_bar;
   __shared__ float gall[8][CH], ball[8][CH];   // the group's gates, prefetched (first 8 value heads)
   __shared__ uint32_t tslot;
   __shared__ float rq[CH], rk[CH], Gs[CH], bs[CH], gs[CH], decs[CH], eGr[CH], eGi[CH];
   __shared__ int gsafe;
-  __shared__ float rowB[GK_NWG][CH], sdot[GK_THREADS / 32], cdiff[CH];
+  __shared__ float part[6][4][CH];             // per-token partial sums, one row per 32-lane quarter
+  __shared__ float colC[2][4][CH];             // column sums of C (dAqk . Aqk, dA . A) per quarter
+  __shared__ float rowC[GK_NWG][CH], rowB[GK_NWG][CH], sdot[GK_THREADS / 32];
   const int c = blockIdx.x, j = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wg = tid >> 7, w4 = warp & 3;
@@ -442,36 +474,37 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
   if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {
     mbar_init(&bar_qk, 1);
-    mbar_init(&bar_vd, 1);
-    mbar_init(&bar_t, 1);
-    mbar_init(&bar_s, 1);
-    mbar_init(&bar_ds, 1);
+    mbar_init(&bar_vn, 1);
+    mbar_init(&bar_sv, 1);
+    mbar_init(&bar_do, 1);
+    mbar_init(&bar_dt, 1);
     mbar_init(&mma_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   __syncthreads();
   const uint32_t tb = tslot;
-  // Each value head's inputs land on four barriers, requested as soon as the
-  // buffer they overwrite is dead in the previous value head.
-  auto issue_vd = [&](int hv) {   // V, dO tiles
-    mbar_expect_tx(&bar_vd, 32768u);
-    tma_load_3d(sm + GK_V, &a.tv, 0, hv, tok0, &bar_vd);
-    tma_load_3d(sm + GK_V + 8192, &a.tv, 64, hv, tok0, &bar_vd);
-    tma_load_3d(sm + GK_DO, &a.tdo, 0, hv, tok0, &bar_vd);
-    tma_load_3d(sm + GK_DO + 8192, &a.tdo, 64, hv, tok0, &bar_vd);
+  const size_t tile_idx0 = (size_t)c * a.HV;
+  auto issue_vn = [&](int hv) {   // V_new^T
+    mbar_expect_tx(&bar_vn, (uint32_t)VN_BYTES);
+    bulk_load(sm + GK_VN, a.vn + (tile_idx0 + hv) * VN_BYTES, VN_BYTES, &bar_vn);
   };
-  auto issue_t = [&](int hv) {
-    mbar_expect_tx(&bar_t, (uint32_t)TILE64_BYTES);
-    bulk_load(sm + GK_T, a.cb + ((size_t)c * a.HV + hv) * CB_BYTES + CB_T, TILE64_BYTES, &bar_t);
+  auto issue_sv = [&](int hv) {   // S, dS', V and the chunk scalars
+    mbar_expect_tx(&bar_sv, (uint32_t)(2 * STATE_BYTES + 16384 + CB_SCAL_BYTES));
+    bulk_load(sm + GK_S, a.tape + (tile_idx0 + hv) * STATE_BYTES, STATE_BYTES, &bar_sv);
+    bulk_load(sm + GK_DS, a.dtape + (tile_idx0 + hv) * STATE_BYTES, STATE_BYTES, &bar_sv);
+    tma_load_3d(sm + GK_V, &a.tv, 0, hv, tok0, &bar_sv);
+    tma_load_3d(sm + GK_V + 8192, &a.tv, 64, hv, tok0, &bar_sv);
+    bulk_load(sm + GK_SCAL, a.cb + (tile_idx0 + hv) * CB_BYTES + CB_SCAL, CB_SCAL_BYTES, &bar_sv);
   };
-  auto issue_s = [&](int hv) {
-    mbar_expect_tx(&bar_s, (uint32_t)STATE_BYTES);
-    bulk_load(sm + GK_S, a.tape + ((size_t)c * a.HV + hv) * STATE_BYTES, STATE_BYTES, &bar_s);
+  auto issue_do = [&](int hv) {
+    mbar_expect_tx(&bar_do, 16384u);
+    tma_load_3d(sm + GK_DO, &a.tdo, 0, hv, tok0, &bar_do);
+    tma_load_3d(sm + GK_DO + 8192, &a.tdo, 64, hv, tok0, &bar_do);
   };
-  auto issue_ds = [&](int hv) {   // dS' tile and the chunk scalars
-    mbar_expect_tx(&bar_ds, (uint32_t)(STATE_BYTES + CB_SCAL_BYTES));
-    bulk_load(sm + GK_DS, a.dtape + ((size_t)c * a.HV + hv) * STATE_BYTES, STATE_BYTES, &bar_ds);
-    bulk_load(sm + GK_SCAL, a.cb + ((size_t)c * a.HV + hv) * CB_BYTES + CB_SCAL, CB_SCAL_BYTES, &bar_ds);
+  auto issue_dt = [&](int hv) {   // dV_new^T and T
+    mbar_expect_tx(&bar_dt, (uint32_t)(VN_BYTES + TILE64_BYTES));
+    bulk_load(sm + GK_DV, a.dvn + (tile_idx0 + hv) * VN_BYTES, VN_BYTES, &bar_dt);
+    bulk_load(sm + GK_T, a.cb + (tile_idx0 + hv) * CB_BYTES + CB_T, TILE64_BYTES, &bar_dt);
   };
   if (tid == 0) {
     mbar_expect_tx(&bar_qk, 32768u);
@@ -479,10 +512,10 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     tma_load_3d(sm + GK_Q + 8192, &a.tq, 64, j, tok0, &bar_qk);
     tma_load_3d(sm + GK_K, &a.tk, 0, j, tok0, &bar_qk);
     tma_load_3d(sm + GK_K + 8192, &a.tk, 64, j, tok0, &bar_qk);
-    issue_vd(j * a.G);
-    issue_t(j * a.G);
-    issue_s(j * a.G);
-    issue_ds(j * a.G);
+    issue_vn(j * a.G);
+    issue_sv(j * a.G);
+    issue_do(j * a.G);
+    issue_dt(j * a.G);
   }
   for (int i = tid; i < min(a.G, 8) * CH; i += GK_THREADS) {   // gates of the group
     const int hh = i / CH, r = i % CH;
@@ -509,13 +542,11 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
   const uint32_t s_q = smem_u32(sm + GK_Q), s_k = smem_u32(sm + GK_K), s_v = smem_u32(sm + GK_V),
                  s_do = smem_u32(sm + GK_DO), s_s = smem_u32(sm + GK_S), s_ds = smem_u32(sm + GK_DS),
                  s_t = smem_u32(sm + GK_T), s_wd = smem_u32(sm + GK_WD), s_dv = smem_u32(sm + GK_DV),
-                 s_vn = smem_u32(sm + GK_VN), s_tp = smem_u32(sm + GK_TP), s_tpp = smem_u32(sm + GK_TPP),
-                 s_aq = smem_u32(sm + GK_AQ), s_dt = smem_u32(sm + GK_DT), s_r1 = smem_u32(sm + GK_R1),
+                 s_vn = smem_u32(sm + GK_VN), s_dt = smem_u32(sm + GK_DT), s_r1 = smem_u32(sm + GK_R1),
                  s_h1 = smem_u32(sm + GK_H1), s_h2 = smem_u32(sm + GK_H2), s_f1 = smem_u32(sm + GK_F1),
                  s_f2 = smem_u32(sm + GK_F2);
   const float* scal = reinterpret_cast<const float*>(sm + GK_SCAL);
-  float* Cm = reinterpret_cast<float*>(sm + GK_C);
-  float* part = reinterpret_cast<float*>(sm + GK_PART);
+  float* KQ = reinterpret_cast<float*>(sm + GK_KQ);
   auto tld = [&](int col, float* out) { tmem_ld16(taddr(tb, w4 * 32, col + cb0), out); };
   // issue several TMEM loads, then wait once
   auto tld2 = [&](int c0_, float* o0, int c1_, float* o1) {
@@ -527,7 +558,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     as_float16(r1, o1);
   };
 
-  float dq_acc[GK_CW], dk_acc[GK_CW];   // dq^T, dk^T [row][cb0 + e], summed over the group
+  float dq_acc[GK_CW], dk_acc[GK_CW];   // the column-scaled dq^T, dk^T terms [row][cb0 + e]
 #pragma unroll
   for (int e = 0; e < GK_CW; ++e) dq_acc[e] = dk_acc[e] = 0.f;
 
@@ -537,27 +568,59 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     if (h == 0) {
       ok = __syncthreads_and(mbar_wait(&bar_qk, 0, a.err));
       if (!ok) break;
-    }
-    if (h == 0 && tid < 128) {   // L2 norms of the q/k rows
-      const uint8_t* tile = sm + (tid < 64 ? GK_K : GK_Q);
-      const int r = tid & 63;
-      float ss = 0.f;
-      if (r < L) {   // same summation order as the prep kernel's norms
-#pragma unroll
-        for (int c8 = 0; c8 < 16; ++c8) {
-          const uint4 val = *reinterpret_cast<const uint4*>(tile + sw_chunk(r, c8, 64));
-          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&val);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(h2[e]);
-            ss = fmaf(f.x, f.x, ss);
-            ss = fmaf(f.y, f.y, ss);
-          }
+      if (L < CH) {   // zero the Q, K rows past the document end (they hold the next document)
+        for (int idx = tid; idx < (CH - L) * 32; idx += GK_THREADS) {
+          const int t = idx >> 5, tile = (idx >> 4) & 1, c8 = idx & 15;
+          *reinterpret_cast<uint4*>(sm + (tile ? GK_K : GK_Q) + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      const float rn = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-      if (tid < 64) rk[r] = rn;
-      else rq[r] = rn;
+      if (tid < 128) {   // L2 norms of the q/k rows
+        const uint8_t* tile = sm + (tid < 64 ? GK_K : GK_Q);
+        const int r = tid & 63;
+        float ss = 0.f;
+        if (r < L) {   // same summation order as the prep kernel's norms
+#pragma unroll
+          for (int c8 = 0; c8 < 16; ++c8) {
+            const uint4 val = *reinterpret_cast<const uint4*>(tile + sw_chunk(r, c8, 64));
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&val);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __bfloat1622float2(h2[e]);
+              ss = fmaf(f.x, f.x, ss);
+              ss = fmaf(f.y, f.y, ss);
+            }
+          }
+        }
+        const float rn = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+        if (tid < 64) rk[r] = rn;
+        else rq[r] = rn;
+      }
+      // KK^T and QK^T (M = 64) -> the FP32 table: QK^T on and below the diagonal, KK^T above
+      handoff();
+      if (tid == 0) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_ss(tb + GT_A0, desc_k(s_k, 64, ks), desc_k(s_k, 64, ks), idesc(64, 64, 0, 0), ks > 0);
+          mma_ss(tb + GT_A1, desc_k(s_q, 64, ks), desc_k(s_k, 64, ks), idesc(64, 64, 0, 0), ks > 0);
+        }
+        mma_commit(&mma_bar);
+      }
+      if (!(ok = mma_sync_wait())) break;
+      float kk[GK_CW], qk[GK_CW];
+      tld2(GT_A0, kk, GT_A1, qk);
+      if (lane < 16) {
+#pragma unroll
+        for (int e = 0; e < GK_CW; e += 4) {
+          const int cc = cb0 + e;
+          float4 v;
+          v.x = cc + 0 <= r64 ? qk[e + 0] : kk[e + 0];
+          v.y = cc + 1 <= r64 ? qk[e + 1] : kk[e + 1];
+          v.z = cc + 2 <= r64 ? qk[e + 2] : kk[e + 2];
+          v.w = cc + 3 <= r64 ? qk[e + 3] : kk[e + 3];
+          *reinterpret_cast<float4*>(KQ + r64 * GK_KQLD + cc) = v;
+        }
+      }
+      tc_fence_before();   // the TMEM reads above precede the first MA
     }
     if (warp == 0) {  // gates of this value head
       const int r0 = 2 * lane, r1 = r0 + 1;
@@ -585,14 +648,14 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       }
       const float ex = s - (g0 + g1);
       // cumulative gate in log2 units (the prep kernel's convention)
-      Gs[r0] = (ex + g0) * kLog2e;
-      Gs[r1] = (ex + g0 + g1) * kLog2e;
+      const float G0v = (ex + g0) * kLog2e, G1v = (ex + g0 + g1) * kLog2e;
+      Gs[r0] = G0v;
+      Gs[r1] = G1v;
       bs[r0] = b0;
       bs[r1] = b1;
-      gs[r0] = r0 < L ? exp2f(Gs[r0]) : 0.f;
-      gs[r1] = r1 < L ? exp2f(Gs[r1]) : 0.f;
+      gs[r0] = r0 < L ? exp2f(G0v) : 0.f;
+      gs[r1] = r1 < L ? exp2f(G1v) : 0.f;
       // per-token gate factors: e^{G_r - G_j} = eGr[r] eGi[j] when the chunk's range is FP32-safe
-      const float G0v = Gs[r0], G1v = Gs[r1];
       const float Gfirst = __shfl_sync(0xffffffffu, G0v, 0);
       const float Glast = __shfl_sync(0xffffffffu, G1v, 31);
       const bool sf = (Gfirst - Glast) < 100.f;
@@ -604,152 +667,65 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       decs[r1] = r1 < L ? exp2f(Glast - G1v) : 0.f;
       if (lane == 0) gsafe = sf;
     }
-    __syncthreads();
+    // this value head's tiles
+    ok = __syncthreads_and(mbar_wait(&bar_vn, vph, a.err) & mbar_wait(&bar_sv, vph, a.err) &
+                           mbar_wait(&bar_do, vph, a.err) & mbar_wait(&bar_dt, vph, a.err));
+    if (!ok) break;
     const bool sfac = gsafe;
     auto gamma_rc = [&](int r, int cc) -> float {   // e^{G_r - G_c}, c <= r
       return sfac ? eGr[r] * eGi[cc] : exp2f(Gs[r] - Gs[cc]);
     };
-    if (h == 0) {  // KK^T and QK^T (M = 64), kept in TMEM for the whole group
-      handoff();
-      if (tid == 0) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          mma_ss(tb + GT_KK, desc_k(s_k, 64, ks), desc_k(s_k, 64, ks), idesc(64, 64, 0, 0), ks > 0);
-          mma_ss(tb + GT_QK, desc_k(s_q, 64, ks), desc_k(s_k, 64, ks), idesc(64, 64, 0, 0), ks > 0);
-        }
-        mma_commit(&mma_bar);
-      }
-      if (!(ok = mma_sync_wait())) break;
-    }
-    ok = __syncthreads_and(mbar_wait(&bar_t, vph, a.err));
-    if (!ok) break;
-    // ---- T' = T diag(beta gamma rk), T'' = T diag(beta), Aqk tile
-    for (int idx = tid; idx < 64 * 8; idx += GK_THREADS) {
-      const int r = idx >> 3, c8 = idx & 7;
-      const uint4 raw = *reinterpret_cast<const uint4*>(sm + GK_T + sw_chunk(r, c8, 64));
-      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-      float tp[8], tpp[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(h2[e]);
-        const int c0 = c8 * 8 + 2 * e;
-        tpp[2 * e] = f.x * bs[c0];
-        tpp[2 * e + 1] = f.y * bs[c0 + 1];
-        tp[2 * e] = tpp[2 * e] * gs[c0] * rk[c0];
-        tp[2 * e + 1] = tpp[2 * e + 1] * gs[c0 + 1] * rk[c0 + 1];
-      }
-      store_chunk8(sm + GK_TP, r, c8, 64, tp);
-      store_chunk8(sm + GK_TPP, r, c8, 64, tpp);
-    }
-    {
-      float qk[GK_CW];
-      tld(GT_QK, qk);
-      if (lane < 16) {
-        const int r = r64;
-        const float qr = rq[r];
-#pragma unroll
-        for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
-          float x[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int cc = cb0 + q4 * 8 + e;
-            x[e] = (cc <= r && r < L) ? qr * rk[cc] * gamma_rc(r, cc) * qk[q4 * 8 + e] : 0.f;
-          }
-          store_chunk8(sm + GK_AQ, r, (cb0 >> 3) + q4, 64, x);
-        }
-      }
-    }
-    ok = __syncthreads_and(mbar_wait(&bar_vd, vph, a.err) & mbar_wait(&bar_ds, vph, a.err));
-    if (!ok) break;
-    if (L < CH) {  // zero rows past the document end in the V, dO tiles (Q, K at the first head)
-      const int ntile = h == 0 ? 4 : 2;
-      for (int idx = tid; idx < (CH - L) * 16 * ntile; idx += GK_THREADS) {
-        const int t = idx / (16 * ntile), rem = idx % (16 * ntile), tile = rem / 16, c8 = rem % 16;
-        const int off = tile == 0 ? GK_V : tile == 1 ? GK_DO : tile == 2 ? GK_Q : GK_K;
-        *reinterpret_cast<uint4*>(sm + off + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
     const float gL = scal[128];
-    handoff();
-    // ---- M1: W^T, U^T, dO^T Aqk, dS'^T K^T
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        mma_ss(tb + GT_S0, desc_mn(s_k, 64, ks), desc_k(s_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
-        mma_ss(tb + GT_S1, desc_mn(s_v, 64, ks), desc_k(s_tpp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
-        mma_ss(tb + GT_S2, desc_mn(s_do, 64, ks), desc_mn(s_aq, 64, ks), idesc(128, 64, 1, 1), ks > 0);
-      }
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        mma_ss(tb + GT_S3, desc_k(s_ds, 128, ks), desc_k(s_k, 64, ks), idesc(128, 64, 0, 0), ks > 0);
-      mma_commit(&mma_bar);
-    }
-    if (!(ok = mma_sync_wait())) break;
-    {  // H1: -W^T -> WD; dV_new^T = P dO^T Aqk + kd (dS'^T K^T) -> dV
-      float w[GK_CW], x[GK_CW], y[GK_CW];
-      {
-        uint32_t r0[16], r1[16], r2[16];
-        tmem_ld16_async(taddr(tb, w4 * 32, GT_S0 + cb0), r0);
-        tmem_ld16_async(taddr(tb, w4 * 32, GT_S2 + cb0), r1);
-        tmem_ld16_async(taddr(tb, w4 * 32, GT_S3 + cb0), r2);
-        tmem_wait_ld();
-        as_float16(r0, w);
-        as_float16(r1, x);
-        as_float16(r2, y);
-      }
-      const float* kd = scal + 64;
-#pragma unroll
-      for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
-        float nw[8], dvn[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int jj = q4 * 8 + e;
-          nw[e] = -w[jj];
-          dvn[e] = fmaf(a.scale, x[jj], kd[cb0 + jj] * y[jj]);
-        }
-        store_chunk8(sm + GK_WD, row, (cb0 >> 3) + q4, 128, nw);
-        store_chunk8(sm + GK_DV, row, (cb0 >> 3) + q4, 128, dvn);
+    if (L < CH) {  // zero rows past the document end in the V, dO tiles
+      for (int idx = tid; idx < (CH - L) * 32; idx += GK_THREADS) {
+        const int t = idx >> 5, tile = (idx >> 4) & 1, c8 = idx & 15;
+        *reinterpret_cast<uint4*>(sm + (tile ? GK_DO : GK_V) + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    ok = __syncthreads_and(mbar_wait(&bar_s, vph, a.err));
-    if (!ok) break;
     handoff();
-    // ---- M2: V_new^T, S dV_new^T, dV_new^T T, S dO^T
+    // ---- MA
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        mma_ss(tb + GT_S1, desc_k(s_s, 128, ks), desc_mn(s_wd, 128, ks), idesc(128, 64, 0, 1), 1u);
-        mma_ss(tb + GT_S0, desc_mn(s_s, 128, ks), desc_mn(s_dv, 128, ks), idesc(128, 64, 1, 1), ks > 0);
-        mma_ss(tb + GT_S3, desc_mn(s_s, 128, ks), desc_k(s_do, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+        mma_ss(tb + GT_A4, desc_k(s_do, 64, ks), desc_mn(s_vn, 128, ks), idesc(64, 64, 0, 1), ks > 0);
+        mma_ss(tb + GT_A0, desc_mn(s_s, 128, ks), desc_mn(s_dv, 128, ks), idesc(128, 64, 1, 1), ks > 0);
+        mma_ss(tb + GT_A1, desc_mn(s_s, 128, ks), desc_k(s_do, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+        mma_ss(tb + GT_A3, desc_mn(s_ds, 128, ks), desc_mn(s_vn, 128, ks), idesc(128, 64, 1, 1), ks > 0);
+        mma_ss(tb + GT_A5, desc_mn(s_dv, 128, ks), desc_k(s_v, 64, ks), idesc(64, 64, 1, 0), ks > 0);
       }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tb + GT_S2, desc_k(s_dv, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
+        mma_ss(tb + GT_A2, desc_k(s_dv, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
       mma_commit(&mma_bar);
     }
     if (!(ok = mma_sync_wait())) break;
-    {  // H2
-      float x[GK_CW], x2[GK_CW], cb[GK_CW], cg[GK_CW];
-      tld2(GT_S1, x, GT_S0, x2);   // V_new^T row (dv); S dV_new^T row (dk)
-      {
+    if (tid == 0 && h + 1 < a.G) issue_vn(hv + 1);   // V_new^T is dead from here on
+    // HA: dW^T = -(S dV_new^T) -> shared for MB; X^T kept for the side work
+    float x[GK_CW];
+    {
+      float w[GK_CW];
+      tld2(GT_A0, w, GT_A2, x);
+#pragma unroll
+      for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
         float t8[8];
 #pragma unroll
-        for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) t8[e] = x[q4 * 8 + e];
-          store_chunk8(sm + GK_VN, row, (cb0 >> 3) + q4, 128, t8);
-        }
+        for (int e = 0; e < 8; ++e) t8[e] = -w[q4 * 8 + e];
+        store_chunk8(sm + GK_WD, row, (cb0 >> 3) + q4, 128, t8);
       }
-      {  // dW^T = -(S dV_new^T)
-        float t8[8];
+    }
+    handoff();
+    // ---- MB: dW K^T (M = 64), Y^T = dW^T T
+    if (tid == 0) {
 #pragma unroll
-        for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ss(tb + GT_A0, desc_mn(s_wd, 128, ks), desc_k(s_k, 64, ks), idesc(64, 64, 1, 0), ks > 0);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) t8[e] = -x2[q4 * 8 + e];
-          store_chunk8(sm + GK_WD, row, (cb0 >> 3) + q4, 128, t8);
-        }
-      }
-      tld2(GT_S2, x, GT_S3, x2);   // X^T = dV_new^T T (row = dv index); S dO^T (row = dk index)
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ss(tb + GT_A2, desc_k(s_wd, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
+      mma_commit(&mma_bar);
+    }
+    {  // HA side work: dv, the column-scaled dq / dk terms, partial sums for dbeta / dg
+      float cb[GK_CW];
       __nv_bfloat16* dvp = a.dv + ((size_t)tok0 * a.HV + hv) * D + row;
 #pragma unroll
       for (int e = 0; e < GK_CW; ++e) {
@@ -757,21 +733,28 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         if (cc < L) dvp[(size_t)cc * a.HV * D] = __float2bfloat16_rn(bs[cc] * x[e]);
         cb[e] = ld_bf16(sm + GK_V, cc, row, 64) * x[e];
       }
+      const float sb = colsum16(cb, lane);
+      float y[GK_CW], z[GK_CW];
+      tld2(GT_A1, y, GT_A3, z);   // S dO^T (row = dk index), dKd^T (row = dk index)
 #pragma unroll
       for (int e = 0; e < GK_CW; ++e) {
         const int cc = cb0 + e;
         const float pg = a.scale * gs[cc];
-        dq_acc[e] = fmaf(pg, x2[e], dq_acc[e]);
-        cg[e] = pg * rq[cc] * ld_bf16(sm + GK_Q, cc, row, 64) * x2[e];
+        dq_acc[e] = fmaf(pg, y[e], dq_acc[e]);
+        dk_acc[e] = fmaf(decs[cc], z[e], dk_acc[e]);
+        y[e] = pg * rq[cc] * ld_bf16(sm + GK_Q, cc, row, 64) * y[e];
+        z[e] = rk[cc] * ld_bf16(sm + GK_K, cc, row, 64) * z[e];
       }
-      // <S, dS'> over this thread's half of the row
+      const float sg = colsum16(y, lane);
+      const float sz = colsum16(z, lane);
+      // <S, dS'> over this thread's quarter of the row
       float sd = 0.f;
 #pragma unroll
       for (int c8 = wg * (16 / GK_NWG); c8 < (wg + 1) * (16 / GK_NWG); ++c8) {   // 16-byte chunks in swizzle order
         const uint4 sa = *reinterpret_cast<const uint4*>(sm + GK_S + sw_chunk(row, c8, 128));
-        const uint4 sb = *reinterpret_cast<const uint4*>(sm + GK_DS + sw_chunk(row, c8, 128));
+        const uint4 sb4 = *reinterpret_cast<const uint4*>(sm + GK_DS + sw_chunk(row, c8, 128));
         const __nv_bfloat162* ha = reinterpret_cast<const __nv_bfloat162*>(&sa);
-        const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&sb);
+        const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&sb4);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 fa = __bfloat1622float2(ha[e]), fb = __bfloat1622float2(hb[e]);
@@ -782,193 +765,157 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
       if (lane == 0) sdot[warp] = sd;
-      const float sb = colsum16(cb, lane);
-      const float sg = colsum16(cg, lane);
       if (lane < GK_CW) {
-        part[(0 * 4 + w4) * 64 + cb0 + lane] = sb;
-        part[(1 * 4 + w4) * 64 + cb0 + lane] = sg;
+        part[0][w4][cb0 + lane] = sb;
+        part[1][w4][cb0 + lane] = sg;
+        part[2][w4][cb0 + lane] = sz;
       }
-    }
-    handoff();
-    // ---- M3: dKd^T, dO V_new^T, Y^T = dW^T T, dV_new V^T, dW K^T
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        mma_ss(tb + GT_S4, desc_mn(s_ds, 128, ks), desc_mn(s_vn, 128, ks), idesc(128, 64, 1, 1), ks > 0);
-        mma_ss(tb + GT_S5, desc_k(s_do, 64, ks), desc_mn(s_vn, 128, ks), idesc(64, 64, 0, 1), ks > 0);
-        mma_ss(tb + GT_S2, desc_mn(s_dv, 128, ks), desc_k(s_v, 64, ks), idesc(64, 64, 1, 0), ks > 0);
-        mma_ss(tb + GT_S3, desc_mn(s_wd, 128, ks), desc_k(s_k, 64, ks), idesc(64, 64, 1, 0), ks > 0);
-      }
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tb + GT_S0, desc_k(s_wd, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
-      mma_commit(&mma_bar);
     }
     if (!(ok = mma_sync_wait())) break;
-    if (tid == 0 && h + 1 < a.G) {   // V, dO, dS' and the scalars are dead from here on
-      issue_vd(hv + 1);
-      issue_ds(hv + 1);
-    }
-    {  // H3
-      float x[GK_CW], cz[GK_CW], cy[GK_CW], yv[GK_CW];
-      tld2(GT_S4, x, GT_S0, yv);   // dKd^T and Y^T = dW^T T, rows = dk index
+    if (tid == 0 && h + 1 < a.G) issue_sv(hv + 1);   // S, dS', V, scalars are dead from here on
+    {  // HB: the token-pair terms -> H1, H2, dT for M4; dAqk . Aqk -> row / column sums of C
+      float daq[GK_CW], t1[GK_CW], t2[GK_CW];
+      tld(GT_A4, daq);
+      tld2(GT_A5, t1, GT_A0, t2);
+      float cm[GK_CW], rc = 0.f;
+      const int r = r64;
+      const bool rv = lane < 16;
 #pragma unroll
-      for (int e = 0; e < GK_CW; ++e) {
-        const int cc = cb0 + e;
-        const float dec = decs[cc];
-        dk_acc[e] = fmaf(dec, x[e], dk_acc[e]);
-        cz[e] = rk[cc] * ld_bf16(sm + GK_K, cc, row, 64) * x[e];
-      }
+      for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
+        float h1[8], h2[8], dt[8];
+        const float4 qa = *reinterpret_cast<const float4*>(KQ + (rv ? r : 0) * GK_KQLD + cb0 + q4 * 8);
+        const float4 qb = *reinterpret_cast<const float4*>(KQ + (rv ? r : 0) * GK_KQLD + cb0 + q4 * 8 + 4);
+        const float qk[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
-      for (int e = 0; e < GK_CW; ++e) {
-        const int cc = cb0 + e;
-        dk_acc[e] = fmaf(bs[cc] * gs[cc], yv[e], dk_acc[e]);
-        cy[e] = rk[cc] * ld_bf16(sm + GK_K, cc, row, 64) * yv[e];
-      }
-      const float sz = colsum16(cz, lane);
-      const float sy = colsum16(cy, lane);
-      if (lane < GK_CW) {
-        part[(2 * 4 + w4) * 64 + cb0 + lane] = sz;
-        part[(3 * 4 + w4) * 64 + cb0 + lane] = sy;
-      }
-      // M = 64 results: rows r64 (lanes < 16)
-      float daq[GK_CW], qk[GK_CW], t1[GK_CW], t2[GK_CW];
-      tld2(GT_S5, daq, GT_QK, qk);
-      tld2(GT_S2, t1, GT_S3, t2);
-      if (lane < 16) {
-        const int r = r64;
-#pragma unroll
-        for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
-          float h1[8], h2[8], dt[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int jj = q4 * 8 + e, cc = cb0 + jj;
-            const bool live = cc <= r && r < L;
-            const float gam = live ? gamma_rc(r, cc) : 0.f;
-            const float dA = live ? a.scale * daq[jj] : 0.f;
-            Cm[r * GK_CLD + cc] = dA * gam * rq[r] * rk[cc] * qk[jj];
-            h1[e] = rk[cc] * gam * dA;
-            h2[e] = rq[r] * gam * dA;
-            dt[e] = bs[cc] * fmaf(gs[cc] * rk[cc], t2[jj], t1[jj]);
-          }
+        for (int e = 0; e < 8; ++e) {
+          const int jj = q4 * 8 + e, cc = cb0 + jj;
+          const bool live = rv && cc <= r && r < L;
+          const float gam = live ? gamma_rc(r, cc) : 0.f;
+          const float dA = live ? a.scale * daq[jj] : 0.f;
+          cm[jj] = dA * gam * rq[r & 63] * rk[cc] * qk[e];
+          rc += cm[jj];
+          h1[e] = rk[cc] * gam * dA;
+          h2[e] = rq[r & 63] * gam * dA;
+          dt[e] = bs[cc] * fmaf(gs[cc] * rk[cc], t2[jj], t1[jj]);
+        }
+        if (rv) {
           store_chunk8(sm + GK_H1, r, (cb0 >> 3) + q4, 64, h1);
           store_chunk8(sm + GK_H2, r, (cb0 >> 3) + q4, 64, h2);
           store_chunk8(sm + GK_DT, r, (cb0 >> 3) + q4, 64, dt);
         }
       }
+      if (rv) rowC[wg][r] = rc;
+      const float cs = colsum16(cm, lane);
+      if (lane < GK_CW) colC[0][w4][cb0 + lane] = cs;
     }
     handoff();
-    // ---- M4: R1 = dT T^T, K^T H1 (-> dq^), Q^T H2 (-> dk^)
+    // ---- M4: R1 = dT T^T (M = 64), K^T H1 (+= dq^T), Q^T H2 (+= dk^T)
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        mma_ss(tb + GT_S1, desc_k(s_dt, 64, ks), desc_k(s_t, 64, ks), idesc(64, 64, 0, 0), ks > 0);
-        mma_ss(tb + GT_S4, desc_mn(s_k, 64, ks), desc_k(s_h1, 64, ks), idesc(128, 64, 1, 0), ks > 0);
-        mma_ss(tb + GT_S5, desc_mn(s_q, 64, ks), desc_mn(s_h2, 64, ks), idesc(128, 64, 1, 1), ks > 0);
+        mma_ss(tb + GT_A5, desc_k(s_dt, 64, ks), desc_k(s_t, 64, ks), idesc(64, 64, 0, 0), ks > 0);
+        mma_ss(tb + GT_DQ, desc_mn(s_k, 64, ks), desc_k(s_h1, 64, ks), idesc(128, 64, 1, 0), (h > 0 || ks > 0));
+        mma_ss(tb + GT_DK, desc_mn(s_q, 64, ks), desc_mn(s_h2, 64, ks), idesc(128, 64, 1, 1), (h > 0 || ks > 0));
       }
       mma_commit(&mma_bar);
     }
-    if (!(ok = mma_sync_wait())) break;
-    {  // H4
-      float x[GK_CW], x2[GK_CW];
-      tld2(GT_S4, x, GT_S5, x2);
+    {  // HB side work: Y^T = dW^T T (rows = dk index) -> dk, partial sums
+      float yv[GK_CW];
+      tld(GT_A2, yv);
 #pragma unroll
       for (int e = 0; e < GK_CW; ++e) {
-        dq_acc[e] += x[e];
-        dk_acc[e] += x2[e];
+        const int cc = cb0 + e;
+        dk_acc[e] = fmaf(bs[cc] * gs[cc], yv[e], dk_acc[e]);
+        yv[e] *= rk[cc] * ld_bf16(sm + GK_K, cc, row, 64);
       }
-      tld(GT_S1, x);
+      const float sy = colsum16(yv, lane);
+      if (lane < GK_CW) part[3][w4][cb0 + lane] = sy;
+    }
+    if (!(ok = mma_sync_wait())) break;
+    if (tid == 0 && h + 1 < a.G) issue_do(hv + 1);   // the dO region (H1, H2) is dead
+    {  // H4: R1 -> shared for M5
+      float r1v[GK_CW];
+      tld(GT_A5, r1v);
       if (lane < 16) {
 #pragma unroll
-        for (int q4 = 0; q4 < GK_CW / 8; ++q4) store_chunk8(sm + GK_R1, r64, (cb0 >> 3) + q4, 64, x + q4 * 8);
+        for (int q4 = 0; q4 < GK_CW / 8; ++q4) store_chunk8(sm + GK_R1, r64, (cb0 >> 3) + q4, 64, r1v + q4 * 8);
       }
     }
     handoff();
-    // ---- M5: T^T R1 (= -dA)
+    // ---- M5: T^T R1 (= -dA, M = 64)
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tb + GT_S0, desc_mn(s_t, 64, ks), desc_mn(s_r1, 64, ks), idesc(64, 64, 1, 1), ks > 0);
+        mma_ss(tb + GT_A0, desc_mn(s_t, 64, ks), desc_mn(s_r1, 64, ks), idesc(64, 64, 1, 1), ks > 0);
       mma_commit(&mma_bar);
     }
     if (!(ok = mma_sync_wait())) break;
-    if (tid == 0 && h + 1 < a.G) issue_t(hv + 1);    // T is dead from here on
-    {  // H5: dA rows -> dbeta row terms, C, F1, F2
-      float x[GK_CW], kk[GK_CW];
-      tld2(GT_S0, x, GT_KK, kk);
-      if (lane < 16) {
-        const int r = r64;
-        const float br = bs[r];
-        float rb = 0.f;
+    if (tid == 0 && h + 1 < a.G) issue_dt(hv + 1);   // dV_new^T (dT, R1) and T are dead
+    {  // H5: dA rows -> F1, F2 for M6; dbeta row terms; dA . A -> column sums of C
+      float xa[GK_CW];
+      tld(GT_A0, xa);
+      const int r = r64;
+      const bool rv = lane < 16;
+      const float br = bs[r & 63];
+      float rb = 0.f, cm[GK_CW];
 #pragma unroll
-        for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
-          float f1[8], f2[8];
+      for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
+        float f1[8], f2[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int jj = q4 * 8 + e, cc = cb0 + jj;
-            const bool live = cc < r && r < L;
-            const float gam = live ? gamma_rc(r, cc) : 0.f;
-            const float dA = live ? -x[jj] : 0.f;
-            const float base = dA * gam * rk[r] * rk[cc] * kk[jj];   // dA . (A / beta_r)
-            rb += base;
-            Cm[r * GK_CLD + cc] += br * base;
-            const float E = dA * br * gam;
-            f1[e] = rk[cc] * E;
-            f2[e] = rk[r] * E;
-          }
+        for (int e = 0; e < 8; ++e) {
+          const int jj = q4 * 8 + e, cc = cb0 + jj;
+          const bool live = rv && cc < r && r < L;
+          const float gam = live ? gamma_rc(r, cc) : 0.f;
+          const float dA = live ? -xa[jj] : 0.f;
+          const float kk = live ? KQ[cc * GK_KQLD + r] : 0.f;   // KK^T[r][cc], kept above the diagonal
+          const float base = dA * gam * rk[r & 63] * rk[cc] * kk;   // dA . (A / beta_r)
+          rb += base;
+          cm[jj] = br * base;
+          const float E = dA * br * gam;
+          f1[e] = rk[cc] * E;
+          f2[e] = rk[r & 63] * E;
+        }
+        if (rv) {
           store_chunk8(sm + GK_F1, r, (cb0 >> 3) + q4, 64, f1);
           store_chunk8(sm + GK_F2, r, (cb0 >> 3) + q4, 64, f2);
         }
-        rowB[wg][r] = rb;
       }
+      if (rv) rowB[wg][r] = rb;
+      const float cs = colsum16(cm, lane);
+      if (lane < GK_CW) colC[1][w4][cb0 + lane] = cs;
     }
     handoff();
-    // ---- M6: K^T F1 + K^T F2 (-> dk^)
+    // ---- M6: K^T F1 + K^T F2 (+= dk^T).  Not waited for here: the next
+    // group's commit (or the final one) covers it.
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tb + GT_S2, desc_mn(s_k, 64, ks), desc_k(s_f1, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+        mma_ss(tb + GT_DK, desc_mn(s_k, 64, ks), desc_k(s_f1, 64, ks), idesc(128, 64, 1, 0), 1u);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tb + GT_S2, desc_mn(s_k, 64, ks), desc_mn(s_f2, 64, ks), idesc(128, 64, 1, 1), 1u);
-      mma_commit(&mma_bar);
+        mma_ss(tb + GT_DK, desc_mn(s_k, 64, ks), desc_mn(s_f2, 64, ks), idesc(128, 64, 1, 1), 1u);
     }
-    if (!(ok = mma_sync_wait())) break;
-    if (tid == 0 && h + 1 < a.G) issue_s(hv + 1);    // the S region (H1, H2, F1, F2) is dead
-    {
-      float x[GK_CW];
-      tld(GT_S2, x);
-#pragma unroll
-      for (int e = 0; e < GK_CW; ++e) dk_acc[e] += x[e];
-    }
-    __syncthreads();
     // ---- per-token totals: dbeta, dG -> dg
-    if (tid < 4 * CH) {   // row sum - column sum of C, 4 threads per token
-      const int r = tid >> 2, qq = tid & 3;
-      float d = 0.f;
-#pragma unroll
-      for (int cc = qq * 16; cc < qq * 16 + 16; ++cc) d += Cm[r * GK_CLD + cc] - Cm[cc * GK_CLD + r];
-      d += __shfl_xor_sync(0xffffffffu, d, 1);
-      d += __shfl_xor_sync(0xffffffffu, d, 2);
-      if (qq == 0) cdiff[r] = d;
-    }
-    __syncthreads();
     if (tid < CH) {
       const int r = tid;
-      float sb = 0.f, sg = 0.f, sz = 0.f, sy = 0.f;
+      float sb = 0.f, sg = 0.f, sz = 0.f, sy = 0.f, cr = 0.f, rbs = 0.f;
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
-        sb += part[(0 * 4 + w) * 64 + r];
-        sg += part[(1 * 4 + w) * 64 + r];
-        sz += part[(2 * 4 + w) * 64 + r];
-        sy += part[(3 * 4 + w) * 64 + r];
+        sb += part[0][w][r];
+        sg += part[1][w][r];
+        sz += part[2][w][r];
+        sy += part[3][w][r];
+        cr -= colC[0][w][r] + colC[1][w][r];
       }
-      const float dec = decs[r];
-      const float z = dec * sz;
-      float dG = sg - z + bs[r] * gs[r] * sy + cdiff[r];
-      float db = sb + gs[r] * sy;
 #pragma unroll
-      for (int w = 0; w < GK_NWG; ++w) db += rowB[w][r];
+      for (int w = 0; w < GK_NWG; ++w) {
+        cr += rowC[w][r];
+        rbs += rowB[w][r];
+      }
+      const float z = decs[r] * sz;
+      // row sums - column sums of C = dAqk . Aqk + dA . A (the second row sum is beta_r times rowB)
+      float dG = sg - z + bs[r] * gs[r] * sy + cr + bs[r] * rbs;
+      const float db = sb + gs[r] * sy + rbs;
       // chunk-end terms: gamma_L <S, dS'> and sum_c z_c
       float zs = z;
 #pragma unroll
@@ -987,8 +934,8 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       float acc = dG;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_down_sync(0xffffffffu, acc, o);
-        if (lane + o < 32) acc += y;
+        const float yy = __shfl_down_sync(0xffffffffu, acc, o);
+        if (lane + o < 32) acc += yy;
       }
       if (lane == 0) wtot[warp] = acc;
       named_bar(1, 64);
@@ -1001,8 +948,21 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     __syncthreads();
   }
 
-  // ---- L2-norm backward of the group sums, then dq, dk
+  // ---- the MMA-accumulated dq^T, dk^T; L2-norm backward of the group sums; dq, dk
   if (ok) {
+    if (tid == 0) mma_commit(&mma_bar);
+    ok = mma_sync_wait();
+  }
+  if (ok) {
+    {
+      float xq[GK_CW], xk[GK_CW];
+      tld2(GT_DQ, xq, GT_DK, xk);
+#pragma unroll
+      for (int e = 0; e < GK_CW; ++e) {
+        dq_acc[e] += xq[e];
+        dk_acc[e] += xk[e];
+      }
+    }
     float pq[GK_CW], pk[GK_CW];
 #pragma unroll
     for (int e = 0; e < GK_CW; ++e) {
@@ -1012,8 +972,8 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     }
     const float sq = colsum16(pq, lane), sk = colsum16(pk, lane);
     if (lane < GK_CW) {
-      part[(4 * 4 + w4) * 64 + cb0 + lane] = sq;
-      part[(5 * 4 + w4) * 64 + cb0 + lane] = sk;
+      part[4][w4][cb0 + lane] = sq;
+      part[5][w4][cb0 + lane] = sk;
     }
     __syncthreads();
     __nv_bfloat16* dqp = a.dq + ((size_t)tok0 * a.H + j) * D + row;
@@ -1027,8 +987,8 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         float xq = 0.f, xk = 0.f;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-          xq += part[(4 * 4 + w) * 64 + cc];
-          xk += part[(5 * 4 + w) * 64 + cc];
+          xq += part[4][w][cc];
+          xk += part[5][w][cc];
         }
         const float nq = rq[cc], nk = rk[cc];
         outq = nq * dq_acc[e] - ld_bf16(sm + GK_Q, cc, row, 64) * xq * nq * nq * nq;
@@ -1102,6 +1062,7 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
   ba.nsplit = P.nsplit;
   ba.scale = pr.scale;
   ba.dtape = ws + P.o_dtape;
+  ba.dvn = ws + P.o_dvn;
   ba.ds_init = reinterpret_cast<const float*>(ws + P.o_dsinit);
   ba.dbend = reinterpret_cast<float*>(ws + P.o_dbend);
   ba.err = reinterpret_cast<int*>(ws);
@@ -1139,6 +1100,8 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
   ga.cb = sv + P.s_cb;
   ga.tape = sv + P.s_tape;
   ga.dtape = ws + P.o_dtape;
+  ga.vn = sv + P.s_vn;
+  ga.dvn = ws + P.o_dvn;
   ga.chunk_tok0 = t.chunk_tok0;
   ga.chunk_len = t.chunk_len;
   ga.dq = static_cast<__nv_bfloat16*>(dq);

@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
   const int c0 = a.seg_c0[seg], nch = a.seg_c1[seg] - c0;
   const bool with_o = mode == 0 && a.o != nullptr;
   const bool with_u = mode != 2;
+  const bool with_vn = mode == 0 && a.vn != nullptr;   // V_new^T tiles for the backward
   const uint32_t tx_bytes = mode == 0 ? (with_o ? 74752u : 50176u) : (mode == 1 ? 50176u : 25600u);
   const uint32_t cb_bytes = mode == 2 ? 8192u : (with_o ? 24576u : 16384u);
 
@@ -285,6 +286,11 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
         }
         tmem_st8(taddr(tb, warp * 32, TM_AVS + q * 8), ps);
         if (with_o) tmem_st8(taddr(tb, warp * 32, TM_AVN + q * 8), pn);
+        if (with_vn) {   // staged in the -W^T tile, which MMA1 has finished reading
+          uint8_t* vt = sm + SC_W;
+          *reinterpret_cast<uint4*>(vt + sw_chunk(tid, 2 * q, 128)) = make_uint4(pn[0], pn[1], pn[2], pn[3]);
+          *reinterpret_cast<uint4*>(vt + sw_chunk(tid, 2 * q + 1, 128)) = make_uint4(pn[4], pn[5], pn[6], pn[7]);
+        }
       }
       if (with_o) {  // this chunk's output scales outlive its stage buffer
         float* sd = side + (n & 1) * 68;
@@ -293,10 +299,15 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
       }
       tmem_wait_st();
     }
+    if (with_vn) fence_async_smem();
     tc_fence_before();
     __syncthreads();
     // ---- MMA2: dS^T = (V_new^T diag(kd)) K; O2 = V_new^T Aqk^T; O1 = S^T Q^T
     if (warp == 0) {
+      if (with_vn && tid == 0) {
+        bulk_store(a.vn + ((size_t)(c0 + n) * a.HV + hv) * VN_BYTES, sm + SC_W, VN_BYTES);
+        bulk_commit();
+      }
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
@@ -310,7 +321,7 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
           mma_ss_w(tb + TM_O1, desc_k(sm_s, 128, ks), desc_k(a_q, 64, ks), idesc(128, 64, 0, 0), ks > 0);
       }
       mma_commit_w(&bar_m2);
-      if (tid == 0) bulk_wait_read();   // earlier tape / output stores have read the tiles rewritten below
+      if (tid == 0) bulk_wait_read();   // earlier tape / output / V_new stores have read the tiles rewritten below
     }
     // ---- in its shadow: the -W^T tile of chunk n + 1
     if (next) {

@@ -26,6 +26,8 @@ constexpr int TILE64_BYTES = 8192;
 constexpr int STATE_BYTES = 32768;
 constexpr int STATE_F32 = 128 * 128;   // an FP32 S^T, row-major [dv][dk]
 constexpr int SAVED_HEADER = 4096;
+// one chunk's V_new^T (forward) or dV_new^T (adjoint walk): BF16 SwTile(128 x 64)
+constexpr int VN_BYTES = 16384;
 
 // saved-set header (first bytes of `saved`)
 struct SavedHeader {
@@ -36,7 +38,7 @@ struct SavedHeader {
   uint32_t scale_bits, cu_hash;
 };
 constexpr uint32_t SAVED_MAGIC = 0x4744'4e31u;   // "GDN1"
-constexpr uint32_t SAVED_VERSION = 2;
+constexpr uint32_t SAVED_VERSION = 3;
 
 // ---- device tables built by the table kernel ----
 struct Tables {
@@ -91,6 +93,7 @@ struct ScanArgs {
   int H, HV, G, nsplit, walk;   // walk = 0: full walks over all segments; 1: B and M walks
   float scale;
   uint8_t* tape;              // [NC][HV][STATE_BYTES] or null
+  uint8_t* vn;                // [NC][HV][VN_BYTES] V_new^T tiles, or null
   __nv_bfloat16* o;           // [T][HV][128] or null
   const float* s_init;        // [nsplit][HV][STATE_F32]: start of the segment after split segment i
   float* bend;                // [nsplit][HV][STATE_F32]
@@ -116,10 +119,10 @@ struct Plan {
   // workspace offsets (bytes)
   size_t o_tables[14];
   size_t o_cb, o_bend, o_sinit, o_mend_ws;
-  size_t o_dtape, o_dbend, o_dsinit;   // backward
+  size_t o_dtape, o_dvn, o_dbend, o_dsinit;   // backward
   size_t ws_fwd, ws_bwd;
   // saved offsets
-  size_t s_tape, s_mseg, s_cb, saved_bytes;
+  size_t s_tape, s_mseg, s_cb, s_vn, saved_bytes;
 };
 
 inline Tables tables_at(const Plan& P, uint8_t* ws) {

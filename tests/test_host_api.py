@@ -36,14 +36,14 @@ def test_status_strings():
 def test_saved_and_workspace_bytes():
     p = gdn.problem(320, 2, 2, 4)
     saved, ws = gdn.gdn_saved_bytes(p, [0, 128, 320])
-    # header + 5 chunks x 4 v-heads x (32 KiB BF16 state + 33 KiB UT block), no segment split
-    assert saved == 4096 + 5 * 4 * 32768 + 5 * 4 * 33792
+    # header + 5 chunks x 4 v-heads x (32 KiB BF16 state + 33 KiB UT block + 16 KiB V_new^T), no split
+    assert saved == 4096 + 5 * 4 * 32768 + 5 * 4 * 33792 + 5 * 4 * 16384
     assert ws > 5 * 4 * 33792
     p = gdn.problem(64 * 40, 1, 1, 2, segments=4)
     saved, _ = gdn.gdn_saved_bytes(p, [0, 64 * 40])
     assert gdn.gdn_plan_segment_chunks(p, [0, 64 * 40]) == 10
-    # 4 segments -> 3 transfer operators per v-head in FP32, then the UT blocks
-    assert saved == 4096 + 40 * 2 * 32768 + 3 * 2 * 128 * 128 * 4 + 40 * 2 * 33792
+    # 4 segments -> 3 transfer operators per v-head in FP32, then the UT blocks and V_new^T tiles
+    assert saved == 4096 + 40 * 2 * 32768 + 3 * 2 * 128 * 128 * 4 + 40 * 2 * 33792 + 40 * 2 * 16384
 
 
 @pytest.mark.parametrize("cu,T,N,H,HV,dk,code", [
