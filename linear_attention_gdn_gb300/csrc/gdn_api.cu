@@ -101,6 +101,7 @@ static gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
   P->H = p->H;
   P->HV = p->HV;
   P->G = p->HV / p->H;
+  P->sms = sm_count();
   plan_segments(p, cu, &P->seg_len, &P->split_min, &P->max_doc_chunks);
   int NC = 0, NSEG = 0, nsplit = 0, nsdoc = 0;
   uint32_t h = 2166136261u;

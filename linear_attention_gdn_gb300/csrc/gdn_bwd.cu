@@ -55,7 +55,7 @@ struct BScanArgs {
 };
 
 struct GradArgs {
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk;
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const float* g;
@@ -72,7 +72,7 @@ struct GradArgs {
   __nv_bfloat16* dv;
   float* dg;
   float* dbeta;
-  int H, HV, G, l2norm;
+  int NC, H, HV, G, l2norm;
   float scale;
   int* err;
 };
@@ -437,10 +437,11 @@ __device__ __forceinline__ void store_chunk8(uint8_t* tile, int r, int c8, int R
   *reinterpret_cast<uint4*>(tile + sw_chunk(r, c8, R)) = w;
 }
 
-// One CTA per (chunk, q/k head); its value heads one after another.  Every
-// operand of the first MMA group of a value head comes from memory: S and
-// dS' from the two tapes, V_new^T from the forward, dV_new^T from the
-// adjoint walk, V, dO, and T from the saved UT block.  Per value head:
+// Persistent: one CTA per SM walks (chunk, q/k head) items; within an item
+// its value heads one after another.  Every operand of the first MMA group of
+// a value head comes from memory: S and dS' from the two tapes, V_new^T from
+// the forward, dV_new^T from the adjoint walk, V, dO, and T from the saved UT
+// block.  Per value head:
 //   MA  S dV_new^T (= -dW^T), S dO^T, X^T = dV_new^T T, dKd^T = dS' V_new^T,
 //       dO V_new^T (-> dAqk), dV_new V^T                       (44 MMAs)
 //   MB  dW K^T, Y^T = dW^T T
@@ -449,27 +450,31 @@ __device__ __forceinline__ void store_chunk8(uint8_t* tile, int r, int c8, int R
 //   M6  K^T F1 + K^T F2 (+= dk^T)
 // Each CUDA-core pass first writes what the next group reads, hands off, and
 // does its side work (dv, column-scaled dq / dk terms, per-token partial
-// sums) while that group runs.  The next value head's loads are requested as
-// soon as the buffers they land in are dead.
+// sums) while that group runs.  The next value head's tiles (the next item's
+// first value head after the last one) are requested as soon as the buffers
+// they land in are dead, and its MA is issued right after M6, so that it runs
+// under the per-token totals (warps 2-3) and the next gate scan (warp 4).
 __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_constant__ GradArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t bar_qk, bar_vn, bar_sv, bar_do, bar_dt, mma_bar;
-  __shared__ float gall[8][CH], ball[8][CH];   // the group's gates, prefetched (first 8 value heads)
+  __shared__ uint64_t bar_qk, bar_vn, bar_sv, bar_do, bar_dt, bar_ma, mma_bar;
   __shared__ uint32_t tslot;
-  __shared__ float rq[CH], rk[CH], Gs[CH], bs[CH], gs[CH], decs[CH], eGr[CH], eGi[CH];
-  __shared__ int gsafe;
+  __shared__ float rq[CH], rk[CH];
+  // gates of the current and the next value head (double-buffered)
+  __shared__ float Gs[2][CH], bs[2][CH], gs[2][CH], decs[2][CH], eGr[2][CH], eGi[2][CH];
+  __shared__ int gsafe[2];
   __shared__ float part[6][4][CH];             // per-token partial sums, one row per 32-lane quarter
   __shared__ float colC[2][4][CH];             // column sums of C (dAqk . Aqk, dA . A) per quarter
   __shared__ float rowC[GK_NWG][CH], rowB[GK_NWG][CH], sdot[GK_THREADS / 32];
-  const int c = blockIdx.x, j = blockIdx.y;
+  __shared__ float zpart[2], wtot[2];
+  __shared__ float lq[CH], lk[CH];             // per-token L2-norm backward factors
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wg = tid >> 7, w4 = warp & 3;
   const int row = w4 * 32 + lane;          // TMEM lane / M = 128 row of this thread
   const int cb0 = wg * GK_CW;              // first of this thread's GK_CW columns
   const int r64 = w4 * 16 + lane;          // M = 64 row (valid for lane < 16)
-  if (*(volatile int*)a.err) return;
-  const int tok0 = a.chunk_tok0[c], L = a.chunk_len[c];
+  const int n_items = a.NC * a.H;
+  if (*(volatile int*)a.err || (int)blockIdx.x >= n_items) return;
 
   if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {
@@ -478,54 +483,83 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     mbar_init(&bar_sv, 1);
     mbar_init(&bar_do, 1);
     mbar_init(&bar_dt, 1);
+    mbar_init(&bar_ma, 1);
     mbar_init(&mma_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   __syncthreads();
   const uint32_t tb = tslot;
-  const size_t tile_idx0 = (size_t)c * a.HV;
-  auto issue_vn = [&](int hv) {   // V_new^T
-    mbar_expect_tx(&bar_vn, (uint32_t)VN_BYTES);
-    bulk_load(sm + GK_VN, a.vn + (tile_idx0 + hv) * VN_BYTES, VN_BYTES, &bar_vn);
-  };
-  auto issue_sv = [&](int hv) {   // S, dS', V and the chunk scalars
-    mbar_expect_tx(&bar_sv, (uint32_t)(2 * STATE_BYTES + 16384 + CB_SCAL_BYTES));
-    bulk_load(sm + GK_S, a.tape + (tile_idx0 + hv) * STATE_BYTES, STATE_BYTES, &bar_sv);
-    bulk_load(sm + GK_DS, a.dtape + (tile_idx0 + hv) * STATE_BYTES, STATE_BYTES, &bar_sv);
-    tma_load_3d(sm + GK_V, &a.tv, 0, hv, tok0, &bar_sv);
-    tma_load_3d(sm + GK_V + 8192, &a.tv, 64, hv, tok0, &bar_sv);
-    bulk_load(sm + GK_SCAL, a.cb + (tile_idx0 + hv) * CB_BYTES + CB_SCAL, CB_SCAL_BYTES, &bar_sv);
-  };
-  auto issue_do = [&](int hv) {
-    mbar_expect_tx(&bar_do, 16384u);
-    tma_load_3d(sm + GK_DO, &a.tdo, 0, hv, tok0, &bar_do);
-    tma_load_3d(sm + GK_DO + 8192, &a.tdo, 64, hv, tok0, &bar_do);
-  };
-  auto issue_dt = [&](int hv) {   // dV_new^T and T
-    mbar_expect_tx(&bar_dt, (uint32_t)(VN_BYTES + TILE64_BYTES));
-    bulk_load(sm + GK_DV, a.dvn + (tile_idx0 + hv) * VN_BYTES, VN_BYTES, &bar_dt);
-    bulk_load(sm + GK_T, a.cb + (tile_idx0 + hv) * CB_BYTES + CB_T, TILE64_BYTES, &bar_dt);
-  };
-  if (tid == 0) {
+  auto blk = [&](int c_, int hv_) { return (size_t)c_ * a.HV + hv_; };
+  auto issue_qk = [&](int j_, int tok0_) {
     mbar_expect_tx(&bar_qk, 32768u);
-    tma_load_3d(sm + GK_Q, &a.tq, 0, j, tok0, &bar_qk);
-    tma_load_3d(sm + GK_Q + 8192, &a.tq, 64, j, tok0, &bar_qk);
-    tma_load_3d(sm + GK_K, &a.tk, 0, j, tok0, &bar_qk);
-    tma_load_3d(sm + GK_K + 8192, &a.tk, 64, j, tok0, &bar_qk);
-    issue_vn(j * a.G);
-    issue_sv(j * a.G);
-    issue_do(j * a.G);
-    issue_dt(j * a.G);
-  }
-  for (int i = tid; i < min(a.G, 8) * CH; i += GK_THREADS) {   // gates of the group
-    const int hh = i / CH, r = i % CH;
-    const size_t gi = (size_t)(tok0 + r) * a.HV + j * a.G + hh;
-    gall[hh][r] = r < L ? a.g[gi] : 0.f;
-    ball[hh][r] = r < L ? a.beta[gi] : 0.f;
-  }
-  __syncthreads();
+    tma_load_3d(sm + GK_Q, &a.tq, 0, j_, tok0_, &bar_qk);
+    tma_load_3d(sm + GK_Q + 8192, &a.tq, 64, j_, tok0_, &bar_qk);
+    tma_load_3d(sm + GK_K, &a.tk, 0, j_, tok0_, &bar_qk);
+    tma_load_3d(sm + GK_K + 8192, &a.tk, 64, j_, tok0_, &bar_qk);
+  };
+  auto issue_vn = [&](int c_, int hv_) {   // V_new^T
+    mbar_expect_tx(&bar_vn, (uint32_t)VN_BYTES);
+    bulk_load(sm + GK_VN, a.vn + blk(c_, hv_) * VN_BYTES, VN_BYTES, &bar_vn);
+  };
+  auto issue_sv = [&](int c_, int hv_, int tok0_) {   // S, dS', V and the chunk scalars
+    mbar_expect_tx(&bar_sv, (uint32_t)(2 * STATE_BYTES + 16384 + CB_SCAL_BYTES));
+    bulk_load(sm + GK_S, a.tape + blk(c_, hv_) * STATE_BYTES, STATE_BYTES, &bar_sv);
+    bulk_load(sm + GK_DS, a.dtape + blk(c_, hv_) * STATE_BYTES, STATE_BYTES, &bar_sv);
+    tma_load_3d(sm + GK_V, &a.tv, 0, hv_, tok0_, &bar_sv);
+    tma_load_3d(sm + GK_V + 8192, &a.tv, 64, hv_, tok0_, &bar_sv);
+    bulk_load(sm + GK_SCAL, a.cb + blk(c_, hv_) * CB_BYTES + CB_SCAL, CB_SCAL_BYTES, &bar_sv);
+  };
+  auto issue_do = [&](int hv_, int tok0_) {
+    mbar_expect_tx(&bar_do, 16384u);
+    tma_load_3d(sm + GK_DO, &a.tdo, 0, hv_, tok0_, &bar_do);
+    tma_load_3d(sm + GK_DO + 8192, &a.tdo, 64, hv_, tok0_, &bar_do);
+  };
+  auto issue_dt = [&](int c_, int hv_) {   // dV_new^T and T
+    mbar_expect_tx(&bar_dt, (uint32_t)(VN_BYTES + TILE64_BYTES));
+    bulk_load(sm + GK_DV, a.dvn + blk(c_, hv_) * VN_BYTES, VN_BYTES, &bar_dt);
+    bulk_load(sm + GK_T, a.cb + blk(c_, hv_) * CB_BYTES + CB_T, TILE64_BYTES, &bar_dt);
+  };
+  // gates of one value head into buffer b (one warp): cumulative gate in log2
+  // units (the prep kernel's convention) and the per-token factors with
+  // e^{G_r - G_j} = eGr[r] eGi[j] when the chunk's range is FP32-safe
+  auto gates = [&](int b, int hv_, int tok0_, int L_) {
+    const int r0 = 2 * lane, r1 = r0 + 1;
+    float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+    if (r0 < L_) {
+      g0 = a.g[(size_t)(tok0_ + r0) * a.HV + hv_];
+      b0 = a.beta[(size_t)(tok0_ + r0) * a.HV + hv_];
+    }
+    if (r1 < L_) {
+      g1 = a.g[(size_t)(tok0_ + r1) * a.HV + hv_];
+      b1 = a.beta[(size_t)(tok0_ + r1) * a.HV + hv_];
+    }
+    float s = g0 + g1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    const float ex = s - (g0 + g1);
+    const float G0v = (ex + g0) * kLog2e, G1v = (ex + g0 + g1) * kLog2e;
+    Gs[b][r0] = G0v;
+    Gs[b][r1] = G1v;
+    bs[b][r0] = b0;
+    bs[b][r1] = b1;
+    gs[b][r0] = r0 < L_ ? exp2f(G0v) : 0.f;
+    gs[b][r1] = r1 < L_ ? exp2f(G1v) : 0.f;
+    const float Gfirst = __shfl_sync(0xffffffffu, G0v, 0);
+    const float Glast = __shfl_sync(0xffffffffu, G1v, 31);
+    const bool sf = (Gfirst - Glast) < 100.f;
+    eGr[b][r0] = exp2f(G0v - Gfirst);
+    eGr[b][r1] = exp2f(G1v - Gfirst);
+    eGi[b][r0] = sf ? exp2f(Gfirst - G0v) : 0.f;
+    eGi[b][r1] = sf ? exp2f(Gfirst - G1v) : 0.f;
+    decs[b][r0] = r0 < L_ ? exp2f(Glast - G0v) : 0.f;
+    decs[b][r1] = r1 < L_ ? exp2f(Glast - G1v) : 0.f;
+    if (lane == 0) gsafe[b] = sf;
+  };
 
-  uint32_t mph = 0;
+  uint32_t mph = 0, maph = 0, qkph = 0;
   bool ok = true;
   auto mma_sync_wait = [&]() -> bool {
     bool r = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
@@ -557,57 +591,94 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     as_float16(r0, o0);
     as_float16(r1, o1);
   };
-
-  float dq_acc[GK_CW], dk_acc[GK_CW];   // the column-scaled dq^T, dk^T terms [row][cb0 + e]
+  // MA, from the tiles of the value head in the load buffers
+  auto issue_ma = [&]() {
 #pragma unroll
-  for (int e = 0; e < GK_CW; ++e) dq_acc[e] = dk_acc[e] = 0.f;
+    for (int ks = 0; ks < 8; ++ks) {
+      mma_ss(tb + GT_A4, desc_k(s_do, 64, ks), desc_mn(s_vn, 128, ks), idesc(64, 64, 0, 1), ks > 0);
+      mma_ss(tb + GT_A0, desc_mn(s_s, 128, ks), desc_mn(s_dv, 128, ks), idesc(128, 64, 1, 1), ks > 0);
+      mma_ss(tb + GT_A1, desc_mn(s_s, 128, ks), desc_k(s_do, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+      mma_ss(tb + GT_A3, desc_mn(s_ds, 128, ks), desc_mn(s_vn, 128, ks), idesc(128, 64, 1, 1), ks > 0);
+      mma_ss(tb + GT_A5, desc_mn(s_dv, 128, ks), desc_k(s_v, 64, ks), idesc(64, 64, 1, 0), ks > 0);
+    }
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma_ss(tb + GT_A2, desc_k(s_dv, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
+    mma_commit(&bar_ma);
+  };
 
-  for (int h = 0; h < a.G && ok; ++h) {
-    const int hv = j * a.G + h;
-    const uint32_t vph = h & 1;   // phase of the per-value-head barriers
-    if (h == 0) {
-      ok = __syncthreads_and(mbar_wait(&bar_qk, 0, a.err));
-      if (!ok) break;
-      if (L < CH) {   // zero the Q, K rows past the document end (they hold the next document)
-        for (int idx = tid; idx < (CH - L) * 32; idx += GK_THREADS) {
-          const int t = idx >> 5, tile = (idx >> 4) & 1, c8 = idx & 15;
-          *reinterpret_cast<uint4*>(sm + (tile ? GK_K : GK_Q) + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
-        }
+  uint32_t hc = 0;                      // value heads done by this CTA (phase of the per-head loads)
+  bool ma_issued = false;               // the current value head's MA went out under the last totals
+  {  // the first item's tiles and its first gate scan
+    const int c = blockIdx.x % a.NC, j = blockIdx.x / a.NC;
+    const int tok0 = a.chunk_tok0[c];
+    if (tid == 0) {
+      issue_qk(j, tok0);
+      issue_vn(c, j * a.G);
+      issue_sv(c, j * a.G, tok0);
+      issue_do(j * a.G, tok0);
+      issue_dt(c, j * a.G);
+    }
+    if (warp == 4) gates(0, j * a.G, tok0, a.chunk_len[c]);
+  }
+  // token range of the current item (the next item's is read during its predecessor's last value head)
+  int it_tok0 = a.chunk_tok0[blockIdx.x % a.NC], it_L = a.chunk_len[blockIdx.x % a.NC];
+  for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+    const int c = item % a.NC, j = item / a.NC;
+    const int tok0 = it_tok0, L = it_L;
+    const int nxt = item + gridDim.x;
+    int nx_tok0 = 0, nx_L = 0;
+    // ---- Q, K of the item: norms and the FP32 [QK^T lower | KK^T upper] table
+    ok = __syncthreads_and(mbar_wait(&bar_qk, qkph, a.err));
+    qkph ^= 1;
+    if (!ok) break;
+    if (L < CH) {   // zero the Q, K rows past the document end (they hold the next document)
+      for (int idx = tid; idx < (CH - L) * 32; idx += GK_THREADS) {
+        const int t = idx >> 5, tile = (idx >> 4) & 1, c8 = idx & 15;
+        *reinterpret_cast<uint4*>(sm + (tile ? GK_K : GK_Q) + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
       }
-      if (tid < 128) {   // L2 norms of the q/k rows
-        const uint8_t* tile = sm + (tid < 64 ? GK_K : GK_Q);
-        const int r = tid & 63;
-        float ss = 0.f;
-        if (r < L) {   // same summation order as the prep kernel's norms
+    }
+    {  // L2 norms of the q/k rows: four partial sums of 32 elements, combined as (p0 + p1) + (p2 + p3)
+       // (the prep kernel's order)
+      const int rr = tid >> 2, qq = tid & 3;   // rows 0-63 k, 64-127 q
+      const uint8_t* tile = sm + (rr < 64 ? GK_K : GK_Q);
+      const int r = rr & 63;
+      float ss = 0.f;
+      if (r < L) {
 #pragma unroll
-          for (int c8 = 0; c8 < 16; ++c8) {
-            const uint4 val = *reinterpret_cast<const uint4*>(tile + sw_chunk(r, c8, 64));
-            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&val);
+        for (int c8 = qq * 4; c8 < qq * 4 + 4; ++c8) {
+          const uint4 val = *reinterpret_cast<const uint4*>(tile + sw_chunk(r, c8, 64));
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&val);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __bfloat1622float2(h2[e]);
-              ss = fmaf(f.x, f.x, ss);
-              ss = fmaf(f.y, f.y, ss);
-            }
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(h2[e]);
+            ss = fmaf(f.x, f.x, ss);
+            ss = fmaf(f.y, f.y, ss);
           }
         }
+      }
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      if (qq == 0) {
         const float rn = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-        if (tid < 64) rk[r] = rn;
+        if (rr < 64) rk[r] = rn;
         else rq[r] = rn;
       }
-      // KK^T and QK^T (M = 64) -> the FP32 table: QK^T on and below the diagonal, KK^T above
-      handoff();
-      if (tid == 0) {
+    }
+    if (tid == 0) bulk_wait_read();   // the last item's dq / dk stores have read their staging tiles
+    handoff();
+    if (tid == 0) {   // KK^T, QK^T (M = 64) in the dq / dk accumulator columns, free until M4
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          mma_ss(tb + GT_A0, desc_k(s_k, 64, ks), desc_k(s_k, 64, ks), idesc(64, 64, 0, 0), ks > 0);
-          mma_ss(tb + GT_A1, desc_k(s_q, 64, ks), desc_k(s_k, 64, ks), idesc(64, 64, 0, 0), ks > 0);
-        }
-        mma_commit(&mma_bar);
+      for (int ks = 0; ks < 8; ++ks) {
+        mma_ss(tb + GT_DQ, desc_k(s_k, 64, ks), desc_k(s_k, 64, ks), idesc(64, 64, 0, 0), ks > 0);
+        mma_ss(tb + GT_DK, desc_k(s_q, 64, ks), desc_k(s_k, 64, ks), idesc(64, 64, 0, 0), ks > 0);
       }
-      if (!(ok = mma_sync_wait())) break;
+      mma_commit(&mma_bar);
+    }
+    if (!(ok = mma_sync_wait())) break;
+    {
       float kk[GK_CW], qk[GK_CW];
-      tld2(GT_A0, kk, GT_A1, qk);
+      tld2(GT_DQ, kk, GT_DK, qk);
       if (lane < 16) {
 #pragma unroll
         for (int e = 0; e < GK_CW; e += 4) {
@@ -620,384 +691,451 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
           *reinterpret_cast<float4*>(KQ + r64 * GK_KQLD + cc) = v;
         }
       }
-      tc_fence_before();   // the TMEM reads above precede the first MA
     }
-    if (warp == 0) {  // gates of this value head
-      const int r0 = 2 * lane, r1 = r0 + 1;
-      float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-      if (h < 8) {
-        g0 = gall[h][r0];
-        g1 = gall[h][r1];
-        b0 = ball[h][r0];
-        b1 = ball[h][r1];
-      } else {
-        if (r0 < L) {
-          g0 = a.g[(size_t)(tok0 + r0) * a.HV + hv];
-          b0 = a.beta[(size_t)(tok0 + r0) * a.HV + hv];
+
+    for (int h = 0; h < a.G && ok; ++h, ++hc) {
+      const int hv = j * a.G + h;
+      const uint32_t vph = hc & 1, gb = hc & 1;   // load phase, gate buffer
+      // the value head after this one: the next in the group, else the next item's first
+      int nc = c, nhv = hv + 1, ntok0 = tok0, nL = L;
+      const bool has_next = h + 1 < a.G || nxt < n_items;
+      if (h + 1 == a.G && nxt < n_items) {
+        nc = nxt % a.NC;
+        nhv = (nxt / a.NC) * a.G;
+        ntok0 = nx_tok0 = a.chunk_tok0[nc];
+        nL = nx_L = a.chunk_len[nc];
+      }
+      // this head's tiles (every thread waits: that also makes them visible to its reads)
+      ok = __syncthreads_and(mbar_wait(&bar_vn, vph, a.err) & mbar_wait(&bar_sv, vph, a.err) &
+                             mbar_wait(&bar_do, vph, a.err) & mbar_wait(&bar_dt, vph, a.err));
+      if (!ok) break;
+      const float gL = scal[128];
+      if (!ma_issued) {
+        if (L < CH) {  // zero rows past the document end in the V, dO tiles
+          for (int idx = tid; idx < (CH - L) * 32; idx += GK_THREADS) {
+            const int t = idx >> 5, tile = (idx >> 4) & 1, c8 = idx & 15;
+            *reinterpret_cast<uint4*>(sm + (tile ? GK_DO : GK_V) + sw_chunk(L + t, c8, 64)) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
         }
-        if (r1 < L) {
-          g1 = a.g[(size_t)(tok0 + r1) * a.HV + hv];
-          b1 = a.beta[(size_t)(tok0 + r1) * a.HV + hv];
-        }
+        handoff();
+        if (tid == 0) issue_ma();
       }
-      float s = g0 + g1;
+      ma_issued = false;
+      ok = __syncthreads_and(mbar_wait(&bar_ma, maph, a.err));
+      maph ^= 1;
+      tc_fence_after();
+      if (!ok) break;
+      if (tid == 0 && has_next) issue_vn(nc, nhv);   // V_new^T is dead from here on
+      const bool sfac = gsafe[gb];
+      const float* Gb = Gs[gb];
+      const float* bb = bs[gb];
+      const float* gg = gs[gb];
+      const float* eR = eGr[gb];
+      const float* eI = eGi[gb];
+      auto gamma_rc = [&](int r, int cc) -> float {   // e^{G_r - G_c}, c <= r
+        return sfac ? eR[r] * eI[cc] : exp2f(Gb[r] - Gb[cc]);
+      };
+      // HA: dW^T = -(S dV_new^T) -> shared for MB; X^T kept for the side work
+      float x[GK_CW];
+      {
+        float w[GK_CW];
+        tld2(GT_A0, w, GT_A2, x);
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += y;
-      }
-      const float ex = s - (g0 + g1);
-      // cumulative gate in log2 units (the prep kernel's convention)
-      const float G0v = (ex + g0) * kLog2e, G1v = (ex + g0 + g1) * kLog2e;
-      Gs[r0] = G0v;
-      Gs[r1] = G1v;
-      bs[r0] = b0;
-      bs[r1] = b1;
-      gs[r0] = r0 < L ? exp2f(G0v) : 0.f;
-      gs[r1] = r1 < L ? exp2f(G1v) : 0.f;
-      // per-token gate factors: e^{G_r - G_j} = eGr[r] eGi[j] when the chunk's range is FP32-safe
-      const float Gfirst = __shfl_sync(0xffffffffu, G0v, 0);
-      const float Glast = __shfl_sync(0xffffffffu, G1v, 31);
-      const bool sf = (Gfirst - Glast) < 100.f;
-      eGr[r0] = exp2f(G0v - Gfirst);
-      eGr[r1] = exp2f(G1v - Gfirst);
-      eGi[r0] = sf ? exp2f(Gfirst - G0v) : 0.f;
-      eGi[r1] = sf ? exp2f(Gfirst - G1v) : 0.f;
-      decs[r0] = r0 < L ? exp2f(Glast - G0v) : 0.f;
-      decs[r1] = r1 < L ? exp2f(Glast - G1v) : 0.f;
-      if (lane == 0) gsafe = sf;
-    }
-    // this value head's tiles
-    ok = __syncthreads_and(mbar_wait(&bar_vn, vph, a.err) & mbar_wait(&bar_sv, vph, a.err) &
-                           mbar_wait(&bar_do, vph, a.err) & mbar_wait(&bar_dt, vph, a.err));
-    if (!ok) break;
-    const bool sfac = gsafe;
-    auto gamma_rc = [&](int r, int cc) -> float {   // e^{G_r - G_c}, c <= r
-      return sfac ? eGr[r] * eGi[cc] : exp2f(Gs[r] - Gs[cc]);
-    };
-    const float gL = scal[128];
-    if (L < CH) {  // zero rows past the document end in the V, dO tiles
-      for (int idx = tid; idx < (CH - L) * 32; idx += GK_THREADS) {
-        const int t = idx >> 5, tile = (idx >> 4) & 1, c8 = idx & 15;
-        *reinterpret_cast<uint4*>(sm + (tile ? GK_DO : GK_V) + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-    handoff();
-    // ---- MA
-    if (tid == 0) {
+        for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
+          float t8[8];
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        mma_ss(tb + GT_A4, desc_k(s_do, 64, ks), desc_mn(s_vn, 128, ks), idesc(64, 64, 0, 1), ks > 0);
-        mma_ss(tb + GT_A0, desc_mn(s_s, 128, ks), desc_mn(s_dv, 128, ks), idesc(128, 64, 1, 1), ks > 0);
-        mma_ss(tb + GT_A1, desc_mn(s_s, 128, ks), desc_k(s_do, 64, ks), idesc(128, 64, 1, 0), ks > 0);
-        mma_ss(tb + GT_A3, desc_mn(s_ds, 128, ks), desc_mn(s_vn, 128, ks), idesc(128, 64, 1, 1), ks > 0);
-        mma_ss(tb + GT_A5, desc_mn(s_dv, 128, ks), desc_k(s_v, 64, ks), idesc(64, 64, 1, 0), ks > 0);
-      }
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tb + GT_A2, desc_k(s_dv, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
-      mma_commit(&mma_bar);
-    }
-    if (!(ok = mma_sync_wait())) break;
-    if (tid == 0 && h + 1 < a.G) issue_vn(hv + 1);   // V_new^T is dead from here on
-    // HA: dW^T = -(S dV_new^T) -> shared for MB; X^T kept for the side work
-    float x[GK_CW];
-    {
-      float w[GK_CW];
-      tld2(GT_A0, w, GT_A2, x);
-#pragma unroll
-      for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
-        float t8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) t8[e] = -w[q4 * 8 + e];
-        store_chunk8(sm + GK_WD, row, (cb0 >> 3) + q4, 128, t8);
-      }
-    }
-    handoff();
-    // ---- MB: dW K^T (M = 64), Y^T = dW^T T
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        mma_ss(tb + GT_A0, desc_mn(s_wd, 128, ks), desc_k(s_k, 64, ks), idesc(64, 64, 1, 0), ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tb + GT_A2, desc_k(s_wd, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
-      mma_commit(&mma_bar);
-    }
-    {  // HA side work: dv, the column-scaled dq / dk terms, partial sums for dbeta / dg
-      float cb[GK_CW];
-      __nv_bfloat16* dvp = a.dv + ((size_t)tok0 * a.HV + hv) * D + row;
-#pragma unroll
-      for (int e = 0; e < GK_CW; ++e) {
-        const int cc = cb0 + e;
-        if (cc < L) dvp[(size_t)cc * a.HV * D] = __float2bfloat16_rn(bs[cc] * x[e]);
-        cb[e] = ld_bf16(sm + GK_V, cc, row, 64) * x[e];
-      }
-      const float sb = colsum16(cb, lane);
-      float y[GK_CW], z[GK_CW];
-      tld2(GT_A1, y, GT_A3, z);   // S dO^T (row = dk index), dKd^T (row = dk index)
-#pragma unroll
-      for (int e = 0; e < GK_CW; ++e) {
-        const int cc = cb0 + e;
-        const float pg = a.scale * gs[cc];
-        dq_acc[e] = fmaf(pg, y[e], dq_acc[e]);
-        dk_acc[e] = fmaf(decs[cc], z[e], dk_acc[e]);
-        y[e] = pg * rq[cc] * ld_bf16(sm + GK_Q, cc, row, 64) * y[e];
-        z[e] = rk[cc] * ld_bf16(sm + GK_K, cc, row, 64) * z[e];
-      }
-      const float sg = colsum16(y, lane);
-      const float sz = colsum16(z, lane);
-      // <S, dS'> over this thread's quarter of the row
-      float sd = 0.f;
-#pragma unroll
-      for (int c8 = wg * (16 / GK_NWG); c8 < (wg + 1) * (16 / GK_NWG); ++c8) {   // 16-byte chunks in swizzle order
-        const uint4 sa = *reinterpret_cast<const uint4*>(sm + GK_S + sw_chunk(row, c8, 128));
-        const uint4 sb4 = *reinterpret_cast<const uint4*>(sm + GK_DS + sw_chunk(row, c8, 128));
-        const __nv_bfloat162* ha = reinterpret_cast<const __nv_bfloat162*>(&sa);
-        const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&sb4);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 fa = __bfloat1622float2(ha[e]), fb = __bfloat1622float2(hb[e]);
-          sd = fmaf(fa.x, fb.x, sd);
-          sd = fmaf(fa.y, fb.y, sd);
+          for (int e = 0; e < 8; ++e) t8[e] = -w[q4 * 8 + e];
+          store_chunk8(sm + GK_WD, row, (cb0 >> 3) + q4, 128, t8);
         }
       }
+      handoff();
+      // ---- MB: dW K^T (M = 64), Y^T = dW^T T
+      if (tid == 0) {
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
-      if (lane == 0) sdot[warp] = sd;
-      if (lane < GK_CW) {
-        part[0][w4][cb0 + lane] = sb;
-        part[1][w4][cb0 + lane] = sg;
-        part[2][w4][cb0 + lane] = sz;
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ss(tb + GT_A0, desc_mn(s_wd, 128, ks), desc_k(s_k, 64, ks), idesc(64, 64, 1, 0), ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_ss(tb + GT_A2, desc_k(s_wd, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
+        mma_commit(&mma_bar);
       }
-    }
-    if (!(ok = mma_sync_wait())) break;
-    if (tid == 0 && h + 1 < a.G) issue_sv(hv + 1);   // S, dS', V, scalars are dead from here on
-    {  // HB: the token-pair terms -> H1, H2, dT for M4; dAqk . Aqk -> row / column sums of C
-      float daq[GK_CW], t1[GK_CW], t2[GK_CW];
-      tld(GT_A4, daq);
-      tld2(GT_A5, t1, GT_A0, t2);
-      float cm[GK_CW], rc = 0.f;
-      const int r = r64;
-      const bool rv = lane < 16;
+      {  // HA side work: dv; the column-scaled terms pg S dO^T into dq^T and dec dKd^T into dk^T (TMEM
+         // read-modify-write: no MMA touches them until M4); partial sums for dbeta / dg
+        float cb[GK_CW];
+        __nv_bfloat16* dvp = a.dv + ((size_t)tok0 * a.HV + hv) * D + row;
 #pragma unroll
-      for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
-        float h1[8], h2[8], dt[8];
-        const float4 qa = *reinterpret_cast<const float4*>(KQ + (rv ? r : 0) * GK_KQLD + cb0 + q4 * 8);
-        const float4 qb = *reinterpret_cast<const float4*>(KQ + (rv ? r : 0) * GK_KQLD + cb0 + q4 * 8 + 4);
-        const float qk[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int jj = q4 * 8 + e, cc = cb0 + jj;
-          const bool live = rv && cc <= r && r < L;
-          const float gam = live ? gamma_rc(r, cc) : 0.f;
-          const float dA = live ? a.scale * daq[jj] : 0.f;
-          cm[jj] = dA * gam * rq[r & 63] * rk[cc] * qk[e];
-          rc += cm[jj];
-          h1[e] = rk[cc] * gam * dA;
-          h2[e] = rq[r & 63] * gam * dA;
-          dt[e] = bs[cc] * fmaf(gs[cc] * rk[cc], t2[jj], t1[jj]);
+        for (int e = 0; e < GK_CW; ++e) {
+          const int cc = cb0 + e;
+          if (cc < L) dvp[(size_t)cc * a.HV * D] = __float2bfloat16_rn(bb[cc] * x[e]);
+          cb[e] = ld_bf16(sm + GK_V, cc, row, 64) * x[e];
         }
-        if (rv) {
-          store_chunk8(sm + GK_H1, r, (cb0 >> 3) + q4, 64, h1);
-          store_chunk8(sm + GK_H2, r, (cb0 >> 3) + q4, 64, h2);
-          store_chunk8(sm + GK_DT, r, (cb0 >> 3) + q4, 64, dt);
+        const float sb = colsum16(cb, lane);
+        float y[GK_CW], z[GK_CW];
+        tld2(GT_A1, y, GT_A3, z);   // S dO^T (row = dk index), dKd^T (row = dk index)
+        const float* dd = decs[gb];
+        {
+          float aq[GK_CW], ak[GK_CW];
+          if (h > 0) {
+            tld2(GT_DQ, aq, GT_DK, ak);
+          } else {   // first value head of the item: the columns still hold the KK / QK table
+#pragma unroll
+            for (int e = 0; e < GK_CW; ++e) aq[e] = ak[e] = 0.f;
+          }
+#pragma unroll
+          for (int e = 0; e < GK_CW; ++e) {
+            const int cc = cb0 + e;
+            aq[e] = fmaf(a.scale * gg[cc], y[e], aq[e]);
+            ak[e] = fmaf(dd[cc], z[e], ak[e]);
+          }
+          tmem_st16(taddr(tb, w4 * 32, GT_DQ + cb0), aq);
+          tmem_st16(taddr(tb, w4 * 32, GT_DK + cb0), ak);
         }
-      }
-      if (rv) rowC[wg][r] = rc;
-      const float cs = colsum16(cm, lane);
-      if (lane < GK_CW) colC[0][w4][cb0 + lane] = cs;
-    }
-    handoff();
-    // ---- M4: R1 = dT T^T (M = 64), K^T H1 (+= dq^T), Q^T H2 (+= dk^T)
-    if (tid == 0) {
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        mma_ss(tb + GT_A5, desc_k(s_dt, 64, ks), desc_k(s_t, 64, ks), idesc(64, 64, 0, 0), ks > 0);
-        mma_ss(tb + GT_DQ, desc_mn(s_k, 64, ks), desc_k(s_h1, 64, ks), idesc(128, 64, 1, 0), (h > 0 || ks > 0));
-        mma_ss(tb + GT_DK, desc_mn(s_q, 64, ks), desc_mn(s_h2, 64, ks), idesc(128, 64, 1, 1), (h > 0 || ks > 0));
-      }
-      mma_commit(&mma_bar);
-    }
-    {  // HB side work: Y^T = dW^T T (rows = dk index) -> dk, partial sums
-      float yv[GK_CW];
-      tld(GT_A2, yv);
-#pragma unroll
-      for (int e = 0; e < GK_CW; ++e) {
-        const int cc = cb0 + e;
-        dk_acc[e] = fmaf(bs[cc] * gs[cc], yv[e], dk_acc[e]);
-        yv[e] *= rk[cc] * ld_bf16(sm + GK_K, cc, row, 64);
-      }
-      const float sy = colsum16(yv, lane);
-      if (lane < GK_CW) part[3][w4][cb0 + lane] = sy;
-    }
-    if (!(ok = mma_sync_wait())) break;
-    if (tid == 0 && h + 1 < a.G) issue_do(hv + 1);   // the dO region (H1, H2) is dead
-    {  // H4: R1 -> shared for M5
-      float r1v[GK_CW];
-      tld(GT_A5, r1v);
-      if (lane < 16) {
-#pragma unroll
-        for (int q4 = 0; q4 < GK_CW / 8; ++q4) store_chunk8(sm + GK_R1, r64, (cb0 >> 3) + q4, 64, r1v + q4 * 8);
-      }
-    }
-    handoff();
-    // ---- M5: T^T R1 (= -dA, M = 64)
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tb + GT_A0, desc_mn(s_t, 64, ks), desc_mn(s_r1, 64, ks), idesc(64, 64, 1, 1), ks > 0);
-      mma_commit(&mma_bar);
-    }
-    if (!(ok = mma_sync_wait())) break;
-    if (tid == 0 && h + 1 < a.G) issue_dt(hv + 1);   // dV_new^T (dT, R1) and T are dead
-    {  // H5: dA rows -> F1, F2 for M6; dbeta row terms; dA . A -> column sums of C
-      float xa[GK_CW];
-      tld(GT_A0, xa);
-      const int r = r64;
-      const bool rv = lane < 16;
-      const float br = bs[r & 63];
-      float rb = 0.f, cm[GK_CW];
-#pragma unroll
-      for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
-        float f1[8], f2[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int jj = q4 * 8 + e, cc = cb0 + jj;
-          const bool live = rv && cc < r && r < L;
-          const float gam = live ? gamma_rc(r, cc) : 0.f;
-          const float dA = live ? -xa[jj] : 0.f;
-          const float kk = live ? KQ[cc * GK_KQLD + r] : 0.f;   // KK^T[r][cc], kept above the diagonal
-          const float base = dA * gam * rk[r & 63] * rk[cc] * kk;   // dA . (A / beta_r)
-          rb += base;
-          cm[jj] = br * base;
-          const float E = dA * br * gam;
-          f1[e] = rk[cc] * E;
-          f2[e] = rk[r & 63] * E;
+        for (int e = 0; e < GK_CW; ++e) {
+          const int cc = cb0 + e;
+          y[e] = a.scale * gg[cc] * rq[cc] * ld_bf16(sm + GK_Q, cc, row, 64) * y[e];
+          z[e] = rk[cc] * ld_bf16(sm + GK_K, cc, row, 64) * z[e];
         }
-        if (rv) {
-          store_chunk8(sm + GK_F1, r, (cb0 >> 3) + q4, 64, f1);
-          store_chunk8(sm + GK_F2, r, (cb0 >> 3) + q4, 64, f2);
-        }
-      }
-      if (rv) rowB[wg][r] = rb;
-      const float cs = colsum16(cm, lane);
-      if (lane < GK_CW) colC[1][w4][cb0 + lane] = cs;
-    }
-    handoff();
-    // ---- M6: K^T F1 + K^T F2 (+= dk^T).  Not waited for here: the next
-    // group's commit (or the final one) covers it.
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tb + GT_DK, desc_mn(s_k, 64, ks), desc_k(s_f1, 64, ks), idesc(128, 64, 1, 0), 1u);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tb + GT_DK, desc_mn(s_k, 64, ks), desc_mn(s_f2, 64, ks), idesc(128, 64, 1, 1), 1u);
-    }
-    // ---- per-token totals: dbeta, dG -> dg
-    if (tid < CH) {
-      const int r = tid;
-      float sb = 0.f, sg = 0.f, sz = 0.f, sy = 0.f, cr = 0.f, rbs = 0.f;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        sb += part[0][w][r];
-        sg += part[1][w][r];
-        sz += part[2][w][r];
-        sy += part[3][w][r];
-        cr -= colC[0][w][r] + colC[1][w][r];
-      }
-#pragma unroll
-      for (int w = 0; w < GK_NWG; ++w) {
-        cr += rowC[w][r];
-        rbs += rowB[w][r];
-      }
-      const float z = decs[r] * sz;
-      // row sums - column sums of C = dAqk . Aqk + dA . A (the second row sum is beta_r times rowB)
-      float dG = sg - z + bs[r] * gs[r] * sy + cr + bs[r] * rbs;
-      const float db = sb + gs[r] * sy + rbs;
-      // chunk-end terms: gamma_L <S, dS'> and sum_c z_c
-      float zs = z;
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
-      __shared__ float zpart[2], wtot[2];
-      if (lane == 0) zpart[warp] = zs;
-      named_bar(1, 64);
-      if (r == L - 1) {
+        const float sg = colsum16(y, lane);
+        const float sz = colsum16(z, lane);
+        // <S, dS'> over this thread's quarter of the row
         float sd = 0.f;
 #pragma unroll
-        for (int w = 0; w < GK_THREADS / 32; ++w) sd += sdot[w];
-        dG += gL * sd + zpart[0] + zpart[1];
-      }
-      if (r >= L) dG = 0.f;
-      // dg_r = sum_{i >= r} dG_i: reverse scan within each warp, then add the later warp's total
-      float acc = dG;
+        for (int c8 = wg * (16 / GK_NWG); c8 < (wg + 1) * (16 / GK_NWG); ++c8) {   // 16-byte chunks in swizzle order
+          const uint4 sa = *reinterpret_cast<const uint4*>(sm + GK_S + sw_chunk(row, c8, 128));
+          const uint4 sb4 = *reinterpret_cast<const uint4*>(sm + GK_DS + sw_chunk(row, c8, 128));
+          const __nv_bfloat162* ha = reinterpret_cast<const __nv_bfloat162*>(&sa);
+          const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&sb4);
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float yy = __shfl_down_sync(0xffffffffu, acc, o);
-        if (lane + o < 32) acc += yy;
+          for (int e = 0; e < 4; ++e) {
+            const float2 fa = __bfloat1622float2(ha[e]), fb = __bfloat1622float2(hb[e]);
+            sd = fmaf(fa.x, fb.x, sd);
+            sd = fmaf(fa.y, fb.y, sd);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
+        if (lane == 0) sdot[warp] = sd;
+        if (lane < GK_CW) {
+          part[0][w4][cb0 + lane] = sb;
+          part[1][w4][cb0 + lane] = sg;
+          part[2][w4][cb0 + lane] = sz;
+        }
+        tmem_wait_st();
       }
-      if (lane == 0) wtot[warp] = acc;
-      named_bar(1, 64);
-      if (warp == 0) acc += wtot[1];
-      if (r < L) {
-        a.dg[(size_t)(tok0 + r) * a.HV + hv] = acc;
-        a.dbeta[(size_t)(tok0 + r) * a.HV + hv] = db;
+      if (!(ok = mma_sync_wait())) break;
+      if (tid == 0 && has_next) issue_sv(nc, nhv, ntok0);   // S, dS', V, scalars are dead from here on
+      // The M = 64 token-pair passes spread each 16 x 16 block over the whole warp:
+      // this thread takes rows rb0, rb0 + 8 and columns cbl, cbl + 1, cbl + 8, cbl + 9.
+      const int rb0 = w4 * 16 + (lane >> 2), cbl = cb0 + 2 * (lane & 3);
+      {  // HB: H1, H2, dT for M4; dAqk . Aqk -> row / column sums of C
+        uint32_t u0[8], u1[8], u2[8];
+        tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A4 + cb0), u0);   // dO V_new^T
+        tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A5 + cb0), u1);   // dV_new V^T
+        tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A0 + cb0), u2);   // dW K^T
+        tmem_wait_ld();
+        float rs[2] = {0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int r = rb0 + 8 * hr;
+          const float qr = rq[r];
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const int c0_ = cbl + 8 * hb;
+            const float2 qk = *reinterpret_cast<const float2*>(KQ + r * GK_KQLD + c0_);
+            float h1[2], h2[2], dt[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int i = hb * 4 + hr * 2 + e, cc = c0_ + e;
+              const bool live = cc <= r && r < L;
+              const float gam = live ? gamma_rc(r, cc) : 0.f;
+              const float dA = live ? a.scale * __uint_as_float(u0[i]) : 0.f;
+              const float cm = dA * gam * qr * rk[cc] * (e ? qk.y : qk.x);
+              rs[hr] += cm;
+              cs[hb * 2 + e] += cm;
+              h1[e] = rk[cc] * gam * dA;
+              h2[e] = qr * gam * dA;
+              dt[e] = bb[cc] * fmaf(gg[cc] * rk[cc], __uint_as_float(u2[i]), __uint_as_float(u1[i]));
+            }
+            const uint32_t off = sw_off(r, c0_, 64);
+            *reinterpret_cast<uint32_t*>(sm + GK_H1 + off) = pack_bf16(h1[0], h1[1]);
+            *reinterpret_cast<uint32_t*>(sm + GK_H2 + off) = pack_bf16(h2[0], h2[1]);
+            *reinterpret_cast<uint32_t*>(sm + GK_DT + off) = pack_bf16(dt[0], dt[1]);
+          }
+        }
+        // rows: the 4 lanes of a row group; columns: the 8 lanes of a column pair
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          rs[hr] += __shfl_xor_sync(0xffffffffu, rs[hr], 1);
+          rs[hr] += __shfl_xor_sync(0xffffffffu, rs[hr], 2);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int o = 4; o <= 16; o <<= 1) cs[k] += __shfl_xor_sync(0xffffffffu, cs[k], o);
+        if ((lane & 3) == 0) {
+          rowC[wg][rb0] = rs[0];
+          rowC[wg][rb0 + 8] = rs[1];
+        }
+        if (lane < 4) {
+          colC[0][w4][cbl] = cs[0];
+          colC[0][w4][cbl + 1] = cs[1];
+          colC[0][w4][cbl + 8] = cs[2];
+          colC[0][w4][cbl + 9] = cs[3];
+        }
       }
+      handoff();
+      // ---- M4: R1 = dT T^T (M = 64), K^T H1 (+= dq^T), Q^T H2 (+= dk^T)
+      if (tid == 0) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          mma_ss(tb + GT_A5, desc_k(s_dt, 64, ks), desc_k(s_t, 64, ks), idesc(64, 64, 0, 0), ks > 0);
+          mma_ss(tb + GT_DQ, desc_mn(s_k, 64, ks), desc_k(s_h1, 64, ks), idesc(128, 64, 1, 0), 1u);
+          mma_ss(tb + GT_DK, desc_mn(s_q, 64, ks), desc_mn(s_h2, 64, ks), idesc(128, 64, 1, 1), 1u);
+        }
+        mma_commit(&mma_bar);
+      }
+      if (!(ok = mma_sync_wait())) break;
+      if (tid == 0 && has_next) issue_do(nhv, ntok0);   // the dO region (H1, H2) is dead
+      {  // H4: R1 -> shared for M5
+        uint32_t u[8];
+        tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A5 + cb0), u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const int i = hb * 4 + hr * 2;
+            *reinterpret_cast<uint32_t*>(sm + GK_R1 + sw_off(rb0 + 8 * hr, cbl + 8 * hb, 64)) =
+                pack_bf16(__uint_as_float(u[i]), __uint_as_float(u[i + 1]));
+          }
+      }
+      handoff();
+      // ---- M5: T^T R1 (= -dA, M = 64)
+      if (tid == 0) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_ss(tb + GT_A0, desc_mn(s_t, 64, ks), desc_mn(s_r1, 64, ks), idesc(64, 64, 1, 1), ks > 0);
+        mma_commit(&mma_bar);
+      }
+      {  // H4 side work: beta gamma Y^T into dk^T (TMEM: M4 is done, M6 not yet issued), partial sums
+        float yv[GK_CW], ak[GK_CW];
+        tld2(GT_A2, yv, GT_DK, ak);   // Y^T = dW^T T (rows = dk index)
+#pragma unroll
+        for (int e = 0; e < GK_CW; ++e) {
+          const int cc = cb0 + e;
+          ak[e] = fmaf(bb[cc] * gg[cc], yv[e], ak[e]);
+          yv[e] *= rk[cc] * ld_bf16(sm + GK_K, cc, row, 64);
+        }
+        tmem_st16(taddr(tb, w4 * 32, GT_DK + cb0), ak);
+        const float sy = colsum16(yv, lane);
+        if (lane < GK_CW) part[3][w4][cb0 + lane] = sy;
+        tmem_wait_st();
+      }
+      if (!(ok = mma_sync_wait())) break;
+      if (tid == 0 && has_next) issue_dt(nc, nhv);   // dV_new^T (dT, R1) and T are dead
+      {  // H5: dA rows -> F1, F2 for M6; dbeta row terms; dA . A -> column sums of C
+        uint32_t u[8];
+        tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A0 + cb0), u);
+        tmem_wait_ld();
+        float rbv[2] = {0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int r = rb0 + 8 * hr;
+          const float br = bb[r], rkr = rk[r];
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const int c0_ = cbl + 8 * hb;
+            float f1[2], f2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int i = hb * 4 + hr * 2 + e, cc = c0_ + e;
+              const bool live = cc < r && r < L;
+              const float gam = live ? gamma_rc(r, cc) : 0.f;
+              const float dA = live ? -__uint_as_float(u[i]) : 0.f;
+              const float kk = live ? KQ[cc * GK_KQLD + r] : 0.f;   // KK^T[r][cc], kept above the diagonal
+              const float base = dA * gam * rkr * rk[cc] * kk;      // dA . (A / beta_r)
+              rbv[hr] += base;
+              cs[hb * 2 + e] += br * base;
+              const float E = dA * br * gam;
+              f1[e] = rk[cc] * E;
+              f2[e] = rkr * E;
+            }
+            const uint32_t off = sw_off(r, c0_, 64);
+            *reinterpret_cast<uint32_t*>(sm + GK_F1 + off) = pack_bf16(f1[0], f1[1]);
+            *reinterpret_cast<uint32_t*>(sm + GK_F2 + off) = pack_bf16(f2[0], f2[1]);
+          }
+        }
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          rbv[hr] += __shfl_xor_sync(0xffffffffu, rbv[hr], 1);
+          rbv[hr] += __shfl_xor_sync(0xffffffffu, rbv[hr], 2);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int o = 4; o <= 16; o <<= 1) cs[k] += __shfl_xor_sync(0xffffffffu, cs[k], o);
+        if ((lane & 3) == 0) {
+          rowB[wg][rb0] = rbv[0];
+          rowB[wg][rb0 + 8] = rbv[1];
+        }
+        if (lane < 4) {
+          colC[1][w4][cbl] = cs[0];
+          colC[1][w4][cbl + 1] = cs[1];
+          colC[1][w4][cbl + 8] = cs[2];
+          colC[1][w4][cbl + 9] = cs[3];
+        }
+      }
+      handoff();
+      // ---- M6: K^T F1 + K^T F2 (+= dk^T); then the next value head's MA when
+      // its chunk is full (no rows to zero).  M6 is waited for only at the end
+      // of the item: every later commit of this thread covers it.
+      const bool early = has_next && nL == CH;
+      if (tid == 0) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_ss(tb + GT_DK, desc_mn(s_k, 64, ks), desc_k(s_f1, 64, ks), idesc(128, 64, 1, 0), 1u);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_ss(tb + GT_DK, desc_mn(s_k, 64, ks), desc_mn(s_f2, 64, ks), idesc(128, 64, 1, 1), 1u);
+        if (h + 1 == a.G) mma_commit(&mma_bar);
+        if (early && mbar_wait(&bar_vn, vph ^ 1, a.err) && mbar_wait(&bar_sv, vph ^ 1, a.err) &&
+            mbar_wait(&bar_do, vph ^ 1, a.err) && mbar_wait(&bar_dt, vph ^ 1, a.err))
+          issue_ma();
+      }
+      ma_issued = early;
+      if (warp == 2 || warp == 3) {   // ---- per-token totals: dbeta, dG -> dg
+        const int r = tid - 64, wl = warp - 2;
+        float sb = 0.f, sg = 0.f, sz = 0.f, sy = 0.f, cr = 0.f, rbs = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          sb += part[0][w][r];
+          sg += part[1][w][r];
+          sz += part[2][w][r];
+          sy += part[3][w][r];
+          cr -= colC[0][w][r] + colC[1][w][r];
+        }
+#pragma unroll
+        for (int w = 0; w < GK_NWG; ++w) {
+          cr += rowC[w][r];
+          rbs += rowB[w][r];
+        }
+        const float z = decs[gb][r] * sz;
+        // row sums - column sums of C = dAqk . Aqk + dA . A (the second row sum is beta_r times rowB)
+        float dG = sg - z + bb[r] * gg[r] * sy + cr + bb[r] * rbs;
+        const float db = sb + gg[r] * sy + rbs;
+        // chunk-end terms: gamma_L <S, dS'> and sum_c z_c
+        float zs = z;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
+        if (lane == 0) zpart[wl] = zs;
+        named_bar(1, 64);
+        if (r == L - 1) {
+          float sd = 0.f;
+#pragma unroll
+          for (int w = 0; w < GK_THREADS / 32; ++w) sd += sdot[w];
+          dG += gL * sd + zpart[0] + zpart[1];
+        }
+        if (r >= L) dG = 0.f;
+        // dg_r = sum_{i >= r} dG_i: reverse scan within each warp, then add the later warp's total
+        float acc = dG;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float yy = __shfl_down_sync(0xffffffffu, acc, o);
+          if (lane + o < 32) acc += yy;
+        }
+        if (lane == 0) wtot[wl] = acc;
+        named_bar(1, 64);
+        if (wl == 0) acc += wtot[1];
+        if (r < L) {
+          a.dg[(size_t)(tok0 + r) * a.HV + hv] = acc;
+          a.dbeta[(size_t)(tok0 + r) * a.HV + hv] = db;
+        }
+      }
+      if (warp == 4 && has_next) gates(gb ^ 1, nhv, ntok0, nL);
+      __syncthreads();
     }
-    __syncthreads();
-  }
+    if (!ok) break;
 
-  // ---- the MMA-accumulated dq^T, dk^T; L2-norm backward of the group sums; dq, dk
-  if (ok) {
-    if (tid == 0) mma_commit(&mma_bar);
-    ok = mma_sync_wait();
-  }
-  if (ok) {
+    // ---- item end: the MMA-accumulated dq^T, dk^T; L2-norm backward of the group sums; dq, dk
+    if (!(ok = mma_sync_wait())) break;   // M6 of the last value head
+    uint32_t qk2[GK_CW];                  // BF16 q (low half), k (high half) [cb0 + e][row]: the tiles are
+                                          // reloaded for the next item
+    float xq[GK_CW], xk[GK_CW];           // dq^T, dk^T [row][cb0 + e] (before the L2-norm backward)
     {
-      float xq[GK_CW], xk[GK_CW];
+      float pq[GK_CW], pk[GK_CW];
       tld2(GT_DQ, xq, GT_DK, xk);
 #pragma unroll
       for (int e = 0; e < GK_CW; ++e) {
-        dq_acc[e] += xq[e];
-        dk_acc[e] += xk[e];
+        const int cc = cb0 + e;
+        const uint32_t qb = *reinterpret_cast<const uint16_t*>(sm + GK_Q + sw_off(cc, row, 64));
+        const uint32_t kb = *reinterpret_cast<const uint16_t*>(sm + GK_K + sw_off(cc, row, 64));
+        qk2[e] = qb | (kb << 16);
+        pq[e] = __uint_as_float(qb << 16) * xq[e];
+        pk[e] = __uint_as_float(kb << 16) * xk[e];
+      }
+      const float sq = colsum16(pq, lane), sk = colsum16(pk, lane);
+      if (lane < GK_CW) {
+        part[4][w4][cb0 + lane] = sq;
+        part[5][w4][cb0 + lane] = sk;
       }
     }
-    float pq[GK_CW], pk[GK_CW];
+    tc_fence_before();   // the TMEM reads of DQ / DK precede the next item's table MMAs
+    __syncthreads();     // the Q, K tiles are free
+    if (tid == 0 && nxt < n_items) issue_qk(nxt / a.NC, nx_tok0);
+    if (tid < CH) {      // d|x|/dx . g = (g - x (x . g) / |x|^2) / |x|: the per-token factor (x . g) / |x|^3
+      float xq = 0.f, xk = 0.f;
 #pragma unroll
-    for (int e = 0; e < GK_CW; ++e) {
-      const int cc = cb0 + e;
-      pq[e] = ld_bf16(sm + GK_Q, cc, row, 64) * dq_acc[e];
-      pk[e] = ld_bf16(sm + GK_K, cc, row, 64) * dk_acc[e];
-    }
-    const float sq = colsum16(pq, lane), sk = colsum16(pk, lane);
-    if (lane < GK_CW) {
-      part[4][w4][cb0 + lane] = sq;
-      part[5][w4][cb0 + lane] = sk;
+      for (int w = 0; w < 4; ++w) {
+        xq += part[4][w][tid];
+        xk += part[5][w][tid];
+      }
+      const float nq = rq[tid], nk = rk[tid];
+      lq[tid] = xq * nq * nq * nq;
+      lk[tid] = xk * nk * nk * nk;
     }
     __syncthreads();
-    __nv_bfloat16* dqp = a.dq + ((size_t)tok0 * a.H + j) * D + row;
-    __nv_bfloat16* dkp = a.dk + ((size_t)tok0 * a.H + j) * D + row;
+    {
+      const bool full = L == CH;   // full chunk: staged tiles and TMA stores
+      uint8_t* sq_tile = sm + GK_WD;   // both regions are dead until the next item's first value head
+      uint8_t* sk_tile = sm + GK_KQ;
+      __nv_bfloat16* dqp = a.dq + ((size_t)tok0 * a.H + j) * D + row;
+      __nv_bfloat16* dkp = a.dk + ((size_t)tok0 * a.H + j) * D + row;
 #pragma unroll
-    for (int e = 0; e < GK_CW; ++e) {
-      const int cc = cb0 + e;
-      if (cc >= L) continue;
-      float outq = dq_acc[e], outk = dk_acc[e];
-      if (a.l2norm) {
-        float xq = 0.f, xk = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          xq += part[4][w][cc];
-          xk += part[5][w][cc];
+      for (int e = 0; e < GK_CW; ++e) {
+        const int cc = cb0 + e;
+        float outq = xq[e], outk = xk[e];
+        if (a.l2norm) {
+          outq = rq[cc] * xq[e] - __uint_as_float(qk2[e] << 16) * lq[cc];
+          outk = rk[cc] * xk[e] - __uint_as_float(qk2[e] & 0xffff0000u) * lk[cc];
         }
-        const float nq = rq[cc], nk = rk[cc];
-        outq = nq * dq_acc[e] - ld_bf16(sm + GK_Q, cc, row, 64) * xq * nq * nq * nq;
-        outk = nk * dk_acc[e] - ld_bf16(sm + GK_K, cc, row, 64) * xk * nk * nk * nk;
+        if (full) {
+          *reinterpret_cast<__nv_bfloat16*>(sq_tile + sw_off(cc, row, 64)) = __float2bfloat16_rn(outq);
+          *reinterpret_cast<__nv_bfloat16*>(sk_tile + sw_off(cc, row, 64)) = __float2bfloat16_rn(outk);
+        } else if (cc < L) {
+          dqp[(size_t)cc * a.H * D] = __float2bfloat16_rn(outq);
+          dkp[(size_t)cc * a.H * D] = __float2bfloat16_rn(outk);
+        }
       }
-      dqp[(size_t)cc * a.H * D] = __float2bfloat16_rn(outq);
-      dkp[(size_t)cc * a.H * D] = __float2bfloat16_rn(outk);
+      if (full) {
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+          tma_store_3d(&a.tdq, sq_tile, 0, j, tok0);
+          tma_store_3d(&a.tdq, sq_tile + 8192, 64, j, tok0);
+          tma_store_3d(&a.tdk, sk_tile, 0, j, tok0);
+          tma_store_3d(&a.tdk, sk_tile + 8192, 64, j, tok0);
+          bulk_commit();
+        }
+      }
     }
+    it_tok0 = nx_tok0;
+    it_L = nx_L;
   }
+  if (tid == 0) bulk_wait_all();
+  // an MA issued for a value head that never ran must not be left in flight
+  if (ma_issued && tid == 0) mbar_wait(&bar_ma, maph, a.err);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, 512);
@@ -1092,7 +1230,8 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
   ga.tq = ba.tq;
   ga.tk = ba.tk;
   ga.tdo = ba.tdo;
-  if (!make_tmap(&ga.tv, v, P.T, P.HV)) return GDN_ERR_CUDA;
+  if (!make_tmap(&ga.tv, v, P.T, P.HV) || !make_tmap(&ga.tdq, dq, P.T, P.H) || !make_tmap(&ga.tdk, dk, P.T, P.H))
+    return GDN_ERR_CUDA;
   ga.q = static_cast<const __nv_bfloat16*>(q);
   ga.k = static_cast<const __nv_bfloat16*>(k);
   ga.g = g;
@@ -1109,6 +1248,7 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
   ga.dv = static_cast<__nv_bfloat16*>(dv);
   ga.dg = dg;
   ga.dbeta = dbeta;
+  ga.NC = P.NC;
   ga.H = P.H;
   ga.HV = P.HV;
   ga.G = P.G;
@@ -1116,7 +1256,7 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
   ga.scale = pr.scale;
   ga.err = reinterpret_cast<int*>(ws);
   prof_begin(K_GRAD, s);
-  grad_kernel<<<dim3(P.NC, P.H), GK_THREADS, GK_SMEM_ALLOC, s>>>(ga);
+  grad_kernel<<<std::min(P.NC * P.H, P.sms), GK_THREADS, GK_SMEM_ALLOC, s>>>(ga);
   prof_end(K_GRAD, s);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -115,6 +115,7 @@ struct Plan {
   int64_t T;
   int N, H, HV, G;
   int NC, NSEG, nsplit, nsdoc, seg_len, split_min, max_doc_chunks;
+  int sms;   // SMs of the current device (persistent grids)
   uint32_t cu_hash;
   // workspace offsets (bytes)
   size_t o_tables[14];

@@ -80,22 +80,33 @@ __global__ void __launch_bounds__(PR_THREADS, 2) prep_kernel(PrepArgs a) {
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   __syncthreads();
-  if (tid < 128) {  // L2 norms (row tid of the tile)
-    float ss = 0.f;
+  {  // L2 norms: row tid >> 1 of the tile; four partial sums of 32 elements (two per thread),
+     // combined as (p0 + p1) + (p2 + p3)
+    const int rr = tid >> 1, hh = tid & 1;
+    float pr[2];
 #pragma unroll
-    for (int c8 = 0; c8 < 16; ++c8) {
-      uint4 val = *reinterpret_cast<const uint4*>(sm + sw_chunk(tid, c8, 128));
-      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&val);
+    for (int qq = 0; qq < 2; ++qq) {
+      float ss = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float2 f = __bfloat1622float2(h2[e]);
-        ss = fmaf(f.x, f.x, ss);
-        ss = fmaf(f.y, f.y, ss);
+      for (int c8 = (2 * hh + qq) * 4; c8 < (2 * hh + qq) * 4 + 4; ++c8) {
+        uint4 val = *reinterpret_cast<const uint4*>(sm + sw_chunk(rr, c8, 128));
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&val);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float2 f = __bfloat1622float2(h2[e]);
+          ss = fmaf(f.x, f.x, ss);
+          ss = fmaf(f.y, f.y, ss);
+        }
       }
+      pr[qq] = ss;
     }
+    float ss = pr[0] + pr[1];
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     const float rn = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-    if (tid < 64) rk[tid] = rn;
-    else rq[tid - 64] = rn;
+    if (hh == 0) {
+      if (rr < 64) rk[rr] = rn;
+      else rq[rr - 64] = rn;
+    }
   }
   fence_async_smem();
   tc_fence_before();
