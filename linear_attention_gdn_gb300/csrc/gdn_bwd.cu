@@ -55,7 +55,7 @@ struct BScanArgs {
 };
 
 struct GradArgs {
-  CUtensorMap tq, tk, tv, tdo, tdq, tdk;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const float* g;
@@ -726,7 +726,6 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       maph ^= 1;
       tc_fence_after();
       if (!ok) break;
-      if (tid == 0 && has_next) issue_vn(nc, nhv);   // V_new^T is dead from here on
       const bool sfac = gsafe[gb];
       const float* Gb = Gs[gb];
       const float* bb = bs[gb];
@@ -760,17 +759,20 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
           mma_ss(tb + GT_A2, desc_k(s_wd, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
         mma_commit(&mma_bar);
       }
+      const bool full = L == CH;   // full chunk: dv goes out as a staged tile (TMA store)
       {  // HA side work: dv; the column-scaled terms pg S dO^T into dq^T and dec dKd^T into dk^T (TMEM
-         // read-modify-write: no MMA touches them until M4); partial sums for dbeta / dg
-        float cb[GK_CW];
-        __nv_bfloat16* dvp = a.dv + ((size_t)tok0 * a.HV + hv) * D + row;
+         // read-modify-write: no MMA touches them until M4); partial sums for dg
+        if (full) {   // staged in the V_new^T region (dead after MA; the next V_new^T waits for the store)
 #pragma unroll
-        for (int e = 0; e < GK_CW; ++e) {
-          const int cc = cb0 + e;
-          if (cc < L) dvp[(size_t)cc * a.HV * D] = __float2bfloat16_rn(bb[cc] * x[e]);
-          cb[e] = ld_bf16(sm + GK_V, cc, row, 64) * x[e];
+          for (int e = 0; e < GK_CW; ++e)
+            *reinterpret_cast<__nv_bfloat16*>(sm + GK_VN + sw_off(cb0 + e, row, 64)) = __float2bfloat16_rn(bb[cb0 + e] * x[e]);
+          fence_async_smem();
+        } else {
+          __nv_bfloat16* dvp = a.dv + ((size_t)tok0 * a.HV + hv) * D + row;
+#pragma unroll
+          for (int e = 0; e < GK_CW; ++e)
+            if (cb0 + e < L) dvp[(size_t)(cb0 + e) * a.HV * D] = __float2bfloat16_rn(bb[cb0 + e] * x[e]);
         }
-        const float sb = colsum16(cb, lane);
         float y[GK_CW], z[GK_CW];
         tld2(GT_A1, y, GT_A3, z);   // S dO^T (row = dk index), dKd^T (row = dk index)
         const float* dd = decs[gb];
@@ -818,24 +820,33 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         for (int o = 16; o >= 1; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
         if (lane == 0) sdot[warp] = sd;
         if (lane < GK_CW) {
-          part[0][w4][cb0 + lane] = sb;
           part[1][w4][cb0 + lane] = sg;
           part[2][w4][cb0 + lane] = sz;
         }
         tmem_wait_st();
       }
       if (!(ok = mma_sync_wait())) break;
-      if (tid == 0 && has_next) issue_sv(nc, nhv, ntok0);   // S, dS', V, scalars are dead from here on
+      if (tid == 0) {
+        if (full) {
+          tma_store_3d(&a.tdv, sm + GK_VN, 0, hv, tok0);
+          tma_store_3d(&a.tdv, sm + GK_VN + 8192, 64, hv, tok0);
+          bulk_commit();
+        }
+        if (has_next) issue_sv(nc, nhv, ntok0);   // S, dS', V, scalars are dead from here on
+      }
       // The M = 64 token-pair passes spread each 16 x 16 block over the whole warp:
       // this thread takes rows rb0, rb0 + 8 and columns cbl, cbl + 1, cbl + 8, cbl + 9.
       const int rb0 = w4 * 16 + (lane >> 2), cbl = cb0 + 2 * (lane & 3);
-      {  // HB: H1, H2, dT for M4; dAqk . Aqk -> row / column sums of C
+      {  // HB: H1, H2, dT for M4; dAqk . Aqk -> row / column sums of C; the per-token sums
+         // sum_r T[r][c] (dV_new V^T)[r][c] (= V_c . (T^T dV_new)_c, dbeta) and
+         // sum_r T[r][c] (dW K^T)[r][c] (= K_c . (T^T dW)_c, dg)
         uint32_t u0[8], u1[8], u2[8];
         tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A4 + cb0), u0);   // dO V_new^T
         tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A5 + cb0), u1);   // dV_new V^T
         tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A0 + cb0), u2);   // dW K^T
         tmem_wait_ld();
-        float rs[2] = {0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f};
+        float rs[2] = {0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f}, tb1[4] = {0.f, 0.f, 0.f, 0.f},
+              tb2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int r = rb0 + 8 * hr;
@@ -844,6 +855,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
           for (int hb = 0; hb < 2; ++hb) {
             const int c0_ = cbl + 8 * hb;
             const float2 qk = *reinterpret_cast<const float2*>(KQ + r * GK_KQLD + c0_);
+            const float2 tt = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sm + GK_T + sw_off(r, c0_, 64)));
             float h1[2], h2[2], dt[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -856,7 +868,10 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
               cs[hb * 2 + e] += cm;
               h1[e] = rk[cc] * gam * dA;
               h2[e] = qr * gam * dA;
-              dt[e] = bb[cc] * fmaf(gg[cc] * rk[cc], __uint_as_float(u2[i]), __uint_as_float(u1[i]));
+              const float v1 = __uint_as_float(u1[i]), v2 = __uint_as_float(u2[i]), tv = e ? tt.y : tt.x;
+              dt[e] = bb[cc] * fmaf(gg[cc] * rk[cc], v2, v1);
+              tb1[hb * 2 + e] = fmaf(tv, v1, tb1[hb * 2 + e]);
+              tb2[hb * 2 + e] = fmaf(tv, v2, tb2[hb * 2 + e]);
             }
             const uint32_t off = sw_off(r, c0_, 64);
             *reinterpret_cast<uint32_t*>(sm + GK_H1 + off) = pack_bf16(h1[0], h1[1]);
@@ -873,16 +888,23 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
 #pragma unroll
         for (int k = 0; k < 4; ++k)
 #pragma unroll
-          for (int o = 4; o <= 16; o <<= 1) cs[k] += __shfl_xor_sync(0xffffffffu, cs[k], o);
+          for (int o = 4; o <= 16; o <<= 1) {
+            cs[k] += __shfl_xor_sync(0xffffffffu, cs[k], o);
+            tb1[k] += __shfl_xor_sync(0xffffffffu, tb1[k], o);
+            tb2[k] += __shfl_xor_sync(0xffffffffu, tb2[k], o);
+          }
         if ((lane & 3) == 0) {
           rowC[wg][rb0] = rs[0];
           rowC[wg][rb0 + 8] = rs[1];
         }
         if (lane < 4) {
-          colC[0][w4][cbl] = cs[0];
-          colC[0][w4][cbl + 1] = cs[1];
-          colC[0][w4][cbl + 8] = cs[2];
-          colC[0][w4][cbl + 9] = cs[3];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int cc = cbl + (k >> 1) * 8 + (k & 1);
+            colC[0][w4][cc] = cs[k];
+            part[0][w4][cc] = tb1[k];
+            part[3][w4][cc] = rk[cc] * tb2[k];
+          }
         }
       }
       handoff();
@@ -897,7 +919,11 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         mma_commit(&mma_bar);
       }
       if (!(ok = mma_sync_wait())) break;
-      if (tid == 0 && has_next) issue_do(nhv, ntok0);   // the dO region (H1, H2) is dead
+      if (tid == 0 && has_next) {
+        issue_do(nhv, ntok0);   // the dO region (H1, H2) is dead
+        bulk_wait_read();       // the dv store has read the V_new^T region
+        issue_vn(nc, nhv);
+      }
       {  // H4: R1 -> shared for M5
         uint32_t u[8];
         tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A5 + cb0), u);
@@ -919,18 +945,12 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
           mma_ss(tb + GT_A0, desc_mn(s_t, 64, ks), desc_mn(s_r1, 64, ks), idesc(64, 64, 1, 1), ks > 0);
         mma_commit(&mma_bar);
       }
-      {  // H4 side work: beta gamma Y^T into dk^T (TMEM: M4 is done, M6 not yet issued), partial sums
+      {  // H4 side work: beta gamma Y^T into dk^T (TMEM: M4 is done, M6 not yet issued)
         float yv[GK_CW], ak[GK_CW];
         tld2(GT_A2, yv, GT_DK, ak);   // Y^T = dW^T T (rows = dk index)
 #pragma unroll
-        for (int e = 0; e < GK_CW; ++e) {
-          const int cc = cb0 + e;
-          ak[e] = fmaf(bb[cc] * gg[cc], yv[e], ak[e]);
-          yv[e] *= rk[cc] * ld_bf16(sm + GK_K, cc, row, 64);
-        }
+        for (int e = 0; e < GK_CW; ++e) ak[e] = fmaf(bb[cb0 + e] * gg[cb0 + e], yv[e], ak[e]);
         tmem_st16(taddr(tb, w4 * 32, GT_DK + cb0), ak);
-        const float sy = colsum16(yv, lane);
-        if (lane < GK_CW) part[3][w4][cb0 + lane] = sy;
         tmem_wait_st();
       }
       if (!(ok = mma_sync_wait())) break;
@@ -1230,7 +1250,8 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
   ga.tq = ba.tq;
   ga.tk = ba.tk;
   ga.tdo = ba.tdo;
-  if (!make_tmap(&ga.tv, v, P.T, P.HV) || !make_tmap(&ga.tdq, dq, P.T, P.H) || !make_tmap(&ga.tdk, dk, P.T, P.H))
+  if (!make_tmap(&ga.tv, v, P.T, P.HV) || !make_tmap(&ga.tdq, dq, P.T, P.H) || !make_tmap(&ga.tdk, dk, P.T, P.H) ||
+      !make_tmap(&ga.tdv, dv, P.T, P.HV))
     return GDN_ERR_CUDA;
   ga.q = static_cast<const __nv_bfloat16*>(q);
   ga.k = static_cast<const __nv_bfloat16*>(k);
