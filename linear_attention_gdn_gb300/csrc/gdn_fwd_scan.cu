@@ -34,12 +34,12 @@ constexpr int SC_STAGE = 74752;
 constexpr int SC_S = 2 * SC_STAGE;          // BF16 S^T tile, SwTile(128 x 128)
 constexpr int SC_W = SC_S + STATE_BYTES;    // -W^T tile, SwTile(128 x 64)
 constexpr int SC_O = SC_W + 16384;          // BF16 output staging tile [64 tok][128], SwTile(64 x 128)
-constexpr int SC_SIDE = SC_O + 16384;       // per-token output scales of the last two chunks (+ their L)
-constexpr int SC_SMEM = SC_SIDE + 2 * 272;
+constexpr int SC_SMEM = SC_O + 16384;
 constexpr int SC_SMEM_ALLOC = SC_SMEM + 1024;
+constexpr int SC_THREADS = 256;
 
-// TMEM columns: D1 double-buffered (U^T, then V_new^T, of chunks n and n+1)
-constexpr int TM_D1 = 0, TM_DW = 128, TM_DS = 192, TM_O1 = 320, TM_O2 = 384, TM_AVS = 448, TM_AVN = 480;
+// TMEM columns: D1 (U^T, then V_new^T) and O double-buffered over consecutive chunks
+constexpr int TM_D1 = 0, TM_DW = 128, TM_DS = 192, TM_O = 320, TM_AVS = 448, TM_AVN = 480;
 
 __device__ __forceinline__ void store_state_row(uint8_t* dst, int row, const float* S) {
 #pragma unroll
@@ -53,17 +53,32 @@ __device__ __forceinline__ void store_state_row(uint8_t* dst, int row, const flo
   }
 }
 
-// The chain of one chunk is MMA1 (V_new^T = U^T - S^T W^T) -> V_new hop ->
-// MMA2 (dS^T = (V_new^T diag(kd)) K, with the output products) -> S hop.
-// Work that does not feed the chain runs in the shadow of its MMAs:
-// W^T / U^T of chunk n+1 are issued right after MMA1(n) and their hop overlaps
-// MMA2(n); the output epilogue of chunk n-1 overlaps MMA1(n).
-__global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant__ ScanArgs a) {
+// Two warpgroups.  The chain warpgroup (warps 0-3) owns the state and runs
+// only the dependent chain of each chunk:
+//   MMA1 (V_new^T = U^T - S^T W^T) -> V_new hop -> MMA2 (dS^T = (V_new^T
+//   diag(kd)) K, and the output O^T = S^T Q'^T + V_new^T Aqk^T with
+//   Q'_r = gamma_r rq_r q_r, so that o = scale O) -> S hop.
+// The helper warpgroup (warps 4-7) prepares chunk n + 1 while the chain works
+// on chunk n (tile landing, W^T = K^T T'^T and U^T = V^T T''^T, the -W^T
+// tile, Q'), writes the output of chunk n - 1 and streams the tiles in.  They
+// hand off through mbarriers:
+//   bar_wr    helper -> chain   -W^T(n), U^T(n), Q'(n) are ready
+//   bar_m1    MMA1(n) done      (chain: V_new; helper: -W^T tile and D1 reuse)
+//   bar_m2    MMA2(n) done      (chain: S)
+//   bar_o[b]  MMA2(n) done      (helper: output(n) from O buffer b = n & 1)
+//   bar_of[b] helper -> chain   O buffer b has been read out (MMA2(n + 2) may write it)
+//   bar_sf    chain -> helper   chunk n's stage is no longer read (V_new^T copy)
+// Each completes once per use, and no waiter can fall two phases behind.
+__global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_constant__ ScanArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t full_bar[2], bar_m1, bar_w, bar_m2;
+  __shared__ uint64_t full_bar[2], bar_wr, bar_m1, bar_wu, bar_m2, bar_o[2], bar_of[2], bar_sf;
   __shared__ uint32_t tslot;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  __shared__ int side[2][CH + 4];     // L of chunks n - 1, n: it outlives their stage
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lt = tid & 127;      // row within the warpgroup = TMEM lane
+  const int wq = warp & 3;       // the warp's TMEM lane quarter
+  const bool chain = tid < 128;
   if (*(volatile int*)a.err) return;
 
   int mode, seg, hv, split = -1;
@@ -88,27 +103,33 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
   const bool with_vn = mode == 0 && a.vn != nullptr;   // V_new^T tiles for the backward
   const uint32_t tx_bytes = mode == 0 ? (with_o ? 74752u : 50176u) : (mode == 1 ? 50176u : 25600u);
   const uint32_t cb_bytes = mode == 2 ? 8192u : (with_o ? 24576u : 16384u);
+  uint8_t* s_tile = sm + SC_S;
 
-  // ---- initial state (row tid of S^T)
+  // ---- initial state (chain: row lt of S^T)
   float S[128];
-  {
+  if (chain) {
     const float* src = nullptr;
     if (mode == 0 && a.seg_idx[seg] > 0)
-      src = a.s_init + ((size_t)a.seg_split[seg - 1] * a.HV + hv) * STATE_F32 + (size_t)tid * 128;
+      src = a.s_init + ((size_t)a.seg_split[seg - 1] * a.HV + hv) * STATE_F32 + (size_t)lt * 128;
 #pragma unroll
-    for (int jj = 0; jj < 128; ++jj) S[jj] = src ? src[jj] : (mode == 2 && jj == tid ? 1.f : 0.f);
+    for (int jj = 0; jj < 128; ++jj) S[jj] = src ? src[jj] : (mode == 2 && jj == lt ? 1.f : 0.f);
+    store_state_row(s_tile, lt, S);
+    if (mode == 0 && a.tape) store_state_row(a.tape + ((size_t)c0 * a.HV + hv) * STATE_BYTES, lt, S);
   }
-  uint8_t* s_tile = sm + SC_S;
-  store_state_row(s_tile, tid, S);
-  if (mode == 0 && a.tape) store_state_row(a.tape + ((size_t)c0 * a.HV + hv) * STATE_BYTES, tid, S);
 
   if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {
     mbar_init(&full_bar[0], 1);
     mbar_init(&full_bar[1], 1);
+    mbar_init(&bar_wr, 1);
     mbar_init(&bar_m1, 1);
-    mbar_init(&bar_w, 1);
+    mbar_init(&bar_wu, 1);
     mbar_init(&bar_m2, 1);
+    mbar_init(&bar_o[0], 1);
+    mbar_init(&bar_o[1], 1);
+    mbar_init(&bar_of[0], 1);
+    mbar_init(&bar_of[1], 1);
+    mbar_init(&bar_sf, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   fence_async_smem();
@@ -117,7 +138,7 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
   tc_fence_after();
   const uint32_t tb = tslot;
 
-  auto issue = [&](int n) {
+  auto issue = [&](int n) {   // the tiles of chunk n into stage n & 1
     const int ci = c0 + n;
     uint8_t* st = sm + (n & 1) * SC_STAGE;
     uint64_t* bar = &full_bar[n & 1];
@@ -137,236 +158,243 @@ __global__ void __launch_bounds__(128, 1) fwd_scan_kernel(const __grid_constant_
     bulk_load(st + SC_TP, cbp + CB_TP, cb_bytes, bar);
     bulk_load(st + SC_SCAL, cbp + CB_SCAL, CB_SCAL_BYTES, bar);
   };
-  if (tid == 0) {
+  if (tid == 128) {
     if (nch > 0) issue(0);
     if (nch > 1) issue(1);
   }
-
-  uint32_t ph_m1 = 0, ph_w = 0, ph_m2 = 0;
   bool ok = true;
-  const uint32_t sm_s = smem_u32(s_tile), sm_w = smem_u32(sm + SC_W);
-  float* side = reinterpret_cast<float*>(sm + SC_SIDE);   // [2][68]: sc[64], L
 
-  // wait for chunk n's tiles; zero the rows past a document end (they hold the next document)
-  auto land = [&](int n) -> bool {
-    uint8_t* st = sm + (n & 1) * SC_STAGE;
-    if (!__syncthreads_and(mbar_wait(&full_bar[n & 1], (n >> 1) & 1, a.err))) return false;
-    const int L = reinterpret_cast<const int*>(st + SC_SCAL)[129];
-    if (L < CH) {
-      for (int idx = tid; idx < (CH - L) * 48; idx += 128) {
-        const int t = idx / 48, rem = idx % 48, tile = rem / 16, c8 = rem % 16;
-        const int off = tile == 0 ? SC_K : (tile == 1 ? SC_Q : SC_V);
-        *reinterpret_cast<uint4*>(st + off + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      fence_async_smem();
-      __syncthreads();
-    }
-    return true;
-  };
-  // W^T of chunk n -> DW, U^T -> D1[n & 1]
-  auto issue_wu = [&](int n) {
-    uint8_t* st = sm + (n & 1) * SC_STAGE;
-    const uint32_t a_k = smem_u32(st + SC_K), a_v = smem_u32(st + SC_V);
-    const uint32_t a_tp = smem_u32(st + SC_TP), a_tpp = smem_u32(st + SC_TPP);
-    tc_fence_after();
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-      mma_ss_w(tb + TM_DW, desc_mn(a_k, 64, ks), desc_k(a_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
-    if (with_u) {
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss_w(tb + TM_D1 + (n & 1) * 64, desc_mn(a_v, 64, ks), desc_k(a_tpp, 64, ks), idesc(128, 64, 1, 0),
-               ks > 0);
-    }
-    mma_commit_w(&bar_w);
-  };
-  // -W^T -> shared (row tid = dk index), the MN-major B operand of MMA1
-  auto hop_w = [&]() {
-    float w[64];
-    tmem_ld32(taddr(tb, warp * 32, TM_DW), w);
-    tmem_ld32(taddr(tb, warp * 32, TM_DW + 32), w + 32);
-    uint8_t* wt = sm + SC_W;
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) {
-      uint4 v;
-      v.x = pack_bf16(-w[c8 * 8 + 0], -w[c8 * 8 + 1]);
-      v.y = pack_bf16(-w[c8 * 8 + 2], -w[c8 * 8 + 3]);
-      v.z = pack_bf16(-w[c8 * 8 + 4], -w[c8 * 8 + 5]);
-      v.w = pack_bf16(-w[c8 * 8 + 6], -w[c8 * 8 + 7]);
-      *reinterpret_cast<uint4*>(wt + sw_chunk(tid, c8, 128)) = v;
-    }
-    fence_async_smem();
-  };
-  // output of chunk n from O1, O2 (TMEM) with the saved per-token scales
-  uint8_t* o_stage = sm + SC_O;
-  auto output = [&](int n) {
-    const float* sc = side + (n & 1) * 68;
-    const int L = reinterpret_cast<const int*>(sc)[64];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float x1[32], x2[32];
-      tmem_ld32(taddr(tb, warp * 32, TM_O1 + h * 32), x1);
-      tmem_ld32(taddr(tb, warp * 32, TM_O2 + h * 32), x2);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int r = h * 32 + e;
-        *reinterpret_cast<__nv_bfloat16*>(o_stage + sw_off(r, tid, 64)) =
-            __float2bfloat16_rn(fmaf(sc[r], x1[e], a.scale * x2[e]));
-      }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    const int t0 = a.chunk_tok0[c0 + n];
-    if (L < CH) {  // ragged last chunk: only its own rows (the next rows are another document's)
-      for (int idx = tid; idx < L * 16; idx += 128) {
-        const int r = idx >> 4, c8 = idx & 15;
-        *reinterpret_cast<uint4*>(a.o + ((size_t)(t0 + r) * a.HV + hv) * D + c8 * 8) =
-            *reinterpret_cast<const uint4*>(o_stage + sw_chunk(r, c8, 64));
-      }
-    } else if (tid == 0) {
-      tma_store_3d(&a.to, o_stage, 0, hv, t0);
-      tma_store_3d(&a.to, o_stage + 8192, 64, hv, t0);
-      bulk_commit();
-    }
-  };
-
-  // ---- prologue: W^T, U^T of chunk 0 and its -W^T tile
-  if (nch > 0) {
-    ok = land(0);
-    if (ok && warp == 0) issue_wu(0);
-    ok = ok && __syncthreads_and(mbar_wait(&bar_w, ph_w, a.err));
-    ph_w ^= 1;
-    tc_fence_after();
-    if (ok) hop_w();
-    tc_fence_before();
-    __syncthreads();
-  }
-  for (int n = 0; n < nch && ok; ++n) {
-    uint8_t* st = sm + (n & 1) * SC_STAGE;
-    const uint32_t a_k = smem_u32(st + SC_K), a_q = smem_u32(st + SC_Q), a_aqk = smem_u32(st + SC_AQK);
-    const float* scal = reinterpret_cast<const float*>(st + SC_SCAL);
-    const uint32_t d1 = tb + TM_D1 + (n & 1) * 64;
-    // ---- MMA1: V_new^T = U^T - S^T W^T (into D1[n & 1])
-    if (warp == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        mma_ss_w(d1, desc_k(sm_s, 128, ks), desc_mn(sm_w, 128, ks), idesc(128, 64, 0, 1),
-                 (with_u || ks > 0) ? 1u : 0u);
-      mma_commit_w(&bar_m1);
-    }
-    // ---- in its shadow: the output of chunk n - 1, then W^T / U^T of chunk n + 1
-    if (with_o && n > 0) {
-      tc_fence_after();
-      output(n - 1);
-    }
-    const bool next = n + 1 < nch;
-    if (next) {
-      if (!(ok = land(n + 1))) break;
-      if (warp == 0) issue_wu(n + 1);
-    }
-    ok = __syncthreads_and(mbar_wait(&bar_m1, ph_m1, a.err));
-    ph_m1 ^= 1;
-    if (!ok) break;
-    tc_fence_after();
-    {  // V_new^T row tid -> TMEM A operands: scaled by kd (state update), plain (output)
-      float vn[64];
-      tmem_ld32(taddr(tb, warp * 32, d1 - tb), vn);
-      tmem_ld32(taddr(tb, warp * 32, d1 - tb + 32), vn + 32);
-      const float* kd = scal + 64;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t ps[8], pn[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int r = q * 16 + 2 * e;
-          ps[e] = pack_bf16(vn[r] * kd[r], vn[r + 1] * kd[r + 1]);
-          pn[e] = pack_bf16(vn[r], vn[r + 1]);
-        }
-        tmem_st8(taddr(tb, warp * 32, TM_AVS + q * 8), ps);
-        if (with_o) tmem_st8(taddr(tb, warp * 32, TM_AVN + q * 8), pn);
-        if (with_vn) {   // staged in the -W^T tile, which MMA1 has finished reading
-          uint8_t* vt = sm + SC_W;
-          *reinterpret_cast<uint4*>(vt + sw_chunk(tid, 2 * q, 128)) = make_uint4(pn[0], pn[1], pn[2], pn[3]);
-          *reinterpret_cast<uint4*>(vt + sw_chunk(tid, 2 * q + 1, 128)) = make_uint4(pn[4], pn[5], pn[6], pn[7]);
-        }
-      }
-      if (with_o) {  // this chunk's output scales outlive its stage buffer
-        float* sd = side + (n & 1) * 68;
-        if (tid < 64) sd[tid] = scal[tid];
-        if (tid == 64) reinterpret_cast<int*>(sd)[64] = reinterpret_cast<const int*>(scal)[129];
-      }
-      tmem_wait_st();
-    }
-    if (with_vn) fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    // ---- MMA2: dS^T = (V_new^T diag(kd)) K; O2 = V_new^T Aqk^T; O1 = S^T Q^T
-    if (warp == 0) {
-      if (with_vn && tid == 0) {
-        bulk_store(a.vn + ((size_t)(c0 + n) * a.HV + hv) * VN_BYTES, sm + SC_W, VN_BYTES);
-        bulk_commit();
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ts_w(tb + TM_DS, tb + TM_AVS + ks * 8, desc_mn(a_k, 64, ks), idesc(128, 128, 0, 1), ks > 0);
-      if (with_o) {
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ts_w(tb + TM_O2, tb + TM_AVN + ks * 8, desc_k(a_aqk, 64, ks), idesc(128, 64, 0, 0), ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ss_w(tb + TM_O1, desc_k(sm_s, 128, ks), desc_k(a_q, 64, ks), idesc(128, 64, 0, 0), ks > 0);
-      }
-      mma_commit_w(&bar_m2);
-      if (tid == 0) bulk_wait_read();   // earlier tape / output / V_new stores have read the tiles rewritten below
-    }
-    // ---- in its shadow: the -W^T tile of chunk n + 1
-    if (next) {
-      ok = __syncthreads_and(mbar_wait(&bar_w, ph_w, a.err));
-      ph_w ^= 1;
+  if (chain) {
+    // =================== chain warpgroup ===================
+    const uint32_t sm_s = smem_u32(s_tile), sm_w = smem_u32(sm + SC_W);
+    for (int n = 0; n < nch && ok; ++n) {
+      const uint32_t par = n & 1;
+      uint8_t* st = sm + (n & 1) * SC_STAGE;
+      const uint32_t a_k = smem_u32(st + SC_K), a_q = smem_u32(st + SC_Q), a_aqk = smem_u32(st + SC_AQK);
+      const float* scal = reinterpret_cast<const float*>(st + SC_SCAL);
+      const uint32_t d1 = tb + TM_D1 + (n & 1) * 64;
+      ok = wg_sync_and(1, mbar_wait(&bar_wr, par, a.err) && mbar_wait(&full_bar[n & 1], (n >> 1) & 1, a.err));
       if (!ok) break;
       tc_fence_after();
-      hop_w();
-    }
-    ok = __syncthreads_and(mbar_wait(&bar_m2, ph_m2, a.err));
-    ph_m2 ^= 1;
-    if (!ok) break;
-    tc_fence_after();
-    {  // S^T <- gamma_L S^T + dS^T
-      const float gL = scal[128];
+      if (warp == 0) {   // ---- MMA1: V_new^T = U^T - S^T W^T (into D1[n & 1])
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        float ds[32];
-        tmem_ld32(taddr(tb, warp * 32, TM_DS + h * 32), ds);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) S[h * 32 + e] = fmaf(gL, S[h * 32 + e], ds[e]);
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ss_w(d1, desc_k(sm_s, 128, ks), desc_mn(sm_w, 128, ks), idesc(128, 64, 0, 1),
+                   (with_u || ks > 0) ? 1u : 0u);
+        mma_commit_w(&bar_m1);
+        if (lane == 0 && n > 0) {   // chunk n - 1's V_new^T copy and this chunk's tape entry have been read
+          bulk_wait_read();
+          mbar_arrive(&bar_sf);
+        }
       }
-      store_state_row(s_tile, tid, S);   // also the saved state entering the next chunk
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      if (mode == 0 && a.tape && next) {
+      ok = wg_sync_and(1, mbar_wait(&bar_m1, par, a.err));
+      if (!ok) break;
+      tc_fence_after();
+      {  // V_new^T row lt -> TMEM A operands: scaled by kd (state update), plain (output); and the BF16
+         // V_new^T tile for the backward, staged in the chunk's V tile (its U^T MMA is done)
+        float vn[64];
+        tmem_ld32(taddr(tb, wq * 32, d1 - tb), vn);
+        tmem_ld32(taddr(tb, wq * 32, d1 - tb + 32), vn + 32);
+        const float* kd = scal + 64;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t ps[8], pn[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int r = q * 16 + 2 * e;
+            ps[e] = pack_bf16(vn[r] * kd[r], vn[r + 1] * kd[r + 1]);
+            pn[e] = pack_bf16(vn[r], vn[r + 1]);
+          }
+          tmem_st8(taddr(tb, wq * 32, TM_AVS + q * 8), ps);
+          if (with_o) tmem_st8(taddr(tb, wq * 32, TM_AVN + q * 8), pn);
+          if (with_vn) {
+            *reinterpret_cast<uint4*>(st + SC_V + sw_chunk(lt, 2 * q, 128)) = make_uint4(pn[0], pn[1], pn[2], pn[3]);
+            *reinterpret_cast<uint4*>(st + SC_V + sw_chunk(lt, 2 * q + 1, 128)) = make_uint4(pn[4], pn[5], pn[6], pn[7]);
+          }
+        }
+        tmem_wait_st();
+      }
+      if (with_vn) fence_async_smem();
+      tc_fence_before();
+      named_bar(1, 128);
+      if (warp == 0) {   // ---- MMA2: dS^T = (V_new^T diag(kd)) K; O^T = S^T Q'^T + V_new^T Aqk^T
+        if (with_vn && lane == 0) {
+          bulk_store(a.vn + ((size_t)(c0 + n) * a.HV + hv) * VN_BYTES, st + SC_V, VN_BYTES);
+          bulk_commit();
+        }
+        // the output of chunk n - 2 has been read out of this O buffer
+        const bool go = !(with_o && n > 1) || mbar_wait(&bar_of[n & 1], ((n >> 1) - 1) & 1, a.err);
+        tc_fence_after();
+        if (go) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ts_w(tb + TM_DS, tb + TM_AVS + ks * 8, desc_mn(a_k, 64, ks), idesc(128, 128, 0, 1), ks > 0);
+          mma_commit_w(&bar_m2);
+          if (with_o) {
+            const uint32_t to = tb + TM_O + (n & 1) * 64;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              mma_ss_w(to, desc_k(sm_s, 128, ks), desc_k(a_q, 64, ks), idesc(128, 64, 0, 0), ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_ts_w(to, tb + TM_AVN + ks * 8, desc_k(a_aqk, 64, ks), idesc(128, 64, 0, 0), 1u);
+            mma_commit_w(&bar_o[n & 1]);
+          }
+        }
+      }
+      ok = wg_sync_and(1, mbar_wait(&bar_m2, par, a.err));
+      if (!ok) break;
+      tc_fence_after();
+      {  // S^T <- gamma_L S^T + dS^T (the S^T tile is rewritten below, after the O MMAs have read it)
+        const float gL = scal[128];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          float ds[32];
+          tmem_ld32(taddr(tb, wq * 32, TM_DS + h * 32), ds);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) S[h * 32 + e] = fmaf(gL, S[h * 32 + e], ds[e]);
+        }
+        if (with_o && !mbar_wait(&bar_o[n & 1], (n >> 1) & 1, a.err)) ok = false;
+        store_state_row(s_tile, lt, S);   // also the saved state entering the next chunk
+      }
+      fence_async_smem();
+      tc_fence_before();
+      ok = wg_sync_and(1, ok);
+      if (!ok) break;
+      if (tid == 0 && mode == 0 && a.tape && n + 1 < nch) {
         bulk_store(a.tape + ((size_t)(c0 + n + 1) * a.HV + hv) * STATE_BYTES, s_tile, STATE_BYTES);
         bulk_commit();
       }
-      if (n + 2 < nch) issue(n + 2);   // chunk n's stage is dead: its scales are in `side`
     }
-  }
-  if (ok && with_o && nch > 0) {
-    tc_fence_after();
-    output(nch - 1);
-  }
-  if (tid == 0) bulk_wait_read();
-  if (ok && mode != 0) {
-    float* dst = (mode == 1 ? a.bend : a.mend) + ((size_t)split * a.HV + hv) * STATE_F32 + (size_t)tid * 128;
+    if (tid == 0) bulk_wait_all();
+    if (ok && mode != 0) {
+      float* dst = (mode == 1 ? a.bend : a.mend) + ((size_t)split * a.HV + hv) * STATE_F32 + (size_t)lt * 128;
 #pragma unroll
-    for (int jj = 0; jj < 128; jj += 4)
-      *reinterpret_cast<float4*>(dst + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
+      for (int jj = 0; jj < 128; jj += 4)
+        *reinterpret_cast<float4*>(dst + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
+    }
+  } else {
+    // =================== helper warpgroup ===================
+    uint8_t* o_stage = sm + SC_O;
+    // output of chunk n from O1, O2 (TMEM) with the saved per-token scales
+    auto output = [&](int n) {
+      const int L = side[n & 1][CH];
+      if (tid == 128) bulk_wait_read();   // the previous output store has read the staging tile
+      named_bar(2, 128);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float x[32];
+        tmem_ld32(taddr(tb, wq * 32, TM_O + (n & 1) * 64 + h * 32), x);
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          *reinterpret_cast<__nv_bfloat16*>(o_stage + sw_off(h * 32 + e, lt, 64)) = __float2bfloat16_rn(a.scale * x[e]);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      named_bar(2, 128);
+      if (tid == 128) mbar_arrive(&bar_of[n & 1]);   // this O buffer may be rewritten
+      const int t0 = a.chunk_tok0[c0 + n];
+      if (L < CH) {  // ragged last chunk: only its own rows (the next rows are another document's)
+        for (int idx = lt; idx < L * 16; idx += 128) {
+          const int r = idx >> 4, c8 = idx & 15;
+          *reinterpret_cast<uint4*>(a.o + ((size_t)(t0 + r) * a.HV + hv) * D + c8 * 8) =
+              *reinterpret_cast<const uint4*>(o_stage + sw_chunk(r, c8, 64));
+        }
+      } else if (tid == 128) {
+        tma_store_3d(&a.to, o_stage, 0, hv, t0);
+        tma_store_3d(&a.to, o_stage + 8192, 64, hv, t0);
+        bulk_commit();
+      }
+    };
+    for (int n = 0; n < nch && ok; ++n) {
+      // ---- chunk n: land its tiles, W^T = K^T T'^T -> DW, U^T = V^T T''^T -> D1[n & 1], -W^T -> shared
+      uint8_t* st = sm + (n & 1) * SC_STAGE;
+      ok = wg_sync_and(2, mbar_wait(&full_bar[n & 1], (n >> 1) & 1, a.err));
+      if (!ok) break;
+      const int L = reinterpret_cast<const int*>(st + SC_SCAL)[129];
+      if (L < CH) {   // zero the rows past a document end (they hold the next document)
+        for (int idx = lt; idx < (CH - L) * 48; idx += 128) {
+          const int t = idx / 48, rem = idx % 48, tile = rem / 16, c8 = rem % 16;
+          const int off = tile == 0 ? SC_K : (tile == 1 ? SC_Q : SC_V);
+          *reinterpret_cast<uint4*>(st + off + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_async_smem();
+        named_bar(2, 128);
+      }
+      // MMA1(n - 1) has read the -W^T tile and the chain is done with D1[n & 1] (V_new^T of n - 2)
+      if (n > 0 && !(ok = wg_sync_and(2, mbar_wait(&bar_m1, (n - 1) & 1, a.err)))) break;
+      tc_fence_after();
+      if (warp == 4) {
+        const uint32_t a_k = smem_u32(st + SC_K), a_v = smem_u32(st + SC_V);
+        const uint32_t a_tp = smem_u32(st + SC_TP), a_tpp = smem_u32(st + SC_TPP);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_ss_w(tb + TM_DW, desc_mn(a_k, 64, ks), desc_k(a_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+        if (with_u) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ss_w(tb + TM_D1 + (n & 1) * 64, desc_mn(a_v, 64, ks), desc_k(a_tpp, 64, ks), idesc(128, 64, 1, 0),
+                     ks > 0);
+        }
+        mma_commit_w(&bar_wu);
+      }
+      if (!(ok = wg_sync_and(2, mbar_wait(&bar_wu, n & 1, a.err)))) break;
+      tc_fence_after();
+      {  // -W^T -> shared (row lt = dk index), the MN-major B operand of MMA1
+        float w[64];
+        tmem_ld32(taddr(tb, wq * 32, TM_DW), w);
+        tmem_ld32(taddr(tb, wq * 32, TM_DW + 32), w + 32);
+        uint8_t* wt = sm + SC_W;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          uint4 v;
+          v.x = pack_bf16(-w[c8 * 8 + 0], -w[c8 * 8 + 1]);
+          v.y = pack_bf16(-w[c8 * 8 + 2], -w[c8 * 8 + 3]);
+          v.z = pack_bf16(-w[c8 * 8 + 4], -w[c8 * 8 + 5]);
+          v.w = pack_bf16(-w[c8 * 8 + 6], -w[c8 * 8 + 7]);
+          *reinterpret_cast<uint4*>(wt + sw_chunk(lt, c8, 128)) = v;
+        }
+      }
+      if (with_o) {   // Q'_r = gamma_r rq_r q_r = (sc_r / scale) q_r in place; L for the output copy
+        const float* scal = reinterpret_cast<const float*>(st + SC_SCAL);
+        const int r = lt >> 1;
+        const float f = scal[r] * (1.0f / a.scale);
+#pragma unroll
+        for (int c8 = (lt & 1) * 8; c8 < (lt & 1) * 8 + 8; ++c8) {
+          uint4* p = reinterpret_cast<uint4*>(st + SC_Q + sw_chunk(r, c8, 64));
+          uint4 v = *p;
+          __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 x = __bfloat1622float2(h2[e]);
+            h2[e] = __floats2bfloat162_rn(x.x * f, x.y * f);
+          }
+          *p = v;
+        }
+        if (lt == 0) side[n & 1][CH] = L;
+      }
+      fence_async_smem();
+      tc_fence_before();
+      named_bar(2, 128);
+      if (tid == 128) mbar_arrive(&bar_wr);
+      // ---- chunk n + 1 into the stage of chunk n - 1 once the chain no longer reads it
+      if (n > 0 && n + 1 < nch) {
+        if (!(ok = wg_sync_and(2, mbar_wait(&bar_sf, (n - 1) & 1, a.err)))) break;
+        if (tid == 128) issue(n + 1);
+      }
+      // ---- the output of chunk n - 1
+      if (with_o && n > 0) {
+        if (!(ok = wg_sync_and(2, mbar_wait(&bar_o[(n - 1) & 1], ((n - 1) >> 1) & 1, a.err)))) break;
+        tc_fence_after();
+        output(n - 1);
+      }
+    }
+    if (ok && with_o && nch > 0) {
+      ok = wg_sync_and(2, mbar_wait(&bar_o[(nch - 1) & 1], ((nch - 1) >> 1) & 1, a.err));
+      tc_fence_after();
+      if (ok) output(nch - 1);
+    }
+    if (tid == 128) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -431,7 +459,7 @@ void launch_fwd_scan(const ScanArgs& a, int nchains, cudaStream_t s) {
   if (nchains <= 0) return;
   const int id = a.walk ? K_FWD_WALK : K_FWD_SCAN;
   prof_begin(id, s);
-  fwd_scan_kernel<<<nchains, 128, SC_SMEM_ALLOC, s>>>(a);
+  fwd_scan_kernel<<<nchains, SC_THREADS, SC_SMEM_ALLOC, s>>>(a);
   prof_end(id, s);
 }
 void launch_merge(const MergeArgs& a, int nsdoc, cudaStream_t s) {
