@@ -306,6 +306,7 @@ gdn_status run_prep(const Plan& P, const gdn_problem* p, const void* q, const vo
                     const float* beta, uint8_t* ws, uint8_t* cb, int write_T, cudaStream_t s) {
   Tables t = tables_at(P, ws);
   PrepArgs pa;
+  if (!make_tmap(&pa.tq, q, P.T, P.H) || !make_tmap(&pa.tk, k, P.T, P.H)) return GDN_ERR_CUDA;
   pa.q = static_cast<const __nv_bfloat16*>(q);
   pa.k = static_cast<const __nv_bfloat16*>(k);
   pa.g = g;

@@ -68,6 +68,7 @@ struct TableArgs {
 };
 
 struct PrepArgs {
+  CUtensorMap tq, tk;
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const float* g;

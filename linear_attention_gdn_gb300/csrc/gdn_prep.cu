@@ -48,13 +48,14 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
 
-__global__ void __launch_bounds__(PR_THREADS, 2) prep_kernel(PrepArgs a) {
+__global__ void __launch_bounds__(PR_THREADS, 2) prep_kernel(const __grid_constant__ PrepArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   __shared__ float rq[CH], rk[CH];
   __shared__ float Gs[PR_GR][CH], bs[PR_GR][CH], eGr[PR_GR][CH], eGi[PR_GR][CH];
+  __shared__ __align__(16) float cf[PR_GR][CH];   // rk_j e^{G_0 - G_j}: the column factor of A and Aqk
   __shared__ int safe[PR_GR];
-  __shared__ uint64_t bar;
+  __shared__ uint64_t bar, bar_kq;
   __shared__ uint32_t tslot;
   const int c = blockIdx.x, j = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -64,22 +65,43 @@ __global__ void __launch_bounds__(PR_THREADS, 2) prep_kernel(PrepArgs a) {
   if (*(volatile int*)a.err) return;
   const int tok0 = a.chunk_tok0[c], L = a.chunk_len[c];
 
-  // ---- [K; Q] tile: rows 0..63 = k tokens, 64..127 = q tokens (zero past L)
-  for (int idx = tid; idx < 128 * 16; idx += PR_THREADS) {
-    const int rr = idx >> 4, c8 = idx & 15, r = rr & 63;
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (r < L) {
-      const __nv_bfloat16* src = (rr < 64 ? a.k : a.q) + ((size_t)(tok0 + r) * a.H + j) * D + c8 * 8;
-      val = __ldg(reinterpret_cast<const uint4*>(src));
-    }
-    *reinterpret_cast<uint4*>(sm + sw_chunk(rr, c8, 128)) = val;
-  }
+  // ---- [K; Q] tile by TMA: rows 0..63 = k tokens, 64..127 = q tokens (SwTile(128 x 128))
   if (warp == 0) tmem_alloc(&tslot, 64);
   if (tid == 0) {
     mbar_init(&bar, 1);
+    mbar_init(&bar_kq, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
+    mbar_expect_tx(&bar_kq, 32768u);
+    tma_load_3d(sm, &a.tk, 0, j, tok0, &bar_kq);
+    tma_load_3d(sm + 8192, &a.tq, 0, j, tok0, &bar_kq);
+    tma_load_3d(sm + 16384, &a.tk, 64, j, tok0, &bar_kq);
+    tma_load_3d(sm + 24576, &a.tq, 64, j, tok0, &bar_kq);
+  }
+  // the first round's gates, requested while the tiles land
+  float gq0 = 0.f, gq1 = 0.f, bq0 = 0.f, bq1 = 0.f;
+  if (warp < min(PR_GR, a.G)) {
+    const int hv = j * a.G + warp, r0 = 2 * lane, r1 = r0 + 1;
+    if (r0 < L) {
+      gq0 = a.g[(size_t)(tok0 + r0) * a.HV + hv];
+      bq0 = a.beta[(size_t)(tok0 + r0) * a.HV + hv];
+    }
+    if (r1 < L) {
+      gq1 = a.g[(size_t)(tok0 + r1) * a.HV + hv];
+      bq1 = a.beta[(size_t)(tok0 + r1) * a.HV + hv];
+    }
   }
   __syncthreads();
+  if (!__syncthreads_and(mbar_wait(&bar_kq, 0, a.err))) {
+    if (warp == 0) tmem_dealloc(tslot, 64);
+    return;
+  }
+  if (L < CH) {   // zero the rows past the document end (they hold the next document)
+    for (int idx = tid; idx < (CH - L) * 32; idx += PR_THREADS) {
+      const int t = idx >> 5, half = (idx >> 4) & 1, c8 = idx & 15;
+      *reinterpret_cast<uint4*>(sm + sw_chunk(half * 64 + L + t, c8, 128)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();
+  }
   {  // L2 norms: row tid >> 1 of the tile; four partial sums of 32 elements (two per thread),
      // combined as (p0 + p1) + (p2 + p3)
     const int rr = tid >> 1, hh = tid & 1;
@@ -133,14 +155,17 @@ __global__ void __launch_bounds__(PR_THREADS, 2) prep_kernel(PrepArgs a) {
     if (warp < ng) {
       const int hv = j * a.G + h0 + warp;
       const int r0 = 2 * lane, r1 = r0 + 1;
-      float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-      if (r0 < L) {
-        g0 = a.g[(size_t)(tok0 + r0) * a.HV + hv];
-        b0 = a.beta[(size_t)(tok0 + r0) * a.HV + hv];
-      }
-      if (r1 < L) {
-        g1 = a.g[(size_t)(tok0 + r1) * a.HV + hv];
-        b1 = a.beta[(size_t)(tok0 + r1) * a.HV + hv];
+      float g0 = gq0, g1 = gq1, b0 = bq0, b1 = bq1;
+      if (h0 > 0) {
+        g0 = g1 = b0 = b1 = 0.f;
+        if (r0 < L) {
+          g0 = a.g[(size_t)(tok0 + r0) * a.HV + hv];
+          b0 = a.beta[(size_t)(tok0 + r0) * a.HV + hv];
+        }
+        if (r1 < L) {
+          g1 = a.g[(size_t)(tok0 + r1) * a.HV + hv];
+          b1 = a.beta[(size_t)(tok0 + r1) * a.HV + hv];
+        }
       }
       float s = g0 + g1;
 #pragma unroll
@@ -161,6 +186,8 @@ __global__ void __launch_bounds__(PR_THREADS, 2) prep_kernel(PrepArgs a) {
       const bool sf = (Gfirst - Glast) < kSafeRange;
       eGi[warp][r0] = sf ? exp2f(Gfirst - G0v) : 0.f;
       eGi[warp][r1] = sf ? exp2f(Gfirst - G1v) : 0.f;
+      cf[warp][r0] = rk[r0] * eGi[warp][r0];
+      cf[warp][r1] = rk[r1] * eGi[warp][r1];
       if (lane == 0) safe[warp] = sf;
     }
     __syncthreads();
@@ -175,12 +202,25 @@ __global__ void __launch_bounds__(PR_THREADS, 2) prep_kernel(PrepArgs a) {
       if (row < 64) {
         const int r = row;
         float* At = reinterpret_cast<float*>(sm + hh * PR_VH);
-        const float pr = bh[r] * rk[r] * (sf ? eGr[hh][r] : 1.f);
+        if (sf) {   // A[r][jj] = (beta_r rk_r e^{G_r - G_0}) (rk_jj e^{G_0 - G_jj}) KK[r][jj]
+          const float pr = bh[r] * rk[r] * eGr[hh][r];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int jj = cb0 + e;
-          const float gam = sf ? eGi[hh][jj] : exp2f(Gh[r] - Gh[jj]);
-          At[jj * PR_ALD + r] = (jj < r && r < L) ? pr * rk[jj] * gam * kq[e] : 0.f;
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 f = *reinterpret_cast<const float4*>(&cf[hh][cb0 + 4 * e4]);
+            const float fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+            for (int e = 4 * e4; e < 4 * e4 + 4; ++e) {
+              const int jj = cb0 + e;
+              At[jj * PR_ALD + r] = (jj < r && r < L) ? pr * fv[e - 4 * e4] * kq[e] : 0.f;
+            }
+          }
+        } else {
+          const float pr = bh[r] * rk[r];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int jj = cb0 + e;
+            At[jj * PR_ALD + r] = (jj < r && r < L) ? pr * rk[jj] * exp2f(Gh[r] - Gh[jj]) * kq[e] : 0.f;
+          }
         }
         if (wg == 0) {
           float* sc = reinterpret_cast<float*>(sm + PR_SC + hh * CB_SCAL_BYTES);
@@ -199,11 +239,21 @@ __global__ void __launch_bounds__(PR_THREADS, 2) prep_kernel(PrepArgs a) {
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           float x[8];
+          if (sf) {
+            const float4 fa = *reinterpret_cast<const float4*>(&cf[hh][cb0 + q4 * 8]);
+            const float4 fb = *reinterpret_cast<const float4*>(&cf[hh][cb0 + q4 * 8 + 4]);
+            const float fv[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int jj = cb0 + q4 * 8 + e;
-            const float gam = sf ? eGi[hh][jj] : exp2f(Gh[r] - Gh[jj]);
-            x[e] = (jj <= r && r < L) ? pr * rk[jj] * gam * kq[q4 * 8 + e] : 0.f;
+            for (int e = 0; e < 8; ++e) {
+              const int jj = cb0 + q4 * 8 + e;
+              x[e] = (jj <= r && r < L) ? pr * fv[e] * kq[q4 * 8 + e] : 0.f;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int jj = cb0 + q4 * 8 + e;
+              x[e] = (jj <= r && r < L) ? pr * rk[jj] * exp2f(Gh[r] - Gh[jj]) * kq[q4 * 8 + e] : 0.f;
+            }
           }
           uint4 w;
           w.x = pack_bf16(x[0], x[1]);
@@ -216,26 +266,75 @@ __global__ void __launch_bounds__(PR_THREADS, 2) prep_kernel(PrepArgs a) {
     }
     __syncthreads();
 
-    // ---- T = (I + A)^-1, warp pair per value head, lane = column
+    // ---- T = (I + A)^-1 by 16 x 16 blocks, warp pair per value head (64 lanes).  One FP32 array
+    // S[p][q] (pitch PR_ALD) holds A[r][c] (c < r) at S[c][r] and T[r][c] (c <= r) at S[r][c].
+    //   diagonal blocks  T_bb = (I + A_bb)^-1, forward substitution, lane = column
+    //   block diagonal d T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj (i - j = d), lane = (block, column)
     if ((warp >> 1) < ng) {
       const int hh = warp >> 1;
-      const int col = (warp & 1) * 32 + lane;
-      const float* At = reinterpret_cast<const float*>(sm + hh * PR_VH);
+      const int l = (warp & 1) * 32 + lane;
+      float* Sm = reinterpret_cast<float*>(sm + hh * PR_VH);
+      {  // diagonal blocks
+        const int o = 16 * (l >> 4), cc = l & 15;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = (i == cc) ? 1.f : 0.f;
+#pragma unroll
+        for (int jq = 0; jq < 15; ++jq) {
+          const float xj = x[jq];
+#pragma unroll
+          for (int g4 = (jq + 1) >> 2; g4 < 4; ++g4) {
+            const float4 av = *reinterpret_cast<const float4*>(Sm + (o + jq) * PR_ALD + o + 4 * g4);
+            if (4 * g4 + 0 > jq) x[4 * g4 + 0] = fmaf(-av.x, xj, x[4 * g4 + 0]);
+            if (4 * g4 + 1 > jq) x[4 * g4 + 1] = fmaf(-av.y, xj, x[4 * g4 + 1]);
+            if (4 * g4 + 2 > jq) x[4 * g4 + 2] = fmaf(-av.z, xj, x[4 * g4 + 2]);
+            if (4 * g4 + 3 > jq) x[4 * g4 + 3] = fmaf(-av.w, xj, x[4 * g4 + 3]);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (i >= cc) Sm[(o + i) * PR_ALD + o + cc] = x[i];
+      }
+      named_bar(1 + hh, 64);
+#pragma unroll 1
+      for (int d = 1; d <= 3; ++d) {   // off-diagonal blocks, one block diagonal at a time
+        if (l < (4 - d) * 16) {
+          const int jb = l >> 4, ib = jb + d, c = 16 * jb + (l & 15), oi = 16 * ib;
+          float p[16];
+#pragma unroll
+          for (int r = 0; r < 16; ++r) p[r] = 0.f;
+#pragma unroll 4
+          for (int t = 16 * jb; t < oi; ++t) {   // p = sum_k A_ik T_kj (column c)
+            const float tv = t >= c ? Sm[t * PR_ALD + c] : 0.f;
+#pragma unroll
+            for (int g4 = 0; g4 < 4; ++g4) {
+              const float4 av = *reinterpret_cast<const float4*>(Sm + t * PR_ALD + oi + 4 * g4);
+              p[4 * g4 + 0] = fmaf(av.x, tv, p[4 * g4 + 0]);
+              p[4 * g4 + 1] = fmaf(av.y, tv, p[4 * g4 + 1]);
+              p[4 * g4 + 2] = fmaf(av.z, tv, p[4 * g4 + 2]);
+              p[4 * g4 + 3] = fmaf(av.w, tv, p[4 * g4 + 3]);
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < 16; ++r) {   // T_ij[r][c] = -sum_{s <= r} T_ii[r][s] p[s]
+            float acc = 0.f;
+#pragma unroll
+            for (int g4 = 0; g4 <= (r >> 2); ++g4) {
+              const float4 tv4 = *reinterpret_cast<const float4*>(Sm + (oi + r) * PR_ALD + oi + 4 * g4);
+              if (4 * g4 + 0 <= r) acc = fmaf(tv4.x, p[4 * g4 + 0], acc);
+              if (4 * g4 + 1 <= r) acc = fmaf(tv4.y, p[4 * g4 + 1], acc);
+              if (4 * g4 + 2 <= r) acc = fmaf(tv4.z, p[4 * g4 + 2], acc);
+              if (4 * g4 + 3 <= r) acc = fmaf(tv4.w, p[4 * g4 + 3], acc);
+            }
+            Sm[(oi + r) * PR_ALD + c] = -acc;
+          }
+        }
+        named_bar(1 + hh, 64);
+      }
+      const int col = l;   // the tiles, lane = column
       float x[64];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) x[i] = (i == col) ? 1.f : 0.f;
-#pragma unroll
-      for (int jj = 0; jj < 63; ++jj) {
-        const float xj = x[jj];
-#pragma unroll
-        for (int g4 = (jj + 1) >> 2; g4 < 16; ++g4) {
-          const float4 av = *reinterpret_cast<const float4*>(At + jj * PR_ALD + 4 * g4);
-          if (4 * g4 + 0 > jj) x[4 * g4 + 0] = fmaf(-av.x, xj, x[4 * g4 + 0]);
-          if (4 * g4 + 1 > jj) x[4 * g4 + 1] = fmaf(-av.y, xj, x[4 * g4 + 1]);
-          if (4 * g4 + 2 > jj) x[4 * g4 + 2] = fmaf(-av.z, xj, x[4 * g4 + 2]);
-          if (4 * g4 + 3 > jj) x[4 * g4 + 3] = fmaf(-av.w, xj, x[4 * g4 + 3]);
-        }
-      }
+      for (int i = 0; i < 64; ++i) x[i] = i >= col ? Sm[i * PR_ALD + col] : 0.f;
       named_bar(1 + hh, 64);   // both warps of the pair are done reading A^T
       const float bc = bs[hh][col];
       const float pc = bc * exp2f(Gs[hh][col]) * rk[col];
