@@ -138,11 +138,10 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tb = tslot;
 
-  auto issue = [&](int n) {   // the tiles of chunk n into stage n & 1
+  auto issue = [&](int n, int t0) {   // the tiles of chunk n (first token t0) into stage n & 1
     const int ci = c0 + n;
     uint8_t* st = sm + (n & 1) * SC_STAGE;
     uint64_t* bar = &full_bar[n & 1];
-    const int t0 = a.chunk_tok0[ci];
     const uint8_t* cbp = a.cb + ((size_t)ci * a.HV + hv) * CB_BYTES;
     mbar_expect_tx(bar, tx_bytes);
     tma_load_3d(st + SC_K, &a.tk, 0, kh, t0, bar);
@@ -159,8 +158,8 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
     bulk_load(st + SC_SCAL, cbp + CB_SCAL, CB_SCAL_BYTES, bar);
   };
   if (tid == 128) {
-    if (nch > 0) issue(0);
-    if (nch > 1) issue(1);
+    if (nch > 0) issue(0, a.chunk_tok0[c0]);
+    if (nch > 1) issue(1, a.chunk_tok0[c0 + 1]);
   }
   bool ok = true;
 
@@ -182,8 +181,8 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
           mma_ss_w(d1, desc_k(sm_s, 128, ks), desc_mn(sm_w, 128, ks), idesc(128, 64, 0, 1),
                    (with_u || ks > 0) ? 1u : 0u);
         mma_commit_w(&bar_m1);
-        if (lane == 0 && n > 0) {   // chunk n - 1's V_new^T copy and this chunk's tape entry have been read
-          bulk_wait_read();
+        if (lane == 0 && n > 0) {   // chunk n - 1's V_new^T copy has been read (this chunk's tape entry may still be)
+          bulk_wait_read_but1();
           mbar_arrive(&bar_sf);
         }
       }
@@ -230,6 +229,10 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
           for (int ks = 0; ks < 4; ++ks)
             mma_ts_w(tb + TM_DS, tb + TM_AVS + ks * 8, desc_mn(a_k, 64, ks), idesc(128, 128, 0, 1), ks > 0);
           mma_commit_w(&bar_m2);
+          if (lane == 0) {   // this chunk's tape entry has been read: the S^T tile may be rewritten
+            if (with_vn) bulk_wait_read_but1();   // (the V_new^T copy just committed may still be reading)
+            else bulk_wait_read();
+          }
           if (with_o) {
             const uint32_t to = tb + TM_O + (n & 1) * 64;
 #pragma unroll
@@ -309,6 +312,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
     for (int n = 0; n < nch && ok; ++n) {
       // ---- chunk n: land its tiles, W^T = K^T T'^T -> DW, U^T = V^T T''^T -> D1[n & 1], -W^T -> shared
       uint8_t* st = sm + (n & 1) * SC_STAGE;
+      const int nt0 = n + 1 < nch ? a.chunk_tok0[c0 + n + 1] : 0;   // for the tile request below
       ok = wg_sync_and(2, mbar_wait(&full_bar[n & 1], (n >> 1) & 1, a.err));
       if (!ok) break;
       const int L = reinterpret_cast<const int*>(st + SC_SCAL)[129];
@@ -338,23 +342,6 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
         }
         mma_commit_w(&bar_wu);
       }
-      if (!(ok = wg_sync_and(2, mbar_wait(&bar_wu, n & 1, a.err)))) break;
-      tc_fence_after();
-      {  // -W^T -> shared (row lt = dk index), the MN-major B operand of MMA1
-        float w[64];
-        tmem_ld32(taddr(tb, wq * 32, TM_DW), w);
-        tmem_ld32(taddr(tb, wq * 32, TM_DW + 32), w + 32);
-        uint8_t* wt = sm + SC_W;
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          uint4 v;
-          v.x = pack_bf16(-w[c8 * 8 + 0], -w[c8 * 8 + 1]);
-          v.y = pack_bf16(-w[c8 * 8 + 2], -w[c8 * 8 + 3]);
-          v.z = pack_bf16(-w[c8 * 8 + 4], -w[c8 * 8 + 5]);
-          v.w = pack_bf16(-w[c8 * 8 + 6], -w[c8 * 8 + 7]);
-          *reinterpret_cast<uint4*>(wt + sw_chunk(lt, c8, 128)) = v;
-        }
-      }
       if (with_o) {   // Q'_r = gamma_r rq_r q_r = (sc_r / scale) q_r in place; L for the output copy
         const float* scal = reinterpret_cast<const float*>(st + SC_SCAL);
         const int r = lt >> 1;
@@ -373,6 +360,23 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
         }
         if (lt == 0) side[n & 1][CH] = L;
       }
+      if (!(ok = wg_sync_and(2, mbar_wait(&bar_wu, n & 1, a.err)))) break;
+      tc_fence_after();
+      {  // -W^T -> shared (row lt = dk index), the MN-major B operand of MMA1
+        float w[64];
+        tmem_ld32(taddr(tb, wq * 32, TM_DW), w);
+        tmem_ld32(taddr(tb, wq * 32, TM_DW + 32), w + 32);
+        uint8_t* wt = sm + SC_W;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          uint4 v;
+          v.x = pack_bf16(-w[c8 * 8 + 0], -w[c8 * 8 + 1]);
+          v.y = pack_bf16(-w[c8 * 8 + 2], -w[c8 * 8 + 3]);
+          v.z = pack_bf16(-w[c8 * 8 + 4], -w[c8 * 8 + 5]);
+          v.w = pack_bf16(-w[c8 * 8 + 6], -w[c8 * 8 + 7]);
+          *reinterpret_cast<uint4*>(wt + sw_chunk(lt, c8, 128)) = v;
+        }
+      }
       fence_async_smem();
       tc_fence_before();
       named_bar(2, 128);
@@ -380,7 +384,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
       // ---- chunk n + 1 into the stage of chunk n - 1 once the chain no longer reads it
       if (n > 0 && n + 1 < nch) {
         if (!(ok = wg_sync_and(2, mbar_wait(&bar_sf, (n - 1) & 1, a.err)))) break;
-        if (tid == 128) issue(n + 1);
+        if (tid == 128) issue(n + 1, nt0);
       }
       // ---- the output of chunk n - 1
       if (with_o && n > 0) {

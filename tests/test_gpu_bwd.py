@@ -42,6 +42,11 @@ CASES = [
     ("ragged_g3", inputs.custom([1, 63, 64, 65, 0, 130, 200], 2, 6, seed=5)),
     ("nol2_g1", inputs.custom([100, 28], 1, 1, l2norm=False, prenorm_qk=True, seed=6)),
     ("split4", inputs.custom([1000, 70], 1, 2, seed=7, segments=4)),
+    # nine value heads per q/k head; gates steep enough (about -1 per token) that a chunk's
+    # cumulative gate spans more than 2^100, past the factored per-token exponentials
+    ("g9_steep", inputs.custom([150, 64, 1, 97], 1, 9, g_lo=-1.5, g_hi=-0.5, seed=11)),
+    # four value heads per q/k head and more (chunk, q/k head) items than SMs, ragged and empty documents
+    ("items_g4", inputs.custom([700, 0, 1300, 64, 33, 2100], 3, 12, seed=12)),
 ]
 
 
