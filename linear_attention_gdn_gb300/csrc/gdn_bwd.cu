@@ -459,9 +459,9 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t bar_qk, bar_vn, bar_sv, bar_do, bar_dt, bar_ma, mma_bar;
   __shared__ uint32_t tslot;
-  __shared__ float rq[CH], rk[CH];
+  __shared__ __align__(16) float rq[CH], rk[CH];
   // gates of the current and the next value head (double-buffered)
-  __shared__ float Gs[2][CH], bs[2][CH], gs[2][CH], decs[2][CH], eGr[2][CH], eGi[2][CH];
+  __shared__ __align__(16) float Gs[2][CH], bs[2][CH], gs[2][CH], decs[2][CH], eGr[2][CH], eGi[2][CH];
   __shared__ int gsafe[2];
   __shared__ float part[6][4][CH];             // per-token partial sums, one row per 32-lane quarter
   __shared__ float colC[2][4][CH];             // column sums of C (dAqk . Aqk, dA . A) per quarter
@@ -581,7 +581,6 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
                  s_f2 = smem_u32(sm + GK_F2);
   const float* scal = reinterpret_cast<const float*>(sm + GK_SCAL);
   float* KQ = reinterpret_cast<float*>(sm + GK_KQ);
-  auto tld = [&](int col, float* out) { tmem_ld16(taddr(tb, w4 * 32, col + cb0), out); };
   // issue several TMEM loads, then wait once
   auto tld2 = [&](int c0_, float* o0, int c1_, float* o1) {
     uint32_t r0[16], r1[16];
@@ -732,9 +731,6 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       const float* gg = gs[gb];
       const float* eR = eGr[gb];
       const float* eI = eGi[gb];
-      auto gamma_rc = [&](int r, int cc) -> float {   // e^{G_r - G_c}, c <= r
-        return sfac ? eR[r] * eI[cc] : exp2f(Gb[r] - Gb[cc]);
-      };
       // HA: dW^T = -(S dV_new^T) -> shared for MB; X^T kept for the side work
       float x[GK_CW];
       {
@@ -762,10 +758,24 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       const bool full = L == CH;   // full chunk: dv goes out as a staged tile (TMA store)
       {  // HA side work: dv; the column-scaled terms pg S dO^T into dq^T and dec dKd^T into dk^T (TMEM
          // read-modify-write: no MMA touches them until M4); partial sums for dg
+        // per-column factors of this thread's 16 columns, four at a time (16-byte loads)
+        auto col4 = [&](const float* arr, int i, float (&f)[4]) {
+          const float4 v = *reinterpret_cast<const float4*>(arr + cb0 + 4 * i);
+          f[0] = v.x;
+          f[1] = v.y;
+          f[2] = v.z;
+          f[3] = v.w;
+        };
         if (full) {   // staged in the V_new^T region (dead after MA; the next V_new^T waits for the store)
 #pragma unroll
-          for (int e = 0; e < GK_CW; ++e)
-            *reinterpret_cast<__nv_bfloat16*>(sm + GK_VN + sw_off(cb0 + e, row, 64)) = __float2bfloat16_rn(bb[cb0 + e] * x[e]);
+          for (int i = 0; i < 4; ++i) {
+            float f[4];
+            col4(bb, i, f);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<__nv_bfloat16*>(sm + GK_VN + sw_off(cb0 + 4 * i + j, row, 64)) =
+                  __float2bfloat16_rn(f[j] * x[4 * i + j]);
+          }
           fence_async_smem();
         } else {
           __nv_bfloat16* dvp = a.dv + ((size_t)tok0 * a.HV + hv) * D + row;
@@ -785,19 +795,32 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
             for (int e = 0; e < GK_CW; ++e) aq[e] = ak[e] = 0.f;
           }
 #pragma unroll
-          for (int e = 0; e < GK_CW; ++e) {
-            const int cc = cb0 + e;
-            aq[e] = fmaf(a.scale * gg[cc], y[e], aq[e]);
-            ak[e] = fmaf(dd[cc], z[e], ak[e]);
+          for (int i = 0; i < 4; ++i) {
+            float fg[4], fd[4];
+            col4(gg, i, fg);
+            col4(dd, i, fd);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int e = 4 * i + j;
+              aq[e] = fmaf(a.scale * fg[j], y[e], aq[e]);
+              ak[e] = fmaf(fd[j], z[e], ak[e]);
+            }
           }
           tmem_st16(taddr(tb, w4 * 32, GT_DQ + cb0), aq);
           tmem_st16(taddr(tb, w4 * 32, GT_DK + cb0), ak);
         }
 #pragma unroll
-        for (int e = 0; e < GK_CW; ++e) {
-          const int cc = cb0 + e;
-          y[e] = a.scale * gg[cc] * rq[cc] * ld_bf16(sm + GK_Q, cc, row, 64) * y[e];
-          z[e] = rk[cc] * ld_bf16(sm + GK_K, cc, row, 64) * z[e];
+        for (int i = 0; i < 4; ++i) {
+          float fg[4], fq[4], fk[4];
+          col4(gg, i, fg);
+          col4(rq, i, fq);
+          col4(rk, i, fk);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int e = 4 * i + j, cc = cb0 + e;
+            y[e] = a.scale * fg[j] * fq[j] * ld_bf16(sm + GK_Q, cc, row, 64) * y[e];
+            z[e] = fk[j] * ld_bf16(sm + GK_K, cc, row, 64) * z[e];
+          }
         }
         const float sg = colsum16(y, lane);
         const float sz = colsum16(z, lane);
@@ -847,13 +870,19 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         tmem_wait_ld();
         float rs[2] = {0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f}, tb1[4] = {0.f, 0.f, 0.f, 0.f},
               tb2[4] = {0.f, 0.f, 0.f, 0.f};
+        const float qr2[2] = {rq[rb0], rq[rb0 + 8]}, eR2[2] = {eR[rb0], eR[rb0 + 8]};
 #pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int r = rb0 + 8 * hr;
-          const float qr = rq[r];
+        for (int hb = 0; hb < 2; ++hb) {
+          const int c0_ = cbl + 8 * hb;
+          // per-column factors of the column pair (8-byte loads)
+          const float2 rk2 = *reinterpret_cast<const float2*>(rk + c0_), bb2 = *reinterpret_cast<const float2*>(bb + c0_),
+                       gg2 = *reinterpret_cast<const float2*>(gg + c0_), eI2 = *reinterpret_cast<const float2*>(eI + c0_);
+          const float rkc[2] = {rk2.x, rk2.y}, bbc[2] = {bb2.x, bb2.y}, eIc[2] = {eI2.x, eI2.y};
+          const float bgk[2] = {bb2.x * gg2.x * rk2.x, bb2.y * gg2.y * rk2.y};
 #pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            const int c0_ = cbl + 8 * hb;
+          for (int hr = 0; hr < 2; ++hr) {
+            const int r = rb0 + 8 * hr;
+            const float qr = qr2[hr];
             const float2 qk = *reinterpret_cast<const float2*>(KQ + r * GK_KQLD + c0_);
             const float2 tt = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sm + GK_T + sw_off(r, c0_, 64)));
             float h1[2], h2[2], dt[2];
@@ -861,15 +890,15 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
             for (int e = 0; e < 2; ++e) {
               const int i = hb * 4 + hr * 2 + e, cc = c0_ + e;
               const bool live = cc <= r && r < L;
-              const float gam = live ? gamma_rc(r, cc) : 0.f;
+              const float gam = live ? (sfac ? eR2[hr] * eIc[e] : exp2f(Gb[r] - Gb[cc])) : 0.f;
               const float dA = live ? a.scale * __uint_as_float(u0[i]) : 0.f;
-              const float cm = dA * gam * qr * rk[cc] * (e ? qk.y : qk.x);
+              const float cm = dA * gam * qr * rkc[e] * (e ? qk.y : qk.x);
               rs[hr] += cm;
               cs[hb * 2 + e] += cm;
-              h1[e] = rk[cc] * gam * dA;
+              h1[e] = rkc[e] * gam * dA;
               h2[e] = qr * gam * dA;
               const float v1 = __uint_as_float(u1[i]), v2 = __uint_as_float(u2[i]), tv = e ? tt.y : tt.x;
-              dt[e] = bb[cc] * fmaf(gg[cc] * rk[cc], v2, v1);
+              dt[e] = fmaf(bgk[e], v2, bbc[e] * v1);
               tb1[hb * 2 + e] = fmaf(tv, v1, tb1[hb * 2 + e]);
               tb2[hb * 2 + e] = fmaf(tv, v2, tb2[hb * 2 + e]);
             }
@@ -949,7 +978,14 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         float yv[GK_CW], ak[GK_CW];
         tld2(GT_A2, yv, GT_DK, ak);   // Y^T = dW^T T (rows = dk index)
 #pragma unroll
-        for (int e = 0; e < GK_CW; ++e) ak[e] = fmaf(bb[cb0 + e] * gg[cb0 + e], yv[e], ak[e]);
+        for (int i = 0; i < 4; ++i) {
+          const float4 b4 = *reinterpret_cast<const float4*>(bb + cb0 + 4 * i);
+          const float4 g4 = *reinterpret_cast<const float4*>(gg + cb0 + 4 * i);
+          ak[4 * i + 0] = fmaf(b4.x * g4.x, yv[4 * i + 0], ak[4 * i + 0]);
+          ak[4 * i + 1] = fmaf(b4.y * g4.y, yv[4 * i + 1], ak[4 * i + 1]);
+          ak[4 * i + 2] = fmaf(b4.z * g4.z, yv[4 * i + 2], ak[4 * i + 2]);
+          ak[4 * i + 3] = fmaf(b4.w * g4.w, yv[4 * i + 3], ak[4 * i + 3]);
+        }
         tmem_st16(taddr(tb, w4 * 32, GT_DK + cb0), ak);
         tmem_wait_st();
       }
@@ -960,26 +996,29 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A0 + cb0), u);
         tmem_wait_ld();
         float rbv[2] = {0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f};
+        const float br2[2] = {bb[rb0], bb[rb0 + 8]}, rkr2[2] = {rk[rb0], rk[rb0 + 8]}, eR2[2] = {eR[rb0], eR[rb0 + 8]};
 #pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int r = rb0 + 8 * hr;
-          const float br = bb[r], rkr = rk[r];
+        for (int hb = 0; hb < 2; ++hb) {
+          const int c0_ = cbl + 8 * hb;
+          const float2 rk2 = *reinterpret_cast<const float2*>(rk + c0_), eI2 = *reinterpret_cast<const float2*>(eI + c0_);
+          const float rkc[2] = {rk2.x, rk2.y}, eIc[2] = {eI2.x, eI2.y};
 #pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            const int c0_ = cbl + 8 * hb;
+          for (int hr = 0; hr < 2; ++hr) {
+            const int r = rb0 + 8 * hr;
+            const float br = br2[hr], rkr = rkr2[hr];
             float f1[2], f2[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int i = hb * 4 + hr * 2 + e, cc = c0_ + e;
               const bool live = cc < r && r < L;
-              const float gam = live ? gamma_rc(r, cc) : 0.f;
+              const float gam = live ? (sfac ? eR2[hr] * eIc[e] : exp2f(Gb[r] - Gb[cc])) : 0.f;
               const float dA = live ? -__uint_as_float(u[i]) : 0.f;
               const float kk = live ? KQ[cc * GK_KQLD + r] : 0.f;   // KK^T[r][cc], kept above the diagonal
-              const float base = dA * gam * rkr * rk[cc] * kk;      // dA . (A / beta_r)
+              const float base = dA * gam * rkr * rkc[e] * kk;      // dA . (A / beta_r)
               rbv[hr] += base;
               cs[hb * 2 + e] += br * base;
               const float E = dA * br * gam;
-              f1[e] = rk[cc] * E;
+              f1[e] = rkc[e] * E;
               f2[e] = rkr * E;
             }
             const uint32_t off = sw_off(r, c0_, 64);
