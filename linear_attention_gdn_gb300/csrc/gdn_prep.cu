@@ -48,6 +48,62 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
 
+
+// One block diagonal d of T = (I + A)^-1 (16 x 16 blocks, 64 lanes of one value
+// head): T_ij = -T_ii p with p = sum_{k=j}^{i-1} A_ik T_kj, for the 4 - d blocks
+// (i, j = i - d).  S holds A[r][c] (c < r) at S[c][r] and T[r][c] (c <= r) at
+// S[r][c].  The (4 - d) * 16 columns are spread over 64 lanes as G = 1, 2, 4
+// lanes per column; lane g of a column accumulates rows [16g/G, 16(g+1)/G) of
+// p over the whole k range, the G lanes exchange their rows by shuffles, and
+// each then forms its rows of T_ij.
+template <int DL>
+__device__ __forceinline__ void offdiag_level(float* Sm, int l) {
+  constexpr int G = DL == 1 ? 1 : (DL == 2 ? 2 : 4);
+  constexpr int R = 16 / G;                 // rows of p per lane
+  constexpr int NCOL = (4 - DL) * 16;       // columns on this block diagonal
+  const int cl = l / G, g = l % G;
+  const bool act = cl < NCOL;
+  const int jb = act ? cl >> 4 : 0, oi = 16 * (jb + DL), c = 16 * jb + (cl & 15);
+  float p[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) p[r] = 0.f;
+  if (act) {
+#pragma unroll 4
+    for (int t = 16 * jb; t < oi; ++t) {
+      const float tv = t >= c ? Sm[t * PR_ALD + c] : 0.f;   // T[t][c]
+#pragma unroll
+      for (int q = 0; q < R / 4; ++q) {                       // A[oi + r][t] = S[t][oi + r]
+        const float4 av = *reinterpret_cast<const float4*>(Sm + t * PR_ALD + oi + g * R + 4 * q);
+        p[4 * q + 0] = fmaf(av.x, tv, p[4 * q + 0]);
+        p[4 * q + 1] = fmaf(av.y, tv, p[4 * q + 1]);
+        p[4 * q + 2] = fmaf(av.z, tv, p[4 * q + 2]);
+        p[4 * q + 3] = fmaf(av.w, tv, p[4 * q + 3]);
+      }
+    }
+  }
+  float pf[16];   // the whole p of this column, gathered from the G lanes
+#pragma unroll
+  for (int og = 0; og < G; ++og)
+#pragma unroll
+    for (int r = 0; r < R; ++r) pf[og * R + r] = __shfl_sync(0xffffffffu, p[r], (l & 31 & ~(G - 1)) + og);
+  if (act) {
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {   // T_ij[r][c] = -sum_{s <= r} T_ii[r][s] p[s]
+      const int r = g * R + rr;
+      float acc = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 tv4 = *reinterpret_cast<const float4*>(Sm + (oi + r) * PR_ALD + oi + 4 * q);
+        acc = 4 * q + 0 <= r ? fmaf(tv4.x, pf[4 * q + 0], acc) : acc;
+        acc = 4 * q + 1 <= r ? fmaf(tv4.y, pf[4 * q + 1], acc) : acc;
+        acc = 4 * q + 2 <= r ? fmaf(tv4.z, pf[4 * q + 2], acc) : acc;
+        acc = 4 * q + 3 <= r ? fmaf(tv4.w, pf[4 * q + 3], acc) : acc;
+      }
+      Sm[(oi + r) * PR_ALD + c] = -acc;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(PR_THREADS, 2) prep_kernel(const __grid_constant__ PrepArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
@@ -296,41 +352,13 @@ __global__ void __launch_bounds__(PR_THREADS, 2) prep_kernel(const __grid_consta
           if (i >= cc) Sm[(o + i) * PR_ALD + o + cc] = x[i];
       }
       named_bar(1 + hh, 64);
-#pragma unroll 1
-      for (int d = 1; d <= 3; ++d) {   // off-diagonal blocks, one block diagonal at a time
-        if (l < (4 - d) * 16) {
-          const int jb = l >> 4, ib = jb + d, c = 16 * jb + (l & 15), oi = 16 * ib;
-          float p[16];
-#pragma unroll
-          for (int r = 0; r < 16; ++r) p[r] = 0.f;
-#pragma unroll 4
-          for (int t = 16 * jb; t < oi; ++t) {   // p = sum_k A_ik T_kj (column c)
-            const float tv = t >= c ? Sm[t * PR_ALD + c] : 0.f;
-#pragma unroll
-            for (int g4 = 0; g4 < 4; ++g4) {
-              const float4 av = *reinterpret_cast<const float4*>(Sm + t * PR_ALD + oi + 4 * g4);
-              p[4 * g4 + 0] = fmaf(av.x, tv, p[4 * g4 + 0]);
-              p[4 * g4 + 1] = fmaf(av.y, tv, p[4 * g4 + 1]);
-              p[4 * g4 + 2] = fmaf(av.z, tv, p[4 * g4 + 2]);
-              p[4 * g4 + 3] = fmaf(av.w, tv, p[4 * g4 + 3]);
-            }
-          }
-#pragma unroll
-          for (int r = 0; r < 16; ++r) {   // T_ij[r][c] = -sum_{s <= r} T_ii[r][s] p[s]
-            float acc = 0.f;
-#pragma unroll
-            for (int g4 = 0; g4 <= (r >> 2); ++g4) {
-              const float4 tv4 = *reinterpret_cast<const float4*>(Sm + (oi + r) * PR_ALD + oi + 4 * g4);
-              if (4 * g4 + 0 <= r) acc = fmaf(tv4.x, p[4 * g4 + 0], acc);
-              if (4 * g4 + 1 <= r) acc = fmaf(tv4.y, p[4 * g4 + 1], acc);
-              if (4 * g4 + 2 <= r) acc = fmaf(tv4.z, p[4 * g4 + 2], acc);
-              if (4 * g4 + 3 <= r) acc = fmaf(tv4.w, p[4 * g4 + 3], acc);
-            }
-            Sm[(oi + r) * PR_ALD + c] = -acc;
-          }
-        }
-        named_bar(1 + hh, 64);
-      }
+      // off-diagonal blocks, one block diagonal d at a time (then T_ij is complete for i - j = d)
+      offdiag_level<1>(Sm, l);
+      named_bar(1 + hh, 64);
+      offdiag_level<2>(Sm, l);
+      named_bar(1 + hh, 64);
+      offdiag_level<3>(Sm, l);
+      named_bar(1 + hh, 64);
       const int col = l;   // the tiles, lane = column
       float x[64];
 #pragma unroll
