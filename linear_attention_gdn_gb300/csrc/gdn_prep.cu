@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(PR_THREADS, 2) prep_kernel(const __grid_consta
   __shared__ float rq[CH], rk[CH];
   __shared__ float Gs[PR_GR][CH], bs[PR_GR][CH], eGr[PR_GR][CH], eGi[PR_GR][CH];
   __shared__ __align__(16) float cf[PR_GR][CH];   // rk_j e^{G_0 - G_j}: the column factor of A and Aqk
+  __shared__ __align__(16) float ca[PR_GR][CH];   // beta_r rk_r e^{G_r - G_0}: the row factor of A
   __shared__ int safe[PR_GR];
   __shared__ uint64_t bar, bar_kq;
   __shared__ uint32_t tslot;
@@ -244,6 +245,8 @@ __global__ void __launch_bounds__(PR_THREADS, 2) prep_kernel(const __grid_consta
       eGi[warp][r1] = sf ? exp2f(Gfirst - G1v) : 0.f;
       cf[warp][r0] = rk[r0] * eGi[warp][r0];
       cf[warp][r1] = rk[r1] * eGi[warp][r1];
+      ca[warp][r0] = b0 * rk[r0] * eGr[warp][r0];
+      ca[warp][r1] = b1 * rk[r1] * eGr[warp][r1];
       if (lane == 0) safe[warp] = sf;
     }
     __syncthreads();
@@ -256,28 +259,38 @@ __global__ void __launch_bounds__(PR_THREADS, 2) prep_kernel(const __grid_consta
       const float* bh = bs[hh];
       const bool sf = safe[hh];
       if (row < 64) {
-        const int r = row;
+        // KK^T is symmetric, so the thread holding its row c writes row c of the transposed A:
+        // S[c][r] = A[r][c] = (beta_r rk_r e^{G_r - G_0}) (rk_c e^{G_0 - G_c}) KK[c][r] for c < r < L
+        const int c = row;
         float* At = reinterpret_cast<float*>(sm + hh * PR_VH);
-        if (sf) {   // A[r][jj] = (beta_r rk_r e^{G_r - G_0}) (rk_jj e^{G_0 - G_jj}) KK[r][jj]
-          const float pr = bh[r] * rk[r] * eGr[hh][r];
+        if (sf) {
+          const float pc = cf[hh][c];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 f = *reinterpret_cast<const float4*>(&cf[hh][cb0 + 4 * e4]);
-            const float fv[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-            for (int e = 4 * e4; e < 4 * e4 + 4; ++e) {
-              const int jj = cb0 + e;
-              At[jj * PR_ALD + r] = (jj < r && r < L) ? pr * fv[e - 4 * e4] * kq[e] : 0.f;
-            }
+            const int r0 = cb0 + 4 * e4;
+            const float4 f = *reinterpret_cast<const float4*>(&ca[hh][r0]);
+            float4 v;
+            v.x = (r0 + 0 > c && r0 + 0 < L) ? pc * f.x * kq[4 * e4 + 0] : 0.f;
+            v.y = (r0 + 1 > c && r0 + 1 < L) ? pc * f.y * kq[4 * e4 + 1] : 0.f;
+            v.z = (r0 + 2 > c && r0 + 2 < L) ? pc * f.z * kq[4 * e4 + 2] : 0.f;
+            v.w = (r0 + 3 > c && r0 + 3 < L) ? pc * f.w * kq[4 * e4 + 3] : 0.f;
+            *reinterpret_cast<float4*>(At + c * PR_ALD + r0) = v;
           }
         } else {
-          const float pr = bh[r] * rk[r];
+          const float pc = rk[c];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int jj = cb0 + e;
-            At[jj * PR_ALD + r] = (jj < r && r < L) ? pr * rk[jj] * exp2f(Gh[r] - Gh[jj]) * kq[e] : 0.f;
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const int r0 = cb0 + 4 * e4;
+            float x[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int r = r0 + q;
+              x[q] = (r > c && r < L) ? bh[r] * rk[r] * pc * exp2f(Gh[r] - Gh[c]) * kq[4 * e4 + q] : 0.f;
+            }
+            *reinterpret_cast<float4*>(At + c * PR_ALD + r0) = make_float4(x[0], x[1], x[2], x[3]);
           }
         }
+        const int r = row;
         if (wg == 0) {
           float* sc = reinterpret_cast<float*>(sm + PR_SC + hh * CB_SCAL_BYTES);
           const float GL = Gh[L - 1];
