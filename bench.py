@@ -182,6 +182,45 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+# ---------------------------------------------------------------------------
+# replica timing (N independent replicas, one process per GPU): shared by the
+# GPU run and the multi-process CPU tests
+# ---------------------------------------------------------------------------
+def make_allmax(world, device):
+    """max over ranks of a float (identity for one process)."""
+    def allmax(v):
+        if world <= 1:
+            return v
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return t.item()
+    return allmax
+
+
+def timed_replicas(step, K, W, barrier, allmax, clock):
+    """W untimed steps, then K timed steps bracketed by `barrier` (all ranks,
+    device synchronised); returns the slowest rank's ms per step.  `clock()`
+    returns (start, stop_ms): start() marks the beginning, stop_ms() the
+    elapsed milliseconds (CUDA events on the launching stream on a GPU)."""
+    for _ in range(W):
+        step()
+    barrier()
+    start, stop_ms = clock()
+    start()
+    for _ in range(K):
+        step()
+    ms = stop_ms()
+    barrier()
+    return allmax(ms / K)
+
+
+def replica_rate(world, tokens_per_replica, ms_per_step):
+    """whole-job Mtokens/s: the units all ranks processed over the slowest rank's time."""
+    return world * tokens_per_replica / ms_per_step / 1e3
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -218,25 +257,19 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def allmax(v):
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([v], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return t.item()
-        return v
+    allmax = make_allmax(world, dev)
+
+    def event_clock():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def stop_ms():
+            e1.record(stream)
+            e1.synchronize()
+            return e0.elapsed_time(e1)
+        return (lambda: e0.record(stream)), stop_ms
 
     def timed(op, K, W):
-        for _ in range(W):
-            step(op)
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(K):
-            step(op)
-        e1.record(stream)
-        barrier()
-        return allmax(e0.elapsed_time(e1) / K)
+        return timed_replicas(lambda: step(op), K, W, barrier, allmax, event_clock)
 
     op = args.op
     try:
@@ -264,7 +297,7 @@ def run_ours(args, rank, world, local_rank):
         for other in ("fwd", "ckpt"):
             if other != op:
                 t_o = timed(other, max(3, args.steps // 2), 2)
-                extra[other] = {"ms": round(t_o, 4), "Mtokens_per_s": round(world * w.T / t_o / 1e3, 3),
+                extra[other] = {"ms": round(t_o, 4), "Mtokens_per_s": round(replica_rate(world, w.T, t_o), 3),
                                 "TFLOP_per_s": round(world * step_flops(w, other) / t_o / 1e9, 1)}
 
     # end to end through the C ABI with pinned host buffers: every step copies
@@ -299,7 +332,7 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
         barrier()
         ms_e2e = allmax(max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3) / ke)
-        e2e = {"value": round(world * w.T / ms_e2e / 1e3, 3), "unit": UNIT, "h2d_bytes_per_step": int(bi),
+        e2e = {"value": round(replica_rate(world, w.T, ms_e2e), 3), "unit": UNIT, "h2d_bytes_per_step": int(bi),
                "d2h_bytes_per_step": int(bo), "ms_per_step": round(ms_e2e, 3)}
 
     if rank != 0:
@@ -338,7 +371,7 @@ def run_ours(args, rank, world, local_rank):
     tflops = world * step_flops(w, op) / ms / 1e9
     in_gb = sum(x[n].numel() * x[n].element_size() for n in ("q", "k", "v", "g", "beta", "dO")) / 1e9
     return {
-        "metric": METRIC, "value": round(world * w.T / ms / 1e3, 3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": round(replica_rate(world, w.T, ms), 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "tokens": w.T, "docs": w.doc_lens, "H": w.H, "HV": w.HV, "dk": D,
