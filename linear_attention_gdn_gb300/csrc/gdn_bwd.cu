@@ -122,7 +122,7 @@ __device__ __forceinline__ float ld_bf16(const uint8_t* tile, int r, int c, int 
 
 __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant__ BScanArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sm = smem_align1024(smem_raw);
   __shared__ uint64_t full_bar[2], mma_bar;
   __shared__ uint32_t tslot;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -456,7 +456,7 @@ __device__ __forceinline__ void store_chunk8(uint8_t* tile, int r, int c8, int R
 // under the per-token totals (warps 2-3) and the next gate scan (warp 4).
 __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_constant__ GradArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sm = smem_align1024(smem_raw);
   __shared__ uint64_t bar_qk, bar_vn, bar_sv, bar_do, bar_dt, bar_ma, mma_bar;
   __shared__ uint32_t tslot;
   __shared__ __align__(16) float rq[CH], rk[CH];

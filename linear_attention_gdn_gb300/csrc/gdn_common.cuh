@@ -30,6 +30,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// The first 1024-byte boundary in a dynamic shared-memory array.  The offset is
+// added to the array itself (not to an integer copy of its address), so that
+// the compiler keeps the result in the shared address space and every access
+// through it stays a shared-memory access.
+__device__ __forceinline__ uint8_t* smem_align1024(uint8_t* raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
 // ----------------------------------------------------------------------------
 // SwTile addressing
 // ----------------------------------------------------------------------------

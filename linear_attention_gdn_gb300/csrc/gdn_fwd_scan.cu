@@ -71,7 +71,7 @@ __device__ __forceinline__ void store_state_row(uint8_t* dst, int row, const flo
 // Each completes once per use, and no waiter can fall two phases behind.
 __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_constant__ ScanArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sm = smem_align1024(smem_raw);
   __shared__ uint64_t full_bar[2], bar_wr, bar_m1, bar_wu, bar_m2, bar_o[2], bar_of[2], bar_sf;
   __shared__ uint32_t tslot;
   __shared__ int side[2][CH + 4];     // L of chunks n - 1, n: it outlives their stage

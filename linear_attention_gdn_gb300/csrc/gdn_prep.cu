@@ -44,10 +44,6 @@ constexpr int PR_SMEM_ALLOC = PR_SMEM + 1024;
 static_assert(PR_VH >= 64 * PR_ALD * 4 && PR_VH >= 3 * TILE64_BYTES, "value-head region");
 static_assert(PR_SMEM >= 32768, "the [K;Q] tile reuses the front of shared memory");
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
-}
-
 
 // One block diagonal d of T = (I + A)^-1 (16 x 16 blocks, 64 lanes of one value
 // head): T_ij = -T_ii p with p = sum_{k=j}^{i-1} A_ik T_kj, for the 4 - d blocks
@@ -106,7 +102,7 @@ __device__ __forceinline__ void offdiag_level(float* Sm, int l) {
 
 __global__ void __launch_bounds__(PR_THREADS, 2) prep_kernel(const __grid_constant__ PrepArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1024(smem_raw);
+  uint8_t* sm = smem_align1024(smem_raw);
   __shared__ float rq[CH], rk[CH];
   __shared__ float Gs[PR_GR][CH], bs[PR_GR][CH], eGr[PR_GR][CH], eGi[PR_GR][CH];
   __shared__ __align__(16) float cf[PR_GR][CH];   // rk_j e^{G_0 - G_j}: the column factor of A and Aqk
