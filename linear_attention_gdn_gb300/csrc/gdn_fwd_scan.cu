@@ -157,9 +157,26 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
     bulk_load(st + SC_TP, cbp + CB_TP, cb_bytes, bar);
     bulk_load(st + SC_SCAL, cbp + CB_SCAL, CB_SCAL_BYTES, bar);
   };
+  auto prefetch = [&](int n) {   // the tiles of chunk n into L2, a stage ahead of their request
+    const int ci = c0 + n, t0 = a.chunk_tok0[ci];
+    const uint8_t* cbp = a.cb + ((size_t)ci * a.HV + hv) * CB_BYTES;
+    tma_prefetch_3d(&a.tk, 0, kh, t0);
+    tma_prefetch_3d(&a.tk, 64, kh, t0);
+    if (with_o) {
+      tma_prefetch_3d(&a.tq, 0, kh, t0);
+      tma_prefetch_3d(&a.tq, 64, kh, t0);
+    }
+    if (with_u) {
+      tma_prefetch_3d(&a.tv, 0, hv, t0);
+      tma_prefetch_3d(&a.tv, 64, hv, t0);
+    }
+    bulk_prefetch(cbp + CB_TP, cb_bytes);
+    bulk_prefetch(cbp + CB_SCAL, CB_SCAL_BYTES);
+  };
   if (tid == 128) {
     if (nch > 0) issue(0, a.chunk_tok0[c0]);
     if (nch > 1) issue(1, a.chunk_tok0[c0 + 1]);
+    if (nch > 2) prefetch(2);
   }
   bool ok = true;
 
@@ -384,7 +401,10 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
       // ---- chunk n + 1 into the stage of chunk n - 1 once the chain no longer reads it
       if (n > 0 && n + 1 < nch) {
         if (!(ok = wg_sync_and(2, mbar_wait(&bar_sf, (n - 1) & 1, a.err)))) break;
-        if (tid == 128) issue(n + 1, nt0);
+        if (tid == 128) {
+          issue(n + 1, nt0);
+          if (n + 2 < nch) prefetch(n + 2);
+        }
       }
       // ---- the output of chunk n - 1
       if (with_o && n > 0) {
