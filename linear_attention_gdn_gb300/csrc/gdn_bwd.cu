@@ -704,6 +704,12 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         ntok0 = nx_tok0 = a.chunk_tok0[nc];
         nL = nx_L = a.chunk_len[nc];
       }
+      if (tid == 0 && h + 1 == a.G && nxt < n_items) {   // the next item's Q, K into L2, ahead of their request
+        tma_prefetch_3d(&a.tq, 0, nhv / a.G, ntok0);
+        tma_prefetch_3d(&a.tq, 64, nhv / a.G, ntok0);
+        tma_prefetch_3d(&a.tk, 0, nhv / a.G, ntok0);
+        tma_prefetch_3d(&a.tk, 64, nhv / a.G, ntok0);
+      }
       // this head's tiles (every thread waits: that also makes them visible to its reads)
       ok = __syncthreads_and(mbar_wait(&bar_vn, vph, a.err) & mbar_wait(&bar_sv, vph, a.err) &
                              mbar_wait(&bar_do, vph, a.err) & mbar_wait(&bar_dt, vph, a.err));
@@ -825,7 +831,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         const float sg = colsum16(y, lane);
         const float sz = colsum16(z, lane);
         // <S, dS'> over this thread's quarter of the row
-        float sd = 0.f;
+        float sda[4] = {0.f, 0.f, 0.f, 0.f};   // four independent chains, combined in a fixed order
 #pragma unroll
         for (int c8 = wg * (16 / GK_NWG); c8 < (wg + 1) * (16 / GK_NWG); ++c8) {   // 16-byte chunks in swizzle order
           const uint4 sa = *reinterpret_cast<const uint4*>(sm + GK_S + sw_chunk(row, c8, 128));
@@ -835,10 +841,11 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 fa = __bfloat1622float2(ha[e]), fb = __bfloat1622float2(hb[e]);
-            sd = fmaf(fa.x, fb.x, sd);
-            sd = fmaf(fa.y, fb.y, sd);
+            sda[e] = fmaf(fa.x, fb.x, sda[e]);
+            sda[e] = fmaf(fa.y, fb.y, sda[e]);
           }
         }
+        float sd = (sda[0] + sda[1]) + (sda[2] + sda[3]);
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
         if (lane == 0) sdot[warp] = sd;

@@ -52,10 +52,12 @@ static_assert(PR_SMEM >= 32768, "the [K; Q] tile fits");
 // One block diagonal d of T = (I + A)^-1 (16 x 16 blocks, 64 lanes of one value
 // head): T_ij = -T_ii p with p = sum_{k=j}^{i-1} A_ik T_kj, for the 4 - d blocks
 // (i, j = i - d).  S holds A[r][c] (c < r) at S[c][r] and T[r][c] (c <= r) at
-// S[r][c].  The (4 - d) * 16 columns are spread over 64 lanes as G = 1, 2, 4
-// lanes per column; lane g of a column accumulates rows [16g/G, 16(g+1)/G) of
-// p over the whole k range, the G lanes exchange their rows by shuffles, and
-// each then forms its rows of T_ij.
+// S[r][c]; the upper triangles of the diagonal blocks hold zeros (their A
+// entries are dead once the diagonal blocks are inverted).  The (4 - d) * 16
+// columns are spread over 64 lanes as G = 1, 2, 4 lanes per column; lane g of
+// a column accumulates rows [16g/G, 16(g+1)/G) of p over the whole k range,
+// the G lanes exchange their rows by shuffles, and each then forms its rows
+// of T_ij.
 template <int DL>
 __device__ __forceinline__ void offdiag_level(float* Sm, int l) {
   constexpr int G = DL == 1 ? 1 : (DL == 2 ? 2 : 4);
@@ -70,7 +72,7 @@ __device__ __forceinline__ void offdiag_level(float* Sm, int l) {
   if (act) {
 #pragma unroll 4
     for (int t = 16 * jb; t < oi; ++t) {
-      const float tv = t >= c ? Sm[t * PR_ALD + c] : 0.f;   // T[t][c]
+      const float tv = Sm[t * PR_ALD + c];   // T[t][c] (zero above the diagonal of the diagonal block)
 #pragma unroll
       for (int q = 0; q < R / 4; ++q) {                       // A[oi + r][t] = S[t][oi + r]
         const float4 av = *reinterpret_cast<const float4*>(Sm + t * PR_ALD + oi + g * R + 4 * q);
@@ -82,10 +84,15 @@ __device__ __forceinline__ void offdiag_level(float* Sm, int l) {
     }
   }
   float pf[16];   // the whole p of this column, gathered from the G lanes
+  if constexpr (G == 1) {
 #pragma unroll
-  for (int og = 0; og < G; ++og)
+    for (int r = 0; r < 16; ++r) pf[r] = p[r];
+  } else {
 #pragma unroll
-    for (int r = 0; r < R; ++r) pf[og * R + r] = __shfl_sync(0xffffffffu, p[r], (l & 31 & ~(G - 1)) + og);
+    for (int og = 0; og < G; ++og)
+#pragma unroll
+      for (int r = 0; r < R; ++r) pf[og * R + r] = __shfl_sync(0xffffffffu, p[r], (l & 31 & ~(G - 1)) + og);
+  }
   if (act) {
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) {   // T_ij[r][c] = -sum_{s <= r} T_ii[r][s] p[s]
@@ -93,11 +100,14 @@ __device__ __forceinline__ void offdiag_level(float* Sm, int l) {
       float acc = 0.f;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
+        // T_ii is zero above its diagonal: the terms s > r are skipped where r is known at compile
+        // time (G = 1) and otherwise add zero
+        if (G == 1 && 4 * q > rr) continue;
         const float4 tv4 = *reinterpret_cast<const float4*>(Sm + (oi + r) * PR_ALD + oi + 4 * q);
-        acc = 4 * q + 0 <= r ? fmaf(tv4.x, pf[4 * q + 0], acc) : acc;
-        acc = 4 * q + 1 <= r ? fmaf(tv4.y, pf[4 * q + 1], acc) : acc;
-        acc = 4 * q + 2 <= r ? fmaf(tv4.z, pf[4 * q + 2], acc) : acc;
-        acc = 4 * q + 3 <= r ? fmaf(tv4.w, pf[4 * q + 3], acc) : acc;
+        acc = fmaf(tv4.x, pf[4 * q + 0], acc);
+        if (G > 1 || 4 * q + 1 <= rr) acc = fmaf(tv4.y, pf[4 * q + 1], acc);
+        if (G > 1 || 4 * q + 2 <= rr) acc = fmaf(tv4.z, pf[4 * q + 2], acc);
+        if (G > 1 || 4 * q + 3 <= rr) acc = fmaf(tv4.w, pf[4 * q + 3], acc);
       }
       Sm[(oi + r) * PR_ALD + c] = -acc;
     }
@@ -331,9 +341,9 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
             if (4 * g4 + 3 > jq) x[4 * g4 + 3] = fmaf(-av.w, xj, x[4 * g4 + 3]);
           }
         }
+        __syncwarp();   // every lane of the block has read its A entries
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (i >= cc) Sm[(o + i) * PR_ALD + o + cc] = x[i];
+        for (int i = 0; i < 16; ++i) Sm[(o + i) * PR_ALD + o + cc] = x[i];   // x[i] = 0 above the diagonal
       }
       named_bar(1, 64);
       // off-diagonal blocks, one block diagonal d at a time (then T_ij is complete for i - j = d)
