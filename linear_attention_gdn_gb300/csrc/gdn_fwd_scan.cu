@@ -54,27 +54,26 @@ __device__ __forceinline__ void store_state_row(uint8_t* dst, int row, const flo
 }
 
 // Two warpgroups.  The chain warpgroup (warps 0-3) owns the state and runs
-// only the dependent chain of each chunk:
+// the dependent chain of each chunk:
 //   MMA1 (V_new^T = U^T - S^T W^T) -> V_new hop -> MMA2 (dS^T = (V_new^T
 //   diag(kd)) K, and the output O^T = S^T Q'^T + V_new^T Aqk^T with
-//   Q'_r = gamma_r rq_r q_r, so that o = scale O) -> S hop.
-// The helper warpgroup (warps 4-7) prepares chunk n + 1 while the chain works
-// on chunk n (tile landing, W^T = K^T T'^T and U^T = V^T T''^T, the -W^T
-// tile, Q'), writes the output of chunk n - 1 and streams the tiles in.  They
-// hand off through mbarriers:
+//   Q'_r = gamma_r rq_r q_r, so that o = scale O) -> S hop,
+// and, while MMA1 of chunk n runs, writes the output of chunk n - 1 from its
+// O buffer.  The helper warpgroup (warps 4-7) prepares chunk n + 1 while the
+// chain works on chunk n (tile landing, W^T = K^T T'^T and U^T = V^T T''^T,
+// the -W^T tile, Q') and streams the tiles in.  They hand off through
+// mbarriers:
 //   bar_wr    helper -> chain   -W^T(n), U^T(n), Q'(n) are ready
 //   bar_m1    MMA1(n) done      (chain: V_new; helper: -W^T tile and D1 reuse)
 //   bar_m2    MMA2(n) done      (chain: S)
-//   bar_o[b]  MMA2(n) done      (helper: output(n) from O buffer b = n & 1)
-//   bar_of[b] helper -> chain   O buffer b has been read out (MMA2(n + 2) may write it)
+//   bar_o[b]  MMA2(n) done      (chain: output(n) from O buffer b = n & 1)
 //   bar_sf    chain -> helper   chunk n's stage is no longer read (V_new^T copy)
 // Each completes once per use, and no waiter can fall two phases behind.
 __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_constant__ ScanArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
-  __shared__ uint64_t full_bar[2], bar_wr, bar_m1, bar_wu, bar_m2, bar_o[2], bar_of[2], bar_sf;
+  __shared__ uint64_t full_bar[2], bar_wr, bar_m1, bar_wu, bar_m2, bar_o[2], bar_sf;
   __shared__ uint32_t tslot;
-  __shared__ int side[2][CH + 4];     // L of chunks n - 1, n: it outlives their stage
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int lt = tid & 127;      // row within the warpgroup = TMEM lane
   const int wq = warp & 3;       // the warp's TMEM lane quarter
@@ -127,8 +126,6 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
     mbar_init(&bar_m2, 1);
     mbar_init(&bar_o[0], 1);
     mbar_init(&bar_o[1], 1);
-    mbar_init(&bar_of[0], 1);
-    mbar_init(&bar_of[1], 1);
     mbar_init(&bar_sf, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
@@ -183,6 +180,36 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
   if (chain) {
     // =================== chain warpgroup ===================
     const uint32_t sm_s = smem_u32(s_tile), sm_w = smem_u32(sm + SC_W);
+    uint8_t* o_stage = sm + SC_O;
+    // the output of chunk m from its O buffer (TMEM), o = scale O; thread 32 owns the staging tile's copies
+    auto output = [&](int m) {
+      const int L = a.chunk_len[c0 + m];
+      if (tid == 32) bulk_wait_read();   // the previous output store has read the staging tile
+      named_bar(1, 128);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float x[32];
+        tmem_ld32(taddr(tb, wq * 32, TM_O + (m & 1) * 64 + h * 32), x);
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          *reinterpret_cast<__nv_bfloat16*>(o_stage + sw_off(h * 32 + e, lt, 64)) = __float2bfloat16_rn(a.scale * x[e]);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      named_bar(1, 128);
+      const int t0 = a.chunk_tok0[c0 + m];
+      if (L < CH) {  // ragged last chunk: only its own rows (the next rows are another document's)
+        for (int idx = lt; idx < L * 16; idx += 128) {
+          const int r = idx >> 4, c8 = idx & 15;
+          *reinterpret_cast<uint4*>(a.o + ((size_t)(t0 + r) * a.HV + hv) * D + c8 * 8) =
+              *reinterpret_cast<const uint4*>(o_stage + sw_chunk(r, c8, 64));
+        }
+      } else if (tid == 32) {
+        tma_store_3d(&a.to, o_stage, 0, hv, t0);
+        tma_store_3d(&a.to, o_stage + 8192, 64, hv, t0);
+        bulk_commit();
+      }
+    };
     for (int n = 0; n < nch && ok; ++n) {
       const uint32_t par = n & 1;
       uint8_t* st = sm + (n & 1) * SC_STAGE;
@@ -202,6 +229,11 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
           bulk_wait_read_but1();
           mbar_arrive(&bar_sf);
         }
+      }
+      if (with_o && n > 0) {   // the output of chunk n - 1, while MMA1 runs
+        if (!(ok = wg_sync_and(1, mbar_wait(&bar_o[(n - 1) & 1], ((n - 1) >> 1) & 1, a.err)))) break;
+        tc_fence_after();
+        output(n - 1);
       }
       ok = wg_sync_and(1, mbar_wait(&bar_m1, par, a.err));
       if (!ok) break;
@@ -238,28 +270,24 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
           bulk_store(a.vn + ((size_t)(c0 + n) * a.HV + hv) * VN_BYTES, st + SC_V, VN_BYTES);
           bulk_commit();
         }
-        // the output of chunk n - 2 has been read out of this O buffer
-        const bool go = !(with_o && n > 1) || mbar_wait(&bar_of[n & 1], ((n >> 1) - 1) & 1, a.err);
-        tc_fence_after();
-        if (go) {
+        // (the O buffer n & 1 was read out by output(n - 2) in this warpgroup's previous step)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_ts_w(tb + TM_DS, tb + TM_AVS + ks * 8, desc_mn(a_k, 64, ks), idesc(128, 128, 0, 1), ks > 0);
+        mma_commit_w(&bar_m2);
+        if (lane == 0) {   // this chunk's tape entry has been read: the S^T tile may be rewritten
+          if (with_vn) bulk_wait_read_but1();   // (the V_new^T copy just committed may still be reading)
+          else bulk_wait_read();
+        }
+        if (with_o) {
+          const uint32_t to = tb + TM_O + (n & 1) * 64;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ss_w(to, desc_k(sm_s, 128, ks), desc_k(a_q, 64, ks), idesc(128, 64, 0, 0), ks > 0);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma_ts_w(tb + TM_DS, tb + TM_AVS + ks * 8, desc_mn(a_k, 64, ks), idesc(128, 128, 0, 1), ks > 0);
-          mma_commit_w(&bar_m2);
-          if (lane == 0) {   // this chunk's tape entry has been read: the S^T tile may be rewritten
-            if (with_vn) bulk_wait_read_but1();   // (the V_new^T copy just committed may still be reading)
-            else bulk_wait_read();
-          }
-          if (with_o) {
-            const uint32_t to = tb + TM_O + (n & 1) * 64;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              mma_ss_w(to, desc_k(sm_s, 128, ks), desc_k(a_q, 64, ks), idesc(128, 64, 0, 0), ks > 0);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_ts_w(to, tb + TM_AVN + ks * 8, desc_k(a_aqk, 64, ks), idesc(128, 64, 0, 0), 1u);
-            mma_commit_w(&bar_o[n & 1]);
-          }
+            mma_ts_w(to, tb + TM_AVN + ks * 8, desc_k(a_aqk, 64, ks), idesc(128, 64, 0, 0), 1u);
+          mma_commit_w(&bar_o[n & 1]);
         }
       }
       ok = wg_sync_and(1, mbar_wait(&bar_m2, par, a.err));
@@ -286,7 +314,12 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
         bulk_commit();
       }
     }
-    if (tid == 0) bulk_wait_all();
+    if (ok && with_o && nch > 0) {   // the last chunk's output
+      ok = wg_sync_and(1, mbar_wait(&bar_o[(nch - 1) & 1], ((nch - 1) >> 1) & 1, a.err));
+      tc_fence_after();
+      if (ok) output(nch - 1);
+    }
+    if (tid == 0 || tid == 32) bulk_wait_all();
     if (ok && mode != 0) {
       float* dst = (mode == 1 ? a.bend : a.mend) + ((size_t)split * a.HV + hv) * STATE_F32 + (size_t)lt * 128;
 #pragma unroll
@@ -295,37 +328,6 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
     }
   } else {
     // =================== helper warpgroup ===================
-    uint8_t* o_stage = sm + SC_O;
-    // output of chunk n from O1, O2 (TMEM) with the saved per-token scales
-    auto output = [&](int n) {
-      const int L = side[n & 1][CH];
-      if (tid == 128) bulk_wait_read();   // the previous output store has read the staging tile
-      named_bar(2, 128);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float x[32];
-        tmem_ld32(taddr(tb, wq * 32, TM_O + (n & 1) * 64 + h * 32), x);
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          *reinterpret_cast<__nv_bfloat16*>(o_stage + sw_off(h * 32 + e, lt, 64)) = __float2bfloat16_rn(a.scale * x[e]);
-      }
-      fence_async_smem();
-      tc_fence_before();
-      named_bar(2, 128);
-      if (tid == 128) mbar_arrive(&bar_of[n & 1]);   // this O buffer may be rewritten
-      const int t0 = a.chunk_tok0[c0 + n];
-      if (L < CH) {  // ragged last chunk: only its own rows (the next rows are another document's)
-        for (int idx = lt; idx < L * 16; idx += 128) {
-          const int r = idx >> 4, c8 = idx & 15;
-          *reinterpret_cast<uint4*>(a.o + ((size_t)(t0 + r) * a.HV + hv) * D + c8 * 8) =
-              *reinterpret_cast<const uint4*>(o_stage + sw_chunk(r, c8, 64));
-        }
-      } else if (tid == 128) {
-        tma_store_3d(&a.to, o_stage, 0, hv, t0);
-        tma_store_3d(&a.to, o_stage + 8192, 64, hv, t0);
-        bulk_commit();
-      }
-    };
     for (int n = 0; n < nch && ok; ++n) {
       // ---- chunk n: land its tiles, W^T = K^T T'^T -> DW, U^T = V^T T''^T -> D1[n & 1], -W^T -> shared
       uint8_t* st = sm + (n & 1) * SC_STAGE;
@@ -359,7 +361,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
         }
         mma_commit_w(&bar_wu);
       }
-      if (with_o) {   // Q'_r = gamma_r rq_r q_r = (sc_r / scale) q_r in place; L for the output copy
+      if (with_o) {   // Q'_r = gamma_r rq_r q_r = (sc_r / scale) q_r in place
         const float* scal = reinterpret_cast<const float*>(st + SC_SCAL);
         const int r = lt >> 1;
         const float f = scal[r] * (1.0f / a.scale);
@@ -375,7 +377,6 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
           }
           *p = v;
         }
-        if (lt == 0) side[n & 1][CH] = L;
       }
       if (!(ok = wg_sync_and(2, mbar_wait(&bar_wu, n & 1, a.err)))) break;
       tc_fence_after();
@@ -406,19 +407,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
           if (n + 2 < nch) prefetch(n + 2);
         }
       }
-      // ---- the output of chunk n - 1
-      if (with_o && n > 0) {
-        if (!(ok = wg_sync_and(2, mbar_wait(&bar_o[(n - 1) & 1], ((n - 1) >> 1) & 1, a.err)))) break;
-        tc_fence_after();
-        output(n - 1);
-      }
     }
-    if (ok && with_o && nch > 0) {
-      ok = wg_sync_and(2, mbar_wait(&bar_o[(nch - 1) & 1], ((nch - 1) >> 1) & 1, a.err));
-      tc_fence_after();
-      if (ok) output(nch - 1);
-    }
-    if (tid == 128) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
