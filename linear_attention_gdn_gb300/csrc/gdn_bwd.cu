@@ -123,8 +123,9 @@ __device__ __forceinline__ float ld_bf16(const uint8_t* tile, int r, int c, int 
 __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant__ BScanArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
-  __shared__ uint64_t full_bar[2], mma_bar;
+  __shared__ uint64_t full_bar[2], mma_bar, bar_pre;
   __shared__ uint32_t tslot;
+  __shared__ int pre_next;   // the next iteration's W^T / X MMAs went out under this one's MMA2
   const int tid = threadIdx.x, warp = tid >> 5;
   if (*(volatile int*)a.err) return;
 
@@ -156,7 +157,9 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
     mbar_init(&full_bar[0], 1);
     mbar_init(&full_bar[1], 1);
     mbar_init(&mma_bar, 1);
+    mbar_init(&bar_pre, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
+    pre_next = 0;
   }
   fence_async_smem();
   tc_fence_before();
@@ -165,36 +168,59 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
   const uint32_t tb = tslot;
 
   // iteration `it` processes chunk c0 + nch - 1 - it
-  auto issue = [&](int it) {
+  // The tiles of iteration `it` in two parts on one barrier: everything but Q (`part` 0: the
+  // stage's K, dO, T', Aqk, scalars are dead once MMA2 has been issued) and Q (`part` 1: MMA2
+  // reads it).  Part 0 sets the barrier's byte count for both.
+  auto issue = [&](int it, int part) {
     const int ci = c0 + nch - 1 - it;
     uint8_t* st = sm + (it & 1) * BS_STAGE;
     uint64_t* bar = &full_bar[it & 1];
     const int t0 = a.chunk_tok0[ci];
-    const uint8_t* cbp = a.cb + ((size_t)ci * a.HV + hv) * CB_BYTES;
-    mbar_expect_tx(bar, (uint32_t)BS_STAGE);
-    tma_load_3d(st + BS_K, &a.tk, 0, kh, t0, bar);
-    tma_load_3d(st + BS_K + 8192, &a.tk, 64, kh, t0, bar);
-    tma_load_3d(st + BS_Q, &a.tq, 0, kh, t0, bar);
-    tma_load_3d(st + BS_Q + 8192, &a.tq, 64, kh, t0, bar);
-    tma_load_3d(st + BS_DO, &a.tdo, 0, hv, t0, bar);
-    tma_load_3d(st + BS_DO + 8192, &a.tdo, 64, hv, t0, bar);
-    bulk_load(st + BS_TP, cbp + CB_TP, TILE64_BYTES, bar);
-    bulk_load(st + BS_AQK, cbp + CB_AQK, TILE64_BYTES, bar);
-    bulk_load(st + BS_SCAL, cbp + CB_SCAL, CB_SCAL_BYTES, bar);
+    if (part == 0) {
+      const uint8_t* cbp = a.cb + ((size_t)ci * a.HV + hv) * CB_BYTES;
+      mbar_expect_tx(bar, (uint32_t)BS_STAGE);
+      tma_load_3d(st + BS_K, &a.tk, 0, kh, t0, bar);
+      tma_load_3d(st + BS_K + 8192, &a.tk, 64, kh, t0, bar);
+      tma_load_3d(st + BS_DO, &a.tdo, 0, hv, t0, bar);
+      tma_load_3d(st + BS_DO + 8192, &a.tdo, 64, hv, t0, bar);
+      bulk_load(st + BS_TP, cbp + CB_TP, TILE64_BYTES, bar);
+      bulk_load(st + BS_AQK, cbp + CB_AQK, TILE64_BYTES, bar);
+      bulk_load(st + BS_SCAL, cbp + CB_SCAL, CB_SCAL_BYTES, bar);
+    } else {
+      tma_load_3d(st + BS_Q, &a.tq, 0, kh, t0, bar);
+      tma_load_3d(st + BS_Q + 8192, &a.tq, 64, kh, t0, bar);
+    }
   };
   if (tid == 0) {
-    if (nch > 0) issue(0);
-    if (nch > 1) issue(1);
+    if (nch > 0) {
+      issue(0, 0);
+      issue(0, 1);
+    }
+    if (nch > 1) {
+      issue(1, 0);
+      issue(1, 1);
+    }
   }
-  uint32_t mph = 0;
-  bool ok = true;
+  uint32_t mph = 0, pph = 0;
+  bool ok = true, pend = false;   // pend: W^T / X MMAs issued by thread 32 and not yet waited for
   const uint32_t sm_ds = smem_u32(ds_tile), sm_w = smem_u32(sm + BS_W);
+  // W^T = K^T T'^T and X = dO^T Aqk^T of the chunk in stage `st` (they need no state)
+  auto issue_wx = [&](const uint8_t* st) {
+    const uint32_t a_k = smem_u32(st + BS_K), a_do = smem_u32(st + BS_DO);
+    const uint32_t a_tp = smem_u32(st + BS_TP), a_aqk = smem_u32(st + BS_AQK);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma_ss(tb + BT_DW, desc_mn(a_k, 64, ks), desc_k(a_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma_ss(tb + BT_DX, desc_mn(a_do, 64, ks), desc_mn(a_aqk, 64, ks), idesc(128, 64, 1, 1), ks > 0);
+  };
   for (int it = 0; it < nch && ok; ++it) {
     const int ci = c0 + nch - 1 - it;
     uint8_t* st = sm + (it & 1) * BS_STAGE;
-    const uint32_t a_k = smem_u32(st + BS_K), a_q = smem_u32(st + BS_Q), a_do = smem_u32(st + BS_DO);
-    const uint32_t a_tp = smem_u32(st + BS_TP), a_aqk = smem_u32(st + BS_AQK);
+    const uint32_t a_k = smem_u32(st + BS_K), a_q = smem_u32(st + BS_Q);
     const float* scal = reinterpret_cast<const float*>(st + BS_SCAL);
+    const bool pre = pre_next;   // written before the last barrier of the previous iteration
     ok = __syncthreads_and(mbar_wait(&full_bar[it & 1], (it >> 1) & 1, a.err));
     if (!ok) break;
     const int L = reinterpret_cast<const int*>(scal)[129];
@@ -214,16 +240,12 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
         bulk_store(a.dtape + ((size_t)ci * a.HV + hv) * STATE_BYTES, ds_tile, STATE_BYTES);
         bulk_commit();
       }
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tb + BT_DW, desc_mn(a_k, 64, ks), desc_k(a_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tb + BT_DX, desc_mn(a_do, 64, ks), desc_mn(a_aqk, 64, ks), idesc(128, 64, 1, 1), ks > 0);
+      if (!pre) issue_wx(st);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
         mma_ss(tb + BT_DY, desc_k(sm_ds, 128, ks), desc_k(a_k, 64, ks), idesc(128, 64, 0, 0), ks > 0);
       mma_commit(&mma_bar);
+      bulk_wait_read_but1();   // the last dV_new^T copy has read its tile (rewritten by the hop below)
     }
     {  // (P gamma_r rq_r dO[r][tid]) -> TMEM A operand, while the MMAs run
 #pragma unroll
@@ -237,8 +259,12 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
         tmem_st8(taddr(tb, warp * 32, BT_ADO + q * 8), p8);
       }
     }
-    ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
+    ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err) && (!pre || mbar_wait(&bar_pre, pph, a.err)));
     mph ^= 1;
+    if (pre) {
+      pph ^= 1;
+      pend = false;
+    }
     if (!ok) break;
     tc_fence_after();
     {
@@ -280,6 +306,7 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
       }
       tmem_wait_st();
     }
+    const float gL = scal[128];   // read before the barrier after which the stage is refilled
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -296,14 +323,29 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
       for (int ks = 0; ks < 4; ++ks)
         mma_ts(tb + BT_DS, tb + BT_ADO + ks * 8, desc_mn(a_q, 64, ks), idesc(128, 128, 0, 1), 1u);
       mma_commit(&mma_bar);
-      bulk_wait_read();   // the tape copies have read the dS'^T and dV_new^T tiles rewritten next
+      bulk_wait_read_but1();   // the tape copy has read the dS'^T tile (rewritten below)
+    }
+    if (tid == 64 && it + 2 < nch) issue(it + 2, 0);   // the stage's K, dO, T', Aqk, scalars are dead
+    if (tid == 32) {   // the next chunk's W^T and X, under MMA2, when its tiles are in and need no zeroing
+      int nx = 0;
+      if (it + 1 < nch) {
+        const uint8_t* st1 = sm + ((it + 1) & 1) * BS_STAGE;
+        if (mbar_wait(&full_bar[(it + 1) & 1], ((it + 1) >> 1) & 1, a.err) &&
+            reinterpret_cast<const int*>(st1 + BS_SCAL)[129] == CH) {
+          tc_fence_after();
+          issue_wx(st1);
+          mma_commit(&bar_pre);
+          nx = 1;
+          pend = true;
+        }
+      }
+      pre_next = nx;
     }
     ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
     mph ^= 1;
     if (!ok) break;
     tc_fence_after();
     {
-      const float gL = scal[128];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         float x[32];
@@ -316,9 +358,10 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && it + 2 < nch) issue(it + 2);
+    if (tid == 0 && it + 2 < nch) issue(it + 2, 1);   // MMA2 is done with Q
   }
   if (tid == 0) bulk_wait_all();
+  if (tid == 32 && pend) mbar_wait(&bar_pre, pph, a.err);   // no MMA may outlive the TMEM allocation
   if (ok && a.walk) {
     float* dst = a.dbend + ((size_t)split * a.HV + hv) * STATE_F32 + (size_t)tid * 128;
 #pragma unroll
