@@ -286,11 +286,13 @@ def run_ours(args, rank, world, local_rank):
     n_launch = sum(v["launches"] for v in launches.values())
     n_launch = int(round(n_launch * args.steps / (args.steps + args.warmup)))
 
-    # per-kernel device times over a second timed pass with launch events
+    # per-kernel device times over a second timed pass with launch events (its warm-up step included:
+    # every step of the pass is recorded)
     gdn.gdn_profile_enable(1)
     timed(op, args.steps, 1)
     gdn.gdn_profile_enable(0)
     kstats = gdn.gdn_profile_read_all()
+    prof_steps = args.steps + 1
 
     extra = {}
     if not args.quick:
@@ -405,8 +407,8 @@ def run_ours(args, rank, world, local_rank):
     kernels = {}
     for k, v in kt.items():
         f, b = kernel_flops(k, w), kernel_bytes(k, w)
-        kernels[k] = {"launches_per_step": round(v["launches"] / args.steps, 2),
-                      "ms_per_step": round(v["total_ms"] / args.steps, 4), "share": round(v["total_ms"] / tot, 4),
+        kernels[k] = {"launches_per_step": round(v["launches"] / prof_steps, 2),
+                      "ms_per_step": round(v["total_ms"] / prof_steps, 4), "share": round(v["total_ms"] / tot, 4),
                       "TFLOP_per_s": round(f * v["timed_launches"] / v["total_ms"] / 1e9, 1) if f else None,
                       "GB_per_s": round(b * v["timed_launches"] / v["total_ms"] / 1e6, 1) if b else None}
     tflops = world * step_flops(w, op) / ms / 1e9
