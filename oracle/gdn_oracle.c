@@ -22,10 +22,17 @@
  * in-kernel q/k L2 norm).  One q/k head serves G = HV/H consecutive value heads
  * (v-head h reads q/k head h / G).
  *
+ * Optionally the document starts from a given state S_0 = S_in instead of
+ * zero and its last state S_L is returned (S_out); the backward then starts
+ * from a given dS_L = dS_out (the gradient of the loss with respect to S_out,
+ * zero if absent) and returns dS_0, the gradient with respect to S_in.  These
+ * are the per-document boundary states that a document split across calls
+ * (or across devices) passes on.
+ *
  * The backward is reverse-mode differentiation of the loop above written out
  * by hand, one token at a time, from the last token of the document to the
- * first.  dS is the gradient with respect to S_t; it starts at zero after the
- * last token (no final state is an output):
+ * first.  dS is the gradient with respect to S_t; it starts at dS_out (zero
+ * without one) after the last token:
  *
  *   dS   += scale q^_t do_t^T            dq^_t += scale S_t do_t
  *   dk^_t += dS u_t        du = dS^T k^_t       da = <dS, S_{t-1}>
@@ -93,27 +100,45 @@ static void token_out(const double *S, int dk, int dv, const double *qh, double 
 }
 
 /*
- * gdn_oracle_group: forward (and, if dout != NULL, backward) of one document
- * segment for one q/k head and its G value heads.
+ * gdn_oracle_group_states: forward (and, if dout != NULL, backward) of one
+ * document segment for one q/k head and its G value heads.
  *
  *   q, k    [L][dk]        v, dout, o, dv_out  [G][L][dv]
  *   g, beta [G][L]         dg, dbeta          [G][L]
  *   dq, dk_out [L][dk]     (sums over the group, after the norm backward)
  *   s_chunk  optional [ceil(L/chunk)][G][dk][dv]: the state entering each
- *            chunk of `chunk` tokens (chunk 0 enters with zero)
+ *            chunk of `chunk` tokens (chunk 0 enters with S_in)
+ *   s_in, ds_out  optional [G][dk][dv]: the state entering the segment and
+ *            the gradient with respect to the state leaving it (zero if NULL)
+ *   s_out, ds_in  optional [G][dk][dv]: the state leaving the segment and
+ *            the gradient with respect to s_in (ds_in needs dout)
  *
  * Returns 0 on success, -1 if memory could not be allocated, -2 on bad sizes.
  */
-int gdn_oracle_group(int L, int dk, int dv, int G,
-                     const double *q, const double *k, const double *v,
-                     const double *g, const double *beta, const double *dout,
-                     int l2norm, double eps, double scale,
-                     double *o, double *dq, double *dk_out, double *dv_out,
-                     double *dg, double *dbeta, double *s_chunk, int chunk)
+int gdn_oracle_group_states(int L, int dk, int dv, int G,
+                            const double *q, const double *k, const double *v,
+                            const double *g, const double *beta, const double *dout,
+                            int l2norm, double eps, double scale,
+                            double *o, double *dq, double *dk_out, double *dv_out,
+                            double *dg, double *dbeta, double *s_chunk, int chunk,
+                            const double *s_in, double *s_out, const double *ds_out,
+                            double *ds_in)
 {
-    if (L < 0 || dk <= 0 || dv <= 0 || G <= 0 || (s_chunk && chunk <= 0)) return -2;
-    if (L == 0) return 0;
+    if (L < 0 || dk <= 0 || dv <= 0 || G <= 0 || (s_chunk && chunk <= 0) || (ds_in && !dout)) return -2;
     const size_t SD = (size_t)dk * dv;
+    if (L == 0) {   /* nothing happens: the state passes through, and so does its gradient */
+        for (int h = 0; h < G; ++h) {
+            if (s_out) {
+                if (s_in) memcpy(s_out + h * SD, s_in + h * SD, sizeof(double) * SD);
+                else memset(s_out + h * SD, 0, sizeof(double) * SD);
+            }
+            if (ds_in) {
+                if (ds_out) memcpy(ds_in + h * SD, ds_out + h * SD, sizeof(double) * SD);
+                else memset(ds_in + h * SD, 0, sizeof(double) * SD);
+            }
+        }
+        return 0;
+    }
     const int nblk = (L + CK - 1) / CK;
     double *qh = malloc(sizeof(double) * (size_t)L * dk);
     double *kh = malloc(sizeof(double) * (size_t)L * dk);
@@ -147,7 +172,8 @@ int gdn_oracle_group(int L, int dk, int dv, int G,
         double *oh = o + (size_t)h * L * dv;
 
         /* ---- forward ---- */
-        memset(S, 0, sizeof(double) * SD);
+        if (s_in) memcpy(S, s_in + (size_t)h * SD, sizeof(double) * SD);
+        else memset(S, 0, sizeof(double) * SD);
         for (int t = 0; t < L; ++t) {
             if (ckpt && t % CK == 0) memcpy(ckpt + (size_t)(t / CK) * SD, S, sizeof(double) * SD);
             if (s_chunk && t % chunk == 0)
@@ -155,6 +181,7 @@ int gdn_oracle_group(int L, int dk, int dv, int G,
             token_step(S, dk, dv, kh + (size_t)t * dk, vh + (size_t)t * dv, exp(gh[t]), bh[t], p, u);
             token_out(S, dk, dv, qh + (size_t)t * dk, scale, oh + (size_t)t * dv);
         }
+        if (s_out) memcpy(s_out + (size_t)h * SD, S, sizeof(double) * SD);
         if (!dout) continue;
 
         /* ---- backward, block by block from the end ---- */
@@ -162,7 +189,8 @@ int gdn_oracle_group(int L, int dk, int dv, int G,
         double *dvh = dv_out + (size_t)h * L * dv;
         double *dgh = dg + (size_t)h * L;
         double *dbh = dbeta + (size_t)h * L;
-        memset(dS, 0, sizeof(double) * SD);
+        if (ds_out) memcpy(dS, ds_out + (size_t)h * SD, sizeof(double) * SD);
+        else memset(dS, 0, sizeof(double) * SD);
         for (int bi = nblk - 1; bi >= 0; --bi) {
             const int t0 = bi * CK;
             const int t1 = (t0 + CK < L) ? t0 + CK : L;
@@ -232,6 +260,7 @@ int gdn_oracle_group(int L, int dk, int dv, int G,
                 dgh[t] = a * da;
             }
         }
+        if (ds_in) memcpy(ds_in + (size_t)h * SD, dS, sizeof(double) * SD);   /* dS_0 */
     }
 
     if (dout) {
@@ -257,4 +286,16 @@ done:
     free(qh); free(kh); free(nq); free(nk); free(S); free(ckpt); free(blk); free(dS);
     free(dqh); free(dkh); free(p); free(u); free(du); free(dp);
     return rc;
+}
+
+/* The same with zero boundary states and none returned. */
+int gdn_oracle_group(int L, int dk, int dv, int G,
+                     const double *q, const double *k, const double *v,
+                     const double *g, const double *beta, const double *dout,
+                     int l2norm, double eps, double scale,
+                     double *o, double *dq, double *dk_out, double *dv_out,
+                     double *dg, double *dbeta, double *s_chunk, int chunk)
+{
+    return gdn_oracle_group_states(L, dk, dv, G, q, k, v, g, beta, dout, l2norm, eps, scale, o, dq,
+                                   dk_out, dv_out, dg, dbeta, s_chunk, chunk, NULL, NULL, NULL, NULL);
 }

@@ -56,6 +56,8 @@ def lib():
         L.gdn_oracle_group.restype = ctypes.c_int
         L.gdn_oracle_group.argtypes = [ctypes.c_int] * 4 + [dp] * 6 + [
             ctypes.c_int, ctypes.c_double, ctypes.c_double] + [dp] * 7 + [ctypes.c_int]
+        L.gdn_oracle_group_states.restype = ctypes.c_int
+        L.gdn_oracle_group_states.argtypes = L.gdn_oracle_group.argtypes + [dp] * 4
         _lib = L
     return _lib
 
@@ -68,13 +70,15 @@ def _p(a):
 
 
 def group(q, k, v, g, beta, dO=None, *, l2norm=True, scale=128 ** -0.5, eps=EPS,
-          chunk_states=False, chunk=64):
+          chunk_states=False, chunk=64, s_in=None, ds_out=None, states=False):
     """Forward (+ backward if dO is given) of one document segment, one group.
 
     q, k [L, dk]; v [G, L, dv]; g, beta [G, L]; dO [G, L, dv]; all float64.
+    s_in, ds_out [G, dk, dv] (optional): the state entering the segment and the
+    gradient with respect to the state leaving it.
     Returns a dict with o [G,L,dv] and, with dO: dq, dk [L,dk], dv [G,L,dv],
     dg, dbeta [G,L]; with chunk_states: S [nchunks, G, dk, dv] entering each
-    chunk."""
+    chunk; with states: s_out [G,dk,dv] and, with dO, ds_in [G,dk,dv]."""
     q, k, v, g, beta = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v, g, beta))
     L, dk = q.shape
     G, _, dv = v.shape
@@ -85,13 +89,20 @@ def group(q, k, v, g, beta, dO=None, *, l2norm=True, scale=128 ** -0.5, eps=EPS,
                    dg=np.zeros((G, L)), dbeta=np.zeros((G, L)))
     if chunk_states:
         out["S"] = np.zeros(((L + chunk - 1) // chunk, G, dk, dv))
-    rc = lib().gdn_oracle_group(L, dk, dv, G, _p(q), _p(k), _p(v), _p(g), _p(beta), _p(dO),
-                                int(bool(l2norm)), float(eps), float(scale), _p(out["o"]),
-                                _p(out.get("dq")), _p(out.get("dk")), _p(out.get("dv")),
-                                _p(out.get("dg")), _p(out.get("dbeta")), _p(out.get("S")),
-                                int(chunk))
+    if states:
+        out["s_out"] = np.zeros((G, dk, dv))
+        if dO is not None:
+            out["ds_in"] = np.zeros((G, dk, dv))
+    s_in = None if s_in is None else np.ascontiguousarray(s_in, dtype=np.float64).reshape(G, dk, dv)
+    ds_out = None if ds_out is None else np.ascontiguousarray(ds_out, dtype=np.float64).reshape(G, dk, dv)
+    rc = lib().gdn_oracle_group_states(L, dk, dv, G, _p(q), _p(k), _p(v), _p(g), _p(beta), _p(dO),
+                                       int(bool(l2norm)), float(eps), float(scale), _p(out["o"]),
+                                       _p(out.get("dq")), _p(out.get("dk")), _p(out.get("dv")),
+                                       _p(out.get("dg")), _p(out.get("dbeta")), _p(out.get("S")),
+                                       int(chunk), _p(s_in), _p(out.get("s_out")), _p(ds_out),
+                                       _p(out.get("ds_in")))
     if rc != 0:
-        raise RuntimeError(f"gdn_oracle_group failed ({rc})")
+        raise RuntimeError(f"gdn_oracle_group_states failed ({rc})")
     return out
 
 
@@ -135,10 +146,14 @@ def window(g_doc: np.ndarray, t0: int, t1: int, warm: int, chunk: int = 64, tol:
 
 
 def run(inputs: dict, H: int, HV: int, *, l2norm: bool, scale: float, units=None,
-        with_grad: bool = True, chunk_states: bool = False, threads: int | None = None):
+        with_grad: bool = True, chunk_states: bool = False, threads: int | None = None,
+        states: bool = False):
     """Run the oracle over `units` (default: every document x group, whole
     documents).  `inputs` holds q, k, v, g, beta, dO (torch or numpy, token
-    major) and cu_seqlens.  Returns a list of (Unit, result dict)."""
+    major) and cu_seqlens, and optionally the per-document boundary states
+    s_in, ds_out [N, HV, dk, dv] (whole-document units only).  With `states`
+    each result also holds s_out and (with gradients) ds_in of its group.
+    Returns a list of (Unit, result dict)."""
     cu = np.asarray(inputs["cu_seqlens"], dtype=np.int64)
     G = HV // H
     if units is None:
@@ -158,8 +173,13 @@ def run(inputs: dict, H: int, HV: int, *, l2norm: bool, scale: float, units=None
         g = _f64(inputs["g"][s:e, hs]).T.copy()
         beta = _f64(inputs["beta"][s:e, hs]).T.copy()
         dO = _f64(inputs["dO"][s:e, hs]).transpose(1, 0, 2).copy() if with_grad else None
+        bnd = {}
+        for name in ("s_in", "ds_out"):
+            if inputs.get(name) is not None:
+                assert u.a == 0 and u.b == int(cu[u.doc + 1] - cu[u.doc]), "boundary states need whole documents"
+                bnd[name] = _f64(inputs[name][u.doc, hs])
         return u, group(q, k, v, g, beta, dO, l2norm=l2norm, scale=scale,
-                        chunk_states=chunk_states)
+                        chunk_states=chunk_states, states=states, **bnd)
 
     nthr = threads or os.cpu_count() or 1
     if nthr == 1 or len(units) == 1:
@@ -168,16 +188,25 @@ def run(inputs: dict, H: int, HV: int, *, l2norm: bool, scale: float, units=None
         return list(ex.map(job, units))
 
 
-def assemble(results, T: int, H: int, HV: int, dk: int, dv: int, cu, with_grad=True):
+def assemble(results, T: int, H: int, HV: int, dk: int, dv: int, cu, with_grad=True, states=False):
     """Scatter whole-document unit results into token-major FP64 arrays
-    o [T,HV,dv], dq/dk [T,H,dk], dv [T,HV,dv], dg/dbeta [T,HV]."""
+    o [T,HV,dv], dq/dk [T,H,dk], dv [T,HV,dv], dg/dbeta [T,HV], and with
+    `states` the per-document s_out (and ds_in) [N,HV,dk,dv]."""
     cu = np.asarray(cu, dtype=np.int64)
     G = HV // H
     out = dict(o=np.zeros((T, HV, dv)))
     if with_grad:
         out.update(dq=np.zeros((T, H, dk)), dk=np.zeros((T, H, dk)), dv=np.zeros((T, HV, dv)),
                    dg=np.zeros((T, HV)), dbeta=np.zeros((T, HV)))
+    if states:
+        out["s_out"] = np.zeros((len(cu) - 1, HV, dk, dv))
+        if with_grad:
+            out["ds_in"] = np.zeros((len(cu) - 1, HV, dk, dv))
     for u, r in results:
+        if states:
+            out["s_out"][u.doc, u.j * G:(u.j + 1) * G] = r["s_out"]
+            if with_grad:
+                out["ds_in"][u.doc, u.j * G:(u.j + 1) * G] = r["ds_in"]
         s = int(cu[u.doc]) + u.a
         w0, w1 = s + (u.t0 - u.a), s + (u.t1 - u.a)
         r0, r1 = u.t0 - u.a, u.t1 - u.a

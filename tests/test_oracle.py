@@ -236,3 +236,80 @@ def test_chunk_tables_enumeration():
     assert t["chunk_doc"].tolist() == [1, 2, 3, 3, 3]
     assert t["chunk_tok0"].tolist() == [0, 64, 65, 129, 193]
     assert t["chunk_len"].tolist() == [64, 1, 64, 64, 7]
+
+
+# ---------------------------------------------------------------------------
+# per-document boundary states (S_in / S_out and their gradients)
+# ---------------------------------------------------------------------------
+def full_states(inp, H, HV, l2norm, scale, with_grad=True):
+    T, _, dk = inp["q"].shape
+    dv = inp["v"].shape[2]
+    res = ref.run(inp, H, HV, l2norm=l2norm, scale=scale, with_grad=with_grad, threads=1, states=True)
+    return ref.assemble(res, T, H, HV, dk, dv, inp["cu_seqlens"], with_grad=with_grad, states=True)
+
+
+@pytest.mark.parametrize("l2norm", [True, False])
+@pytest.mark.parametrize("m", [1, 33, 64, 69])
+def test_boundary_states_split(l2norm, m):
+    """A document cut at token m and run as two segments, the second starting
+    from the first one's S_out (forward) and the first ending on the second
+    one's dS_in (backward), gives the whole document's outputs, gradients and
+    final state bit for bit: the boundary states carry exactly what the zero-
+    start whole-document oracle (pinned above) passes from token m-1 to m."""
+    rng = np.random.default_rng(40 + m)
+    G, dk, dv, L = 2, 8, 6, 70
+    q, k = rng.standard_normal((L, dk)), rng.standard_normal((L, dk))
+    v, dO = rng.standard_normal((G, L, dv)), rng.standard_normal((G, L, dv))
+    g, b = -rng.uniform(0.01, 0.3, (G, L)), rng.uniform(0.0, 1.0, (G, L))
+    kw = dict(l2norm=l2norm, scale=0.4, states=True)
+    whole = ref.group(q, k, v, g, b, dO, **kw)
+    second = ref.group(q[m:], k[m:], v[:, m:], g[:, m:], b[:, m:], dO[:, m:],
+                       s_in=ref.group(q[:m], k[:m], v[:, :m], g[:, :m], b[:, :m], **kw)["s_out"], **kw)
+    first = ref.group(q[:m], k[:m], v[:, :m], g[:, :m], b[:, :m], dO[:, :m], ds_out=second["ds_in"], **kw)
+    assert np.array_equal(np.concatenate([first["o"], second["o"]], 1), whole["o"])
+    assert np.array_equal(second["s_out"], whole["s_out"])
+    for n in ("dq", "dk"):
+        assert np.array_equal(np.concatenate([first[n], second[n]], 0), whole[n]), n
+    for n in ("dv", "dg", "dbeta"):
+        assert np.array_equal(np.concatenate([first[n], second[n]], 1), whole[n]), n
+    assert np.array_equal(first["ds_in"], whole["ds_in"])
+
+
+@pytest.mark.parametrize("l2norm", [True, False])
+def test_boundary_states_finite_differences(l2norm):
+    """Central differences of loss = <dO, o> + <dS_out, S_out> with a nonzero
+    S_in, on 7 tokens over 2 documents: the gradient with respect to S_in is
+    ds_in, and the token gradients include the S_out term."""
+    rng = np.random.default_rng(17)
+    H, HV, dk, dv = 1, 2, 4, 3
+    inp = rand_case(rng, [3, 4], H, HV, dk, dv)
+    inp["s_in"] = 0.5 * rng.standard_normal((2, HV, dk, dv))
+    inp["ds_out"] = rng.standard_normal((2, HV, dk, dv))
+    scale = 0.7
+    grads = full_states(inp, H, HV, l2norm, scale)
+
+    def loss(x):
+        r = full_states(x, H, HV, l2norm, scale, with_grad=False)
+        return float((r["o"] * inp["dO"]).sum() + (r["s_out"] * inp["ds_out"]).sum())
+
+    h = 1e-6
+    for name, gname in (("s_in", "ds_in"), ("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"),
+                        ("beta", "dbeta")):
+        num = np.zeros_like(inp[name])
+        for idx in np.ndindex(inp[name].shape):
+            xp = dict(inp); xp[name] = inp[name].copy(); xp[name][idx] += h
+            xm = dict(inp); xm[name] = inp[name].copy(); xm[name][idx] -= h
+            num[idx] = (loss(xp) - loss(xm)) / (2 * h)
+        err = np.abs(num - grads[gname]).max() / np.abs(num).max()
+        assert err < 1e-6, (name, err)
+
+
+def test_boundary_states_empty_document():
+    """An empty document passes S_in through to S_out and dS_out back to dS_in."""
+    rng = np.random.default_rng(3)
+    G, dk, dv = 2, 4, 3
+    s_in, ds_out = rng.standard_normal((G, dk, dv)), rng.standard_normal((G, dk, dv))
+    z = np.zeros((0, dk))
+    r = ref.group(z, z, np.zeros((G, 0, dv)), np.zeros((G, 0)), np.zeros((G, 0)), np.zeros((G, 0, dv)),
+                  s_in=s_in, ds_out=ds_out, states=True)
+    assert np.array_equal(r["s_out"], s_in) and np.array_equal(r["ds_in"], ds_out)
