@@ -139,6 +139,39 @@ gdn_status gdn_ckpt_fwd_bwd(const gdn_problem *prob, const void *q, const void *
                             float *dbeta, void *saved_scratch, void *workspace,
                             size_t ws_bytes, struct CUstream_st *stream);
 
+/*
+ * Per-document boundary states.  These are gdn_fwd / gdn_bwd for documents
+ * that do not start from a zero state or whose last state is wanted: the
+ * state passed between the pieces of a document split across calls (or
+ * across devices): the pages' incoming boundary states S_in, kept in FP32
+ * ("#8542" page, the save-set table's S_in row).
+ * Every state is FP32 S in [N][HV][dk][dv] layout (document, value head,
+ * k index, v index), 16-byte aligned, caller-owned.
+ *
+ * gdn_fwd_states: as gdn_fwd, with
+ *   s_in   the state each document starts from (NULL: zero);
+ *   s_out  written with the state after each document's last token (NULL:
+ *          not written).  An empty document passes s_in through.
+ *   o, saved and s_out may each be NULL, but not all three.
+ * A saved set written here already holds the effect of s_in (the state
+ * entering every chunk), so the backward needs no s_in.
+ *
+ * gdn_bwd_states: as gdn_bwd, with
+ *   ds_out the gradient of the loss with respect to s_out (NULL: zero);
+ *   ds_in  written with the gradient with respect to s_in (NULL: not
+ *          written).  An empty document passes ds_out through.
+ * The gradients dq, dk, dv, dg, dbeta then include the terms of ds_out.
+ */
+gdn_status gdn_fwd_states(const gdn_problem *prob, const void *q, const void *k, const void *v,
+                          const float *g, const float *beta, const int32_t *cu_seqlens_dev,
+                          const int32_t *cu_seqlens_host, const float *s_in, void *o, float *s_out,
+                          void *saved, void *workspace, size_t ws_bytes, struct CUstream_st *stream);
+gdn_status gdn_bwd_states(const gdn_problem *prob, const void *q, const void *k, const void *v,
+                          const float *g, const float *beta, const int32_t *cu_seqlens_dev,
+                          const int32_t *cu_seqlens_host, const void *dO, const float *ds_out,
+                          const void *saved, void *dq, void *dk, void *dv, float *dg, float *dbeta,
+                          float *ds_in, void *workspace, size_t ws_bytes, struct CUstream_st *stream);
+
 /* Static description of a status code. */
 const char *gdn_status_string(gdn_status s);
 

@@ -21,7 +21,7 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "G
           4: "GDN_ERR_SAVED_MISMATCH", 5: "GDN_ERR_CUDA", 6: "GDN_ERR_TIMEOUT", 7: "GDN_ERR_DEVICE"}
 EXPORTS = ("gdn_saved_bytes", "gdn_fwd", "gdn_bwd", "gdn_ckpt_fwd_bwd", "gdn_status_string",
            "gdn_device_status", "gdn_plan_segment_chunks", "gdn_chunk_table_offsets", "gdn_profile_enable",
-           "gdn_profile_read", "gdn_fwd_noalloc")
+           "gdn_profile_read", "gdn_fwd_noalloc", "gdn_fwd_states", "gdn_bwd_states")
 
 
 class GDNError(RuntimeError):
@@ -56,6 +56,8 @@ def _load():
     L.gdn_fwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, sz, vp]
     L.gdn_bwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.gdn_ckpt_fwd_bwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.gdn_fwd_states.argtypes = [pp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, vp, vp, sz, vp]
+    L.gdn_bwd_states.argtypes = [pp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.gdn_status_string.argtypes = [ctypes.c_int]
     L.gdn_status_string.restype = ctypes.c_char_p
     L.gdn_device_status.argtypes = [vp, vp]
@@ -156,6 +158,18 @@ def gdn_fwd(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, o, saved, w
                        _ptr(saved), _ptr(workspace), ws_bytes, _stream(stream)), "gdn_fwd")
 
 
+def gdn_fwd_states(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, s_in, o, s_out, saved, workspace,
+                   ws_bytes=None, stream=None):
+    """gdn_fwd with per-document boundary states: s_in, s_out FP32 [N, HV, 128, 128] (either may be None);
+    see include/gdn.h."""
+    cu, cup = _cu_host(cu_seqlens_host)
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
+    _check(lib.gdn_fwd_states(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                              ctypes.cast(_ptr(cu_seqlens_dev), ctypes.POINTER(ctypes.c_int32)), cup, _ptr(s_in),
+                              _ptr(o), _ptr(s_out), _ptr(saved), _ptr(workspace), ws_bytes, _stream(stream)),
+           "gdn_fwd_states")
+
+
 def gdn_fwd_noalloc(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, o, stream=None):
     """gdn_fwd without a caller workspace or saved set (the library's fixed
     64 MiB device array serves as the workspace); see include/gdn.h."""
@@ -173,6 +187,18 @@ def gdn_bwd(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, dO, saved, 
                        ctypes.cast(_ptr(cu_seqlens_dev), ctypes.POINTER(ctypes.c_int32)), cup, _ptr(dO),
                        _ptr(saved), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(workspace),
                        ws_bytes, _stream(stream)), "gdn_bwd")
+
+
+def gdn_bwd_states(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, dO, ds_out, saved, dq, dk, dv, dg,
+                   dbeta, ds_in, workspace, ws_bytes=None, stream=None):
+    """gdn_bwd with per-document boundary states: ds_out, ds_in FP32 [N, HV, 128, 128] (either may be None);
+    see include/gdn.h."""
+    cu, cup = _cu_host(cu_seqlens_host)
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
+    _check(lib.gdn_bwd_states(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                              ctypes.cast(_ptr(cu_seqlens_dev), ctypes.POINTER(ctypes.c_int32)), cup, _ptr(dO),
+                              _ptr(ds_out), _ptr(saved), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta),
+                              _ptr(ds_in), _ptr(workspace), ws_bytes, _stream(stream)), "gdn_bwd_states")
 
 
 def gdn_ckpt_fwd_bwd(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, dO, o, dq, dk, dv, dg, dbeta,

@@ -18,13 +18,15 @@ namespace gdn {
 void launch_tables(const TableArgs& a, cudaStream_t s);
 void launch_prep(const PrepArgs& a, int NC, cudaStream_t s);
 void launch_fwd_scan(const ScanArgs& a, int nchains, cudaStream_t s);
+void launch_passthrough(const PassArgs& a, int N, cudaStream_t s);
 void launch_merge(const MergeArgs& a, int nsdoc, cudaStream_t s);
 void setup_fwd_scan_attrs();
 void setup_bwd_attrs();
 void setup_prep_attrs();
 gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const void* k, const void* v,
                    const float* g, const float* beta, const int32_t* cu_dev, const void* dO, const void* saved,
-                   void* dq, void* dk, void* dv, float* dg, float* dbeta, uint8_t* ws, cudaStream_t s);
+                   void* dq, void* dk, void* dv, float* dg, float* dbeta, const float* ds_out, float* ds_in,
+                   uint8_t* ws, cudaStream_t s);
 }  // namespace gdn
 
 using namespace gdn;
@@ -103,13 +105,14 @@ static gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
   P->G = p->HV / p->H;
   P->sms = sm_count();
   plan_segments(p, cu, &P->seg_len, &P->split_min, &P->max_doc_chunks);
-  int NC = 0, NSEG = 0, nsplit = 0, nsdoc = 0;
+  int NC = 0, NSEG = 0, nsplit = 0, nsdoc = 0, n_empty = 0;
   uint32_t h = 2166136261u;
   for (int i = 0; i < p->N; ++i) {
     const int n = (cu[i + 1] - cu[i] + CHUNK - 1) / CHUNK;
     const int Pd = n > P->split_min ? (n + P->seg_len - 1) / P->seg_len : (n > 0 ? 1 : 0);
     NC += n;
     NSEG += Pd;
+    n_empty += n == 0 ? 1 : 0;
     if (Pd > 1) {
       nsplit += Pd - 1;
       nsdoc += 1;
@@ -124,6 +127,7 @@ static gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
   P->NSEG = NSEG;
   P->nsplit = nsplit;
   P->nsdoc = nsdoc;
+  P->n_empty = n_empty;
   P->cu_hash = h;
   // workspace
   size_t off = 256;   // control block (error word)
@@ -237,7 +241,7 @@ static bool device_setup() {
 static const char* const kKernelNames[K_NUM] = {
     "tables_scan_kernel", "tables_fill_kernel", "prep_kernel",    "fwd_scan_kernel(walk)",
     "merge_kernel",       "fwd_scan_kernel",    "check_saved_kernel", "bwd_scan_kernel(walk)",
-    "merge_bwd_kernel",   "bwd_scan_kernel",    "grad_kernel"};
+    "merge_bwd_kernel",   "bwd_scan_kernel",    "grad_kernel",        "passthrough_kernel"};
 struct ProfRec {
   int id;
   cudaEvent_t e0, e1;
@@ -326,11 +330,19 @@ gdn_status run_prep(const Plan& P, const gdn_problem* p, const void* q, const vo
 }
 
 static gdn_status run_fwd(const Plan& P, const gdn_problem* p, const void* q, const void* k, const void* v,
-                          const float* g, const float* beta, const int32_t* cu_dev, void* o, void* saved,
-                          uint8_t* ws, cudaStream_t s) {
+                          const float* g, const float* beta, const int32_t* cu_dev, const float* s_in, void* o,
+                          float* s_out, void* saved, uint8_t* ws, cudaStream_t s) {
   gdn_status st = run_tables(P, p, cu_dev, ws, saved, s);
   if (st != GDN_OK) return st;
-  if (P.NC == 0) return GDN_OK;
+  if (s_out && P.n_empty > 0) {   // documents without chunks pass S_in straight through
+    PassArgs pa;
+    pa.chunk_offsets = tables_at(P, ws).chunk_offsets;
+    pa.src = s_in;
+    pa.dst = s_out;
+    pa.HV = P.HV;
+    launch_passthrough(pa, P.N, s);
+  }
+  if (P.NC == 0) return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
   // with a saved set, the per-chunk UT blocks (with T) go into it for the backward
   uint8_t* cb = saved ? static_cast<uint8_t*>(saved) + P.s_cb : ws + P.o_cb;
   st = run_prep(P, p, q, k, g, beta, ws, cb, saved ? 1 : 0, s);
@@ -357,6 +369,10 @@ static gdn_status run_fwd(const Plan& P, const gdn_problem* p, const void* q, co
   sa.s_init = reinterpret_cast<float*>(ws + P.o_sinit);
   sa.mend = saved ? reinterpret_cast<float*>(static_cast<uint8_t*>(saved) + P.s_mseg)
                   : reinterpret_cast<float*>(ws + P.o_mend_ws);
+  sa.seg_doc = t.seg_doc;
+  sa.seg_offsets = t.seg_offsets;
+  sa.s_in = s_in;
+  sa.s_out = s_out;
   sa.err = reinterpret_cast<int*>(ws);
   if (P.nsplit > 0) {
     sa.walk = 1;
@@ -416,26 +432,38 @@ int32_t gdn_plan_segment_chunks(const gdn_problem* prob, const int32_t* cu_host)
   return P.split_min == INT32_MAX ? P.max_doc_chunks : P.seg_len;
 }
 
-gdn_status gdn_fwd(const gdn_problem* prob, const void* q, const void* k, const void* v, const float* g,
-                   const float* beta, const int32_t* cu_dev, const int32_t* cu_host, void* o, void* saved,
-                   void* workspace, size_t ws_bytes, struct CUstream_st* stream) {
+gdn_status gdn_fwd_states(const gdn_problem* prob, const void* q, const void* k, const void* v, const float* g,
+                          const float* beta, const int32_t* cu_dev, const int32_t* cu_host, const float* s_in,
+                          void* o, float* s_out, void* saved, void* workspace, size_t ws_bytes,
+                          struct CUstream_st* stream) {
   Plan P;
   gdn_status st = make_plan(prob, cu_host, &P);
   if (st != GDN_OK) return st;
-  if (!cu_dev || !workspace || (!o && !saved)) return GDN_ERR_INVALID_ARG;
+  if (!cu_dev || !workspace || (!o && !saved && !s_out)) return GDN_ERR_INVALID_ARG;
   if (P.T > 0 && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
                   (o && !aligned16(o))))
     return GDN_ERR_INVALID_ARG;
+  if ((s_in && !aligned16(s_in)) || (s_out && !aligned16(s_out))) return GDN_ERR_INVALID_ARG;
   if (!aligned16(workspace) || (saved && !aligned16(saved))) return GDN_ERR_INVALID_ARG;
   if (ws_bytes < P.ws_fwd) return GDN_ERR_WORKSPACE_TOO_SMALL;
   if (!device_setup()) return GDN_ERR_CUDA;
-  return run_fwd(P, prob, q, k, v, g, beta, cu_dev, o, saved, static_cast<uint8_t*>(workspace), stream);
+  return run_fwd(P, prob, q, k, v, g, beta, cu_dev, s_in, o, s_out, saved, static_cast<uint8_t*>(workspace),
+                 stream);
 }
 
-gdn_status gdn_bwd(const gdn_problem* prob, const void* q, const void* k, const void* v, const float* g,
-                   const float* beta, const int32_t* cu_dev, const int32_t* cu_host, const void* dO,
-                   const void* saved, void* dq, void* dk, void* dv, float* dg, float* dbeta, void* workspace,
-                   size_t ws_bytes, struct CUstream_st* stream) {
+gdn_status gdn_fwd(const gdn_problem* prob, const void* q, const void* k, const void* v, const float* g,
+                   const float* beta, const int32_t* cu_dev, const int32_t* cu_host, void* o, void* saved,
+                   void* workspace, size_t ws_bytes, struct CUstream_st* stream) {
+  if (!o && !saved) return GDN_ERR_INVALID_ARG;
+  return gdn_fwd_states(prob, q, k, v, g, beta, cu_dev, cu_host, nullptr, o, nullptr, saved, workspace, ws_bytes,
+                        stream);
+}
+
+gdn_status gdn_bwd_states(const gdn_problem* prob, const void* q, const void* k, const void* v, const float* g,
+                          const float* beta, const int32_t* cu_dev, const int32_t* cu_host, const void* dO,
+                          const float* ds_out, const void* saved, void* dq, void* dk, void* dv, float* dg,
+                          float* dbeta, float* ds_in, void* workspace, size_t ws_bytes,
+                          struct CUstream_st* stream) {
   Plan P;
   gdn_status st = make_plan(prob, cu_host, &P);
   if (st != GDN_OK) return st;
@@ -444,11 +472,20 @@ gdn_status gdn_bwd(const gdn_problem* prob, const void* q, const void* k, const 
                   !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(dg) ||
                   !aligned16(dbeta)))
     return GDN_ERR_INVALID_ARG;
+  if ((ds_out && !aligned16(ds_out)) || (ds_in && !aligned16(ds_in))) return GDN_ERR_INVALID_ARG;
   if (!aligned16(workspace) || !aligned16(saved)) return GDN_ERR_INVALID_ARG;
   if (ws_bytes < P.ws_bwd) return GDN_ERR_WORKSPACE_TOO_SMALL;
   if (!device_setup()) return GDN_ERR_CUDA;
-  return run_bwd(P, *prob, q, k, v, g, beta, cu_dev, dO, saved, dq, dk, dv, dg, dbeta,
+  return run_bwd(P, *prob, q, k, v, g, beta, cu_dev, dO, saved, dq, dk, dv, dg, dbeta, ds_out, ds_in,
                  static_cast<uint8_t*>(workspace), stream);
+}
+
+gdn_status gdn_bwd(const gdn_problem* prob, const void* q, const void* k, const void* v, const float* g,
+                   const float* beta, const int32_t* cu_dev, const int32_t* cu_host, const void* dO,
+                   const void* saved, void* dq, void* dk, void* dv, float* dg, float* dbeta, void* workspace,
+                   size_t ws_bytes, struct CUstream_st* stream) {
+  return gdn_bwd_states(prob, q, k, v, g, beta, cu_dev, cu_host, dO, nullptr, saved, dq, dk, dv, dg, dbeta,
+                        nullptr, workspace, ws_bytes, stream);
 }
 
 gdn_status gdn_ckpt_fwd_bwd(const gdn_problem* prob, const void* q, const void* k, const void* v,

@@ -34,6 +34,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 bool make_tmap(CUtensorMap* m, const void* base, int64_t T, int heads);
 gdn_status run_tables(const Plan& P, const gdn_problem* p, const int32_t* cu_dev, uint8_t* ws, void* saved,
                       cudaStream_t s);
+void launch_passthrough(const PassArgs& a, int N, cudaStream_t s);
 gdn_status run_prep(const Plan& P, const gdn_problem* p, const void* q, const void* k, const float* g,
                     const float* beta, uint8_t* ws, uint8_t* cb, int write_T, cudaStream_t s);
 
@@ -51,6 +52,11 @@ struct BScanArgs {
   uint8_t* dvn;          // [NC][HV][VN_BYTES] dV_new^T tiles (full walks)
   const float* ds_init;  // [nsplit][HV][STATE_F32]: adjoint at the end of split segment i
   float* dbend;          // [nsplit][HV][STATE_F32]
+  const int* seg_doc;    // [NSEG]
+  const int* seg_offsets;  // [N+1]
+  const int* seg_idx;    // [NSEG]
+  const float* ds_out;   // [N][HV][128][128] FP32 gradient of each document's S_out, or null (zero)
+  float* ds_in;          // [N][HV][128][128] FP32 gradient of each document's S_in, or null
   int* err;
 };
 
@@ -141,13 +147,21 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
   const int kh = hv / a.G;
   const int c0 = a.seg_c0[seg], nch = a.seg_c1[seg] - c0;
 
+  // the adjoint at the segment end: merged for a segment followed by a split point, the document's
+  // dS_out for its last segment, else zero
+  const int doc = a.seg_doc[seg];
   float dS[128];
   {
     const float* src = nullptr;
-    if (!a.walk && a.seg_split[seg] >= 0)
+    int stride = 1;
+    if (!a.walk && a.seg_split[seg] >= 0) {
       src = a.ds_init + ((size_t)a.seg_split[seg] * a.HV + hv) * STATE_F32 + (size_t)tid * 128;
+    } else if (a.ds_out && seg + 1 == a.seg_offsets[doc + 1]) {   // column tid of dS_out [dk][dv]
+      src = a.ds_out + ((size_t)doc * a.HV + hv) * STATE_F32 + tid;
+      stride = 128;
+    }
 #pragma unroll
-    for (int jj = 0; jj < 128; ++jj) dS[jj] = src ? src[jj] : 0.f;
+    for (int jj = 0; jj < 128; ++jj) dS[jj] = src ? src[jj * stride] : 0.f;
   }
   uint8_t* ds_tile = sm + BS_DS;
   store_row128(ds_tile, tid, dS);
@@ -367,6 +381,11 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
 #pragma unroll
     for (int jj = 0; jj < 128; jj += 4)
       *reinterpret_cast<float4*>(dst + jj) = make_float4(dS[jj], dS[jj + 1], dS[jj + 2], dS[jj + 3]);
+  }
+  if (ok && !a.walk && a.ds_in && a.seg_idx[seg] == 0) {   // the adjoint entering the document: dS_in
+    float* dst = a.ds_in + ((size_t)doc * a.HV + hv) * STATE_F32 + tid;   // column tid of dS_in [dk][dv]
+#pragma unroll
+    for (int jj = 0; jj < 128; ++jj) dst[jj * 128] = dS[jj];
   }
   tc_fence_before();
   __syncthreads();
@@ -1261,9 +1280,18 @@ void setup_bwd_attrs() {
 
 gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const void* k, const void* v,
                    const float* g, const float* beta, const int32_t* cu_dev, const void* dO, const void* saved,
-                   void* dq, void* dk, void* dv, float* dg, float* dbeta, uint8_t* ws, cudaStream_t s) {
+                   void* dq, void* dk, void* dv, float* dg, float* dbeta, const float* ds_out, float* ds_in,
+                   uint8_t* ws, cudaStream_t s) {
   gdn_status st = run_tables(P, &pr, cu_dev, ws, nullptr, s);
   if (st != GDN_OK) return st;
+  if (ds_in && P.n_empty > 0) {   // documents without chunks pass dS_out straight through
+    PassArgs pa;
+    pa.chunk_offsets = tables_at(P, ws).chunk_offsets;
+    pa.src = ds_out;
+    pa.dst = ds_in;
+    pa.HV = P.HV;
+    launch_passthrough(pa, P.N, s);
+  }
   {
     CheckArgs ca;
     ca.saved = static_cast<const uint8_t*>(saved);
@@ -1312,6 +1340,11 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
   ba.dvn = ws + P.o_dvn;
   ba.ds_init = reinterpret_cast<const float*>(ws + P.o_dsinit);
   ba.dbend = reinterpret_cast<float*>(ws + P.o_dbend);
+  ba.seg_doc = t.seg_doc;
+  ba.seg_offsets = t.seg_offsets;
+  ba.seg_idx = t.seg_idx;
+  ba.ds_out = ds_out;
+  ba.ds_in = ds_in;
   ba.err = reinterpret_cast<int*>(ws);
   if (P.nsplit > 0) {
     ba.walk = 1;

@@ -104,14 +104,21 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
   const uint32_t cb_bytes = mode == 2 ? 8192u : (with_o ? 24576u : 16384u);
   uint8_t* s_tile = sm + SC_S;
 
-  // ---- initial state (chain: row lt of S^T)
+  // ---- initial state (chain: row lt of S^T): the merged start of a later segment, the document's
+  // S_in for its first segment (full and B walks), else zero (the identity for M walks)
   float S[128];
+  const int doc = a.seg_doc[seg];
   if (chain) {
     const float* src = nullptr;
-    if (mode == 0 && a.seg_idx[seg] > 0)
+    int stride = 1;
+    if (mode == 0 && a.seg_idx[seg] > 0) {
       src = a.s_init + ((size_t)a.seg_split[seg - 1] * a.HV + hv) * STATE_F32 + (size_t)lt * 128;
+    } else if (mode != 2 && a.seg_idx[seg] == 0 && a.s_in) {   // column lt of S_in [dk][dv]
+      src = a.s_in + ((size_t)doc * a.HV + hv) * STATE_F32 + lt;
+      stride = 128;
+    }
 #pragma unroll
-    for (int jj = 0; jj < 128; ++jj) S[jj] = src ? src[jj] : (mode == 2 && jj == lt ? 1.f : 0.f);
+    for (int jj = 0; jj < 128; ++jj) S[jj] = src ? src[jj * stride] : (mode == 2 && jj == lt ? 1.f : 0.f);
     store_state_row(s_tile, lt, S);
     if (mode == 0 && a.tape) store_state_row(a.tape + ((size_t)c0 * a.HV + hv) * STATE_BYTES, lt, S);
   }
@@ -326,6 +333,11 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
       for (int jj = 0; jj < 128; jj += 4)
         *reinterpret_cast<float4*>(dst + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
     }
+    if (ok && mode == 0 && a.s_out && seg + 1 == a.seg_offsets[doc + 1]) {   // the document's S_out
+      float* dst = a.s_out + ((size_t)doc * a.HV + hv) * STATE_F32 + lt;      // column lt of S [dk][dv]
+#pragma unroll
+      for (int jj = 0; jj < 128; ++jj) dst[jj * 128] = S[jj];
+    }
   } else {
     // =================== helper warpgroup ===================
     for (int n = 0; n < nch && ok; ++n) {
@@ -466,6 +478,22 @@ __global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
       }
     __syncthreads();
   }
+}
+
+// documents without chunks: their boundary state passes through unchanged
+__global__ void __launch_bounds__(256) passthrough_kernel(PassArgs a) {
+  const int d = blockIdx.x;
+  if (a.chunk_offsets[d + 1] != a.chunk_offsets[d]) return;
+  const size_t n4 = (size_t)a.HV * STATE_F32 / 4, base = (size_t)d * a.HV * STATE_F32;
+  float4* dst = reinterpret_cast<float4*>(a.dst + base);
+  const float4* src = a.src ? reinterpret_cast<const float4*>(a.src + base) : nullptr;
+  for (size_t i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = src ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+void launch_passthrough(const PassArgs& a, int N, cudaStream_t s) {
+  if (N <= 0) return;
+  prof_begin(K_PASS, s);
+  passthrough_kernel<<<N, 256, 0, s>>>(a);
+  prof_end(K_PASS, s);
 }
 
 void launch_fwd_scan(const ScanArgs& a, int nchains, cudaStream_t s) {

@@ -99,7 +99,19 @@ struct ScanArgs {
   const float* s_init;        // [nsplit][HV][STATE_F32]: start of the segment after split segment i
   float* bend;                // [nsplit][HV][STATE_F32]
   float* mend;                // [nsplit][HV][STATE_F32]
+  const int* seg_doc;         // [NSEG]
+  const int* seg_offsets;     // [N+1]
+  const float* s_in;          // [N][HV][128][128] FP32 S entering each document, or null (zero)
+  float* s_out;               // [N][HV][128][128] FP32 S leaving each document, or null
   int* err;
+};
+
+// boundary states of documents without chunks: dst[d] = src[d] (zero if src is null)
+struct PassArgs {
+  const int* chunk_offsets;   // [N+1]
+  const float* src;           // [N][HV][STATE_F32] or null
+  float* dst;                 // [N][HV][STATE_F32]
+  int HV;
 };
 
 struct MergeArgs {
@@ -116,6 +128,7 @@ struct Plan {
   int64_t T;
   int N, H, HV, G;
   int NC, NSEG, nsplit, nsdoc, seg_len, split_min, max_doc_chunks;
+  int n_empty;   // documents without tokens
   int sms;   // SMs of the current device (persistent grids)
   uint32_t cu_hash;
   // workspace offsets (bytes)
