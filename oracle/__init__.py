@@ -9,4 +9,5 @@ Modules:
   ref.py        ctypes binding, per-(document, q/k-head group) driver, threads
   chunked.py    the chunk-64 (WY/UT) form in FP64 numpy, forward and backward
   tables.py     brute-force enumeration of the varlen chunk tables
+  conv1d.py     the short causal convolution + SiLU front, forward and backward
 """
