@@ -172,6 +172,38 @@ gdn_status gdn_bwd_states(const gdn_problem *prob, const void *q, const void *k,
                           const void *saved, void *dq, void *dk, void *dv, float *dg, float *dbeta,
                           float *ds_in, void *workspace, size_t ws_bytes, struct CUstream_st *stream);
 
+/*
+ * The short causal convolution + SiLU in front of the GDN layer, over the
+ * packed q/k/v channels (C = (2 H + HV) x 128 = 10,240 at (16, 48)), restarting
+ * at every document ("#8542" page: the B23 shape description and the family's
+ * conv1d + SiLU training backend; its save-set table keeps at most three
+ * history rows, a four-tap kernel).  Per channel c, with W taps:
+ *     z[t, c] = b[c] + sum_{i<W} w[c, i] x[t - (W-1) + i, c]   (x = 0 before t's document)
+ *     y[t, c] = z / (1 + exp(-z))
+ * Layouts: x, y, dy, dx [T][C] BF16 (token-major, contiguous); w, dw [C][W]
+ * FP32; b, db [C] FP32 (b may be NULL: no bias; db may be NULL: not
+ * written).  C must be a multiple of 8, 1 <= W <= 4 (else
+ * GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED).  Pointers 16-byte aligned.
+ * Accumulation is FP32 in a fixed order; dw and db are sums of per-range
+ * partials added in range order (bitwise reproducible).  The caller owns
+ * every buffer; the backward needs `workspace` of gdn_conv1d_workspace_bytes.
+ */
+typedef struct {
+    int64_t T;   /* total packed tokens (= cu_seqlens[N]) */
+    int32_t N;   /* documents */
+    int32_t C;   /* channels */
+    int32_t W;   /* taps */
+} gdn_conv_problem;
+gdn_status gdn_conv1d_workspace_bytes(const gdn_conv_problem *prob, const int32_t *cu_seqlens_host,
+                                      size_t *workspace_bytes);
+gdn_status gdn_conv1d_fwd(const gdn_conv_problem *prob, const void *x, const float *w, const float *b,
+                          const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host, void *y,
+                          struct CUstream_st *stream);
+gdn_status gdn_conv1d_bwd(const gdn_conv_problem *prob, const void *x, const float *w, const float *b,
+                          const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host, const void *dy,
+                          void *dx, float *dw, float *db, void *workspace, size_t ws_bytes,
+                          struct CUstream_st *stream);
+
 /* Static description of a status code. */
 const char *gdn_status_string(gdn_status s);
 

@@ -21,7 +21,8 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "G
           4: "GDN_ERR_SAVED_MISMATCH", 5: "GDN_ERR_CUDA", 6: "GDN_ERR_TIMEOUT", 7: "GDN_ERR_DEVICE"}
 EXPORTS = ("gdn_saved_bytes", "gdn_fwd", "gdn_bwd", "gdn_ckpt_fwd_bwd", "gdn_status_string",
            "gdn_device_status", "gdn_plan_segment_chunks", "gdn_chunk_table_offsets", "gdn_profile_enable",
-           "gdn_profile_read", "gdn_fwd_noalloc", "gdn_fwd_states", "gdn_bwd_states")
+           "gdn_profile_read", "gdn_fwd_noalloc", "gdn_fwd_states", "gdn_bwd_states", "gdn_conv1d_workspace_bytes",
+           "gdn_conv1d_fwd", "gdn_conv1d_bwd")
 
 
 class GDNError(RuntimeError):
@@ -39,6 +40,14 @@ class gdn_problem(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("N", ctypes.c_int32), ("H", ctypes.c_int32), ("HV", ctypes.c_int32),
                 ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("scale", ctypes.c_float),
                 ("l2norm", ctypes.c_int32), ("segments", ctypes.c_int32)]
+
+
+class gdn_conv_problem(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("N", ctypes.c_int32), ("C", ctypes.c_int32), ("W", ctypes.c_int32)]
+
+
+def conv_problem(T, N, C, W=4) -> gdn_conv_problem:
+    return gdn_conv_problem(int(T), int(N), int(C), int(W))
 
 
 def problem(T, N, H, HV, scale=128 ** -0.5, l2norm=True, segments=0, dk=128, dv=128) -> gdn_problem:
@@ -66,6 +75,13 @@ def _load():
     L.gdn_chunk_table_offsets.argtypes = [pp, i32p, ctypes.POINTER(sz), i32p]
     L.gdn_fwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, i32p, i32p, vp, vp]
     L.gdn_fwd_noalloc.restype = ctypes.c_int
+    cp = ctypes.POINTER(gdn_conv_problem)
+    L.gdn_conv1d_workspace_bytes.argtypes = [cp, i32p, ctypes.POINTER(sz)]
+    L.gdn_conv1d_fwd.argtypes = [cp, vp, vp, vp, vp, i32p, vp, vp]
+    L.gdn_conv1d_bwd.argtypes = [cp, vp, vp, vp, vp, i32p, vp, vp, vp, vp, vp, sz, vp]
+    for name in ("gdn_conv1d_workspace_bytes", "gdn_conv1d_fwd", "gdn_conv1d_bwd", "gdn_fwd_states",
+                 "gdn_bwd_states"):
+        getattr(L, name).restype = ctypes.c_int
     L.gdn_profile_enable.argtypes = [ctypes.c_int]
     L.gdn_profile_enable.restype = None
     L.gdn_profile_read.argtypes = [ctypes.POINTER(gdn_kernel_stat), ctypes.c_int]
@@ -234,6 +250,31 @@ def gdn_device_status(workspace, stream=None) -> int:
 # ---------------------------------------------------------------------------
 # allocation helpers (torch owns the memory; the library allocates nothing)
 # ---------------------------------------------------------------------------
+def gdn_conv1d_workspace_bytes(prob, cu_seqlens_host) -> int:
+    cu, cup = _cu_host(cu_seqlens_host)
+    n = ctypes.c_size_t(0)
+    _check(lib.gdn_conv1d_workspace_bytes(ctypes.byref(prob), cup, ctypes.byref(n)), "gdn_conv1d_workspace_bytes")
+    return int(n.value)
+
+
+def gdn_conv1d_fwd(prob, x, w, b, cu_seqlens_dev, cu_seqlens_host, y, stream=None):
+    """The short causal conv1d + SiLU front (see include/gdn.h): x, y [T, C] BF16; w [C, W], b [C] FP32."""
+    cu, cup = _cu_host(cu_seqlens_host)
+    _check(lib.gdn_conv1d_fwd(ctypes.byref(prob), _ptr(x), _ptr(w), _ptr(b),
+                              ctypes.cast(_ptr(cu_seqlens_dev), ctypes.POINTER(ctypes.c_int32)), cup, _ptr(y),
+                              _stream(stream)), "gdn_conv1d_fwd")
+
+
+def gdn_conv1d_bwd(prob, x, w, b, cu_seqlens_dev, cu_seqlens_host, dy, dx, dw, db, workspace, ws_bytes=None,
+                   stream=None):
+    cu, cup = _cu_host(cu_seqlens_host)
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
+    _check(lib.gdn_conv1d_bwd(ctypes.byref(prob), _ptr(x), _ptr(w), _ptr(b),
+                              ctypes.cast(_ptr(cu_seqlens_dev), ctypes.POINTER(ctypes.c_int32)), cup, _ptr(dy),
+                              _ptr(dx), _ptr(dw), _ptr(db), _ptr(workspace), ws_bytes, _stream(stream)),
+           "gdn_conv1d_bwd")
+
+
 class Buffers:
     """Caller-side saved set and workspace for one problem, allocated with torch."""
 

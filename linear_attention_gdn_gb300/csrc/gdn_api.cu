@@ -40,7 +40,7 @@ namespace gdn {
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-static int sm_count() {
+int sm_count() {
   int dev = 0, n = 152;
   if (cudaGetDevice(&dev) == cudaSuccess) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 152;
@@ -241,7 +241,8 @@ static bool device_setup() {
 static const char* const kKernelNames[K_NUM] = {
     "tables_scan_kernel", "tables_fill_kernel", "prep_kernel",    "fwd_scan_kernel(walk)",
     "merge_kernel",       "fwd_scan_kernel",    "check_saved_kernel", "bwd_scan_kernel(walk)",
-    "merge_bwd_kernel",   "bwd_scan_kernel",    "grad_kernel",        "passthrough_kernel"};
+    "merge_bwd_kernel",   "bwd_scan_kernel",    "grad_kernel",        "passthrough_kernel",
+    "conv_fwd_kernel",    "conv_bwd_kernel(+reduce)"};
 struct ProfRec {
   int id;
   cudaEvent_t e0, e1;

@@ -7,9 +7,10 @@ that both sides see exactly the same BF16 / FP32 values.
 The workloads mirror the shapes the flashinfer Cake GDN pages time and test:
 packed variable-length documents, head dim 128, (H, HV) = (16, 48) query/key
 and value heads, BF16 q/k/v and output gradient, FP32 gate g and beta
-("feat(cake_gdn_kcp) ... #8172" page, #8181 section: "head dim 128, BF16
-q/k/v and output gradient, and FP32 g and beta"; the "shape A" pack of 4
-documents 98304/65536/57344/40960 is from the "#8542" page, Conventions).
+("feat(cake_gdn_kcp) ... #8172" page, #8181 section, which fixes the head
+dimension at 128, q/k/v and the output gradient in BF16 and g, beta in FP32;
+the "shape A" pack of 4 documents 98304/65536/57344/40960 is from the "#8542"
+page, Conventions).
 
 Value distributions (all seeded):
   q, k, v, dO ~ N(0, 1), rounded to BF16
@@ -131,3 +132,18 @@ def generate(w: Workload, device="cpu", with_grad=True) -> dict:
     if with_grad:
         out["dO"] = normal((T, HV, w.dv)).to(torch.bfloat16)
     return out
+
+
+def conv_inputs(doc_lens, C: int, W: int = 4, seed: int = 0, with_bias: bool = True) -> dict:
+    """Seeded inputs of the causal conv1d + SiLU front: x, dy [T, C] ~ N(0, 1) in
+    BF16; taps w [C, W] ~ N(0, 0.5^2) and bias b [C] ~ N(0, 0.1^2) in FP32 (the
+    pages give no initialisation; these keep z = conv + b of order one).  One
+    generator draws x, w, b, dy in that order."""
+    gen = torch.Generator().manual_seed(seed)
+    T = int(sum(doc_lens))
+    x = torch.randn((T, C), generator=gen).to(torch.bfloat16)
+    w = 0.5 * torch.randn((C, W), generator=gen)
+    b = 0.1 * torch.randn((C,), generator=gen)
+    dy = torch.randn((T, C), generator=gen).to(torch.bfloat16)
+    cu = np.concatenate([[0], np.cumsum(doc_lens)]).astype(np.int32)
+    return dict(x=x, w=w, b=b if with_bias else None, dy=dy, cu_seqlens=cu)
