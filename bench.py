@@ -250,6 +250,14 @@ def run_ours(args, rank, world, local_rank):
         if op == "ckpt":
             gdn.gdn_ckpt_fwd_bwd(prob, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_dev, w.cu_seqlens,
                                  xx["dO"], o, dq, dk, dv, dg, db, buf.saved, buf.workspace, stream=stream)
+        if op == "fwd+bwd with states":   # per-document S_in in, S_out out; dS_out in, dS_in out
+            gdn.gdn_fwd_states(prob, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_dev, w.cu_seqlens,
+                               bnd["s_in"], o, bnd["s_out"], buf.saved, buf.workspace, stream=stream)
+            gdn.gdn_bwd_states(prob, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_dev, w.cu_seqlens,
+                               xx["dO"], bnd["ds_out"], buf.saved, dq, dk, dv, dg, db, bnd["ds_in"],
+                               buf.workspace, stream=stream)
+
+    bnd = {}
 
     def barrier():
         if world > 1:
@@ -296,11 +304,36 @@ def run_ours(args, rank, world, local_rank):
 
     extra = {}
     if not args.quick:
-        for other in ("fwd", "ckpt"):
+        bnd.update({n: 0.1 * torch.randn((w.N, w.HV, D, D), device=dev) for n in ("s_in", "ds_out")})
+        bnd.update({n: torch.empty((w.N, w.HV, D, D), device=dev) for n in ("s_out", "ds_in")})
+        for other in ("fwd", "ckpt", "fwd+bwd with states"):
             if other != op:
                 t_o = timed(other, max(3, args.steps // 2), 2)
+                fl = step_flops(w, "fwd+bwd" if other == "fwd+bwd with states" else other)
                 extra[other] = {"ms": round(t_o, 4), "Mtokens_per_s": round(replica_rate(world, w.T, t_o), 3),
-                                "TFLOP_per_s": round(world * step_flops(w, other) / t_o / 1e9, 1)}
+                                "TFLOP_per_s": round(world * fl / t_o / 1e9, 1)}
+        # the short causal conv1d + SiLU front over the workload's packed q/k/v channels (4 taps),
+        # timed alone: fwd reads x and writes y, bwd reads x and dy and writes dx (BF16 [T, C])
+        C_qkv = (2 * w.H + w.HV) * D
+        cp = gdn.conv_problem(w.T, w.N, C_qkv, 4)
+        cx = torch.randn((w.T, C_qkv), device=dev).to(torch.bfloat16)
+        cdy = torch.randn_like(cx)
+        cw, cb = 0.5 * torch.randn((C_qkv, 4), device=dev), 0.1 * torch.randn((C_qkv,), device=dev)
+        cy, cdx = torch.empty_like(cx), torch.empty_like(cx)
+        cdw, cdb = torch.empty_like(cw), torch.empty_like(cb)
+        cws = torch.empty((max(gdn.gdn_conv1d_workspace_bytes(cp, w.cu_seqlens), 16),), dtype=torch.uint8,
+                          device=dev)
+        row_bytes = w.T * C_qkv * 2
+        for name, fn, nbytes in (
+                ("conv1d_silu fwd", lambda: gdn.gdn_conv1d_fwd(cp, cx, cw, cb, cu_dev, w.cu_seqlens, cy,
+                                                               stream=stream), 2 * row_bytes),
+                ("conv1d_silu bwd", lambda: gdn.gdn_conv1d_bwd(cp, cx, cw, cb, cu_dev, w.cu_seqlens, cdy, cdx,
+                                                               cdw, cdb, cws, stream=stream), 3 * row_bytes)):
+            t_c = timed_replicas(fn, max(3, args.steps // 2), 2, barrier, allmax, event_clock)
+            extra[name] = {"ms": round(t_c, 4), "channels": C_qkv, "taps": 4,
+                           "GB_per_s": round(nbytes / (t_c * 1e-3) / 1e9, 1),
+                           "Mtokens_per_s": round(replica_rate(world, w.T, t_c), 3)}
+        del cx, cdy, cy, cdx
 
     # end to end through the C ABI with pinned host buffers: every step copies
     # its inputs in and all of its outputs back

@@ -17,7 +17,8 @@
 // contiguous token range, which it walks in order with the last W - 1 input
 // rows (and, backward, the last W values of dz) in registers, so every
 // element is read from HBM once plus a halo of W - 1 rows per range.  Rows are
-// requested four at a time before any is used.  The backward writes per-range
+// requested in batches of 16 (forward) or 8 (backward, x and dy), one batch
+// ahead of their use, over ranges of 256 / 1,024 tokens.  The backward writes per-range
 // partial sums of dw and db; a second kernel adds them in range order, so the
 // result does not depend on scheduling.
 #include <algorithm>
@@ -30,13 +31,14 @@
 
 namespace gdn {
 
-int sm_count();
-
 constexpr int CV_THREADS = 128;
 constexpr int CV_VEC = 4;                         // channels per thread
 constexpr int CV_CH = CV_THREADS * CV_VEC;        // channels per CTA
 constexpr int CV_MAXW = 4;
-constexpr int CV_U = 4;                           // rows requested together
+constexpr int CV_UF = 16;                         // rows requested together (forward)
+constexpr int CV_UB = 8;                          // rows requested together (backward: x and dy)
+constexpr int CV_RF = 256;                        // tokens per range (forward)
+constexpr int CV_RB = 1024;                       // tokens per range (backward: one dw / db partial each)
 
 struct ConvArgs {
   const __nv_bfloat16* x;
@@ -53,8 +55,10 @@ struct ConvArgs {
   int N, C, W, R;        // R: tokens per range (grid.y ranges)
 };
 
-__device__ __forceinline__ void ld_row(const __nv_bfloat16* p, float (&v)[CV_VEC]) {
-  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+__device__ __forceinline__ uint2 ld_raw(const __nv_bfloat16* p) {
+  return __ldg(reinterpret_cast<const uint2*>(p));
+}
+__device__ __forceinline__ void unpack_row(const uint2 u, float (&v)[CV_VEC]) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
   for (int e = 0; e < CV_VEC / 2; ++e) {
@@ -63,13 +67,16 @@ __device__ __forceinline__ void ld_row(const __nv_bfloat16* p, float (&v)[CV_VEC
     v[2 * e + 1] = f.y;
   }
 }
+__device__ __forceinline__ void ld_row(const __nv_bfloat16* p, float (&v)[CV_VEC]) { unpack_row(ld_raw(p), v); }
 __device__ __forceinline__ void st_row(__nv_bfloat16* p, const float (&v)[CV_VEC]) {
   uint2 u;
   u.x = pack_bf16(v[0], v[1]);
   u.y = pack_bf16(v[2], v[3]);
   *reinterpret_cast<uint2*>(p) = u;
 }
-__device__ __forceinline__ float sigmoidf(float z) { return 1.0f / (1.0f + expf(-z)); }
+// 1 / (1 + e^{-z}) with the fast exponential and division (a few ulp; the result is rounded to
+// BF16 or feeds an FP32 gradient)
+__device__ __forceinline__ float sigmoidf(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 // the document containing token t: the largest d with cu[d] <= t (skipping empty documents)
 __device__ __forceinline__ int doc_of(const int* cu, int N, int64_t t) {
@@ -82,98 +89,90 @@ __device__ __forceinline__ int doc_of(const int* cu, int N, int64_t t) {
   return lo;
 }
 
-// per-thread setup shared by both directions: taps, bias, the document of the first row, and the
-// last W - 1 input rows before it (zero where they precede the document start)
+// One thread's state for W taps: the taps and bias of its channels, the last W - 1 input rows
+// (hist[W-2] the newest; zero before the document start), and the document bookkeeping.
+template <int W>
 struct ConvThread {
-  float w[CV_MAXW][CV_VEC], b[CV_VEC];
-  float xw[CV_MAXW - 1][CV_VEC];   // xw[W-2] is the row just before the current one
-  int start, next;                 // current document's first token, the next document's
-  int d;
-};
+  static constexpr int H = W > 1 ? W - 1 : 1;
+  float w[W][CV_VEC], b[CV_VEC];
+  float hist[H][CV_VEC];
+  int start, next, d;
 
-__device__ __forceinline__ void conv_setup(const ConvArgs& a, int c0, int64_t lo, ConvThread& th) {
-#pragma unroll
-  for (int i = 0; i < CV_MAXW; ++i)
-#pragma unroll
-    for (int e = 0; e < CV_VEC; ++e) th.w[i][e] = i < a.W ? a.w[(size_t)(c0 + e) * a.W + i] : 0.f;
-#pragma unroll
-  for (int e = 0; e < CV_VEC; ++e) th.b[e] = a.b ? a.b[c0 + e] : 0.f;
-  th.d = doc_of(a.cu, a.N, lo);
-  th.start = a.cu[th.d];
-  th.next = a.cu[th.d + 1];
-#pragma unroll
-  for (int j = 0; j < CV_MAXW - 1; ++j) {   // xw[j] = x[lo - (W-1) + j]
-    const int64_t s = lo - (a.W - 1) + j;
-    if (j < a.W - 1 && s >= th.start) ld_row(a.x + s * a.C + c0, th.xw[j]);
-    else
-#pragma unroll
-      for (int e = 0; e < CV_VEC; ++e) th.xw[j][e] = 0.f;
-  }
-}
-
-// advance the document bookkeeping to token t; true when t starts a document (history reset)
-__device__ __forceinline__ bool conv_enter(const ConvArgs& a, int64_t t, ConvThread& th) {
-  if (t < th.next) return false;
-  while (th.d + 1 < a.N && a.cu[th.d + 1] <= t) ++th.d;
-  th.start = a.cu[th.d];
-  th.next = a.cu[th.d + 1];
-  return true;
-}
-
-// z for the current row xt, the history in th.xw; then shift xt into the history
-__device__ __forceinline__ void conv_z(const ConvArgs& a, const float (&xt)[CV_VEC], ConvThread& th,
-                                       float (&z)[CV_VEC], float (&xs)[CV_MAXW][CV_VEC]) {
-  // xs[i] = x[t - (W-1) + i]: the input that tap i multiplies
-#pragma unroll
-  for (int i = 0; i < CV_MAXW; ++i)
-#pragma unroll
-    for (int e = 0; e < CV_VEC; ++e)
-      xs[i][e] = i < a.W - 1 ? th.xw[i][e] : (i == a.W - 1 ? xt[e] : 0.f);
-#pragma unroll
-  for (int e = 0; e < CV_VEC; ++e) {
-    float acc = th.b[e];
-#pragma unroll
-    for (int i = 0; i < CV_MAXW; ++i) acc = fmaf(th.w[i][e], xs[i][e], acc);
-    z[e] = acc;
-  }
-  // the history moves down one row: xw[j] <- xw[j + 1] for j < W - 2, xw[W - 2] <- xt
-#pragma unroll
-  for (int j = 0; j < CV_MAXW - 1; ++j) {
-    constexpr int LAST = CV_MAXW - 2;
-    const int up = j < LAST ? j + 1 : LAST;   // (a compile-time index)
+  __device__ __forceinline__ void setup(const ConvArgs& a, int c0, int64_t lo) {
 #pragma unroll
     for (int e = 0; e < CV_VEC; ++e) {
-      const float nx = j < a.W - 2 ? th.xw[up][e] : xt[e];
-      if (j <= a.W - 2) th.xw[j][e] = nx;
+#pragma unroll
+      for (int i = 0; i < W; ++i) w[i][e] = a.w[(size_t)(c0 + e) * W + i];
+      b[e] = a.b ? a.b[c0 + e] : 0.f;
+    }
+    d = doc_of(a.cu, a.N, lo);
+    start = a.cu[d];
+    next = a.cu[d + 1];
+#pragma unroll
+    for (int j = 0; j < H; ++j) {   // hist[j] = x[lo - (W-1) + j]
+      const int64_t s = lo - (W - 1) + j;
+      if (W > 1 && s >= start) ld_row(a.x + s * a.C + c0, hist[j]);
+      else
+#pragma unroll
+        for (int e = 0; e < CV_VEC; ++e) hist[j][e] = 0.f;
     }
   }
-}
-
-__device__ __forceinline__ void conv_reset(ConvThread& th) {
+  // advance the document bookkeeping to token t; a new document clears the history
+  __device__ __forceinline__ void enter(const ConvArgs& a, int64_t t) {
+    if (t < next) return;
+    while (d + 1 < a.N && a.cu[d + 1] <= t) ++d;
+    start = a.cu[d];
+    next = a.cu[d + 1];
 #pragma unroll
-  for (int j = 0; j < CV_MAXW - 1; ++j)
+    for (int j = 0; j < H; ++j)
 #pragma unroll
-    for (int e = 0; e < CV_VEC; ++e) th.xw[j][e] = 0.f;
-}
+      for (int e = 0; e < CV_VEC; ++e) hist[j][e] = 0.f;
+  }
+  // z of the row xt; xs[i] = the input tap i multiplies; then xt joins the history
+  __device__ __forceinline__ void step(const float (&xt)[CV_VEC], float (&z)[CV_VEC], float (&xs)[W][CV_VEC]) {
+#pragma unroll
+    for (int e = 0; e < CV_VEC; ++e) {
+#pragma unroll
+      for (int i = 0; i < W - 1; ++i) xs[i][e] = hist[i][e];
+      xs[W - 1][e] = xt[e];
+      float acc = b[e];
+#pragma unroll
+      for (int i = 0; i < W; ++i) acc = fmaf(w[i][e], xs[i][e], acc);
+      z[e] = acc;
+#pragma unroll
+      for (int j = 0; j + 1 < W - 1; ++j) hist[j][e] = hist[j + 1][e];
+      if (W > 1) hist[H - 1][e] = xt[e];
+    }
+  }
+};
 
+template <int W>
 __global__ void __launch_bounds__(CV_THREADS) conv_fwd_kernel(const ConvArgs a) {
   const int c0 = (blockIdx.x * CV_THREADS + threadIdx.x) * CV_VEC;
   const int64_t lo = (int64_t)blockIdx.y * a.R, hi = min(a.T, lo + a.R);
   if (c0 >= a.C || lo >= hi) return;
-  ConvThread th;
-  conv_setup(a, c0, lo, th);
-  for (int64_t t0 = lo; t0 < hi; t0 += CV_U) {
-    float xr[CV_U][CV_VEC];
+  ConvThread<W> th;
+  th.setup(a, c0, lo);
+  // rows are requested one batch ahead of their use
+  uint2 nx[CV_UF];
 #pragma unroll
-    for (int u = 0; u < CV_U; ++u)
-      if (t0 + u < hi) ld_row(a.x + (t0 + u) * a.C + c0, xr[u]);
+  for (int u = 0; u < CV_UF; ++u)
+    if (lo + u < hi) nx[u] = ld_raw(a.x + (lo + u) * a.C + c0);
+  for (int64_t t0 = lo; t0 < hi; t0 += CV_UF) {
+    uint2 xr[CV_UF];
 #pragma unroll
-    for (int u = 0; u < CV_U; ++u) {
+    for (int u = 0; u < CV_UF; ++u) {
+      xr[u] = nx[u];
+      if (t0 + CV_UF + u < hi) nx[u] = ld_raw(a.x + (t0 + CV_UF + u) * a.C + c0);
+    }
+#pragma unroll
+    for (int u = 0; u < CV_UF; ++u) {
       const int64_t t = t0 + u;
       if (t >= hi) break;
-      if (conv_enter(a, t, th)) conv_reset(th);
-      float z[CV_VEC], xs[CV_MAXW][CV_VEC], y[CV_VEC];
-      conv_z(a, xr[u], th, z, xs);
+      th.enter(a, t);
+      float xt[CV_VEC], z[CV_VEC], xs[W][CV_VEC], y[CV_VEC];
+      unpack_row(xr[u], xt);
+      th.step(xt, z, xs);
 #pragma unroll
       for (int e = 0; e < CV_VEC; ++e) y[e] = z[e] * sigmoidf(z[e]);
       st_row(a.y + t * a.C + c0, y);
@@ -183,101 +182,109 @@ __global__ void __launch_bounds__(CV_THREADS) conv_fwd_kernel(const ConvArgs a) 
 
 // Backward over the range [lo, hi): dz for rows [lo, hi + W - 1) (the last W - 1 only feed dx of
 // rows below hi), dx for rows [lo, hi), partial dw / db over rows [lo, hi).
+template <int W>
 __global__ void __launch_bounds__(CV_THREADS) conv_bwd_kernel(const ConvArgs a) {
   const int c0 = (blockIdx.x * CV_THREADS + threadIdx.x) * CV_VEC;
   const int64_t lo = (int64_t)blockIdx.y * a.R, hi = min(a.T, lo + a.R);
   if (c0 >= a.C || lo >= hi) return;
-  ConvThread th;
-  conv_setup(a, c0, lo, th);
-  float dzw[CV_MAXW][CV_VEC];   // dz of rows t' - (W-1) .. t' (dzw[W-1] newest)
-  int dsw[CV_MAXW];             // the document start of each of those rows (-1: none)
+  ConvThread<W> th;
+  th.setup(a, c0, lo);
+  float dzw[W][CV_VEC];   // dz of rows t - (W-1) .. t (dzw[W-1] the newest)
+  int dsw[W];             // the document start of each of those rows (-1: past the end)
 #pragma unroll
-  for (int j = 0; j < CV_MAXW; ++j) {
+  for (int j = 0; j < W; ++j) {
     dsw[j] = -1;
 #pragma unroll
     for (int e = 0; e < CV_VEC; ++e) dzw[j][e] = 0.f;
   }
-  float pw[CV_MAXW][CV_VEC], pb[CV_VEC];
+  float pw[W][CV_VEC], pb[CV_VEC];
 #pragma unroll
   for (int e = 0; e < CV_VEC; ++e) {
     pb[e] = 0.f;
 #pragma unroll
-    for (int i = 0; i < CV_MAXW; ++i) pw[i][e] = 0.f;
+    for (int i = 0; i < W; ++i) pw[i][e] = 0.f;
   }
-  const int64_t end = hi + a.W - 1;
-  for (int64_t t0 = lo; t0 < end; t0 += CV_U) {
-    float xr[CV_U][CV_VEC], gr[CV_U][CV_VEC];
+  const int64_t end = hi + W - 1, lim = min(end, a.T);
+  // rows are requested one batch ahead of their use
+  uint2 nxr[CV_UB], ngr[CV_UB];
 #pragma unroll
-    for (int u = 0; u < CV_U; ++u)
-      if (t0 + u < end && t0 + u < a.T) {
-        ld_row(a.x + (t0 + u) * a.C + c0, xr[u]);
-        ld_row(a.dy + (t0 + u) * a.C + c0, gr[u]);
+  for (int u = 0; u < CV_UB; ++u)
+    if (lo + u < lim) {
+      nxr[u] = ld_raw(a.x + (lo + u) * a.C + c0);
+      ngr[u] = ld_raw(a.dy + (lo + u) * a.C + c0);
+    }
+  for (int64_t t0 = lo; t0 < end; t0 += CV_UB) {
+    uint2 xr[CV_UB], gr[CV_UB];
+#pragma unroll
+    for (int u = 0; u < CV_UB; ++u) {
+      xr[u] = nxr[u];
+      gr[u] = ngr[u];
+      if (t0 + CV_UB + u < lim) {
+        nxr[u] = ld_raw(a.x + (t0 + CV_UB + u) * a.C + c0);
+        ngr[u] = ld_raw(a.dy + (t0 + CV_UB + u) * a.C + c0);
       }
+    }
 #pragma unroll
-    for (int u = 0; u < CV_U; ++u) {
+    for (int u = 0; u < CV_UB; ++u) {
       const int64_t t = t0 + u;
       if (t >= end) break;
       float dz[CV_VEC];
       int ds = -1;
       if (t < a.T) {
-        if (conv_enter(a, t, th)) conv_reset(th);
+        th.enter(a, t);
         ds = th.start;
-        float z[CV_VEC], xs[CV_MAXW][CV_VEC];
-        conv_z(a, xr[u], th, z, xs);
+        float xt[CV_VEC], gt[CV_VEC], z[CV_VEC], xs[W][CV_VEC];
+        unpack_row(xr[u], xt);
+        unpack_row(gr[u], gt);
+        th.step(xt, z, xs);
 #pragma unroll
         for (int e = 0; e < CV_VEC; ++e) {
           const float sg = sigmoidf(z[e]);
-          dz[e] = gr[u][e] * sg * (1.0f + z[e] * (1.0f - sg));
+          dz[e] = gt[e] * sg * (1.0f + z[e] * (1.0f - sg));
         }
         if (t < hi) {
 #pragma unroll
           for (int e = 0; e < CV_VEC; ++e) {
             pb[e] += dz[e];
 #pragma unroll
-            for (int i = 0; i < CV_MAXW; ++i) pw[i][e] = fmaf(dz[e], xs[i][e], pw[i][e]);
+            for (int i = 0; i < W; ++i) pw[i][e] = fmaf(dz[e], xs[i][e], pw[i][e]);
           }
         }
       } else {
 #pragma unroll
         for (int e = 0; e < CV_VEC; ++e) dz[e] = 0.f;
       }
-      // window of the last W rows' dz
 #pragma unroll
-      for (int j = 0; j < CV_MAXW - 1; ++j) {
+      for (int j = 0; j + 1 < W; ++j) {
         dsw[j] = dsw[j + 1];
 #pragma unroll
         for (int e = 0; e < CV_VEC; ++e) dzw[j][e] = dzw[j + 1][e];
       }
-      dsw[CV_MAXW - 1] = ds;
+      dsw[W - 1] = ds;
 #pragma unroll
-      for (int e = 0; e < CV_VEC; ++e) dzw[CV_MAXW - 1][e] = dz[e];
-      // dx of row s = t - (W-1): taps i see dz of row s + (W-1) - i = window slot CV_MAXW - 1 - i
-      const int64_t s = t - (a.W - 1);
+      for (int e = 0; e < CV_VEC; ++e) dzw[W - 1][e] = dz[e];
+      // dx of row s = t - (W-1), the oldest slot: tap i sees dz of row s + (W-1) - i, slot W-1-i,
+      // when that row is in s's document
+      const int64_t s = t - (W - 1);
       if (s >= lo && s < hi) {
-        int sds = -2;   // the document start of row s, which sits in slot CV_MAXW - W
-#pragma unroll
-        for (int slot = 0; slot < CV_MAXW; ++slot)
-          if (slot == CV_MAXW - a.W) sds = dsw[slot];
         float dx[CV_VEC];
 #pragma unroll
         for (int e = 0; e < CV_VEC; ++e) {
           float acc = 0.f;
 #pragma unroll
-          for (int i = CV_MAXW - 1; i >= 0; --i) {
-            const int slot = CV_MAXW - 1 - i;
-            if (i < a.W && dsw[slot] == sds) acc = fmaf(th.w[i][e], dzw[slot][e], acc);
-          }
+          for (int i = W - 1; i >= 0; --i)
+            if (dsw[W - 1 - i] == dsw[0]) acc = fmaf(th.w[i][e], dzw[W - 1 - i][e], acc);
           dx[e] = acc;
         }
         st_row(a.dx + s * a.C + c0, dx);
       }
     }
   }
-  float* pp = a.part + (size_t)blockIdx.y * (a.W + 1) * a.C + c0;
+  float* pp = a.part + (size_t)blockIdx.y * (W + 1) * a.C + c0;
 #pragma unroll
-  for (int i = 0; i < CV_MAXW; ++i)
-    if (i < a.W) *reinterpret_cast<float4*>(pp + (size_t)i * a.C) = make_float4(pw[i][0], pw[i][1], pw[i][2], pw[i][3]);
-  *reinterpret_cast<float4*>(pp + (size_t)a.W * a.C) = make_float4(pb[0], pb[1], pb[2], pb[3]);
+  for (int i = 0; i < W; ++i)
+    *reinterpret_cast<float4*>(pp + (size_t)i * a.C) = make_float4(pw[i][0], pw[i][1], pw[i][2], pw[i][3]);
+  *reinterpret_cast<float4*>(pp + (size_t)W * a.C) = make_float4(pb[0], pb[1], pb[2], pb[3]);
 }
 
 // dw, db: the ranges' partial sums added in range order
@@ -292,15 +299,8 @@ __global__ void __launch_bounds__(256) conv_reduce_kernel(const ConvArgs a, int 
   }
 }
 
-// token ranges: enough CTAs to fill the GPU four times over, at least 64 tokens each
-static void conv_ranges(int64_t T, int C, int sms, int* S, int* R) {
-  const int nblk = (C + CV_CH - 1) / CV_CH;
-  int64_t s = std::max<int64_t>(1, (4 * (int64_t)sms + nblk - 1) / nblk);
-  s = std::min<int64_t>(s, std::max<int64_t>(1, (T + 63) / 64));
-  const int64_t r = std::max<int64_t>(1, (T + s - 1) / s);
-  *R = (int)std::min<int64_t>(r, INT32_MAX);
-  *S = (int)((T + r - 1) / r);
-}
+// token ranges of R tokens (the last one shorter): S of them
+static int conv_ranges(int64_t T, int R) { return (int)((T + R - 1) / R); }
 
 }  // namespace gdn
 
@@ -324,9 +324,7 @@ gdn_status gdn_conv1d_workspace_bytes(const gdn_conv_problem* p, const int32_t* 
   gdn_status st = conv_check(p, cu_host);
   if (st != GDN_OK) return st;
   if (!ws_bytes) return GDN_ERR_INVALID_ARG;
-  int S = 0, R = 0;
-  conv_ranges(p->T, p->C, sm_count(), &S, &R);
-  *ws_bytes = p->T > 0 ? (size_t)S * (p->W + 1) * p->C * sizeof(float) : 0;
+  *ws_bytes = p->T > 0 ? (size_t)conv_ranges(p->T, CV_RB) * (p->W + 1) * p->C * sizeof(float) : 0;
   return GDN_OK;
 }
 
@@ -348,10 +346,17 @@ gdn_status gdn_conv1d_fwd(const gdn_conv_problem* p, const void* x, const float*
   a.N = p->N;
   a.C = p->C;
   a.W = p->W;
-  int S = 0;
-  conv_ranges(p->T, p->C, sm_count(), &S, &a.R);
+  a.R = CV_RF;
+  const int S = conv_ranges(p->T, CV_RF);
+  if (S > 65535) return GDN_ERR_UNSUPPORTED;   // grid.y: more than 16.7 M tokens
+  const dim3 grid((p->C + CV_CH - 1) / CV_CH, S);
   prof_begin(K_CONV_FWD, stream);
-  conv_fwd_kernel<<<dim3((p->C + CV_CH - 1) / CV_CH, S), CV_THREADS, 0, stream>>>(a);
+  switch (p->W) {
+    case 1: conv_fwd_kernel<1><<<grid, CV_THREADS, 0, stream>>>(a); break;
+    case 2: conv_fwd_kernel<2><<<grid, CV_THREADS, 0, stream>>>(a); break;
+    case 3: conv_fwd_kernel<3><<<grid, CV_THREADS, 0, stream>>>(a); break;
+    default: conv_fwd_kernel<4><<<grid, CV_THREADS, 0, stream>>>(a); break;
+  }
   prof_end(K_CONV_FWD, stream);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -386,10 +391,16 @@ gdn_status gdn_conv1d_bwd(const gdn_conv_problem* p, const void* x, const float*
   a.N = p->N;
   a.C = p->C;
   a.W = p->W;
-  int S = 0;
-  conv_ranges(p->T, p->C, sm_count(), &S, &a.R);
+  a.R = CV_RB;
+  const int S = conv_ranges(p->T, CV_RB);
+  const dim3 grid((p->C + CV_CH - 1) / CV_CH, S);
   prof_begin(K_CONV_BWD, stream);
-  conv_bwd_kernel<<<dim3((p->C + CV_CH - 1) / CV_CH, S), CV_THREADS, 0, stream>>>(a);
+  switch (p->W) {
+    case 1: conv_bwd_kernel<1><<<grid, CV_THREADS, 0, stream>>>(a); break;
+    case 2: conv_bwd_kernel<2><<<grid, CV_THREADS, 0, stream>>>(a); break;
+    case 3: conv_bwd_kernel<3><<<grid, CV_THREADS, 0, stream>>>(a); break;
+    default: conv_bwd_kernel<4><<<grid, CV_THREADS, 0, stream>>>(a); break;
+  }
   conv_reduce_kernel<<<(p->C + 255) / 256, 256, 0, stream>>>(a, S);
   prof_end(K_CONV_BWD, stream);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
