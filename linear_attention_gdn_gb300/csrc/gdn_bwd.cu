@@ -365,7 +365,8 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
         float x[32];
         tmem_ld32(taddr(tb, warp * 32, BT_DS + h * 32), x);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) dS[h * 32 + e] = fmaf(gL, dS[h * 32 + e], x[e]);
+        for (int e = 0; e < 32; e += 2)
+          fma2_to(dS[h * 32 + e], dS[h * 32 + e + 1], gL, dS[h * 32 + e], dS[h * 32 + e + 1], x[e], x[e + 1]);
       }
       store_row128(ds_tile, tid, dS);
     }

@@ -195,6 +195,20 @@ __device__ __forceinline__ void tmem_ld_m64_async(uint32_t addr, uint32_t (&r)[8
                : "r"(addr));
 }
 
+// d0 = a0 b + d0, d1 = a1 b + d1 as one paired FP32 FMA (each component rounds as fmaf)
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b) {
+  const float2 r = __ffma2_rn(make_float2(a0, a1), make_float2(b, b), make_float2(d0, d1));
+  d0 = r.x;
+  d1 = r.y;
+}
+
+// (d0, d1) = (b a0 + c0, b a1 + c1) as one paired FP32 FMA
+__device__ __forceinline__ void fma2_to(float& d0, float& d1, float b, float a0, float a1, float c0, float c1) {
+  const float2 r = __ffma2_rn(make_float2(a0, a1), make_float2(b, b), make_float2(c0, c1));
+  d0 = r.x;
+  d1 = r.y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

@@ -307,7 +307,8 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
           float ds[32];
           tmem_ld32(taddr(tb, wq * 32, TM_DS + h * 32), ds);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) S[h * 32 + e] = fmaf(gL, S[h * 32 + e], ds[e]);
+          for (int e = 0; e < 32; e += 2)
+            fma2_to(S[h * 32 + e], S[h * 32 + e + 1], gL, S[h * 32 + e], S[h * 32 + e + 1], ds[e], ds[e + 1]);
         }
         if (with_o && !mbar_wait(&bar_o[n & 1], (n >> 1) & 1, a.err)) ok = false;
         store_state_row(s_tile, lt, S);   // also the saved state entering the next chunk

@@ -76,10 +76,8 @@ __device__ __forceinline__ void offdiag_level(float* Sm, int l) {
 #pragma unroll
       for (int q = 0; q < R / 4; ++q) {                       // A[oi + r][t] = S[t][oi + r]
         const float4 av = *reinterpret_cast<const float4*>(Sm + t * PR_ALD + oi + g * R + 4 * q);
-        p[4 * q + 0] = fmaf(av.x, tv, p[4 * q + 0]);
-        p[4 * q + 1] = fmaf(av.y, tv, p[4 * q + 1]);
-        p[4 * q + 2] = fmaf(av.z, tv, p[4 * q + 2]);
-        p[4 * q + 3] = fmaf(av.w, tv, p[4 * q + 3]);
+        fma2(p[4 * q + 0], p[4 * q + 1], av.x, av.y, tv);
+        fma2(p[4 * q + 2], p[4 * q + 3], av.z, av.w, tv);
       }
     }
   }
@@ -335,10 +333,11 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
 #pragma unroll
           for (int g4 = (jq + 1) >> 2; g4 < 4; ++g4) {
             const float4 av = *reinterpret_cast<const float4*>(Sm + (o + jq) * PR_ALD + o + 4 * g4);
-            if (4 * g4 + 0 > jq) x[4 * g4 + 0] = fmaf(-av.x, xj, x[4 * g4 + 0]);
-            if (4 * g4 + 1 > jq) x[4 * g4 + 1] = fmaf(-av.y, xj, x[4 * g4 + 1]);
-            if (4 * g4 + 2 > jq) x[4 * g4 + 2] = fmaf(-av.z, xj, x[4 * g4 + 2]);
-            if (4 * g4 + 3 > jq) x[4 * g4 + 3] = fmaf(-av.w, xj, x[4 * g4 + 3]);
+            // (pairs whose both rows lie below jq go as one paired FMA)
+            if (4 * g4 + 0 > jq) fma2(x[4 * g4 + 0], x[4 * g4 + 1], -av.x, -av.y, xj);
+            else if (4 * g4 + 1 > jq) x[4 * g4 + 1] = fmaf(-av.y, xj, x[4 * g4 + 1]);
+            if (4 * g4 + 2 > jq) fma2(x[4 * g4 + 2], x[4 * g4 + 3], -av.z, -av.w, xj);
+            else if (4 * g4 + 3 > jq) x[4 * g4 + 3] = fmaf(-av.w, xj, x[4 * g4 + 3]);
           }
         }
         __syncwarp();   // every lane of the block has read its A entries
