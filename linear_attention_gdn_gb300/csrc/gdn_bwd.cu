@@ -869,10 +869,12 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
             col4(gg, i, fg);
             col4(dd, i, fd);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 4; j += 2) {   // aq += (scale g) y, ak += dec z, two columns at a time
               const int e = 4 * i + j;
-              aq[e] = fmaf(a.scale * fg[j], y[e], aq[e]);
-              ak[e] = fmaf(fd[j], z[e], ak[e]);
+              float s0, s1;
+              mul2v(s0, s1, a.scale, a.scale, fg[j], fg[j + 1]);
+              fma2v(aq[e], aq[e + 1], s0, s1, y[e], y[e + 1]);
+              fma2v(ak[e], ak[e + 1], fd[j], fd[j + 1], z[e], z[e + 1]);
             }
           }
           tmem_st16(taddr(tb, w4 * 32, GT_DQ + cb0), aq);
@@ -885,10 +887,15 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
           col4(rq, i, fq);
           col4(rk, i, fk);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < 4; j += 2) {   // (((scale g) rq) q) y and (rk k) z, two columns at a time
             const int e = 4 * i + j, cc = cb0 + e;
-            y[e] = a.scale * fg[j] * fq[j] * ld_bf16(sm + GK_Q, cc, row, 64) * y[e];
-            z[e] = fk[j] * ld_bf16(sm + GK_K, cc, row, 64) * z[e];
+            float m0, m1, n0, n1;
+            mul2v(m0, m1, a.scale, a.scale, fg[j], fg[j + 1]);
+            mul2v(m0, m1, m0, m1, fq[j], fq[j + 1]);
+            mul2v(m0, m1, m0, m1, ld_bf16(sm + GK_Q, cc, row, 64), ld_bf16(sm + GK_Q, cc + 1, row, 64));
+            mul2v(y[e], y[e + 1], m0, m1, y[e], y[e + 1]);
+            mul2v(n0, n1, fk[j], fk[j + 1], ld_bf16(sm + GK_K, cc, row, 64), ld_bf16(sm + GK_K, cc + 1, row, 64));
+            mul2v(z[e], z[e + 1], n0, n1, z[e], z[e + 1]);
           }
         }
         const float sg = colsum16(y, lane);
@@ -902,10 +909,11 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
           const __nv_bfloat162* ha = reinterpret_cast<const __nv_bfloat162*>(&sa);
           const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&sb4);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 fa = __bfloat1622float2(ha[e]), fb = __bfloat1622float2(hb[e]);
-            sda[e] = fmaf(fa.x, fb.x, sda[e]);
-            sda[e] = fmaf(fa.y, fb.y, sda[e]);
+          for (int e = 0; e < 4; e += 2) {   // chains e and e + 1 together
+            const float2 fa0 = __bfloat1622float2(ha[e]), fb0 = __bfloat1622float2(hb[e]);
+            const float2 fa1 = __bfloat1622float2(ha[e + 1]), fb1 = __bfloat1622float2(hb[e + 1]);
+            fma2v(sda[e], sda[e + 1], fa0.x, fa1.x, fb0.x, fb1.x);
+            fma2v(sda[e], sda[e + 1], fa0.y, fa1.y, fb0.y, fb1.y);
           }
         }
         float sd = (sda[0] + sda[1]) + (sda[2] + sda[3]);

@@ -209,6 +209,18 @@ __device__ __forceinline__ void fma2_to(float& d0, float& d1, float b, float a0,
   d1 = r.y;
 }
 
+// (d0, d1) += (a0 b0, a1 b1) and (d0, d1) = (a0 b0, a1 b1) as paired FP32 instructions
+__device__ __forceinline__ void fma2v(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  const float2 r = __ffma2_rn(make_float2(a0, a1), make_float2(b0, b1), make_float2(d0, d1));
+  d0 = r.x;
+  d1 = r.y;
+}
+__device__ __forceinline__ void mul2v(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  const float2 r = __fmul2_rn(make_float2(a0, a1), make_float2(b0, b1));
+  d0 = r.x;
+  d1 = r.y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
