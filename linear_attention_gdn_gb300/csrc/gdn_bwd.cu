@@ -700,13 +700,14 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         *reinterpret_cast<uint4*>(sm + (tile ? GK_K : GK_Q) + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    {  // L2 norms of the q/k rows: four partial sums of 32 elements, combined as (p0 + p1) + (p2 + p3)
-       // (the prep kernel's order)
+    {  // L2 norms of the q/k rows: four partial sums of 32 elements (even- plus odd-element chain),
+       // combined as (p0 + p1) + (p2 + p3) (the prep kernel's order)
       const int rr = tid >> 2, qq = tid & 3;   // rows 0-63 k, 64-127 q
       const uint8_t* tile = sm + (rr < 64 ? GK_K : GK_Q);
       const int r = rr & 63;
       float ss = 0.f;
       if (r < L) {
+        float se = 0.f, so = 0.f;
 #pragma unroll
         for (int c8 = qq * 4; c8 < qq * 4 + 4; ++c8) {
           const uint4 val = *reinterpret_cast<const uint4*>(tile + sw_chunk(r, c8, 64));
@@ -714,10 +715,10 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 f = __bfloat1622float2(h2[e]);
-            ss = fmaf(f.x, f.x, ss);
-            ss = fmaf(f.y, f.y, ss);
+            fma2v(se, so, f.x, f.y, f.x, f.y);
           }
         }
+        ss = se + so;
       }
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
       ss += __shfl_xor_sync(0xffffffffu, ss, 2);

@@ -170,11 +170,12 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
     }
     __syncthreads();
   }
-  {  // L2 norm of row `row` of the tile: four partial sums of 32 elements, combined as (p0 + p1) + (p2 + p3)
+  {  // L2 norm of row `row` of the tile: four partial sums of 32 elements (each the sum of its even-
+     // and its odd-element chain, the two run as paired FMAs), combined as (p0 + p1) + (p2 + p3)
     float pr[4];
 #pragma unroll
     for (int qq = 0; qq < 4; ++qq) {
-      float ss = 0.f;
+      float se = 0.f, so = 0.f;
 #pragma unroll
       for (int c8 = qq * 4; c8 < qq * 4 + 4; ++c8) {
         const uint4 val = *reinterpret_cast<const uint4*>(sm + PR_KQ + sw_chunk(row, c8, 128));
@@ -182,11 +183,10 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = __bfloat1622float2(h2[e]);
-          ss = fmaf(f.x, f.x, ss);
-          ss = fmaf(f.y, f.y, ss);
+          fma2v(se, so, f.x, f.y, f.x, f.y);
         }
       }
-      pr[qq] = ss;
+      pr[qq] = se + so;
     }
     const float ss = (pr[0] + pr[1]) + (pr[2] + pr[3]);
     const float rn = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
