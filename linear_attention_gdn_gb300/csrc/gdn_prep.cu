@@ -112,10 +112,11 @@ __device__ __forceinline__ void offdiag_level(float* Sm, int l) {
   }
 }
 
-// One CTA per (chunk, value head); the three value heads of a q/k group are
-// adjacent in the grid, so two of them find the [K; Q] tile in L2.  Five CTAs
-// share an SM, so the serial phases of one (tile load, MMA, inverse, stores)
-// run under the others.
+// One CTA per (chunk, q/k head): the tile load, the norms and the KK^T / QK^T
+// MMA once, then the group's value heads one after another on that product
+// (each head's stores drain while the next one is prepared).  Five CTAs share
+// an SM, so the serial phases of one (tile load, MMA, inverse) run under the
+// others.
 __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(const __grid_constant__ PrepArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
   __shared__ int safe;
   __shared__ uint64_t bar, bar_kq;
   __shared__ uint32_t tslot;
-  const int c = blockIdx.x / a.HV, hv = blockIdx.x % a.HV, j = hv / a.G;
+  const int c = blockIdx.x / a.H, j = blockIdx.x % a.H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = tid;                   // TMEM lane = row of [KK^T; QK^T]
   if (*(volatile int*)a.err) return;
@@ -145,19 +146,22 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
     tma_load_3d(sm + PR_KQ + 16384, &a.tk, 64, j, tok0, &bar_kq);
     tma_load_3d(sm + PR_KQ + 24576, &a.tq, 64, j, tok0, &bar_kq);
   }
-  // the gates, requested while the tile lands (warp 3 scans them after the norms)
-  float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-  if (warp == 3) {
+  // the gates of a value head (warp 3: tokens 2 lane, 2 lane + 1); the first head's are requested
+  // while the tile lands, each later head's while the one before it is prepared
+  float gn0 = 0.f, gn1 = 0.f, bn0 = 0.f, bn1 = 0.f;
+  auto load_gates = [&](int hv_) {
     const int r0 = 2 * lane, r1 = r0 + 1;
+    gn0 = gn1 = bn0 = bn1 = 0.f;
     if (r0 < L) {
-      g0 = a.g[(size_t)(tok0 + r0) * a.HV + hv];
-      b0 = a.beta[(size_t)(tok0 + r0) * a.HV + hv];
+      gn0 = a.g[(size_t)(tok0 + r0) * a.HV + hv_];
+      bn0 = a.beta[(size_t)(tok0 + r0) * a.HV + hv_];
     }
     if (r1 < L) {
-      g1 = a.g[(size_t)(tok0 + r1) * a.HV + hv];
-      b1 = a.beta[(size_t)(tok0 + r1) * a.HV + hv];
+      gn1 = a.g[(size_t)(tok0 + r1) * a.HV + hv_];
+      bn1 = a.beta[(size_t)(tok0 + r1) * a.HV + hv_];
     }
-  }
+  };
+  if (warp == 3) load_gates(j * a.G);
   __syncthreads();
   if (!__syncthreads_and(mbar_wait(&bar_kq, 0, a.err))) {
     if (warp == 0) tmem_dealloc(tslot, 64);
@@ -205,208 +209,218 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
       mma_ss(tb, desc_k(sm_a, 128, ks), desc_k(sm_a, 128, ks), idesc(128, 64, 0, 0), ks > 0);
     mma_commit(&bar);
   }
-  if (warp == 3) {   // ---- gates (log2 units), under the MMA
-    const int r0 = 2 * lane, r1 = r0 + 1;
-    float s = g0 + g1;
+  // ---- the value heads of the group, one after another, on the one KK^T / QK^T
+  bool ok = true;
+  for (int hh = 0; hh < a.G; ++hh) {
+    const int hv = j * a.G + hh;
+    if (warp == 3) {   // ---- gates (log2 units)
+      const int r0 = 2 * lane, r1 = r0 + 1;
+      const float g0 = gn0, g1 = gn1, b0 = bn0, b1 = bn1;
+      if (hh + 1 < a.G) load_gates(hv + 1);
+      float s = g0 + g1;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += y;
+      }
+      const float ex = s - (g0 + g1);
+      const float G0v = (ex + g0) * kLog2e, G1v = (ex + g0 + g1) * kLog2e;
+      Gs[r0] = G0v;
+      Gs[r1] = G1v;
+      bs[r0] = b0;
+      bs[r1] = b1;
+      const float Gfirst = __shfl_sync(0xffffffffu, G0v, 0);
+      const float Glast = __shfl_sync(0xffffffffu, G1v, 31);   // = G_{L-1} (gates past L are 0)
+      eGr[r0] = exp2f(G0v - Gfirst);
+      eGr[r1] = exp2f(G1v - Gfirst);
+      const bool sf = (Gfirst - Glast) < kSafeRange;
+      eGi[r0] = sf ? exp2f(Gfirst - G0v) : 0.f;
+      eGi[r1] = sf ? exp2f(Gfirst - G1v) : 0.f;
+      cf[r0] = rk[r0] * eGi[r0];
+      cf[r1] = rk[r1] * eGi[r1];
+      ca[r0] = b0 * rk[r0] * eGr[r0];
+      ca[r1] = b1 * rk[r1] * eGr[r1];
+      pcol[r0] = b0 * exp2f(G0v) * rk[r0];
+      pcol[r1] = b1 * exp2f(G1v) * rk[r1];
+      if (lane == 0) safe = sf;
     }
-    const float ex = s - (g0 + g1);
-    const float G0v = (ex + g0) * kLog2e, G1v = (ex + g0 + g1) * kLog2e;
-    Gs[r0] = G0v;
-    Gs[r1] = G1v;
-    bs[r0] = b0;
-    bs[r1] = b1;
-    const float Gfirst = __shfl_sync(0xffffffffu, G0v, 0);
-    const float Glast = __shfl_sync(0xffffffffu, G1v, 31);   // = G_{L-1} (gates past L are 0)
-    eGr[r0] = exp2f(G0v - Gfirst);
-    eGr[r1] = exp2f(G1v - Gfirst);
-    const bool sf = (Gfirst - Glast) < kSafeRange;
-    eGi[r0] = sf ? exp2f(Gfirst - G0v) : 0.f;
-    eGi[r1] = sf ? exp2f(Gfirst - G1v) : 0.f;
-    cf[r0] = rk[r0] * eGi[r0];
-    cf[r1] = rk[r1] * eGi[r1];
-    ca[r0] = b0 * rk[r0] * eGr[r0];
-    ca[r1] = b1 * rk[r1] * eGr[r1];
-    pcol[r0] = b0 * exp2f(G0v) * rk[r0];
-    pcol[r1] = b1 * exp2f(G1v) * rk[r1];
-    if (lane == 0) safe = sf;
-  }
-  const bool ok = __syncthreads_and(mbar_wait(&bar, 0, a.err));
-  tc_fence_after();
-  float* Sm = reinterpret_cast<float*>(sm + PR_S);
-  if (ok) {
-    // ---- A^T (FP32, from the rows of KK^T), Aqk tile (rows of QK^T), scalars
-    const bool sf = safe;
+    // (the first head waits for the KK^T / QK^T MMA, every later one for the previous head's copies
+    // to have read the staging buffers it rewrites)
+    if (hh > 0 && tid == 0) bulk_wait_read();
+    ok = __syncthreads_and((hh > 0 || mbar_wait(&bar, 0, a.err)) && ok);
+    tc_fence_after();
+    float* Sm = reinterpret_cast<float*>(sm + PR_S);
+    if (ok) {
+      // ---- A^T (FP32, from the rows of KK^T), Aqk tile (rows of QK^T), scalars
+      const bool sf = safe;
 #pragma unroll 1
-    for (int cb0 = 0; cb0 < CH; cb0 += 32) {
-      float kq[32];   // row `row` of [KK^T; QK^T], columns cb0 .. cb0 + 31
-      tmem_ld32(taddr(tb, warp * 32, cb0), kq);
-      if (row < 64) {
-        // KK^T is symmetric, so the thread holding its row c writes row c of the transposed A:
-        // S[c][r] = A[r][c] = (beta_r rk_r e^{G_r - G_0}) (rk_c e^{G_0 - G_c}) KK[c][r] for c < r < L
-        const int cc = row;
-        if (sf) {
-          const float pc = cf[cc];
-#pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const int r0 = cb0 + 4 * e4;
-            const float4 f = *reinterpret_cast<const float4*>(&ca[r0]);
-            float4 v;
-            v.x = (r0 + 0 > cc && r0 + 0 < L) ? pc * f.x * kq[4 * e4 + 0] : 0.f;
-            v.y = (r0 + 1 > cc && r0 + 1 < L) ? pc * f.y * kq[4 * e4 + 1] : 0.f;
-            v.z = (r0 + 2 > cc && r0 + 2 < L) ? pc * f.z * kq[4 * e4 + 2] : 0.f;
-            v.w = (r0 + 3 > cc && r0 + 3 < L) ? pc * f.w * kq[4 * e4 + 3] : 0.f;
-            *reinterpret_cast<float4*>(Sm + cc * PR_ALD + r0) = v;
-          }
-        } else {
-          const float pc = rk[cc];
-#pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const int r0 = cb0 + 4 * e4;
-            float x[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int r = r0 + q;
-              x[q] = (r > cc && r < L) ? bs[r] * rk[r] * pc * exp2f(Gs[r] - Gs[cc]) * kq[4 * e4 + q] : 0.f;
-            }
-            *reinterpret_cast<float4*>(Sm + cc * PR_ALD + r0) = make_float4(x[0], x[1], x[2], x[3]);
-          }
-        }
-      } else {
-        const int r = row - 64;
-        const float pr = rq[r] * (sf ? eGr[r] : 1.f);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float x[8];
+      for (int cb0 = 0; cb0 < CH; cb0 += 32) {
+        float kq[32];   // row `row` of [KK^T; QK^T], columns cb0 .. cb0 + 31
+        tmem_ld32(taddr(tb, warp * 32, cb0), kq);
+        if (row < 64) {
+          // KK^T is symmetric, so the thread holding its row c writes row c of the transposed A:
+          // S[c][r] = A[r][c] = (beta_r rk_r e^{G_r - G_0}) (rk_c e^{G_0 - G_c}) KK[c][r] for c < r < L
+          const int cc = row;
           if (sf) {
-            const float4 fa = *reinterpret_cast<const float4*>(&cf[cb0 + q4 * 8]);
-            const float4 fb = *reinterpret_cast<const float4*>(&cf[cb0 + q4 * 8 + 4]);
-            const float fv[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+            const float pc = cf[cc];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int jj = cb0 + q4 * 8 + e;
-              x[e] = (jj <= r && r < L) ? pr * fv[e] * kq[q4 * 8 + e] : 0.f;
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const int r0 = cb0 + 4 * e4;
+              const float4 f = *reinterpret_cast<const float4*>(&ca[r0]);
+              float4 v;
+              v.x = (r0 + 0 > cc && r0 + 0 < L) ? pc * f.x * kq[4 * e4 + 0] : 0.f;
+              v.y = (r0 + 1 > cc && r0 + 1 < L) ? pc * f.y * kq[4 * e4 + 1] : 0.f;
+              v.z = (r0 + 2 > cc && r0 + 2 < L) ? pc * f.z * kq[4 * e4 + 2] : 0.f;
+              v.w = (r0 + 3 > cc && r0 + 3 < L) ? pc * f.w * kq[4 * e4 + 3] : 0.f;
+              *reinterpret_cast<float4*>(Sm + cc * PR_ALD + r0) = v;
             }
           } else {
+            const float pc = rk[cc];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int jj = cb0 + q4 * 8 + e;
-              x[e] = (jj <= r && r < L) ? pr * rk[jj] * exp2f(Gs[r] - Gs[jj]) * kq[q4 * 8 + e] : 0.f;
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const int r0 = cb0 + 4 * e4;
+              float x[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int r = r0 + q;
+                x[q] = (r > cc && r < L) ? bs[r] * rk[r] * pc * exp2f(Gs[r] - Gs[cc]) * kq[4 * e4 + q] : 0.f;
+              }
+              *reinterpret_cast<float4*>(Sm + cc * PR_ALD + r0) = make_float4(x[0], x[1], x[2], x[3]);
             }
           }
-          uint4 w;
-          w.x = pack_bf16(x[0], x[1]);
-          w.y = pack_bf16(x[2], x[3]);
-          w.z = pack_bf16(x[4], x[5]);
-          w.w = pack_bf16(x[6], x[7]);
-          *reinterpret_cast<uint4*>(sm + PR_AQ + sw_chunk(r, (cb0 >> 3) + q4, 64)) = w;
-        }
-      }
-    }
-    if (row < 64) {
-      const int r = row;
-      float* sc = reinterpret_cast<float*>(sm + PR_SC);
-      const float GL = Gs[L - 1];
-      sc[r] = r < L ? a.scale * exp2f(Gs[r]) * rq[r] : 0.f;
-      sc[64 + r] = r < L ? exp2f(GL - Gs[r]) * rk[r] : 0.f;
-      if (r == 0) {
-        sc[128] = exp2f(GL);
-        reinterpret_cast<int*>(sc)[129] = L;
-      }
-      // ---- T = (I + A)^-1 by 16 x 16 blocks on warps 0-1 (64 lanes).  One FP32 array S[p][q]
-      // (pitch PR_ALD) holds A[r][c] (c < r) at S[c][r] and T[r][c] (c <= r) at S[r][c].
-      //   diagonal blocks  T_bb = (I + A_bb)^-1, forward substitution, lane = column
-      //   block diagonal d T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj (i - j = d), lane = (block, column)
-      const int l = row;
-      named_bar(1, 64);
-      {  // diagonal blocks
-        const int o = 16 * (l >> 4), cc = l & 15;
-        float x[16];
+        } else {
+          const int r = row - 64;
+          const float pr = rq[r] * (sf ? eGr[r] : 1.f);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = (i == cc) ? 1.f : 0.f;
+          for (int q4 = 0; q4 < 4; ++q4) {
+            float x[8];
+            if (sf) {
+              const float4 fa = *reinterpret_cast<const float4*>(&cf[cb0 + q4 * 8]);
+              const float4 fb = *reinterpret_cast<const float4*>(&cf[cb0 + q4 * 8 + 4]);
+              const float fv[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
 #pragma unroll
-        for (int jq = 0; jq < 15; ++jq) {
-          const float xj = x[jq];
+              for (int e = 0; e < 8; ++e) {
+                const int jj = cb0 + q4 * 8 + e;
+                x[e] = (jj <= r && r < L) ? pr * fv[e] * kq[q4 * 8 + e] : 0.f;
+              }
+            } else {
 #pragma unroll
-          for (int g4 = (jq + 1) >> 2; g4 < 4; ++g4) {
-            const float4 av = *reinterpret_cast<const float4*>(Sm + (o + jq) * PR_ALD + o + 4 * g4);
-            // (pairs whose both rows lie below jq go as one paired FMA)
-            if (4 * g4 + 0 > jq) fma2(x[4 * g4 + 0], x[4 * g4 + 1], -av.x, -av.y, xj);
-            else if (4 * g4 + 1 > jq) x[4 * g4 + 1] = fmaf(-av.y, xj, x[4 * g4 + 1]);
-            if (4 * g4 + 2 > jq) fma2(x[4 * g4 + 2], x[4 * g4 + 3], -av.z, -av.w, xj);
-            else if (4 * g4 + 3 > jq) x[4 * g4 + 3] = fmaf(-av.w, xj, x[4 * g4 + 3]);
+              for (int e = 0; e < 8; ++e) {
+                const int jj = cb0 + q4 * 8 + e;
+                x[e] = (jj <= r && r < L) ? pr * rk[jj] * exp2f(Gs[r] - Gs[jj]) * kq[q4 * 8 + e] : 0.f;
+              }
+            }
+            uint4 w;
+            w.x = pack_bf16(x[0], x[1]);
+            w.y = pack_bf16(x[2], x[3]);
+            w.z = pack_bf16(x[4], x[5]);
+            w.w = pack_bf16(x[6], x[7]);
+            *reinterpret_cast<uint4*>(sm + PR_AQ + sw_chunk(r, (cb0 >> 3) + q4, 64)) = w;
           }
         }
-        __syncwarp();   // every lane of the block has read its A entries
-#pragma unroll
-        for (int i = 0; i < 16; ++i) Sm[(o + i) * PR_ALD + o + cc] = x[i];   // x[i] = 0 above the diagonal
       }
-      named_bar(1, 64);
-      // off-diagonal blocks, one block diagonal d at a time (then T_ij is complete for i - j = d)
-      offdiag_level<1>(Sm, l);
-      named_bar(1, 64);
-      offdiag_level<2>(Sm, l);
-      named_bar(1, 64);
-      offdiag_level<3>(Sm, l);
+      if (row < 64) {
+        const int r = row;
+        float* sc = reinterpret_cast<float*>(sm + PR_SC);
+        const float GL = Gs[L - 1];
+        sc[r] = r < L ? a.scale * exp2f(Gs[r]) * rq[r] : 0.f;
+        sc[64 + r] = r < L ? exp2f(GL - Gs[r]) * rk[r] : 0.f;
+        if (r == 0) {
+          sc[128] = exp2f(GL);
+          reinterpret_cast<int*>(sc)[129] = L;
+        }
+        // ---- T = (I + A)^-1 by 16 x 16 blocks on warps 0-1 (64 lanes).  One FP32 array S[p][q]
+        // (pitch PR_ALD) holds A[r][c] (c < r) at S[c][r] and T[r][c] (c <= r) at S[r][c].
+        //   diagonal blocks  T_bb = (I + A_bb)^-1, forward substitution, lane = column
+        //   block diagonal d T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj (i - j = d), lane = (block, column)
+        const int l = row;
+        named_bar(1, 64);
+        {  // diagonal blocks
+          const int o = 16 * (l >> 4), cc = l & 15;
+          float x[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[i] = (i == cc) ? 1.f : 0.f;
+#pragma unroll
+          for (int jq = 0; jq < 15; ++jq) {
+            const float xj = x[jq];
+#pragma unroll
+            for (int g4 = (jq + 1) >> 2; g4 < 4; ++g4) {
+              const float4 av = *reinterpret_cast<const float4*>(Sm + (o + jq) * PR_ALD + o + 4 * g4);
+              // (pairs whose both rows lie below jq go as one paired FMA)
+              if (4 * g4 + 0 > jq) fma2(x[4 * g4 + 0], x[4 * g4 + 1], -av.x, -av.y, xj);
+              else if (4 * g4 + 1 > jq) x[4 * g4 + 1] = fmaf(-av.y, xj, x[4 * g4 + 1]);
+              if (4 * g4 + 2 > jq) fma2(x[4 * g4 + 2], x[4 * g4 + 3], -av.z, -av.w, xj);
+              else if (4 * g4 + 3 > jq) x[4 * g4 + 3] = fmaf(-av.w, xj, x[4 * g4 + 3]);
+            }
+          }
+          __syncwarp();   // every lane of the block has read its A entries
+#pragma unroll
+          for (int i = 0; i < 16; ++i) Sm[(o + i) * PR_ALD + o + cc] = x[i];   // x[i] = 0 above the diagonal
+        }
+        named_bar(1, 64);
+        // off-diagonal blocks, one block diagonal d at a time (then T_ij is complete for i - j = d)
+        offdiag_level<1>(Sm, l);
+        named_bar(1, 64);
+        offdiag_level<2>(Sm, l);
+        named_bar(1, 64);
+        offdiag_level<3>(Sm, l);
+      }
     }
-  }
-  __syncthreads();   // T complete, Aqk and the scalars staged
-  if (ok) {
-    // ---- the T', T'', T tiles, all 128 threads: 16-byte chunks (row i, columns 8 c8 .. 8 c8 + 7);
-    // first every thread reads its four chunks of T, then (after a barrier) overwrites the array
-    float tv[4][8];
+    __syncthreads();   // T complete, Aqk and the scalars staged
+    if (ok) {
+      // ---- the T', T'', T tiles, all 128 threads: 16-byte chunks (row i, columns 8 c8 .. 8 c8 + 7);
+      // first every thread reads its four chunks of T, then (after a barrier) overwrites the array
+      float tv[4][8];
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int item = tid + PR_THREADS * it, i = item >> 3, c8 = item & 7;
-      const float4 u0 = *reinterpret_cast<const float4*>(Sm + i * PR_ALD + 8 * c8);
-      const float4 u1 = *reinterpret_cast<const float4*>(Sm + i * PR_ALD + 8 * c8 + 4);
-      const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      for (int it = 0; it < 4; ++it) {
+        const int item = tid + PR_THREADS * it, i = item >> 3, c8 = item & 7;
+        const float4 u0 = *reinterpret_cast<const float4*>(Sm + i * PR_ALD + 8 * c8);
+        const float4 u1 = *reinterpret_cast<const float4*>(Sm + i * PR_ALD + 8 * c8 + 4);
+        const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) tv[it][e] = 8 * c8 + e <= i ? u[e] : 0.f;   // above the diagonal: A^T
+        for (int e = 0; e < 8; ++e) tv[it][e] = 8 * c8 + e <= i ? u[e] : 0.f;   // above the diagonal: A^T
+      }
+      __syncthreads();
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int item = tid + PR_THREADS * it, i = item >> 3, c8 = item & 7;
+        const float4 p0 = *reinterpret_cast<const float4*>(pcol + 8 * c8);
+        const float4 p1 = *reinterpret_cast<const float4*>(pcol + 8 * c8 + 4);
+        const float4 q0 = *reinterpret_cast<const float4*>(bs + 8 * c8);
+        const float4 q1 = *reinterpret_cast<const float4*>(bs + 8 * c8 + 4);
+        const float pc[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        const float bc[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        uint4 w1, w2, w3;
+        w1.x = pack_bf16(tv[it][0] * pc[0], tv[it][1] * pc[1]);
+        w1.y = pack_bf16(tv[it][2] * pc[2], tv[it][3] * pc[3]);
+        w1.z = pack_bf16(tv[it][4] * pc[4], tv[it][5] * pc[5]);
+        w1.w = pack_bf16(tv[it][6] * pc[6], tv[it][7] * pc[7]);
+        w2.x = pack_bf16(tv[it][0] * bc[0], tv[it][1] * bc[1]);
+        w2.y = pack_bf16(tv[it][2] * bc[2], tv[it][3] * bc[3]);
+        w2.z = pack_bf16(tv[it][4] * bc[4], tv[it][5] * bc[5]);
+        w2.w = pack_bf16(tv[it][6] * bc[6], tv[it][7] * bc[7]);
+        w3.x = pack_bf16(tv[it][0], tv[it][1]);
+        w3.y = pack_bf16(tv[it][2], tv[it][3]);
+        w3.z = pack_bf16(tv[it][4], tv[it][5]);
+        w3.w = pack_bf16(tv[it][6], tv[it][7]);
+        const uint32_t off = sw_chunk(i, c8, 64);
+        *reinterpret_cast<uint4*>(sm + PR_TP + off) = w1;                  // T'
+        *reinterpret_cast<uint4*>(sm + PR_TP + TILE64_BYTES + off) = w2;   // T''
+        if (a.write_T) *reinterpret_cast<uint4*>(sm + PR_T + off) = w3;     // T
+      }
+      fence_async_smem();
     }
     __syncthreads();
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int item = tid + PR_THREADS * it, i = item >> 3, c8 = item & 7;
-      const float4 p0 = *reinterpret_cast<const float4*>(pcol + 8 * c8);
-      const float4 p1 = *reinterpret_cast<const float4*>(pcol + 8 * c8 + 4);
-      const float4 q0 = *reinterpret_cast<const float4*>(bs + 8 * c8);
-      const float4 q1 = *reinterpret_cast<const float4*>(bs + 8 * c8 + 4);
-      const float pc[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-      const float bc[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-      uint4 w1, w2, w3;
-      w1.x = pack_bf16(tv[it][0] * pc[0], tv[it][1] * pc[1]);
-      w1.y = pack_bf16(tv[it][2] * pc[2], tv[it][3] * pc[3]);
-      w1.z = pack_bf16(tv[it][4] * pc[4], tv[it][5] * pc[5]);
-      w1.w = pack_bf16(tv[it][6] * pc[6], tv[it][7] * pc[7]);
-      w2.x = pack_bf16(tv[it][0] * bc[0], tv[it][1] * bc[1]);
-      w2.y = pack_bf16(tv[it][2] * bc[2], tv[it][3] * bc[3]);
-      w2.z = pack_bf16(tv[it][4] * bc[4], tv[it][5] * bc[5]);
-      w2.w = pack_bf16(tv[it][6] * bc[6], tv[it][7] * bc[7]);
-      w3.x = pack_bf16(tv[it][0], tv[it][1]);
-      w3.y = pack_bf16(tv[it][2], tv[it][3]);
-      w3.z = pack_bf16(tv[it][4], tv[it][5]);
-      w3.w = pack_bf16(tv[it][6], tv[it][7]);
-      const uint32_t off = sw_chunk(i, c8, 64);
-      *reinterpret_cast<uint4*>(sm + PR_TP + off) = w1;                  // T'
-      *reinterpret_cast<uint4*>(sm + PR_TP + TILE64_BYTES + off) = w2;   // T''
-      if (a.write_T) *reinterpret_cast<uint4*>(sm + PR_T + off) = w3;     // T
+    if (ok && tid == 0) {   // ship the staged blocks: T' T'' (contiguous), Aqk, T, scalars
+      uint8_t* cbp = a.cb + ((size_t)c * a.HV + hv) * CB_BYTES;
+      bulk_store(cbp + CB_TP, sm + PR_TP, 2 * TILE64_BYTES);
+      bulk_store(cbp + CB_AQK, sm + PR_AQ, TILE64_BYTES);
+      if (a.write_T) bulk_store(cbp + CB_T, sm + PR_T, TILE64_BYTES);
+      bulk_store(cbp + CB_SCAL, sm + PR_SC, CB_SCAL_BYTES);
+      bulk_commit();
     }
-    fence_async_smem();
   }
-  __syncthreads();
-  if (ok && tid == 0) {   // ship the staged blocks: T' T'' (contiguous), Aqk, T, scalars
-    uint8_t* cbp = a.cb + ((size_t)c * a.HV + hv) * CB_BYTES;
-    bulk_store(cbp + CB_TP, sm + PR_TP, 2 * TILE64_BYTES);
-    bulk_store(cbp + CB_AQK, sm + PR_AQ, TILE64_BYTES);
-    if (a.write_T) bulk_store(cbp + CB_T, sm + PR_T, TILE64_BYTES);
-    bulk_store(cbp + CB_SCAL, sm + PR_SC, CB_SCAL_BYTES);
-    bulk_commit();
-    bulk_wait_read();   // shared memory must outlive the copies' reads
-  }
+  if (tid == 0) bulk_wait_read();   // shared memory must outlive the copies' reads
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, 64);
@@ -418,7 +432,7 @@ void setup_prep_attrs() {
 void launch_prep(const PrepArgs& a, int NC, cudaStream_t s) {
   if (NC <= 0) return;
   prof_begin(K_PREP, s);
-  prep_kernel<<<NC * a.HV, PR_THREADS, PR_SMEM_ALLOC, s>>>(a);
+  prep_kernel<<<NC * a.H, PR_THREADS, PR_SMEM_ALLOC, s>>>(a);
   prof_end(K_PREP, s);
 }
 
