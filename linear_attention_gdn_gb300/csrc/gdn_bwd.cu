@@ -273,15 +273,9 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
         tmem_st8(taddr(tb, warp * 32, BT_ADO + q * 8), p8);
       }
     }
-    ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err) && (!pre || mbar_wait(&bar_pre, pph, a.err)));
-    mph ^= 1;
-    if (pre) {
-      pph ^= 1;
-      pend = false;
-    }
-    if (!ok) break;
-    tc_fence_after();
-    {
+    // -W^T -> shared (row tid = dk index), the B operand of MMA2: while DY runs when W^T came from
+    // the previous iteration, else after it
+    auto w_hop = [&]() {
       float w[64];
       tmem_ld32(taddr(tb, warp * 32, BT_DW), w);
       tmem_ld32(taddr(tb, warp * 32, BT_DW + 32), w + 32);
@@ -295,6 +289,21 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
         v.w = pack_bf16(-w[c8 * 8 + 6], -w[c8 * 8 + 7]);
         *reinterpret_cast<uint4*>(wt + sw_chunk(tid, c8, 128)) = v;
       }
+    };
+    if (pre) {
+      const bool got = mbar_wait(&bar_pre, pph, a.err);
+      pph ^= 1;
+      pend = false;
+      tc_fence_after();
+      if (got) w_hop();
+      ok = got;
+    }
+    ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err) && ok);
+    mph ^= 1;
+    if (!ok) break;
+    tc_fence_after();
+    {
+      if (!pre) w_hop();
       const float* kd = scal + 64;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
