@@ -483,7 +483,13 @@ constexpr int GT_DQ = 0, GT_DK = 64, GT_A0 = 128, GT_A1 = 192, GT_A2 = 256, GT_A
 
 constexpr int GK_NWG = 4;                    // warpgroups; each takes GK_CW of the 64 token columns
 constexpr int GK_CW = 64 / GK_NWG;
-constexpr int GK_THREADS = 128 * GK_NWG;
+constexpr int GK_THREADS = 128 * GK_NWG;     // the compute warpgroups
+constexpr int GK_LAUNCH = GK_THREADS + 128;  // plus one warpgroup whose first warp issues MB and M5
+// registers per thread after the split (the launch gives 65536 / 640 = 96): the MMA warpgroup gives
+// up all but 32, the compute warpgroups take them
+constexpr int GK_REG_COMPUTE = 112, GK_REG_MMA = 32;
+static_assert(GK_THREADS * GK_REG_COMPUTE + 128 * GK_REG_MMA <= GK_LAUNCH * 96, "register split");
+constexpr int GK_BAR = 2;                    // named barrier of the compute warpgroups
 
 // sum over the 32 lanes of a warp of column `lane & 15` of v[16] (fixed order)
 __device__ __forceinline__ float colsum16(float (&v)[16], int lane) {
@@ -526,10 +532,10 @@ __device__ __forceinline__ void store_chunk8(uint8_t* tile, int r, int c8, int R
 // first value head after the last one) are requested as soon as the buffers
 // they land in are dead, and its MA is issued right after M6, so that it runs
 // under the per-token totals (warps 2-3) and the next gate scan (warp 4).
-__global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_constant__ GradArgs a) {
+__global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constant__ GradArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
-  __shared__ uint64_t bar_qk, bar_vn, bar_sv, bar_do, bar_dt, bar_ma, mma_bar;
+  __shared__ uint64_t bar_qk, bar_vn, bar_sv, bar_do, bar_dt, bar_ma, mma_bar, go_mma, done_mma;
   __shared__ uint32_t tslot;
   __shared__ __align__(16) float rq[CH], rk[CH];
   // gates of the current and the next value head (double-buffered)
@@ -557,6 +563,8 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     mbar_init(&bar_dt, 1);
     mbar_init(&bar_ma, 1);
     mbar_init(&mma_bar, 1);
+    mbar_init(&go_mma, 1);
+    mbar_init(&done_mma, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   __syncthreads();
@@ -634,7 +642,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
   uint32_t mph = 0, maph = 0, qkph = 0;
   bool ok = true;
   auto mma_sync_wait = [&]() -> bool {
-    bool r = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
+    bool r = bar_and(GK_BAR, GK_THREADS, mbar_wait(&mma_bar, mph, a.err));
     mph ^= 1;
     tc_fence_after();
     return r;
@@ -642,8 +650,14 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
   auto handoff = [&]() {   // generic smem/TMEM writes -> visible to the next MMAs
     fence_async_smem();
     tc_fence_before();
-    __syncthreads();
+    named_bar(GK_BAR, GK_THREADS);
     tc_fence_after();
+  };
+  auto handoff_to_mma_warp = [&]() {   // the same, with the MMA warp issuing the next group
+    fence_async_smem();
+    tc_fence_before();
+    named_bar(GK_BAR, GK_THREADS);
+    if (tid == 0) mbar_arrive(&go_mma);
   };
   const uint32_t s_q = smem_u32(sm + GK_Q), s_k = smem_u32(sm + GK_K), s_v = smem_u32(sm + GK_V),
                  s_do = smem_u32(sm + GK_DO), s_s = smem_u32(sm + GK_S), s_ds = smem_u32(sm + GK_DS),
@@ -692,6 +706,40 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     }
     if (warp == 4) gates(0, j * a.G, tok0, a.chunk_len[c]);
   }
+  if (tid >= GK_THREADS) {
+    // ================= MMA warpgroup: its first warp issues MB and M5 of every value head =========
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(GK_REG_MMA));
+    if (warp == GK_THREADS / 32) {
+      uint32_t gph = 0;
+      bool live = true;
+      for (int item = blockIdx.x; live && item < n_items; item += gridDim.x)
+        for (int h = 0; live && h < a.G; ++h) {
+          // MB: dW K^T (M = 64), Y^T = dW^T T
+          if (!(live = mbar_wait(&go_mma, gph, a.err))) break;
+          gph ^= 1;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ss_w(tb + GT_A0, desc_mn(s_wd, 128, ks), desc_k(s_k, 64, ks), idesc(64, 64, 1, 0), ks > 0);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ss_w(tb + GT_A2, desc_k(s_wd, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
+          mma_commit_w(&mma_bar);
+          // M5: T^T R1 (= -dA, M = 64)
+          if (!(live = mbar_wait(&go_mma, gph, a.err))) break;
+          gph ^= 1;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ss_w(tb + GT_A0, desc_mn(s_t, 64, ks), desc_mn(s_r1, 64, ks), idesc(64, 64, 1, 1), ks > 0);
+          mma_commit_w(&mma_bar);
+        }
+      mma_commit_w(&done_mma);   // arrives once every MMA this warp issued has completed
+    }
+    return;
+  }
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(GK_REG_COMPUTE));
+  // ================= compute warpgroups ============================================================
   // token range of the current item (the next item's is read during its predecessor's last value head)
   int it_tok0 = a.chunk_tok0[blockIdx.x % a.NC], it_L = a.chunk_len[blockIdx.x % a.NC];
   for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
@@ -700,7 +748,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     const int nxt = item + gridDim.x;
     int nx_tok0 = 0, nx_L = 0;
     // ---- Q, K of the item: norms and the FP32 [QK^T lower | KK^T upper] table
-    ok = __syncthreads_and(mbar_wait(&bar_qk, qkph, a.err));
+    ok = bar_and(GK_BAR, GK_THREADS, mbar_wait(&bar_qk, qkph, a.err));
     qkph ^= 1;
     if (!ok) break;
     if (L < CH) {   // zero the Q, K rows past the document end (they hold the next document)
@@ -784,7 +832,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         tma_prefetch_3d(&a.tk, 64, nhv / a.G, ntok0);
       }
       // this head's tiles (every thread waits: that also makes them visible to its reads)
-      ok = __syncthreads_and(mbar_wait(&bar_vn, vph, a.err) & mbar_wait(&bar_sv, vph, a.err) &
+      ok = bar_and(GK_BAR, GK_THREADS, mbar_wait(&bar_vn, vph, a.err) & mbar_wait(&bar_sv, vph, a.err) &
                              mbar_wait(&bar_do, vph, a.err) & mbar_wait(&bar_dt, vph, a.err));
       if (!ok) break;
       const float gL = scal[128];
@@ -800,7 +848,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         if (tid == 0) issue_ma();
       }
       ma_issued = false;
-      ok = __syncthreads_and(mbar_wait(&bar_ma, maph, a.err));
+      ok = bar_and(GK_BAR, GK_THREADS, mbar_wait(&bar_ma, maph, a.err));
       maph ^= 1;
       tc_fence_after();
       if (!ok) break;
@@ -823,17 +871,8 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
           store_chunk8(sm + GK_WD, row, (cb0 >> 3) + q4, 128, t8);
         }
       }
-      handoff();
-      // ---- MB: dW K^T (M = 64), Y^T = dW^T T
-      if (tid == 0) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ss(tb + GT_A0, desc_mn(s_wd, 128, ks), desc_k(s_k, 64, ks), idesc(64, 64, 1, 0), ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ss(tb + GT_A2, desc_k(s_wd, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
-        mma_commit(&mma_bar);
-      }
+      // ---- MB: dW K^T (M = 64), Y^T = dW^T T, issued by the MMA warp
+      handoff_to_mma_warp();
       const bool full = L == CH;   // full chunk: dv goes out as a staged tile (TMA store)
       {  // HA side work: dv; the column-scaled terms pg S dO^T into dq^T and dec dKd^T into dk^T (TMEM
          // read-modify-write: no MMA touches them until M4); partial sums for dg
@@ -1054,14 +1093,8 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
                 pack_bf16(__uint_as_float(u[i]), __uint_as_float(u[i + 1]));
           }
       }
-      handoff();
-      // ---- M5: T^T R1 (= -dA, M = 64)
-      if (tid == 0) {
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ss(tb + GT_A0, desc_mn(s_t, 64, ks), desc_mn(s_r1, 64, ks), idesc(64, 64, 1, 1), ks > 0);
-        mma_commit(&mma_bar);
-      }
+      // ---- M5: T^T R1 (= -dA, M = 64), issued by the MMA warp
+      handoff_to_mma_warp();
       {  // H4 side work: beta gamma Y^T into dk^T (TMEM: M4 is done, M6 not yet issued)
         float yv[GK_CW], ak[GK_CW];
         tld2(GT_A2, yv, GT_DK, ak);   // Y^T = dW^T T (rows = dk index)
@@ -1201,7 +1234,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
         }
       }
       if (warp == 4 && has_next) gates(gb ^ 1, nhv, ntok0, nL);
-      __syncthreads();
+      named_bar(GK_BAR, GK_THREADS);
     }
     if (!ok) break;
 
@@ -1229,7 +1262,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       }
     }
     tc_fence_before();   // the TMEM reads of DQ / DK precede the next item's table MMAs
-    __syncthreads();     // the Q, K tiles are free
+    named_bar(GK_BAR, GK_THREADS);     // the Q, K tiles are free
     if (tid == 0 && nxt < n_items) issue_qk(nxt / a.NC, nx_tok0);
     if (tid < CH) {      // d|x|/dx . g = (g - x (x . g) / |x|^2) / |x|: the per-token factor (x . g) / |x|^3
       float xq = 0.f, xk = 0.f;
@@ -1242,7 +1275,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       lq[tid] = xq * nq * nq * nq;
       lk[tid] = xk * nk * nk * nk;
     }
-    __syncthreads();
+    named_bar(GK_BAR, GK_THREADS);
     {
       const bool full = L == CH;   // full chunk: staged tiles and TMA stores
       uint8_t* sq_tile = sm + GK_WD;   // both regions are dead until the next item's first value head
@@ -1267,7 +1300,7 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
       }
       if (full) {
         fence_async_smem();
-        __syncthreads();
+        named_bar(GK_BAR, GK_THREADS);
         if (tid == 0) {
           tma_store_3d(&a.tdq, sq_tile, 0, j, tok0);
           tma_store_3d(&a.tdq, sq_tile + 8192, 64, j, tok0);
@@ -1281,10 +1314,12 @@ __global__ void __launch_bounds__(GK_THREADS, 1) grad_kernel(const __grid_consta
     it_L = nx_L;
   }
   if (tid == 0) bulk_wait_all();
-  // an MA issued for a value head that never ran must not be left in flight
+  // an MA issued for a value head that never ran must not be left in flight, nor any MMA of the
+  // MMA warp
   if (ma_issued && tid == 0) mbar_wait(&bar_ma, maph, a.err);
+  if (tid == 0) mbar_wait(&done_mma, 0, a.err);
   tc_fence_before();
-  __syncthreads();
+  named_bar(GK_BAR, GK_THREADS);
   if (warp == 0) tmem_dealloc(tb, 512);
 }
 
@@ -1418,7 +1453,7 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
   ga.scale = pr.scale;
   ga.err = reinterpret_cast<int*>(ws);
   prof_begin(K_GRAD, s);
-  grad_kernel<<<std::min(P.NC * P.H, P.sms), GK_THREADS, GK_SMEM_ALLOC, s>>>(ga);
+  grad_kernel<<<std::min(P.NC * P.H, P.sms), GK_LAUNCH, GK_SMEM_ALLOC, s>>>(ga);
   prof_end(K_GRAD, s);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
