@@ -484,7 +484,7 @@ constexpr int GT_DQ = 0, GT_DK = 64, GT_A0 = 128, GT_A1 = 192, GT_A2 = 256, GT_A
 constexpr int GK_NWG = 4;                    // warpgroups; each takes GK_CW of the 64 token columns
 constexpr int GK_CW = 64 / GK_NWG;
 constexpr int GK_THREADS = 128 * GK_NWG;     // the compute warpgroups
-constexpr int GK_LAUNCH = GK_THREADS + 128;  // plus one warpgroup whose first warp issues MB and M5
+constexpr int GK_LAUNCH = GK_THREADS + 128;  // plus one warpgroup whose first warp issues most MMAs
 // registers per thread after the split (the launch gives 65536 / 640 = 96): the MMA warpgroup gives
 // up all but 32, the compute warpgroups take them
 constexpr int GK_REG_COMPUTE = 112, GK_REG_MMA = 32;
@@ -535,7 +535,10 @@ __device__ __forceinline__ void store_chunk8(uint8_t* tile, int r, int c8, int R
 __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constant__ GradArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
-  __shared__ uint64_t bar_qk, bar_vn, bar_sv, bar_do, bar_dt, bar_ma, mma_bar, go_mma, done_mma;
+  // go_mma / go_ma: the compute warpgroups hand MB, M5, M6 / a value head's first MA to the MMA warp.
+  // Consecutive arrivals on each are separated by a wait on a commit the MMA warp makes after
+  // consuming the earlier one, so no phase is passed before its waiter saw it.
+  __shared__ uint64_t bar_qk, bar_vn, bar_sv, bar_do, bar_dt, bar_ma, mma_bar, go_mma, go_ma, done_mma;
   __shared__ uint32_t tslot;
   __shared__ __align__(16) float rq[CH], rk[CH];
   // gates of the current and the next value head (double-buffered)
@@ -564,6 +567,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
     mbar_init(&bar_ma, 1);
     mbar_init(&mma_bar, 1);
     mbar_init(&go_mma, 1);
+    mbar_init(&go_ma, 1);
     mbar_init(&done_mma, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
@@ -653,11 +657,11 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
     named_bar(GK_BAR, GK_THREADS);
     tc_fence_after();
   };
-  auto handoff_to_mma_warp = [&]() {   // the same, with the MMA warp issuing the next group
+  auto handoff_to_mma_warp = [&](uint64_t* go_bar) {   // the same, with the MMA warp issuing next
     fence_async_smem();
     tc_fence_before();
     named_bar(GK_BAR, GK_THREADS);
-    if (tid == 0) mbar_arrive(&go_mma);
+    if (tid == 0) mbar_arrive(go_bar);
   };
   const uint32_t s_q = smem_u32(sm + GK_Q), s_k = smem_u32(sm + GK_K), s_v = smem_u32(sm + GK_V),
                  s_do = smem_u32(sm + GK_DO), s_s = smem_u32(sm + GK_S), s_ds = smem_u32(sm + GK_DS),
@@ -676,24 +680,30 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
     as_float16(r0, o0);
     as_float16(r1, o1);
   };
-  // MA, from the tiles of the value head in the load buffers
-  auto issue_ma = [&]() {
+  // MA, from the tiles of the value head in the load buffers, in two parts: the products of
+  // V_new^T, S, dS', dO (loads vn, sv, do), then those of dV_new^T and T (load dt)
+  auto issue_ma1 = [&]() {
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      mma_ss(tb + GT_A4, desc_k(s_do, 64, ks), desc_mn(s_vn, 128, ks), idesc(64, 64, 0, 1), ks > 0);
-      mma_ss(tb + GT_A0, desc_mn(s_s, 128, ks), desc_mn(s_dv, 128, ks), idesc(128, 64, 1, 1), ks > 0);
-      mma_ss(tb + GT_A1, desc_mn(s_s, 128, ks), desc_k(s_do, 64, ks), idesc(128, 64, 1, 0), ks > 0);
-      mma_ss(tb + GT_A3, desc_mn(s_ds, 128, ks), desc_mn(s_vn, 128, ks), idesc(128, 64, 1, 1), ks > 0);
-      mma_ss(tb + GT_A5, desc_mn(s_dv, 128, ks), desc_k(s_v, 64, ks), idesc(64, 64, 1, 0), ks > 0);
+      mma_ss_w(tb + GT_A4, desc_k(s_do, 64, ks), desc_mn(s_vn, 128, ks), idesc(64, 64, 0, 1), ks > 0);
+      mma_ss_w(tb + GT_A1, desc_mn(s_s, 128, ks), desc_k(s_do, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+      mma_ss_w(tb + GT_A3, desc_mn(s_ds, 128, ks), desc_mn(s_vn, 128, ks), idesc(128, 64, 1, 1), ks > 0);
+    }
+  };
+  auto issue_ma2 = [&]() {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      mma_ss_w(tb + GT_A0, desc_mn(s_s, 128, ks), desc_mn(s_dv, 128, ks), idesc(128, 64, 1, 1), ks > 0);
+      mma_ss_w(tb + GT_A5, desc_mn(s_dv, 128, ks), desc_k(s_v, 64, ks), idesc(64, 64, 1, 0), ks > 0);
     }
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-      mma_ss(tb + GT_A2, desc_k(s_dv, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
-    mma_commit(&bar_ma);
+      mma_ss_w(tb + GT_A2, desc_k(s_dv, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
+    mma_commit_w(&bar_ma);
   };
 
   uint32_t hc = 0;                      // value heads done by this CTA (phase of the per-head loads)
-  bool ma_issued = false;               // the current value head's MA went out under the last totals
+  bool ma_issued = false;               // the MMA warp issued the current value head's MA under the last M6
   {  // the first item's tiles and its first gate scan
     const int c = blockIdx.x % a.NC, j = blockIdx.x / a.NC;
     const int tok0 = a.chunk_tok0[c];
@@ -707,17 +717,31 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
     if (warp == 4) gates(0, j * a.G, tok0, a.chunk_len[c]);
   }
   if (tid >= GK_THREADS) {
-    // ================= MMA warpgroup: its first warp issues MB and M5 of every value head =========
+    // ================= MMA warpgroup: its first warp issues MA, MB, M5 and M6 of every value head ====
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(GK_REG_MMA));
     if (warp == GK_THREADS / 32) {
-      uint32_t gph = 0;
-      bool live = true;
-      for (int item = blockIdx.x; live && item < n_items; item += gridDim.x)
-        for (int h = 0; live && h < a.G; ++h) {
+      uint32_t gph = 0, gaph = 0, hcm = 0;
+      bool live = true, pend = false;   // pend: this value head's MA went out under the last M6
+      auto go = [&]() {
+        live = mbar_wait(&go_mma, gph, a.err);
+        gph ^= 1;
+        tc_fence_after();
+        return live;
+      };
+      for (int item = blockIdx.x; live && item < n_items; item += gridDim.x) {
+        const int L = a.chunk_len[item % a.NC];
+        const int nxt = item + gridDim.x;
+        for (int h = 0; h < a.G; ++h, ++hcm) {
+          const uint32_t vph = hcm & 1;
+          if (!pend) {   // MA once the rows past the document end are zeroed
+            if (!(live = mbar_wait(&go_ma, gaph, a.err))) break;
+            gaph ^= 1;
+            tc_fence_after();
+            issue_ma1();
+            issue_ma2();
+          }
           // MB: dW K^T (M = 64), Y^T = dW^T T
-          if (!(live = mbar_wait(&go_mma, gph, a.err))) break;
-          gph ^= 1;
-          tc_fence_after();
+          if (!go()) break;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             mma_ss_w(tb + GT_A0, desc_mn(s_wd, 128, ks), desc_k(s_k, 64, ks), idesc(64, 64, 1, 0), ks > 0);
@@ -726,14 +750,35 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
             mma_ss_w(tb + GT_A2, desc_k(s_wd, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
           mma_commit_w(&mma_bar);
           // M5: T^T R1 (= -dA, M = 64)
-          if (!(live = mbar_wait(&go_mma, gph, a.err))) break;
-          gph ^= 1;
-          tc_fence_after();
+          if (!go()) break;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             mma_ss_w(tb + GT_A0, desc_mn(s_t, 64, ks), desc_mn(s_r1, 64, ks), idesc(64, 64, 1, 1), ks > 0);
           mma_commit_w(&mma_bar);
+          // M6: K^T F1 + K^T F2 (+= dk^T), waited for at the end of the item (every later commit
+          // of this warp covers it); then the next value head's MA when its chunk is full, each
+          // part as soon as its tiles have landed
+          if (!go()) break;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ss_w(tb + GT_DK, desc_mn(s_k, 64, ks), desc_k(s_f1, 64, ks), idesc(128, 64, 1, 0), 1u);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ss_w(tb + GT_DK, desc_mn(s_k, 64, ks), desc_mn(s_f2, 64, ks), idesc(128, 64, 1, 1), 1u);
+          if (h + 1 == a.G) mma_commit_w(&mma_bar);
+          const bool has_next = h + 1 < a.G || nxt < n_items;
+          const int nL = h + 1 < a.G ? L : (nxt < n_items ? a.chunk_len[nxt % a.NC] : 0);
+          pend = has_next && nL == CH;
+          if (pend) {
+            if (!(live = mbar_wait(&bar_vn, vph ^ 1, a.err) && mbar_wait(&bar_sv, vph ^ 1, a.err) &&
+                         mbar_wait(&bar_do, vph ^ 1, a.err)))
+              break;
+            issue_ma1();
+            if (!(live = mbar_wait(&bar_dt, vph ^ 1, a.err))) break;
+            issue_ma2();
+          }
         }
+      }
       mma_commit_w(&done_mma);   // arrives once every MMA this warp issued has completed
     }
     return;
@@ -844,8 +889,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
                 make_uint4(0u, 0u, 0u, 0u);
           }
         }
-        handoff();
-        if (tid == 0) issue_ma();
+        handoff_to_mma_warp(&go_ma);
       }
       ma_issued = false;
       ok = bar_and(GK_BAR, GK_THREADS, mbar_wait(&bar_ma, maph, a.err));
@@ -872,7 +916,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
         }
       }
       // ---- MB: dW K^T (M = 64), Y^T = dW^T T, issued by the MMA warp
-      handoff_to_mma_warp();
+      handoff_to_mma_warp(&go_mma);
       const bool full = L == CH;   // full chunk: dv goes out as a staged tile (TMA store)
       {  // HA side work: dv; the column-scaled terms pg S dO^T into dq^T and dec dKd^T into dk^T (TMEM
          // read-modify-write: no MMA touches them until M4); partial sums for dg
@@ -1094,7 +1138,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
           }
       }
       // ---- M5: T^T R1 (= -dA, M = 64), issued by the MMA warp
-      handoff_to_mma_warp();
+      handoff_to_mma_warp(&go_mma);
       {  // H4 side work: beta gamma Y^T into dk^T (TMEM: M4 is done, M6 not yet issued)
         float yv[GK_CW], ak[GK_CW];
         tld2(GT_A2, yv, GT_DK, ak);   // Y^T = dW^T T (rows = dk index)
@@ -1167,24 +1211,10 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
           colC[1][w4][cbl + 9] = cs[3];
         }
       }
-      handoff();
-      // ---- M6: K^T F1 + K^T F2 (+= dk^T); then the next value head's MA when
-      // its chunk is full (no rows to zero).  M6 is waited for only at the end
-      // of the item: every later commit of this thread covers it.
-      const bool early = has_next && nL == CH;
-      if (tid == 0) {
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ss(tb + GT_DK, desc_mn(s_k, 64, ks), desc_k(s_f1, 64, ks), idesc(128, 64, 1, 0), 1u);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ss(tb + GT_DK, desc_mn(s_k, 64, ks), desc_mn(s_f2, 64, ks), idesc(128, 64, 1, 1), 1u);
-        if (h + 1 == a.G) mma_commit(&mma_bar);
-        if (early && mbar_wait(&bar_vn, vph ^ 1, a.err) && mbar_wait(&bar_sv, vph ^ 1, a.err) &&
-            mbar_wait(&bar_do, vph ^ 1, a.err) && mbar_wait(&bar_dt, vph ^ 1, a.err))
-          issue_ma();
-      }
-      ma_issued = early;
+      // ---- M6: K^T F1 + K^T F2 (+= dk^T), then the next value head's MA when its chunk is full
+      // (no rows to zero), issued by the MMA warp
+      handoff_to_mma_warp(&go_mma);
+      ma_issued = has_next && nL == CH;
       if (warp == 2 || warp == 3) {   // ---- per-token totals: dbeta, dG -> dg
         const int r = tid - 64, wl = warp - 2;
         float sb = 0.f, sg = 0.f, sz = 0.f, sy = 0.f, cr = 0.f, rbs = 0.f;
@@ -1314,9 +1344,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
     it_L = nx_L;
   }
   if (tid == 0) bulk_wait_all();
-  // an MA issued for a value head that never ran must not be left in flight, nor any MMA of the
-  // MMA warp
-  if (ma_issued && tid == 0) mbar_wait(&bar_ma, maph, a.err);
+  // no MMA of the MMA warp may be left in flight (an MA for a value head that never ran included)
   if (tid == 0) mbar_wait(&done_mma, 0, a.err);
   tc_fence_before();
   named_bar(GK_BAR, GK_THREADS);
