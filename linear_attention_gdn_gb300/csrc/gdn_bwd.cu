@@ -538,7 +538,10 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
   // go_mma / go_ma: the compute warpgroups hand MB, M5, M6 / a value head's first MA to the MMA warp.
   // Consecutive arrivals on each are separated by a wait on a commit the MMA warp makes after
   // consuming the earlier one, so no phase is passed before its waiter saw it.
-  __shared__ uint64_t bar_qk, bar_vn, bar_sv, bar_do, bar_dt, bar_ma, mma_bar, go_mma, go_ma, done_mma;
+  // go_kq: the next item's Q, K load went out (the dq / dk accumulator columns are free); kq_bar:
+  // the item's KK^T / QK^T products are in those columns
+  __shared__ uint64_t bar_qk, bar_vn, bar_sv, bar_do, bar_dt, bar_ma, mma_bar, go_mma, go_ma, go_kq, kq_bar,
+      done_mma;
   __shared__ uint32_t tslot;
   __shared__ __align__(16) float rq[CH], rk[CH];
   // gates of the current and the next value head (double-buffered)
@@ -568,6 +571,8 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
     mbar_init(&mma_bar, 1);
     mbar_init(&go_mma, 1);
     mbar_init(&go_ma, 1);
+    mbar_init(&go_kq, 1);
+    mbar_init(&kq_bar, 1);
     mbar_init(&done_mma, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
@@ -643,7 +648,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
     if (lane == 0) gsafe[b] = sf;
   };
 
-  uint32_t mph = 0, maph = 0, qkph = 0;
+  uint32_t mph = 0, maph = 0, qkph = 0, kqph = 0;
   bool ok = true;
   auto mma_sync_wait = [&]() -> bool {
     bool r = bar_and(GK_BAR, GK_THREADS, mbar_wait(&mma_bar, mph, a.err));
@@ -720,7 +725,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
     // ================= MMA warpgroup: its first warp issues MA, MB, M5 and M6 of every value head ====
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(GK_REG_MMA));
     if (warp == GK_THREADS / 32) {
-      uint32_t gph = 0, gaph = 0, hcm = 0;
+      uint32_t gph = 0, gaph = 0, gkph = 0, qph = 0, hcm = 0;
       bool live = true, pend = false;   // pend: this value head's MA went out under the last M6
       auto go = [&]() {
         live = mbar_wait(&go_mma, gph, a.err);
@@ -731,6 +736,25 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
       for (int item = blockIdx.x; live && item < n_items; item += gridDim.x) {
         const int L = a.chunk_len[item % a.NC];
         const int nxt = item + gridDim.x;
+        // KK^T, QK^T (M = 64) in the dq / dk accumulator columns (free until M4), as soon as the
+        // item's Q, K tiles have landed (and, in a partial chunk, their rows past the end are zeroed)
+        if (item != (int)blockIdx.x) {
+          if (!(live = mbar_wait(&go_kq, gkph, a.err))) break;
+          gkph ^= 1;
+        }
+        if (!(live = mbar_wait(&bar_qk, qph, a.err))) break;
+        qph ^= 1;
+        if (L < CH) {
+          if (!(live = mbar_wait(&go_ma, gaph, a.err))) break;
+          gaph ^= 1;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_ss_w(tb + GT_DQ, desc_k(s_k, 64, ks), desc_k(s_k, 64, ks), idesc(64, 64, 0, 0), ks > 0);
+          mma_ss_w(tb + GT_DK, desc_k(s_q, 64, ks), desc_k(s_k, 64, ks), idesc(64, 64, 0, 0), ks > 0);
+        }
+        mma_commit_w(&kq_bar);
         for (int h = 0; h < a.G; ++h, ++hcm) {
           const uint32_t vph = hcm & 1;
           if (!pend) {   // MA once the rows past the document end are zeroed
@@ -801,6 +825,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
         const int t = idx >> 5, tile = (idx >> 4) & 1, c8 = idx & 15;
         *reinterpret_cast<uint4*>(sm + (tile ? GK_K : GK_Q) + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
       }
+      handoff_to_mma_warp(&go_ma);   // then the MMA warp's KK^T / QK^T
     }
     {  // L2 norms of the q/k rows: four partial sums of 32 elements (even- plus odd-element chain),
        // combined as (p0 + p1) + (p2 + p3) (the prep kernel's order)
@@ -831,16 +856,10 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
       }
     }
     if (tid == 0) bulk_wait_read();   // the last item's dq / dk stores have read their staging tiles
-    handoff();
-    if (tid == 0) {   // KK^T, QK^T (M = 64) in the dq / dk accumulator columns, free until M4
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        mma_ss(tb + GT_DQ, desc_k(s_k, 64, ks), desc_k(s_k, 64, ks), idesc(64, 64, 0, 0), ks > 0);
-        mma_ss(tb + GT_DK, desc_k(s_q, 64, ks), desc_k(s_k, 64, ks), idesc(64, 64, 0, 0), ks > 0);
-      }
-      mma_commit(&mma_bar);
-    }
-    if (!(ok = mma_sync_wait())) break;
+    ok = bar_and(GK_BAR, GK_THREADS, mbar_wait(&kq_bar, kqph, a.err));   // the MMA warp's KK^T / QK^T
+    kqph ^= 1;
+    tc_fence_after();
+    if (!ok) break;
     {
       float kk[GK_CW], qk[GK_CW];
       tld2(GT_DQ, kk, GT_DK, qk);
@@ -1293,7 +1312,10 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
     }
     tc_fence_before();   // the TMEM reads of DQ / DK precede the next item's table MMAs
     named_bar(GK_BAR, GK_THREADS);     // the Q, K tiles are free
-    if (tid == 0 && nxt < n_items) issue_qk(nxt / a.NC, nx_tok0);
+    if (tid == 0 && nxt < n_items) {
+      issue_qk(nxt / a.NC, nx_tok0);
+      mbar_arrive(&go_kq);
+    }
     if (tid < CH) {      // d|x|/dx . g = (g - x (x . g) / |x|^2) / |x|: the per-token factor (x . g) / |x|^3
       float xq = 0.f, xk = 0.f;
 #pragma unroll
