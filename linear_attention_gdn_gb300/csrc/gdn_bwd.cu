@@ -992,26 +992,6 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
           tmem_st16(taddr(tb, w4 * 32, GT_DQ + cb0), aq);
           tmem_st16(taddr(tb, w4 * 32, GT_DK + cb0), ak);
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float fg[4], fq[4], fk[4];
-          col4(gg, i, fg);
-          col4(rq, i, fq);
-          col4(rk, i, fk);
-#pragma unroll
-          for (int j = 0; j < 4; j += 2) {   // (((scale g) rq) q) y and (rk k) z, two columns at a time
-            const int e = 4 * i + j, cc = cb0 + e;
-            float m0, m1, n0, n1;
-            mul2v(m0, m1, a.scale, a.scale, fg[j], fg[j + 1]);
-            mul2v(m0, m1, m0, m1, fq[j], fq[j + 1]);
-            mul2v(m0, m1, m0, m1, ld_bf16(sm + GK_Q, cc, row, 64), ld_bf16(sm + GK_Q, cc + 1, row, 64));
-            mul2v(y[e], y[e + 1], m0, m1, y[e], y[e + 1]);
-            mul2v(n0, n1, fk[j], fk[j + 1], ld_bf16(sm + GK_K, cc, row, 64), ld_bf16(sm + GK_K, cc + 1, row, 64));
-            mul2v(z[e], z[e + 1], n0, n1, z[e], z[e + 1]);
-          }
-        }
-        const float sg = colsum16(y, lane);
-        const float sz = colsum16(z, lane);
         // <S, dS'> over this thread's quarter of the row
         float sda[4] = {0.f, 0.f, 0.f, 0.f};   // four independent chains, combined in a fixed order
 #pragma unroll
@@ -1032,10 +1012,6 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
         if (lane == 0) sdot[warp] = sd;
-        if (lane < GK_CW) {
-          part[1][w4][cb0 + lane] = sg;
-          part[2][w4][cb0 + lane] = sz;
-        }
         tmem_wait_st();
       }
       if (!(ok = mma_sync_wait())) break;
@@ -1050,6 +1026,9 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
       // The M = 64 token-pair passes spread each 16 x 16 block over the whole warp:
       // this thread takes rows rb0, rb0 + 8 and columns cbl, cbl + 1, cbl + 8, cbl + 9.
       const int rb0 = w4 * 16 + (lane >> 2), cbl = cb0 + 2 * (lane & 3);
+      // this thread's shares of the HB sums, reduced across the warp while M4 runs
+      float rs[2] = {0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f}, tb1[4] = {0.f, 0.f, 0.f, 0.f},
+            tb2[4] = {0.f, 0.f, 0.f, 0.f};
       {  // HB: H1, H2, dT for M4; dAqk . Aqk -> row / column sums of C; the per-token sums
          // sum_r T[r][c] (dV_new V^T)[r][c] (= V_c . (T^T dV_new)_c, dbeta) and
          // sum_r T[r][c] (dW K^T)[r][c] (= K_c . (T^T dW)_c, dg)
@@ -1058,8 +1037,6 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
         tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A5 + cb0), u1);   // dV_new V^T
         tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A0 + cb0), u2);   // dW K^T
         tmem_wait_ld();
-        float rs[2] = {0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f}, tb1[4] = {0.f, 0.f, 0.f, 0.f},
-              tb2[4] = {0.f, 0.f, 0.f, 0.f};
         const float qr2[2] = {rq[rb0], rq[rb0 + 8]}, eR2[2] = {eR[rb0], eR[rb0 + 8]};
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
@@ -1098,6 +1075,20 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
             *reinterpret_cast<uint32_t*>(sm + GK_DT + off) = pack_bf16(dt[0], dt[1]);
           }
         }
+      }
+      handoff();
+      // ---- M4: R1 = dT T^T (M = 64), K^T H1 (+= dq^T), Q^T H2 (+= dk^T)
+      if (tid == 0) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          mma_ss(tb + GT_A5, desc_k(s_dt, 64, ks), desc_k(s_t, 64, ks), idesc(64, 64, 0, 0), ks > 0);
+          mma_ss(tb + GT_DQ, desc_mn(s_k, 64, ks), desc_k(s_h1, 64, ks), idesc(128, 64, 1, 0), 1u);
+          mma_ss(tb + GT_DK, desc_mn(s_q, 64, ks), desc_mn(s_h2, 64, ks), idesc(128, 64, 1, 1), 1u);
+        }
+        mma_commit(&mma_bar);
+      }
+      {  // while M4 runs: the HB sums across the warp, and the dg partial sums of the HA terms,
+         // (((scale g) rq) q) (S dO^T) and (rk k) dKd^T (TMEM columns no MMA writes until the next MA)
         // rows: the 4 lanes of a row group; columns: the 8 lanes of a column pair
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
@@ -1125,17 +1116,33 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
             part[3][w4][cc] = rk[cc] * tb2[k];
           }
         }
-      }
-      handoff();
-      // ---- M4: R1 = dT T^T (M = 64), K^T H1 (+= dq^T), Q^T H2 (+= dk^T)
-      if (tid == 0) {
+        float y[GK_CW], z[GK_CW];
+        tld2(GT_A1, y, GT_A3, z);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          mma_ss(tb + GT_A5, desc_k(s_dt, 64, ks), desc_k(s_t, 64, ks), idesc(64, 64, 0, 0), ks > 0);
-          mma_ss(tb + GT_DQ, desc_mn(s_k, 64, ks), desc_k(s_h1, 64, ks), idesc(128, 64, 1, 0), 1u);
-          mma_ss(tb + GT_DK, desc_mn(s_q, 64, ks), desc_mn(s_h2, 64, ks), idesc(128, 64, 1, 1), 1u);
+        for (int i = 0; i < 4; ++i) {
+          const float4 fg = *reinterpret_cast<const float4*>(gg + cb0 + 4 * i);
+          const float4 fq = *reinterpret_cast<const float4*>(rq + cb0 + 4 * i);
+          const float4 fk = *reinterpret_cast<const float4*>(rk + cb0 + 4 * i);
+          const float g4[4] = {fg.x, fg.y, fg.z, fg.w}, q4[4] = {fq.x, fq.y, fq.z, fq.w},
+                      k4[4] = {fk.x, fk.y, fk.z, fk.w};
+#pragma unroll
+          for (int j = 0; j < 4; j += 2) {   // two columns at a time
+            const int e = 4 * i + j, cc = cb0 + e;
+            float m0, m1, n0, n1;
+            mul2v(m0, m1, a.scale, a.scale, g4[j], g4[j + 1]);
+            mul2v(m0, m1, m0, m1, q4[j], q4[j + 1]);
+            mul2v(m0, m1, m0, m1, ld_bf16(sm + GK_Q, cc, row, 64), ld_bf16(sm + GK_Q, cc + 1, row, 64));
+            mul2v(y[e], y[e + 1], m0, m1, y[e], y[e + 1]);
+            mul2v(n0, n1, k4[j], k4[j + 1], ld_bf16(sm + GK_K, cc, row, 64), ld_bf16(sm + GK_K, cc + 1, row, 64));
+            mul2v(z[e], z[e + 1], n0, n1, z[e], z[e + 1]);
+          }
         }
-        mma_commit(&mma_bar);
+        const float sg = colsum16(y, lane);
+        const float sz = colsum16(z, lane);
+        if (lane < GK_CW) {
+          part[1][w4][cb0 + lane] = sg;
+          part[2][w4][cb0 + lane] = sz;
+        }
       }
       if (!(ok = mma_sync_wait())) break;
       if (tid == 0 && has_next) {
