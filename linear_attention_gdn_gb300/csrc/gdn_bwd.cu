@@ -855,6 +855,14 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
         else rq[r] = rn;
       }
     }
+    // this thread's q, k elements [cb0 + e][row] of the item, as BF16 pairs (q low, k high)
+    uint32_t qk2[GK_CW];
+#pragma unroll
+    for (int e = 0; e < GK_CW; ++e) {
+      const uint32_t off = sw_off(cb0 + e, row, 64);
+      qk2[e] = (uint32_t)*reinterpret_cast<const uint16_t*>(sm + GK_Q + off) |
+               ((uint32_t)*reinterpret_cast<const uint16_t*>(sm + GK_K + off) << 16);
+    }
     if (tid == 0) bulk_wait_read();   // the last item's dq / dk stores have read their staging tiles
     ok = bar_and(GK_BAR, GK_THREADS, mbar_wait(&kq_bar, kqph, a.err));   // the MMA warp's KK^T / QK^T
     kqph ^= 1;
@@ -1127,13 +1135,14 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
                       k4[4] = {fk.x, fk.y, fk.z, fk.w};
 #pragma unroll
           for (int j = 0; j < 4; j += 2) {   // two columns at a time
-            const int e = 4 * i + j, cc = cb0 + e;
+            const int e = 4 * i + j;
             float m0, m1, n0, n1;
             mul2v(m0, m1, a.scale, a.scale, g4[j], g4[j + 1]);
             mul2v(m0, m1, m0, m1, q4[j], q4[j + 1]);
-            mul2v(m0, m1, m0, m1, ld_bf16(sm + GK_Q, cc, row, 64), ld_bf16(sm + GK_Q, cc + 1, row, 64));
+            mul2v(m0, m1, m0, m1, __uint_as_float(qk2[e] << 16), __uint_as_float(qk2[e + 1] << 16));
             mul2v(y[e], y[e + 1], m0, m1, y[e], y[e + 1]);
-            mul2v(n0, n1, k4[j], k4[j + 1], ld_bf16(sm + GK_K, cc, row, 64), ld_bf16(sm + GK_K, cc + 1, row, 64));
+            mul2v(n0, n1, k4[j], k4[j + 1], __uint_as_float(qk2[e] & 0xffff0000u),
+                  __uint_as_float(qk2[e + 1] & 0xffff0000u));
             mul2v(z[e], z[e + 1], n0, n1, z[e], z[e + 1]);
           }
         }
@@ -1296,20 +1305,14 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
 
     // ---- item end: the MMA-accumulated dq^T, dk^T; L2-norm backward of the group sums; dq, dk
     if (!(ok = mma_sync_wait())) break;   // M6 of the last value head
-    uint32_t qk2[GK_CW];                  // BF16 q (low half), k (high half) [cb0 + e][row]: the tiles are
-                                          // reloaded for the next item
     float xq[GK_CW], xk[GK_CW];           // dq^T, dk^T [row][cb0 + e] (before the L2-norm backward)
     {
       float pq[GK_CW], pk[GK_CW];
       tld2(GT_DQ, xq, GT_DK, xk);
 #pragma unroll
       for (int e = 0; e < GK_CW; ++e) {
-        const int cc = cb0 + e;
-        const uint32_t qb = *reinterpret_cast<const uint16_t*>(sm + GK_Q + sw_off(cc, row, 64));
-        const uint32_t kb = *reinterpret_cast<const uint16_t*>(sm + GK_K + sw_off(cc, row, 64));
-        qk2[e] = qb | (kb << 16);
-        pq[e] = __uint_as_float(qb << 16) * xq[e];
-        pk[e] = __uint_as_float(kb << 16) * xk[e];
+        pq[e] = __uint_as_float(qk2[e] << 16) * xq[e];
+        pk[e] = __uint_as_float(qk2[e] & 0xffff0000u) * xk[e];
       }
       const float sq = colsum16(pq, lane), sk = colsum16(pk, lane);
       if (lane < GK_CW) {
