@@ -526,12 +526,18 @@ __device__ __forceinline__ void store_chunk8(uint8_t* tile, int r, int c8, int R
 //   M4  R1 = dT T^T, K^T H1 (+= dq^T), Q^T H2 (+= dk^T)
 //   M5  T^T R1 (= -dA)
 //   M6  K^T F1 + K^T F2 (+= dk^T)
-// Each CUDA-core pass first writes what the next group reads, hands off, and
-// does its side work (dv, column-scaled dq / dk terms, per-token partial
-// sums) while that group runs.  The next value head's tiles (the next item's
-// first value head after the last one) are requested as soon as the buffers
-// they land in are dead, and its MA is issued right after M6, so that it runs
-// under the per-token totals (warps 2-3) and the next gate scan (warp 4).
+// Four compute warpgroups run the CUDA-core passes; one more warp issues MA,
+// MB, M5, M6 and the item's KK^T / QK^T, each on an mbarrier handoff (M4 is
+// issued by the first compute thread).  Each pass first writes what the next
+// group reads, hands off, and does its side work (dv, column-scaled dq / dk
+// terms, per-token partial sums) while that group runs.  The next value
+// head's tiles (the next item's first value head after the last one) are
+// requested as soon as the buffers they land in are dead, and its MA is issued
+// right after M6 (the products of V_new^T, S, dS', dO as soon as those tiles
+// land, then those of dV_new^T and T), so that it runs under the per-token
+// totals (warps 2-3) and the next gate scan (warp 4).  The next item's
+// KK^T / QK^T likewise runs as soon as its Q, K tiles land, under this item's
+// dq / dk epilogue.
 __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constant__ GradArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
