@@ -186,7 +186,9 @@ gdn_status gdn_bwd_states(const gdn_problem *prob, const void *q, const void *k,
  * GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED).  Pointers 16-byte aligned.
  * Accumulation is FP32 in a fixed order; dw and db are sums of per-range
  * partials added in range order (bitwise reproducible).  The caller owns
- * every buffer; the backward needs `workspace` of gdn_conv1d_workspace_bytes.
+ * every buffer; the backward needs `workspace` of gdn_conv1d_workspace_bytes,
+ * which opens with the device status word that gdn_device_status reads (a
+ * bounded wait on a row copy that never completes sets GDN_ERR_TIMEOUT there).
  */
 typedef struct {
     int64_t T;   /* total packed tokens (= cu_seqlens[N]) */

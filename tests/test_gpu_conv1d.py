@@ -37,7 +37,7 @@ def run(case, d):
     ws = torch.full((max(gdn.gdn_conv1d_workspace_bytes(prob, cu), 16),), 255, dtype=torch.uint8, device="cuda")
     gdn.gdn_conv1d_fwd(prob, x, w, b, cu_dev, cu, y)
     gdn.gdn_conv1d_bwd(prob, x, w, b, cu_dev, cu, dy, dx, dw, db, ws)
-    torch.cuda.synchronize()
+    assert gdn.gdn_device_status(ws) == 0   # the backward's status word (it syncs the stream)
     return y, dx, dw, db
 
 

@@ -87,3 +87,16 @@ def test_invalid_arguments_refused_before_launch():
                                           *[ctypes.c_void_p(A)] * 5, ctypes.c_void_p(A), wsb, None)
     assert bw(0, ws) == 1                                 # backward needs the saved set
     assert bw(A, 10) == 3
+
+
+def test_conv1d_problem_checks_and_workspace():
+    """The conv1d front refuses C not a multiple of 8 and W outside 1..4, and
+    its backward workspace is the 16-byte status word plus one FP32 partial of
+    dw and db per 1,024-token range (host checks only)."""
+    cu = np.array([0, 1000, 2500], dtype=np.int32)
+    cup = cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    n = ctypes.c_size_t(0)
+    for C, W, code in ((12, 4, 1), (16, 5, 2), (16, 0, 1), (16, 4, 0)):
+        p = gdn.conv_problem(2500, 2, C, W)
+        assert gdn.lib.gdn_conv1d_workspace_bytes(ctypes.byref(p), cup, ctypes.byref(n)) == code
+    assert n.value == 16 + 3 * (4 + 1) * 16 * 4
