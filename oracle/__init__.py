@@ -10,4 +10,5 @@ Modules:
   chunked.py    the chunk-64 (WY/UT) form in FP64 numpy, forward and backward
   tables.py     brute-force enumeration of the varlen chunk tables
   conv1d.py     the short causal convolution + SiLU front, forward and backward
+  kda.py        the per-channel-decay (KDA) recurrence, forward and backward
 """

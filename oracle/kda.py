@@ -1,0 +1,105 @@
+"""FP64 per-token oracle of the gated delta rule with a per-channel decay (KDA).
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+The pages name a sibling "Cake packed KDA" training family beside the GDN one
+("perf(cake_kda) ... #7097" page and its "#7117" table notes: a chunked
+training backend for packed documents, single-device and context-parallel)
+but print no formula.  The plainest reading, and the one taken here, is the
+GDN recurrence of gdn_oracle.c with its scalar decay a_t = exp(g_t) replaced
+by one decay per key channel, a_t = exp(g_t) with g_t in R^dk:
+
+  q^, k^ = l2norm(q), l2norm(k)   (or q, k when the norm is off)
+  S'_t = Diag(a_t) S_{t-1}                       (dk x dv, row i scaled by a_t[i])
+  S_t  = S'_t + beta_t k^_t (v_t - S'_t^T k^_t)^T
+  o_t  = scale S_t^T q^_t
+
+per document (S = 0 at each start) and value head; value head h reads q/k head
+h / G.  The backward is the reverse mode of those four lines, token by token
+from the end; per token, with dS the adjoint of S_t:
+
+  dS += scale q^ do^T;  dq^ = scale S_t do
+  u = v - S'^T k^:  dbeta = k^^T dS u;  du = beta dS^T k^;  dv = du
+  dk^ = beta dS u - S' du;  dS' = dS - k^ du^T
+  dg = a . rowsum(dS' . S_{t-1});  dS_{t-1} = Diag(a) dS'
+
+followed by the L2-norm backward of q and k.  Shapes follow ref.group: q, k
+[L, dk]; v [G, L, dv]; g [G, L, dk]; beta [G, L]; dO [G, L, dv].  numpy
+vector operations over the channels serve as steps; nothing is blocked or
+reordered beyond the lines above.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+EPS = 1e-6
+
+
+def _l2(x, on, eps):
+    if not on:
+        return x.copy(), np.ones(x.shape[0])
+    n = np.sqrt((x * x).sum(-1) + eps)
+    return x / n[:, None], n
+
+
+def _l2_back(x, n, dxh, on):
+    """d|x|-normalise backward: dx = dxh / n - x (x . dxh) / n^3 per row."""
+    if not on:
+        return dxh
+    return dxh / n[:, None] - x * ((x * dxh).sum(-1) / n ** 3)[:, None]
+
+
+def group(q, k, v, g, beta, dO=None, *, l2norm=True, scale=128 ** -0.5, eps=EPS, s_in=None):
+    """Forward (+ backward when dO is given) of one document, one q/k group.
+
+    Returns o [G, L, dv] and, with dO: dq, dk [L, dk], dv [G, L, dv],
+    dg [G, L, dk], dbeta [G, L]; s_out [G, dk, dv] (the state after the last
+    token).  s_in [G, dk, dv] is the state entering the document (zero if None).
+    """
+    q, k, v, g, beta = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta))
+    L, dk = q.shape
+    G, _, dv = v.shape
+    qh, nq = _l2(q, l2norm, eps)
+    kh, nk = _l2(k, l2norm, eps)
+    a = np.exp(g)                                        # [G, L, dk]
+    S = np.zeros((G, dk, dv)) if s_in is None else np.array(s_in, dtype=np.float64).reshape(G, dk, dv)
+    states = np.zeros((L + 1, G, dk, dv))               # S_{t-1} entering token t, then S_L
+    o = np.zeros((G, L, dv))
+    for t in range(L):
+        states[t] = S
+        Sp = a[:, t, :, None] * S                        # S'_t = Diag(a_t) S_{t-1}
+        u = v[:, t] - np.einsum("gij,i->gj", Sp, kh[t])  # v - S'^T k^
+        S = Sp + beta[:, t, None, None] * kh[t][None, :, None] * u[:, None, :]
+        o[:, t] = scale * np.einsum("gij,i->gj", S, qh[t])
+    states[L] = S
+    out = dict(o=o, s_out=S.copy())
+    if dO is None:
+        return out
+    dO = np.asarray(dO, dtype=np.float64)
+    dqh = np.zeros((L, dk))
+    dkh = np.zeros((L, dk))
+    dvv = np.zeros((G, L, dv))
+    dg = np.zeros((G, L, dk))
+    db = np.zeros((G, L))
+    dS = np.zeros((G, dk, dv))
+    for t in range(L - 1, -1, -1):
+        S_prev, S_t = states[t], states[t + 1]
+        Sp = a[:, t, :, None] * S_prev
+        u = v[:, t] - np.einsum("gij,i->gj", Sp, kh[t])
+        # o_t = scale S_t^T q^
+        dS = dS + scale * qh[t][None, :, None] * dO[:, t][:, None, :]
+        dqh[t] += scale * np.einsum("gij,gj->i", S_t, dO[:, t])
+        # S_t = S' + beta k^ u^T
+        db[:, t] = np.einsum("i,gij,gj->g", kh[t], dS, u)
+        du = beta[:, t, None] * np.einsum("gij,i->gj", dS, kh[t])
+        dvv[:, t] = du
+        dkh[t] += np.einsum("g,gij,gj->i", beta[:, t], dS, u)
+        # u = v - S'^T k^
+        dkh[t] -= np.einsum("gij,gj->i", Sp, du)
+        dSp = dS - kh[t][None, :, None] * du[:, None, :]
+        # S' = Diag(a) S_{t-1}
+        dg[:, t] = a[:, t] * (dSp * S_prev).sum(-1)
+        dS = a[:, t, :, None] * dSp
+    out.update(dq=_l2_back(q, nq, dqh, l2norm), dk=_l2_back(k, nk, dkh, l2norm), dv=dvv, dg=dg, dbeta=db,
+               ds_in=dS)
+    return out
