@@ -103,3 +103,50 @@ def group(q, k, v, g, beta, dO=None, *, l2norm=True, scale=128 ** -0.5, eps=EPS,
     out.update(dq=_l2_back(q, nq, dqh, l2norm), dk=_l2_back(k, nk, dkh, l2norm), dv=dvv, dg=dg, dbeta=db,
                ds_in=dS)
     return out
+
+
+def chunk_forward(q, k, v, g, beta, *, l2norm=True, scale=128 ** -0.5, chunk=64, eps=EPS):
+    """The chunk form of the same forward (the algebra a chunked kernel follows).
+
+    Unrolling the recurrence over a chunk from its entering state S, with the
+    per-channel cumulative log decay G_r = sum_{i<=r} g_i (a dk vector),
+    gamma_r = exp(G_r) and the relative decays exp(G_r - G_c) (c <= r, every
+    entry <= 1):
+      M_rc = k^_r . (exp(G_r - G_c) k^_c)   A = strict_tril(diag(beta) M)
+      T = (I + A)^-1,  U = T diag(beta) V,  W = T diag(beta) (gamma . K^)
+      X = U - W S                          (X_r = beta_r times the new value u_r)
+      O = scale ((gamma . Q^) S + tril_incl(P) X),  P_rc = q^_r . (exp(G_r - G_c) k^_c)
+      S_next = Diag(gamma_L) S + ((exp(G_L - G_c) k^_c) rows)^T X
+    which is the GDN chunk form with each decay moved inside the channel sums.
+    Returns o [G, L, dv] and the states entering each chunk [n_chunks, G, dk, dv].
+    """
+    q, k, v, g, beta = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta))
+    L, dk = q.shape
+    Gh, _, dv = v.shape
+    qh, _ = _l2(q, l2norm, eps)
+    kh, _ = _l2(k, l2norm, eps)
+    bounds = [(c0, min(c0 + chunk, L)) for c0 in range(0, L, chunk)]
+    o = np.zeros((Gh, L, dv))
+    S_tape = np.zeros((len(bounds), Gh, dk, dv))
+    for h in range(Gh):
+        S = np.zeros((dk, dv))
+        for c, (s, e) in enumerate(bounds):
+            S_tape[c, h] = S
+            n = e - s
+            Gc = np.cumsum(g[h, s:e], axis=0)                        # [n, dk]
+            gam = np.exp(Gc)
+            low = np.tril(np.ones((n, n), dtype=bool))                # c <= r
+            D = np.where(low[:, :, None], Gc[:, None, :] - Gc[None, :, :], -np.inf)
+            R = np.exp(D)                                             # [r, c, channel], 0 above the diagonal
+            M = np.einsum("ri,rci,ci->rc", kh[s:e], R, kh[s:e])
+            P = np.einsum("ri,rci,ci->rc", qh[s:e], R, kh[s:e])
+            b = beta[h, s:e]
+            A = np.tril(b[:, None] * M, -1)
+            T = np.linalg.inv(np.eye(n) + A)
+            U = T @ (b[:, None] * v[h, s:e])
+            W = T @ (b[:, None] * gam * kh[s:e])
+            X = U - W @ S
+            o[h, s:e] = scale * ((gam * qh[s:e]) @ S + P @ X)
+            Kd = np.exp(Gc[-1][None, :] - Gc) * kh[s:e]
+            S = gam[-1][:, None] * S + Kd.T @ X
+    return dict(o=o, S=S_tape)

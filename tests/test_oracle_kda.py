@@ -96,3 +96,22 @@ def test_finite_differences(l2norm):
             xm[name][idx] -= h
             num[idx] = (f(xp) - f(xm)) / (2 * h)
         np.testing.assert_allclose(grads[name], num, rtol=1e-6, atol=1e-8, err_msg=name)
+
+
+@pytest.mark.parametrize("l2norm", [True, False])
+def test_chunk_form_matches_the_recurrence(l2norm):
+    """The chunk form (several chunks and a ragged tail) equals the per-token
+    recurrence: outputs and the state entering each chunk."""
+    rng = np.random.default_rng(14)
+    L, dk, dv, G, C = 45, 6, 5, 2, 16
+    q, k, v, g, beta, _ = _inputs(rng, L, dk, dv, G)
+    if not l2norm:
+        q /= np.linalg.norm(q, axis=1, keepdims=True)
+        k /= np.linalg.norm(k, axis=1, keepdims=True)
+    r = kda.group(q, k, v, g, beta, l2norm=l2norm, scale=0.5)
+    c = kda.chunk_forward(q, k, v, g, beta, l2norm=l2norm, scale=0.5, chunk=C)
+    np.testing.assert_allclose(c["o"], r["o"], rtol=1e-10, atol=1e-12)
+    for i, t0 in enumerate(range(0, L, C)):
+        ent = kda.group(q[:t0], k[:t0], v[:, :t0], g[:, :t0], beta[:, :t0], l2norm=l2norm, scale=0.5)["s_out"] \
+            if t0 > 0 else np.zeros((G, dk, dv))
+        np.testing.assert_allclose(c["S"][i], ent, rtol=1e-10, atol=1e-12)
