@@ -150,3 +150,96 @@ def chunk_forward(q, k, v, g, beta, *, l2norm=True, scale=128 ** -0.5, chunk=64,
             Kd = np.exp(Gc[-1][None, :] - Gc) * kh[s:e]
             S = gam[-1][:, None] * S + Kd.T @ X
     return dict(o=o, S=S_tape)
+
+
+def chunk_backward(q, k, v, g, beta, dO, *, l2norm=True, scale=128 ** -0.5, chunk=64, eps=EPS):
+    """The reverse of chunk_forward, chunk by chunk from the end (the algebra a
+    chunked gradient kernel follows).  Per chunk, with dS the adjoint of the
+    state leaving it and the forward's intermediates recomputed:
+      dX = scale P^T dO + Kd dS                     dP = scale dO X^T (c <= r)
+      dS_in = scale (gamma . Q^)^T dO + Diag(gamma_L) dS - W^T dX
+      dU = dX,  dW = -dX S^T,  dT = dU (beta V)^T + dW (beta gamma . K^)^T
+      dA = -T^T dT T^T (strictly lower),  dM = diag(beta) dA
+    then dM, dP, the gamma and Kd terms go back through the per-channel decay
+    products to q^, k^ and the cumulative log decay, and dg is its reverse
+    cumulative sum within the chunk.  Returns the dict of group()'s gradients.
+    """
+    q, k, v, g, beta, dO = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta, dO))
+    L, dk = q.shape
+    Gh, _, dv = v.shape
+    qh, nq = _l2(q, l2norm, eps)
+    kh, nk = _l2(k, l2norm, eps)
+    states = chunk_forward(q, k, v, g, beta, l2norm=l2norm, scale=scale, chunk=chunk, eps=eps)["S"]
+    bounds = [(c0, min(c0 + chunk, L)) for c0 in range(0, L, chunk)]
+    dqh = np.zeros((L, dk))
+    dkh = np.zeros((L, dk))
+    dvv = np.zeros((Gh, L, dv))
+    dg = np.zeros((Gh, L, dk))
+    db = np.zeros((Gh, L))
+    ds_in = np.zeros((Gh, dk, dv))
+    for h in range(Gh):
+        dS = np.zeros((dk, dv))
+        for c in range(len(bounds) - 1, -1, -1):
+            s, e = bounds[c]
+            n = e - s
+            S = states[c, h]
+            Q, K, V, b = qh[s:e], kh[s:e], v[h, s:e], beta[h, s:e]
+            # the forward of this chunk
+            Gc = np.cumsum(g[h, s:e], axis=0)
+            gam = np.exp(Gc)
+            low = np.tril(np.ones((n, n), dtype=bool))
+            R = np.exp(np.where(low[:, :, None], Gc[:, None, :] - Gc[None, :, :], -np.inf))
+            M = np.einsum("ri,rci,ci->rc", K, R, K)
+            P = np.einsum("ri,rci,ci->rc", Q, R, K)
+            A = np.tril(b[:, None] * M, -1)
+            T = np.linalg.inv(np.eye(n) + A)
+            Y = b[:, None] * gam * K                      # W = T Y
+            W = T @ Y
+            X = T @ (b[:, None] * V) - W @ S
+            E = np.exp(Gc[-1][None, :] - Gc)              # Kd = E . K
+            Kd = E * K
+            # O = scale ((gamma . Q) S + P X);  S_next = Diag(gamma_L) S + Kd^T X
+            dOc = dO[h, s:e]
+            dX = scale * P.T @ dOc + Kd @ dS
+            dP = np.where(low, scale * dOc @ X.T, 0.0)
+            dQg = scale * dOc @ S.T                       # adjoint of gamma . Q
+            dQ = gam * dQg
+            dgam = Q * dQg
+            dS_prev = scale * (gam * Q).T @ dOc + gam[-1][:, None] * dS - W.T @ dX
+            dGL = gam[-1] * (dS * S).sum(-1)              # through Diag(gamma_L)
+            dKd = X @ dS.T
+            dK = E * dKd
+            dE = K * dKd * E                              # d(G_L - G_c) per entry
+            dGL += dE.sum(0)
+            dGc = -dE
+            # X = U - W S,  U = T (beta V),  W = T Y
+            dU = dX
+            dW = -dX @ S.T
+            dT = dU @ (b[:, None] * V).T + dW @ Y.T
+            TdU = T.T @ dU
+            dvv[h, s:e] = b[:, None] * TdU
+            dbc = (V * TdU).sum(-1)
+            dY = T.T @ dW
+            dK += b[:, None] * gam * dY
+            dgam += b[:, None] * K * dY
+            dbc += (gam * K * dY).sum(-1)
+            # T = (I + A)^-1,  A = strict_tril(diag(beta) M)
+            dA = np.tril(-T.T @ dT @ T.T, -1)
+            dbc += (dA * M).sum(-1)
+            dM = b[:, None] * dA
+            # M_rc = K_r . (R_rc . K_c),  P_rc = Q_r . (R_rc . K_c)
+            dK += np.einsum("rc,rci,ci->ri", dM, R, K) + np.einsum("rc,rci,ri->ci", dM, R, K)
+            dQ += np.einsum("rc,rci,ci->ri", dP, R, K)
+            dK += np.einsum("rc,rci,ri->ci", dP, R, Q)
+            dRR = (dM[:, :, None] * K[:, None, :] * K[None, :, :] + dP[:, :, None] * Q[:, None, :] * K[None, :, :]) * R
+            dGc += dRR.sum(1) - dRR.sum(0)                # R_rc = exp(G_r - G_c)
+            dGc += dgam * gam                             # gamma = exp(G)
+            dGc[-1] += dGL                                # G_L = G of the last row
+            dg[h, s:e] = np.cumsum(dGc[::-1], axis=0)[::-1]
+            db[h, s:e] = dbc
+            dqh[s:e] += dQ
+            dkh[s:e] += dK
+            dS = dS_prev
+        ds_in[h] = dS
+    return dict(dq=_l2_back(q, nq, dqh, l2norm), dk=_l2_back(k, nk, dkh, l2norm), dv=dvv, dg=dg, dbeta=db,
+                ds_in=ds_in)
