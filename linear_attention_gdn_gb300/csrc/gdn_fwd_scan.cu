@@ -36,7 +36,12 @@ constexpr int SC_W = SC_S + STATE_BYTES;    // -W^T tile, SwTile(128 x 64)
 constexpr int SC_O = SC_W + 16384;          // BF16 output staging tile [64 tok][128], SwTile(64 x 128)
 constexpr int SC_SMEM = SC_O + 16384;
 constexpr int SC_SMEM_ALLOC = SC_SMEM + 1024;
-constexpr int SC_THREADS = 256;
+constexpr int SC_WORK = 256;                 // the chain and the helper warpgroup
+constexpr int SC_THREADS = SC_WORK + 128;    // plus one warpgroup whose first warp issues the chain's MMAs
+// registers per thread after the split (the launch gives 65536 / 384 = 168): the MMA warpgroup gives
+// all but 24 back, the chain and the helper take them
+constexpr int SC_REG_WORK = 240, SC_REG_MMA = 24;
+static_assert(SC_WORK * SC_REG_WORK + 128 * SC_REG_MMA <= SC_THREADS * 168, "register split");
 
 // TMEM columns: D1 (U^T, then V_new^T) and O double-buffered over consecutive chunks
 constexpr int TM_D1 = 0, TM_DW = 128, TM_DS = 192, TM_O = 320, TM_AVS = 448, TM_AVN = 480;
@@ -72,9 +77,11 @@ __device__ __forceinline__ void store_state_row(uint8_t* dst, int row, const flo
 __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_constant__ ScanArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
-  __shared__ uint64_t full_bar[2], bar_wr, bar_m1, bar_wu, bar_m2, bar_o[2], bar_sf;
+  // go1: S^T of the chunk is in its tile (MMA1 may read it); go2: the V_new^T A operands are in TMEM
+  // (MMA2 and the output MMAs may go); done: every MMA of the MMA warp has completed
+  __shared__ uint64_t full_bar[2], bar_wr, bar_m1, bar_wu, bar_m2, bar_o[2], bar_sf, go1, go2, done;
   __shared__ uint32_t tslot;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int lt = tid & 127;      // row within the warpgroup = TMEM lane
   const int wq = warp & 3;       // the warp's TMEM lane quarter
   const bool chain = tid < 128;
@@ -104,24 +111,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
   const uint32_t cb_bytes = mode == 2 ? 8192u : (with_o ? 24576u : 16384u);
   uint8_t* s_tile = sm + SC_S;
 
-  // ---- initial state (chain: row lt of S^T): the merged start of a later segment, the document's
-  // S_in for its first segment (full and B walks), else zero (the identity for M walks)
-  float S[128];
   const int doc = a.seg_doc[seg];
-  if (chain) {
-    const float* src = nullptr;
-    int stride = 1;
-    if (mode == 0 && a.seg_idx[seg] > 0) {
-      src = a.s_init + ((size_t)a.seg_split[seg - 1] * a.HV + hv) * STATE_F32 + (size_t)lt * 128;
-    } else if (mode != 2 && a.seg_idx[seg] == 0 && a.s_in) {   // column lt of S_in [dk][dv]
-      src = a.s_in + ((size_t)doc * a.HV + hv) * STATE_F32 + lt;
-      stride = 128;
-    }
-#pragma unroll
-    for (int jj = 0; jj < 128; ++jj) S[jj] = src ? src[jj * stride] : (mode == 2 && jj == lt ? 1.f : 0.f);
-    store_state_row(s_tile, lt, S);
-    if (mode == 0 && a.tape) store_state_row(a.tape + ((size_t)c0 * a.HV + hv) * STATE_BYTES, lt, S);
-  }
 
   if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {
@@ -134,6 +124,9 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
     mbar_init(&bar_o[0], 1);
     mbar_init(&bar_o[1], 1);
     mbar_init(&bar_sf, 1);
+    mbar_init(&go1, 1);
+    mbar_init(&go2, 1);
+    mbar_init(&done, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   fence_async_smem();
@@ -183,10 +176,74 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
     if (nch > 2) prefetch(2);
   }
   bool ok = true;
+  const uint32_t sm_s = smem_u32(s_tile), sm_w = smem_u32(sm + SC_W);
+
+  if (tid >= SC_WORK) {
+    // =================== MMA warpgroup: its first warp issues MMA1, MMA2 and the output MMAs ======
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(SC_REG_MMA));
+    if (warp == SC_WORK / 32) {
+      bool live = true;
+      for (int n = 0; n < nch && live; ++n) {
+        const uint8_t* st = sm + (n & 1) * SC_STAGE;
+        // MMA1: V_new^T = U^T - S^T W^T (into D1[n & 1]), once S^T, -W^T, U^T and the tiles are in
+        live = mbar_wait(&go1, n & 1, a.err) && mbar_wait(&bar_wr, n & 1, a.err) &&
+               mbar_wait(&full_bar[n & 1], (n >> 1) & 1, a.err);
+        if (!live) break;
+        tc_fence_after();
+        const uint32_t d1 = tb + TM_D1 + (n & 1) * 64;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ss_w(d1, desc_k(sm_s, 128, ks), desc_mn(sm_w, 128, ks), idesc(128, 64, 0, 1),
+                   (with_u || ks > 0) ? 1u : 0u);
+        mma_commit_w(&bar_m1);
+        // MMA2: dS^T = (V_new^T diag(kd)) K; then O^T = S^T Q'^T + V_new^T Aqk^T (into O[n & 1])
+        if (!(live = mbar_wait(&go2, n & 1, a.err))) break;
+        tc_fence_after();
+        const uint32_t a_k = smem_u32(st + SC_K);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_ts_w(tb + TM_DS, tb + TM_AVS + ks * 8, desc_mn(a_k, 64, ks), idesc(128, 128, 0, 1), ks > 0);
+        mma_commit_w(&bar_m2);
+        if (with_o) {   // (the O buffer n & 1 was read out by output(n - 2) in the chain's previous step)
+          const uint32_t to = tb + TM_O + (n & 1) * 64;
+          const uint32_t a_q = smem_u32(st + SC_Q), a_aqk = smem_u32(st + SC_AQK);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ss_w(to, desc_k(sm_s, 128, ks), desc_k(a_q, 64, ks), idesc(128, 64, 0, 0), ks > 0);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ts_w(to, tb + TM_AVN + ks * 8, desc_k(a_aqk, 64, ks), idesc(128, 64, 0, 0), 1u);
+          mma_commit_w(&bar_o[n & 1]);
+        }
+      }
+      mma_commit_w(&done);   // arrives once every MMA this warp issued has completed
+    }
+    return;
+  }
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SC_REG_WORK));
 
   if (chain) {
     // =================== chain warpgroup ===================
-    const uint32_t sm_s = smem_u32(s_tile), sm_w = smem_u32(sm + SC_W);
+    // ---- initial state (row lt of S^T): the merged start of a later segment, the document's S_in
+    // for its first segment (full and B walks), else zero (the identity for M walks)
+    float S[128];
+    {
+      const float* src = nullptr;
+      int stride = 1;
+      if (mode == 0 && a.seg_idx[seg] > 0) {
+        src = a.s_init + ((size_t)a.seg_split[seg - 1] * a.HV + hv) * STATE_F32 + (size_t)lt * 128;
+      } else if (mode != 2 && a.seg_idx[seg] == 0 && a.s_in) {   // column lt of S_in [dk][dv]
+        src = a.s_in + ((size_t)doc * a.HV + hv) * STATE_F32 + lt;
+        stride = 128;
+      }
+#pragma unroll
+      for (int jj = 0; jj < 128; ++jj) S[jj] = src ? src[jj * stride] : (mode == 2 && jj == lt ? 1.f : 0.f);
+      store_state_row(s_tile, lt, S);
+      if (mode == 0 && a.tape) store_state_row(a.tape + ((size_t)c0 * a.HV + hv) * STATE_BYTES, lt, S);
+    }
+    fence_async_smem();
+    named_bar(1, 128);
+    if (tid == 0 && nch > 0) mbar_arrive(&go1);   // S^T of the first chunk is in its tile
     uint8_t* o_stage = sm + SC_O;
     // the output of chunk m from its O buffer (TMEM), o = scale O; thread 32 owns the staging tile's copies
     auto output = [&](int m) {
@@ -226,16 +283,10 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
       ok = wg_sync_and(1, mbar_wait(&bar_wr, par, a.err) && mbar_wait(&full_bar[n & 1], (n >> 1) & 1, a.err));
       if (!ok) break;
       tc_fence_after();
-      if (warp == 0) {   // ---- MMA1: V_new^T = U^T - S^T W^T (into D1[n & 1])
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ss_w(d1, desc_k(sm_s, 128, ks), desc_mn(sm_w, 128, ks), idesc(128, 64, 0, 1),
-                   (with_u || ks > 0) ? 1u : 0u);
-        mma_commit_w(&bar_m1);
-        if (lane == 0 && n > 0) {   // chunk n - 1's V_new^T copy has been read (this chunk's tape entry may still be)
-          bulk_wait_read_but1();
-          mbar_arrive(&bar_sf);
-        }
+      // (MMA1 goes out from the MMA warp)
+      if (tid == 0 && n > 0) {   // chunk n - 1's V_new^T copy has been read (this chunk's tape entry may still be)
+        bulk_wait_read_but1();
+        mbar_arrive(&bar_sf);
       }
       if (with_o && n > 0) {   // the output of chunk n - 1, while MMA1 runs
         if (!(ok = wg_sync_and(1, mbar_wait(&bar_o[(n - 1) & 1], ((n - 1) >> 1) & 1, a.err)))) break;
@@ -272,30 +323,15 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
       if (with_vn) fence_async_smem();
       tc_fence_before();
       named_bar(1, 128);
-      if (warp == 0) {   // ---- MMA2: dS^T = (V_new^T diag(kd)) K; O^T = S^T Q'^T + V_new^T Aqk^T
-        if (with_vn && lane == 0) {
+      if (tid == 0) {   // ---- MMA2 and the output MMAs go out from the MMA warp
+        mbar_arrive(&go2);
+        if (with_vn) {
           bulk_store(a.vn + ((size_t)(c0 + n) * a.HV + hv) * VN_BYTES, st + SC_V, VN_BYTES);
           bulk_commit();
         }
-        // (the O buffer n & 1 was read out by output(n - 2) in this warpgroup's previous step)
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ts_w(tb + TM_DS, tb + TM_AVS + ks * 8, desc_mn(a_k, 64, ks), idesc(128, 128, 0, 1), ks > 0);
-        mma_commit_w(&bar_m2);
-        if (lane == 0) {   // this chunk's tape entry has been read: the S^T tile may be rewritten
-          if (with_vn) bulk_wait_read_but1();   // (the V_new^T copy just committed may still be reading)
-          else bulk_wait_read();
-        }
-        if (with_o) {
-          const uint32_t to = tb + TM_O + (n & 1) * 64;
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_ss_w(to, desc_k(sm_s, 128, ks), desc_k(a_q, 64, ks), idesc(128, 64, 0, 0), ks > 0);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_ts_w(to, tb + TM_AVN + ks * 8, desc_k(a_aqk, 64, ks), idesc(128, 64, 0, 0), 1u);
-          mma_commit_w(&bar_o[n & 1]);
-        }
+        // this chunk's tape entry has been read: the S^T tile may be rewritten
+        if (with_vn) bulk_wait_read_but1();   // (the V_new^T copy just committed may still be reading)
+        else bulk_wait_read();
       }
       ok = wg_sync_and(1, mbar_wait(&bar_m2, par, a.err));
       if (!ok) break;
@@ -321,6 +357,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
         bulk_store(a.tape + ((size_t)(c0 + n + 1) * a.HV + hv) * STATE_BYTES, s_tile, STATE_BYTES);
         bulk_commit();
       }
+      if (tid == 0 && n + 1 < nch) mbar_arrive(&go1);   // S^T of the next chunk is in its tile
     }
     if (ok && with_o && nch > 0) {   // the last chunk's output
       ok = wg_sync_and(1, mbar_wait(&bar_o[(nch - 1) & 1], ((nch - 1) >> 1) & 1, a.err));
@@ -422,8 +459,9 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
       }
     }
   }
+  if (tid == 0) mbar_wait(&done, 0, a.err);   // no MMA may outlive the TMEM allocation
   tc_fence_before();
-  __syncthreads();
+  named_bar(3, SC_WORK);
   if (warp == 0) tmem_dealloc(tb, 512);
 }
 
