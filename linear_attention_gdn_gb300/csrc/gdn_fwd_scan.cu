@@ -58,7 +58,7 @@ __device__ __forceinline__ void store_state_row(uint8_t* dst, int row, const flo
   }
 }
 
-// Two warpgroups.  The chain warpgroup (warps 0-3) owns the state and runs
+// Three warpgroups.  The chain warpgroup (warps 0-3) owns the state and runs
 // the dependent chain of each chunk:
 //   MMA1 (V_new^T = U^T - S^T W^T) -> V_new hop -> MMA2 (dS^T = (V_new^T
 //   diag(kd)) K, and the output O^T = S^T Q'^T + V_new^T Aqk^T with
@@ -66,8 +66,12 @@ __device__ __forceinline__ void store_state_row(uint8_t* dst, int row, const flo
 // and, while MMA1 of chunk n runs, writes the output of chunk n - 1 from its
 // O buffer.  The helper warpgroup (warps 4-7) prepares chunk n + 1 while the
 // chain works on chunk n (tile landing, W^T = K^T T'^T and U^T = V^T T''^T,
-// the -W^T tile, Q') and streams the tiles in.  They hand off through
-// mbarriers:
+// the -W^T tile, Q') and streams the tiles in.  The first warp of the third
+// warpgroup issues the chain's MMAs (MMA1; MMA2 then the output), so that no
+// chain warp is held by the issue; the rest of that warpgroup exits.  They
+// hand off through mbarriers:
+//   go1       chain -> MMA warp S^T(n) is in its tile
+//   go2       chain -> MMA warp the V_new^T(n) A operands are in TMEM
 //   bar_wr    helper -> chain   -W^T(n), U^T(n), Q'(n) are ready
 //   bar_m1    MMA1(n) done      (chain: V_new; helper: -W^T tile and D1 reuse)
 //   bar_m2    MMA2(n) done      (chain: S)
