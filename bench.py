@@ -39,8 +39,20 @@ C = 64
 
 
 # ---------------------------------------------------------------------------
-# algorithmic work per kernel launch: the dense tile products the chunked
-# method needs (KK^T, QK^T once per q/k head; the O(C^3) inverse not counted)
+# algorithmic work: the method's own FLOPs and HBM bytes (the dense tile
+# products of the chunked algorithm, KK^T and QK^T once per q/k head, the O(C^3)
+# inverse not counted; bytes = the method's inputs read once, its outputs
+# written once and the BF16 state saved every 64 tokens written once and read
+# once).  Per full chunk and value head this is the scope table's count:
+#   fwd  F_f = HV (6 d^2 + 6 C d) + H (4 C d) FLOP / token,
+#        57,728 B / token at (16, 48): q, k, v, g, beta in; o, states out
+#   bwd  F_b = HV (14 d^2 + 24 C d) + H (4 C d) FLOP / token,
+#        78,592 B / token: q, k, v, g, beta, dO, states in; dq, dk, dv, dg, dbeta out
+# Partial chunks use their real length L in place of C.  Each kernel is
+# credited with the method tensors it reads or writes (so a tensor two kernels
+# read counts for both) and with its share of the products; the intermediate
+# tapes this design keeps in HBM (dS', V_new^T, dV_new^T, T blocks) are never
+# credited: they are reported apart, as design bytes.
 # ---------------------------------------------------------------------------
 def chunk_lens(w):
     out = []
@@ -49,40 +61,54 @@ def chunk_lens(w):
     return out
 
 
+# per kernel: coefficients (a, b, c) of HV (a L d^2 + b L^2 d) + H (c L^2 d) per chunk of L tokens
+KERNEL_FLOP_TERMS = {
+    "prep_kernel": (0, 0, 4),        # KK^T, QK^T
+    "fwd_scan_kernel": (6, 6, 0),    # W S, S Q, Kd^T V_new; W, U, Aqk V_new
+    "fwd_walk_kernel": (6, 6, 4),    # the same with the UT stage (KK^T, QK^T) inside the walk
+    "bwd_scan_kernel": (6, 4, 0),    # dS' K^T, dV_new W, dO' Q; W, dO^T Aqk
+    "bwd_walk_kernel": (6, 4, 4),    # the same with the UT stage inside the walk
+    "grad_kernel": (8, 20, 4),       # the rest of F_b
+}
+
+
 def kernel_flops(name, w):
-    """FLOPs of one launch of `name` on workload w (real chunk lengths)."""
-    Ls = chunk_lens(w)
-    HV, H = w.HV, w.H
-    if name == "fwd_scan_kernel":        # W, U, Aqk V_new (C^2 d) + W S, S Q, Kd^T V_new (C d^2)
-        return sum(HV * (3 * 2 * L * L * D + 3 * 2 * L * D * D) for L in Ls)
-    if name == "bwd_scan_kernel":        # W, dO^T Aqk (C^2 d) + dS' K^T, dV W, dO' Q (C d^2)
-        return sum(HV * (2 * 2 * L * L * D + 3 * 2 * L * D * D) for L in Ls)
-    if name == "grad_kernel":            # 5 C d^2, 12 C^2 d, 2 C^3 per v-head; KK^T, QK^T per q/k head
-        return sum(HV * (5 * 2 * L * D * D + 12 * 2 * L * L * D + 2 * 2 * L ** 3) + H * 2 * 2 * L * L * D
-                   for L in Ls)
-    if name == "prep_kernel":            # KK^T, QK^T per q/k head
-        return sum(H * 2 * 2 * L * L * D for L in Ls)
-    return 0
+    """Method FLOPs of one launch of `name` on workload w (real chunk lengths)."""
+    a, b, c = KERNEL_FLOP_TERMS.get(name, (0, 0, 0))
+    return sum(w.HV * (a * L * D * D + b * L * L * D) + w.H * c * L * L * D for L in chunk_lens(w))
+
+
+def method_tensors(w):
+    """Bytes of each tensor the method reads or writes once (states: one BF16 128 x 128 per chunk and value
+    head)."""
+    T, H, HV, NC = w.T, w.H, w.HV, w.num_chunks
+    qk, vh, gb = T * H * D * 2 * 2, T * HV * D * 2, T * HV * 4 * 2
+    return {"qk": qk, "v": vh, "gb": gb, "o": vh, "dO": vh, "states": NC * HV * D * D * 2,
+            "dqdk": qk, "dv": vh, "dgdb": gb}
+
+
+KERNEL_METHOD_TENSORS = {
+    "prep_kernel": ("qk", "gb"),
+    "fwd_scan_kernel": ("qk", "v", "o", "states"),
+    "fwd_walk_kernel": ("qk", "v", "gb", "o", "states"),
+    "bwd_scan_kernel": ("qk", "dO"),
+    "bwd_walk_kernel": ("qk", "v", "gb", "dO", "states"),
+    "grad_kernel": ("qk", "v", "gb", "dO", "states", "dqdk", "dv", "dgdb"),
+}
 
 
 def kernel_bytes(name, w):
-    """Algorithmic HBM bytes of one launch: each tensor the kernel needs read once, each output
-    written once (the saved-set blocks at their stored sizes)."""
-    T, H, HV, NC = w.T, w.H, w.HV, w.num_chunks
-    qk = T * H * D * 2 * 2            # q and k, BF16
-    vh = T * HV * D * 2               # one [T, HV, 128] BF16 tensor (v, o, dO, dv)
-    gb = T * HV * 4 * 2               # g and beta, FP32
-    tile, state, scal = 8192, 32768, 1024
-    if name == "prep_kernel":         # -> T', T'', Aqk, T, scalars per (chunk, value head)
-        return qk + gb + NC * HV * (4 * tile + scal)
-    if name == "fwd_scan_kernel":     # q, k, v, T', T'', Aqk, scalars -> o, state tape, V_new^T
-        return qk + vh + NC * HV * (3 * tile + scal) + vh + NC * HV * (state + 2 * tile)
-    if name == "bwd_scan_kernel":     # q, k, dO, T', Aqk, scalars -> dS' tape, dV_new^T
-        return qk + vh + NC * HV * (2 * tile + scal) + NC * HV * (state + 2 * tile)
-    if name == "grad_kernel":         # q, k, v, dO, g, beta, tapes, V_new^T, dV_new^T, T, scalars -> dq, dk, dv, dg, dbeta
-        return (qk + 2 * vh + gb + NC * HV * (2 * state + 4 * tile + tile + scal)
-                + qk + vh + gb)
-    return 0
+    """Method bytes of one launch of `name` (the scope table's tensors it reads or writes)."""
+    m = method_tensors(w)
+    return sum(m[t] for t in KERNEL_METHOD_TENSORS.get(name, ()))
+
+
+def step_bytes(w, op):
+    m = method_tensors(w)
+    fwd = m["qk"] + m["v"] + m["gb"] + m["o"] + m["states"]
+    fwd_nosave = fwd - m["states"]
+    bwd = m["qk"] + m["v"] + m["gb"] + m["dO"] + m["states"] + m["dqdk"] + m["dv"] + m["dgdb"]
+    return {"fwd": fwd, "fwd+bwd": fwd + bwd, "ckpt": fwd_nosave + fwd + bwd}[op]
 
 
 def step_flops(w, op):
@@ -268,6 +294,38 @@ def run_ours(args, rank, world, local_rank):
 
     bnd = {}
 
+    def time_workload(idx, K, W):
+        """fwd + bwd of workload `idx` on its own inputs and buffers (freed afterwards)."""
+        ww = inputs.workload(idx)
+        xx = inputs.generate(ww, dev)
+        cu_w = torch.from_numpy(ww.cu_seqlens).to(dev)
+        pw = gdn.problem(ww.T, ww.N, ww.H, ww.HV, ww.scale, ww.l2norm, ww.segments)
+        bw = gdn.Buffers(pw, ww.cu_seqlens, device=dev)
+        ow = torch.empty((ww.T, ww.HV, D), dtype=torch.bfloat16, device=dev)
+        gr = (torch.empty_like(xx["q"]), torch.empty_like(xx["k"]), torch.empty_like(xx["v"]),
+              torch.empty_like(xx["g"]), torch.empty_like(xx["beta"]))
+
+        def st():
+            gdn.gdn_fwd(pw, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_w, ww.cu_seqlens, ow, bw.saved,
+                        bw.workspace, stream=stream)
+            gdn.gdn_bwd(pw, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_w, ww.cu_seqlens, xx["dO"],
+                        bw.saved, *gr, bw.workspace, stream=stream)
+        t_w = timed_replicas(st, K, W, barrier, allmax, event_clock)
+        stw = gdn.gdn_device_status(bw.workspace, stream)
+        assert stw == 0, gdn.gdn_status_string(stw)
+        seg = gdn.gdn_plan_segment_chunks(pw, ww.cu_seqlens)
+        max_chunks = max((n + C - 1) // C for n in ww.doc_lens)
+        pk_ = peaks()
+        fl = step_flops(ww, "fwd+bwd")
+        res = {"ms": round(t_w, 4), "Mtokens_per_s": round(replica_rate(world, ww.T, t_w), 3),
+               "TFLOP_per_s": round(world * fl / t_w / 1e9, 1),
+               "tensor_frac": round(world * fl / t_w / 1e9 / pk_["bf16_tflops_sustained"], 4),
+               "tokens": ww.T, "docs": ww.N, "l2norm": ww.l2norm,
+               "segments_of_longest_doc": -(-max_chunks // seg) if seg else None, "segment_chunks": seg}
+        del xx, bw, ow, gr
+        torch.cuda.empty_cache()
+        return res
+
     def barrier():
         if world > 1:
             import torch.distributed as dist
@@ -343,6 +401,11 @@ def run_ours(args, rank, world, local_rank):
                            "GB_per_s": round(nbytes / (t_c * 1e-3) / 1e9, 1),
                            "Mtokens_per_s": round(replica_rate(world, w.T, t_c), 3)}
         del cx, cdy, cy, cdx
+        # fwd+bwd of the scope table's other full-size workloads (8,192-token document; ~156 log-uniform
+        # documents of 262,144 tokens with L2 off; one 524,288-token document split into segments)
+        for widx in (1, 3, 4):
+            if widx != args.workload:
+                extra[f"workload{widx} fwd+bwd"] = time_workload(widx, max(3, args.steps // 2), 2)
 
     # end to end through the C ABI with pinned host buffers: every step copies
     # its inputs in and all of its outputs back
@@ -426,25 +489,7 @@ def run_ours(args, rank, world, local_rank):
     kt = {k: v for k, v in kstats.items() if v["timed_launches"] > 0}
     top = max(kt, key=lambda k: kt[k]["total_ms"])
     per_launch_ms = kt[top]["total_ms"] / kt[top]["timed_launches"]
-    fl = kernel_flops(top, w)
-    # the binding roof: the larger of the two time floors at the kernel's arithmetic intensity
-    if fl > 0 and fl / (pk["bf16_tflops_sustained"] * 1e12) >= kernel_bytes(top, w) / (pk["hbm_gbs"] * 1e9):
-        achieved = fl / (per_launch_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops_sustained"], 4)}
-        note = f"{pk['src']} sustained BF16 (the kernel is timed inside a multi-ms step)"
-    else:
-        by = kernel_bytes(top, w)
-        achieved = by / (per_launch_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / pk["hbm_gbs"], 4)}
-        if fl > 0:
-            roof["achieved_tflops"] = round(fl / (per_launch_ms * 1e-3) / 1e12, 2)
-        note = f"{pk['src']} HBM copy bandwidth"
-    roof.update({"traffic": ncu_traffic(top), "kernel": top, "peak_note": note,
-                 "launch_ms": round(per_launch_ms, 4), "algorithmic_flops_per_launch": fl,
-                 "algorithmic_bytes_per_launch": kernel_bytes(top, w),
-                 "achieved_hbm_gbs": round(kernel_bytes(top, w) / (per_launch_ms * 1e-3) / 1e9, 1)})
+    roof = roofline(top, w, per_launch_ms, pk)
     tot = sum(u["total_ms"] for u in kt.values())
     kernels = {}
     for k, v in kt.items():
@@ -452,8 +497,9 @@ def run_ours(args, rank, world, local_rank):
         kernels[k] = {"launches_per_step": round(v["launches"] / prof_steps, 2),
                       "ms_per_step": round(v["total_ms"] / prof_steps, 4), "share": round(v["total_ms"] / tot, 4),
                       "TFLOP_per_s": round(f * v["timed_launches"] / v["total_ms"] / 1e9, 1) if f else None,
-                      "GB_per_s": round(b * v["timed_launches"] / v["total_ms"] / 1e6, 1) if b else None}
+                      "method_GB_per_s": round(b * v["timed_launches"] / v["total_ms"] / 1e6, 1) if b else None}
     tflops = world * step_flops(w, op) / ms / 1e9
+    step_gbs = world * step_bytes(w, op) / ms / 1e6
     in_gb = sum(x[n].numel() * x[n].element_size() for n in ("q", "k", "v", "g", "beta", "dO")) / 1e9
     return {
         "metric": METRIC, "value": round(replica_rate(world, w.T, ms), 3), "unit": UNIT, "n_gpus": world,
@@ -464,9 +510,38 @@ def run_ours(args, rank, world, local_rank):
                    "l2_flush": f"none needed: {in_gb:.1f} GB of inputs per step exceed the 129 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "tflops": round(tflops, 1), "tensor_frac_of_step": round(tflops / pk["bf16_tflops_sustained"], 4),
+        "step_method_GB_per_s": round(step_gbs, 1), "hbm_frac_of_step": round(step_gbs / pk["hbm_gbs"], 4),
         "roofline": roof, "kernels": kernels, "gpu_launches": n_launch, "clocks": clk.summary(),
         "e2e": e2e, "ops": extra,
     }
+
+
+def roofline(kernel, w, launch_ms, pk):
+    """The roofline object of one kernel: method FLOPs and bytes of one launch (the scope table's per-token
+    counts over the workload's real chunks) over its measured launch time, against the binding roof (the
+    larger of the two time floors at those counts)."""
+    fl, by = kernel_flops(kernel, w), kernel_bytes(kernel, w)
+    t_tensor = fl / (pk["bf16_tflops_sustained"] * 1e12)
+    t_hbm = by / (pk["hbm_gbs"] * 1e9)
+    if fl > 0 and t_tensor >= t_hbm:
+        achieved = fl / (launch_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops_sustained"], 4)}
+        note = f"{pk['src']} sustained BF16 (the kernel is timed inside a multi-ms step)"
+    else:
+        achieved = by / (launch_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 4)}
+        note = f"{pk['src']} HBM copy bandwidth"
+    traffic = ncu_traffic(kernel)
+    roof.update({"traffic": traffic, "kernel": kernel, "peak_note": note, "launch_ms": round(launch_ms, 4),
+                 "method_flops_per_launch": fl, "method_bytes_per_launch": by,
+                 "tensor_frac": round(fl / (launch_ms * 1e-3) / 1e12 / pk["bf16_tflops_sustained"], 4),
+                 "hbm_frac": round(by / (launch_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                 "traffic_over_method_bytes": round(traffic / by, 3) if traffic and by else None,
+                 "counting": "method FLOPs / bytes per the scope table's per-token counts (real chunk lengths); "
+                             "the design's own intermediate tapes are not credited (traffic shows them)"})
+    return roof
 
 
 # ---------------------------------------------------------------------------

@@ -30,11 +30,16 @@
  *     segment plan, buffer sizes) and the device copy drives the kernels.  The
  *     two must hold the same values.
  *   - Ownership: the caller allocates and owns every buffer (inputs, outputs,
- *     `saved`, `workspace`).  The library allocates no device memory, keeps no
- *     per-call global state, and launches everything asynchronously on
- *     `stream` in stream order; it never synchronises the host except in
- *     gdn_device_status().  Calls on different streams must use different
- *     workspaces.
+ *     `saved`, `workspace`).  The library allocates no device memory at run
+ *     time and launches everything asynchronously on `stream` in stream order;
+ *     it never synchronises the host except in gdn_device_status().  Calls on
+ *     different streams must use different workspaces.  The library keeps no
+ *     per-call state outside the caller's buffers, except two process-wide
+ *     items: the optional launch counters and timing events of
+ *     gdn_profile_enable() / gdn_profile_read(), and the fixed device array of
+ *     gdn_fwd_noalloc(), which every GPU that loads the library reserves
+ *     (GDN_FWD_NOALLOC_SCRATCH_BYTES) whether or not that entry point is
+ *     called.
  *   - Errors are returned, never thrown.  Host-side checks (null pointers,
  *     sizes, cu_seqlens, alignment, buffer sizes) return before any launch.
  *     Conditions only the device can see (a saved buffer whose header does
@@ -248,9 +253,13 @@ gdn_status gdn_chunk_table_offsets(const gdn_problem *prob, const int32_t *cu_se
  *     contents; the forward rewrites everything it reads.  Calls that overlap
  *     on the GPU (different streams, or different host threads) race on the
  *     array and must be serialised by the caller.
- *   - Device-side conditions (a bounded wait that ran out) are recorded in the
- *     array, which the caller cannot address, so this entry point reports only
- *     host-side statuses.
+ *   - Device-side conditions (a device copy of cu_seqlens that disagrees with
+ *     the host copy, a bounded wait that ran out) are recorded in the array,
+ *     which the caller cannot address, so this entry point reports only
+ *     host-side statuses; after such a condition the kernels skip their work
+ *     and `o` is left undefined (whatever it held before the call).  A caller
+ *     that needs the device-side status uses gdn_fwd with its own workspace
+ *     and gdn_device_status.
  * No cudaMalloc, cudaFree or allocating library routine is called.
  */
 #define GDN_FWD_NOALLOC_SCRATCH_BYTES (64u << 20)

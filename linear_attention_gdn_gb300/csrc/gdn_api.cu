@@ -106,7 +106,7 @@ static gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
   P->sms = sm_count();
   plan_segments(p, cu, &P->seg_len, &P->split_min, &P->max_doc_chunks);
   int NC = 0, NSEG = 0, nsplit = 0, nsdoc = 0, n_empty = 0;
-  uint32_t h = 2166136261u;
+  uint32_t h = 0u;
   for (int i = 0; i < p->N; ++i) {
     const int n = (cu[i + 1] - cu[i] + CHUNK - 1) / CHUNK;
     const int Pd = n > P->split_min ? (n + P->seg_len - 1) / P->seg_len : (n > 0 ? 1 : 0);
@@ -117,11 +117,7 @@ static gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
       nsplit += Pd - 1;
       nsdoc += 1;
     }
-    uint32_t x = (uint32_t)cu[i + 1];
-    for (int b = 0; b < 4; ++b) {
-      h ^= (x >> (8 * b)) & 0xffu;
-      h *= 16777619u;
-    }
+    h += cu_entry_hash(i, cu[i + 1]);
   }
   P->NC = NC;
   P->NSEG = NSEG;
@@ -292,6 +288,8 @@ gdn_status run_tables(const Plan& P, const gdn_problem* p, const int32_t* cu_dev
   if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return GDN_ERR_CUDA;
   TableArgs ta;
   ta.cu = cu_dev;
+  ta.T = P.T;
+  ta.cu_hash = P.cu_hash;
   ta.N = P.N;
   ta.NC = P.NC;
   ta.NSEG = P.NSEG;

@@ -57,8 +57,26 @@ struct Tables {
   int* sdoc_first;     // [nsdoc+1] first split index of each split document
 };
 
+// Hash of one cu_seqlens entry (document d ends at token `end`): murmur3's
+// 32-bit finaliser of the entry mixed with its index.  The hash of a whole
+// cu_seqlens is the sum of its entries' hashes mod 2^32, which the host and
+// the table kernel both compute (the kernel in parallel, in any order).
+__host__ __device__ inline uint32_t fmix32(uint32_t h) {
+  h ^= h >> 16;
+  h *= 0x85ebca6bu;
+  h ^= h >> 13;
+  h *= 0xc2b2ae35u;
+  h ^= h >> 16;
+  return h;
+}
+__host__ __device__ inline uint32_t cu_entry_hash(int d, int end) {
+  return fmix32((uint32_t)end ^ fmix32((uint32_t)d + 0x9e3779b9u));
+}
+
 struct TableArgs {
   const int* cu;
+  int64_t T;
+  uint32_t cu_hash;         // sum over d of cu_entry_hash(d, cu[d + 1]) of the host copy
   int N, NC, NSEG, nsplit, nsdoc;
   int seg_len, split_min;   // a document of n chunks is split iff n > split_min
   Tables t;

@@ -55,12 +55,24 @@ __device__ __forceinline__ void block_scan4(int v[4], int excl[4], int total[4])
 }
 
 __global__ void __launch_bounds__(1024) tables_scan_kernel(TableArgs a) {
+  __shared__ uint32_t s_hash;
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) {
+    s_hash = 0u;
+    s_bad = 0;
+  }
+  __syncthreads();
   int carry[4] = {0, 0, 0, 0};   // chunks, segments, split segments, split documents
+  uint32_t hsum = 0u;            // this thread's share of the cu_seqlens hash
+  int bad = 0;
   for (int base = 0; base < a.N; base += 1024) {
     const int d = base + (int)threadIdx.x;
     int v[4] = {0, 0, 0, 0};
     if (d < a.N) {
-      const int len = a.cu[d + 1] - a.cu[d];
+      const int lo = a.cu[d], hi = a.cu[d + 1];
+      hsum += cu_entry_hash(d, hi);
+      bad |= hi < lo;
+      const int len = hi < lo ? 0 : hi - lo;
       const int n = (len + CH - 1) / CH;
       const int P = n > a.split_min ? (n + a.seg_len - 1) / a.seg_len : (n > 0 ? 1 : 0);
       v[0] = n;
@@ -79,16 +91,25 @@ __global__ void __launch_bounds__(1024) tables_scan_kernel(TableArgs a) {
 #pragma unroll
     for (int m = 0; m < 4; ++m) carry[m] += total[m];
   }
+  atomicAdd(&s_hash, hsum);   // a sum mod 2^32: the order of the additions does not matter
+  if (bad) atomicOr(&s_bad, 1);
+  __syncthreads();
   if (threadIdx.x == 0) {
     a.t.chunk_offsets[a.N] = carry[0];
     a.t.seg_offsets[a.N] = carry[1];
     a.t.split_offsets[a.N] = carry[2];
     if (carry[3] <= a.nsdoc) a.t.sdoc_first[carry[3]] = carry[2];
-    // the host planned from its copy of cu_seqlens; a device copy that
-    // disagrees is reported instead of indexing out of bounds
-    if (carry[0] != a.NC || carry[1] != a.NSEG || carry[2] != a.nsplit || carry[3] != a.nsdoc)
+    // The host planned from its copy of cu_seqlens.  The device copy must hold
+    // the same values: cu[0] = 0, non-decreasing, cu[N] = T, and the same hash
+    // of every entry (which catches, say, two documents with swapped lengths,
+    // where every count above still agrees).  On any mismatch the error word
+    // is set here, before the fill kernel and every later kernel of the call,
+    // which all skip their work once it is set.
+    if (a.cu[0] != 0 || (int64_t)a.cu[a.N] != a.T || s_bad || s_hash != a.cu_hash || carry[0] != a.NC ||
+        carry[1] != a.NSEG || carry[2] != a.nsplit || carry[3] != a.nsdoc)
       atomicCAS(a.err, 0, 1 /* GDN_ERR_INVALID_ARG */);
-    if (a.saved) *reinterpret_cast<SavedHeader*>(a.saved) = a.hdr;
+    else if (a.saved)
+      *reinterpret_cast<SavedHeader*>(a.saved) = a.hdr;
   }
 }
 

@@ -99,3 +99,31 @@ def test_saved_mismatch_refused():
     assert gdn.gdn_device_status(buf.workspace) == 4
     for n in GRADS:
         assert torch.isnan(g2[n].float()).all(), n
+
+
+@pytest.mark.parametrize("dev_cu", [
+    [0, 192, 320],    # the two documents' lengths swapped: same total, same chunk count
+    [0, 128, 300],    # the last document cut short: the device copy ends before T
+    [0, 200, 160],    # decreasing
+])
+def test_disagreeing_device_cu_seqlens_refused(dev_cu):
+    """The host copy of cu_seqlens plans the call and the device copy drives the
+    kernels.  A device copy that differs from the host copy is caught by the
+    table kernel (GDN_ERR_INVALID_ARG) before any kernel indexes with it; every
+    output stays unwritten."""
+    import linear_attention_gdn_gb300 as gdn
+    w = inputs.workload(0)   # host cu_seqlens [0, 128, 320]
+    d = to_dev(inputs.generate(w, "cpu"))
+    bad = torch.tensor(dev_cu, dtype=torch.int32, device="cuda")
+    prob = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm)
+    buf = gdn.Buffers(prob, w.cu_seqlens, fill=255)
+    o = torch.full((w.T, w.HV, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_fwd(prob, d["q"], d["k"], d["v"], d["g"], d["beta"], bad, w.cu_seqlens, o, buf.saved, buf.workspace)
+    assert gdn.gdn_device_status(buf.workspace) == 1
+    assert torch.isnan(o.float()).all()
+    gr = alloc_grads(w)
+    gdn.gdn_bwd(prob, d["q"], d["k"], d["v"], d["g"], d["beta"], bad, w.cu_seqlens, d["dO"], buf.saved,
+                gr["dq"], gr["dk"], gr["dv"], gr["dg"], gr["dbeta"], buf.workspace)
+    assert gdn.gdn_device_status(buf.workspace) == 1
+    for n in GRADS:
+        assert torch.isnan(gr[n].float()).all(), n

@@ -75,21 +75,22 @@ def test_full_size_parity(idx):
     res = ref.run(x, w.H, w.HV, l2norm=w.l2norm, scale=w.scale, units=units)
     cu = w.cu_seqlens
     G = w.HV // w.H
-    for name in GRADS:
-        gv, rv = [], []
-        for u, r in res:
-            s0 = int(cu[u.doc]) + u.t0
-            s1 = int(cu[u.doc]) + u.t1
-            r0, r1 = u.t0 - u.a, u.t1 - u.a
-            hs = slice(u.j * G, (u.j + 1) * G)
+    # every sampled (document, q/k-head group) unit is compared on its own, so that one bad unit
+    # cannot hide under the others
+    for u, r in res:
+        s0 = int(cu[u.doc]) + u.t0
+        s1 = int(cu[u.doc]) + u.t1
+        r0, r1 = u.t0 - u.a, u.t1 - u.a
+        hs = slice(u.j * G, (u.j + 1) * G)
+        tag = f"workload{idx}/doc{u.doc}/group{u.j}/tokens{u.t0}-{u.t1}"
+        for name in GRADS:
             if name in ("dq", "dk"):
-                gv.append(got[name][s0:s1, u.j].double().cpu().numpy())
-                rv.append(r[name][r0:r1])
+                gv = got[name][s0:s1, u.j].double().cpu().numpy()
+                rv = r[name][r0:r1]
             elif name in ("dg", "dbeta"):
-                gv.append(got[name][s0:s1, hs].double().cpu().numpy())
-                rv.append(r[name][:, r0:r1].T)
+                gv = got[name][s0:s1, hs].double().cpu().numpy()
+                rv = r[name][:, r0:r1].T
             else:
-                gv.append(got[name][s0:s1, hs].double().cpu().numpy())
-                rv.append(r[name][:, r0:r1].transpose(1, 0, 2))
-        compare(f"workload{idx}/{name}", np.concatenate([a.ravel() for a in gv]),
-                np.concatenate([a.ravel() for a in rv]))
+                gv = got[name][s0:s1, hs].double().cpu().numpy()
+                rv = r[name][:, r0:r1].transpose(1, 0, 2)
+            compare(f"{tag}/{name}", gv, rv)
