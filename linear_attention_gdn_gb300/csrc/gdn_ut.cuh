@@ -1,0 +1,349 @@
+// gdn_ut.cuh -- the on-chip UT / WY stage of one 64-token chunk and one value
+// head, run by one 128-thread warpgroup inside the walk kernels.
+//
+// For the chunk's tokens r < L (q/k head j, value head h):
+//   rk_r, rq_r   1/sqrt(x.x + 1e-6) of k_r, q_r (or 1 with l2norm off)
+//   G_r   = sum_{i<=r} g_i        (chunk-local cumulative gate: the pages'
+//                                  "GLM prep" gate prefix rows)
+//   A     = strict_tril(beta_r e^{G_r - G_c} k^_r.k^_c)          ("Akk")
+//   T     = (I + A)^-1
+//   Aqk   = tril(e^{G_r - G_c} q^_r.k^_c)                         ("Aqk")
+//   T'    = T diag(beta gamma rk),  T'' = T diag(beta)
+// so that W = T diag(beta gamma) K^ = T' K and U = T diag(beta) V = T'' V are
+// the WY program's w and u ("feat(cake_gdn_kcp) ... #8172" page, commit notes
+// on the intra / WY / GLM-prep programs; "#8542" page, the save-set table,
+// which lists gcum, Akk, Aqk, w and u among what the replay form recomputes).
+// KK^T and QK^T come from one tcgen05 MMA on the stacked [K; Q] tile (M = 128)
+// into 64 TMEM columns; the unit lower-triangular inverse is FP32, blocked by
+// 16 x 16: the four diagonal blocks by forward substitution (one lane per
+// column), then the three block diagonals, each block from the finished ones
+// (T_ij = -T_ii sum_k A_ik T_kj), on 64 lanes.
+//
+// Gate factors: e^{G_r - G_c} for c <= r is the product e^{G_r - G_0}
+// e^{G_0 - G_c} of per-token factors when the chunk's gate range G_0 - G_{L-1}
+// is below 2^100 (log2 units, safe in FP32), and one exp2f per element
+// otherwise.
+//
+// Tiles: the [K; Q] tile is a SwTile(128 x 128) with rows 0-63 the chunk's k
+// tokens and rows 64-127 its q tokens (64-column panels 16 KB apart: four TMA
+// boxes land it); Aqk, T', T'', T are SwTile(64 x 64) BF16.  The scalar block
+// holds sc_r = scale gamma_r rq_r [64], kd_r = e^{G_L - G_r} rk_r [64],
+// e^{G_L} and L (as an int), 1 KB.
+#pragma once
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+constexpr float kUtLog2e = 1.4426950408889634f;
+constexpr float kUtSafeRange = 100.f;   // log2 units
+constexpr int UT_ALD = 68;              // row pitch (floats) of the FP32 A^T / T array
+constexpr int UT_WORK_BYTES = 64 * UT_ALD * 4;   // 17,408: the FP32 array; T' then T'' are written over it
+constexpr int UT_SCAL_BYTES = 1024;
+static_assert(2 * 8192 <= UT_WORK_BYTES, "T' and T'' fit in the FP32 array's space");
+
+// per-token factors of one chunk, shared by the warpgroup
+struct UtTok {
+  float rq[64], rk[64];
+  float Gs[64], bs[64], eGr[64], eGi[64];
+  float cf[64];     // rk_c e^{G_0 - G_c}: the column factor of A and Aqk
+  float ca[64];     // beta_r rk_r e^{G_r - G_0}: the row factor of A
+  float pcol[64];   // beta_c e^{G_c} rk_c: the column factor of T'
+  int safe;
+};
+
+// Zero the rows L..63 of the [K; Q] tile (they hold the next document's tokens).
+__device__ __forceinline__ void ut_zero_tail(uint8_t* kq, int L, int lt) {
+  for (int idx = lt; idx < (CH - L) * 32; idx += 128) {
+    const int t = idx >> 5, half = (idx >> 4) & 1, c8 = idx & 15;
+    *reinterpret_cast<uint4*>(kq + sw_chunk(half * 64 + L + t, c8, 128)) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// L2 norm of row lt of the [K; Q] tile: four partial sums of 32 elements (each the sum of its even-
+// and its odd-element chain, the two run as paired FMAs), combined as (p0 + p1) + (p2 + p3).  The
+// gradient kernel sums in the same order.
+__device__ __forceinline__ void ut_norm_row(const uint8_t* kq, int lt, int l2norm, UtTok& u) {
+  float pr[4];
+#pragma unroll
+  for (int qq = 0; qq < 4; ++qq) {
+    float se = 0.f, so = 0.f;
+#pragma unroll
+    for (int c8 = qq * 4; c8 < qq * 4 + 4; ++c8) {
+      const uint4 val = *reinterpret_cast<const uint4*>(kq + sw_chunk(lt, c8, 128));
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&val);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h2[e]);
+        fma2v(se, so, f.x, f.y, f.x, f.y);
+      }
+    }
+    pr[qq] = se + so;
+  }
+  const float ss = (pr[0] + pr[1]) + (pr[2] + pr[3]);
+  const float rn = l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+  if (lt < 64) u.rk[lt] = rn;
+  else u.rq[lt - 64] = rn;
+}
+
+// The gate loads of one warp (lane -> tokens 2 lane, 2 lane + 1); zero past L.
+__device__ __forceinline__ void ut_load_gates(const float* g, const float* beta, int HV, int hv, int tok0, int L,
+                                              int lane, float (&gb)[4]) {
+  const int r0 = 2 * lane, r1 = r0 + 1;
+  gb[0] = gb[1] = gb[2] = gb[3] = 0.f;
+  if (r0 < L) {
+    gb[0] = g[(size_t)(tok0 + r0) * HV + hv];
+    gb[2] = beta[(size_t)(tok0 + r0) * HV + hv];
+  }
+  if (r1 < L) {
+    gb[1] = g[(size_t)(tok0 + r1) * HV + hv];
+    gb[3] = beta[(size_t)(tok0 + r1) * HV + hv];
+  }
+}
+
+// The per-token gate factors (one warp; needs rk): cumulative gate in log2 units and the factors above.
+__device__ __forceinline__ void ut_gates(const float (&gb)[4], int lane, UtTok& u) {
+  const int r0 = 2 * lane, r1 = r0 + 1;
+  const float g0 = gb[0], g1 = gb[1], b0 = gb[2], b1 = gb[3];
+  float s = g0 + g1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, s, o);
+    if (lane >= o) s += y;
+  }
+  const float ex = s - (g0 + g1);
+  const float G0v = (ex + g0) * kUtLog2e, G1v = (ex + g0 + g1) * kUtLog2e;
+  u.Gs[r0] = G0v;
+  u.Gs[r1] = G1v;
+  u.bs[r0] = b0;
+  u.bs[r1] = b1;
+  const float Gfirst = __shfl_sync(0xffffffffu, G0v, 0);
+  const float Glast = __shfl_sync(0xffffffffu, G1v, 31);   // = G_{L-1} (gates past L are 0)
+  const float er0 = exp2f(G0v - Gfirst), er1 = exp2f(G1v - Gfirst);
+  u.eGr[r0] = er0;
+  u.eGr[r1] = er1;
+  const bool sf = (Gfirst - Glast) < kUtSafeRange;
+  const float ei0 = sf ? exp2f(Gfirst - G0v) : 0.f, ei1 = sf ? exp2f(Gfirst - G1v) : 0.f;
+  u.eGi[r0] = ei0;
+  u.eGi[r1] = ei1;
+  const float k0 = u.rk[r0], k1 = u.rk[r1];
+  u.cf[r0] = k0 * ei0;
+  u.cf[r1] = k1 * ei1;
+  u.ca[r0] = b0 * k0 * er0;
+  u.ca[r1] = b1 * k1 * er1;
+  u.pcol[r0] = b0 * exp2f(G0v) * k0;
+  u.pcol[r1] = b1 * exp2f(G1v) * k1;
+  if (lane == 0) u.safe = sf;
+}
+
+// Issue KK^T and QK^T (one M = 128, N = 64 MMA of [K; Q] against K) into 64 TMEM columns at `dst`
+// (warp-uniform; one lane issues).
+__device__ __forceinline__ void ut_issue_kkqk(uint32_t dst, uint32_t kq_addr) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks)
+    mma_ss_w(dst, desc_k(kq_addr, 128, ks), desc_k(kq_addr, 128, ks), idesc(128, 64, 0, 0), ks > 0);
+}
+
+// From row lt of [KK^T; QK^T] in TMEM (columns `kk` .. kk + 63, lane quarter wq): threads lt < 64 write
+// row lt of the transposed A into the FP32 array Sm and the chunk scalars; threads lt >= 64 write row
+// lt - 64 of Aqk into `aqk` (if non-null).
+__device__ __forceinline__ void ut_build(uint32_t tb, int wq, int kk, int lt, int L, float scale, const UtTok& u,
+                                         float* Sm, uint8_t* aqk, float* scal) {
+  const bool sf = u.safe;
+  if (lt >= 64 && aqk == nullptr) return;
+#pragma unroll 1
+  for (int cb0 = 0; cb0 < CH; cb0 += 32) {
+    float kq[32];   // row lt of [KK^T; QK^T], columns cb0 .. cb0 + 31
+    tmem_ld32(taddr(tb, wq * 32, kk + cb0), kq);
+    if (lt < 64) {
+      // KK^T is symmetric, so the thread holding its row c writes row c of the transposed A:
+      // S[c][r] = A[r][c] = (beta_r rk_r e^{G_r - G_0}) (rk_c e^{G_0 - G_c}) KK[c][r] for c < r < L
+      const int cc = lt;
+      if (sf) {
+        const float pc = u.cf[cc];
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const int r0 = cb0 + 4 * e4;
+          const float4 f = *reinterpret_cast<const float4*>(&u.ca[r0]);
+          float4 v;
+          v.x = (r0 + 0 > cc && r0 + 0 < L) ? pc * f.x * kq[4 * e4 + 0] : 0.f;
+          v.y = (r0 + 1 > cc && r0 + 1 < L) ? pc * f.y * kq[4 * e4 + 1] : 0.f;
+          v.z = (r0 + 2 > cc && r0 + 2 < L) ? pc * f.z * kq[4 * e4 + 2] : 0.f;
+          v.w = (r0 + 3 > cc && r0 + 3 < L) ? pc * f.w * kq[4 * e4 + 3] : 0.f;
+          *reinterpret_cast<float4*>(Sm + cc * UT_ALD + r0) = v;
+        }
+      } else {
+        const float pc = u.rk[cc];
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const int r0 = cb0 + 4 * e4;
+          float x[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int r = r0 + q;
+            x[q] = (r > cc && r < L) ? u.bs[r] * u.rk[r] * pc * exp2f(u.Gs[r] - u.Gs[cc]) * kq[4 * e4 + q] : 0.f;
+          }
+          *reinterpret_cast<float4*>(Sm + cc * UT_ALD + r0) = make_float4(x[0], x[1], x[2], x[3]);
+        }
+      }
+    } else {
+      const int r = lt - 64;
+      const float pr = u.rq[r] * (sf ? u.eGr[r] : 1.f);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float x[8];
+        if (sf) {
+          const float4 fa = *reinterpret_cast<const float4*>(&u.cf[cb0 + q4 * 8]);
+          const float4 fb = *reinterpret_cast<const float4*>(&u.cf[cb0 + q4 * 8 + 4]);
+          const float fv[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int jj = cb0 + q4 * 8 + e;
+            x[e] = (jj <= r && r < L) ? pr * fv[e] * kq[q4 * 8 + e] : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int jj = cb0 + q4 * 8 + e;
+            x[e] = (jj <= r && r < L) ? pr * u.rk[jj] * exp2f(u.Gs[r] - u.Gs[jj]) * kq[q4 * 8 + e] : 0.f;
+          }
+        }
+        uint4 w;
+        w.x = pack_bf16(x[0], x[1]);
+        w.y = pack_bf16(x[2], x[3]);
+        w.z = pack_bf16(x[4], x[5]);
+        w.w = pack_bf16(x[6], x[7]);
+        *reinterpret_cast<uint4*>(aqk + sw_chunk(r, (cb0 >> 3) + q4, 64)) = w;
+      }
+    }
+  }
+  if (lt < 64) {
+    const int r = lt;
+    const float GL = u.Gs[L - 1];
+    scal[r] = r < L ? scale * exp2f(u.Gs[r]) * u.rq[r] : 0.f;
+    scal[64 + r] = r < L ? exp2f(GL - u.Gs[r]) * u.rk[r] : 0.f;
+    if (r == 0) {
+      scal[128] = exp2f(GL);
+      reinterpret_cast<int*>(scal)[129] = L;
+    }
+  }
+}
+
+// One block diagonal d of T = (I + A)^-1 (16 x 16 blocks, 64 lanes): T_ij = -T_ii p with
+// p = sum_{k=j}^{i-1} A_ik T_kj, for the 4 - d blocks (i, j = i - d).  Sm holds A[r][c] (c < r) at
+// Sm[c][r] and T[r][c] (c <= r) at Sm[r][c]; the upper triangles of the diagonal blocks hold zeros.
+// The (4 - d) * 16 columns are spread over 64 lanes as G = 1, 2, 4 lanes per column; lane g of a
+// column accumulates rows [16g/G, 16(g+1)/G) of p over the whole k range, the G lanes exchange their
+// rows by shuffles, and each then forms its rows of T_ij.
+template <int DL>
+__device__ __forceinline__ void ut_offdiag_level(float* Sm, int l) {
+  constexpr int G = DL == 1 ? 1 : (DL == 2 ? 2 : 4);
+  constexpr int R = 16 / G;
+  constexpr int NCOL = (4 - DL) * 16;
+  const int cl = l / G, g = l % G;
+  const bool act = cl < NCOL;
+  const int jb = act ? cl >> 4 : 0, oi = 16 * (jb + DL), c = 16 * jb + (cl & 15);
+  float p[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) p[r] = 0.f;
+  if (act) {
+#pragma unroll 4
+    for (int t = 16 * jb; t < oi; ++t) {
+      const float tv = Sm[t * UT_ALD + c];
+#pragma unroll
+      for (int q = 0; q < R / 4; ++q) {
+        const float4 av = *reinterpret_cast<const float4*>(Sm + t * UT_ALD + oi + g * R + 4 * q);
+        fma2(p[4 * q + 0], p[4 * q + 1], av.x, av.y, tv);
+        fma2(p[4 * q + 2], p[4 * q + 3], av.z, av.w, tv);
+      }
+    }
+  }
+  float pf[16];
+  if constexpr (G == 1) {
+#pragma unroll
+    for (int r = 0; r < 16; ++r) pf[r] = p[r];
+  } else {
+#pragma unroll
+    for (int og = 0; og < G; ++og)
+#pragma unroll
+      for (int r = 0; r < R; ++r) pf[og * R + r] = __shfl_sync(0xffffffffu, p[r], (l & 31 & ~(G - 1)) + og);
+  }
+  if (act) {
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {   // T_ij[r][c] = -sum_{s <= r} T_ii[r][s] p[s]
+      const int r = g * R + rr;
+      float acc = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (G == 1 && 4 * q > rr) continue;
+        const float4 tv4 = *reinterpret_cast<const float4*>(Sm + (oi + r) * UT_ALD + oi + 4 * q);
+        acc = fmaf(tv4.x, pf[4 * q + 0], acc);
+        if (G > 1 || 4 * q + 1 <= rr) acc = fmaf(tv4.y, pf[4 * q + 1], acc);
+        if (G > 1 || 4 * q + 2 <= rr) acc = fmaf(tv4.z, pf[4 * q + 2], acc);
+        if (G > 1 || 4 * q + 3 <= rr) acc = fmaf(tv4.w, pf[4 * q + 3], acc);
+      }
+      Sm[(oi + r) * UT_ALD + c] = -acc;
+    }
+  }
+}
+
+// T = (I + A)^-1 in place in Sm, on lanes l = 0..63 (warps of one 64-thread group that syncs on named
+// barrier `bar_id`).  Call after the A^T rows of ut_build are written.
+__device__ __forceinline__ void ut_inverse(float* Sm, int l, int bar_id) {
+  named_bar(bar_id, 64);
+  {  // diagonal blocks T_bb = (I + A_bb)^-1 by forward substitution, lane = column
+    const int o = 16 * (l >> 4), cc = l & 15;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = (i == cc) ? 1.f : 0.f;
+#pragma unroll
+    for (int jq = 0; jq < 15; ++jq) {
+      const float xj = x[jq];
+#pragma unroll
+      for (int g4 = (jq + 1) >> 2; g4 < 4; ++g4) {
+        const float4 av = *reinterpret_cast<const float4*>(Sm + (o + jq) * UT_ALD + o + 4 * g4);
+        if (4 * g4 + 0 > jq) fma2(x[4 * g4 + 0], x[4 * g4 + 1], -av.x, -av.y, xj);
+        else if (4 * g4 + 1 > jq) x[4 * g4 + 1] = fmaf(-av.y, xj, x[4 * g4 + 1]);
+        if (4 * g4 + 2 > jq) fma2(x[4 * g4 + 2], x[4 * g4 + 3], -av.z, -av.w, xj);
+        else if (4 * g4 + 3 > jq) x[4 * g4 + 3] = fmaf(-av.w, xj, x[4 * g4 + 3]);
+      }
+    }
+    __syncwarp();   // every lane of the block has read its A entries
+#pragma unroll
+    for (int i = 0; i < 16; ++i) Sm[(o + i) * UT_ALD + o + cc] = x[i];   // x[i] = 0 above the diagonal
+  }
+  named_bar(bar_id, 64);
+  ut_offdiag_level<1>(Sm, l);
+  named_bar(bar_id, 64);
+  ut_offdiag_level<2>(Sm, l);
+  named_bar(bar_id, 64);
+  ut_offdiag_level<3>(Sm, l);
+}
+
+// The four 16-byte chunks (row i, columns 8 c8 .. 8 c8 + 7) of T that thread lt of the warpgroup
+// handles, read from the FP32 array (zero above the diagonal, where the array still holds A^T).
+__device__ __forceinline__ void ut_read_T(const float* Sm, int lt, float (&tv)[4][8]) {
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int item = lt + 128 * it, i = item >> 3, c8 = item & 7;
+    const float4 u0 = *reinterpret_cast<const float4*>(Sm + i * UT_ALD + 8 * c8);
+    const float4 u1 = *reinterpret_cast<const float4*>(Sm + i * UT_ALD + 8 * c8 + 4);
+    const float x[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) tv[it][e] = 8 * c8 + e <= i ? x[e] : 0.f;
+  }
+}
+
+// 16-byte chunk `it` of T with its columns scaled by f (f == nullptr: unscaled), as BF16
+__device__ __forceinline__ uint4 ut_chunk(const float (&tv)[4][8], int it, int c8, const float* f) {
+  float y[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) y[e] = f ? tv[it][e] * f[8 * c8 + e] : tv[it][e];
+  uint4 w;
+  w.x = pack_bf16(y[0], y[1]);
+  w.y = pack_bf16(y[2], y[3]);
+  w.z = pack_bf16(y[4], y[5]);
+  w.w = pack_bf16(y[6], y[7]);
+  return w;
+}
+
+}  // namespace gdn
