@@ -69,6 +69,7 @@ KERNEL_FLOP_TERMS = {
     "bwd_scan_kernel": (6, 4, 0),    # dS' K^T, dV_new W, dO' Q; W, dO^T Aqk
     "bwd_walk_kernel": (6, 4, 4),    # the same with the UT stage inside the walk
     "grad_kernel": (8, 20, 4),       # the rest of F_b
+    "vnew_kernel": (2, 4, 0),        # replay form: W, U and W S again
 }
 
 
@@ -83,7 +84,7 @@ def method_tensors(w):
     head)."""
     T, H, HV, NC = w.T, w.H, w.HV, w.num_chunks
     qk, vh, gb = T * H * D * 2 * 2, T * HV * D * 2, T * HV * 4 * 2
-    return {"qk": qk, "v": vh, "gb": gb, "o": vh, "dO": vh, "states": NC * HV * D * D * 2,
+    return {"qk": qk, "k": qk // 2, "v": vh, "gb": gb, "o": vh, "dO": vh, "states": NC * HV * D * D * 2,
             "dqdk": qk, "dv": vh, "dgdb": gb}
 
 
@@ -94,6 +95,7 @@ KERNEL_METHOD_TENSORS = {
     "bwd_scan_kernel": ("qk", "dO"),
     "bwd_walk_kernel": ("qk", "v", "gb", "dO", "states"),
     "grad_kernel": ("qk", "v", "gb", "dO", "states", "dqdk", "dv", "dgdb"),
+    "vnew_kernel": ("k", "v", "states"),
 }
 
 
@@ -285,6 +287,11 @@ def run_ours(args, rank, world, local_rank):
         if op == "ckpt":
             gdn.gdn_ckpt_fwd_bwd(prob, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_dev, w.cu_seqlens,
                                  xx["dO"], o, dq, dk, dv, dg, db, buf.saved, buf.workspace, stream=stream)
+        if op == "fwd+bwd replay form":   # the replay saved form: states only, the backward recomputes
+            gdn.gdn_fwd(prob_r, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_dev, w.cu_seqlens, o,
+                        buf_r.saved, buf_r.workspace, stream=stream)
+            gdn.gdn_bwd(prob_r, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_dev, w.cu_seqlens, xx["dO"],
+                        buf_r.saved, dq, dk, dv, dg, db, buf_r.workspace, stream=stream)
         if op == "fwd+bwd with states":   # per-document S_in in, S_out out; dS_out in, dS_in out
             gdn.gdn_fwd_states(prob, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_dev, w.cu_seqlens,
                                bnd["s_in"], o, bnd["s_out"], buf.saved, buf.workspace, stream=stream)
@@ -293,6 +300,8 @@ def run_ours(args, rank, world, local_rank):
                                buf.workspace, stream=stream)
 
     bnd = {}
+    prob_r = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm, w.segments, saved_form=gdn.SAVED_REPLAY)
+    buf_r = gdn.Buffers(prob_r, w.cu_seqlens, device=dev) if not args.quick else None
 
     def time_workload(idx, K, W):
         """fwd + bwd of workload `idx` on its own inputs and buffers (freed afterwards)."""
@@ -373,12 +382,24 @@ def run_ours(args, rank, world, local_rank):
     if not args.quick:
         bnd.update({n: 0.1 * torch.randn((w.N, w.HV, D, D), device=dev) for n in ("s_in", "ds_out")})
         bnd.update({n: torch.empty((w.N, w.HV, D, D), device=dev) for n in ("s_out", "ds_in")})
-        for other in ("fwd", "ckpt", "fwd+bwd with states"):
+        for other in ("fwd", "ckpt", "fwd+bwd with states", "fwd+bwd replay form"):
             if other != op:
+                if other == "fwd+bwd replay form":
+                    gdn.gdn_profile_read_all()
+                    gdn.gdn_profile_enable(1)
                 t_o = timed(other, max(3, args.steps // 2), 2)
-                fl = step_flops(w, "fwd+bwd" if other == "fwd+bwd with states" else other)
+                fl = step_flops(w, "fwd+bwd" if other.startswith("fwd+bwd") else other)
                 extra[other] = {"ms": round(t_o, 4), "Mtokens_per_s": round(replica_rate(world, w.T, t_o), 3),
                                 "TFLOP_per_s": round(world * fl / t_o / 1e9, 1)}
+                if other == "fwd+bwd replay form":
+                    gdn.gdn_profile_enable(0)
+                    ks = gdn.gdn_profile_read_all()
+                    n_st = max(3, args.steps // 2) + 2
+                    extra[other].update({
+                        "saved_bytes_per_token": round(buf_r.saved_bytes / w.T, 1),
+                        "full_form_saved_bytes_per_token": round(buf.saved_bytes / w.T, 1),
+                        "kernels_ms_per_step": {k: round(v["total_ms"] / n_st, 4) for k, v in ks.items()
+                                                if v["timed_launches"]}})
         # the short causal conv1d + SiLU front over the workload's packed q/k/v channels (4 taps),
         # timed alone: fwd reads x and writes y, bwd reads x and dy and writes dx (BF16 [T, C])
         C_qkv = (2 * w.H + w.HV) * D

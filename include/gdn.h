@@ -73,7 +73,18 @@ typedef struct {
     int32_t segments; /* 0: the planner chooses the segment split;
                          > 0: split the longest document into `segments`
                          segments (see gdn_plan_segment_chunks()) */
+    int32_t saved_form; /* what the forward keeps for the backward:
+                           GDN_SAVED_FULL (0): the state tape plus the per-chunk
+                             UT blocks and V_new (the backward recomputes nothing);
+                           GDN_SAVED_REPLAY (1): the state tape only; the backward
+                             runs the UT / WY preparation again and recomputes
+                             V_new = U - W S from the saved states (the pages'
+                             replay form, "#8542" page, save-set table).
+                           Both give the same bits; see gdn_saved_bytes(). */
 } gdn_problem;
+
+#define GDN_SAVED_FULL 0
+#define GDN_SAVED_REPLAY 1
 
 typedef enum {
     GDN_OK = 0,
@@ -95,13 +106,16 @@ typedef enum {
  *                    document is split into P > 1 segments, the FP32 segment
  *                    transfer plane M_seg ((P-1) x HV x 64 KiB per document)
  *                    that the backward's merges read ("#8542" page: the full
- *                    saved set keeps M_seg at P > 1), and the per-chunk UT
- *                    blocks (T = (I + A)^-1 with its scaled forms and the gated
- *                    Aqk rows, 33 KiB per chunk and value head) and the BF16
- *                    V_new^T = (U - W S)^T of every chunk (16 KiB per chunk
- *                    and value head; the pages' v_new rows), so that the
- *                    backward does not recompute them.
- *   workspace_bytes  scratch for one gdn_fwd / gdn_bwd / gdn_ckpt_fwd_bwd call.
+ *                    saved set keeps M_seg at P > 1).  In the full form
+ *                    (prob->saved_form == GDN_SAVED_FULL) it also keeps the
+ *                    per-chunk UT blocks (T = (I + A)^-1 with its scaled forms
+ *                    and the gated Aqk rows, 33 KiB per chunk and value head)
+ *                    and the BF16 V_new^T = (U - W S)^T of every chunk (16 KiB
+ *                    per chunk and value head; the pages' v_new rows); the
+ *                    replay form (GDN_SAVED_REPLAY) keeps neither and the
+ *                    backward recomputes them.
+ *   workspace_bytes  scratch for one gdn_fwd / gdn_bwd / gdn_ckpt_fwd_bwd call
+ *                    (in the replay form it also holds the recomputed blocks).
  * Returns GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED on a bad problem.
  */
 gdn_status gdn_saved_bytes(const gdn_problem *prob, const int32_t *cu_seqlens_host,
@@ -230,6 +244,20 @@ gdn_status gdn_device_status(void *workspace, struct CUstream_st *stream);
  */
 gdn_status gdn_chunk_table_offsets(const gdn_problem *prob, const int32_t *cu_seqlens_host,
                                    size_t offsets[4], int32_t *num_chunks);
+
+/*
+ * Introspection for tests and tools: byte offsets, into the workspace, of the
+ * intermediate tapes a gdn_bwd() call leaves there (each [NC][HV] blocks):
+ *   offsets[0] UT blocks, 33,792 B each (T' at 0, T'' at 8 KiB, Aqk at 16 KiB,
+ *              T at 24 KiB: BF16 64 x 64 tiles in the kernels' swizzled tile
+ *              layout; then 1 KiB of per-token scalars)      (replay form; else 0)
+ *   offsets[1] V_new^T tiles, 16 KiB each (BF16 128 x 64)   (replay form; else 0)
+ *   offsets[2] dS' tiles, 32 KiB each (BF16 128 x 128 dS'^T: the gradient of
+ *              the state leaving each chunk)
+ *   offsets[3] dV_new^T tiles, 16 KiB each (BF16 128 x 64)
+ */
+gdn_status gdn_backward_tape_offsets(const gdn_problem *prob, const int32_t *cu_seqlens_host,
+                                     size_t offsets[4]);
 
 /*
  * Forward for callers that cannot allocate device memory.  The pages have no

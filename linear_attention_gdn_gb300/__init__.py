@@ -22,7 +22,8 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "G
 EXPORTS = ("gdn_saved_bytes", "gdn_fwd", "gdn_bwd", "gdn_ckpt_fwd_bwd", "gdn_status_string",
            "gdn_device_status", "gdn_plan_segment_chunks", "gdn_chunk_table_offsets", "gdn_profile_enable",
            "gdn_profile_read", "gdn_fwd_noalloc", "gdn_fwd_states", "gdn_bwd_states", "gdn_conv1d_workspace_bytes",
-           "gdn_conv1d_fwd", "gdn_conv1d_bwd")
+           "gdn_conv1d_fwd", "gdn_conv1d_bwd", "gdn_backward_tape_offsets")
+SAVED_FULL, SAVED_REPLAY = 0, 1   # gdn_problem.saved_form
 
 
 class GDNError(RuntimeError):
@@ -39,7 +40,7 @@ class gdn_kernel_stat(ctypes.Structure):
 class gdn_problem(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("N", ctypes.c_int32), ("H", ctypes.c_int32), ("HV", ctypes.c_int32),
                 ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("scale", ctypes.c_float),
-                ("l2norm", ctypes.c_int32), ("segments", ctypes.c_int32)]
+                ("l2norm", ctypes.c_int32), ("segments", ctypes.c_int32), ("saved_form", ctypes.c_int32)]
 
 
 class gdn_conv_problem(ctypes.Structure):
@@ -50,9 +51,10 @@ def conv_problem(T, N, C, W=4) -> gdn_conv_problem:
     return gdn_conv_problem(int(T), int(N), int(C), int(W))
 
 
-def problem(T, N, H, HV, scale=128 ** -0.5, l2norm=True, segments=0, dk=128, dv=128) -> gdn_problem:
+def problem(T, N, H, HV, scale=128 ** -0.5, l2norm=True, segments=0, dk=128, dv=128,
+            saved_form=SAVED_FULL) -> gdn_problem:
     return gdn_problem(int(T), int(N), int(H), int(HV), int(dk), int(dv), float(scale), int(bool(l2norm)),
-                       int(segments))
+                       int(segments), int(saved_form))
 
 
 def _load():
@@ -73,6 +75,7 @@ def _load():
     L.gdn_plan_segment_chunks.argtypes = [pp, i32p]
     L.gdn_plan_segment_chunks.restype = ctypes.c_int32
     L.gdn_chunk_table_offsets.argtypes = [pp, i32p, ctypes.POINTER(sz), i32p]
+    L.gdn_backward_tape_offsets.argtypes = [pp, i32p, ctypes.POINTER(sz)]
     L.gdn_fwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, i32p, i32p, vp, vp]
     L.gdn_fwd_noalloc.restype = ctypes.c_int
     cp = ctypes.POINTER(gdn_conv_problem)
@@ -87,7 +90,7 @@ def _load():
     L.gdn_profile_read.argtypes = [ctypes.POINTER(gdn_kernel_stat), ctypes.c_int]
     L.gdn_profile_read.restype = ctypes.c_int
     for name in ("gdn_saved_bytes", "gdn_fwd", "gdn_bwd", "gdn_ckpt_fwd_bwd", "gdn_device_status",
-                 "gdn_chunk_table_offsets"):
+                 "gdn_chunk_table_offsets", "gdn_backward_tape_offsets"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -163,6 +166,15 @@ def gdn_chunk_table_offsets(prob: gdn_problem, cu_seqlens_host):
     nc = ctypes.c_int32(0)
     _check(lib.gdn_chunk_table_offsets(ctypes.byref(prob), cup, offs, ctypes.byref(nc)), "gdn_chunk_table_offsets")
     return list(offs), nc.value
+
+
+def gdn_backward_tape_offsets(prob: gdn_problem, cu_seqlens_host):
+    """Workspace byte offsets of the UT blocks, V_new^T, dS' and dV_new^T tapes a gdn_bwd call leaves
+    (the first two only in the replay saved form); see include/gdn.h."""
+    cu, cup = _cu_host(cu_seqlens_host)
+    offs = (ctypes.c_size_t * 4)()
+    _check(lib.gdn_backward_tape_offsets(ctypes.byref(prob), cup, offs), "gdn_backward_tape_offsets")
+    return list(offs)
 
 
 def gdn_fwd(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, o, saved, workspace, ws_bytes=None,

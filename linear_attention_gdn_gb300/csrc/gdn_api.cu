@@ -23,6 +23,7 @@ void launch_merge(const MergeArgs& a, int nsdoc, cudaStream_t s);
 void setup_fwd_scan_attrs();
 void setup_bwd_attrs();
 void setup_prep_attrs();
+void setup_vnew_attrs();
 gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const void* k, const void* v,
                    const float* g, const float* beta, const int32_t* cu_dev, const void* dO, const void* saved,
                    void* dq, void* dk, void* dv, float* dg, float* dbeta, const float* ds_out, float* ds_in,
@@ -55,6 +56,7 @@ static gdn_status validate_problem(const gdn_problem* p, const int32_t* cu) {
   if (p->HV % p->H != 0) return GDN_ERR_UNSUPPORTED;
   if (p->T > (int64_t)INT32_MAX / 2) return GDN_ERR_UNSUPPORTED;
   if (p->segments < 0) return GDN_ERR_INVALID_ARG;
+  if (p->saved_form != GDN_SAVED_FULL && p->saved_form != GDN_SAVED_REPLAY) return GDN_ERR_INVALID_ARG;
   if (cu[0] != 0) return GDN_ERR_INVALID_ARG;
   for (int i = 0; i < p->N; ++i)
     if (cu[i + 1] < cu[i]) return GDN_ERR_INVALID_ARG;
@@ -103,6 +105,7 @@ static gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
   P->H = p->H;
   P->HV = p->HV;
   P->G = p->HV / p->H;
+  P->form = p->saved_form;
   P->sms = sm_count();
   plan_segments(p, cu, &P->seg_len, &P->split_min, &P->max_doc_chunks);
   int NC = 0, NSEG = 0, nsplit = 0, nsdoc = 0, n_empty = 0;
@@ -134,6 +137,7 @@ static gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
     off = align_up(off + (size_t)counts[i] * 4, 256);
   }
   off = align_up(off, 1024);
+  // the UT blocks of a forward without a full saved set, and of a replay-form backward
   P->o_cb = off;
   off += (size_t)NC * P->HV * CB_BYTES;
   const size_t st_f32 = (size_t)nsplit * P->HV * STATE_F32 * 4;
@@ -152,13 +156,23 @@ static gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
   off += st_f32;
   P->o_dsinit = off;
   off += st_f32;
+  P->o_vnb = 0;
+  if (P->form == GDN_SAVED_REPLAY) {
+    P->o_vnb = off;
+    off += (size_t)NC * P->HV * VN_BYTES;
+  }
   P->ws_bwd = off;
-  // saved set
+  // saved set: header, state tape, M_seg; the full form adds the UT blocks and V_new^T
   P->s_tape = SAVED_HEADER;
   P->s_mseg = P->s_tape + (size_t)NC * P->HV * STATE_BYTES;
   P->s_cb = align_up(P->s_mseg + st_f32, 1024);
-  P->s_vn = P->s_cb + (size_t)NC * P->HV * CB_BYTES;
-  P->saved_bytes = P->s_vn + (size_t)NC * P->HV * VN_BYTES;
+  if (P->form == GDN_SAVED_FULL) {
+    P->s_vn = P->s_cb + (size_t)NC * P->HV * CB_BYTES;
+    P->saved_bytes = P->s_vn + (size_t)NC * P->HV * VN_BYTES;
+  } else {
+    P->s_vn = P->s_cb;
+    P->saved_bytes = P->s_cb;
+  }
   return GDN_OK;
 }
 
@@ -181,6 +195,7 @@ static SavedHeader header_of(const Plan& P, const gdn_problem* p) {
   h.seg_len = P.seg_len;
   memcpy(&h.scale_bits, &p->scale, 4);
   h.cu_hash = P.cu_hash;
+  h.form = P.form;
   return h;
 }
 
@@ -225,6 +240,7 @@ static bool device_setup() {
     setup_fwd_scan_attrs();
     setup_bwd_attrs();
     setup_prep_attrs();
+    setup_vnew_attrs();
     done[dev] = true;
   }
   return true;
@@ -238,7 +254,7 @@ static const char* const kKernelNames[K_NUM] = {
     "tables_scan_kernel", "tables_fill_kernel", "prep_kernel",    "fwd_scan_kernel(walk)",
     "merge_kernel",       "fwd_scan_kernel",    "check_saved_kernel", "bwd_scan_kernel(walk)",
     "merge_bwd_kernel",   "bwd_scan_kernel",    "grad_kernel",        "passthrough_kernel",
-    "conv_fwd_kernel",    "conv_bwd_kernel(+reduce)"};
+    "conv_fwd_kernel",    "conv_bwd_kernel(+reduce)", "vnew_kernel"};
 struct ProfRec {
   int id;
   cudaEvent_t e0, e1;
@@ -342,9 +358,11 @@ static gdn_status run_fwd(const Plan& P, const gdn_problem* p, const void* q, co
     launch_passthrough(pa, P.N, s);
   }
   if (P.NC == 0) return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
-  // with a saved set, the per-chunk UT blocks (with T) go into it for the backward
-  uint8_t* cb = saved ? static_cast<uint8_t*>(saved) + P.s_cb : ws + P.o_cb;
-  st = run_prep(P, p, q, k, g, beta, ws, cb, saved ? 1 : 0, s);
+  // with a full-form saved set, the per-chunk UT blocks (with T) go into it for the backward; else
+  // they are the walk's scratch in the workspace
+  const bool full = saved && P.form == GDN_SAVED_FULL;
+  uint8_t* cb = full ? static_cast<uint8_t*>(saved) + P.s_cb : ws + P.o_cb;
+  st = run_prep(P, p, q, k, g, beta, ws, cb, full ? 1 : 0, s);
   if (st != GDN_OK) return st;
   Tables t = tables_at(P, ws);
   ScanArgs sa;
@@ -387,7 +405,7 @@ static gdn_status run_fwd(const Plan& P, const gdn_problem* p, const void* q, co
   }
   sa.walk = 0;
   sa.tape = saved ? static_cast<uint8_t*>(saved) + P.s_tape : nullptr;
-  sa.vn = saved ? static_cast<uint8_t*>(saved) + P.s_vn : nullptr;
+  sa.vn = full ? static_cast<uint8_t*>(saved) + P.s_vn : nullptr;
   sa.o = static_cast<__nv_bfloat16*>(o);
   if (o && !make_tmap(&sa.to, o, P.T, P.HV)) return GDN_ERR_CUDA;
   launch_fwd_scan(sa, P.NSEG * P.HV, s);
@@ -522,6 +540,19 @@ gdn_status gdn_chunk_table_offsets(const gdn_problem* prob, const int32_t* cu_ho
   return GDN_OK;
 }
 
+
+gdn_status gdn_backward_tape_offsets(const gdn_problem* prob, const int32_t* cu_host, size_t offsets[4]) {
+  Plan P;
+  gdn_status st = make_plan(prob, cu_host, &P);
+  if (st != GDN_OK) return st;
+  if (!offsets) return GDN_ERR_INVALID_ARG;
+  const bool replay = P.form == GDN_SAVED_REPLAY;
+  offsets[0] = replay ? P.o_cb : 0;
+  offsets[1] = replay ? P.o_vnb : 0;
+  offsets[2] = P.o_dtape;
+  offsets[3] = P.o_dvn;
+  return GDN_OK;
+}
 
 void gdn_profile_enable(int on) {
   std::lock_guard<std::mutex> lk(g_prof_mu);

@@ -37,6 +37,7 @@ gdn_status run_tables(const Plan& P, const gdn_problem* p, const int32_t* cu_dev
 void launch_passthrough(const PassArgs& a, int N, cudaStream_t s);
 gdn_status run_prep(const Plan& P, const gdn_problem* p, const void* q, const void* k, const float* g,
                     const float* beta, uint8_t* ws, uint8_t* cb, int write_T, cudaStream_t s);
+void launch_vnew(const VnewArgs& a, int NC, cudaStream_t s);
 
 struct BScanArgs {
   CUtensorMap tq, tk, tdo;
@@ -460,7 +461,7 @@ __global__ void check_saved_kernel(CheckArgs a) {
   if (h->magic != e.magic || h->version != e.version || h->T != e.T || h->N != e.N || h->H != e.H ||
       h->HV != e.HV || h->dk != e.dk || h->dv != e.dv || h->l2norm != e.l2norm || h->NC != e.NC ||
       h->NSEG != e.NSEG || h->nsplit != e.nsplit || h->seg_len != e.seg_len || h->scale_bits != e.scale_bits ||
-      h->cu_hash != e.cu_hash)
+      h->cu_hash != e.cu_hash || h->form != e.form)
     atomicCAS(a.err, 0, ST_SAVED_MISMATCH);
 }
 
@@ -1432,6 +1433,7 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
     h.seg_len = P.seg_len;
     memcpy(&h.scale_bits, &pr.scale, 4);
     h.cu_hash = P.cu_hash;
+    h.form = P.form;
     ca.expect = h;
     ca.err = reinterpret_cast<int*>(ws);
     prof_begin(K_CHECK_SAVED, s);
@@ -1439,14 +1441,37 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
     prof_end(K_CHECK_SAVED, s);
   }
   if (P.NC == 0) return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
-  // the per-chunk UT blocks come from the saved set (written by the forward)
   Tables t = tables_at(P, ws);
   const uint8_t* sv = static_cast<const uint8_t*>(saved);
+  // The per-chunk UT blocks and V_new^T tiles: read from a full-form saved set; recomputed into the
+  // workspace for the replay form (the UT / WY preparation again, then V_new = U - W S from the
+  // saved states)
+  const uint8_t* cb = sv + P.s_cb;
+  const uint8_t* vn = sv + P.s_vn;
+  if (P.form == GDN_SAVED_REPLAY) {
+    gdn_status st2 = run_prep(P, &pr, q, k, g, beta, ws, ws + P.o_cb, 1, s);
+    if (st2 != GDN_OK) return st2;
+    VnewArgs va;
+    memset(&va, 0, sizeof(va));
+    if (!make_tmap(&va.tk, k, P.T, P.H) || !make_tmap(&va.tv, v, P.T, P.HV)) return GDN_ERR_CUDA;
+    va.tape = sv + P.s_tape;
+    va.cb = ws + P.o_cb;
+    va.chunk_tok0 = t.chunk_tok0;
+    va.chunk_len = t.chunk_len;
+    va.vn = ws + P.o_vnb;
+    va.H = P.H;
+    va.HV = P.HV;
+    va.G = P.G;
+    va.err = reinterpret_cast<int*>(ws);
+    launch_vnew(va, P.NC, s);
+    cb = ws + P.o_cb;
+    vn = ws + P.o_vnb;
+  }
   BScanArgs ba;
   memset(&ba, 0, sizeof(ba));
   if (!make_tmap(&ba.tq, q, P.T, P.H) || !make_tmap(&ba.tk, k, P.T, P.H) || !make_tmap(&ba.tdo, dO, P.T, P.HV))
     return GDN_ERR_CUDA;
-  ba.cb = sv + P.s_cb;
+  ba.cb = cb;
   ba.chunk_tok0 = t.chunk_tok0;
   ba.seg_c0 = t.seg_c0;
   ba.seg_c1 = t.seg_c1;
@@ -1499,10 +1524,10 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
   ga.k = static_cast<const __nv_bfloat16*>(k);
   ga.g = g;
   ga.beta = beta;
-  ga.cb = sv + P.s_cb;
+  ga.cb = cb;
   ga.tape = sv + P.s_tape;
   ga.dtape = ws + P.o_dtape;
-  ga.vn = sv + P.s_vn;
+  ga.vn = vn;
   ga.dvn = ws + P.o_dvn;
   ga.chunk_tok0 = t.chunk_tok0;
   ga.chunk_len = t.chunk_len;

@@ -36,9 +36,10 @@ struct SavedHeader {
   int32_t N, H, HV, dk, dv, l2norm;
   int32_t NC, NSEG, nsplit, seg_len;
   uint32_t scale_bits, cu_hash;
+  int32_t form, pad;   // saved form (0 full, 1 replay)
 };
 constexpr uint32_t SAVED_MAGIC = 0x4744'4e31u;   // "GDN1"
-constexpr uint32_t SAVED_VERSION = 3;
+constexpr uint32_t SAVED_VERSION = 4;
 
 // ---- device tables built by the table kernel ----
 struct Tables {
@@ -124,6 +125,18 @@ struct ScanArgs {
   int* err;
 };
 
+// V_new^T of every (chunk, value head) from the saved states (replay form)
+struct VnewArgs {
+  CUtensorMap tk, tv;
+  const uint8_t* tape;        // [NC][HV][STATE_BYTES] saved S^T
+  const uint8_t* cb;          // [NC][HV][CB_BYTES] UT blocks of this call
+  const int* chunk_tok0;
+  const int* chunk_len;
+  uint8_t* vn;                // [NC][HV][VN_BYTES] out
+  int H, HV, G;
+  int* err;
+};
+
 // boundary states of documents without chunks: dst[d] = src[d] (zero if src is null)
 struct PassArgs {
   const int* chunk_offsets;   // [N+1]
@@ -147,12 +160,14 @@ struct Plan {
   int N, H, HV, G;
   int NC, NSEG, nsplit, nsdoc, seg_len, split_min, max_doc_chunks;
   int n_empty;   // documents without tokens
+  int form;      // saved form: 0 full (UT blocks and V_new^T saved), 1 replay (the backward recomputes them)
   int sms;   // SMs of the current device (persistent grids)
   uint32_t cu_hash;
   // workspace offsets (bytes)
   size_t o_tables[14];
   size_t o_cb, o_bend, o_sinit, o_mend_ws;
   size_t o_dtape, o_dvn, o_dbend, o_dsinit;   // backward
+  size_t o_vnb;                               // backward, replay form: recomputed V_new^T tiles
   size_t ws_fwd, ws_bwd;
   // saved offsets
   size_t s_tape, s_mseg, s_cb, s_vn, saved_bytes;

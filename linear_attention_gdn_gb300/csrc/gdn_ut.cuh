@@ -30,6 +30,8 @@
 // holds sc_r = scale gamma_r rq_r [64], kd_r = e^{G_L - G_r} rk_r [64],
 // e^{G_L} and L (as an int), 1 KB.
 #pragma once
+#include <stddef.h>
+
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -41,8 +43,8 @@ constexpr int UT_WORK_BYTES = 64 * UT_ALD * 4;   // 17,408: the FP32 array; T' t
 constexpr int UT_SCAL_BYTES = 1024;
 static_assert(2 * 8192 <= UT_WORK_BYTES, "T' and T'' fit in the FP32 array's space");
 
-// per-token factors of one chunk, shared by the warpgroup
-struct UtTok {
+// per-token factors of one chunk, shared by the warpgroup (16-byte aligned: read as float4)
+struct __align__(16) UtTok {
   float rq[64], rk[64];
   float Gs[64], bs[64], eGr[64], eGi[64];
   float cf[64];     // rk_c e^{G_0 - G_c}: the column factor of A and Aqk
@@ -50,6 +52,8 @@ struct UtTok {
   float pcol[64];   // beta_c e^{G_c} rk_c: the column factor of T'
   int safe;
 };
+static_assert(alignof(UtTok) >= 16 && offsetof(UtTok, ca) % 16 == 0 && offsetof(UtTok, cf) % 16 == 0,
+              "UtTok members are read as float4");
 
 // Zero the rows L..63 of the [K; Q] tile (they hold the next document's tokens).
 __device__ __forceinline__ void ut_zero_tail(uint8_t* kq, int L, int lt) {

@@ -46,6 +46,34 @@ def test_saved_and_workspace_bytes():
     assert saved == 4096 + 40 * 2 * 32768 + 3 * 2 * 128 * 128 * 4 + 40 * 2 * 33792 + 40 * 2 * 16384
 
 
+def test_replay_form_saved_bytes():
+    # the replay form keeps the header and the BF16 state tape (plus M_seg when a document is split)
+    p = gdn.problem(320, 2, 2, 4, saved_form=gdn.SAVED_REPLAY)
+    saved, ws = gdn.gdn_saved_bytes(p, [0, 128, 320])
+    assert saved == 4096 + 5 * 4 * 32768
+    full_saved, full_ws = gdn.gdn_saved_bytes(gdn.problem(320, 2, 2, 4), [0, 128, 320])
+    assert full_saved - saved == 5 * 4 * (33792 + 16384)
+    assert ws - full_ws == 5 * 4 * 16384   # the recomputed V_new^T tiles
+    p = gdn.problem(64 * 40, 1, 1, 2, segments=4, saved_form=gdn.SAVED_REPLAY)
+    saved, _ = gdn.gdn_saved_bytes(p, [0, 64 * 40])
+    assert saved == 4096 + 40 * 2 * 32768 + 3 * 2 * 128 * 128 * 4
+    # at the 4-document bench workload: 24 KiB of states per token, under 30 KB
+    w = [0, 98304, 163840, 221184, 262144]
+    saved, _ = gdn.gdn_saved_bytes(gdn.problem(262144, 4, 16, 48, saved_form=gdn.SAVED_REPLAY), w)
+    assert saved / 262144 < 30e3
+    offs = gdn.gdn_backward_tape_offsets(gdn.problem(320, 2, 2, 4, saved_form=gdn.SAVED_REPLAY), [0, 128, 320])
+    assert all(o > 0 and o % 1024 == 0 for o in offs)
+    offs = gdn.gdn_backward_tape_offsets(gdn.problem(320, 2, 2, 4), [0, 128, 320])
+    assert offs[0] == 0 and offs[1] == 0 and offs[2] > 0 and offs[3] > 0
+
+
+def test_bad_saved_form_refused():
+    p = gdn.problem(320, 2, 2, 4, saved_form=2)
+    with pytest.raises(gdn.GDNError) as e:
+        gdn.gdn_saved_bytes(p, [0, 128, 320])
+    assert e.value.status == 1
+
+
 @pytest.mark.parametrize("cu,T,N,H,HV,dk,code", [
     ([0, 10, 5], 5, 2, 1, 1, 128, 1),      # decreasing cu_seqlens
     ([1, 10], 9, 1, 1, 1, 128, 1),         # cu[0] != 0
