@@ -269,7 +269,8 @@ def run_ours(args, rank, world, local_rank):
     w = inputs.workload(args.workload)
     x = inputs.generate(w, dev)
     cu_dev = torch.from_numpy(w.cu_seqlens).to(dev)
-    prob = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm, w.segments)
+    form = gdn.SAVED_REPLAY if args.form == "replay" else gdn.SAVED_FULL
+    prob = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm, w.segments, saved_form=form)
     buf = gdn.Buffers(prob, w.cu_seqlens, device=dev)
     stream = torch.cuda.current_stream(dev)
     o = torch.empty((w.T, w.HV, D), dtype=torch.bfloat16, device=dev)
@@ -527,7 +528,7 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "tokens": w.T, "docs": w.doc_lens, "H": w.H, "HV": w.HV, "dk": D,
-                   "dv": D, "chunk": C, "l2norm": w.l2norm, "op": op,
+                   "dv": D, "chunk": C, "l2norm": w.l2norm, "op": op, "saved_form": args.form,
                    "l2_flush": f"none needed: {in_gb:.1f} GB of inputs per step exceed the 129 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "tflops": round(tflops, 1), "tensor_frac_of_step": round(tflops / pk["bf16_tflops_sustained"], 4),
@@ -624,6 +625,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--op", default="fwd+bwd", choices=("fwd", "fwd+bwd", "ckpt"))
+    ap.add_argument("--form", default="full", choices=("full", "replay"),
+                    help="saved form of the timed step (the other one is timed in ops)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the extra fwd / ckpt timings")

@@ -22,6 +22,8 @@
 //   grad_kernel       per (chunk, q/k head): everything chunk-local, summing
 //                     dq^, dk^ over the group's value heads, then the L2-norm
 //                     backward
+#include <stdlib.h>
+
 #include "gdn.h"
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
@@ -1463,6 +1465,10 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
     va.HV = P.HV;
     va.G = P.G;
     va.err = reinterpret_cast<int*>(ws);
+    // Test hook for the device-side timeout path: with GDN_TEST_WITHHOLD_LOAD set in the environment,
+    // one CTA of this kernel never requests its first tiles; its bounded wait gives up after about a
+    // second, records GDN_ERR_TIMEOUT and returns, and every later kernel of the call skips its work.
+    va.withhold_first_load = getenv("GDN_TEST_WITHHOLD_LOAD") != nullptr;
     launch_vnew(va, P.NC, s);
     cb = ws + P.o_cb;
     vn = ws + P.o_vnb;

@@ -263,6 +263,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   }
 }
 
+// Wait up to ~1 s for phase `parity` of `bar`, whatever the error word says: on an
+// error path, lets copies this CTA already has in flight land before it exits.
+// Returns whether the phase completed.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
+  uint32_t done = 0;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 0;; ++it) {
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity));
+    if (done) return true;
+    if ((it & 1023) == 1023 && globaltimer() - t0 > 1000000000ull) return false;
+  }
+}
+
 // ----------------------------------------------------------------------------
 // TMA and bulk copies (completion counted on an mbarrier)
 // ----------------------------------------------------------------------------

@@ -134,6 +134,8 @@ struct VnewArgs {
   const int* chunk_len;
   uint8_t* vn;                // [NC][HV][VN_BYTES] out
   int H, HV, G;
+  int withhold_first_load;    // test hook: CTA 0 never requests its first tiles, so its bounded wait
+                              // runs out and the call reports GDN_ERR_TIMEOUT (nothing is left in flight)
   int* err;
 };
 

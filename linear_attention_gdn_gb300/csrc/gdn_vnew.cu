@@ -58,7 +58,13 @@ __global__ void __launch_bounds__(VW_THREADS, 2) vnew_kernel(const __grid_consta
     mbar_expect_tx(&bar_k, 16384u);
     tma_load_3d(sm + VW_K, &a.tk, 0, j, tok0, &bar_k);
     tma_load_3d(sm + VW_K + 8192, &a.tk, 64, j, tok0, &bar_k);
+  }
+  // Thread 0 issues every tile request and (in warp 0) every MMA; for the error path it keeps the
+  // phase of a request or a commit whose completion has not been seen yet (-1: none).
+  int ld_par = -1, mma_par = -1;
+  if (tid == 0 && !(a.withhold_first_load && blockIdx.x == 0)) {
     issue_head(j * a.G);
+    ld_par = 0;
   }
   tc_fence_before();
   __syncthreads();
@@ -76,6 +82,7 @@ __global__ void __launch_bounds__(VW_THREADS, 2) vnew_kernel(const __grid_consta
     const int hv = j * a.G + hh;
     ok = __syncthreads_and(mbar_wait(&bar_ld, hh & 1, a.err));
     if (!ok) break;
+    ld_par = -1;
     if (L < CH) {   // zero the V rows past the document end
       for (int idx = tid; idx < (CH - L) * 16; idx += VW_THREADS)
         *reinterpret_cast<uint4*>(sm + VW_V + sw_chunk(L + (idx >> 4), idx & 15, 64)) = make_uint4(0u, 0u, 0u, 0u);
@@ -92,11 +99,13 @@ __global__ void __launch_bounds__(VW_THREADS, 2) vnew_kernel(const __grid_consta
       for (int ks = 0; ks < 4; ++ks)
         mma_ss_w(tb + VT_U, desc_mn(s_v, 64, ks), desc_k(s_tpp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
       mma_commit_w(&bar_mma);
+      mma_par = (int)mph;
     }
     if (tid == 0) bulk_wait_read();   // the previous head's V_new^T store has read the staging tile
     ok = __syncthreads_and(mbar_wait(&bar_mma, mph, a.err));
     mph ^= 1;
     if (!ok) break;
+    mma_par = -1;
     tc_fence_after();
     {  // -W^T -> shared (row tid = dk index), the MN-major B operand of the V_new MMA
       float w[64];
@@ -121,12 +130,17 @@ __global__ void __launch_bounds__(VW_THREADS, 2) vnew_kernel(const __grid_consta
       for (int ks = 0; ks < 8; ++ks)
         mma_ss_w(tb + VT_U, desc_k(s_s, 128, ks), desc_mn(s_w, 128, ks), idesc(128, 64, 0, 1), 1u);
       mma_commit_w(&bar_mma);
+      mma_par = (int)mph;
     }
     ok = __syncthreads_and(mbar_wait(&bar_mma, mph, a.err));
     mph ^= 1;
     if (!ok) break;
+    mma_par = -1;
     tc_fence_after();
-    if (tid == 0 && hh + 1 < a.G) issue_head(hv + 1);   // S^T, V, T' T'' of this head are dead
+    if (tid == 0 && hh + 1 < a.G) {   // S^T, V, T' T'' of this head are dead
+      issue_head(hv + 1);
+      ld_par = (hh + 1) & 1;
+    }
     {  // V_new^T row tid -> BF16 staging tile (over -W^T, which the finished MMA no longer reads)
       float x[64];
       tmem_ld32(taddr(tb, warp * 32, VT_U), x);
@@ -150,7 +164,10 @@ __global__ void __launch_bounds__(VW_THREADS, 2) vnew_kernel(const __grid_consta
     }
   }
   if (tid == 0) bulk_wait_all();
-  if (!ok && tid == 0) mbar_wait(&bar_mma, mph, a.err);   // (bounded) no MMA outlives the allocation
+  if (!ok && tid == 0) {   // error path (bounded waits): no copy or MMA may outlive the CTA's memory
+    if (mma_par >= 0) mbar_drain(&bar_mma, (uint32_t)mma_par);
+    if (ld_par >= 0) mbar_drain(&bar_ld, (uint32_t)ld_par);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, 128);
