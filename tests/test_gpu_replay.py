@@ -143,3 +143,31 @@ def test_stage_parity_replay_intermediates(name, w):
     for k in got:
         compare(f"{name}/{k}", np.concatenate([a.ravel() for a in got[k]]),
                 np.concatenate([a.ravel() for a in ref[k]]))
+
+
+@pytest.mark.parametrize("idx", [3, 4])
+def test_replay_form_equals_full_form_full_size(idx):
+    """The full-size workloads: the 166-document pack with L2 off, and the 524,288-token document whose
+    walks are split into segments (its backward merges read the saved segment transfers in both
+    forms).  Every output and gradient agrees bit for bit between the saved forms."""
+    import linear_attention_gdn_gb300 as gdn
+    w = inputs.workload(idx)
+    x = inputs.generate(w, "cuda")
+    cu = torch.from_numpy(w.cu_seqlens).cuda()
+    res = {}
+    for form in (gdn.SAVED_FULL, gdn.SAVED_REPLAY):
+        prob = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm, w.segments, saved_form=form)
+        buf = gdn.Buffers(prob, w.cu_seqlens)
+        out = dict(o=torch.empty((w.T, w.HV, 128), dtype=torch.bfloat16, device="cuda"),
+                   dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]), dv=torch.empty_like(x["v"]),
+                   dg=torch.empty_like(x["g"]), dbeta=torch.empty_like(x["beta"]))
+        gdn.gdn_fwd(prob, x["q"], x["k"], x["v"], x["g"], x["beta"], cu, w.cu_seqlens, out["o"], buf.saved,
+                    buf.workspace)
+        gdn.gdn_bwd(prob, x["q"], x["k"], x["v"], x["g"], x["beta"], cu, w.cu_seqlens, x["dO"], buf.saved,
+                    out["dq"], out["dk"], out["dv"], out["dg"], out["dbeta"], buf.workspace)
+        assert gdn.gdn_device_status(buf.workspace) == 0
+        res[form] = out
+        del buf
+        torch.cuda.empty_cache()
+    for n in ("o",) + GRADS:
+        assert torch.equal(res[gdn.SAVED_FULL][n], res[gdn.SAVED_REPLAY][n]), f"workload{idx}/{n}"
