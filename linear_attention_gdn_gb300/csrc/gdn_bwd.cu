@@ -1314,6 +1314,9 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
 
     // ---- item end: the MMA-accumulated dq^T, dk^T; L2-norm backward of the group sums; dq, dk
     if (!(ok = mma_sync_wait())) break;   // M6 of the last value head
+    // the Q, K tiles are free (M6 was their last reader): the next item's are requested now, while
+    // dq^T / dk^T are read out; its KK^T / QK^T waits for go_kq below (they overwrite those columns)
+    if (tid == 0 && nxt < n_items) issue_qk(nxt / a.NC, nx_tok0);
     float xq[GK_CW], xk[GK_CW];           // dq^T, dk^T [row][cb0 + e] (before the L2-norm backward)
     {
       float pq[GK_CW], pk[GK_CW];
@@ -1330,11 +1333,8 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
       }
     }
     tc_fence_before();   // the TMEM reads of DQ / DK precede the next item's table MMAs
-    named_bar(GK_BAR, GK_THREADS);     // the Q, K tiles are free
-    if (tid == 0 && nxt < n_items) {
-      issue_qk(nxt / a.NC, nx_tok0);
-      mbar_arrive(&go_kq);
-    }
+    named_bar(GK_BAR, GK_THREADS);
+    if (tid == 0 && nxt < n_items) mbar_arrive(&go_kq);
     if (tid < CH) {      // d|x|/dx . g = (g - x (x . g) / |x|^2) / |x|: the per-token factor (x . g) / |x|^3
       float xq = 0.f, xk = 0.f;
 #pragma unroll
