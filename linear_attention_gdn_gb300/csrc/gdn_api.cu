@@ -70,7 +70,9 @@ static gdn_status validate_problem(const gdn_problem* p, const int32_t* cu) {
 // extra walks per split segment (B and M), so it pays only when the longest
 // chains would otherwise leave most SMs idle: the planner splits a document
 // of n chunks when n exceeds both 512 and three times the balanced per-SM
-// share of all chain steps, into segments of that share.
+// share of all chain steps, into P = ceil(n / share) segments of equal length
+// (the walks of one launch run in waves of one CTA per SM, so a short last
+// segment would leave its wave idle).
 static void plan_segments(const gdn_problem* p, const int32_t* cu, int* seg_len, int* split_min,
                           int* max_doc) {
   int64_t total = 0;
@@ -89,7 +91,8 @@ static void plan_segments(const gdn_problem* p, const int32_t* cu, int* seg_len,
   }
   const int64_t share = (total * p->HV + sm_count() - 1) / sm_count();
   if (mx > 512 && mx > 3 * share) {
-    *seg_len = (int)std::max<int64_t>(256, share);
+    const int64_t parts = (mx + share - 1) / share;
+    *seg_len = (int)std::max<int64_t>(256, (mx + parts - 1) / parts);
     *split_min = *seg_len;
   } else {
     *seg_len = std::max(mx, 1);
@@ -130,9 +133,9 @@ static gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
   P->cu_hash = h;
   // workspace
   size_t off = 256;   // control block (error word)
-  const int counts[14] = {P->N + 1, P->N + 1, P->N + 1, NC, NC, NC, NSEG, NSEG, NSEG, NSEG, NSEG, nsplit,
-                          nsdoc + 1, 0};
-  for (int i = 0; i < 14; ++i) {
+  const int counts[17] = {P->N + 1, P->N + 1, P->N + 1, NC, NC, NC, NSEG, NSEG, NSEG, NSEG, NSEG, nsplit,
+                          nsdoc + 1, P->N + 1, NSEG - nsdoc, NSEG - nsdoc, 0};
+  for (int i = 0; i < 17; ++i) {
     P->o_tables[i] = off;
     off = align_up(off + (size_t)counts[i] * 4, 256);
   }
@@ -377,6 +380,7 @@ static gdn_status run_fwd(const Plan& P, const gdn_problem* p, const void* q, co
   sa.seg_idx = t.seg_idx;
   sa.seg_split = t.seg_split;
   sa.split_seg = t.split_seg;
+  sa.walk_seg = t.fwalk_seg;
   sa.H = P.H;
   sa.HV = P.HV;
   sa.G = P.G;
@@ -391,6 +395,11 @@ static gdn_status run_fwd(const Plan& P, const gdn_problem* p, const void* q, co
   sa.s_in = s_in;
   sa.s_out = s_out;
   sa.err = reinterpret_cast<int*>(ws);
+  // (the first segment of a split document walks in full in the split launch: it writes o and the tape)
+  sa.tape = saved ? static_cast<uint8_t*>(saved) + P.s_tape : nullptr;
+  sa.vn = full ? static_cast<uint8_t*>(saved) + P.s_vn : nullptr;
+  sa.o = static_cast<__nv_bfloat16*>(o);
+  if (o && !make_tmap(&sa.to, o, P.T, P.HV)) return GDN_ERR_CUDA;
   if (P.nsplit > 0) {
     sa.walk = 1;
     launch_fwd_scan(sa, 2 * P.nsplit * P.HV, s);
@@ -404,11 +413,7 @@ static gdn_status run_fwd(const Plan& P, const gdn_problem* p, const void* q, co
     launch_merge(ma, P.nsdoc, s);
   }
   sa.walk = 0;
-  sa.tape = saved ? static_cast<uint8_t*>(saved) + P.s_tape : nullptr;
-  sa.vn = full ? static_cast<uint8_t*>(saved) + P.s_vn : nullptr;
-  sa.o = static_cast<__nv_bfloat16*>(o);
-  if (o && !make_tmap(&sa.to, o, P.T, P.HV)) return GDN_ERR_CUDA;
-  launch_fwd_scan(sa, P.NSEG * P.HV, s);
+  launch_fwd_scan(sa, (P.NSEG - P.nsdoc) * P.HV, s);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -18,6 +18,8 @@
 //   bwd_scan_kernel   reverse dS walk per (segment, value head); writes the
 //                     BF16 dS' tape (gradient leaving each chunk), or, in the
 //                     split's zero-start mode, the adjoint at a segment start
+//                     (a split document's last segment starts from its true end,
+//                     so there it is the full walk and writes the tape too)
 //   merge_bwd_kernel  dS_end(p) = dS_end(p+1) M_{p+1} + B'_{p+1} over segments
 //   grad_kernel       per (chunk, q/k head): everything chunk-local, summing
 //                     dq^, dk^ over the group's value heads, then the L2-norm
@@ -49,6 +51,7 @@ struct BScanArgs {
   const int* seg_c1;
   const int* seg_split;
   const int* split_seg;
+  const int* walk_seg;   // walk = 0: the segments to walk (one per CTA group of HV)
   int HV, G, nsplit, walk;
   float scale;
   uint8_t* dtape;        // [NC][HV][STATE_BYTES]
@@ -139,13 +142,17 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
   if (*(volatile int*)a.err) return;
 
   int seg, hv, split = -1;
+  bool full = true;   // writes the dS' tape and dV_new^T (and dS_in at a document start)
   if (!a.walk) {
-    seg = blockIdx.x / a.HV;
+    seg = a.walk_seg[blockIdx.x / a.HV];
     hv = blockIdx.x % a.HV;
   } else {  // zero-start reverse walk of the segment after split point `split`
     split = blockIdx.x / a.HV;
     hv = blockIdx.x % a.HV;
     seg = a.split_seg[split] + 1;
+    // the last segment of a document starts from its true end (zero, or dS_out): its zero-start walk
+    // is its full walk, which writes the tapes here and is not repeated after the merge
+    full = seg + 1 == a.seg_offsets[a.seg_doc[seg] + 1];
   }
   const int kh = hv / a.G;
   const int c0 = a.seg_c0[seg], nch = a.seg_c1[seg] - c0;
@@ -253,7 +260,7 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
     tc_fence_after();
     if (tid == 0) {
       // the dS'^T tile (written and fenced last iteration) is this chunk's tape entry
-      if (!a.walk) {
+      if (full) {
         bulk_store(a.dtape + ((size_t)ci * a.HV + hv) * STATE_BYTES, ds_tile, STATE_BYTES);
         bulk_commit();
       }
@@ -322,7 +329,7 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
             p8[e] = pack_bf16(fmaf(a.scale, x[j], kd[r] * y[j]), fmaf(a.scale, x[j + 1], kd[r + 1] * y[j + 1]));
           }
           tmem_st8(taddr(tb, warp * 32, BT_ADV + h * 16 + q * 8), p8);
-          if (!a.walk) {
+          if (full) {
             uint8_t* dvt = sm + BS_DV;
             const int c8 = h * 4 + q * 2;
             *reinterpret_cast<uint4*>(dvt + sw_chunk(tid, c8, 128)) = make_uint4(p8[0], p8[1], p8[2], p8[3]);
@@ -338,7 +345,7 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
     __syncthreads();
     tc_fence_after();
     if (tid == 0) {
-      if (!a.walk) {   // this chunk's dV_new^T for the gradient kernel
+      if (full) {   // this chunk's dV_new^T for the gradient kernel
         bulk_store(a.dvn + ((size_t)ci * a.HV + hv) * VN_BYTES, sm + BS_DV, VN_BYTES);
         bulk_commit();
       }
@@ -395,7 +402,7 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
     for (int jj = 0; jj < 128; jj += 4)
       *reinterpret_cast<float4*>(dst + jj) = make_float4(dS[jj], dS[jj + 1], dS[jj + 2], dS[jj + 3]);
   }
-  if (ok && !a.walk && a.ds_in && a.seg_idx[seg] == 0) {   // the adjoint entering the document: dS_in
+  if (ok && full && a.ds_in && a.seg_idx[seg] == 0) {   // the adjoint entering the document: dS_in
     float* dst = a.ds_in + ((size_t)doc * a.HV + hv) * STATE_F32 + tid;   // column tid of dS_in [dk][dv]
 #pragma unroll
     for (int jj = 0; jj < 128; ++jj) dst[jj * 128] = dS[jj];
@@ -1483,6 +1490,7 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
   ba.seg_c1 = t.seg_c1;
   ba.seg_split = t.seg_split;
   ba.split_seg = t.split_seg;
+  ba.walk_seg = t.bwalk_seg;
   ba.HV = P.HV;
   ba.G = P.G;
   ba.nsplit = P.nsplit;
@@ -1515,7 +1523,7 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
   }
   ba.walk = 0;
   prof_begin(K_BWD_SCAN, s);
-  bwd_scan_kernel<<<P.NSEG * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
+  bwd_scan_kernel<<<(P.NSEG - P.nsdoc) * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
   prof_end(K_BWD_SCAN, s);
 
   GradArgs ga;

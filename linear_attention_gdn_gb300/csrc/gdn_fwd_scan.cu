@@ -17,8 +17,12 @@
 //
 // Walk modes for the intra-GPU segment split ("#8542" page: segment transfers
 // M_seg and the merges that read them):
-//   full (walk = 0)  every segment, from its true start state; writes o, tape
-//   B    (walk = 1)  segment from a zero state; writes its end state B_p^T
+//   full (walk = 0)  every segment but a split document's first, from its true
+//                    start state (after the merge); writes o, tape
+//   B    (walk = 1)  segment from a zero state; writes its end state B_p^T.  The
+//                    first segment of a split document starts from its true
+//                    start (zero, or the document's S_in), so its B walk is its
+//                    full walk: it also writes o and the tape
 //   M    (walk = 2)  the segment after a split point, with U = 0 from S^T = I;
 //                    its end state is M^T, the transfer of that segment
 //                    (S_end = M S_start + B)
@@ -92,9 +96,10 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
   if (*(volatile int*)a.err) return;
 
   int mode, seg, hv, split = -1;
+  bool write_bend = false;
   if (!a.walk) {
     mode = 0;
-    seg = blockIdx.x / a.HV;
+    seg = a.walk_seg[blockIdx.x / a.HV];
     hv = blockIdx.x % a.HV;
   } else {
     const int half = a.nsplit * a.HV;
@@ -105,6 +110,10 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
     // B walks run on split segment p, M walks on segment p + 1: the merges
     // use M_1 .. M_{P-1} (M_0 only ever multiplies the zero start state)
     seg = a.split_seg[split] + (mode == 2 ? 1 : 0);
+    if (mode == 1 && a.seg_idx[seg] == 0) {   // a document's first segment: the full walk, plus B
+      mode = 0;
+      write_bend = true;
+    }
   }
   const int kh = hv / a.G;
   const int c0 = a.seg_c0[seg], nch = a.seg_c1[seg] - c0;
@@ -369,8 +378,8 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
       if (ok) output(nch - 1);
     }
     if (tid == 0 || tid == 32) bulk_wait_all();
-    if (ok && mode != 0) {
-      float* dst = (mode == 1 ? a.bend : a.mend) + ((size_t)split * a.HV + hv) * STATE_F32 + (size_t)lt * 128;
+    if (ok && (mode != 0 || write_bend)) {
+      float* dst = (mode == 2 ? a.mend : a.bend) + ((size_t)split * a.HV + hv) * STATE_F32 + (size_t)lt * 128;
 #pragma unroll
       for (int jj = 0; jj < 128; jj += 4)
         *reinterpret_cast<float4*>(dst + jj) = make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);

@@ -56,6 +56,12 @@ struct Tables {
   int* seg_split;      // [NSEG] index in the split list, or -1
   int* split_seg;      // [nsplit] segments that get transfer walks (p < P-1 of split docs)
   int* sdoc_first;     // [nsdoc+1] first split index of each split document
+  int* sdoc_offsets;   // [N+1]  split documents before each document, prefix sum
+  int* fwalk_seg;      // [NSEG - nsdoc] segments whose full forward walk runs after the merge: all
+                       //        but the first segment of each split document (that one runs with
+                       //        the transfer walks, from its true start)
+  int* bwalk_seg;      // [NSEG - nsdoc] segments whose full reverse walk runs after the backward
+                       //        merge: all but the last segment of each split document
 };
 
 // Hash of one cu_seqlens entry (document d ends at token `end`): murmur3's
@@ -110,7 +116,9 @@ struct ScanArgs {
   const int* seg_idx;
   const int* seg_split;
   const int* split_seg;
-  int H, HV, G, nsplit, walk;   // walk = 0: full walks over all segments; 1: B and M walks
+  const int* walk_seg;        // walk = 0: the segments to walk (one per CTA group of HV)
+  int H, HV, G, nsplit, walk;   // walk = 0: full walks after the merge; 1: B and M walks (the first
+                                // segment of a split document walks in full here, writing its B)
   float scale;
   uint8_t* tape;              // [NC][HV][STATE_BYTES] or null
   uint8_t* vn;                // [NC][HV][VN_BYTES] V_new^T tiles, or null
@@ -166,7 +174,7 @@ struct Plan {
   int sms;   // SMs of the current device (persistent grids)
   uint32_t cu_hash;
   // workspace offsets (bytes)
-  size_t o_tables[14];
+  size_t o_tables[17];
   size_t o_cb, o_bend, o_sinit, o_mend_ws;
   size_t o_dtape, o_dvn, o_dbend, o_dsinit;   // backward
   size_t o_vnb;                               // backward, replay form: recomputed V_new^T tiles
@@ -177,10 +185,10 @@ struct Plan {
 
 inline Tables tables_at(const Plan& P, uint8_t* ws) {
   Tables t;
-  int** f[13] = {&t.chunk_offsets, &t.seg_offsets, &t.split_offsets, &t.chunk_doc, &t.chunk_tok0,
-                 &t.chunk_len,     &t.seg_doc,     &t.seg_c0,        &t.seg_c1,    &t.seg_idx,
-                 &t.seg_split,     &t.split_seg,   &t.sdoc_first};
-  for (int i = 0; i < 13; ++i) *f[i] = reinterpret_cast<int*>(ws + P.o_tables[i]);
+  int** f[16] = {&t.chunk_offsets, &t.seg_offsets, &t.split_offsets, &t.chunk_doc,    &t.chunk_tok0, &t.chunk_len,
+                 &t.seg_doc,       &t.seg_c0,      &t.seg_c1,        &t.seg_idx,      &t.seg_split,  &t.split_seg,
+                 &t.sdoc_first,    &t.sdoc_offsets, &t.fwalk_seg,    &t.bwalk_seg};
+  for (int i = 0; i < 16; ++i) *f[i] = reinterpret_cast<int*>(ws + P.o_tables[i]);
   return t;
 }
 

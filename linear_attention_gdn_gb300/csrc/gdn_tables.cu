@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(1024) tables_scan_kernel(TableArgs a) {
       a.t.chunk_offsets[d] = carry[0] + excl[0];
       a.t.seg_offsets[d] = carry[1] + excl[1];
       a.t.split_offsets[d] = carry[2] + excl[2];
+      a.t.sdoc_offsets[d] = carry[3] + excl[3];
       if (v[3] && carry[3] + excl[3] <= a.nsdoc) a.t.sdoc_first[carry[3] + excl[3]] = carry[2] + excl[2];
     }
 #pragma unroll
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(1024) tables_scan_kernel(TableArgs a) {
     a.t.chunk_offsets[a.N] = carry[0];
     a.t.seg_offsets[a.N] = carry[1];
     a.t.split_offsets[a.N] = carry[2];
+    a.t.sdoc_offsets[a.N] = carry[3];
     if (carry[3] <= a.nsdoc) a.t.sdoc_first[carry[3]] = carry[2];
     // The host planned from its copy of cu_seqlens.  The device copy must hold
     // the same values: cu[0] = 0, non-decreasing, cu[N] = T, and the same hash
@@ -154,6 +156,12 @@ __global__ void __launch_bounds__(256) tables_fill_kernel(TableArgs a) {
       a.t.split_seg[sp] = i;
     }
     a.t.seg_split[i] = sp;
+    // the segments walked in full after the merges: in the forward all but a split document's first
+    // segment, in the backward all but its last (those walk from their true start / end with the
+    // transfer walks); both lists keep segment order
+    const int sd = a.t.sdoc_offsets[d];
+    if (!(P > 1 && p == 0)) a.t.fwalk_seg[i - sd - (P > 1 ? 1 : 0)] = i;
+    if (!(P > 1 && p == P - 1)) a.t.bwalk_seg[i - sd] = i;
   }
 }
 
