@@ -97,8 +97,10 @@ def _tiles(ws, off, n_blocks, block_bytes, start, R, C):
 
 @pytest.mark.parametrize("name,w", [CASES[0], CASES[1]], ids=[CASES[0][0], CASES[1][0]])
 def test_stage_parity_replay_intermediates(name, w):
-    """T (the UT inverse), V_new (recomputed from the saved states), the adjoint walk's dS' (gradient of the
-    state leaving each chunk) and dV_new, against the chunked FP64 oracle's intermediates."""
+    """T (the UT inverse) and the matrices that define W = T' K and U = T'' V, the gated Aqk and the
+    per-token scalars of the UT blocks, V_new (recomputed from the saved states), the adjoint walk's dS'
+    (gradient of the state leaving each chunk) and dV_new, against the chunked FP64 oracle's
+    intermediates."""
     import linear_attention_gdn_gb300 as gdn
     x = inputs.generate(w, "cpu")
     d = to_dev(x)
@@ -108,13 +110,19 @@ def test_stage_parity_replay_intermediates(name, w):
     nb = NC * HV
     ws = buf.workspace
     T_gpu = _tiles(ws, o_cb, nb, 33792, 24576, 64, 64).reshape(NC, HV, 64, 64)
+    Tp_gpu = _tiles(ws, o_cb, nb, 33792, 0, 64, 64).reshape(NC, HV, 64, 64)        # T' = T diag(beta gamma rk)
+    Tpp_gpu = _tiles(ws, o_cb, nb, 33792, 8192, 64, 64).reshape(NC, HV, 64, 64)    # T'' = T diag(beta)
+    Aqk_gpu = _tiles(ws, o_cb, nb, 33792, 16384, 64, 64).reshape(NC, HV, 64, 64)
+    scal = ws[o_cb: o_cb + nb * 33792].view(nb, 33792)[:, 32768: 32768 + 129 * 4].contiguous()
+    scal = scal.view(torch.float32).double().cpu().numpy().reshape(NC, HV, 129)   # sc[64], kd[64], e^{G_L}
     vn_gpu = _tiles(ws, o_vn, nb, 16384, 0, 128, 64).reshape(NC, HV, 128, 64)        # [dv][token]
     ds_gpu = _tiles(ws, o_ds, nb, 32768, 0, 128, 128).reshape(NC, HV, 128, 128)      # dS'^T [dv][dk]
     dvn_gpu = _tiles(ws, o_dv, nb, 16384, 0, 128, 64).reshape(NC, HV, 128, 64)       # [dv][token]
     t = tables.chunk_tables(w.cu_seqlens)
     f64 = lambda a: a.double().numpy()
-    got = {k: [] for k in ("T", "Vn", "dS", "dVn")}
-    ref = {k: [] for k in ("T", "Vn", "dS", "dVn")}
+    keys = ("T", "Tp", "Tpp", "Aqk", "sc", "kd", "gL", "Vn", "dS", "dVn")
+    got = {k: [] for k in keys}
+    ref = {k: [] for k in keys}
     cu = w.cu_seqlens
     for doc in range(w.N):
         s0, s1 = int(cu[doc]), int(cu[doc + 1])
@@ -126,13 +134,31 @@ def test_stage_parity_replay_intermediates(name, w):
                                 f64(x["v"][s0:s1, hs]).transpose(1, 0, 2), f64(x["g"][s0:s1, hs]).T,
                                 f64(x["beta"][s0:s1, hs]).T, f64(x["dO"][s0:s1, hs]).transpose(1, 0, 2),
                                 l2norm=w.l2norm, scale=w.scale)
+            qd, kd_ = f64(x["q"][s0:s1, j]), f64(x["k"][s0:s1, j])
+            rq = 1 / np.sqrt((qd * qd).sum(1) + 1e-6) if w.l2norm else np.ones(s1 - s0)
+            rk = 1 / np.sqrt((kd_ * kd_).sum(1) + 1e-6) if w.l2norm else np.ones(s1 - s0)
             for h in range(G):
                 hv = j * G + h
                 for c, it in enumerate(out["inter"][h]):
                     gc = int(t["chunk_offsets"][doc]) + c
                     L = len(it["G"])
+                    b_c = f64(x["beta"][s0 + 64 * c: s0 + 64 * c + L, hv])
+                    rk_c, rq_c = rk[64 * c: 64 * c + L], rq[64 * c: 64 * c + L]
                     got["T"].append(T_gpu[gc, hv, :L, :L])
                     ref["T"].append(it["T"])
+                    # W = T' K (raw k rows) and U = T'' V: the matrices that define them
+                    got["Tp"].append(Tp_gpu[gc, hv, :L, :L])
+                    ref["Tp"].append(it["T"] * (b_c * it["gam"] * rk_c)[None, :])
+                    got["Tpp"].append(Tpp_gpu[gc, hv, :L, :L])
+                    ref["Tpp"].append(it["T"] * b_c[None, :])
+                    got["Aqk"].append(Aqk_gpu[gc, hv, :L, :L])
+                    ref["Aqk"].append(np.tril(it["Aqk"]))
+                    got["sc"].append(scal[gc, hv, :L])
+                    ref["sc"].append(w.scale * it["gam"] * rq_c)
+                    got["kd"].append(scal[gc, hv, 64: 64 + L])
+                    ref["kd"].append(it["dec"] * rk_c)
+                    got["gL"].append(scal[gc, hv, 128: 129])
+                    ref["gL"].append(it["gam"][-1:])
                     got["Vn"].append(vn_gpu[gc, hv, :, :L].T)
                     ref["Vn"].append(it["Vn"])
                     got["dS"].append(ds_gpu[gc, hv].T)
