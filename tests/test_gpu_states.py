@@ -30,13 +30,16 @@ def boundary(w, seed, scale=0.2):
     return s_in, ds_out
 
 
+@pytest.mark.parametrize("form", [0, 1], ids=["full_form", "replay_form"])
 @pytest.mark.parametrize("name,w", CASES, ids=[c[0] for c in CASES])
-def test_boundary_states_parity(name, w):
+def test_boundary_states_parity(name, w, form):
+    """Both saved forms: the replay form's backward rebuilds the UT blocks and V_new from a saved set
+    that already holds S_in's effect, and its walks take dS_out in the same way."""
     import linear_attention_gdn_gb300 as gdn
     x = inputs.generate(w, "cpu")
     d = to_dev(x)
     s_in, ds_out = boundary(w, 100 + len(name))
-    prob = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm, w.segments)
+    prob = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm, w.segments, saved_form=form)
     buf = gdn.Buffers(prob, w.cu_seqlens, fill=255)
     nan = float("nan")
     o = torch.full((w.T, w.HV, 128), nan, dtype=torch.bfloat16, device="cuda")
