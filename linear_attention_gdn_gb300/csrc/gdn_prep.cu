@@ -6,7 +6,8 @@
 // (the WY / intra / GLM-prep programs of the pages: "feat(cake_gdn_kcp) ...
 // #8172" page, commit notes on those programs; "#8542" page, save-set table).
 // The forward runs it before the state walk; the backward of the replay saved
-// form runs it again instead of reading the blocks from the saved set.
+// form runs it again instead of reading the blocks from the saved set.  The
+// inverse's block diagonals run on the tensor cores (see prep_kernel).
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "gdn_prof.h"
@@ -15,34 +16,45 @@
 namespace gdn {
 
 constexpr int PR_THREADS = 128;
-constexpr int PR_BLOCKS_PER_SM = 5;
+constexpr int PR_BLOCKS_PER_SM = 4;
 // Shared memory (bytes, 1024-aligned tiles).  The [K; Q] tile is dead once the
-// KK^T / QK^T MMA has completed; its space then holds the FP32 array, the Aqk
-// staging tile and the scalars, and finally the T' and T'' tiles (written over
-// the FP32 array after every thread has read its part of T into registers).
+// item's KK^T / QK^T MMA has completed; its space then holds, for each value
+// head in turn, the FP32 A^T array, then the BF16 tiles of the inverse (D, the
+// inverted diagonal blocks; L^T, then X; N; N^2), and finally the T', T'' and T
+// output tiles.  Aqk and the scalars sit past it.
 constexpr int PR_KQ = 0;                             // [K; Q] SwTile(128 x 128), 32 KB
 constexpr int PR_S = 0;                              // FP32 S[64][UT_ALD]
+constexpr int PR_D = 0;                              // D (inverted diagonal blocks), SwTile(64 x 64)
+constexpr int PR_LX = TILE64_BYTES;                  // L^T, then X = I - N + N^2 - N^3
+constexpr int PR_N = 2 * TILE64_BYTES;               // N = D L
+constexpr int PR_N2 = 3 * TILE64_BYTES;              // N^2
 constexpr int PR_TP = 0;                             // T', then T'' (contiguous, one bulk store)
-constexpr int PR_AQ = 17408;                         // Aqk tile
+constexpr int PR_T = 2 * TILE64_BYTES;               // T tile
+constexpr int PR_AQ = 32768;                         // Aqk tile
 constexpr int PR_SC = PR_AQ + TILE64_BYTES;          // scalars
-constexpr int PR_T = PR_SC + CB_SCAL_BYTES;          // T tile
-constexpr int PR_SMEM = PR_T + TILE64_BYTES;
+constexpr int PR_SMEM = PR_SC + CB_SCAL_BYTES;
 constexpr int PR_SMEM_ALLOC = PR_SMEM + 1024;
-static_assert(UT_WORK_BYTES <= PR_AQ && 2 * TILE64_BYTES <= PR_AQ, "FP32 array and T', T'' fit below Aqk");
+static_assert(UT_WORK_BYTES <= PR_N + TILE64_BYTES, "the FP32 array is dead before N^2 is written");
+static_assert(4 * TILE64_BYTES <= PR_AQ, "the inverse's tiles fit below Aqk");
 static_assert(PR_AQ % 1024 == 0 && PR_T % 1024 == 0, "swizzled tiles are 1024-aligned");
-static_assert(PR_SMEM >= 32768, "the [K; Q] tile fits");
 static_assert(CB_SCAL_BYTES == UT_SCAL_BYTES, "one scalar block layout");
+// TMEM columns: the item's [KK^T; QK^T] (read by every value head), then the inverse's products
+constexpr int PT_KK = 0, PT_INV = 64, PT_COLS = 128;
 
 // One CTA per (chunk, q/k head): the tile load, the norms and the KK^T / QK^T
 // MMA once, then the group's value heads one after another on that product
-// (each head's stores drain while the next one is prepared).  Five CTAs share
-// an SM, so the serial phases of one (tile load, MMA, inverse) run under the
-// others.  The UT arithmetic is gdn_ut.cuh's.
+// (each head's stores drain while the next one is prepared).  Four CTAs share
+// an SM, so the serial phases of one run under the others.  The UT arithmetic
+// is gdn_ut.cuh's, except for the inverse's block diagonals, which run on the
+// tensor cores: with D the inverted 16 x 16 diagonal blocks (FP32 forward
+// substitution) and L the strictly block-lower part of A,
+//   I + A = D^-1 (I + N),  N = D L,  N^4 = 0   =>   T = (I - N + N^2 - N^3) D,
+// four dependent M = 64 tcgen05 products (BF16 operands, FP32 accumulation).
 __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(const __grid_constant__ PrepArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
   __shared__ UtTok ut;
-  __shared__ uint64_t bar, bar_kq;
+  __shared__ uint64_t bar, bar_kq, bar_t;
   __shared__ uint32_t tslot;
   const int c = blockIdx.x / a.H, j = blockIdx.x % a.H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -50,10 +62,11 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
   const int tok0 = a.chunk_tok0[c], L = a.chunk_len[c];
 
   // ---- [K; Q] tile by TMA: rows 0..63 = k tokens, 64..127 = q tokens (SwTile(128 x 128))
-  if (warp == 0) tmem_alloc(&tslot, 64);
+  if (warp == 0) tmem_alloc(&tslot, PT_COLS);
   if (tid == 0) {
     mbar_init(&bar, 1);
     mbar_init(&bar_kq, 1);
+    mbar_init(&bar_t, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
     mbar_expect_tx(&bar_kq, 32768u);
     tma_load_3d(sm + PR_KQ, &a.tk, 0, j, tok0, &bar_kq);
@@ -67,7 +80,7 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
   if (warp == 3) ut_load_gates(a.g, a.beta, a.HV, j * a.G, tok0, L, lane, gb);
   __syncthreads();
   if (!__syncthreads_and(mbar_wait(&bar_kq, 0, a.err))) {
-    if (warp == 0) tmem_dealloc(tslot, 64);
+    if (warp == 0) tmem_dealloc(tslot, PT_COLS);
     return;
   }
   if (L < CH) {   // zero the rows past the document end (they hold the next document)
@@ -81,12 +94,40 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
   tc_fence_after();
   const uint32_t tb = tslot;
   if (warp == 0) {
-    ut_issue_kkqk(tb, smem_u32(sm + PR_KQ));
+    ut_issue_kkqk(tb + PT_KK, smem_u32(sm + PR_KQ));
     mma_commit_w(&bar);
   }
   // ---- the value heads of the group, one after another, on the one KK^T / QK^T
   bool ok = true;
+  uint32_t tph = 0;   // phase of bar_t (four products per value head)
   float* Sm = reinterpret_cast<float*>(sm + PR_S);
+  const uint32_t s_d = smem_u32(sm + PR_D), s_lx = smem_u32(sm + PR_LX), s_n = smem_u32(sm + PR_N),
+                 s_n2 = smem_u32(sm + PR_N2);
+  // this thread's 32 elements of an M = 64 result (the .16x256b lane map): rows r0, r0 + 8, columns
+  // 16 g + cq, cq + 1, cq + 8, cq + 9 for g = 0..3
+  const int r0 = 16 * warp + (lane >> 2), cq = 2 * (lane & 3);
+  auto ld_result = [&](uint32_t (&u)[4][8]) {   // the inverse's current product, FP32 bits
+#pragma unroll
+    for (int g = 0; g < 4; ++g) tmem_ld_m64_async(taddr(tb, warp * 32, PT_INV + 16 * g), u[g]);
+    tmem_wait_ld();
+  };
+  auto product = [&](uint32_t a_tile, uint32_t b_tile, bool b_mn) -> bool {   // D(TMEM) = A B, M = N = K = 64
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) {
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ss_w(tb + PT_INV, desc_k(a_tile, 64, ks), b_mn ? desc_mn(b_tile, 64, ks) : desc_k(b_tile, 64, ks),
+                 idesc(64, 64, 0, b_mn ? 1 : 0), ks > 0);
+      mma_commit_w(&bar_t);
+    }
+    const bool r = __syncthreads_and(mbar_wait(&bar_t, tph, a.err));
+    tph ^= 1;
+    tc_fence_after();
+    return r;
+  };
   for (int hh = 0; hh < a.G; ++hh) {
     const int hv = j * a.G + hh;
     if (warp == 3) {   // ---- gates (log2 units), then the next head's loads
@@ -101,25 +142,92 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
     tc_fence_after();
     float* sc = reinterpret_cast<float*>(sm + PR_SC);
     if (ok) {
-      // ---- A^T (FP32, from the rows of KK^T), Aqk tile (rows of QK^T), scalars; then the inverse
-      ut_build(tb, warp, 0, tid, L, a.scale, ut, Sm, sm + PR_AQ, sc);
-      if (tid < 64) ut_inverse(Sm, tid, 1);
+      // ---- A^T (FP32, from the rows of KK^T), Aqk tile (rows of QK^T), scalars; the diagonal blocks
+      ut_build(tb + PT_KK, warp, 0, tid, L, a.scale, ut, Sm, sm + PR_AQ, sc);
+      if (tid < 64) ut_diag_blocks(Sm, tid, 1);
     }
-    __syncthreads();   // T complete, Aqk and the scalars staged
-    if (ok) {
-      // ---- the T', T'', T tiles, all 128 threads: 16-byte chunks (row i, columns 8 c8 .. 8 c8 + 7);
-      // first every thread reads its four chunks of T, then (after a barrier) overwrites the array
-      float tv[4][8];
-      ut_read_T(Sm, tid, tv);
-      __syncthreads();
+    __syncthreads();
+    if (!ok) continue;
+    {  // ---- D and L^T as BF16 tiles from rows of the array: row n of it holds T_bb (columns of n's
+       // block, zero above the diagonal) and, in the later blocks' columns c, A[c][n] = L^T[n][c]
+      uint4 dch[4], lch[4];
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
-        const int item = tid + PR_THREADS * it, i = item >> 3, c8 = item & 7;
-        const uint32_t off = sw_chunk(i, c8, 64);
-        *reinterpret_cast<uint4*>(sm + PR_TP + off) = ut_chunk(tv, it, c8, ut.pcol);               // T'
-        *reinterpret_cast<uint4*>(sm + PR_TP + TILE64_BYTES + off) = ut_chunk(tv, it, c8, ut.bs);  // T''
-        if (a.write_T) *reinterpret_cast<uint4*>(sm + PR_T + off) = ut_chunk(tv, it, c8, nullptr); // T
+        const int item = tid + PR_THREADS * it, n = item >> 3, c8 = item & 7;
+        const float4 u0 = *reinterpret_cast<const float4*>(Sm + n * UT_ALD + 8 * c8);
+        const float4 u1 = *reinterpret_cast<const float4*>(Sm + n * UT_ALD + 8 * c8 + 4);
+        const uint4 w = make_uint4(pack_bf16(u0.x, u0.y), pack_bf16(u0.z, u0.w), pack_bf16(u1.x, u1.y),
+                                   pack_bf16(u1.z, u1.w));
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        const int bn = n >> 4, bc = c8 >> 1;
+        dch[it] = bc == bn ? w : z;
+        lch[it] = bc > bn ? w : z;
       }
+      __syncthreads();   // the array is read: its space takes the tiles
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int item = tid + PR_THREADS * it, n = item >> 3, c8 = item & 7;
+        *reinterpret_cast<uint4*>(sm + PR_D + sw_chunk(n, c8, 64)) = dch[it];
+        *reinterpret_cast<uint4*>(sm + PR_LX + sw_chunk(n, c8, 64)) = lch[it];
+      }
+    }
+    uint32_t u[4][8];
+    // (a K-major B tile is rows N, columns K; L^T is that form of L.  An MN-major B tile is rows K,
+    // columns N: a row-major N or D.)
+    ok = product(s_d, s_lx, false);   // N = D L
+    if (ok) {  // N -> BF16 tile
+      ld_result(u);
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * g + 8 * (i >> 2) + cq;
+          *reinterpret_cast<uint32_t*>(sm + PR_N + sw_off(r, cc, 64)) =
+              pack_bf16(__uint_as_float(u[g][i]), __uint_as_float(u[g][i + 1]));
+        }
+    }
+    ok = ok && product(s_n, s_n, true);   // N^2 = N N
+    if (ok) {
+      ld_result(u);
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * g + 8 * (i >> 2) + cq;
+          *reinterpret_cast<uint32_t*>(sm + PR_N2 + sw_off(r, cc, 64)) =
+              pack_bf16(__uint_as_float(u[g][i]), __uint_as_float(u[g][i + 1]));
+        }
+    }
+    ok = ok && product(s_n2, s_n, true);   // N^3 = N^2 N
+    if (ok) {  // X = I - N + N^2 - N^3 -> BF16 tile (over L^T, which N = D L has finished reading)
+      ld_result(u);
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * g + 8 * (i >> 2) + cq;
+          const uint32_t off = sw_off(r, cc, 64);
+          const float2 n1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sm + PR_N + off));
+          const float2 n2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sm + PR_N2 + off));
+          const float x0 = (r == cc ? 1.f : 0.f) - n1.x + n2.x - __uint_as_float(u[g][i]);
+          const float x1 = (r == cc + 1 ? 1.f : 0.f) - n1.y + n2.y - __uint_as_float(u[g][i + 1]);
+          *reinterpret_cast<uint32_t*>(sm + PR_LX + off) = pack_bf16(x0, x1);
+        }
+    }
+    ok = ok && product(s_lx, s_d, true);   // T = X D
+    if (ok) {  // T', T'', T tiles (over D, X, N: the last product has read them)
+      ld_result(u);
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * g + 8 * (i >> 2) + cq;
+          const uint32_t off = sw_off(r, cc, 64);
+          const float t0 = __uint_as_float(u[g][i]), t1 = __uint_as_float(u[g][i + 1]);
+          *reinterpret_cast<uint32_t*>(sm + PR_TP + off) = pack_bf16(t0 * ut.pcol[cc], t1 * ut.pcol[cc + 1]);
+          *reinterpret_cast<uint32_t*>(sm + PR_TP + TILE64_BYTES + off) = pack_bf16(t0 * ut.bs[cc], t1 * ut.bs[cc + 1]);
+          if (a.write_T) *reinterpret_cast<uint32_t*>(sm + PR_T + off) = pack_bf16(t0, t1);
+        }
       fence_async_smem();
     }
     __syncthreads();
@@ -135,7 +243,7 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
   if (tid == 0) bulk_wait_read();   // shared memory must outlive the copies' reads
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tb, 64);
+  if (warp == 0) tmem_dealloc(tb, PT_COLS);
 }
 
 void setup_prep_attrs() {

@@ -290,11 +290,13 @@ __device__ __forceinline__ void ut_offdiag_level(float* Sm, int l) {
   }
 }
 
-// T = (I + A)^-1 in place in Sm, on lanes l = 0..63 (warps of one 64-thread group that syncs on named
-// barrier `bar_id`).  Call after the A^T rows of ut_build are written.
-__device__ __forceinline__ void ut_inverse(float* Sm, int l, int bar_id) {
+// The four diagonal blocks T_bb = (I + A_bb)^-1 of T, in place in Sm, on lanes l = 0..63 (the
+// warps of one 64-thread group that syncs on named barrier `bar_id`): forward substitution, lane =
+// column; the upper triangles of the blocks are zeroed.  Call after the A^T rows of ut_build are
+// written.
+__device__ __forceinline__ void ut_diag_blocks(float* Sm, int l, int bar_id) {
   named_bar(bar_id, 64);
-  {  // diagonal blocks T_bb = (I + A_bb)^-1 by forward substitution, lane = column
+  {
     const int o = 16 * (l >> 4), cc = l & 15;
     float x[16];
 #pragma unroll
@@ -315,6 +317,13 @@ __device__ __forceinline__ void ut_inverse(float* Sm, int l, int bar_id) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) Sm[(o + i) * UT_ALD + o + cc] = x[i];   // x[i] = 0 above the diagonal
   }
+}
+
+// T = (I + A)^-1 in place in Sm, on lanes l = 0..63 (warps of one 64-thread group that syncs on named
+// barrier `bar_id`): the diagonal blocks, then the three block diagonals.  Call after the A^T rows of
+// ut_build are written.
+__device__ __forceinline__ void ut_inverse(float* Sm, int l, int bar_id) {
+  ut_diag_blocks(Sm, l, bar_id);
   named_bar(bar_id, 64);
   ut_offdiag_level<1>(Sm, l);
   named_bar(bar_id, 64);
