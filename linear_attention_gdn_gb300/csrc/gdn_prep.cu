@@ -79,7 +79,9 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
   float gb[4] = {0.f, 0.f, 0.f, 0.f};
   if (warp == 3) ut_load_gates(a.g, a.beta, a.HV, j * a.G, tok0, L, lane, gb);
   __syncthreads();
-  if (!__syncthreads_and(mbar_wait(&bar_kq, 0, a.err))) {
+  if (!__syncthreads_and(mbar_wait(&bar_kq, 0, a.err))) {   // error path: the tile copy must land first
+    if (tid == 0) mbar_drain(&bar_kq, 0);
+    __syncthreads();
     if (warp == 0) tmem_dealloc(tslot, PT_COLS);
     return;
   }
@@ -100,6 +102,7 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
   // ---- the value heads of the group, one after another, on the one KK^T / QK^T
   bool ok = true;
   uint32_t tph = 0;   // phase of bar_t (four products per value head)
+  int t_pend = -1;    // error path: phase of a product whose completion was not seen (-1: none)
   float* Sm = reinterpret_cast<float*>(sm + PR_S);
   const uint32_t s_d = smem_u32(sm + PR_D), s_lx = smem_u32(sm + PR_LX), s_n = smem_u32(sm + PR_N),
                  s_n2 = smem_u32(sm + PR_N2);
@@ -124,6 +127,7 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
       mma_commit_w(&bar_t);
     }
     const bool r = __syncthreads_and(mbar_wait(&bar_t, tph, a.err));
+    if (!r) t_pend = (int)tph;
     tph ^= 1;
     tc_fence_after();
     return r;
@@ -241,6 +245,10 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
     }
   }
   if (tid == 0) bulk_wait_read();   // shared memory must outlive the copies' reads
+  if (!ok && tid == 0) {   // error path (bounded waits): no MMA may outlive the CTA's TMEM
+    mbar_drain(&bar, 0);
+    if (t_pend >= 0) mbar_drain(&bar_t, (uint32_t)t_pend);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, PT_COLS);

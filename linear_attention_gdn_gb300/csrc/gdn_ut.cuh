@@ -1,5 +1,5 @@
 // gdn_ut.cuh -- the on-chip UT / WY stage of one 64-token chunk and one value
-// head, run by one 128-thread warpgroup inside the walk kernels.
+// head, run by one 128-thread warpgroup of the preparation kernel.
 //
 // For the chunk's tokens r < L (q/k head j, value head h):
 //   rk_r, rq_r   1/sqrt(x.x + 1e-6) of k_r, q_r (or 1 with l2norm off)
@@ -14,10 +14,9 @@
 // on the intra / WY / GLM-prep programs; "#8542" page, the save-set table,
 // which lists gcum, Akk, Aqk, w and u among what the replay form recomputes).
 // KK^T and QK^T come from one tcgen05 MMA on the stacked [K; Q] tile (M = 128)
-// into 64 TMEM columns; the unit lower-triangular inverse is FP32, blocked by
-// 16 x 16: the four diagonal blocks by forward substitution (one lane per
-// column), then the three block diagonals, each block from the finished ones
-// (T_ij = -T_ii sum_k A_ik T_kj), on 64 lanes.
+// into 64 TMEM columns; of the unit lower-triangular inverse, the four 16 x 16
+// diagonal blocks are formed here in FP32 by forward substitution (one lane
+// per column); the kernel that calls these routines completes T from them.
 //
 // Gate factors: e^{G_r - G_c} for c <= r is the product e^{G_r - G_0}
 // e^{G_0 - G_c} of per-token factors when the chunk's gate range G_0 - G_{L-1}
@@ -232,64 +231,6 @@ __device__ __forceinline__ void ut_build(uint32_t tb, int wq, int kk, int lt, in
   }
 }
 
-// One block diagonal d of T = (I + A)^-1 (16 x 16 blocks, 64 lanes): T_ij = -T_ii p with
-// p = sum_{k=j}^{i-1} A_ik T_kj, for the 4 - d blocks (i, j = i - d).  Sm holds A[r][c] (c < r) at
-// Sm[c][r] and T[r][c] (c <= r) at Sm[r][c]; the upper triangles of the diagonal blocks hold zeros.
-// The (4 - d) * 16 columns are spread over 64 lanes as G = 1, 2, 4 lanes per column; lane g of a
-// column accumulates rows [16g/G, 16(g+1)/G) of p over the whole k range, the G lanes exchange their
-// rows by shuffles, and each then forms its rows of T_ij.
-template <int DL>
-__device__ __forceinline__ void ut_offdiag_level(float* Sm, int l) {
-  constexpr int G = DL == 1 ? 1 : (DL == 2 ? 2 : 4);
-  constexpr int R = 16 / G;
-  constexpr int NCOL = (4 - DL) * 16;
-  const int cl = l / G, g = l % G;
-  const bool act = cl < NCOL;
-  const int jb = act ? cl >> 4 : 0, oi = 16 * (jb + DL), c = 16 * jb + (cl & 15);
-  float p[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) p[r] = 0.f;
-  if (act) {
-#pragma unroll 4
-    for (int t = 16 * jb; t < oi; ++t) {
-      const float tv = Sm[t * UT_ALD + c];
-#pragma unroll
-      for (int q = 0; q < R / 4; ++q) {
-        const float4 av = *reinterpret_cast<const float4*>(Sm + t * UT_ALD + oi + g * R + 4 * q);
-        fma2(p[4 * q + 0], p[4 * q + 1], av.x, av.y, tv);
-        fma2(p[4 * q + 2], p[4 * q + 3], av.z, av.w, tv);
-      }
-    }
-  }
-  float pf[16];
-  if constexpr (G == 1) {
-#pragma unroll
-    for (int r = 0; r < 16; ++r) pf[r] = p[r];
-  } else {
-#pragma unroll
-    for (int og = 0; og < G; ++og)
-#pragma unroll
-      for (int r = 0; r < R; ++r) pf[og * R + r] = __shfl_sync(0xffffffffu, p[r], (l & 31 & ~(G - 1)) + og);
-  }
-  if (act) {
-#pragma unroll
-    for (int rr = 0; rr < R; ++rr) {   // T_ij[r][c] = -sum_{s <= r} T_ii[r][s] p[s]
-      const int r = g * R + rr;
-      float acc = 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (G == 1 && 4 * q > rr) continue;
-        const float4 tv4 = *reinterpret_cast<const float4*>(Sm + (oi + r) * UT_ALD + oi + 4 * q);
-        acc = fmaf(tv4.x, pf[4 * q + 0], acc);
-        if (G > 1 || 4 * q + 1 <= rr) acc = fmaf(tv4.y, pf[4 * q + 1], acc);
-        if (G > 1 || 4 * q + 2 <= rr) acc = fmaf(tv4.z, pf[4 * q + 2], acc);
-        if (G > 1 || 4 * q + 3 <= rr) acc = fmaf(tv4.w, pf[4 * q + 3], acc);
-      }
-      Sm[(oi + r) * UT_ALD + c] = -acc;
-    }
-  }
-}
-
 // The four diagonal blocks T_bb = (I + A_bb)^-1 of T, in place in Sm, on lanes l = 0..63 (the
 // warps of one 64-thread group that syncs on named barrier `bar_id`): forward substitution, lane =
 // column; the upper triangles of the blocks are zeroed.  Call after the A^T rows of ut_build are
@@ -317,46 +258,6 @@ __device__ __forceinline__ void ut_diag_blocks(float* Sm, int l, int bar_id) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) Sm[(o + i) * UT_ALD + o + cc] = x[i];   // x[i] = 0 above the diagonal
   }
-}
-
-// T = (I + A)^-1 in place in Sm, on lanes l = 0..63 (warps of one 64-thread group that syncs on named
-// barrier `bar_id`): the diagonal blocks, then the three block diagonals.  Call after the A^T rows of
-// ut_build are written.
-__device__ __forceinline__ void ut_inverse(float* Sm, int l, int bar_id) {
-  ut_diag_blocks(Sm, l, bar_id);
-  named_bar(bar_id, 64);
-  ut_offdiag_level<1>(Sm, l);
-  named_bar(bar_id, 64);
-  ut_offdiag_level<2>(Sm, l);
-  named_bar(bar_id, 64);
-  ut_offdiag_level<3>(Sm, l);
-}
-
-// The four 16-byte chunks (row i, columns 8 c8 .. 8 c8 + 7) of T that thread lt of the warpgroup
-// handles, read from the FP32 array (zero above the diagonal, where the array still holds A^T).
-__device__ __forceinline__ void ut_read_T(const float* Sm, int lt, float (&tv)[4][8]) {
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int item = lt + 128 * it, i = item >> 3, c8 = item & 7;
-    const float4 u0 = *reinterpret_cast<const float4*>(Sm + i * UT_ALD + 8 * c8);
-    const float4 u1 = *reinterpret_cast<const float4*>(Sm + i * UT_ALD + 8 * c8 + 4);
-    const float x[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-    for (int e = 0; e < 8; ++e) tv[it][e] = 8 * c8 + e <= i ? x[e] : 0.f;
-  }
-}
-
-// 16-byte chunk `it` of T with its columns scaled by f (f == nullptr: unscaled), as BF16
-__device__ __forceinline__ uint4 ut_chunk(const float (&tv)[4][8], int it, int c8, const float* f) {
-  float y[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) y[e] = f ? tv[it][e] * f[8 * c8 + e] : tv[it][e];
-  uint4 w;
-  w.x = pack_bf16(y[0], y[1]);
-  w.y = pack_bf16(y[2], y[3]);
-  w.z = pack_bf16(y[4], y[5]);
-  w.w = pack_bf16(y[6], y[7]);
-  return w;
 }
 
 }  // namespace gdn
