@@ -94,7 +94,9 @@ typedef enum {
     GDN_ERR_SAVED_MISMATCH = 4,     /* device-side: `saved` was not written by a forward of this problem */
     GDN_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed */
     GDN_ERR_TIMEOUT = 6,            /* device-side: a bounded wait ran out */
-    GDN_ERR_DEVICE = 7              /* device-side: any other kernel-detected fault */
+    GDN_ERR_DEVICE = 7,             /* device-side: any other kernel-detected fault */
+    GDN_ERR_GATE_RANGE = 8          /* device-side (KDA entry points): a key channel's decay within one
+                                       16-token block is steeper than 2^-96 (see gdn_kda_fwd) */
 } gdn_status;
 
 /*
@@ -224,6 +226,37 @@ gdn_status gdn_conv1d_bwd(const gdn_conv_problem *prob, const void *x, const flo
                           const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host, const void *dy,
                           void *dx, float *dw, float *db, void *workspace, size_t ws_bytes,
                           struct CUstream_st *stream);
+
+/*
+ * The per-channel-decay form (KDA): the same recurrence with one decay per key channel,
+ *
+ *     S_t = Diag(a_t) S_{t-1} + beta_t k^_t (v_t - (Diag(a_t) S_{t-1})^T k^_t)^T,   a_t = exp(g_t) in R^dk
+ *     o_t = scale * S_t^T q^_t
+ *
+ * ("perf(cake_kda) ... #7097" page: the packed KDA training family beside the GDN one; the pages
+ * print no formula, and this is the GDN rule above with its scalar decay replaced by a per-channel
+ * one).  Conventions as for the GDN entry points, except:
+ *   - g and dg are [T][HV][128] FP32: the log decay of each key channel (g <= 0 for a decay);
+ *   - prob->saved_form is ignored.  The saved set holds the header, the BF16 state entering every
+ *     chunk (32 KiB per chunk and value head), M_seg where a document is split, and the BF16
+ *     V_new^T of every chunk (16 KiB per chunk and value head); the backward recomputes the
+ *     per-chunk decay products and UT blocks (the pages' replay of w, u and the A matrices);
+ *   - a chunk in which some key channel decays by more than 2^-96 within one 16-token block (a
+ *     log decay below -66.5 over 16 tokens) is refused on the device: the error word is set to
+ *     GDN_ERR_GATE_RANGE and the outputs are left unwritten.  Below that bound every chunk is
+ *     computed (the kernels factor the decays per 16-token block, and the factors must stay in
+ *     BF16's exponent range).
+ * gdn_kda_saved_bytes: the sizes of `saved` and of the workspace (forward and backward).
+ * gdn_kda_fwd: writes o (required) and, if `saved` is non-null, the saved set.
+ * gdn_kda_bwd: given dO and the saved set of a gdn_kda_fwd of the same problem and inputs, writes
+ *   dq, dk, dv (BF16), dg [T][HV][128] and dbeta [T][HV] (FP32).
+ */
+gdn_status gdn_kda_saved_bytes(const gdn_problem *prob, const int32_t *cu_seqlens_host,
+                               size_t *saved_bytes, size_t *workspace_bytes);
+gdn_status gdn_kda_fwd(const gdn_problem *prob, const void *q, const void *k, const void *v,
+                       const float *g, const float *beta, const int32_t *cu_seqlens_dev,
+                       const int32_t *cu_seqlens_host, void *o, void *saved, void *workspace,
+                       size_t ws_bytes, struct CUstream_st *stream);
 
 /* Static description of a status code. */
 const char *gdn_status_string(gdn_status s);

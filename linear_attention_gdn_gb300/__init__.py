@@ -18,11 +18,12 @@ from . import build as _build
 
 LIB_PATH = _build.LIB
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_WORKSPACE_TOO_SMALL",
-          4: "GDN_ERR_SAVED_MISMATCH", 5: "GDN_ERR_CUDA", 6: "GDN_ERR_TIMEOUT", 7: "GDN_ERR_DEVICE"}
+          4: "GDN_ERR_SAVED_MISMATCH", 5: "GDN_ERR_CUDA", 6: "GDN_ERR_TIMEOUT", 7: "GDN_ERR_DEVICE",
+          8: "GDN_ERR_GATE_RANGE"}
 EXPORTS = ("gdn_saved_bytes", "gdn_fwd", "gdn_bwd", "gdn_ckpt_fwd_bwd", "gdn_status_string",
            "gdn_device_status", "gdn_plan_segment_chunks", "gdn_chunk_table_offsets", "gdn_profile_enable",
            "gdn_profile_read", "gdn_fwd_noalloc", "gdn_fwd_states", "gdn_bwd_states", "gdn_conv1d_workspace_bytes",
-           "gdn_conv1d_fwd", "gdn_conv1d_bwd", "gdn_backward_tape_offsets")
+           "gdn_conv1d_fwd", "gdn_conv1d_bwd", "gdn_backward_tape_offsets", "gdn_kda_saved_bytes", "gdn_kda_fwd")
 SAVED_FULL, SAVED_REPLAY = 0, 1   # gdn_problem.saved_form
 
 
@@ -76,6 +77,8 @@ def _load():
     L.gdn_plan_segment_chunks.restype = ctypes.c_int32
     L.gdn_chunk_table_offsets.argtypes = [pp, i32p, ctypes.POINTER(sz), i32p]
     L.gdn_backward_tape_offsets.argtypes = [pp, i32p, ctypes.POINTER(sz)]
+    L.gdn_kda_saved_bytes.argtypes = [pp, i32p, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    L.gdn_kda_fwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, sz, vp]
     L.gdn_fwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, i32p, i32p, vp, vp]
     L.gdn_fwd_noalloc.restype = ctypes.c_int
     cp = ctypes.POINTER(gdn_conv_problem)
@@ -186,6 +189,25 @@ def gdn_fwd(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, o, saved, w
                        _ptr(saved), _ptr(workspace), ws_bytes, _stream(stream)), "gdn_fwd")
 
 
+def gdn_kda_saved_bytes(prob: gdn_problem, cu_seqlens_host):
+    """(saved bytes, workspace bytes) of the per-channel-decay (KDA) entry points."""
+    cu, cup = _cu_host(cu_seqlens_host)
+    s, w = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(lib.gdn_kda_saved_bytes(ctypes.byref(prob), cup, ctypes.byref(s), ctypes.byref(w)),
+           "gdn_kda_saved_bytes")
+    return s.value, w.value
+
+
+def gdn_kda_fwd(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, o, saved, workspace, ws_bytes=None,
+                stream=None):
+    """KDA forward: g is FP32 [T, HV, 128] (a log decay per key channel); see include/gdn.h."""
+    cu, cup = _cu_host(cu_seqlens_host)
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
+    _check(lib.gdn_kda_fwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                           ctypes.cast(_ptr(cu_seqlens_dev), ctypes.POINTER(ctypes.c_int32)), cup, _ptr(o),
+                           _ptr(saved), _ptr(workspace), ws_bytes, _stream(stream)), "gdn_kda_fwd")
+
+
 def gdn_fwd_states(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, s_in, o, s_out, saved, workspace,
                    ws_bytes=None, stream=None):
     """gdn_fwd with per-document boundary states: s_in, s_out FP32 [N, HV, 128, 128] (either may be None);
@@ -290,9 +312,10 @@ def gdn_conv1d_bwd(prob, x, w, b, cu_seqlens_dev, cu_seqlens_host, dy, dx, dw, d
 class Buffers:
     """Caller-side saved set and workspace for one problem, allocated with torch."""
 
-    def __init__(self, prob: gdn_problem, cu_seqlens_host, device="cuda", fill=None):
+    def __init__(self, prob: gdn_problem, cu_seqlens_host, device="cuda", fill=None, kda=False):
         import torch
-        self.saved_bytes, self.ws_bytes = gdn_saved_bytes(prob, cu_seqlens_host)
+        sizes = gdn_kda_saved_bytes if kda else gdn_saved_bytes
+        self.saved_bytes, self.ws_bytes = sizes(prob, cu_seqlens_host)
         mk = (lambda n: torch.full((max(n, 1024),), fill, dtype=torch.uint8, device=device)) if fill is not None \
             else (lambda n: torch.empty((max(n, 1024),), dtype=torch.uint8, device=device))
         self.saved = mk(self.saved_bytes)

@@ -24,6 +24,7 @@ void setup_fwd_scan_attrs();
 void setup_bwd_attrs();
 void setup_prep_attrs();
 void setup_vnew_attrs();
+void setup_kda_attrs();
 gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const void* k, const void* v,
                    const float* g, const float* beta, const int32_t* cu_dev, const void* dO, const void* saved,
                    void* dq, void* dk, void* dv, float* dg, float* dbeta, const float* ds_out, float* ds_in,
@@ -100,7 +101,7 @@ static void plan_segments(const gdn_problem* p, const int32_t* cu, int* seg_len,
   }
 }
 
-static gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
+gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
   gdn_status st = validate_problem(p, cu);
   if (st != GDN_OK) return st;
   P->T = p->T;
@@ -233,7 +234,7 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t T, int heads) {
   return r == CUDA_SUCCESS;
 }
 
-static bool device_setup() {
+bool device_setup() {
   static std::mutex mu;
   static bool done[128] = {};
   int dev = 0;
@@ -244,6 +245,7 @@ static bool device_setup() {
     setup_bwd_attrs();
     setup_prep_attrs();
     setup_vnew_attrs();
+    setup_kda_attrs();
     done[dev] = true;
   }
   return true;
@@ -257,7 +259,8 @@ static const char* const kKernelNames[K_NUM] = {
     "tables_scan_kernel", "tables_fill_kernel", "prep_kernel",    "fwd_scan_kernel(walk)",
     "merge_kernel",       "fwd_scan_kernel",    "check_saved_kernel", "bwd_scan_kernel(walk)",
     "merge_bwd_kernel",   "bwd_scan_kernel",    "grad_kernel",        "passthrough_kernel",
-    "conv_fwd_kernel",    "conv_bwd_kernel(+reduce)", "vnew_kernel"};
+    "conv_fwd_kernel",    "conv_bwd_kernel(+reduce)", "vnew_kernel",      "kda_prep_kernel",
+    "kda_out_kernel",     "kda_grad_kernel"};
 struct ProfRec {
   int id;
   cudaEvent_t e0, e1;
@@ -297,7 +300,7 @@ void prof_end(int id, cudaStream_t s) {
   g_open[id] = nullptr;
 }
 
-static bool aligned16(const void* p) { return p && ((uintptr_t)p & 15) == 0; }
+bool aligned16(const void* p) { return p && ((uintptr_t)p & 15) == 0; }
 
 // ---------------------------------------------------------------------------
 // forward
@@ -434,6 +437,7 @@ const char* gdn_status_string(gdn_status s) {
     case GDN_ERR_CUDA: return "CUDA error";
     case GDN_ERR_TIMEOUT: return "a bounded device wait ran out";
     case GDN_ERR_DEVICE: return "device-side error";
+    case GDN_ERR_GATE_RANGE: return "a per-channel decay too steep within 16 tokens (KDA)";
   }
   return "unknown status";
 }
@@ -598,7 +602,7 @@ gdn_status gdn_device_status(void* workspace, struct CUstream_st* stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return GDN_ERR_CUDA;
   int e = 0;
   if (cudaMemcpy(&e, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
-  if (e < 0 || e > 7) return GDN_ERR_DEVICE;
+  if (e < 0 || e > 8) return GDN_ERR_DEVICE;
   return (gdn_status)e;
 }
 

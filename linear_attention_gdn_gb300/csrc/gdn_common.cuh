@@ -25,6 +25,7 @@ constexpr int D = 128;   // head dim (dk = dv)
 constexpr int ST_TIMEOUT = 6;
 constexpr int ST_DEVICE = 7;
 constexpr int ST_SAVED_MISMATCH = 4;
+constexpr int ST_GATE_RANGE = 8;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);

@@ -82,6 +82,13 @@ __device__ __forceinline__ void store_state_row(uint8_t* dst, int row, const flo
 //   bar_o[b]  MMA2(n) done      (chain: output(n) from O buffer b = n & 1)
 //   bar_sf    chain -> helper   chunk n's stage is no longer read (V_new^T copy)
 // Each completes once per use, and no waiter can fall two phases behind.
+//
+// KDA = true: the per-channel-decay form (one decay per key channel).  The
+// stage then holds the chunk's -W^T and Kd (from kda_prep_kernel) in the K and
+// Q slots, V, T'' and gamma_L; MMA1 reads -W^T from the stage (the helper only
+// forms U^T), MMA2 is dS^T = V_new^T Kd, the state update scales column i of
+// S^T by gamma_L[i], and the output is left to kda_out_kernel.
+template <bool KDA>
 __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_constant__ ScanArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
@@ -117,10 +124,11 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
   }
   const int kh = hv / a.G;
   const int c0 = a.seg_c0[seg], nch = a.seg_c1[seg] - c0;
-  const bool with_o = mode == 0 && a.o != nullptr;
+  const bool with_o = !KDA && mode == 0 && a.o != nullptr;
   const bool with_u = mode != 2;
   const bool with_vn = mode == 0 && a.vn != nullptr;   // V_new^T tiles for the backward
-  const uint32_t tx_bytes = mode == 0 ? (with_o ? 74752u : 50176u) : (mode == 1 ? 50176u : 25600u);
+  const uint32_t tx_bytes = KDA ? (with_u ? 58368u : 33792u)
+                                : (mode == 0 ? (with_o ? 74752u : 50176u) : (mode == 1 ? 50176u : 25600u));
   const uint32_t cb_bytes = mode == 2 ? 8192u : (with_o ? 24576u : 16384u);
   uint8_t* s_tile = sm + SC_S;
 
@@ -152,8 +160,19 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
     const int ci = c0 + n;
     uint8_t* st = sm + (n & 1) * SC_STAGE;
     uint64_t* bar = &full_bar[n & 1];
-    const uint8_t* cbp = a.cb + ((size_t)ci * a.HV + hv) * CB_BYTES;
     mbar_expect_tx(bar, tx_bytes);
+    if (KDA) {   // -W^T and Kd (contiguous in the block and in the stage), V, T'', gamma_L
+      const uint8_t* kbp = a.cb + ((size_t)ci * a.HV + hv) * KB_BYTES;
+      bulk_load(st + SC_K, kbp + KB_WT, 32768u, bar);
+      if (with_u) {
+        tma_load_3d(st + SC_V, &a.tv, 0, hv, t0, bar);
+        tma_load_3d(st + SC_V + 8192, &a.tv, 64, hv, t0, bar);
+        bulk_load(st + SC_TPP, kbp + KB_TPP, TILE64_BYTES, bar);
+      }
+      bulk_load(st + SC_SCAL, kbp + KB_SCAL, CB_SCAL_BYTES, bar);
+      return;
+    }
+    const uint8_t* cbp = a.cb + ((size_t)ci * a.HV + hv) * CB_BYTES;
     tma_load_3d(st + SC_K, &a.tk, 0, kh, t0, bar);
     tma_load_3d(st + SC_K + 8192, &a.tk, 64, kh, t0, bar);
     if (with_o) {
@@ -169,6 +188,17 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
   };
   auto prefetch = [&](int n) {   // the tiles of chunk n into L2, a stage ahead of their request
     const int ci = c0 + n, t0 = a.chunk_tok0[ci];
+    if (KDA) {
+      const uint8_t* kbp = a.cb + ((size_t)ci * a.HV + hv) * KB_BYTES;
+      bulk_prefetch(kbp + KB_WT, 32768u);
+      if (with_u) {
+        tma_prefetch_3d(&a.tv, 0, hv, t0);
+        tma_prefetch_3d(&a.tv, 64, hv, t0);
+        bulk_prefetch(kbp + KB_TPP, TILE64_BYTES);
+      }
+      bulk_prefetch(kbp + KB_SCAL, CB_SCAL_BYTES);
+      return;
+    }
     const uint8_t* cbp = a.cb + ((size_t)ci * a.HV + hv) * CB_BYTES;
     tma_prefetch_3d(&a.tk, 0, kh, t0);
     tma_prefetch_3d(&a.tk, 64, kh, t0);
@@ -204,15 +234,16 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
         if (!live) break;
         tc_fence_after();
         const uint32_t d1 = tb + TM_D1 + (n & 1) * 64;
+        const uint32_t b_w = KDA ? smem_u32(st + SC_K) : sm_w;   // -W^T: the stage's (KDA) or the helper's
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          mma_ss_w(d1, desc_k(sm_s, 128, ks), desc_mn(sm_w, 128, ks), idesc(128, 64, 0, 1),
+          mma_ss_w(d1, desc_k(sm_s, 128, ks), desc_mn(b_w, 128, ks), idesc(128, 64, 0, 1),
                    (with_u || ks > 0) ? 1u : 0u);
         mma_commit_w(&bar_m1);
         // MMA2: dS^T = (V_new^T diag(kd)) K; then O^T = S^T Q'^T + V_new^T Aqk^T (into O[n & 1])
         if (!(live = mbar_wait(&go2, n & 1, a.err))) break;
         tc_fence_after();
-        const uint32_t a_k = smem_u32(st + SC_K);
+        const uint32_t a_k = smem_u32(st + (KDA ? SC_Q : SC_K));   // K (scaled by kd in the A operand), or Kd
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           mma_ts_w(tb + TM_DS, tb + TM_AVS + ks * 8, desc_mn(a_k, 64, ks), idesc(128, 128, 0, 1), ks > 0);
@@ -321,8 +352,8 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int r = q * 16 + 2 * e;
-            ps[e] = pack_bf16(vn[r] * kd[r], vn[r + 1] * kd[r + 1]);
             pn[e] = pack_bf16(vn[r], vn[r + 1]);
+            ps[e] = KDA ? pn[e] : pack_bf16(vn[r] * kd[r], vn[r + 1] * kd[r + 1]);
           }
           tmem_st8(taddr(tb, wq * 32, TM_AVS + q * 8), ps);
           if (with_o) tmem_st8(taddr(tb, wq * 32, TM_AVN + q * 8), pn);
@@ -355,9 +386,22 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
         for (int h = 0; h < 4; ++h) {
           float ds[32];
           tmem_ld32(taddr(tb, wq * 32, TM_DS + h * 32), ds);
+          if (KDA) {   // column i (key channel) decays by gamma_L[i]
 #pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            fma2_to(S[h * 32 + e], S[h * 32 + e + 1], gL, S[h * 32 + e], S[h * 32 + e + 1], ds[e], ds[e + 1]);
+            for (int e = 0; e < 32; e += 4) {
+              const float4 gv = *reinterpret_cast<const float4*>(scal + h * 32 + e);
+              fma2v(ds[e], ds[e + 1], gv.x, gv.y, S[h * 32 + e], S[h * 32 + e + 1]);
+              fma2v(ds[e + 2], ds[e + 3], gv.z, gv.w, S[h * 32 + e + 2], S[h * 32 + e + 3]);
+              S[h * 32 + e] = ds[e];
+              S[h * 32 + e + 1] = ds[e + 1];
+              S[h * 32 + e + 2] = ds[e + 2];
+              S[h * 32 + e + 3] = ds[e + 3];
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2)
+              fma2_to(S[h * 32 + e], S[h * 32 + e + 1], gL, S[h * 32 + e], S[h * 32 + e + 1], ds[e], ds[e + 1]);
+          }
         }
         if (with_o && !mbar_wait(&bar_o[n & 1], (n >> 1) & 1, a.err)) ok = false;
         store_state_row(s_tile, lt, S);   // also the saved state entering the next chunk
@@ -398,7 +442,13 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
       ok = wg_sync_and(2, mbar_wait(&full_bar[n & 1], (n >> 1) & 1, a.err));
       if (!ok) break;
       const int L = reinterpret_cast<const int*>(st + SC_SCAL)[129];
-      if (L < CH) {   // zero the rows past a document end (they hold the next document)
+      if (KDA && L < CH && with_u) {   // zero the V rows past a document end (-W^T, Kd are zero there)
+        for (int idx = lt; idx < (CH - L) * 16; idx += 128)
+          *reinterpret_cast<uint4*>(st + SC_V + sw_chunk(L + (idx >> 4), idx & 15, 64)) = make_uint4(0u, 0u, 0u, 0u);
+        fence_async_smem();
+        named_bar(2, 128);
+      }
+      if (!KDA && L < CH) {   // zero the rows past a document end (they hold the next document)
         for (int idx = lt; idx < (CH - L) * 48; idx += 128) {
           const int t = idx / 48, rem = idx % 48, tile = rem / 16, c8 = rem % 16;
           const int off = tile == 0 ? SC_K : (tile == 1 ? SC_Q : SC_V);
@@ -410,7 +460,22 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
       // MMA1(n - 1) has read the -W^T tile and the chain is done with D1[n & 1] (V_new^T of n - 2)
       if (n > 0 && !(ok = wg_sync_and(2, mbar_wait(&bar_m1, (n - 1) & 1, a.err)))) break;
       tc_fence_after();
-      if (warp == 4) {
+      if (KDA) {   // U^T = V^T T''^T -> D1[n & 1] (-W^T came with the stage)
+        if (with_u) {
+          if (warp == 4) {
+            const uint32_t a_v = smem_u32(st + SC_V), a_tpp = smem_u32(st + SC_TPP);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_ss_w(tb + TM_D1 + (n & 1) * 64, desc_mn(a_v, 64, ks), desc_k(a_tpp, 64, ks),
+                       idesc(128, 64, 1, 0), ks > 0);
+            mma_commit_w(&bar_wu);
+          }
+          if (!(ok = wg_sync_and(2, mbar_wait(&bar_wu, n & 1, a.err)))) break;
+          tc_fence_before();
+        }
+        named_bar(2, 128);
+        if (tid == 128) mbar_arrive(&bar_wr);
+      } else if (warp == 4) {
         const uint32_t a_k = smem_u32(st + SC_K), a_v = smem_u32(st + SC_V);
         const uint32_t a_tp = smem_u32(st + SC_TP), a_tpp = smem_u32(st + SC_TPP);
 #pragma unroll
@@ -441,6 +506,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
           *p = v;
         }
       }
+      if (!KDA) {
       if (!(ok = wg_sync_and(2, mbar_wait(&bar_wu, n & 1, a.err)))) break;
       tc_fence_after();
       {  // -W^T -> shared (row lt = dk index), the MN-major B operand of MMA1
@@ -462,6 +528,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
       tc_fence_before();
       named_bar(2, 128);
       if (tid == 128) mbar_arrive(&bar_wr);
+      }
       // ---- chunk n + 1 into the stage of chunk n - 1 once the chain no longer reads it
       if (n > 0 && n + 1 < nch) {
         if (!(ok = wg_sync_and(2, mbar_wait(&bar_sf, (n - 1) & 1, a.err)))) break;
@@ -552,7 +619,8 @@ void launch_fwd_scan(const ScanArgs& a, int nchains, cudaStream_t s) {
   if (nchains <= 0) return;
   const int id = a.walk ? K_FWD_WALK : K_FWD_SCAN;
   prof_begin(id, s);
-  fwd_scan_kernel<<<nchains, SC_THREADS, SC_SMEM_ALLOC, s>>>(a);
+  if (a.kda) fwd_scan_kernel<true><<<nchains, SC_THREADS, SC_SMEM_ALLOC, s>>>(a);
+  else fwd_scan_kernel<false><<<nchains, SC_THREADS, SC_SMEM_ALLOC, s>>>(a);
   prof_end(id, s);
 }
 void launch_merge(const MergeArgs& a, int nsdoc, cudaStream_t s) {
@@ -562,7 +630,8 @@ void launch_merge(const MergeArgs& a, int nsdoc, cudaStream_t s) {
   prof_end(K_FWD_MERGE, s);
 }
 void setup_fwd_scan_attrs() {
-  cudaFuncSetAttribute(fwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_SMEM_ALLOC);
+  cudaFuncSetAttribute(fwd_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_SMEM_ALLOC);
+  cudaFuncSetAttribute(fwd_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_SMEM_ALLOC);
   cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 128 * 129 * 4);
 }
 

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "gdn.h"
+
 namespace gdn {
 
 constexpr int CHUNK = 64;   // tokens per chunk
@@ -21,6 +23,18 @@ constexpr int CB_SCAL = 32768;   // float sc[64], kd[64], gL, (int) L
 constexpr int CB_SCAL_BYTES = 1024;
 constexpr int CB_BYTES = 33792;
 constexpr int TILE64_BYTES = 8192;
+
+// ---- per (chunk, value head) block of the per-channel-decay (KDA) form, written by kda_prep_kernel ----
+// With G the chunk-local cumulative log decay per key channel (a 64 x 128 array), gamma = exp(G):
+constexpr int KB_WT = 0;         // -W^T = -(T'' (gamma . K^))^T, BF16 SwTile(128 x 64) (rows: dk index)
+constexpr int KB_KD = 16384;     // Kd = exp(G_L - G) . K^, BF16 SwTile(64 x 128)
+constexpr int KB_TPP = 32768;    // T'' = T diag(beta), SwTile(64 x 64)
+constexpr int KB_SCAL = 40960;   // float gamma_L[128] (per key channel); (int) L at float index 129
+constexpr int KB_QT = 41984;     // Q~ = gamma . Q^, SwTile(64 x 128)
+constexpr int KB_AQK = 58368;    // P = tril_incl(Q^_r . (exp(G_r - G_c) . K^_c)), SwTile(64 x 64)
+constexpr int KB_T = 66560;      // T = (I + A)^-1, SwTile(64 x 64)
+constexpr int KB_MT = 74752;     // M^T, M = strict_tril(K^_r . (exp(G_r - G_c) . K^_c)), SwTile(64 x 64)
+constexpr int KB_BYTES = 82944;
 
 // one saved state: BF16 S^T (dv rows x dk cols) as SwTile(128 x 128)
 constexpr int STATE_BYTES = 32768;
@@ -130,6 +144,33 @@ struct ScanArgs {
   const int* seg_offsets;     // [N+1]
   const float* s_in;          // [N][HV][128][128] FP32 S entering each document, or null (zero)
   float* s_out;               // [N][HV][128][128] FP32 S leaving each document, or null
+  int kda;                    // 1: per-channel decay; cb holds KB_BYTES blocks (-W^T, Kd, T'', gamma_L)
+  int* err;
+};
+
+// the per-channel-decay preparation of every (chunk, value head)
+struct KdaPrepArgs {
+  CUtensorMap tq, tk;
+  const float* g;             // [T][HV][128] log decay per key channel
+  const float* beta;          // [T][HV]
+  const int* chunk_tok0;
+  const int* chunk_len;
+  uint8_t* kb;                // [NC][HV][KB_BYTES] out
+  int H, HV, G, l2norm;
+  int* err;
+};
+
+// o = scale (Q~ S + P V_new) of every (chunk, value head), from the states and V_new^T
+struct KdaOutArgs {
+  CUtensorMap to;
+  const uint8_t* tape;        // [NC][HV][STATE_BYTES] S^T entering each chunk
+  const uint8_t* vn;          // [NC][HV][VN_BYTES] V_new^T
+  const uint8_t* kb;          // [NC][HV][KB_BYTES]
+  const int* chunk_tok0;
+  const int* chunk_len;
+  __nv_bfloat16* o;
+  int HV;
+  float scale;
   int* err;
 };
 
@@ -178,6 +219,7 @@ struct Plan {
   size_t o_cb, o_bend, o_sinit, o_mend_ws;
   size_t o_dtape, o_dvn, o_dbend, o_dsinit;   // backward
   size_t o_vnb;                               // backward, replay form: recomputed V_new^T tiles
+  size_t o_ktape, o_kvn;                      // KDA forward without a saved set: its tape and V_new^T
   size_t ws_fwd, ws_bwd;
   // saved offsets
   size_t s_tape, s_mseg, s_cb, s_vn, saved_bytes;
@@ -191,5 +233,16 @@ inline Tables tables_at(const Plan& P, uint8_t* ws) {
   for (int i = 0; i < 16; ++i) *f[i] = reinterpret_cast<int*>(ws + P.o_tables[i]);
   return t;
 }
+
+// ---- host layer (gdn_api.cu) pieces that the KDA entry points (gdn_kda.cu) share ----
+gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P);
+gdn_status make_kda_plan(const gdn_problem* p, const int32_t* cu, Plan* P);
+bool device_setup();
+bool aligned16(const void* p);
+bool make_tmap(CUtensorMap* m, const void* base, int64_t T, int heads);
+gdn_status run_tables(const Plan& P, const gdn_problem* p, const int32_t* cu_dev, uint8_t* ws, void* saved,
+                      cudaStream_t s);
+void launch_fwd_scan(const ScanArgs& a, int nchains, cudaStream_t s);
+void launch_merge(const MergeArgs& a, int nsdoc, cudaStream_t s);
 
 }  // namespace gdn

@@ -104,34 +104,8 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
   uint32_t tph = 0;   // phase of bar_t (four products per value head)
   int t_pend = -1;    // error path: phase of a product whose completion was not seen (-1: none)
   float* Sm = reinterpret_cast<float*>(sm + PR_S);
-  const uint32_t s_d = smem_u32(sm + PR_D), s_lx = smem_u32(sm + PR_LX), s_n = smem_u32(sm + PR_N),
-                 s_n2 = smem_u32(sm + PR_N2);
-  // this thread's 32 elements of an M = 64 result (the .16x256b lane map): rows r0, r0 + 8, columns
-  // 16 g + cq, cq + 1, cq + 8, cq + 9 for g = 0..3
-  const int r0 = 16 * warp + (lane >> 2), cq = 2 * (lane & 3);
-  auto ld_result = [&](uint32_t (&u)[4][8]) {   // the inverse's current product, FP32 bits
-#pragma unroll
-    for (int g = 0; g < 4; ++g) tmem_ld_m64_async(taddr(tb, warp * 32, PT_INV + 16 * g), u[g]);
-    tmem_wait_ld();
-  };
-  auto product = [&](uint32_t a_tile, uint32_t b_tile, bool b_mn) -> bool {   // D(TMEM) = A B, M = N = K = 64
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 0) {
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss_w(tb + PT_INV, desc_k(a_tile, 64, ks), b_mn ? desc_mn(b_tile, 64, ks) : desc_k(b_tile, 64, ks),
-                 idesc(64, 64, 0, b_mn ? 1 : 0), ks > 0);
-      mma_commit_w(&bar_t);
-    }
-    const bool r = __syncthreads_and(mbar_wait(&bar_t, tph, a.err));
-    if (!r) t_pend = (int)tph;
-    tph ^= 1;
-    tc_fence_after();
-    return r;
-  };
+  const UtInvTiles tiles{sm + PR_D, sm + PR_LX, sm + PR_N, sm + PR_N2};
+  const int r0 = 16 * warp + (lane >> 2), cq = 2 * (lane & 3);   // this thread's elements of T (see ut_ld_result)
   for (int hh = 0; hh < a.G; ++hh) {
     const int hv = j * a.G + hh;
     if (warp == 3) {   // ---- gates (log2 units), then the next head's loads
@@ -152,75 +126,10 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
     }
     __syncthreads();
     if (!ok) continue;
-    {  // ---- D and L^T as BF16 tiles from rows of the array: row n of it holds T_bb (columns of n's
-       // block, zero above the diagonal) and, in the later blocks' columns c, A[c][n] = L^T[n][c]
-      uint4 dch[4], lch[4];
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int item = tid + PR_THREADS * it, n = item >> 3, c8 = item & 7;
-        const float4 u0 = *reinterpret_cast<const float4*>(Sm + n * UT_ALD + 8 * c8);
-        const float4 u1 = *reinterpret_cast<const float4*>(Sm + n * UT_ALD + 8 * c8 + 4);
-        const uint4 w = make_uint4(pack_bf16(u0.x, u0.y), pack_bf16(u0.z, u0.w), pack_bf16(u1.x, u1.y),
-                                   pack_bf16(u1.z, u1.w));
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-        const int bn = n >> 4, bc = c8 >> 1;
-        dch[it] = bc == bn ? w : z;
-        lch[it] = bc > bn ? w : z;
-      }
-      __syncthreads();   // the array is read: its space takes the tiles
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int item = tid + PR_THREADS * it, n = item >> 3, c8 = item & 7;
-        *reinterpret_cast<uint4*>(sm + PR_D + sw_chunk(n, c8, 64)) = dch[it];
-        *reinterpret_cast<uint4*>(sm + PR_LX + sw_chunk(n, c8, 64)) = lch[it];
-      }
-    }
+    ok = ut_tc_inverse(Sm, tiles, tb, PT_INV, &bar_t, tph, a.err, t_pend);
     uint32_t u[4][8];
-    // (a K-major B tile is rows N, columns K; L^T is that form of L.  An MN-major B tile is rows K,
-    // columns N: a row-major N or D.)
-    ok = product(s_d, s_lx, false);   // N = D L
-    if (ok) {  // N -> BF16 tile
-      ld_result(u);
-#pragma unroll
-      for (int g = 0; g < 4; ++g)
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * g + 8 * (i >> 2) + cq;
-          *reinterpret_cast<uint32_t*>(sm + PR_N + sw_off(r, cc, 64)) =
-              pack_bf16(__uint_as_float(u[g][i]), __uint_as_float(u[g][i + 1]));
-        }
-    }
-    ok = ok && product(s_n, s_n, true);   // N^2 = N N
-    if (ok) {
-      ld_result(u);
-#pragma unroll
-      for (int g = 0; g < 4; ++g)
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * g + 8 * (i >> 2) + cq;
-          *reinterpret_cast<uint32_t*>(sm + PR_N2 + sw_off(r, cc, 64)) =
-              pack_bf16(__uint_as_float(u[g][i]), __uint_as_float(u[g][i + 1]));
-        }
-    }
-    ok = ok && product(s_n2, s_n, true);   // N^3 = N^2 N
-    if (ok) {  // X = I - N + N^2 - N^3 -> BF16 tile (over L^T, which N = D L has finished reading)
-      ld_result(u);
-#pragma unroll
-      for (int g = 0; g < 4; ++g)
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * g + 8 * (i >> 2) + cq;
-          const uint32_t off = sw_off(r, cc, 64);
-          const float2 n1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sm + PR_N + off));
-          const float2 n2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sm + PR_N2 + off));
-          const float x0 = (r == cc ? 1.f : 0.f) - n1.x + n2.x - __uint_as_float(u[g][i]);
-          const float x1 = (r == cc + 1 ? 1.f : 0.f) - n1.y + n2.y - __uint_as_float(u[g][i + 1]);
-          *reinterpret_cast<uint32_t*>(sm + PR_LX + off) = pack_bf16(x0, x1);
-        }
-    }
-    ok = ok && product(s_lx, s_d, true);   // T = X D
     if (ok) {  // T', T'', T tiles (over D, X, N: the last product has read them)
-      ld_result(u);
+      ut_ld_result(tb, PT_INV, warp, u);
 #pragma unroll
       for (int g = 0; g < 4; ++g)
 #pragma unroll

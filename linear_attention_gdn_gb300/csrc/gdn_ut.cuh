@@ -65,7 +65,7 @@ __device__ __forceinline__ void ut_zero_tail(uint8_t* kq, int L, int lt) {
 // L2 norm of row lt of the [K; Q] tile: four partial sums of 32 elements (each the sum of its even-
 // and its odd-element chain, the two run as paired FMAs), combined as (p0 + p1) + (p2 + p3).  The
 // gradient kernel sums in the same order.
-__device__ __forceinline__ void ut_norm_row(const uint8_t* kq, int lt, int l2norm, UtTok& u) {
+__device__ __forceinline__ float ut_row_rnorm(const uint8_t* kq, int lt, int l2norm) {
   float pr[4];
 #pragma unroll
   for (int qq = 0; qq < 4; ++qq) {
@@ -83,7 +83,10 @@ __device__ __forceinline__ void ut_norm_row(const uint8_t* kq, int lt, int l2nor
     pr[qq] = se + so;
   }
   const float ss = (pr[0] + pr[1]) + (pr[2] + pr[3]);
-  const float rn = l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+  return l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+}
+__device__ __forceinline__ void ut_norm_row(const uint8_t* kq, int lt, int l2norm, UtTok& u) {
+  const float rn = ut_row_rnorm(kq, lt, l2norm);
   if (lt < 64) u.rk[lt] = rn;
   else u.rq[lt - 64] = rn;
 }
@@ -258,6 +261,125 @@ __device__ __forceinline__ void ut_diag_blocks(float* Sm, int l, int bar_id) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) Sm[(o + i) * UT_ALD + o + cc] = x[i];   // x[i] = 0 above the diagonal
   }
+}
+
+// ---------------------------------------------------------------------------
+// The rest of T = (I + A)^-1 on the tensor cores, after ut_diag_blocks.  With D the inverted 16 x 16
+// diagonal blocks and L the strictly block-lower part of A,
+//   I + A = D^-1 (I + N),  N = D L,  N^4 = 0   =>   T = (I - N + N^2 - N^3) D,
+// four dependent M = 64 tcgen05 products (BF16 operands, FP32 accumulation).  Run by all 128 threads
+// of the CTA; thread 0 issues.  The FP32 array Sm (row n: T_bb in n's block, A[c][n] in the later
+// blocks' columns c) is read into registers before the tiles are written, so tiles d and lx may lie
+// over it; n and n2 are written after the first product.  T is left in TMEM columns inv .. inv + 63
+// (M = 64 layout; read it with ut_ld_result).  tph is the phase of `bar`; t_pend receives the phase
+// of a product whose completion was not seen when a wait runs out (the caller drains it).
+// ---------------------------------------------------------------------------
+struct UtInvTiles {
+  uint8_t* d;    // D, SwTile(64 x 64)
+  uint8_t* lx;   // L^T, then X = I - N + N^2 - N^3
+  uint8_t* n;    // N
+  uint8_t* n2;   // N^2
+};
+
+// This thread's 32 elements of an M = 64, N = 64 result at TMEM column `col` (the .16x256b lane map):
+// u[g][i] is row 16 warp + lane / 4 + 8 ((i >> 1) & 1), column 16 g + 8 (i >> 2) + 2 (lane % 4) + (i & 1).
+__device__ __forceinline__ void ut_ld_result(uint32_t tb, int col, int warp, uint32_t (&u)[4][8]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) tmem_ld_m64_async(taddr(tb, warp * 32, col + 16 * g), u[g]);
+  tmem_wait_ld();
+}
+
+__device__ __forceinline__ bool ut_tc_inverse(const float* Sm, const UtInvTiles& tl, uint32_t tb, int inv,
+                                              uint64_t* bar, uint32_t& tph, int* err, int& t_pend) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r0 = 16 * warp + (lane >> 2), cq = 2 * (lane & 3);
+  {  // D and L^T as BF16 tiles from rows of the array: row n holds T_bb (columns of n's block, zero
+     // above the diagonal) and, in the later blocks' columns c, A[c][n] = L^T[n][c]
+    uint4 dch[4], lch[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int item = tid + 128 * it, n = item >> 3, c8 = item & 7;
+      const float4 u0 = *reinterpret_cast<const float4*>(Sm + n * UT_ALD + 8 * c8);
+      const float4 u1 = *reinterpret_cast<const float4*>(Sm + n * UT_ALD + 8 * c8 + 4);
+      const uint4 w = make_uint4(pack_bf16(u0.x, u0.y), pack_bf16(u0.z, u0.w), pack_bf16(u1.x, u1.y),
+                                 pack_bf16(u1.z, u1.w));
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      const int bn = n >> 4, bc = c8 >> 1;
+      dch[it] = bc == bn ? w : z;
+      lch[it] = bc > bn ? w : z;
+    }
+    __syncthreads();   // the array is read: its space takes the tiles
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int item = tid + 128 * it, n = item >> 3, c8 = item & 7;
+      *reinterpret_cast<uint4*>(tl.d + sw_chunk(n, c8, 64)) = dch[it];
+      *reinterpret_cast<uint4*>(tl.lx + sw_chunk(n, c8, 64)) = lch[it];
+    }
+  }
+  auto product = [&](const uint8_t* a_tile, const uint8_t* b_tile, bool b_mn) -> bool {   // TMEM = A B
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) {
+      const uint32_t sa = smem_u32(a_tile), sb = smem_u32(b_tile);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ss_w(tb + inv, desc_k(sa, 64, ks), b_mn ? desc_mn(sb, 64, ks) : desc_k(sb, 64, ks),
+                 idesc(64, 64, 0, b_mn ? 1 : 0), ks > 0);
+      mma_commit_w(bar);
+    }
+    const bool r = __syncthreads_and(mbar_wait(bar, tph, err));
+    if (!r) t_pend = (int)tph;
+    tph ^= 1;
+    tc_fence_after();
+    return r;
+  };
+  uint32_t u[4][8];
+  // (a K-major B tile is rows N, columns K; L^T is that form of L.  An MN-major B tile is rows K,
+  // columns N: a row-major N or D.)
+  bool ok = product(tl.d, tl.lx, false);   // N = D L
+  if (ok) {  // N -> BF16 tile
+    ut_ld_result(tb, inv, warp, u);
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * g + 8 * (i >> 2) + cq;
+        *reinterpret_cast<uint32_t*>(tl.n + sw_off(r, cc, 64)) =
+            pack_bf16(__uint_as_float(u[g][i]), __uint_as_float(u[g][i + 1]));
+      }
+  }
+  ok = ok && product(tl.n, tl.n, true);   // N^2 = N N
+  if (ok) {
+    ut_ld_result(tb, inv, warp, u);
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * g + 8 * (i >> 2) + cq;
+        *reinterpret_cast<uint32_t*>(tl.n2 + sw_off(r, cc, 64)) =
+            pack_bf16(__uint_as_float(u[g][i]), __uint_as_float(u[g][i + 1]));
+      }
+  }
+  ok = ok && product(tl.n2, tl.n, true);   // N^3 = N^2 N
+  if (ok) {  // X = I - N + N^2 - N^3 -> BF16 tile (over L^T, which N = D L has finished reading)
+    ut_ld_result(tb, inv, warp, u);
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * g + 8 * (i >> 2) + cq;
+        const uint32_t off = sw_off(r, cc, 64);
+        const float2 n1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(tl.n + off));
+        const float2 n2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(tl.n2 + off));
+        const float x0 = (r == cc ? 1.f : 0.f) - n1.x + n2.x - __uint_as_float(u[g][i]);
+        const float x1 = (r == cc + 1 ? 1.f : 0.f) - n1.y + n2.y - __uint_as_float(u[g][i + 1]);
+        *reinterpret_cast<uint32_t*>(tl.lx + off) = pack_bf16(x0, x1);
+      }
+  }
+  ok = ok && product(tl.lx, tl.d, true);   // T = X D
+  return ok;
 }
 
 }  // namespace gdn

@@ -134,6 +134,35 @@ def generate(w: Workload, device="cpu", with_grad=True) -> dict:
     return out
 
 
+def generate_kda(w: Workload, device="cpu", with_grad=True) -> dict:
+    """Inputs of the per-channel-decay (KDA) form for workload `w`: as generate(),
+    except g [T,HV,dk] FP32, one log decay per key channel,
+    g = logsigmoid(U(g_lo, g_hi)) drawn per (token, v-head, channel)."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed)
+    T, H, HV = w.T, w.H, w.HV
+
+    def normal(shape):
+        return torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+
+    q = normal((T, H, w.dk))
+    k = normal((T, H, w.dk))
+    if w.prenorm_qk:
+        q = q / q.norm(dim=-1, keepdim=True)
+        k = k / k.norm(dim=-1, keepdim=True)
+    q = q.to(torch.bfloat16)
+    k = k.to(torch.bfloat16)
+    v = normal((T, HV, w.dv)).to(torch.bfloat16)
+    x = torch.rand((T, HV, w.dk), generator=gen, device=dev, dtype=torch.float32)
+    g = torch.nn.functional.logsigmoid(w.g_lo + (w.g_hi - w.g_lo) * x)
+    beta = torch.sigmoid(normal((T, HV)))
+    out = dict(q=q, k=k, v=v, g=g, beta=beta, cu_seqlens=w.cu_seqlens)
+    if with_grad:
+        out["dO"] = normal((T, HV, w.dv)).to(torch.bfloat16)
+    return out
+
+
 def conv_inputs(doc_lens, C: int, W: int = 4, seed: int = 0, with_bias: bool = True) -> dict:
     """Seeded inputs of the causal conv1d + SiLU front: x, dy [T, C] ~ N(0, 1) in
     BF16; taps w [C, W] ~ N(0, 0.5^2) and bias b [C] ~ N(0, 0.1^2) in FP32 (the

@@ -1,0 +1,131 @@
+"""GPU parity of the per-channel-decay (KDA) path against the FP64 KDA oracle
+(oracle/kda.py), through the C ABI (gdn_kda_fwd / gdn_kda_bwd)."""
+import numpy as np
+import pytest
+import torch
+
+from linear_attention_gdn_gb300 import inputs
+from oracle import kda, tables
+from tests.gdn_testutil import compare, decode_tape, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _f64(x):
+    return x.detach().to("cpu", torch.float64).numpy()
+
+
+def oracle_kda(w, d, with_grad=False, chunk_states=False):
+    """Whole documents, every q/k group: o (and gradients) token-major, and with
+    chunk_states the state entering every chunk [NC, HV, dk, dv]."""
+    cu = w.cu_seqlens
+    G = w.HV // w.H
+    T = w.T
+    out = dict(o=np.zeros((T, w.HV, 128)))
+    if with_grad:
+        out.update(dq=np.zeros((T, w.H, 128)), dk=np.zeros((T, w.H, 128)), dv=np.zeros((T, w.HV, 128)),
+                   dg=np.zeros((T, w.HV, 128)), dbeta=np.zeros((T, w.HV)))
+    t = tables.chunk_tables(cu)
+    tape = np.zeros((w.num_chunks, w.HV, 128, 128)) if chunk_states else None
+    for doc in range(w.N):
+        s, e = int(cu[doc]), int(cu[doc + 1])
+        if e == s:
+            continue
+        for j in range(w.H):
+            hs = slice(j * G, (j + 1) * G)
+            q = _f64(d["q"][s:e, j])
+            k = _f64(d["k"][s:e, j])
+            v = _f64(d["v"][s:e, hs]).transpose(1, 0, 2).copy()
+            g = _f64(d["g"][s:e, hs]).transpose(1, 0, 2).copy()
+            beta = _f64(d["beta"][s:e, hs]).T.copy()
+            dO = _f64(d["dO"][s:e, hs]).transpose(1, 0, 2).copy() if with_grad else None
+            r = kda.group(q, k, v, g, beta, dO, l2norm=w.l2norm, scale=w.scale)
+            out["o"][s:e, hs] = r["o"].transpose(1, 0, 2)
+            if with_grad:
+                out["dq"][s:e, j] = r["dq"]
+                out["dk"][s:e, j] = r["dk"]
+                out["dv"][s:e, hs] = r["dv"].transpose(1, 0, 2)
+                out["dg"][s:e, hs] = r["dg"].transpose(1, 0, 2)
+                out["dbeta"][s:e, hs] = r["dbeta"].T
+            if chunk_states:
+                cf = kda.chunk_forward(q, k, v, g, beta, l2norm=w.l2norm, scale=w.scale)
+                c0 = t["chunk_offsets"][doc]
+                tape[c0:c0 + cf["S"].shape[0], hs] = cf["S"]
+    return out, tape
+
+
+def run_kda_fwd(w, d, save=True):
+    import linear_attention_gdn_gb300 as gdn
+    prob = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm, w.segments)
+    buf = gdn.Buffers(prob, w.cu_seqlens, fill=255, kda=True)
+    o = torch.full((w.T, w.HV, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_kda_fwd(prob, d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_dev"], w.cu_seqlens, o,
+                    buf.saved if save else None, buf.workspace)
+    st = gdn.gdn_device_status(buf.workspace)
+    torch.cuda.synchronize()
+    return prob, buf, o, st
+
+
+# per-channel decays logsigmoid(U(g_lo, g_hi)): from about -1.3 per token (fast channels) to almost 1
+KDA_CASES = [
+    ("tiny", inputs.custom([128, 192], 2, 4, g_lo=-1.0, g_hi=6.0, seed=21)),
+    ("ragged_g3", inputs.custom([1, 63, 64, 65, 0, 130, 200], 2, 6, g_lo=-1.0, g_hi=6.0, seed=22)),
+    ("nol2_g1", inputs.custom([100, 28], 1, 1, l2norm=False, prenorm_qk=True, g_lo=-1.0, g_hi=6.0, seed=23)),
+    ("split4", inputs.custom([1000, 70], 1, 2, g_lo=0.0, g_hi=6.0, seed=24, segments=4)),
+    # about -4 per token on every channel: 16 tokens decay by 2^-95, just inside the factored range
+    ("steep", inputs.custom([150, 64, 1, 97], 1, 3, g_lo=-4.1, g_hi=-3.9, seed=25)),
+]
+
+
+@pytest.mark.parametrize("name,w", KDA_CASES, ids=[c[0] for c in KDA_CASES])
+def test_kda_forward_parity(name, w):
+    d = to_dev(inputs.generate_kda(w, "cpu", with_grad=False))
+    prob, buf, o, st = run_kda_fwd(w, d)
+    assert st == 0
+    r, ref_tape = oracle_kda(w, {n: (x.cpu() if hasattr(x, "cpu") else x) for n, x in d.items()},
+                             chunk_states=True)
+    compare(f"kda/{name}/o", o.double().cpu().numpy(), r["o"])
+    tape = decode_tape(buf.saved, w.num_chunks, w.HV)
+    compare(f"kda/{name}/tape", tape, ref_tape)
+
+
+def test_kda_forward_without_saved_set():
+    w = KDA_CASES[1][1]
+    d = to_dev(inputs.generate_kda(w, "cpu", with_grad=False))
+    _, _, o1, st1 = run_kda_fwd(w, d, save=True)
+    _, _, o2, st2 = run_kda_fwd(w, d, save=False)
+    assert st1 == 0 and st2 == 0
+    assert torch.equal(o1, o2)
+
+
+def test_kda_uniform_decay_matches_gdn():
+    """A decay equal on every key channel is the GDN recurrence: gdn_kda_fwd with g repeated over the
+    channels agrees with gdn_fwd (different kernels, so within the accuracy budget, not bitwise)."""
+    import linear_attention_gdn_gb300 as gdn
+    w = inputs.custom([300, 64, 129], 2, 4, g_lo=0.0, g_hi=6.0, seed=26)
+    d = to_dev(inputs.generate(w, "cpu", with_grad=False))
+    prob = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm)
+    buf = gdn.Buffers(prob, w.cu_seqlens)
+    o_gdn = torch.empty((w.T, w.HV, 128), dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_fwd(prob, d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_dev"], w.cu_seqlens, o_gdn, None,
+                buf.workspace)
+    dk = dict(d)
+    dk["g"] = d["g"][:, :, None].expand(w.T, w.HV, 128).contiguous()
+    _, _, o_kda, st = run_kda_fwd(w, dk, save=False)
+    assert st == 0 and gdn.gdn_device_status(buf.workspace) == 0
+    compare("kda_vs_gdn/o", o_kda.double().cpu().numpy(), o_gdn.double().cpu().numpy())
+
+
+def test_kda_gate_range_refused():
+    """A channel decaying by more than 2^-96 within 16 tokens is refused on the device with
+    GDN_ERR_GATE_RANGE; the call returns and the context stays usable."""
+    import linear_attention_gdn_gb300 as gdn
+    w = inputs.custom([96, 64], 1, 2, g_lo=-5.5, g_hi=-5.0, seed=27)
+    d = to_dev(inputs.generate_kda(w, "cpu", with_grad=False))
+    _, _, _, st = run_kda_fwd(w, d)
+    assert st == 8, gdn.STATUS.get(st, st)
+    # the next call on a fresh workspace is unaffected
+    w2 = KDA_CASES[0][1]
+    d2 = to_dev(inputs.generate_kda(w2, "cpu", with_grad=False))
+    _, _, _, st2 = run_kda_fwd(w2, d2)
+    assert st2 == 0
