@@ -257,6 +257,11 @@ gdn_status gdn_kda_fwd(const gdn_problem *prob, const void *q, const void *k, co
                        const float *g, const float *beta, const int32_t *cu_seqlens_dev,
                        const int32_t *cu_seqlens_host, void *o, void *saved, void *workspace,
                        size_t ws_bytes, struct CUstream_st *stream);
+gdn_status gdn_kda_bwd(const gdn_problem *prob, const void *q, const void *k, const void *v,
+                       const float *g, const float *beta, const int32_t *cu_seqlens_dev,
+                       const int32_t *cu_seqlens_host, const void *dO, const void *saved, void *dq,
+                       void *dk, void *dv, float *dg, float *dbeta, void *workspace, size_t ws_bytes,
+                       struct CUstream_st *stream);
 
 /* Static description of a status code. */
 const char *gdn_status_string(gdn_status s);

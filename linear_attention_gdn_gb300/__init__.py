@@ -23,7 +23,8 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "G
 EXPORTS = ("gdn_saved_bytes", "gdn_fwd", "gdn_bwd", "gdn_ckpt_fwd_bwd", "gdn_status_string",
            "gdn_device_status", "gdn_plan_segment_chunks", "gdn_chunk_table_offsets", "gdn_profile_enable",
            "gdn_profile_read", "gdn_fwd_noalloc", "gdn_fwd_states", "gdn_bwd_states", "gdn_conv1d_workspace_bytes",
-           "gdn_conv1d_fwd", "gdn_conv1d_bwd", "gdn_backward_tape_offsets", "gdn_kda_saved_bytes", "gdn_kda_fwd")
+           "gdn_conv1d_fwd", "gdn_conv1d_bwd", "gdn_backward_tape_offsets", "gdn_kda_saved_bytes", "gdn_kda_fwd",
+           "gdn_kda_bwd")
 SAVED_FULL, SAVED_REPLAY = 0, 1   # gdn_problem.saved_form
 
 
@@ -79,6 +80,7 @@ def _load():
     L.gdn_backward_tape_offsets.argtypes = [pp, i32p, ctypes.POINTER(sz)]
     L.gdn_kda_saved_bytes.argtypes = [pp, i32p, ctypes.POINTER(sz), ctypes.POINTER(sz)]
     L.gdn_kda_fwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, sz, vp]
+    L.gdn_kda_bwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.gdn_fwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, i32p, i32p, vp, vp]
     L.gdn_fwd_noalloc.restype = ctypes.c_int
     cp = ctypes.POINTER(gdn_conv_problem)
@@ -206,6 +208,17 @@ def gdn_kda_fwd(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, o, save
     _check(lib.gdn_kda_fwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                            ctypes.cast(_ptr(cu_seqlens_dev), ctypes.POINTER(ctypes.c_int32)), cup, _ptr(o),
                            _ptr(saved), _ptr(workspace), ws_bytes, _stream(stream)), "gdn_kda_fwd")
+
+
+def gdn_kda_bwd(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, dO, saved, dq, dk, dv, dg, dbeta,
+                workspace, ws_bytes=None, stream=None):
+    """KDA backward: dg is FP32 [T, HV, 128]; see include/gdn.h."""
+    cu, cup = _cu_host(cu_seqlens_host)
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
+    _check(lib.gdn_kda_bwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                           ctypes.cast(_ptr(cu_seqlens_dev), ctypes.POINTER(ctypes.c_int32)), cup, _ptr(dO),
+                           _ptr(saved), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(workspace),
+                           ws_bytes, _stream(stream)), "gdn_kda_bwd")
 
 
 def gdn_fwd_states(prob, q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, s_in, o, s_out, saved, workspace,

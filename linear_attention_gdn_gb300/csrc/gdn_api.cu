@@ -25,6 +25,7 @@ void setup_bwd_attrs();
 void setup_prep_attrs();
 void setup_vnew_attrs();
 void setup_kda_attrs();
+void setup_kda_bwd_attrs();
 gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const void* k, const void* v,
                    const float* g, const float* beta, const int32_t* cu_dev, const void* dO, const void* saved,
                    void* dq, void* dk, void* dv, float* dg, float* dbeta, const float* ds_out, float* ds_in,
@@ -246,6 +247,7 @@ bool device_setup() {
     setup_prep_attrs();
     setup_vnew_attrs();
     setup_kda_attrs();
+    setup_kda_bwd_attrs();
     done[dev] = true;
   }
   return true;

@@ -63,6 +63,7 @@ struct BScanArgs {
   const int* seg_idx;    // [NSEG]
   const float* ds_out;   // [N][HV][128][128] FP32 gradient of each document's S_out, or null (zero)
   float* ds_in;          // [N][HV][128][128] FP32 gradient of each document's S_in, or null
+  int kda;               // 1: per-channel decay; cb holds KB_BYTES blocks
   int* err;
 };
 
@@ -109,7 +110,9 @@ struct CheckArgs {
 // ===========================================================================
 constexpr int BS_K = 0, BS_Q = 16384, BS_DO = 32768, BS_TP = 49152, BS_AQK = 57344, BS_SCAL = 65536;
 constexpr int BS_STAGE = 66560;
-constexpr int BS_DS = 2 * BS_STAGE;           // BF16 dS'^T tile
+// the per-channel-decay stage: Kd and Q~ in the K and Q slots, dO, -W^T, P, gamma_L
+constexpr int BSK_WT = 49152, BSK_AQK = 65536, BSK_SCAL = 73728, BSK_STAGE = 74752;
+constexpr int BS_DS = 2 * BSK_STAGE;          // BF16 dS'^T tile (after the larger of the two stage pairs)
 constexpr int BS_W = BS_DS + STATE_BYTES;     // -W^T tile, SwTile(128 x 64)
 constexpr int BS_DV = BS_W + 16384;           // dV_new^T staging, SwTile(128 x 64)
 constexpr int BS_SMEM = BS_DV + VN_BYTES;
@@ -132,10 +135,18 @@ __device__ __forceinline__ float ld_bf16(const uint8_t* tile, int r, int c, int 
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + sw_off(r, c, R)));
 }
 
+// KDA = true: the per-channel-decay form.  The stage then holds Kd and Q~ in the K and Q slots (DY =
+// dS'^T Kd^T needs no kd scaling; the dO^T A operand of MMA2 is scale dO^T, against Q~), -W^T from the
+// block (no W^T product or hop), P, and gamma_L, which scales column i of dS'^T.
+template <bool KDA>
 __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant__ BScanArgs a) {
+  constexpr int STAGE = KDA ? BSK_STAGE : BS_STAGE;
+  constexpr int S_AQK = KDA ? BSK_AQK : BS_AQK;
+  constexpr int S_SCAL = KDA ? BSK_SCAL : BS_SCAL;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
   __shared__ uint64_t full_bar[2], mma_bar, bar_pre;
+  __shared__ __align__(16) float glc[KDA ? 128 : 4];   // this chunk's gamma_L (KDA), read before the stage refill
   __shared__ uint32_t tslot;
   __shared__ int pre_next;   // the next iteration's W^T / X MMAs went out under this one's MMA2
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -197,9 +208,24 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
   // reads it).  Part 0 sets the barrier's byte count for both.
   auto issue = [&](int it, int part) {
     const int ci = c0 + nch - 1 - it;
-    uint8_t* st = sm + (it & 1) * BS_STAGE;
+    uint8_t* st = sm + (it & 1) * STAGE;
     uint64_t* bar = &full_bar[it & 1];
     const int t0 = a.chunk_tok0[ci];
+    if (KDA) {
+      const uint8_t* kbp = a.cb + ((size_t)ci * a.HV + hv) * KB_BYTES;
+      if (part == 0) {
+        mbar_expect_tx(bar, (uint32_t)STAGE);
+        bulk_load(st + BS_K, kbp + KB_KD, 16384u, bar);
+        tma_load_3d(st + BS_DO, &a.tdo, 0, hv, t0, bar);
+        tma_load_3d(st + BS_DO + 8192, &a.tdo, 64, hv, t0, bar);
+        bulk_load(st + BSK_WT, kbp + KB_WT, 16384u, bar);
+        bulk_load(st + BSK_AQK, kbp + KB_AQK, TILE64_BYTES, bar);
+        bulk_load(st + BSK_SCAL, kbp + KB_SCAL, CB_SCAL_BYTES, bar);
+      } else {
+        bulk_load(st + BS_Q, kbp + KB_QT, 16384u, bar);
+      }
+      return;
+    }
     if (part == 0) {
       const uint8_t* cbp = a.cb + ((size_t)ci * a.HV + hv) * CB_BYTES;
       mbar_expect_tx(bar, (uint32_t)BS_STAGE);
@@ -231,19 +257,21 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
   // W^T = K^T T'^T and X = dO^T Aqk^T of the chunk in stage `st` (they need no state)
   auto issue_wx = [&](const uint8_t* st) {
     const uint32_t a_k = smem_u32(st + BS_K), a_do = smem_u32(st + BS_DO);
-    const uint32_t a_tp = smem_u32(st + BS_TP), a_aqk = smem_u32(st + BS_AQK);
+    const uint32_t a_tp = smem_u32(st + BS_TP), a_aqk = smem_u32(st + S_AQK);
+    if (!KDA) {
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-      mma_ss(tb + BT_DW, desc_mn(a_k, 64, ks), desc_k(a_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ss(tb + BT_DW, desc_mn(a_k, 64, ks), desc_k(a_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+    }
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
       mma_ss(tb + BT_DX, desc_mn(a_do, 64, ks), desc_mn(a_aqk, 64, ks), idesc(128, 64, 1, 1), ks > 0);
   };
   for (int it = 0; it < nch && ok; ++it) {
     const int ci = c0 + nch - 1 - it;
-    uint8_t* st = sm + (it & 1) * BS_STAGE;
+    uint8_t* st = sm + (it & 1) * STAGE;
     const uint32_t a_k = smem_u32(st + BS_K), a_q = smem_u32(st + BS_Q);
-    const float* scal = reinterpret_cast<const float*>(st + BS_SCAL);
+    const float* scal = reinterpret_cast<const float*>(st + S_SCAL);
     const bool pre = pre_next;   // written before the last barrier of the previous iteration
     ok = __syncthreads_and(mbar_wait(&full_bar[it & 1], (it >> 1) & 1, a.err));
     if (!ok) break;
@@ -278,7 +306,8 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int r = q * 16 + 2 * e;
-          p8[e] = pack_bf16(scal[r] * ld_bf16(st + BS_DO, r, tid, 64), scal[r + 1] * ld_bf16(st + BS_DO, r + 1, tid, 64));
+          const float f0 = KDA ? a.scale : scal[r], f1 = KDA ? a.scale : scal[r + 1];
+          p8[e] = pack_bf16(f0 * ld_bf16(st + BS_DO, r, tid, 64), f1 * ld_bf16(st + BS_DO, r + 1, tid, 64));
         }
         tmem_st8(taddr(tb, warp * 32, BT_ADO + q * 8), p8);
       }
@@ -305,7 +334,7 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
       pph ^= 1;
       pend = false;
       tc_fence_after();
-      if (got) w_hop();
+      if (got && !KDA) w_hop();
       ok = got;
     }
     ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err) && ok);
@@ -313,7 +342,7 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
     if (!ok) break;
     tc_fence_after();
     {
-      if (!pre) w_hop();
+      if (!pre && !KDA) w_hop();
       const float* kd = scal + 64;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -326,7 +355,8 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int j = q * 16 + 2 * e, r = h * 32 + j;
-            p8[e] = pack_bf16(fmaf(a.scale, x[j], kd[r] * y[j]), fmaf(a.scale, x[j + 1], kd[r + 1] * y[j + 1]));
+            p8[e] = KDA ? pack_bf16(fmaf(a.scale, x[j], y[j]), fmaf(a.scale, x[j + 1], y[j + 1]))
+                        : pack_bf16(fmaf(a.scale, x[j], kd[r] * y[j]), fmaf(a.scale, x[j + 1], kd[r + 1] * y[j + 1]));
           }
           tmem_st8(taddr(tb, warp * 32, BT_ADV + h * 16 + q * 8), p8);
           if (full) {
@@ -340,6 +370,7 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
       tmem_wait_st();
     }
     const float gL = scal[128];   // read before the barrier after which the stage is refilled
+    if (KDA) glc[tid] = scal[tid];
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -349,9 +380,10 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
         bulk_store(a.dvn + ((size_t)ci * a.HV + hv) * VN_BYTES, sm + BS_DV, VN_BYTES);
         bulk_commit();
       }
+      const uint32_t b_w = KDA ? smem_u32(st + BSK_WT) : sm_w;   // -W^T: the stage's (KDA) or the hop's
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_ts(tb + BT_DS, tb + BT_ADV + ks * 8, desc_k(sm_w, 128, ks), idesc(128, 128, 0, 0), ks > 0);
+        mma_ts(tb + BT_DS, tb + BT_ADV + ks * 8, desc_k(b_w, 128, ks), idesc(128, 128, 0, 0), ks > 0);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_ts(tb + BT_DS, tb + BT_ADO + ks * 8, desc_mn(a_q, 64, ks), idesc(128, 128, 0, 1), 1u);
@@ -362,9 +394,9 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
     if (tid == 32) {   // the next chunk's W^T and X, under MMA2, when its tiles are in and need no zeroing
       int nx = 0;
       if (it + 1 < nch) {
-        const uint8_t* st1 = sm + ((it + 1) & 1) * BS_STAGE;
+        const uint8_t* st1 = sm + ((it + 1) & 1) * STAGE;
         if (mbar_wait(&full_bar[(it + 1) & 1], ((it + 1) >> 1) & 1, a.err) &&
-            reinterpret_cast<const int*>(st1 + BS_SCAL)[129] == CH) {
+            reinterpret_cast<const int*>(st1 + S_SCAL)[129] == CH) {
           tc_fence_after();
           issue_wx(st1);
           mma_commit(&bar_pre);
@@ -383,9 +415,22 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
       for (int h = 0; h < 4; ++h) {
         float x[32];
         tmem_ld32(taddr(tb, warp * 32, BT_DS + h * 32), x);
+        if (KDA) {   // column i (key channel) of dS'^T decays by gamma_L[i]
 #pragma unroll
-        for (int e = 0; e < 32; e += 2)
-          fma2_to(dS[h * 32 + e], dS[h * 32 + e + 1], gL, dS[h * 32 + e], dS[h * 32 + e + 1], x[e], x[e + 1]);
+          for (int e = 0; e < 32; e += 4) {
+            const float4 gv = *reinterpret_cast<const float4*>(glc + h * 32 + e);
+            fma2v(x[e], x[e + 1], gv.x, gv.y, dS[h * 32 + e], dS[h * 32 + e + 1]);
+            fma2v(x[e + 2], x[e + 3], gv.z, gv.w, dS[h * 32 + e + 2], dS[h * 32 + e + 3]);
+            dS[h * 32 + e] = x[e];
+            dS[h * 32 + e + 1] = x[e + 1];
+            dS[h * 32 + e + 2] = x[e + 2];
+            dS[h * 32 + e + 3] = x[e + 3];
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            fma2_to(dS[h * 32 + e], dS[h * 32 + e + 1], gL, dS[h * 32 + e], dS[h * 32 + e + 1], x[e], x[e + 1]);
+        }
       }
       store_row128(ds_tile, tid, dS);
     }
@@ -1403,9 +1448,97 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
 // host side
 // ===========================================================================
 void setup_bwd_attrs() {
-  cudaFuncSetAttribute(bwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BS_SMEM_ALLOC);
+  cudaFuncSetAttribute(bwd_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, BS_SMEM_ALLOC);
+  cudaFuncSetAttribute(bwd_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, BS_SMEM_ALLOC);
   cudaFuncSetAttribute(grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GK_SMEM_ALLOC);
   cudaFuncSetAttribute(merge_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 128 * 129 * 4);
+}
+
+// the device-side check that `saved` was written by a forward of this problem
+void launch_check_saved(const Plan& P, const gdn_problem& pr, const void* saved, uint8_t* ws, cudaStream_t s) {
+  CheckArgs ca;
+  ca.saved = static_cast<const uint8_t*>(saved);
+  SavedHeader h;
+  memset(&h, 0, sizeof(h));
+  h.magic = SAVED_MAGIC;
+  h.version = SAVED_VERSION;
+  h.T = P.T;
+  h.N = P.N;
+  h.H = P.H;
+  h.HV = P.HV;
+  h.dk = pr.dk;
+  h.dv = pr.dv;
+  h.l2norm = pr.l2norm ? 1 : 0;
+  h.NC = P.NC;
+  h.NSEG = P.NSEG;
+  h.nsplit = P.nsplit;
+  h.seg_len = P.seg_len;
+  memcpy(&h.scale_bits, &pr.scale, 4);
+  h.cu_hash = P.cu_hash;
+  h.form = P.form;
+  ca.expect = h;
+  ca.err = reinterpret_cast<int*>(ws);
+  prof_begin(K_CHECK_SAVED, s);
+  check_saved_kernel<<<1, 1, 0, s>>>(ca);
+  prof_end(K_CHECK_SAVED, s);
+}
+
+// The adjoint walks of one backward: the split segments' zero-start walks and their merge, then the
+// full walks (the dS' tape and dV_new^T of every chunk).  kda: the per-channel-decay block layout.
+gdn_status run_bwd_walks(const Plan& P, const gdn_problem& pr, const void* q, const void* k, const void* dO,
+                         const uint8_t* cb, int kda, const void* saved, const float* ds_out, float* ds_in,
+                         uint8_t* ws, cudaStream_t s) {
+  Tables t = tables_at(P, ws);
+  const uint8_t* sv = static_cast<const uint8_t*>(saved);
+  BScanArgs ba;
+  memset(&ba, 0, sizeof(ba));
+  if (!make_tmap(&ba.tq, q, P.T, P.H) || !make_tmap(&ba.tk, k, P.T, P.H) || !make_tmap(&ba.tdo, dO, P.T, P.HV))
+    return GDN_ERR_CUDA;
+  ba.cb = cb;
+  ba.chunk_tok0 = t.chunk_tok0;
+  ba.seg_c0 = t.seg_c0;
+  ba.seg_c1 = t.seg_c1;
+  ba.seg_split = t.seg_split;
+  ba.split_seg = t.split_seg;
+  ba.walk_seg = t.bwalk_seg;
+  ba.HV = P.HV;
+  ba.G = P.G;
+  ba.nsplit = P.nsplit;
+  ba.scale = pr.scale;
+  ba.dtape = ws + P.o_dtape;
+  ba.dvn = ws + P.o_dvn;
+  ba.ds_init = reinterpret_cast<const float*>(ws + P.o_dsinit);
+  ba.dbend = reinterpret_cast<float*>(ws + P.o_dbend);
+  ba.seg_doc = t.seg_doc;
+  ba.seg_offsets = t.seg_offsets;
+  ba.seg_idx = t.seg_idx;
+  ba.ds_out = ds_out;
+  ba.ds_in = ds_in;
+  ba.kda = kda;
+  ba.err = reinterpret_cast<int*>(ws);
+  if (P.nsplit > 0) {
+    ba.walk = 1;
+    prof_begin(K_BWD_WALK, s);
+    if (kda) bwd_scan_kernel<true><<<P.nsplit * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
+    else bwd_scan_kernel<false><<<P.nsplit * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
+    prof_end(K_BWD_WALK, s);
+    MergeBwdArgs ma;
+    ma.sdoc_first = t.sdoc_first;
+    ma.dbend = ba.dbend;
+    ma.mend = reinterpret_cast<const float*>(sv + P.s_mseg);
+    ma.ds_init = reinterpret_cast<float*>(ws + P.o_dsinit);
+    ma.HV = P.HV;
+    ma.err = ba.err;
+    prof_begin(K_BWD_MERGE, s);
+    merge_bwd_kernel<<<dim3(P.nsdoc, P.HV), 256, 2 * 128 * 129 * 4, s>>>(ma);
+    prof_end(K_BWD_MERGE, s);
+  }
+  ba.walk = 0;
+  prof_begin(K_BWD_SCAN, s);
+  if (kda) bwd_scan_kernel<true><<<(P.NSEG - P.nsdoc) * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
+  else bwd_scan_kernel<false><<<(P.NSEG - P.nsdoc) * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
+  prof_end(K_BWD_SCAN, s);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const void* k, const void* v,
@@ -1422,33 +1555,7 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
     pa.HV = P.HV;
     launch_passthrough(pa, P.N, s);
   }
-  {
-    CheckArgs ca;
-    ca.saved = static_cast<const uint8_t*>(saved);
-    SavedHeader h;
-    memset(&h, 0, sizeof(h));
-    h.magic = SAVED_MAGIC;
-    h.version = SAVED_VERSION;
-    h.T = P.T;
-    h.N = P.N;
-    h.H = P.H;
-    h.HV = P.HV;
-    h.dk = pr.dk;
-    h.dv = pr.dv;
-    h.l2norm = pr.l2norm ? 1 : 0;
-    h.NC = P.NC;
-    h.NSEG = P.NSEG;
-    h.nsplit = P.nsplit;
-    h.seg_len = P.seg_len;
-    memcpy(&h.scale_bits, &pr.scale, 4);
-    h.cu_hash = P.cu_hash;
-    h.form = P.form;
-    ca.expect = h;
-    ca.err = reinterpret_cast<int*>(ws);
-    prof_begin(K_CHECK_SAVED, s);
-    check_saved_kernel<<<1, 1, 0, s>>>(ca);
-    prof_end(K_CHECK_SAVED, s);
-  }
+  launch_check_saved(P, pr, saved, ws, s);
   if (P.NC == 0) return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
   Tables t = tables_at(P, ws);
   const uint8_t* sv = static_cast<const uint8_t*>(saved);
@@ -1480,52 +1587,12 @@ gdn_status run_bwd(const Plan& P, const gdn_problem& pr, const void* q, const vo
     cb = ws + P.o_cb;
     vn = ws + P.o_vnb;
   }
-  BScanArgs ba;
+  st = run_bwd_walks(P, pr, q, k, dO, cb, 0, saved, ds_out, ds_in, ws, s);
+  if (st != GDN_OK) return st;
+  BScanArgs ba;   // (its tensor maps serve the gradient kernel too)
   memset(&ba, 0, sizeof(ba));
   if (!make_tmap(&ba.tq, q, P.T, P.H) || !make_tmap(&ba.tk, k, P.T, P.H) || !make_tmap(&ba.tdo, dO, P.T, P.HV))
     return GDN_ERR_CUDA;
-  ba.cb = cb;
-  ba.chunk_tok0 = t.chunk_tok0;
-  ba.seg_c0 = t.seg_c0;
-  ba.seg_c1 = t.seg_c1;
-  ba.seg_split = t.seg_split;
-  ba.split_seg = t.split_seg;
-  ba.walk_seg = t.bwalk_seg;
-  ba.HV = P.HV;
-  ba.G = P.G;
-  ba.nsplit = P.nsplit;
-  ba.scale = pr.scale;
-  ba.dtape = ws + P.o_dtape;
-  ba.dvn = ws + P.o_dvn;
-  ba.ds_init = reinterpret_cast<const float*>(ws + P.o_dsinit);
-  ba.dbend = reinterpret_cast<float*>(ws + P.o_dbend);
-  ba.seg_doc = t.seg_doc;
-  ba.seg_offsets = t.seg_offsets;
-  ba.seg_idx = t.seg_idx;
-  ba.ds_out = ds_out;
-  ba.ds_in = ds_in;
-  ba.err = reinterpret_cast<int*>(ws);
-  if (P.nsplit > 0) {
-    ba.walk = 1;
-    prof_begin(K_BWD_WALK, s);
-    bwd_scan_kernel<<<P.nsplit * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
-    prof_end(K_BWD_WALK, s);
-    MergeBwdArgs ma;
-    ma.sdoc_first = t.sdoc_first;
-    ma.dbend = ba.dbend;
-    ma.mend = reinterpret_cast<const float*>(sv + P.s_mseg);
-    ma.ds_init = reinterpret_cast<float*>(ws + P.o_dsinit);
-    ma.HV = P.HV;
-    ma.err = ba.err;
-    prof_begin(K_BWD_MERGE, s);
-    merge_bwd_kernel<<<dim3(P.nsdoc, P.HV), 256, 2 * 128 * 129 * 4, s>>>(ma);
-    prof_end(K_BWD_MERGE, s);
-  }
-  ba.walk = 0;
-  prof_begin(K_BWD_SCAN, s);
-  bwd_scan_kernel<<<(P.NSEG - P.nsdoc) * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
-  prof_end(K_BWD_SCAN, s);
-
   GradArgs ga;
   memset(&ga, 0, sizeof(ga));
   ga.tq = ba.tq;

@@ -244,5 +244,9 @@ gdn_status run_tables(const Plan& P, const gdn_problem* p, const int32_t* cu_dev
                       cudaStream_t s);
 void launch_fwd_scan(const ScanArgs& a, int nchains, cudaStream_t s);
 void launch_merge(const MergeArgs& a, int nsdoc, cudaStream_t s);
+void launch_check_saved(const Plan& P, const gdn_problem& pr, const void* saved, uint8_t* ws, cudaStream_t s);
+gdn_status run_bwd_walks(const Plan& P, const gdn_problem& pr, const void* q, const void* k, const void* dO,
+                         const uint8_t* cb, int kda, const void* saved, const float* ds_out, float* ds_in,
+                         uint8_t* ws, cudaStream_t s);
 
 }  // namespace gdn

@@ -129,3 +129,94 @@ def test_kda_gate_range_refused():
     d2 = to_dev(inputs.generate_kda(w2, "cpu", with_grad=False))
     _, _, _, st2 = run_kda_fwd(w2, d2)
     assert st2 == 0
+
+
+def run_kda_fwd_bwd(w, d):
+    import linear_attention_gdn_gb300 as gdn
+    prob, buf, o, st = run_kda_fwd(w, d)
+    assert st == 0
+    dq = torch.full((w.T, w.H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dk = torch.full_like(dq, float("nan"))
+    dv = torch.full((w.T, w.HV, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dg = torch.full((w.T, w.HV, 128), float("nan"), dtype=torch.float32, device="cuda")
+    dbeta = torch.full((w.T, w.HV), float("nan"), dtype=torch.float32, device="cuda")
+    gdn.gdn_kda_bwd(prob, d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_dev"], w.cu_seqlens, d["dO"],
+                    buf.saved, dq, dk, dv, dg, dbeta, buf.workspace)
+    st = gdn.gdn_device_status(buf.workspace)
+    torch.cuda.synchronize()
+    return dict(o=o, dq=dq, dk=dk, dv=dv, dg=dg, dbeta=dbeta), st
+
+
+@pytest.mark.parametrize("name,w", KDA_CASES, ids=[c[0] for c in KDA_CASES])
+def test_kda_backward_parity(name, w):
+    d = to_dev(inputs.generate_kda(w, "cpu", with_grad=True))
+    out, st = run_kda_fwd_bwd(w, d)
+    assert st == 0
+    r, _ = oracle_kda(w, {n: (x.cpu() if hasattr(x, "cpu") else x) for n, x in d.items()}, with_grad=True)
+    for n in ("o", "dq", "dk", "dv", "dg", "dbeta"):
+        compare(f"kda/{name}/{n}", out[n].double().cpu().numpy(), r[n])
+
+
+def test_kda_backward_bitwise_repeatable():
+    w = KDA_CASES[1][1]
+    d = to_dev(inputs.generate_kda(w, "cpu", with_grad=True))
+    a1, s1 = run_kda_fwd_bwd(w, d)
+    a2, s2 = run_kda_fwd_bwd(w, d)
+    assert s1 == 0 and s2 == 0
+    for n in a1:
+        assert torch.equal(a1[n], a2[n]), n
+
+
+def test_kda_backward_rejects_a_gdn_saved_set():
+    """A saved set written by the GDN forward is not a KDA one: the backward sets
+    GDN_ERR_SAVED_MISMATCH on the device and writes no gradient."""
+    import linear_attention_gdn_gb300 as gdn
+    w = KDA_CASES[0][1]
+    d = to_dev(inputs.generate_kda(w, "cpu", with_grad=True))
+    prob = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm)
+    s_g, _ = gdn.gdn_saved_bytes(prob, w.cu_seqlens)
+    s_k, ws_k = gdn.gdn_kda_saved_bytes(prob, w.cu_seqlens)
+    saved = torch.zeros(max(s_g, s_k), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(ws_k, dtype=torch.uint8, device="cuda")
+    dg1 = d["g"][:, :, 0].contiguous()
+    o = torch.empty((w.T, w.HV, 128), dtype=torch.bfloat16, device="cuda")
+    buf = gdn.Buffers(prob, w.cu_seqlens)
+    gdn.gdn_fwd(prob, d["q"], d["k"], d["v"], dg1, d["beta"], d["cu_dev"], w.cu_seqlens, o, saved, buf.workspace)
+    assert gdn.gdn_device_status(buf.workspace) == 0
+    dq = torch.full((w.T, w.H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dk = torch.full_like(dq, float("nan"))
+    dv = torch.full((w.T, w.HV, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dg = torch.full((w.T, w.HV, 128), float("nan"), dtype=torch.float32, device="cuda")
+    dbeta = torch.full((w.T, w.HV), float("nan"), dtype=torch.float32, device="cuda")
+    gdn.gdn_kda_bwd(prob, d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_dev"], w.cu_seqlens, d["dO"], saved,
+                    dq, dk, dv, dg, dbeta, ws)
+    assert gdn.gdn_device_status(ws) == 4
+    assert torch.isnan(dg).all() and torch.isnan(dq.float()).all()
+
+
+def test_kda_uniform_decay_backward_matches_gdn():
+    """With the same decay on every channel the KDA gradients equal the GDN ones, and the per-channel gate
+    gradients sum to the GDN gate gradient (within the accuracy budget: different kernels)."""
+    import linear_attention_gdn_gb300 as gdn
+    w = inputs.custom([300, 64, 129], 2, 4, g_lo=0.0, g_hi=6.0, seed=28)
+    d = to_dev(inputs.generate(w, "cpu", with_grad=True))
+    prob = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm)
+    buf = gdn.Buffers(prob, w.cu_seqlens)
+    o = torch.empty((w.T, w.HV, 128), dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_fwd(prob, d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_dev"], w.cu_seqlens, o, buf.saved,
+                buf.workspace)
+    ref = dict(dq=torch.empty((w.T, w.H, 128), dtype=torch.bfloat16, device="cuda"))
+    ref["dk"] = torch.empty_like(ref["dq"])
+    ref["dv"] = torch.empty((w.T, w.HV, 128), dtype=torch.bfloat16, device="cuda")
+    ref["dg"] = torch.empty((w.T, w.HV), dtype=torch.float32, device="cuda")
+    ref["dbeta"] = torch.empty((w.T, w.HV), dtype=torch.float32, device="cuda")
+    gdn.gdn_bwd(prob, d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_dev"], w.cu_seqlens, d["dO"], buf.saved,
+                ref["dq"], ref["dk"], ref["dv"], ref["dg"], ref["dbeta"], buf.workspace)
+    assert gdn.gdn_device_status(buf.workspace) == 0
+    dk_in = dict(d)
+    dk_in["g"] = d["g"][:, :, None].expand(w.T, w.HV, 128).contiguous()
+    out, st = run_kda_fwd_bwd(w, dk_in)
+    assert st == 0
+    for n in ("dq", "dk", "dv", "dbeta"):
+        compare(f"kda_vs_gdn/{n}", out[n].double().cpu().numpy(), ref[n].double().cpu().numpy())
+    compare("kda_vs_gdn/dg", out["dg"].double().sum(-1).cpu().numpy(), ref["dg"].double().cpu().numpy())
