@@ -120,6 +120,24 @@ def step_flops(w, op):
     return {"fwd": f_fwd, "fwd+bwd": f_fwd + f_bwd, "ckpt": 2 * f_fwd + f_bwd}[op]
 
 
+# The per-channel-decay (KDA) form on the same shapes: the decay products M = K^ (exp(G_r - G_c) . K^)^T
+# and P are per value head (the decay differs per head), and g, dg are [T, HV, 128] FP32:
+#   fwd  F_f = HV (6 d^2 + 10 C d) FLOP / token
+#   bwd  F_b = HV (14 d^2 + 28 C d) FLOP / token (the GDN count with its KK^T, QK^T term per value head)
+# bytes: the GDN method tensors with g (and dg) 128 FP32 values per token and value head.
+def kda_step_flops(w):
+    Ls = chunk_lens(w)
+    return sum(w.HV * ((6 + 14) * L * D * D + (10 + 28) * L * L * D) for L in Ls)
+
+
+def kda_step_bytes(w):
+    m = method_tensors(w)
+    g_extra = w.T * w.HV * (D - 1) * 4   # g (or dg) per channel instead of per token
+    fwd = m["qk"] + m["v"] + m["gb"] + g_extra + m["o"] + m["states"]
+    bwd = m["qk"] + m["v"] + m["gb"] + g_extra + m["dO"] + m["states"] + m["dqdk"] + m["dv"] + m["dgdb"] + g_extra
+    return fwd + bwd
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -336,6 +354,45 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         return res
 
+    def time_kda(K, W):
+        """fwd + bwd of the per-channel-decay (KDA) form on the bench workload's shapes (own inputs with
+        g [T, HV, 128], own buffers, freed afterwards); per-kernel times from the launch events."""
+        xx = inputs.generate_kda(w, dev)
+        pk_ = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm, w.segments)
+        bk = gdn.Buffers(pk_, w.cu_seqlens, device=dev, kda=True)
+        ok_ = torch.empty((w.T, w.HV, D), dtype=torch.bfloat16, device=dev)
+        gr = (torch.empty_like(xx["q"]), torch.empty_like(xx["k"]), torch.empty_like(xx["v"]),
+              torch.empty_like(xx["g"]), torch.empty_like(xx["beta"]))
+
+        def st():
+            gdn.gdn_kda_fwd(pk_, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_dev, w.cu_seqlens, ok_,
+                            bk.saved, bk.workspace, stream=stream)
+            gdn.gdn_kda_bwd(pk_, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_dev, w.cu_seqlens, xx["dO"],
+                            bk.saved, *gr, bk.workspace, stream=stream)
+        t_k = timed_replicas(st, K, W, barrier, allmax, event_clock)
+        stk = gdn.gdn_device_status(bk.workspace, stream)
+        assert stk == 0, gdn.gdn_status_string(stk)
+        gdn.gdn_profile_read_all()
+        gdn.gdn_profile_enable(1)
+        timed_replicas(st, K, 1, barrier, allmax, event_clock)
+        gdn.gdn_profile_enable(0)
+        ks = gdn.gdn_profile_read_all()
+        pk2 = peaks()
+        fl, by = kda_step_flops(w), kda_step_bytes(w)
+        res = {"ms": round(t_k, 4), "Mtokens_per_s": round(replica_rate(world, w.T, t_k), 3),
+               "TFLOP_per_s": round(world * fl / t_k / 1e9, 1),
+               "tensor_frac": round(world * fl / t_k / 1e9 / pk2["bf16_tflops_sustained"], 4),
+               "method_GB_per_s": round(by / (t_k * 1e-3) / 1e9, 1),
+               "hbm_frac": round(by / (t_k * 1e-3) / 1e9 / pk2["hbm_gbs"], 4),
+               "saved_bytes_per_token": round(bk.saved_bytes / w.T, 1),
+               "counting": "F = HV (20 d^2 + 38 C d) FLOP / token; bytes: the method tensors with g, dg "
+                           "[T, HV, 128] FP32",
+               "kernels_ms_per_step": {k: round(v["total_ms"] / (K + 1), 4) for k, v in ks.items()
+                                       if v["timed_launches"]}}
+        del xx, bk, ok_, gr
+        torch.cuda.empty_cache()
+        return res
+
     def barrier():
         if world > 1:
             import torch.distributed as dist
@@ -428,6 +485,8 @@ def run_ours(args, rank, world, local_rank):
         for widx in (1, 3, 4):
             if widx != args.workload:
                 extra[f"workload{widx} fwd+bwd"] = time_workload(widx, max(3, args.steps // 2), 2)
+        # the per-channel-decay form on the same workload
+        extra["kda fwd+bwd"] = time_kda(max(3, args.steps // 2), 2)
 
     # end to end through the C ABI with pinned host buffers: every step copies
     # its inputs in and all of its outputs back

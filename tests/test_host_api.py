@@ -28,8 +28,9 @@ def test_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for code in range(8):
+    for code in range(9):
         assert gdn.gdn_status_string(code)
+    assert "KDA" in gdn.gdn_status_string(8)
     assert gdn.gdn_status_string(99) == "unknown status"
 
 
@@ -128,3 +129,43 @@ def test_conv1d_problem_checks_and_workspace():
         p = gdn.conv_problem(2500, 2, C, W)
         assert gdn.lib.gdn_conv1d_workspace_bytes(ctypes.byref(p), cup, ctypes.byref(n)) == code
     assert n.value == 16 + 3 * (4 + 1) * 16 * 4
+
+
+def test_kda_saved_and_workspace_bytes():
+    """The per-channel-decay entry points: saved = header + (BF16 state + BF16 V_new^T) per chunk and
+    value head (the decay products and UT blocks are recomputed); the workspace holds the per-chunk
+    blocks (82,944 B each) and the backward's tapes."""
+    p = gdn.problem(320, 2, 2, 4)
+    saved, ws = gdn.gdn_kda_saved_bytes(p, [0, 128, 320])
+    assert saved == 4096 + 5 * 4 * (32768 + 16384)
+    assert ws >= 5 * 4 * (82944 + 32768 + 16384)
+    # saved_form does not change the KDA layout
+    p2 = gdn.problem(320, 2, 2, 4, saved_form=gdn.SAVED_REPLAY)
+    assert gdn.gdn_kda_saved_bytes(p2, [0, 128, 320]) == (saved, ws)
+
+
+def test_kda_invalid_arguments_refused_before_launch():
+    p = gdn.problem(128, 1, 1, 2)
+    cu = np.array([0, 128], dtype=np.int32)
+    cup = cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    fake = ctypes.c_void_p(1 << 20)   # 16-byte aligned, never dereferenced: every check fails first
+    # o is required
+    st = gdn.lib.gdn_kda_fwd(ctypes.byref(p), fake, fake, fake, fake, fake, fake, cup, None, None, fake, 1 << 30,
+                             None)
+    assert st == 1
+    # misaligned input
+    bad = ctypes.c_void_p((1 << 20) + 4)
+    st = gdn.lib.gdn_kda_fwd(ctypes.byref(p), bad, fake, fake, fake, fake, fake, cup, fake, None, fake, 1 << 30,
+                             None)
+    assert st == 1
+    # workspace too small
+    st = gdn.lib.gdn_kda_fwd(ctypes.byref(p), fake, fake, fake, fake, fake, fake, cup, fake, None, fake, 16, None)
+    assert st == 3
+    # backward without a saved set
+    st = gdn.lib.gdn_kda_bwd(ctypes.byref(p), fake, fake, fake, fake, fake, fake, cup, fake, None, fake, fake,
+                             fake, fake, fake, fake, 1 << 30, None)
+    assert st == 1
+    # unsupported head size
+    p3 = gdn.problem(128, 1, 1, 2, dk=64)
+    s = ctypes.c_size_t(0)
+    assert gdn.lib.gdn_kda_saved_bytes(ctypes.byref(p3), cup, ctypes.byref(s), ctypes.byref(s)) == 2
