@@ -103,31 +103,22 @@ __global__ void __launch_bounds__(128, 2) kda_prep_kernel(const __grid_constant_
     mbar_init(&bar_t, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
     unsafe = 0;
-    mbar_expect_tx(&bar_ld, 32768u);
+    // the K, Q tiles and the value head's g rows (512 B each, one bulk copy per token) on one barrier
+    mbar_expect_tx(&bar_ld, 32768u + (uint32_t)L * 512u);
     tma_load_3d(kq, &a.tk, 0, j, tok0, &bar_ld);
     tma_load_3d(kq + 8192, &a.tq, 0, j, tok0, &bar_ld);
     tma_load_3d(kq + 16384, &a.tk, 64, j, tok0, &bar_ld);
     tma_load_3d(kq + 24576, &a.tq, 64, j, tok0, &bar_ld);
-  }
-  {  // g (log2 units) and beta of this value head; rows past L are zero
     const float* gp = a.g + ((size_t)tok0 * a.HV + hv) * D;
-    const size_t rs = (size_t)a.HV * D;
-    for (int idx = tid; idx < CH * 32; idx += 128) {
-      const int r = idx >> 5, q4 = idx & 31;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (r < L) {
-        v = *reinterpret_cast<const float4*>(gp + r * rs + 4 * q4);
-        v.x *= kUtLog2e;
-        v.y *= kUtLog2e;
-        v.z *= kUtLog2e;
-        v.w *= kUtLog2e;
-      }
-      *reinterpret_cast<float4*>(Gm + r * D + 4 * q4) = v;
-    }
-    if (tid < CH) bs[tid] = tid < L ? a.beta[(size_t)(tok0 + tid) * a.HV + hv] : 0.f;
+    for (int r = 0; r < L; ++r) bulk_load(Gm + r * D, gp + (size_t)r * a.HV * D, 512u, &bar_ld);
   }
-  __syncthreads();
-  {  // channel tid: the cumulative decay G (rows past L keep G_{L-1}), the block entries, the factors
+  for (int idx = tid; idx < (CH - L) * 32; idx += 128)   // rows past L: zero
+    *reinterpret_cast<float4*>(Gm + (L + (idx >> 5)) * D + 4 * (idx & 31)) = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (tid < CH) bs[tid] = tid < L ? a.beta[(size_t)(tok0 + tid) * a.HV + hv] : 0.f;
+  __syncthreads();   // the barriers' initialisation is visible before any thread waits on them
+  bool landed = __syncthreads_and(mbar_wait(&bar_ld, 0, a.err));
+  if (landed) {  // channel tid: the cumulative decay G in log2 units (rows past L keep G_{L-1}), the block
+                 // entries, the factors
     const int i = tid;
     float run = 0.f, ref = 0.f, mx = 0.f;
     for (int r = 0; r < CH; ++r) {
@@ -135,7 +126,7 @@ __global__ void __launch_bounds__(128, 2) kda_prep_kernel(const __grid_constant_
         ref = run;
         gx[r >> 4][i] = run;
       }
-      run += Gm[r * D + i];
+      run = fmaf(Gm[r * D + i], kUtLog2e, run);
       Gm[r * D + i] = run;
       mx = fmaxf(mx, fabsf(run - ref));
     }
@@ -165,12 +156,11 @@ __global__ void __launch_bounds__(128, 2) kda_prep_kernel(const __grid_constant_
   const uint32_t tb = tslot;
   int vpend = 0;   // error path: versions whose completion was not seen (bit v & 1 -> bar_v, phase v >> 1)
   int t_pend = -1;
-  bool ok = true;
-  if (unsafe) {
+  bool ok = landed;
+  if (ok && unsafe) {
     if (tid == 0) atomicCAS(a.err, 0, ST_GATE_RANGE);
     ok = false;
   }
-  ok = __syncthreads_and(ok && mbar_wait(&bar_ld, 0, a.err));
   if (!ok) {
     if (tid == 0) mbar_drain(&bar_ld, 0);
     __syncthreads();

@@ -19,10 +19,11 @@
 // "perf(cake_kda) ... #7097" page for the family; the chunk algebra is the GDN one of the
 // "feat(cake_gdn_kcp) ... #8172" page with every decay inside the channel sums).
 //
-// The decay-weighted products rowM, rowP, col run on the tensor cores per 16-token block, as the
-// forward's M and P do (gdn_kda.cu): rows r of block a use R_a (k^_c exp(Gx_a - G_c)) and the factor
-// exp(G_r - Gx_a); columns c of block b use C_b = k^_r exp(G_r - Gx_b), D_b = q^_r exp(G_r - Gx_b)
-// and the factor exp(Gx_b - G_c).  Each is an N = 16 slice of an M = 128 product over the key channels.
+// The decay-weighted products rowM, rowP, col run on the tensor cores per pair of 16-token blocks
+// (a, b), with Gx_a the log decay entering block a and every token carrying its own block's factor:
+// Lk_r = k^_r exp(G_r - Gx_{blk r}), Lq_r likewise, Rb_c = k^_c exp(Gx_{blk c} - G_c), so that
+// exp(G_r - G_c) k^_c = exp(G_r - Gx_a) F(a, b) Rb_c with F(a, b) = exp(Gx_a - Gx_b) per channel.
+// The block products (one K = 16 MMA step each) are summed with F in FP32 afterwards.
 //
 // kda_grad_kernel: one CTA of 256 threads per (chunk, q/k head); the group's value heads one after
 // another, each a fixed sequence of MMA groups and CUDA-core passes (no overlap between heads); dq^
@@ -68,12 +69,16 @@ constexpr int KX_S = 0, KX_DS = 32768, KX_VN = 65536, KX_DV = 81920, KX_DO = 983
 constexpr int KX_WD = 0, KX_KT = 16384;                                      // dW^T, K~ (MB)
 constexpr int KX_DT = 32768, KX_R1 = 40960, KX_DM = 49152, KX_DMT = 57344, KX_DP = 65536, KX_DPT = 73728;
 constexpr int KX_LK = 81920, KX_LQ = 98304, KX_RB = 114688;                   // after MA
-constexpr int KX_V0 = 0, KX_V1 = 16384;                                      // block tiles (after MB)
 constexpr int KG_SMEM = KG_X + 131072;
 constexpr int KG_SMEM_ALLOC = KG_SMEM + 1024;
 // TMEM columns
 constexpr int KGT_DQ = 0, KGT_DK = 64, KGT_A0 = 128, KGT_A1 = 192, KGT_A2 = 256, KGT_A3 = 320, KGT_A4 = 384,
               KGT_A5 = 448;
+// the decay-weighted products (every other result is dead by then): Z_b (64 - 16 b columns each, from
+// column 16 b of the result), Zp_b, then Y_a (16 a + 16 columns each) over the Z columns
+constexpr int KGT_Z = 128, KGT_ZP = 288;
+__constant__ int kZOff[4] = {0, 64, 112, 144};
+__constant__ int kYOff[4] = {0, 16, 48, 96};
 
 __device__ __forceinline__ int kg_pair(int a, int b) { return a * (a - 1) / 2 + b; }   // b < a
 
@@ -199,14 +204,15 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
                  s_t = smem_u32(sm + KG_T), s_wd = smem_u32(X + KX_WD), s_kt = smem_u32(X + KX_KT),
                  s_dt = smem_u32(X + KX_DT), s_r1 = smem_u32(X + KX_R1), s_dm = smem_u32(X + KX_DM),
                  s_dmt = smem_u32(X + KX_DMT), s_dp = smem_u32(X + KX_DP), s_dpt = smem_u32(X + KX_DPT),
-                 s_v0 = smem_u32(X + KX_V0), s_v1 = smem_u32(X + KX_V1);
+                 s_lk = smem_u32(X + KX_LK), s_lq = smem_u32(X + KX_LQ), s_rb = smem_u32(X + KX_RB);
 
   for (int hh = 0; hh < a.G && ok; ++hh) {
     const int hv = j * a.G + hh;
     const size_t blk = (size_t)c * a.HV + hv;
     if (tid == 0) {   // this value head's tiles
       const uint8_t* kbp = a.kb + blk * KB_BYTES;
-      mbar_expect_tx(&bar_ld, (uint32_t)(2 * STATE_BYTES + 2 * VN_BYTES + 2 * 16384 + 2 * TILE64_BYTES));
+      mbar_expect_tx(&bar_ld, (uint32_t)(2 * STATE_BYTES + 2 * VN_BYTES + 2 * 16384 + 2 * TILE64_BYTES) +
+                                  (uint32_t)L * 512u);
       bulk_load(X + KX_S, a.tape + blk * STATE_BYTES, STATE_BYTES, &bar_ld);
       bulk_load(X + KX_DS, a.dtape + blk * STATE_BYTES, STATE_BYTES, &bar_ld);
       bulk_load(X + KX_VN, a.vn + blk * VN_BYTES, VN_BYTES, &bar_ld);
@@ -217,32 +223,23 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
       tma_load_3d(X + KX_V + 8192, &a.tv, 64, hv, tok0, &bar_ld);
       bulk_load(sm + KG_T, kbp + KB_T, TILE64_BYTES, &bar_ld);
       bulk_load(sm + KG_MT, kbp + KB_MT, TILE64_BYTES, &bar_ld);
+      const float* gp = a.g + ((size_t)tok0 * a.HV + hv) * D;   // g: one 512-byte row per token
+      for (int r = 0; r < L; ++r) bulk_load(Gm + r * D, gp + (size_t)r * a.HV * D, 512u, &bar_ld);
     }
     ld_pend = true;
-    {  // g (log2 units) and beta; rows past L are zero
-      const float* gp = a.g + ((size_t)tok0 * a.HV + hv) * D;
-      const size_t rs = (size_t)a.HV * D;
-      for (int idx = tid; idx < CH * 32; idx += 256) {
-        const int r = idx >> 5, q4 = idx & 31;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < L) {
-          v = *reinterpret_cast<const float4*>(gp + r * rs + 4 * q4);
-          v.x *= kUtLog2e;
-          v.y *= kUtLog2e;
-          v.z *= kUtLog2e;
-          v.w *= kUtLog2e;
-        }
-        *reinterpret_cast<float4*>(Gm + r * D + 4 * q4) = v;
-      }
-      if (tid < CH) bs[tid] = tid < L ? a.beta[(size_t)(tok0 + tid) * a.HV + hv] : 0.f;
-    }
-    __syncthreads();
-    if (tid < 128) {   // channel tid: cumulative decay, block entries, block ratios
+    for (int idx = tid; idx < (CH - L) * 32; idx += 256)   // g rows past L: zero
+      *reinterpret_cast<float4*>(Gm + (L + (idx >> 5)) * D + 4 * (idx & 31)) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid < CH) bs[tid] = tid < L ? a.beta[(size_t)(tok0 + tid) * a.HV + hv] : 0.f;
+    ok = __syncthreads_and(mbar_wait(&bar_ld, ldph, a.err));
+    if (!ok) break;
+    ldph ^= 1;
+    ld_pend = false;
+    if (tid < 128) {   // channel tid: cumulative decay (log2 units), block entries, block ratios
       const int i = tid;
       float run = 0.f;
       for (int r = 0; r < CH; ++r) {
         if ((r & 15) == 0) gx[r >> 4][i] = run;
-        run += Gm[r * D + i];
+        run = fmaf(Gm[r * D + i], kUtLog2e, run);
         Gm[r * D + i] = run;
       }
       glL[i] = run;
@@ -251,10 +248,6 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
 #pragma unroll
         for (int b = 0; b < aa; ++b) fab[kg_pair(aa, b)][i] = exp2f(gx[aa][i] - gx[b][i]);
     }
-    ok = __syncthreads_and(mbar_wait(&bar_ld, ldph, a.err));
-    if (!ok) break;
-    ldph ^= 1;
-    ld_pend = false;
     if (L < CH) {   // zero the dO, V rows past the document end
       for (int idx = tid; idx < (CH - L) * 32; idx += 256) {
         const int t = idx >> 5, tile = (idx >> 4) & 1, c8 = idx & 15;
@@ -515,79 +508,78 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
         rowdb[wg][ra + 8] = rsum[1];
       }
     }
-    // ---- rows of block a: rowM^T, rowP^T slices (A1, A3) from R_a = Rb . exp2(gx[a] - gx[blk c])
-    auto build_r = [&](int v, uint8_t* dst) {
-#pragma unroll 2
-      for (int it = 0; it < 4; ++it) {
-        const int idx = tid + 256 * it, r = idx >> 4, c8 = idx & 15, bk = r >> 4;
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (bk == v) {
-          w = *reinterpret_cast<const uint4*>(X + KX_RB + sw_chunk(r, c8, 64));
-        } else if (bk < v) {
-          float x[8];
-          kg_unpack8(*reinterpret_cast<const uint4*>(X + KX_RB + sw_chunk(r, c8, 64)), x);
+    // ---- the decay-weighted products, one 16-token block pair per MMA step (K = 16):
+    //   Z_b[i][r]  = sum_{c in b} Rb[c][i] dM[r][c]   (r >= 16 b)   rowM_r = Lk-side factor . sum_b F(a, b) Z_b
+    //   Zp_b       likewise with dP                                  rowP_r
+    //   Y_a[i][c]  = sum_{r in a} Lk[r][i] dM[r][c] + Lq[r][i] dP[r][c]   (c < 16 a + 16)
+    //                                                                col_c = sum_{a >= b} F(a, b) Y_a
+    // with F(a, b) = exp2(gx[a] - gx[b]) per channel applied in FP32 afterwards, so both sides of every
+    // pair (r, c) carry the same BF16 roundings (Lk_r, Rb_c, dM_rc) and cancel in the cumulative sum.
+    if (tid == 0) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] *= fab[kg_pair(v, bk)][8 * c8 + e];
-          w = kg_pack8(x);
-        }
-        *reinterpret_cast<uint4*>(dst + sw_chunk(r, c8, 64)) = w;
+      for (int b = 0; b < 4; ++b) {
+        const int n = 64 - 16 * b;
+        mma_ss(tb + KGT_Z + kZOff[b], desc_mn(s_rb, 64, b), desc_k(s_dm, 64, b, 16 * b), idesc(128, n, 1, 0), 0u);
+        mma_ss(tb + KGT_ZP + kZOff[b], desc_mn(s_rb, 64, b), desc_k(s_dp, 64, b, 16 * b), idesc(128, n, 1, 0), 0u);
       }
-    };
-    build_r(0, X + KX_V0);
-    to_tc();
-    for (int v = 0; v < 4 && ok; ++v) {
-      if (tid == 0) {
-        const uint32_t sv = (v & 1) ? s_v1 : s_v0;
-        for (int ks = 0; ks <= v; ++ks) {
-          mma_ss(tb + KGT_A1 + 16 * v, desc_mn(sv, 64, ks), desc_k(s_dm, 64, ks, 16 * v), idesc(128, 16, 1, 0),
-                 ks > 0);
-          mma_ss(tb + KGT_A3 + 16 * v, desc_mn(sv, 64, ks), desc_k(s_dp, 64, ks, 16 * v), idesc(128, 16, 1, 0),
-                 ks > 0);
-        }
-        commit();
-      }
-      if (v + 1 < 4) build_r(v + 1, X + ((v & 1) ? KX_V0 : KX_V1));   // the other buffer, while the MMA runs
-      if (!(ok = mma_wait())) break;
-      to_tc();
+      commit();
     }
-    if (!ok) break;
-    // ---- columns of block b: col^T slices (A4) from C_b = Lk . exp2(gx[blk r] - gx[b]), D_b likewise (rows >= 16 b)
-    for (int b = 0; b < 4 && ok; ++b) {
-#pragma unroll 2
-      for (int it = 0; it < 8; ++it) {
-        const int idx = tid + 256 * it, half = idx >> 10, r = (idx >> 4) & 63, c8 = idx & 15, bk = r >> 4;
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        const uint8_t* src = X + (half ? KX_LQ : KX_LK) + sw_chunk(r, c8, 64);
-        if (bk == b) {
-          w = *reinterpret_cast<const uint4*>(src);
-        } else if (bk > b) {
-          float x[8];
-          kg_unpack8(*reinterpret_cast<const uint4*>(src), x);
+    if (!(ok = mma_wait())) break;
+    float rowm[32], rowp[32];
+    {
+      const int i = lt;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] *= fab[kg_pair(bk, b)][8 * c8 + e];
-          w = kg_pack8(x);
+      for (int h = 0; h < 2; ++h) {
+        const int aa = (c0 >> 4) + h;   // the block of columns c0 + 16 h .. + 15
+        float zm[16], zp[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) rowm[16 * h + e] = rowp[16 * h + e] = 0.f;
+        for (int b = 0; b <= aa; ++b) {
+          const float f = b == aa ? 1.f : fab[kg_pair(aa, b)][i];
+          tmem_ld16(taddr(tb, wq * 32, KGT_Z + kZOff[b] + 16 * (aa - b)), zm);
+          tmem_ld16(taddr(tb, wq * 32, KGT_ZP + kZOff[b] + 16 * (aa - b)), zp);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            rowm[16 * h + e] = fmaf(f, zm[e], rowm[16 * h + e]);
+            rowp[16 * h + e] = fmaf(f, zp[e], rowp[16 * h + e]);
+          }
         }
-        *reinterpret_cast<uint4*>(X + (half ? KX_V1 : KX_V0) + sw_chunk(r, c8, 64)) = w;
       }
-      to_tc();
-      if (tid == 0) {
-        for (int ks = b; ks < 4; ++ks) {
-          mma_ss(tb + KGT_A4 + 16 * b, desc_mn(s_v0, 64, ks), desc_k(s_dmt, 64, ks, 16 * b), idesc(128, 16, 1, 0),
-                 ks > b);
-          mma_ss(tb + KGT_A4 + 16 * b, desc_mn(s_v1, 64, ks), desc_k(s_dpt, 64, ks, 16 * b), idesc(128, 16, 1, 0),
-                 1u);
-        }
-        commit();
-      }
-      if (!(ok = mma_wait())) break;
     }
-    if (!ok) break;
+    to_tc();   // (the Z columns are read before the Y products overwrite them)
+    if (tid == 0) {
+#pragma unroll
+      for (int aa = 0; aa < 4; ++aa) {
+        const int n = 16 * (aa + 1);
+        mma_ss(tb + KGT_Z + kYOff[aa], desc_mn(s_lk, 64, aa), desc_k(s_dmt, 64, aa), idesc(128, n, 1, 0), 0u);
+        mma_ss(tb + KGT_Z + kYOff[aa], desc_mn(s_lq, 64, aa), desc_k(s_dpt, 64, aa), idesc(128, n, 1, 0), 1u);
+      }
+      commit();
+    }
+    if (!(ok = mma_wait())) break;
+    float colv[32];
+    {
+      const int i = lt;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int b = (c0 >> 4) + h;   // the block of columns c0 + 16 h .. + 15
+        float y[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) colv[16 * h + e] = 0.f;
+        for (int aa = b; aa < 4; ++aa) {
+          const float f = aa == b ? 1.f : fab[kg_pair(aa, b)][i];
+          tmem_ld16(taddr(tb, wq * 32, KGT_Z + kYOff[aa] + c0 + 16 * h), y);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) colv[16 * h + e] = fmaf(f, y[e], colv[16 * h + e]);
+        }
+      }
+    }
     {  // final pass: the block-relative factors, dq^T, dk^T, dG^T; dg = reverse cumulative sum of dG
       const int i = lt;
-      float rm[32], rp[32], cl[32], aq[32], ak[32];
-      tld32(KGT_A1, rm);
-      tld32(KGT_A3, rp);
-      tld32(KGT_A4, cl);
+      const float* rm = rowm;
+      const float* rp = rowp;
+      const float* cl = colv;
+      float aq[32], ak[32];
       tld32(KGT_DQ, aq);
       tld32(KGT_DK, ak);
 #pragma unroll
