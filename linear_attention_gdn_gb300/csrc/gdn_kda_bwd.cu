@@ -76,8 +76,12 @@ constexpr int KGT_DQ = 0, KGT_DK = 64, KGT_A0 = 128, KGT_A1 = 192, KGT_A2 = 256,
               KGT_A5 = 448;
 // the decay-weighted products (every other result is dead by then): Z_b (64 - 16 b columns each, from
 // column 16 b of the result), Zp_b, then Y_a (16 a + 16 columns each) over the Z columns
-constexpr int KGT_Z = 128, KGT_ZP = 288;
+// dG^T of the value head takes over A1 once A1 is read; the decay-weighted products then use the other
+// result columns: Z_b (64 - 16 b columns each, from column 16 b of the result) from column 256, Zp_b
+// at kZPCol[b], and Y_a (16 a + 16 columns each) over the Z columns
+constexpr int KGT_DG = KGT_A1, KGT_Z = 256;
 __constant__ int kZOff[4] = {0, 64, 112, 144};
+__constant__ int kZPCol[4] = {128, 416, 464, 496};
 __constant__ int kYOff[4] = {0, 16, 48, 96};
 
 __device__ __forceinline__ int kg_pair(int a, int b) { return a * (a - 1) / 2 + b; }   // b < a
@@ -168,6 +172,9 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
   auto kraw = [&](int r, int i) { return bf16_at(kq, r, i, 128); };
   auto qraw = [&](int r, int i) { return bf16_at(kq, 64 + r, i, 128); };
   auto tld32 = [&](int col, float* o) { tmem_ld32(taddr(tb, wq * 32, col + c0), o); };
+  auto tld16c = [&](int col, float* o) { tmem_ld16(taddr(tb, wq * 32, col), o); };   // absolute column
+  auto tst16c = [&](int col, const float* v) { tmem_st16(taddr(tb, wq * 32, col), v); };
+  constexpr int kZPColH[4] = {128, 416, 464, 496};   // (kZPCol, as compile-time values for the MMA issue)
   auto tst32 = [&](int col, const float* v) {
     tmem_st16(taddr(tb, wq * 32, col + c0), v);
     tmem_st16(taddr(tb, wq * 32, col + c0 + 16), v + 16);
@@ -319,36 +326,40 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
         mma_ss(tb + KGT_A2, desc_k(s_wd, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
       commit();
     }
-    float dGt[32], gam[32];   // dG^T[i][c0 + e] of this value head; exp2(G) at those entries
-    {  // side work: the A1 (dO S^T)^T and A3 (dKd^T) terms into dq^T, dk^T, dG^T and dG_L
+    {  // side work: the A1 (dO S^T)^T and A3 (dKd^T) terms into dq^T, dk^T, dG_L and dG^T, which takes
+       // over A1's columns for the rest of the value head
       const int i = lt;
-      float p1[32], p3[32], aq[32], ak[32];
-      tld32(KGT_A1, p1);
-      tld32(KGT_A3, p3);
-      if (hh > 0) {
-        tld32(KGT_DQ, aq);
-        tld32(KGT_DK, ak);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) aq[e] = ak[e] = 0.f;
-      }
       const float GLi = glL[i];
       float kdsum = 0.f;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const int cb = c0 + 16 * h;
+        float p1[16], p3[16], aq[16], ak[16], dg[16];
+        tld16c(KGT_A1 + cb, p1);
+        tld16c(KGT_A3 + cb, p3);
+        if (hh > 0) {
+          tld16c(KGT_DQ + cb, aq);
+          tld16c(KGT_DK + cb, ak);
+        } else {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int r = c0 + e;
-        const float Gri = Gm[r * D + i];
-        const float gm = exp2f(Gri), Ee = exp2f(GLi - Gri);
-        gam[e] = gm;
-        const float qh = rq[r] * qraw(r, i), kh = rk[r] * kraw(r, i);
-        aq[e] = fmaf(a.scale * gm, p1[e], aq[e]);
-        ak[e] = fmaf(Ee, p3[e], ak[e]);
-        const float kdp = kh * Ee * p3[e];
-        dGt[e] = a.scale * qh * gm * p1[e] - kdp;
-        kdsum += kdp;
+          for (int e = 0; e < 16; ++e) aq[e] = ak[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int r = cb + e;
+          const float Gri = Gm[r * D + i];
+          const float gm = exp2f(Gri), Ee = exp2f(GLi - Gri);
+          const float qh = rq[r] * qraw(r, i), kh = rk[r] * kraw(r, i);
+          aq[e] = fmaf(a.scale * gm, p1[e], aq[e]);
+          ak[e] = fmaf(Ee, p3[e], ak[e]);
+          const float kdp = kh * Ee * p3[e];
+          dg[e] = a.scale * qh * gm * p1[e] - kdp;
+          kdsum += kdp;
+        }
+        tst16c(KGT_DQ + cb, aq);
+        tst16c(KGT_DK + cb, ak);
+        tst16c(KGT_DG + cb, dg);
       }
-      tst32(KGT_DQ, aq);
-      tst32(KGT_DK, ak);
       tmem_wait_st();
       dgl[wg][i] += kdsum;
     }
@@ -409,17 +420,23 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
     }
     {  // dY^T (A2): dk^T += beta gamma . dY, dG^T += beta K~ . dY
       const int i = lt;
-      float y[32], ak[32];
-      tld32(KGT_A2, y);
-      tld32(KGT_DK, ak);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const int cb = c0 + 16 * h;
+        float y[16], ak[16], dg[16];
+        tld16c(KGT_A2 + cb, y);
+        tld16c(KGT_DK + cb, ak);
+        tld16c(KGT_DG + cb, dg);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int r = c0 + e;
-        const float bg = bs[r] * gam[e];
-        ak[e] = fmaf(bg, y[e], ak[e]);
-        dGt[e] = fmaf(bg * rk[r] * kraw(r, i), y[e], dGt[e]);
+        for (int e = 0; e < 16; ++e) {
+          const int r = cb + e;
+          const float bg = bs[r] * exp2f(Gm[r * D + i]);
+          ak[e] = fmaf(bg, y[e], ak[e]);
+          dg[e] = fmaf(bg * rk[r] * kraw(r, i), y[e], dg[e]);
+        }
+        tst16c(KGT_DK + cb, ak);
+        tst16c(KGT_DG + cb, dg);
       }
-      tst32(KGT_DK, ak);
       tmem_wait_st();
     }
     to_tc();
@@ -520,31 +537,48 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
       for (int b = 0; b < 4; ++b) {
         const int n = 64 - 16 * b;
         mma_ss(tb + KGT_Z + kZOff[b], desc_mn(s_rb, 64, b), desc_k(s_dm, 64, b, 16 * b), idesc(128, n, 1, 0), 0u);
-        mma_ss(tb + KGT_ZP + kZOff[b], desc_mn(s_rb, 64, b), desc_k(s_dp, 64, b, 16 * b), idesc(128, n, 1, 0), 0u);
+        mma_ss(tb + kZPColH[b], desc_mn(s_rb, 64, b), desc_k(s_dp, 64, b, 16 * b), idesc(128, n, 1, 0), 0u);
       }
       commit();
     }
     if (!(ok = mma_wait())) break;
-    float rowm[32], rowp[32];
-    {
+    {  // rows: rowM = sum_b F(a, b) Z_b, rowP likewise (block a of the row); then dq^T += lam rowP + dP_rr k^,
+       // dk^T += lam rowM + dP_rr q^, dG^T += Lk rowM + Lq rowP
       const int i = lt;
-#pragma unroll
+#pragma unroll 1
       for (int h = 0; h < 2; ++h) {
-        const int aa = (c0 >> 4) + h;   // the block of columns c0 + 16 h .. + 15
-        float zm[16], zp[16];
+        const int aa = (c0 >> 4) + h, cb = c0 + 16 * h;
+        float rm[16], rp[16], z[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) rowm[16 * h + e] = rowp[16 * h + e] = 0.f;
+        for (int e = 0; e < 16; ++e) rm[e] = rp[e] = 0.f;
         for (int b = 0; b <= aa; ++b) {
           const float f = b == aa ? 1.f : fab[kg_pair(aa, b)][i];
-          tmem_ld16(taddr(tb, wq * 32, KGT_Z + kZOff[b] + 16 * (aa - b)), zm);
-          tmem_ld16(taddr(tb, wq * 32, KGT_ZP + kZOff[b] + 16 * (aa - b)), zp);
+          tld16c(KGT_Z + kZOff[b] + 16 * (aa - b), z);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            rowm[16 * h + e] = fmaf(f, zm[e], rowm[16 * h + e]);
-            rowp[16 * h + e] = fmaf(f, zp[e], rowp[16 * h + e]);
-          }
+          for (int e = 0; e < 16; ++e) rm[e] = fmaf(f, z[e], rm[e]);
+          tld16c(kZPCol[b] + 16 * (aa - b), z);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) rp[e] = fmaf(f, z[e], rp[e]);
         }
+        float aq[16], ak[16], dg[16];
+        tld16c(KGT_DQ + cb, aq);
+        tld16c(KGT_DK + cb, ak);
+        tld16c(KGT_DG + cb, dg);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int r = cb + e;
+          const float lam = exp2f(Gm[r * D + i] - gx[aa][i]);
+          const float kh = rk[r] * kraw(r, i), qh = rq[r] * qraw(r, i);
+          aq[e] += lam * rp[e] + pdiag[r] * kh;
+          ak[e] += lam * rm[e] + pdiag[r] * qh;
+          // (k^ lam and q^ lam as the BF16 Lk, Lq that the column products read: see below)
+          dg[e] += bf16_at(X + KX_LK, r, i, 64) * rm[e] + bf16_at(X + KX_LQ, r, i, 64) * rp[e];
+        }
+        tst16c(KGT_DQ + cb, aq);
+        tst16c(KGT_DK + cb, ak);
+        tst16c(KGT_DG + cb, dg);
       }
+      tmem_wait_st();
     }
     to_tc();   // (the Z columns are read before the Y products overwrite them)
     if (tid == 0) {
@@ -557,59 +591,55 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
       commit();
     }
     if (!(ok = mma_wait())) break;
-    float colv[32];
-    {
+    {  // columns: col = sum_{a >= b} F(a, b) Y_a (block b of the column); dk^T += ein col, dG^T -= Rb col
+       // (Rb = k^ ein in BF16, as the row products read it, so that each pair (r, c) cancels in the
+       // cumulative sum to FP32 accuracy)
       const int i = lt;
-#pragma unroll
+#pragma unroll 1
       for (int h = 0; h < 2; ++h) {
-        const int b = (c0 >> 4) + h;   // the block of columns c0 + 16 h .. + 15
-        float y[16];
+        const int b = (c0 >> 4) + h, cb = c0 + 16 * h;
+        float cl[16], y[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) colv[16 * h + e] = 0.f;
+        for (int e = 0; e < 16; ++e) cl[e] = 0.f;
         for (int aa = b; aa < 4; ++aa) {
           const float f = aa == b ? 1.f : fab[kg_pair(aa, b)][i];
-          tmem_ld16(taddr(tb, wq * 32, KGT_Z + kYOff[aa] + c0 + 16 * h), y);
+          tld16c(KGT_Z + kYOff[aa] + cb, y);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) colv[16 * h + e] = fmaf(f, y[e], colv[16 * h + e]);
+          for (int e = 0; e < 16; ++e) cl[e] = fmaf(f, y[e], cl[e]);
         }
+        float ak[16], dg[16];
+        tld16c(KGT_DK + cb, ak);
+        tld16c(KGT_DG + cb, dg);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int r = cb + e;
+          const float ein = exp2f(gx[b][i] - Gm[r * D + i]);
+          ak[e] += ein * cl[e];
+          dg[e] -= bf16_at(X + KX_RB, r, i, 64) * cl[e];
+        }
+        tst16c(KGT_DK + cb, ak);
+        tst16c(KGT_DG + cb, dg);
       }
+      tmem_wait_st();
     }
-    {  // final pass: the block-relative factors, dq^T, dk^T, dG^T; dg = reverse cumulative sum of dG
+    {  // dG_L at the last token, then dg = reverse cumulative sum of dG over the chunk's tokens
       const int i = lt;
-      const float* rm = rowm;
-      const float* rp = rowp;
-      const float* cl = colv;
-      float aq[32], ak[32];
-      tld32(KGT_DQ, aq);
-      tld32(KGT_DK, ak);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int r = c0 + e, bk = r >> 4;
-        const float d = Gm[r * D + i] - gx[bk][i];
-        const float lam = exp2f(d), ein = exp2f(-d);
-        const float kh = rk[r] * kraw(r, i), qh = rq[r] * qraw(r, i);
-        const float rowM = lam * rm[e], rowP = lam * rp[e], col = ein * cl[e];
-        ak[e] += rowM + col + pdiag[r] * qh;
-        aq[e] += rowP + pdiag[r] * kh;
-        // dG: k^ . rowM + q^ . rowP - k^ . col, with k^ lam, q^ lam and k^ ein taken as the BF16 Lk, Lq, Rb
-        // that the opposite side's block products read, so that every pair (r, c) enters both sums with the
-        // same rounding and the reverse cumulative sum cancels it to FP32 accuracy
-        dGt[e] += bf16_at(X + KX_LK, r, i, 64) * rm[e] + bf16_at(X + KX_LQ, r, i, 64) * rp[e] -
-                  bf16_at(X + KX_RB, r, i, 64) * cl[e];
-      }
-      tst32(KGT_DQ, aq);
-      tst32(KGT_DK, ak);
-      if (L - 1 >= c0 && L - 1 < c0 + 32) {   // dG_L at the last token
-        const float gl = dgl[0][i] + dgl[1][i];
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (c0 + e == L - 1) dGt[e] += gl;
-      }
+      const float gl = dgl[0][i] + dgl[1][i];
       float acc = 0.f;
+#pragma unroll 1
+      for (int h = 1; h >= 0; --h) {   // this thread's 32 columns, high to low
+        const int cb = c0 + 16 * h;
+        float dg[16];
+        tld16c(KGT_DG + cb, dg);
 #pragma unroll
-      for (int e = 31; e >= 0; --e) {
-        acc += (c0 + e < L) ? dGt[e] : 0.f;
-        dGt[e] = acc;
+        for (int e = 15; e >= 0; --e) {
+          const int r = cb + e;
+          float x = r < L ? dg[e] : 0.f;
+          if (r == L - 1) x += gl;
+          acc += x;
+          dg[e] = acc;
+        }
+        tst16c(KGT_DG + cb, dg);
       }
       cum[wg][i] = acc;
       tmem_wait_st();
@@ -618,10 +648,16 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
     {
       const int i = lt;
       const float add = wg == 0 ? cum[1][i] : 0.f;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const int cb = c0 + 16 * h;
+        float dg[16];
+        tld16c(KGT_DG + cb, dg);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int r = c0 + e;
-        if (r < L) a.dg[((size_t)(tok0 + r) * a.HV + hv) * D + i] = dGt[e] + add;
+        for (int e = 0; e < 16; ++e) {
+          const int r = cb + e;
+          if (r < L) a.dg[((size_t)(tok0 + r) * a.HV + hv) * D + i] = dg[e] + add;
+        }
       }
       if (tid < L) {
         float db = rowdb[0][tid] + rowdb[1][tid];
