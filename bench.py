@@ -1,7 +1,7 @@
 """Benchmark of the GB300 chunked Gated DeltaNet training step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 2] [--op fwd+bwd|fwd|ckpt]
+                    [--workload 2] [--op fwd+bwd|fwd|ckpt] [--kda]
 
 A step is one pass of the whole hot path over one batch: gdn_fwd (writing the
 saved states) + gdn_bwd on the packed 4-document workload of 262,144 tokens
@@ -413,6 +413,13 @@ def run_ours(args, rank, world, local_rank):
     def timed(op, K, W):
         return timed_replicas(lambda: step(op), K, W, barrier, allmax, event_clock)
 
+    if args.kda:   # the per-channel-decay form alone
+        res = time_kda(args.steps, args.warmup)
+        return {"metric": "KDA fwd+bwd Mtokens/s on 1 GB300 (H16/HV48, d=128)", "value": res["Mtokens_per_s"],
+                "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": res["ms"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic", "config": {"workload": w.name, "op": "kda fwd+bwd"},
+                "kda": res}
     op = args.op
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
@@ -684,6 +691,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--op", default="fwd+bwd", choices=("fwd", "fwd+bwd", "ckpt"))
+    ap.add_argument("--kda", action="store_true",
+                    help="time only the per-channel-decay (KDA) fwd+bwd on the workload (for profiling)")
     ap.add_argument("--form", default="full", choices=("full", "replay"),
                     help="saved form of the timed step (the other one is timed in ops)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -706,7 +715,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     out = run_ours(args, rank, world, local_rank)
     if rank == 0:
-        if not args.no_cpu:
+        if not args.no_cpu and not args.kda:
             from linear_attention_gdn_gb300 import inputs
             w = inputs.workload(args.workload)
             threads = cpu_count()
