@@ -220,3 +220,57 @@ def test_kda_uniform_decay_backward_matches_gdn():
     for n in ("dq", "dk", "dv", "dbeta"):
         compare(f"kda_vs_gdn/{n}", out[n].double().cpu().numpy(), ref[n].double().cpu().numpy())
     compare("kda_vs_gdn/dg", out["dg"].double().sum(-1).cpu().numpy(), ref["dg"].double().cpu().numpy())
+
+
+def test_kda_full_size_sampled():
+    """The bench workload's shapes (four documents, 262,144 tokens, H = 16, HV = 48) in the launch
+    configuration bench.py times, KDA inputs of that workload (per-channel decays logsigmoid(U(2, 6)));
+    sampled output windows of every gradient against the KDA oracle run on a warmed-up sub-range whose
+    damping (the product of the slowest channel's decays of the group, which bounds the dropped history:
+    |(I - beta k^ k^^T) Diag(a)| <= max a) is below 1e-12 on both sides."""
+    from oracle import ref
+    import linear_attention_gdn_gb300 as gdn
+    w = inputs.workload(2)
+    x = inputs.generate_kda(w, "cuda")
+    cu_dev = torch.from_numpy(w.cu_seqlens).cuda()
+    prob = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm, w.segments)
+    buf = gdn.Buffers(prob, w.cu_seqlens, kda=True)
+    got = dict(o=torch.empty((w.T, w.HV, 128), dtype=torch.bfloat16, device="cuda"),
+               dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]), dv=torch.empty_like(x["v"]),
+               dg=torch.empty_like(x["g"]), dbeta=torch.empty_like(x["beta"]))
+    gdn.gdn_kda_fwd(prob, x["q"], x["k"], x["v"], x["g"], x["beta"], cu_dev, w.cu_seqlens, got["o"], buf.saved,
+                    buf.workspace)
+    gdn.gdn_kda_bwd(prob, x["q"], x["k"], x["v"], x["g"], x["beta"], cu_dev, w.cu_seqlens, x["dO"], buf.saved,
+                    got["dq"], got["dk"], got["dv"], got["dg"], got["dbeta"], buf.workspace)
+    assert gdn.gdn_device_status(buf.workspace) == 0
+    del buf
+    cu = w.cu_seqlens
+    G = w.HV // w.H
+    rng = np.random.default_rng(202)
+    win = 128
+    for i, d in enumerate([0, 3, 1, 2]):
+        j = int(rng.integers(w.H))
+        Ld = int(cu[d + 1] - cu[d])
+        t0 = [0, Ld - win, int(rng.integers(win, Ld - 2 * win)), int(rng.integers(win, Ld - 2 * win))][i]
+        hs = slice(j * G, (j + 1) * G)
+        s = int(cu[d])
+        gdoc = x["g"][s:s + Ld, hs].amax(dim=2).double().cpu().numpy().T   # slowest channel per token and head
+        a, b, left, right = ref.window(gdoc, t0, t0 + win, warm=1024)
+        assert left <= 1e-12 and right <= 1e-12
+        sl = slice(s + a, s + b)
+        q = _f64(x["q"][sl, j])
+        k = _f64(x["k"][sl, j])
+        v = _f64(x["v"][sl, hs]).transpose(1, 0, 2).copy()
+        g = _f64(x["g"][sl, hs]).transpose(1, 0, 2).copy()
+        beta = _f64(x["beta"][sl, hs]).T.copy()
+        dO = _f64(x["dO"][sl, hs]).transpose(1, 0, 2).copy()
+        r = kda.group(q, k, v, g, beta, dO, l2norm=w.l2norm, scale=w.scale)
+        r0, r1 = t0 - a, t0 + win - a
+        w0, w1 = s + t0, s + t0 + win
+        tag = f"kda_full/doc{d}/group{j}/tokens{t0}-{t0 + win}"
+        compare(f"{tag}/o", got["o"][w0:w1, hs].double().cpu().numpy(), r["o"][:, r0:r1].transpose(1, 0, 2))
+        compare(f"{tag}/dq", got["dq"][w0:w1, j].double().cpu().numpy(), r["dq"][r0:r1])
+        compare(f"{tag}/dk", got["dk"][w0:w1, j].double().cpu().numpy(), r["dk"][r0:r1])
+        compare(f"{tag}/dv", got["dv"][w0:w1, hs].double().cpu().numpy(), r["dv"][:, r0:r1].transpose(1, 0, 2))
+        compare(f"{tag}/dg", got["dg"][w0:w1, hs].double().cpu().numpy(), r["dg"][:, r0:r1].transpose(1, 0, 2))
+        compare(f"{tag}/dbeta", got["dbeta"][w0:w1, hs].double().cpu().numpy(), r["dbeta"][:, r0:r1].T)
