@@ -25,7 +25,7 @@
 // exp(G_r - G_c) k^_c = exp(G_r - Gx_a) F(a, b) Rb_c with F(a, b) = exp(Gx_a - Gx_b) per channel.
 // The block products (one K = 16 MMA step each) are summed with F in FP32 afterwards.
 //
-// kda_grad_kernel: one CTA of 256 threads per (chunk, q/k head); the group's value heads one after
+// kda_grad_kernel: one CTA of 512 threads per (chunk, q/k head); the group's value heads one after
 // another, each a fixed sequence of MMA groups and CUDA-core passes (no overlap between heads); dq^
 // and dk^ accumulate over the heads in TMEM.
 #include <cstring>
@@ -86,6 +86,28 @@ __constant__ int kYOff[4] = {0, 16, 48, 96};
 
 __device__ __forceinline__ int kg_pair(int a, int b) { return a * (a - 1) / 2 + b; }   // b < a
 
+// four warpgroups; thread t owns row t % 128 (TMEM lane) and KG_CW of the 64 token columns of a result
+constexpr int KG_WG = 4;
+constexpr int KG_THREADS = 128 * KG_WG;
+constexpr int KG_CW = 64 / KG_WG;
+constexpr int KG_NH = KG_CW / 16;   // 16-column groups per thread
+static_assert(KG_CW % 16 == 0, "whole 16-column groups per thread");
+
+// sum over the 32 lanes of a warp of column `lane & 15` of v[16] (fixed order)
+__device__ __forceinline__ float kg_colsum16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int kq = 0; kq < o; ++kq) {
+      const float mine = up ? v[kq + o] : v[kq];
+      const float other = up ? v[kq] : v[kq + o];
+      v[kq] = mine + __shfl_xor_sync(0xffffffffu, other, o);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+
 // sum over the 32 lanes of a warp of column `lane` of v[32] (fixed order)
 __device__ __forceinline__ float colsum32(float (&v)[32], int lane) {
 #pragma unroll
@@ -117,22 +139,22 @@ __device__ __forceinline__ float bf16_at(const uint8_t* tile, int r, int c, int 
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + sw_off(r, c, R)));
 }
 
-__global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant__ KdaGradArgs a) {
+__global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_constant__ KdaGradArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
   __shared__ __align__(16) float rk[CH], rq[CH], bs[CH];
   __shared__ __align__(16) float gx[4][D];     // log2 decay entering each 16-token block
   __shared__ __align__(16) float fab[6][D];    // exp2(gx[a] - gx[b]), b < a
   __shared__ __align__(16) float glL[D];       // log2 G_L per channel
-  __shared__ __align__(16) float dgl[2][D];    // partial dG_L per key channel (two column halves)
+  __shared__ __align__(16) float dgl[KG_WG][D];   // partial dG_L per key channel (per warpgroup)
   __shared__ __align__(16) float red[8][CH];   // per-warp partial column sums
-  __shared__ __align__(16) float rowdb[2][CH]; // partial row sums (two column halves)
-  __shared__ __align__(16) float cum[2][D];    // column-half totals of the reverse cumulative sum
+  __shared__ __align__(16) float rowdb[KG_WG][CH];   // partial row sums (per warpgroup's columns)
+  __shared__ __align__(16) float cum[KG_WG][D];      // per-warpgroup totals of the reverse cumulative sum
   __shared__ __align__(16) float pdiag[CH];    // dP_rr (kept out of the decay-weighted products)
   __shared__ uint64_t bar_qk, bar_ld, bar_m;
   __shared__ uint32_t tslot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = tid >> 7, lt = tid & 127, wq = warp & 3;
-  const int c0 = 32 * wg;   // this thread's 32 columns (tokens) of a 64-column result
+  const int c0 = KG_CW * wg;   // this thread's columns (tokens) of a 64-column result
   const int c = blockIdx.x / a.H, j = blockIdx.x % a.H;
   if (*(volatile int*)a.err) return;
   const int tok0 = a.chunk_tok0[c], L = a.chunk_len[c];
@@ -171,14 +193,14 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
   }
   auto kraw = [&](int r, int i) { return bf16_at(kq, r, i, 128); };
   auto qraw = [&](int r, int i) { return bf16_at(kq, 64 + r, i, 128); };
-  auto tld32 = [&](int col, float* o) { tmem_ld32(taddr(tb, wq * 32, col + c0), o); };
+  auto tldc = [&](int col, float* o) {   // this thread's KG_CW columns of a result
+    if constexpr (KG_CW == 32) tmem_ld32(taddr(tb, wq * 32, col + c0), o);
+    else tmem_ld16(taddr(tb, wq * 32, col + c0), o);
+  };
   auto tld16c = [&](int col, float* o) { tmem_ld16(taddr(tb, wq * 32, col), o); };   // absolute column
   auto tst16c = [&](int col, const float* v) { tmem_st16(taddr(tb, wq * 32, col), v); };
   constexpr int kZPColH[4] = {128, 416, 464, 496};   // (kZPCol, as compile-time values for the MMA issue)
-  auto tst32 = [&](int col, const float* v) {
-    tmem_st16(taddr(tb, wq * 32, col + c0), v);
-    tmem_st16(taddr(tb, wq * 32, col + c0 + 16), v + 16);
-  };
+
   auto to_tc = [&]() {   // generic smem / TMEM writes -> visible to the next MMAs
     fence_async_smem();
     tc_fence_before();
@@ -201,9 +223,9 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
   // M = 64 results: this thread's rows ra, ra + 8 and, per load g, columns c0 + 16 g + 8 (i >> 2) +
   // 2 (lane & 3) + (i & 1) for value i
   const int ra = 16 * wq + (lane >> 2);
-  auto ld_m64 = [&](int col, uint32_t (&u)[2][8]) {
-    tmem_ld_m64_async(taddr(tb, wq * 32, col + c0), u[0]);
-    tmem_ld_m64_async(taddr(tb, wq * 32, col + c0 + 16), u[1]);
+  auto ld_m64 = [&](int col, uint32_t (&u)[KG_NH][8]) {
+#pragma unroll
+    for (int g = 0; g < KG_NH; ++g) tmem_ld_m64_async(taddr(tb, wq * 32, col + c0 + 16 * g), u[g]);
     tmem_wait_ld();
   };
   const uint32_t s_s = smem_u32(X + KX_S), s_ds = smem_u32(X + KX_DS), s_vn = smem_u32(X + KX_VN),
@@ -234,7 +256,7 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
       for (int r = 0; r < L; ++r) bulk_load(Gm + r * D, gp + (size_t)r * a.HV * D, 512u, &bar_ld);
     }
     ld_pend = true;
-    for (int idx = tid; idx < (CH - L) * 32; idx += 256)   // g rows past L: zero
+    for (int idx = tid; idx < (CH - L) * 32; idx += KG_THREADS)   // g rows past L: zero
       *reinterpret_cast<float4*>(Gm + (L + (idx >> 5)) * D + 4 * (idx & 31)) = make_float4(0.f, 0.f, 0.f, 0.f);
     if (tid < CH) bs[tid] = tid < L ? a.beta[(size_t)(tok0 + tid) * a.HV + hv] : 0.f;
     ok = __syncthreads_and(mbar_wait(&bar_ld, ldph, a.err));
@@ -256,7 +278,7 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
         for (int b = 0; b < aa; ++b) fab[kg_pair(aa, b)][i] = exp2f(gx[aa][i] - gx[b][i]);
     }
     if (L < CH) {   // zero the dO, V rows past the document end
-      for (int idx = tid; idx < (CH - L) * 32; idx += 256) {
+      for (int idx = tid; idx < (CH - L) * 32; idx += KG_THREADS) {
         const int t = idx >> 5, tile = (idx >> 4) & 1, c8 = idx & 15;
         *reinterpret_cast<uint4*>(X + (tile ? KX_V : KX_DO) + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
       }
@@ -280,7 +302,7 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
     {  // while MA runs: gamma_L . <S, dS'> per key channel over this thread's 64 value rows
       const int i = lt;
       float acc0 = 0.f, acc1 = 0.f;
-      for (int jj = 64 * wg; jj < 64 * wg + 64; jj += 2) {
+      for (int jj = (128 / KG_WG) * wg; jj < (128 / KG_WG) * (wg + 1); jj += 2) {
         acc0 = fmaf(bf16_at(X + KX_S, jj, i, 128), bf16_at(X + KX_DS, jj, i, 128), acc0);
         acc1 = fmaf(bf16_at(X + KX_S, jj + 1, i, 128), bf16_at(X + KX_DS, jj + 1, i, 128), acc1);
       }
@@ -290,25 +312,25 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
     // ---- HA: dW^T (= -A0) and K~ tiles for MB; dv from A2
     {
       const int i = lt;
-      float w[32], x[32];
-      tld32(KGT_A0, w);
-      tld32(KGT_A2, x);
+      float w[KG_CW], x[KG_CW];
+      tldc(KGT_A0, w);
+      tldc(KGT_A2, x);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < KG_CW / 8; ++q4) {
         float t8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) t8[e] = -w[q4 * 8 + e];
         *reinterpret_cast<uint4*>(X + KX_WD + sw_chunk(i, (c0 >> 3) + q4, 128)) = kg_pack8(t8);
       }
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {   // dv[r][j] = beta_r (T^T dX)[r][j], row lt = j
+      for (int e = 0; e < KG_CW; ++e) {   // dv[r][j] = beta_r (T^T dX)[r][j], row lt = j
         const int r = c0 + e;
         if (r < L) a.dv[((size_t)(tok0 + r) * a.HV + hv) * D + i] = __float2bfloat16_rn(bs[r] * x[e]);
       }
     }
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {   // K~[r] = rk_r k_r . exp2(G_r)
-      const int idx = tid + 256 * it, r = idx >> 4, c8 = idx & 15;
+    for (int it = 0; it < 1024 / KG_THREADS; ++it) {   // K~[r] = rk_r k_r . exp2(G_r)
+      const int idx = tid + KG_THREADS * it, r = idx >> 4, c8 = idx & 15;
       float kf[8], y[8];
       kg_unpack8(*reinterpret_cast<const uint4*>(kq + sw_chunk(r, c8, 128)), kf);
 #pragma unroll
@@ -332,7 +354,7 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
       const float GLi = glL[i];
       float kdsum = 0.f;
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < KG_NH; ++h) {
         const int cb = c0 + 16 * h;
         float p1[16], p3[16], aq[16], ak[16], dg[16];
         tld16c(KGT_A1 + cb, p1);
@@ -366,17 +388,17 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
     if (!(ok = mma_wait())) break;
     // ---- HB: dT = (dX V^T + dW K~^T) diag(beta), dbeta column sums of T . (those), dP tiles; dY terms
     {
-      uint32_t u6a[2][8], u6b[2][8], u2[2][8];
+      uint32_t u6a[KG_NH][8], u6b[KG_NH][8], u2[KG_NH][8];
       ld_m64(KGT_A5, u6a);
       ld_m64(KGT_A0, u6b);
       ld_m64(KGT_A4, u2);
-      float tbs[2][4];
+      float tbs[KG_NH][4];
 #pragma unroll
-      for (int g = 0; g < 2; ++g)
+      for (int g = 0; g < KG_NH; ++g)
 #pragma unroll
         for (int q = 0; q < 4; ++q) tbs[g][q] = 0.f;
 #pragma unroll
-      for (int g = 0; g < 2; ++g)
+      for (int g = 0; g < KG_NH; ++g)
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int r = ra + 8 * hr;
@@ -406,14 +428,14 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
         }
       // column sums over the warp's 16 rows: lanes with equal lane & 3 hold the same columns
 #pragma unroll
-      for (int g = 0; g < 2; ++g)
+      for (int g = 0; g < KG_NH; ++g)
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
           for (int o = 4; o <= 16; o <<= 1) tbs[g][q] += __shfl_xor_sync(0xffffffffu, tbs[g][q], o);
       if (lane < 4) {
 #pragma unroll
-        for (int g = 0; g < 2; ++g)
+        for (int g = 0; g < KG_NH; ++g)
 #pragma unroll
           for (int q = 0; q < 4; ++q) red[wq][c0 + 16 * g + 8 * (q >> 1) + 2 * lane + (q & 1)] = tbs[g][q];
       }
@@ -421,7 +443,7 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
     {  // dY^T (A2): dk^T += beta gamma . dY, dG^T += beta K~ . dY
       const int i = lt;
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < KG_NH; ++h) {
         const int cb = c0 + 16 * h;
         float y[16], ak[16], dg[16];
         tld16c(KGT_A2 + cb, y);
@@ -449,8 +471,8 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
     }
     // while M4 runs: the block-relative tiles Lk, Lq (exp2(G_r - gx[blk]) . k^, q^) and Rb (exp2(gx[blk] - G_c) . k^)
 #pragma unroll 2
-    for (int it = 0; it < 4; ++it) {
-      const int idx = tid + 256 * it, r = idx >> 4, c8 = idx & 15, bk = r >> 4;
+    for (int it = 0; it < 1024 / KG_THREADS; ++it) {
+      const int idx = tid + KG_THREADS * it, r = idx >> 4, c8 = idx & 15, bk = r >> 4;
       float kf[8], qf[8], lk[8], lq[8], rb[8];
       kg_unpack8(*reinterpret_cast<const uint4*>(kq + sw_chunk(r, c8, 128)), kf);
       kg_unpack8(*reinterpret_cast<const uint4*>(kq + sw_chunk(64 + r, c8, 128)), qf);
@@ -468,10 +490,10 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
     }
     if (!(ok = mma_wait())) break;
     {  // R1 -> BF16 tile for M5
-      uint32_t u[2][8];
+      uint32_t u[KG_NH][8];
       ld_m64(KGT_A5, u);
 #pragma unroll
-      for (int g = 0; g < 2; ++g)
+      for (int g = 0; g < KG_NH; ++g)
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
@@ -491,11 +513,11 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
     }
     if (!(ok = mma_wait())) break;
     {  // dA (strictly lower, rows < L): dM = diag(beta) dA tiles; dbeta row sums of dA . M
-      uint32_t u[2][8];
+      uint32_t u[KG_NH][8];
       ld_m64(KGT_A0, u);
       float rsum[2] = {0.f, 0.f};
 #pragma unroll
-      for (int g = 0; g < 2; ++g)
+      for (int g = 0; g < KG_NH; ++g)
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int r = ra + 8 * hr;
@@ -546,7 +568,7 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
        // dk^T += lam rowM + dP_rr q^, dG^T += Lk rowM + Lq rowP
       const int i = lt;
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < KG_NH; ++h) {
         const int aa = (c0 >> 4) + h, cb = c0 + 16 * h;
         float rm[16], rp[16], z[16];
 #pragma unroll
@@ -596,7 +618,7 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
        // cumulative sum to FP32 accuracy)
       const int i = lt;
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < KG_NH; ++h) {
         const int b = (c0 >> 4) + h, cb = c0 + 16 * h;
         float cl[16], y[16];
 #pragma unroll
@@ -624,10 +646,12 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
     }
     {  // dG_L at the last token, then dg = reverse cumulative sum of dG over the chunk's tokens
       const int i = lt;
-      const float gl = dgl[0][i] + dgl[1][i];
+      float gl = 0.f;
+#pragma unroll
+      for (int w = 0; w < KG_WG; ++w) gl += dgl[w][i];
       float acc = 0.f;
 #pragma unroll 1
-      for (int h = 1; h >= 0; --h) {   // this thread's 32 columns, high to low
+      for (int h = KG_NH - 1; h >= 0; --h) {   // this thread's columns, high to low
         const int cb = c0 + 16 * h;
         float dg[16];
         tld16c(KGT_DG + cb, dg);
@@ -647,9 +671,10 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
     __syncthreads();
     {
       const int i = lt;
-      const float add = wg == 0 ? cum[1][i] : 0.f;
+      float add = 0.f;   // the later columns' totals
+      for (int w = wg + 1; w < KG_WG; ++w) add += cum[w][i];
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < KG_NH; ++h) {
         const int cb = c0 + 16 * h;
         float dg[16];
         tld16c(KGT_DG + cb, dg);
@@ -660,7 +685,9 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
         }
       }
       if (tid < L) {
-        float db = rowdb[0][tid] + rowdb[1][tid];
+        float db = 0.f;
+#pragma unroll
+        for (int w = 0; w < KG_WG; ++w) db += rowdb[w][tid];
 #pragma unroll
         for (int w = 0; w < 4; ++w) db += red[w][tid];
         a.dbeta[(size_t)(tok0 + tid) * a.HV + hv] = db;
@@ -672,17 +699,27 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
   }
   if (ok) {  // ---- item end: the L2-norm backward of the group sums dq^, dk^; dq, dk
     const int i = lt;
-    float aq[32], ak[32], pq[32], pk[32];
-    tld32(KGT_DQ, aq);
-    tld32(KGT_DK, ak);
+    float aq[KG_CW], ak[KG_CW], pq[KG_CW], pk[KG_CW];
+    tldc(KGT_DQ, aq);
+    tldc(KGT_DK, ak);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
+    for (int e = 0; e < KG_CW; ++e) {
       pq[e] = qraw(c0 + e, i) * aq[e];
       pk[e] = kraw(c0 + e, i) * ak[e];
     }
-    const float sq = colsum32(pq, lane), sk = colsum32(pk, lane);
-    red[wq][c0 + lane] = sq;
-    red[4 + wq][c0 + lane] = sk;
+    if constexpr (KG_CW == 32) {
+      const float sq = colsum32(*reinterpret_cast<float(*)[32]>(pq), lane);
+      const float sk = colsum32(*reinterpret_cast<float(*)[32]>(pk), lane);
+      red[wq][c0 + lane] = sq;
+      red[4 + wq][c0 + lane] = sk;
+    } else {
+      const float sq = kg_colsum16(*reinterpret_cast<float(*)[16]>(pq), lane);
+      const float sk = kg_colsum16(*reinterpret_cast<float(*)[16]>(pk), lane);
+      if (lane < 16) {
+        red[wq][c0 + lane] = sq;
+        red[4 + wq][c0 + lane] = sk;
+      }
+    }
     __syncthreads();
     if (tid < CH) {
       float xq = 0.f, xk = 0.f;
@@ -697,7 +734,7 @@ __global__ void __launch_bounds__(256, 1) kda_grad_kernel(const __grid_constant_
     }
     __syncthreads();
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
+    for (int e = 0; e < KG_CW; ++e) {
       const int r = c0 + e;
       if (r >= L) continue;
       float oq = aq[e], ok2 = ak[e];
@@ -768,7 +805,7 @@ static gdn_status run_kda_bwd(const Plan& P, const gdn_problem& pr, const void* 
   ga.scale = pr.scale;
   ga.err = reinterpret_cast<int*>(ws);
   prof_begin(K_KDA_GRAD, s);
-  kda_grad_kernel<<<P.NC * P.H, 256, KG_SMEM_ALLOC, s>>>(ga);
+  kda_grad_kernel<<<P.NC * P.H, KG_THREADS, KG_SMEM_ALLOC, s>>>(ga);
   prof_end(K_KDA_GRAD, s);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
