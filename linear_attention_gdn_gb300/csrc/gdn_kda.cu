@@ -73,8 +73,9 @@ __device__ __forceinline__ void ld8(const float* p, float (&f)[8]) {
   f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
-// One CTA per (chunk, value head); 128 threads, two CTAs per SM.
-__global__ void __launch_bounds__(128, 2) kda_prep_kernel(const __grid_constant__ KdaPrepArgs a) {
+// One CTA per (chunk, value head); two warpgroups, two CTAs per SM.
+constexpr int KP_THREADS = 256;
+__global__ void __launch_bounds__(KP_THREADS, 2) kda_prep_kernel(const __grid_constant__ KdaPrepArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
   __shared__ __align__(16) float rk[CH], rq[CH], bs[CH];
@@ -112,13 +113,13 @@ __global__ void __launch_bounds__(128, 2) kda_prep_kernel(const __grid_constant_
     const float* gp = a.g + ((size_t)tok0 * a.HV + hv) * D;
     for (int r = 0; r < L; ++r) bulk_load(Gm + r * D, gp + (size_t)r * a.HV * D, 512u, &bar_ld);
   }
-  for (int idx = tid; idx < (CH - L) * 32; idx += 128)   // rows past L: zero
+  for (int idx = tid; idx < (CH - L) * 32; idx += KP_THREADS)   // rows past L: zero
     *reinterpret_cast<float4*>(Gm + (L + (idx >> 5)) * D + 4 * (idx & 31)) = make_float4(0.f, 0.f, 0.f, 0.f);
   if (tid < CH) bs[tid] = tid < L ? a.beta[(size_t)(tok0 + tid) * a.HV + hv] : 0.f;
   __syncthreads();   // the barriers' initialisation is visible before any thread waits on them
   bool landed = __syncthreads_and(mbar_wait(&bar_ld, 0, a.err));
-  if (landed) {  // channel tid: the cumulative decay G in log2 units (rows past L keep G_{L-1}), the block
-                 // entries, the factors
+  if (landed && tid < 128) {  // channel tid: the cumulative decay G in log2 units (rows past L keep
+                              // G_{L-1}), the block entries, the factors
     const int i = tid;
     float run = 0.f, ref = 0.f, mx = 0.f;
     for (int r = 0; r < CH; ++r) {
@@ -168,10 +169,10 @@ __global__ void __launch_bounds__(128, 2) kda_prep_kernel(const __grid_constant_
     return;
   }
   if (L < CH) {
-    ut_zero_tail(kq, L, tid);
+    if (tid < 128) ut_zero_tail(kq, L, tid);
     __syncthreads();
   }
-  {
+  if (tid < 128) {
     const float rn = ut_row_rnorm(kq, tid, a.l2norm);
     if (tid < 64) rk[tid] = rn;
     else rq[tid - 64] = rn;
@@ -179,8 +180,8 @@ __global__ void __launch_bounds__(128, 2) kda_prep_kernel(const __grid_constant_
   __syncthreads();
   // ---- pass 1: Lk, Lq in place; Rb (own-block reference) into its tile
 #pragma unroll 2
-  for (int it = 0; it < 8; ++it) {
-    const int idx = tid + 128 * it, r = idx >> 4, c8 = idx & 15, blk = r >> 4;
+  for (int it = 0; it < 1024 / KP_THREADS; ++it) {
+    const int idx = tid + KP_THREADS * it, r = idx >> 4, c8 = idx & 15, blk = r >> 4;
     float g8[8], x8[8], kf[8], qf[8];
     ld8(Gm + r * D + 8 * c8, g8);
     ld8(&gx[blk][8 * c8], x8);
@@ -208,8 +209,8 @@ __global__ void __launch_bounds__(128, 2) kda_prep_kernel(const __grid_constant_
   // M^T | P^T products, two buffers in the (now dead) G region
   auto build_version = [&](int v, uint8_t* dst) {
 #pragma unroll 2
-    for (int it = 0; it < 8; ++it) {
-      const int idx = tid + 128 * it, r = idx >> 4, c8 = idx & 15, blk = r >> 4;
+    for (int it = 0; it < 1024 / KP_THREADS; ++it) {
+      const int idx = tid + KP_THREADS * it, r = idx >> 4, c8 = idx & 15, blk = r >> 4;
       uint4 w = make_uint4(0u, 0u, 0u, 0u);
       if (blk == v) {
         w = *reinterpret_cast<const uint4*>(rbt + sw_chunk(r, c8, 64));
@@ -278,8 +279,8 @@ __global__ void __launch_bounds__(128, 2) kda_prep_kernel(const __grid_constant_
   if (ok) {
     // ---- Kd = Rb . exp2(G_L - gx[blk]) in place; shipped now
 #pragma unroll 2
-    for (int it = 0; it < 8; ++it) {
-      const int idx = tid + 128 * it, r = idx >> 4, c8 = idx & 15, blk = r >> 4;
+    for (int it = 0; it < 1024 / KP_THREADS; ++it) {
+      const int idx = tid + KP_THREADS * it, r = idx >> 4, c8 = idx & 15, blk = r >> 4;
       float f[8], x[8];
       uint4* p = reinterpret_cast<uint4*>(rbt + sw_chunk(r, c8, 64));
       unpack8(*p, x);
@@ -297,11 +298,11 @@ __global__ void __launch_bounds__(128, 2) kda_prep_kernel(const __grid_constant_
     // ---- the FP32 array: row c holds A[r][c] = beta_r M[r][c] for c < r < L (row c of M^T)
     float* Sm = reinterpret_cast<float*>(sm + KP_G);
 #pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
-      float mp[32];   // M^T[c][16 blk + u] at u, P^T at 16 + u (lanes 0-15 of the warp: rows 16 warp + lane)
-      tmem_ld32(taddr(tb, warp * 32, KT_MP + 32 * blk), mp);
+    for (int blk = 2 * (warp >> 2); blk < 2 * (warp >> 2) + 2; ++blk) {   // the warpgroups split the blocks
+      float mp[32];   // M^T[c][16 blk + u] at u, P^T at 16 + u (lanes 0-15 of the warp: rows 16 (warp % 4) + lane)
+      tmem_ld32(taddr(tb, (warp & 3) * 32, KT_MP + 32 * blk), mp);
       if (lane < 16) {
-        const int cc = 16 * warp + lane;
+        const int cc = 16 * (warp & 3) + lane;
 #pragma unroll
         for (int u = 0; u < 16; u += 4) {
           const int r = 16 * blk + u;
@@ -318,19 +319,20 @@ __global__ void __launch_bounds__(128, 2) kda_prep_kernel(const __grid_constant_
     if (tid < 64) ut_diag_blocks(Sm, tid, 1);
     __syncthreads();
     const UtInvTiles tiles{sm + KP_G, sm + KP_G + 8192, sm + KP_G + 16384, sm + KP_G + 24576};
-    ok = ut_tc_inverse(Sm, tiles, tb, KT_INV, &bar_t, tph, a.err, t_pend);
+    ok = ut_tc_inverse<KP_THREADS>(Sm, tiles, tb, KT_INV, &bar_t, tph, a.err, t_pend);
   }
   if (ok) {
     // ---- T'' and T tiles (over D and X: the last product has read them)
     {
-      uint32_t u[4][8];
-      ut_ld_result(tb, KT_INV, warp, u);
-      const int r0 = 16 * warp + (lane >> 2), cq = 2 * (lane & 3);
+      constexpr int NG = UtGroups<KP_THREADS>::NG;
+      uint32_t u[NG][8];
+      ut_ld_result<KP_THREADS>(tb, KT_INV, warp, u);
+      const int r0 = 16 * (warp & 3) + (lane >> 2), cq = 2 * (lane & 3), g0 = UtGroups<KP_THREADS>::first(warp);
 #pragma unroll
-      for (int g = 0; g < 4; ++g)
+      for (int g = 0; g < NG; ++g)
 #pragma unroll
         for (int i = 0; i < 8; i += 2) {
-          const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * g + 8 * (i >> 2) + cq;
+          const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * (g0 + g) + 8 * (i >> 2) + cq;
           const uint32_t off = sw_off(r, cc, 64);
           const float t0 = __uint_as_float(u[g][i]), t1 = __uint_as_float(u[g][i + 1]);
           *reinterpret_cast<uint32_t*>(sm + KP_G + off) = pack_bf16(t0 * bs[cc], t1 * bs[cc + 1]);
@@ -341,11 +343,11 @@ __global__ void __launch_bounds__(128, 2) kda_prep_kernel(const __grid_constant_
     __syncthreads();
     // ---- P and M^T tiles (BF16) into the Rb tile's space, from the rows of [M^T | P^T]
 #pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
+    for (int blk = 2 * (warp >> 2); blk < 2 * (warp >> 2) + 2; ++blk) {
       float mp[32];
-      tmem_ld32(taddr(tb, warp * 32, KT_MP + 32 * blk), mp);
+      tmem_ld32(taddr(tb, (warp & 3) * 32, KT_MP + 32 * blk), mp);
       if (lane < 16) {
-        const int cc = 16 * warp + lane;
+        const int cc = 16 * (warp & 3) + lane;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           float x[8];
@@ -376,8 +378,8 @@ __global__ void __launch_bounds__(128, 2) kda_prep_kernel(const __grid_constant_
     }
     // ---- K~ = Lk . exp2(gx[blk]), Q~ likewise, in place
 #pragma unroll 4
-    for (int it = 0; it < 16; ++it) {
-      const int idx = tid + 128 * it, R = idx >> 4, c8 = idx & 15, blk = (R & 63) >> 4;
+    for (int it = 0; it < 2048 / KP_THREADS; ++it) {
+      const int idx = tid + KP_THREADS * it, R = idx >> 4, c8 = idx & 15, blk = (R & 63) >> 4;
       float f[8], x[8];
       uint4* p = reinterpret_cast<uint4*>(kq + sw_chunk(R, c8, 128));
       unpack8(*p, x);
@@ -400,16 +402,16 @@ __global__ void __launch_bounds__(128, 2) kda_prep_kernel(const __grid_constant_
     tc_fence_after();
   }
   if (ok) {
-    {  // -W^T row tid (dk index) -> BF16 SwTile(128 x 64)
-      float w[64];
-      tmem_ld32(taddr(tb, warp * 32, KT_INV), w);
-      tmem_ld32(taddr(tb, warp * 32, KT_INV + 32), w + 32);
+    {  // -W^T row tid % 128 (dk index) -> BF16 SwTile(128 x 64); the warpgroups split the 64 columns
+      const int hw = warp >> 2;
+      float w[32];
+      tmem_ld32(taddr(tb, (warp & 3) * 32, KT_INV + 32 * hw), w);
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
+      for (int c = 0; c < 4; ++c) {
         float x[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = -w[8 * c8 + e];
-        *reinterpret_cast<uint4*>(sm + KP_G + 16384 + sw_chunk(tid, c8, 128)) = pack8(x);
+        for (int e = 0; e < 8; ++e) x[e] = -w[8 * c + e];
+        *reinterpret_cast<uint4*>(sm + KP_G + 16384 + sw_chunk(tid & 127, 4 * hw + c, 128)) = pack8(x);
       }
     }
     fence_async_smem();
@@ -578,7 +580,7 @@ gdn_status make_kda_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
 void launch_kda_prep(const KdaPrepArgs& a, int NC, cudaStream_t s) {
   if (NC <= 0) return;
   prof_begin(K_KDA_PREP, s);
-  kda_prep_kernel<<<NC * a.HV, 128, KP_SMEM_ALLOC, s>>>(a);
+  kda_prep_kernel<<<NC * a.HV, KP_THREADS, KP_SMEM_ALLOC, s>>>(a);
   prof_end(K_KDA_PREP, s);
 }
 

@@ -126,10 +126,10 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
     }
     __syncthreads();
     if (!ok) continue;
-    ok = ut_tc_inverse(Sm, tiles, tb, PT_INV, &bar_t, tph, a.err, t_pend);
+    ok = ut_tc_inverse<PR_THREADS>(Sm, tiles, tb, PT_INV, &bar_t, tph, a.err, t_pend);
     uint32_t u[4][8];
     if (ok) {  // T', T'', T tiles (over D, X, N: the last product has read them)
-      ut_ld_result(tb, PT_INV, warp, u);
+      ut_ld_result<PR_THREADS>(tb, PT_INV, warp, u);
 #pragma unroll
       for (int g = 0; g < 4; ++g)
 #pragma unroll

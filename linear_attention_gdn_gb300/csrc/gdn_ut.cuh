@@ -281,24 +281,39 @@ struct UtInvTiles {
   uint8_t* n2;   // N^2
 };
 
-// This thread's 32 elements of an M = 64, N = 64 result at TMEM column `col` (the .16x256b lane map):
-// u[g][i] is row 16 warp + lane / 4 + 8 ((i >> 1) & 1), column 16 g + 8 (i >> 2) + 2 (lane % 4) + (i & 1).
-__device__ __forceinline__ void ut_ld_result(uint32_t tb, int col, int warp, uint32_t (&u)[4][8]) {
+// The 16-column groups of an M = 64, N = 64 result that warp `warp` of an NT-thread CTA reads: the
+// warps of one TMEM lane quarter (warp % 4) split the four groups between them.
+template <int NT>
+struct UtGroups {
+  static constexpr int NG = 4 * 128 / NT;   // groups per warp
+  static __device__ __forceinline__ int first(int warp) { return (warp >> 2) * NG; }
+};
+
+// This thread's elements of an M = 64, N = 64 result at TMEM column `col` (the .16x256b lane map):
+// u[g][i] is row 16 (warp % 4) + lane / 4 + 8 ((i >> 1) & 1), column 16 (g0 + g) + 8 (i >> 2) +
+// 2 (lane % 4) + (i & 1), for the groups g0 .. g0 + NG - 1 of UtGroups<NT>.
+template <int NT>
+__device__ __forceinline__ void ut_ld_result(uint32_t tb, int col, int warp, uint32_t (&u)[UtGroups<NT>::NG][8]) {
+  const int g0 = UtGroups<NT>::first(warp);
 #pragma unroll
-  for (int g = 0; g < 4; ++g) tmem_ld_m64_async(taddr(tb, warp * 32, col + 16 * g), u[g]);
+  for (int g = 0; g < UtGroups<NT>::NG; ++g) tmem_ld_m64_async(taddr(tb, (warp & 3) * 32, col + 16 * (g0 + g)), u[g]);
   tmem_wait_ld();
 }
 
+// NT = 128 or 256 threads (all of the CTA) take part.
+template <int NT>
 __device__ __forceinline__ bool ut_tc_inverse(const float* Sm, const UtInvTiles& tl, uint32_t tb, int inv,
                                               uint64_t* bar, uint32_t& tph, int* err, int& t_pend) {
+  static_assert(NT == 128 || NT == 256, "one or two warpgroups");
+  constexpr int NG = UtGroups<NT>::NG;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r0 = 16 * warp + (lane >> 2), cq = 2 * (lane & 3);
+  const int r0 = 16 * (warp & 3) + (lane >> 2), cq = 2 * (lane & 3), g0 = UtGroups<NT>::first(warp);
   {  // D and L^T as BF16 tiles from rows of the array: row n holds T_bb (columns of n's block, zero
      // above the diagonal) and, in the later blocks' columns c, A[c][n] = L^T[n][c]
-    uint4 dch[4], lch[4];
+    uint4 dch[512 / NT], lch[512 / NT];
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int item = tid + 128 * it, n = item >> 3, c8 = item & 7;
+    for (int it = 0; it < 512 / NT; ++it) {
+      const int item = tid + NT * it, n = item >> 3, c8 = item & 7;
       const float4 u0 = *reinterpret_cast<const float4*>(Sm + n * UT_ALD + 8 * c8);
       const float4 u1 = *reinterpret_cast<const float4*>(Sm + n * UT_ALD + 8 * c8 + 4);
       const uint4 w = make_uint4(pack_bf16(u0.x, u0.y), pack_bf16(u0.z, u0.w), pack_bf16(u1.x, u1.y),
@@ -310,8 +325,8 @@ __device__ __forceinline__ bool ut_tc_inverse(const float* Sm, const UtInvTiles&
     }
     __syncthreads();   // the array is read: its space takes the tiles
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int item = tid + 128 * it, n = item >> 3, c8 = item & 7;
+    for (int it = 0; it < 512 / NT; ++it) {
+      const int item = tid + NT * it, n = item >> 3, c8 = item & 7;
       *reinterpret_cast<uint4*>(tl.d + sw_chunk(n, c8, 64)) = dch[it];
       *reinterpret_cast<uint4*>(tl.lx + sw_chunk(n, c8, 64)) = lch[it];
     }
@@ -335,41 +350,41 @@ __device__ __forceinline__ bool ut_tc_inverse(const float* Sm, const UtInvTiles&
     tc_fence_after();
     return r;
   };
-  uint32_t u[4][8];
+  uint32_t u[NG][8];
   // (a K-major B tile is rows N, columns K; L^T is that form of L.  An MN-major B tile is rows K,
   // columns N: a row-major N or D.)
   bool ok = product(tl.d, tl.lx, false);   // N = D L
   if (ok) {  // N -> BF16 tile
-    ut_ld_result(tb, inv, warp, u);
+    ut_ld_result<NT>(tb, inv, warp, u);
 #pragma unroll
-    for (int g = 0; g < 4; ++g)
+    for (int g = 0; g < NG; ++g)
 #pragma unroll
       for (int i = 0; i < 8; i += 2) {
-        const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * g + 8 * (i >> 2) + cq;
+        const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * (g0 + g) + 8 * (i >> 2) + cq;
         *reinterpret_cast<uint32_t*>(tl.n + sw_off(r, cc, 64)) =
             pack_bf16(__uint_as_float(u[g][i]), __uint_as_float(u[g][i + 1]));
       }
   }
   ok = ok && product(tl.n, tl.n, true);   // N^2 = N N
   if (ok) {
-    ut_ld_result(tb, inv, warp, u);
+    ut_ld_result<NT>(tb, inv, warp, u);
 #pragma unroll
-    for (int g = 0; g < 4; ++g)
+    for (int g = 0; g < NG; ++g)
 #pragma unroll
       for (int i = 0; i < 8; i += 2) {
-        const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * g + 8 * (i >> 2) + cq;
+        const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * (g0 + g) + 8 * (i >> 2) + cq;
         *reinterpret_cast<uint32_t*>(tl.n2 + sw_off(r, cc, 64)) =
             pack_bf16(__uint_as_float(u[g][i]), __uint_as_float(u[g][i + 1]));
       }
   }
   ok = ok && product(tl.n2, tl.n, true);   // N^3 = N^2 N
   if (ok) {  // X = I - N + N^2 - N^3 -> BF16 tile (over L^T, which N = D L has finished reading)
-    ut_ld_result(tb, inv, warp, u);
+    ut_ld_result<NT>(tb, inv, warp, u);
 #pragma unroll
-    for (int g = 0; g < 4; ++g)
+    for (int g = 0; g < NG; ++g)
 #pragma unroll
       for (int i = 0; i < 8; i += 2) {
-        const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * g + 8 * (i >> 2) + cq;
+        const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * (g0 + g) + 8 * (i >> 2) + cq;
         const uint32_t off = sw_off(r, cc, 64);
         const float2 n1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(tl.n + off));
         const float2 n2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(tl.n2 + off));
