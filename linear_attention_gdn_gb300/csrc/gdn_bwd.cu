@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
   __shared__ __align__(16) float glc[KDA ? 128 : 4];   // this chunk's gamma_L (KDA), read before the stage refill
   __shared__ uint32_t tslot;
   __shared__ int pre_next;   // the next iteration's W^T / X MMAs went out under this one's MMA2
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (*(volatile int*)a.err) return;
 
   int seg, hv, split = -1;
@@ -252,20 +252,21 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
     }
   }
   uint32_t mph = 0, pph = 0;
-  bool ok = true, pend = false;   // pend: W^T / X MMAs issued by thread 32 and not yet waited for
+  bool ok = true, pend = false;   // pend: W^T / X MMAs issued by warp 1 and not yet waited for
   const uint32_t sm_ds = smem_u32(ds_tile), sm_w = smem_u32(sm + BS_W);
-  // W^T = K^T T'^T and X = dO^T Aqk^T of the chunk in stage `st` (they need no state)
+  // W^T = K^T T'^T and X = dO^T Aqk^T of the chunk in stage `st` (they need no state).  Every MMA
+  // here is issued by a whole warp (one elected lane), so that its descriptors stay warp-uniform.
   auto issue_wx = [&](const uint8_t* st) {
     const uint32_t a_k = smem_u32(st + BS_K), a_do = smem_u32(st + BS_DO);
     const uint32_t a_tp = smem_u32(st + BS_TP), a_aqk = smem_u32(st + S_AQK);
     if (!KDA) {
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tb + BT_DW, desc_mn(a_k, 64, ks), desc_k(a_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+        mma_ss_w(tb + BT_DW, desc_mn(a_k, 64, ks), desc_k(a_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
     }
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-      mma_ss(tb + BT_DX, desc_mn(a_do, 64, ks), desc_mn(a_aqk, 64, ks), idesc(128, 64, 1, 1), ks > 0);
+      mma_ss_w(tb + BT_DX, desc_mn(a_do, 64, ks), desc_mn(a_aqk, 64, ks), idesc(128, 64, 1, 1), ks > 0);
   };
   for (int it = 0; it < nch && ok; ++it) {
     const int ci = c0 + nch - 1 - it;
@@ -286,18 +287,19 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
       __syncthreads();
     }
     tc_fence_after();
-    if (tid == 0) {
+    if (warp == 0) {
       // the dS'^T tile (written and fenced last iteration) is this chunk's tape entry
-      if (full) {
+      if (full && lane == 0) {
         bulk_store(a.dtape + ((size_t)ci * a.HV + hv) * STATE_BYTES, ds_tile, STATE_BYTES);
         bulk_commit();
       }
       if (!pre) issue_wx(st);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        mma_ss(tb + BT_DY, desc_k(sm_ds, 128, ks), desc_k(a_k, 64, ks), idesc(128, 64, 0, 0), ks > 0);
-      mma_commit(&mma_bar);
-      bulk_wait_read_but1();   // the last dV_new^T copy has read its tile (rewritten by the hop below)
+        mma_ss_w(tb + BT_DY, desc_k(sm_ds, 128, ks), desc_k(a_k, 64, ks), idesc(128, 64, 0, 0), ks > 0);
+      mma_commit_w(&mma_bar);
+      if (lane == 0) bulk_wait_read_but1();   // the last dV_new^T copy has read its tile (rewritten below)
+      __syncwarp();
     }
     {  // (P gamma_r rq_r dO[r][tid]) -> TMEM A operand, while the MMAs run
 #pragma unroll
@@ -375,36 +377,39 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0) {
-      if (full) {   // this chunk's dV_new^T for the gradient kernel
+    if (warp == 0) {
+      if (full && lane == 0) {   // this chunk's dV_new^T for the gradient kernel
         bulk_store(a.dvn + ((size_t)ci * a.HV + hv) * VN_BYTES, sm + BS_DV, VN_BYTES);
         bulk_commit();
       }
       const uint32_t b_w = KDA ? smem_u32(st + BSK_WT) : sm_w;   // -W^T: the stage's (KDA) or the hop's
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_ts(tb + BT_DS, tb + BT_ADV + ks * 8, desc_k(b_w, 128, ks), idesc(128, 128, 0, 0), ks > 0);
+        mma_ts_w(tb + BT_DS, tb + BT_ADV + ks * 8, desc_k(b_w, 128, ks), idesc(128, 128, 0, 0), ks > 0);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_ts(tb + BT_DS, tb + BT_ADO + ks * 8, desc_mn(a_q, 64, ks), idesc(128, 128, 0, 1), 1u);
-      mma_commit(&mma_bar);
-      bulk_wait_read_but1();   // the tape copy has read the dS'^T tile (rewritten below)
+        mma_ts_w(tb + BT_DS, tb + BT_ADO + ks * 8, desc_mn(a_q, 64, ks), idesc(128, 128, 0, 1), 1u);
+      mma_commit_w(&mma_bar);
+      if (lane == 0) bulk_wait_read_but1();   // the tape copy has read the dS'^T tile (rewritten below)
+      __syncwarp();
     }
     if (tid == 64 && it + 2 < nch) issue(it + 2, 0);   // the stage's K, dO, T', Aqk, scalars are dead
-    if (tid == 32) {   // the next chunk's W^T and X, under MMA2, when its tiles are in and need no zeroing
+    if (warp == 1) {   // the next chunk's W^T and X, under MMA2, when its tiles are in and need no zeroing
       int nx = 0;
       if (it + 1 < nch) {
         const uint8_t* st1 = sm + ((it + 1) & 1) * STAGE;
-        if (mbar_wait(&full_bar[(it + 1) & 1], ((it + 1) >> 1) & 1, a.err) &&
+        // (a warp vote: every lane takes the same branch, as the elected issue needs)
+        if (__all_sync(0xffffffffu, mbar_wait(&full_bar[(it + 1) & 1], ((it + 1) >> 1) & 1, a.err)) &&
             reinterpret_cast<const int*>(st1 + S_SCAL)[129] == CH) {
           tc_fence_after();
           issue_wx(st1);
-          mma_commit(&bar_pre);
+          mma_commit_w(&bar_pre);
           nx = 1;
           pend = true;
         }
       }
-      pre_next = nx;
+      __syncwarp();
+      if (lane == 0) pre_next = nx;
     }
     ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
     mph ^= 1;
@@ -440,7 +445,7 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
     if (tid == 0 && it + 2 < nch) issue(it + 2, 1);   // MMA2 is done with Q
   }
   if (tid == 0) bulk_wait_all();
-  if (tid == 32 && pend) mbar_wait(&bar_pre, pph, a.err);   // no MMA may outlive the TMEM allocation
+  if (warp == 1 && lane == 0 && pend) mbar_wait(&bar_pre, pph, a.err);   // no MMA may outlive the TMEM allocation
   if (ok && a.walk) {
     float* dst = a.dbend + ((size_t)split * a.HV + hv) * STATE_F32 + (size_t)tid * 128;
 #pragma unroll
@@ -531,8 +536,9 @@ constexpr int GK_KQLD = 68;   // row pitch (floats) of the FP32 [QK^T lower | KK
 static_assert(GK_KQ + 64 * GK_KQLD * 4 <= GK_V, "KQ table");
 // regions reused once their first contents are dead
 constexpr int GK_H1 = GK_DO, GK_H2 = GK_DO + 8192;   // after MA (dO dead)
-constexpr int GK_DT = GK_DV, GK_R1 = GK_DV + 8192;   // after MA (dV_new dead)
-constexpr int GK_F1 = GK_WD, GK_F2 = GK_WD + 8192;   // after MB (dW dead)
+constexpr int GK_DT = GK_DV;                         // after MA (dV_new dead); dead again after M4
+constexpr int GK_R1 = GK_WD;                         // after MB (dW dead), read by M5
+constexpr int GK_F1 = GK_WD, GK_F2 = GK_WD + 8192;   // after M5 (R1 dead)
 // TMEM columns: dq^T, dk^T accumulators of the group, then six 64-column results
 constexpr int GT_DQ = 0, GT_DK = 64, GT_A0 = 128, GT_A1 = 192, GT_A2 = 256, GT_A3 = 320, GT_A4 = 384, GT_A5 = 448;
 
@@ -664,9 +670,13 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
     tma_load_3d(sm + GK_DO, &a.tdo, 0, hv_, tok0_, &bar_do);
     tma_load_3d(sm + GK_DO + 8192, &a.tdo, 64, hv_, tok0_, &bar_do);
   };
-  auto issue_dt = [&](int c_, int hv_) {   // dV_new^T and T
+  // dV_new^T and T, one transaction count: dV_new^T goes out once M4 has read dT (its region), T
+  // once M5 has read it
+  auto issue_dvn = [&](int c_, int hv_) {
     mbar_expect_tx(&bar_dt, (uint32_t)(VN_BYTES + TILE64_BYTES));
     bulk_load(sm + GK_DV, a.dvn + blk(c_, hv_) * VN_BYTES, VN_BYTES, &bar_dt);
+  };
+  auto issue_t = [&](int c_, int hv_) {
     bulk_load(sm + GK_T, a.cb + blk(c_, hv_) * CB_BYTES + CB_T, TILE64_BYTES, &bar_dt);
   };
   // gates of one value head into buffer b (one warp): cumulative gate in log2
@@ -778,7 +788,8 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
       issue_vn(c, j * a.G);
       issue_sv(c, j * a.G, tok0);
       issue_do(j * a.G, tok0);
-      issue_dt(c, j * a.G);
+      issue_dvn(c, j * a.G);
+      issue_t(c, j * a.G);
     }
     if (warp == 4) gates(0, j * a.G, tok0, a.chunk_len[c]);
   }
@@ -1217,6 +1228,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
       if (!(ok = mma_sync_wait())) break;
       if (tid == 0 && has_next) {
         issue_do(nhv, ntok0);   // the dO region (H1, H2) is dead
+        issue_dvn(nc, nhv);     // and the dV_new^T region (dT)
         bulk_wait_read();       // the dv store has read the V_new^T region
         issue_vn(nc, nhv);
       }
@@ -1251,7 +1263,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
         tmem_wait_st();
       }
       if (!(ok = mma_sync_wait())) break;
-      if (tid == 0 && has_next) issue_dt(nc, nhv);   // dV_new^T (dT, R1) and T are dead
+      if (tid == 0 && has_next) issue_t(nc, nhv);   // T is dead
       {  // H5: dA rows -> F1, F2 for M6; dbeta row terms; dA . A -> column sums of C
         uint32_t u[8];
         tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A0 + cb0), u);
