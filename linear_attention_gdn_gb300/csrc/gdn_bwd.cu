@@ -117,6 +117,7 @@ constexpr int BS_W = BS_DS + STATE_BYTES;     // -W^T tile, SwTile(128 x 64)
 constexpr int BS_DV = BS_W + 16384;           // dV_new^T staging, SwTile(128 x 64)
 constexpr int BS_SMEM = BS_DV + VN_BYTES;
 constexpr int BS_SMEM_ALLOC = BS_SMEM + 1024;
+// TMEM columns of the adjoint walk
 constexpr int BT_DW = 0, BT_DX = 64, BT_DY = 128, BT_DS = 192, BT_ADV = 320, BT_ADO = 352;
 
 __device__ __forceinline__ void store_row128(uint8_t* dst, int row, const float* S) {
@@ -138,18 +139,26 @@ __device__ __forceinline__ float ld_bf16(const uint8_t* tile, int r, int c, int 
 // KDA = true: the per-channel-decay form.  The stage then holds Kd and Q~ in the K and Q slots (DY =
 // dS'^T Kd^T needs no kd scaling; the dO^T A operand of MMA2 is scale dO^T, against Q~), -W^T from the
 // block (no W^T product or hop), P, and gamma_L, which scales column i of dS'^T.
+constexpr int BS_CHAIN = 128;                // the chain warpgroup (row tid of dS^T per thread)
+constexpr int BS_THREADS = BS_CHAIN + 32;     // plus one warp that issues every MMA
+constexpr int BS_BAR = 1;                     // named barrier of the chain warpgroup
+
 template <bool KDA>
-__global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant__ BScanArgs a) {
+__global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_kernel(const __grid_constant__ BScanArgs a) {
   constexpr int STAGE = KDA ? BSK_STAGE : BS_STAGE;
   constexpr int S_AQK = KDA ? BSK_AQK : BS_AQK;
   constexpr int S_SCAL = KDA ? BSK_SCAL : BS_SCAL;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
-  __shared__ uint64_t full_bar[2], mma_bar, bar_pre;
+  // go_ds: chain -> MMA warp, the dS'^T tile of the next chunk is written; go_z: its stage's rows past
+  // the document end are zeroed (partial chunks only); go2: the MMA2 operands are in place.
+  // mma_bar: DY (with W^T / X when they were not issued early) done; mma2_bar: MMA2 done; bar_pre:
+  // the next chunk's W^T / X done; done: every MMA of the MMA warp has completed
+  __shared__ uint64_t full_bar[2], mma_bar, mma2_bar, bar_pre, go_ds, go_z, go2, done;
   __shared__ __align__(16) float glc[KDA ? 128 : 4];   // this chunk's gamma_L (KDA), read before the stage refill
   __shared__ uint32_t tslot;
-  __shared__ int pre_next;   // the next iteration's W^T / X MMAs went out under this one's MMA2
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const bool chain = tid < BS_CHAIN;
   if (*(volatile int*)a.err) return;
 
   int seg, hv, split = -1;
@@ -172,7 +181,8 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
   // dS_out for its last segment, else zero
   const int doc = a.seg_doc[seg];
   float dS[128];
-  {
+  uint8_t* ds_tile = sm + BS_DS;
+  if (chain) {
     const float* src = nullptr;
     int stride = 1;
     if (!a.walk && a.seg_split[seg] >= 0) {
@@ -183,18 +193,21 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
     }
 #pragma unroll
     for (int jj = 0; jj < 128; ++jj) dS[jj] = src ? src[jj * stride] : 0.f;
+    store_row128(ds_tile, tid, dS);
   }
-  uint8_t* ds_tile = sm + BS_DS;
-  store_row128(ds_tile, tid, dS);
 
   if (warp == 0) tmem_alloc(&tslot, 512);
   if (tid == 0) {
     mbar_init(&full_bar[0], 1);
     mbar_init(&full_bar[1], 1);
     mbar_init(&mma_bar, 1);
+    mbar_init(&mma2_bar, 1);
     mbar_init(&bar_pre, 1);
+    mbar_init(&go_ds, 1);
+    mbar_init(&go_z, 1);
+    mbar_init(&go2, 1);
+    mbar_init(&done, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
-    pre_next = 0;
   }
   fence_async_smem();
   tc_fence_before();
@@ -204,8 +217,9 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
 
   // iteration `it` processes chunk c0 + nch - 1 - it
   // The tiles of iteration `it` in two parts on one barrier: everything but Q (`part` 0: the
-  // stage's K, dO, T', Aqk, scalars are dead once MMA2 has been issued) and Q (`part` 1: MMA2
-  // reads it).  Part 0 sets the barrier's byte count for both.
+  // stage's K, dO, T', Aqk, scalars are dead once the chain has formed the MMA2 operands) and Q
+  // (`part` 1: MMA2 reads it).  Part 0 sets the barrier's byte count for both; it goes out before
+  // part 1 in every iteration.
   auto issue = [&](int it, int part) {
     const int ci = c0 + nch - 1 - it;
     uint8_t* st = sm + (it & 1) * STAGE;
@@ -250,212 +264,236 @@ __global__ void __launch_bounds__(128, 1) bwd_scan_kernel(const __grid_constant_
       issue(1, 0);
       issue(1, 1);
     }
+    mbar_arrive(&go_ds);   // the first chunk's dS'^T tile (the segment-end adjoint) is written
   }
-  uint32_t mph = 0, pph = 0;
-  bool ok = true, pend = false;   // pend: W^T / X MMAs issued by warp 1 and not yet waited for
   const uint32_t sm_ds = smem_u32(ds_tile), sm_w = smem_u32(sm + BS_W);
-  // W^T = K^T T'^T and X = dO^T Aqk^T of the chunk in stage `st` (they need no state).  Every MMA
-  // here is issued by a whole warp (one elected lane), so that its descriptors stay warp-uniform.
-  auto issue_wx = [&](const uint8_t* st) {
-    const uint32_t a_k = smem_u32(st + BS_K), a_do = smem_u32(st + BS_DO);
-    const uint32_t a_tp = smem_u32(st + BS_TP), a_aqk = smem_u32(st + S_AQK);
-    if (!KDA) {
+  auto chunk_len = [&](int it) { return reinterpret_cast<const int*>(sm + (it & 1) * STAGE + S_SCAL)[129]; };
+
+  if (!chain) {
+    // ================= MMA warp: DY, MMA2, and the next chunk's W^T / X of every chunk =============
+    // Each product is issued by the whole warp (one elected lane), so that its descriptors stay
+    // warp-uniform; every wait is a warp vote, so that all lanes take the same branch.
+    // W^T = K^T T'^T and X = dO^T Aqk^T of the chunk in stage `st` (they need no state)
+    auto issue_wx = [&](const uint8_t* st) {
+      const uint32_t a_k = smem_u32(st + BS_K), a_do = smem_u32(st + BS_DO);
+      const uint32_t a_tp = smem_u32(st + BS_TP), a_aqk = smem_u32(st + S_AQK);
+      if (!KDA) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_ss_w(tb + BT_DW, desc_mn(a_k, 64, ks), desc_k(a_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
+      }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_ss_w(tb + BT_DW, desc_mn(a_k, 64, ks), desc_k(a_tp, 64, ks), idesc(128, 64, 1, 0), ks > 0);
-    }
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-      mma_ss_w(tb + BT_DX, desc_mn(a_do, 64, ks), desc_mn(a_aqk, 64, ks), idesc(128, 64, 1, 1), ks > 0);
-  };
-  for (int it = 0; it < nch && ok; ++it) {
-    const int ci = c0 + nch - 1 - it;
-    uint8_t* st = sm + (it & 1) * STAGE;
-    const uint32_t a_k = smem_u32(st + BS_K), a_q = smem_u32(st + BS_Q);
-    const float* scal = reinterpret_cast<const float*>(st + S_SCAL);
-    const bool pre = pre_next;   // written before the last barrier of the previous iteration
-    ok = __syncthreads_and(mbar_wait(&full_bar[it & 1], (it >> 1) & 1, a.err));
-    if (!ok) break;
-    const int L = reinterpret_cast<const int*>(scal)[129];
-    if (L < CH) {
-      for (int idx = tid; idx < (CH - L) * 48; idx += 128) {
-        const int t = idx / 48, rem = idx % 48, tile = rem / 16, c8 = rem % 16;
-        const int off = tile == 0 ? BS_K : (tile == 1 ? BS_Q : BS_DO);
-        *reinterpret_cast<uint4*>(st + off + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
+        mma_ss_w(tb + BT_DX, desc_mn(a_do, 64, ks), desc_mn(a_aqk, 64, ks), idesc(128, 64, 1, 1), ks > 0);
+    };
+    uint32_t gph = 0, zph = 0, g2ph = 0;
+    for (int it = 0; it < nch; ++it) {
+      const uint8_t* st = sm + (it & 1) * STAGE;
+      if (!__all_sync(0xffffffffu, mbar_wait(&go_ds, gph, a.err) &&
+                                       mbar_wait(&full_bar[it & 1], (it >> 1) & 1, a.err)))
+        break;
+      gph ^= 1;
+      const int L = chunk_len(it);
+      if (L < CH) {   // the chain zeroes the rows past the document end first
+        if (!__all_sync(0xffffffffu, mbar_wait(&go_z, zph, a.err))) break;
+        zph ^= 1;
       }
-      fence_async_smem();
-      __syncthreads();
-    }
-    tc_fence_after();
-    if (warp == 0) {
-      // the dS'^T tile (written and fenced last iteration) is this chunk's tape entry
-      if (full && lane == 0) {
-        bulk_store(a.dtape + ((size_t)ci * a.HV + hv) * STATE_BYTES, ds_tile, STATE_BYTES);
-        bulk_commit();
-      }
-      if (!pre) issue_wx(st);
+      tc_fence_after();
+      if (it == 0 || L < CH) issue_wx(st);   // else issued after the last MMA2
+      const uint32_t a_k = smem_u32(st + BS_K);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
         mma_ss_w(tb + BT_DY, desc_k(sm_ds, 128, ks), desc_k(a_k, 64, ks), idesc(128, 64, 0, 0), ks > 0);
       mma_commit_w(&mma_bar);
-      if (lane == 0) bulk_wait_read_but1();   // the last dV_new^T copy has read its tile (rewritten below)
-      __syncwarp();
-    }
-    {  // (P gamma_r rq_r dO[r][tid]) -> TMEM A operand, while the MMAs run
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t p8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int r = q * 16 + 2 * e;
-          const float f0 = KDA ? a.scale : scal[r], f1 = KDA ? a.scale : scal[r + 1];
-          p8[e] = pack_bf16(f0 * ld_bf16(st + BS_DO, r, tid, 64), f1 * ld_bf16(st + BS_DO, r + 1, tid, 64));
-        }
-        tmem_st8(taddr(tb, warp * 32, BT_ADO + q * 8), p8);
-      }
-    }
-    // -W^T -> shared (row tid = dk index), the B operand of MMA2: while DY runs when W^T came from
-    // the previous iteration, else after it
-    auto w_hop = [&]() {
-      float w[64];
-      tmem_ld32(taddr(tb, warp * 32, BT_DW), w);
-      tmem_ld32(taddr(tb, warp * 32, BT_DW + 32), w + 32);
-      uint8_t* wt = sm + BS_W;
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        uint4 v;
-        v.x = pack_bf16(-w[c8 * 8 + 0], -w[c8 * 8 + 1]);
-        v.y = pack_bf16(-w[c8 * 8 + 2], -w[c8 * 8 + 3]);
-        v.z = pack_bf16(-w[c8 * 8 + 4], -w[c8 * 8 + 5]);
-        v.w = pack_bf16(-w[c8 * 8 + 6], -w[c8 * 8 + 7]);
-        *reinterpret_cast<uint4*>(wt + sw_chunk(tid, c8, 128)) = v;
-      }
-    };
-    if (pre) {
-      const bool got = mbar_wait(&bar_pre, pph, a.err);
-      pph ^= 1;
-      pend = false;
+      if (!__all_sync(0xffffffffu, mbar_wait(&go2, g2ph, a.err))) break;
+      g2ph ^= 1;
       tc_fence_after();
-      if (got && !KDA) w_hop();
-      ok = got;
-    }
-    ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err) && ok);
-    mph ^= 1;
-    if (!ok) break;
-    tc_fence_after();
-    {
-      if (!pre && !KDA) w_hop();
-      const float* kd = scal + 64;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float x[32], y[32];
-        tmem_ld32(taddr(tb, warp * 32, BT_DX + h * 32), x);
-        tmem_ld32(taddr(tb, warp * 32, BT_DY + h * 32), y);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t p8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = q * 16 + 2 * e, r = h * 32 + j;
-            p8[e] = KDA ? pack_bf16(fmaf(a.scale, x[j], y[j]), fmaf(a.scale, x[j + 1], y[j + 1]))
-                        : pack_bf16(fmaf(a.scale, x[j], kd[r] * y[j]), fmaf(a.scale, x[j + 1], kd[r + 1] * y[j + 1]));
-          }
-          tmem_st8(taddr(tb, warp * 32, BT_ADV + h * 16 + q * 8), p8);
-          if (full) {
-            uint8_t* dvt = sm + BS_DV;
-            const int c8 = h * 4 + q * 2;
-            *reinterpret_cast<uint4*>(dvt + sw_chunk(tid, c8, 128)) = make_uint4(p8[0], p8[1], p8[2], p8[3]);
-            *reinterpret_cast<uint4*>(dvt + sw_chunk(tid, c8 + 1, 128)) = make_uint4(p8[4], p8[5], p8[6], p8[7]);
-          }
-        }
-      }
-      tmem_wait_st();
-    }
-    const float gL = scal[128];   // read before the barrier after which the stage is refilled
-    if (KDA) glc[tid] = scal[tid];
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 0) {
-      if (full && lane == 0) {   // this chunk's dV_new^T for the gradient kernel
-        bulk_store(a.dvn + ((size_t)ci * a.HV + hv) * VN_BYTES, sm + BS_DV, VN_BYTES);
-        bulk_commit();
-      }
       const uint32_t b_w = KDA ? smem_u32(st + BSK_WT) : sm_w;   // -W^T: the stage's (KDA) or the hop's
+      const uint32_t a_q = smem_u32(st + BS_Q);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_ts_w(tb + BT_DS, tb + BT_ADV + ks * 8, desc_k(b_w, 128, ks), idesc(128, 128, 0, 0), ks > 0);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_ts_w(tb + BT_DS, tb + BT_ADO + ks * 8, desc_mn(a_q, 64, ks), idesc(128, 128, 0, 1), 1u);
-      mma_commit_w(&mma_bar);
-      if (lane == 0) bulk_wait_read_but1();   // the tape copy has read the dS'^T tile (rewritten below)
-      __syncwarp();
-    }
-    if (tid == 64 && it + 2 < nch) issue(it + 2, 0);   // the stage's K, dO, T', Aqk, scalars are dead
-    if (warp == 1) {   // the next chunk's W^T and X, under MMA2, when its tiles are in and need no zeroing
-      int nx = 0;
+      mma_commit_w(&mma2_bar);
+      // the next chunk's W^T and X, under MMA2, when its tiles are in and need no zeroing
       if (it + 1 < nch) {
-        const uint8_t* st1 = sm + ((it + 1) & 1) * STAGE;
-        // (a warp vote: every lane takes the same branch, as the elected issue needs)
-        if (__all_sync(0xffffffffu, mbar_wait(&full_bar[(it + 1) & 1], ((it + 1) >> 1) & 1, a.err)) &&
-            reinterpret_cast<const int*>(st1 + S_SCAL)[129] == CH) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[(it + 1) & 1], ((it + 1) >> 1) & 1, a.err))) break;
+        if (chunk_len(it + 1) == CH) {
           tc_fence_after();
-          issue_wx(st1);
+          issue_wx(sm + ((it + 1) & 1) * STAGE);
           mma_commit_w(&bar_pre);
-          nx = 1;
-          pend = true;
         }
       }
-      __syncwarp();
-      if (lane == 0) pre_next = nx;
     }
-    ok = __syncthreads_and(mbar_wait(&mma_bar, mph, a.err));
-    mph ^= 1;
-    if (!ok) break;
-    tc_fence_after();
-    {
+    mma_commit_w(&done);   // arrives once every MMA this warp issued has completed
+  } else {
+    // ================= chain warpgroup ==========================================================
+    uint32_t mph = 0, m2ph = 0, pph = 0;
+    bool ok = true;
+    for (int it = 0; it < nch && ok; ++it) {
+      const int ci = c0 + nch - 1 - it;
+      uint8_t* st = sm + (it & 1) * STAGE;
+      const float* scal = reinterpret_cast<const float*>(st + S_SCAL);
+      if (tid == 0) {
+        // the dS'^T tile (written and fenced last iteration) is this chunk's tape entry
+        if (full) {
+          bulk_store(a.dtape + ((size_t)ci * a.HV + hv) * STATE_BYTES, ds_tile, STATE_BYTES);
+          bulk_commit();
+        }
+        bulk_wait_read_but1();   // the last dV_new^T copy has read its tile (rewritten by the hop below)
+      }
+      ok = bar_and(BS_BAR, BS_CHAIN, mbar_wait(&full_bar[it & 1], (it >> 1) & 1, a.err));
+      if (!ok) break;
+      const int L = reinterpret_cast<const int*>(scal)[129];
+      if (L < CH) {
+        for (int idx = tid; idx < (CH - L) * 48; idx += BS_CHAIN) {
+          const int t = idx / 48, rem = idx % 48, tile = rem / 16, c8 = rem % 16;
+          const int off = tile == 0 ? BS_K : (tile == 1 ? BS_Q : BS_DO);
+          *reinterpret_cast<uint4*>(st + off + sw_chunk(L + t, c8, 64)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_async_smem();
+        named_bar(BS_BAR, BS_CHAIN);
+        if (tid == 0) mbar_arrive(&go_z);
+      }
+      const bool pre = it > 0 && L == CH;   // this chunk's W^T / X went out after the last MMA2
+      {  // (P gamma_r rq_r dO[r][tid]) -> TMEM A operand of MMA2, while DY runs
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        float x[32];
-        tmem_ld32(taddr(tb, warp * 32, BT_DS + h * 32), x);
-        if (KDA) {   // column i (key channel) of dS'^T decays by gamma_L[i]
+        for (int q = 0; q < 4; ++q) {
+          uint32_t p8[8];
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 gv = *reinterpret_cast<const float4*>(glc + h * 32 + e);
-            fma2v(x[e], x[e + 1], gv.x, gv.y, dS[h * 32 + e], dS[h * 32 + e + 1]);
-            fma2v(x[e + 2], x[e + 3], gv.z, gv.w, dS[h * 32 + e + 2], dS[h * 32 + e + 3]);
-            dS[h * 32 + e] = x[e];
-            dS[h * 32 + e + 1] = x[e + 1];
-            dS[h * 32 + e + 2] = x[e + 2];
-            dS[h * 32 + e + 3] = x[e + 3];
+          for (int e = 0; e < 8; ++e) {
+            const int r = q * 16 + 2 * e;
+            const float f0 = KDA ? a.scale : scal[r], f1 = KDA ? a.scale : scal[r + 1];
+            p8[e] = pack_bf16(f0 * ld_bf16(st + BS_DO, r, tid, 64), f1 * ld_bf16(st + BS_DO, r + 1, tid, 64));
           }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            fma2_to(dS[h * 32 + e], dS[h * 32 + e + 1], gL, dS[h * 32 + e], dS[h * 32 + e + 1], x[e], x[e + 1]);
+          tmem_st8(taddr(tb, warp * 32, BT_ADO + q * 8), p8);
         }
       }
-      store_row128(ds_tile, tid, dS);
+      // -W^T -> shared (row tid = dk index), the B operand of MMA2: while DY runs when W^T went out
+      // early, else after it
+      auto w_hop = [&]() {
+        float w[64];
+        tmem_ld32(taddr(tb, warp * 32, BT_DW), w);
+        tmem_ld32(taddr(tb, warp * 32, BT_DW + 32), w + 32);
+        uint8_t* wt = sm + BS_W;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          uint4 v;
+          v.x = pack_bf16(-w[c8 * 8 + 0], -w[c8 * 8 + 1]);
+          v.y = pack_bf16(-w[c8 * 8 + 2], -w[c8 * 8 + 3]);
+          v.z = pack_bf16(-w[c8 * 8 + 4], -w[c8 * 8 + 5]);
+          v.w = pack_bf16(-w[c8 * 8 + 6], -w[c8 * 8 + 7]);
+          *reinterpret_cast<uint4*>(wt + sw_chunk(tid, c8, 128)) = v;
+        }
+      };
+      if (pre) {
+        ok = mbar_wait(&bar_pre, pph, a.err);
+        pph ^= 1;
+        tc_fence_after();
+        if (ok && !KDA) w_hop();
+      }
+      ok = bar_and(BS_BAR, BS_CHAIN, mbar_wait(&mma_bar, mph, a.err) && ok);
+      mph ^= 1;
+      if (!ok) break;
+      tc_fence_after();
+      {
+        if (!pre && !KDA) w_hop();
+        const float* kd = scal + 64;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float x[32], y[32];
+          tmem_ld32(taddr(tb, warp * 32, BT_DX + h * 32), x);
+          tmem_ld32(taddr(tb, warp * 32, BT_DY + h * 32), y);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t p8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int j = q * 16 + 2 * e, r = h * 32 + j;
+              p8[e] = KDA ? pack_bf16(fmaf(a.scale, x[j], y[j]), fmaf(a.scale, x[j + 1], y[j + 1]))
+                          : pack_bf16(fmaf(a.scale, x[j], kd[r] * y[j]), fmaf(a.scale, x[j + 1], kd[r + 1] * y[j + 1]));
+            }
+            tmem_st8(taddr(tb, warp * 32, BT_ADV + h * 16 + q * 8), p8);
+            if (full) {
+              uint8_t* dvt = sm + BS_DV;
+              const int c8 = h * 4 + q * 2;
+              *reinterpret_cast<uint4*>(dvt + sw_chunk(tid, c8, 128)) = make_uint4(p8[0], p8[1], p8[2], p8[3]);
+              *reinterpret_cast<uint4*>(dvt + sw_chunk(tid, c8 + 1, 128)) = make_uint4(p8[4], p8[5], p8[6], p8[7]);
+            }
+          }
+        }
+        tmem_wait_st();
+      }
+      const float gL = scal[128];   // read before the barrier after which the stage is refilled
+      if (KDA) glc[tid] = scal[tid];
+      fence_async_smem();
+      tc_fence_before();
+      named_bar(BS_BAR, BS_CHAIN);
+      if (tid == 0) {
+        mbar_arrive(&go2);   // MMA2 may go
+        if (full) {   // this chunk's dV_new^T for the gradient kernel
+          bulk_store(a.dvn + ((size_t)ci * a.HV + hv) * VN_BYTES, sm + BS_DV, VN_BYTES);
+          bulk_commit();
+        }
+        bulk_wait_read_but1();   // the tape copy has read the dS'^T tile (rewritten below)
+      }
+      // the stage's K, dO, T', Aqk, scalars are dead (the per-channel-decay stage also holds -W^T, which
+      // MMA2 reads: its refill waits for MMA2)
+      if (!KDA && tid == 64 && it + 2 < nch) issue(it + 2, 0);
+      ok = bar_and(BS_BAR, BS_CHAIN, mbar_wait(&mma2_bar, m2ph, a.err));
+      m2ph ^= 1;
+      if (!ok) break;
+      if (KDA && tid == 64 && it + 2 < nch) issue(it + 2, 0);
+      tc_fence_after();
+      {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          float x[32];
+          tmem_ld32(taddr(tb, warp * 32, BT_DS + h * 32), x);
+          if (KDA) {   // column i (key channel) of dS'^T decays by gamma_L[i]
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const float4 gv = *reinterpret_cast<const float4*>(glc + h * 32 + e);
+              fma2v(x[e], x[e + 1], gv.x, gv.y, dS[h * 32 + e], dS[h * 32 + e + 1]);
+              fma2v(x[e + 2], x[e + 3], gv.z, gv.w, dS[h * 32 + e + 2], dS[h * 32 + e + 3]);
+              dS[h * 32 + e] = x[e];
+              dS[h * 32 + e + 1] = x[e + 1];
+              dS[h * 32 + e + 2] = x[e + 2];
+              dS[h * 32 + e + 3] = x[e + 3];
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2)
+              fma2_to(dS[h * 32 + e], dS[h * 32 + e + 1], gL, dS[h * 32 + e], dS[h * 32 + e + 1], x[e], x[e + 1]);
+          }
+        }
+        store_row128(ds_tile, tid, dS);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      named_bar(BS_BAR, BS_CHAIN);
+      if (tid == 0) {
+        if (it + 1 < nch) mbar_arrive(&go_ds);   // the next chunk's DY may read the tile
+        if (it + 2 < nch) issue(it + 2, 1);      // MMA2 is done with Q
+      }
     }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && it + 2 < nch) issue(it + 2, 1);   // MMA2 is done with Q
-  }
-  if (tid == 0) bulk_wait_all();
-  if (warp == 1 && lane == 0 && pend) mbar_wait(&bar_pre, pph, a.err);   // no MMA may outlive the TMEM allocation
-  if (ok && a.walk) {
-    float* dst = a.dbend + ((size_t)split * a.HV + hv) * STATE_F32 + (size_t)tid * 128;
+    if (ok && a.walk) {
+      float* dst = a.dbend + ((size_t)split * a.HV + hv) * STATE_F32 + (size_t)tid * 128;
 #pragma unroll
-    for (int jj = 0; jj < 128; jj += 4)
-      *reinterpret_cast<float4*>(dst + jj) = make_float4(dS[jj], dS[jj + 1], dS[jj + 2], dS[jj + 3]);
-  }
-  if (ok && full && a.ds_in && a.seg_idx[seg] == 0) {   // the adjoint entering the document: dS_in
-    float* dst = a.ds_in + ((size_t)doc * a.HV + hv) * STATE_F32 + tid;   // column tid of dS_in [dk][dv]
+      for (int jj = 0; jj < 128; jj += 4)
+        *reinterpret_cast<float4*>(dst + jj) = make_float4(dS[jj], dS[jj + 1], dS[jj + 2], dS[jj + 3]);
+    }
+    if (ok && full && a.ds_in && a.seg_idx[seg] == 0) {   // the adjoint entering the document: dS_in
+      float* dst = a.ds_in + ((size_t)doc * a.HV + hv) * STATE_F32 + tid;   // column tid of dS_in [dk][dv]
 #pragma unroll
-    for (int jj = 0; jj < 128; ++jj) dst[jj * 128] = dS[jj];
+      for (int jj = 0; jj < 128; ++jj) dst[jj * 128] = dS[jj];
+    }
+    if (tid == 0) {
+      bulk_wait_all();
+      mbar_wait(&done, 0, a.err);   // no MMA may outlive the TMEM allocation
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1531,8 +1569,8 @@ gdn_status run_bwd_walks(const Plan& P, const gdn_problem& pr, const void* q, co
   if (P.nsplit > 0) {
     ba.walk = 1;
     prof_begin(K_BWD_WALK, s);
-    if (kda) bwd_scan_kernel<true><<<P.nsplit * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
-    else bwd_scan_kernel<false><<<P.nsplit * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
+    if (kda) bwd_scan_kernel<true><<<P.nsplit * P.HV, BS_THREADS, BS_SMEM_ALLOC, s>>>(ba);
+    else bwd_scan_kernel<false><<<P.nsplit * P.HV, BS_THREADS, BS_SMEM_ALLOC, s>>>(ba);
     prof_end(K_BWD_WALK, s);
     MergeBwdArgs ma;
     ma.sdoc_first = t.sdoc_first;
@@ -1547,8 +1585,8 @@ gdn_status run_bwd_walks(const Plan& P, const gdn_problem& pr, const void* q, co
   }
   ba.walk = 0;
   prof_begin(K_BWD_SCAN, s);
-  if (kda) bwd_scan_kernel<true><<<(P.NSEG - P.nsdoc) * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
-  else bwd_scan_kernel<false><<<(P.NSEG - P.nsdoc) * P.HV, 128, BS_SMEM_ALLOC, s>>>(ba);
+  if (kda) bwd_scan_kernel<true><<<(P.NSEG - P.nsdoc) * P.HV, BS_THREADS, BS_SMEM_ALLOC, s>>>(ba);
+  else bwd_scan_kernel<false><<<(P.NSEG - P.nsdoc) * P.HV, BS_THREADS, BS_SMEM_ALLOC, s>>>(ba);
   prof_end(K_BWD_SCAN, s);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
