@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(KP_THREADS, 2) kda_prep_kernel(const __grid_co
     __syncthreads();
     if (tid < 64) ut_diag_blocks(Sm, tid, 1);
     __syncthreads();
-    const UtInvTiles tiles{sm + KP_G, sm + KP_G + 8192, sm + KP_G + 16384, sm + KP_G + 24576};
+    const UtInvTiles tiles{sm + KP_G, sm + KP_G + 8192};
     ok = ut_tc_inverse<KP_THREADS>(Sm, tiles, tb, KT_INV, &bar_t, tph, a.err, t_pend);
   }
   if (ok) {

@@ -20,22 +20,19 @@ constexpr int PR_BLOCKS_PER_SM = 4;
 // Shared memory (bytes, 1024-aligned tiles).  The [K; Q] tile is dead once the
 // item's KK^T / QK^T MMA has completed; its space then holds, for each value
 // head in turn, the FP32 A^T array, then the BF16 tiles of the inverse (D, the
-// inverted diagonal blocks; L^T, then X; N; N^2), and finally the T', T'' and T
-// output tiles.  Aqk and the scalars sit past it.
+// inverted diagonal blocks; L^T, then X), and finally the T', T'' and T output
+// tiles.  Aqk and the scalars sit past it.
 constexpr int PR_KQ = 0;                             // [K; Q] SwTile(128 x 128), 32 KB
 constexpr int PR_S = 0;                              // FP32 S[64][UT_ALD]
 constexpr int PR_D = 0;                              // D (inverted diagonal blocks), SwTile(64 x 64)
-constexpr int PR_LX = TILE64_BYTES;                  // L^T, then X = I - N + N^2 - N^3
-constexpr int PR_N = 2 * TILE64_BYTES;               // N = D L
-constexpr int PR_N2 = 3 * TILE64_BYTES;              // N^2
+constexpr int PR_LX = TILE64_BYTES;                  // L^T, then X = I - N
 constexpr int PR_TP = 0;                             // T', then T'' (contiguous, one bulk store)
 constexpr int PR_T = 2 * TILE64_BYTES;               // T tile
 constexpr int PR_AQ = 32768;                         // Aqk tile
 constexpr int PR_SC = PR_AQ + TILE64_BYTES;          // scalars
 constexpr int PR_SMEM = PR_SC + CB_SCAL_BYTES;
 constexpr int PR_SMEM_ALLOC = PR_SMEM + 1024;
-static_assert(UT_WORK_BYTES <= PR_N + TILE64_BYTES, "the FP32 array is dead before N^2 is written");
-static_assert(4 * TILE64_BYTES <= PR_AQ, "the inverse's tiles fit below Aqk");
+static_assert(UT_WORK_BYTES <= PR_AQ && 3 * TILE64_BYTES <= PR_AQ, "the FP32 array and the tiles lie below Aqk");
 static_assert(PR_AQ % 1024 == 0 && PR_T % 1024 == 0, "swizzled tiles are 1024-aligned");
 static_assert(CB_SCAL_BYTES == UT_SCAL_BYTES, "one scalar block layout");
 // TMEM columns: the item's [KK^T; QK^T] (read by every value head), then the inverse's products
@@ -46,10 +43,10 @@ constexpr int PT_KK = 0, PT_INV = 64, PT_COLS = 128;
 // (each head's stores drain while the next one is prepared).  Four CTAs share
 // an SM, so the serial phases of one run under the others.  The UT arithmetic
 // is gdn_ut.cuh's, except for the inverse's block diagonals, which run on the
-// tensor cores: with D the inverted 16 x 16 diagonal blocks (FP32 forward
+// tensor cores: with D the inverted 32 x 32 diagonal blocks (FP32 forward
 // substitution) and L the strictly block-lower part of A,
-//   I + A = D^-1 (I + N),  N = D L,  N^4 = 0   =>   T = (I - N + N^2 - N^3) D,
-// four dependent M = 64 tcgen05 products (BF16 operands, FP32 accumulation).
+//   I + A = D^-1 (I + N),  N = D L,  N^2 = 0   =>   T = (I - N) D,
+// two dependent M = 64 tcgen05 products (BF16 operands, FP32 accumulation).
 __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(const __grid_constant__ PrepArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
@@ -101,10 +98,10 @@ __global__ void __launch_bounds__(PR_THREADS, PR_BLOCKS_PER_SM) prep_kernel(cons
   }
   // ---- the value heads of the group, one after another, on the one KK^T / QK^T
   bool ok = true;
-  uint32_t tph = 0;   // phase of bar_t (four products per value head)
+  uint32_t tph = 0;   // phase of bar_t (two products per value head)
   int t_pend = -1;    // error path: phase of a product whose completion was not seen (-1: none)
   float* Sm = reinterpret_cast<float*>(sm + PR_S);
-  const UtInvTiles tiles{sm + PR_D, sm + PR_LX, sm + PR_N, sm + PR_N2};
+  const UtInvTiles tiles{sm + PR_D, sm + PR_LX};
   const int r0 = 16 * warp + (lane >> 2), cq = 2 * (lane & 3);   // this thread's elements of T (see ut_ld_result)
   for (int hh = 0; hh < a.G; ++hh) {
     const int hv = j * a.G + hh;

@@ -14,9 +14,9 @@
 // on the intra / WY / GLM-prep programs; "#8542" page, the save-set table,
 // which lists gcum, Akk, Aqk, w and u among what the replay form recomputes).
 // KK^T and QK^T come from one tcgen05 MMA on the stacked [K; Q] tile (M = 128)
-// into 64 TMEM columns; of the unit lower-triangular inverse, the four 16 x 16
+// into 64 TMEM columns; of the unit lower-triangular inverse, the two 32 x 32
 // diagonal blocks are formed here in FP32 by forward substitution (one lane
-// per column); the kernel that calls these routines completes T from them.
+// per column), and two tensor-core products complete T (ut_tc_inverse).
 //
 // Gate factors: e^{G_r - G_c} for c <= r is the product e^{G_r - G_0}
 // e^{G_0 - G_c} of per-token factors when the chunk's gate range G_0 - G_{L-1}
@@ -234,22 +234,22 @@ __device__ __forceinline__ void ut_build(uint32_t tb, int wq, int kk, int lt, in
   }
 }
 
-// The four diagonal blocks T_bb = (I + A_bb)^-1 of T, in place in Sm, on lanes l = 0..63 (the
-// warps of one 64-thread group that syncs on named barrier `bar_id`): forward substitution, lane =
-// column; the upper triangles of the blocks are zeroed.  Call after the A^T rows of ut_build are
-// written.
+// The two diagonal blocks T_bb = (I + A_bb)^-1 of T (32 x 32 each), in place in Sm, on lanes l = 0..63
+// (the two warps of one 64-thread group that syncs on named barrier `bar_id`; warp b takes block b):
+// forward substitution in FP32, lane = column; the upper triangles of the blocks are zeroed.  Call
+// after the A^T rows of ut_build are written.
 __device__ __forceinline__ void ut_diag_blocks(float* Sm, int l, int bar_id) {
   named_bar(bar_id, 64);
   {
-    const int o = 16 * (l >> 4), cc = l & 15;
-    float x[16];
+    const int o = 32 * (l >> 5), cc = l & 31;
+    float x[32];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = (i == cc) ? 1.f : 0.f;
+    for (int i = 0; i < 32; ++i) x[i] = (i == cc) ? 1.f : 0.f;
 #pragma unroll
-    for (int jq = 0; jq < 15; ++jq) {
+    for (int jq = 0; jq < 31; ++jq) {   // x[i] -= A[i][jq] x[jq] for i > jq (row jq of the array: A[.][jq])
       const float xj = x[jq];
 #pragma unroll
-      for (int g4 = (jq + 1) >> 2; g4 < 4; ++g4) {
+      for (int g4 = (jq + 1) >> 2; g4 < 8; ++g4) {
         const float4 av = *reinterpret_cast<const float4*>(Sm + (o + jq) * UT_ALD + o + 4 * g4);
         if (4 * g4 + 0 > jq) fma2(x[4 * g4 + 0], x[4 * g4 + 1], -av.x, -av.y, xj);
         else if (4 * g4 + 1 > jq) x[4 * g4 + 1] = fmaf(-av.y, xj, x[4 * g4 + 1]);
@@ -259,26 +259,24 @@ __device__ __forceinline__ void ut_diag_blocks(float* Sm, int l, int bar_id) {
     }
     __syncwarp();   // every lane of the block has read its A entries
 #pragma unroll
-    for (int i = 0; i < 16; ++i) Sm[(o + i) * UT_ALD + o + cc] = x[i];   // x[i] = 0 above the diagonal
+    for (int i = 0; i < 32; ++i) Sm[(o + i) * UT_ALD + o + cc] = x[i];   // x[i] = 0 above the diagonal
   }
 }
 
 // ---------------------------------------------------------------------------
-// The rest of T = (I + A)^-1 on the tensor cores, after ut_diag_blocks.  With D the inverted 16 x 16
-// diagonal blocks and L the strictly block-lower part of A,
-//   I + A = D^-1 (I + N),  N = D L,  N^4 = 0   =>   T = (I - N + N^2 - N^3) D,
-// four dependent M = 64 tcgen05 products (BF16 operands, FP32 accumulation).  Run by all 128 threads
-// of the CTA; thread 0 issues.  The FP32 array Sm (row n: T_bb in n's block, A[c][n] in the later
-// blocks' columns c) is read into registers before the tiles are written, so tiles d and lx may lie
-// over it; n and n2 are written after the first product.  T is left in TMEM columns inv .. inv + 63
-// (M = 64 layout; read it with ut_ld_result).  tph is the phase of `bar`; t_pend receives the phase
-// of a product whose completion was not seen when a wait runs out (the caller drains it).
+// The rest of T = (I + A)^-1 on the tensor cores, after ut_diag_blocks.  With D the two inverted
+// 32 x 32 diagonal blocks and L the strictly block-lower part of A (its lower-left 32 x 32 block),
+//   I + A = D^-1 (I + N),  N = D L,  N^2 = 0   =>   T = (I - N) D,
+// two dependent M = 64 tcgen05 products (BF16 operands, FP32 accumulation).  Run by all NT threads
+// of the CTA; warp 0 issues.  The FP32 array Sm (row n: T_bb in n's block, A[c][n] in the later
+// block's columns c) is read into registers before the tiles are written, so the tiles may lie over
+// it.  T is left in TMEM columns inv .. inv + 63 (M = 64 layout; read it with ut_ld_result).  tph is
+// the phase of `bar`; t_pend receives the phase of a product whose completion was not seen when a
+// wait runs out (the caller drains it).
 // ---------------------------------------------------------------------------
 struct UtInvTiles {
   uint8_t* d;    // D, SwTile(64 x 64)
-  uint8_t* lx;   // L^T, then X = I - N + N^2 - N^3
-  uint8_t* n;    // N
-  uint8_t* n2;   // N^2
+  uint8_t* lx;   // L^T, then X = I - N
 };
 
 // The 16-column groups of an M = 64, N = 64 result that warp `warp` of an NT-thread CTA reads: the
@@ -309,7 +307,7 @@ __device__ __forceinline__ bool ut_tc_inverse(const float* Sm, const UtInvTiles&
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r0 = 16 * (warp & 3) + (lane >> 2), cq = 2 * (lane & 3), g0 = UtGroups<NT>::first(warp);
   {  // D and L^T as BF16 tiles from rows of the array: row n holds T_bb (columns of n's block, zero
-     // above the diagonal) and, in the later blocks' columns c, A[c][n] = L^T[n][c]
+     // above the diagonal) and, in the later block's columns c, A[c][n] = L^T[n][c]
     uint4 dch[512 / NT], lch[512 / NT];
 #pragma unroll
     for (int it = 0; it < 512 / NT; ++it) {
@@ -319,7 +317,7 @@ __device__ __forceinline__ bool ut_tc_inverse(const float* Sm, const UtInvTiles&
       const uint4 w = make_uint4(pack_bf16(u0.x, u0.y), pack_bf16(u0.z, u0.w), pack_bf16(u1.x, u1.y),
                                  pack_bf16(u1.z, u1.w));
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      const int bn = n >> 4, bc = c8 >> 1;
+      const int bn = n >> 5, bc = c8 >> 2;
       dch[it] = bc == bn ? w : z;
       lch[it] = bc > bn ? w : z;
     }
@@ -352,45 +350,18 @@ __device__ __forceinline__ bool ut_tc_inverse(const float* Sm, const UtInvTiles&
   };
   uint32_t u[NG][8];
   // (a K-major B tile is rows N, columns K; L^T is that form of L.  An MN-major B tile is rows K,
-  // columns N: a row-major N or D.)
+  // columns N: a row-major D.)
   bool ok = product(tl.d, tl.lx, false);   // N = D L
-  if (ok) {  // N -> BF16 tile
+  if (ok) {  // X = I - N -> BF16 tile (over L^T, which N = D L has finished reading)
     ut_ld_result<NT>(tb, inv, warp, u);
 #pragma unroll
     for (int g = 0; g < NG; ++g)
 #pragma unroll
       for (int i = 0; i < 8; i += 2) {
         const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * (g0 + g) + 8 * (i >> 2) + cq;
-        *reinterpret_cast<uint32_t*>(tl.n + sw_off(r, cc, 64)) =
-            pack_bf16(__uint_as_float(u[g][i]), __uint_as_float(u[g][i + 1]));
-      }
-  }
-  ok = ok && product(tl.n, tl.n, true);   // N^2 = N N
-  if (ok) {
-    ut_ld_result<NT>(tb, inv, warp, u);
-#pragma unroll
-    for (int g = 0; g < NG; ++g)
-#pragma unroll
-      for (int i = 0; i < 8; i += 2) {
-        const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * (g0 + g) + 8 * (i >> 2) + cq;
-        *reinterpret_cast<uint32_t*>(tl.n2 + sw_off(r, cc, 64)) =
-            pack_bf16(__uint_as_float(u[g][i]), __uint_as_float(u[g][i + 1]));
-      }
-  }
-  ok = ok && product(tl.n2, tl.n, true);   // N^3 = N^2 N
-  if (ok) {  // X = I - N + N^2 - N^3 -> BF16 tile (over L^T, which N = D L has finished reading)
-    ut_ld_result<NT>(tb, inv, warp, u);
-#pragma unroll
-    for (int g = 0; g < NG; ++g)
-#pragma unroll
-      for (int i = 0; i < 8; i += 2) {
-        const int r = r0 + 8 * ((i >> 1) & 1), cc = 16 * (g0 + g) + 8 * (i >> 2) + cq;
-        const uint32_t off = sw_off(r, cc, 64);
-        const float2 n1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(tl.n + off));
-        const float2 n2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(tl.n2 + off));
-        const float x0 = (r == cc ? 1.f : 0.f) - n1.x + n2.x - __uint_as_float(u[g][i]);
-        const float x1 = (r == cc + 1 ? 1.f : 0.f) - n1.y + n2.y - __uint_as_float(u[g][i + 1]);
-        *reinterpret_cast<uint32_t*>(tl.lx + off) = pack_bf16(x0, x1);
+        const float x0 = (r == cc ? 1.f : 0.f) - __uint_as_float(u[g][i]);
+        const float x1 = (r == cc + 1 ? 1.f : 0.f) - __uint_as_float(u[g][i + 1]);
+        *reinterpret_cast<uint32_t*>(tl.lx + sw_off(r, cc, 64)) = pack_bf16(x0, x1);
       }
   }
   ok = ok && product(tl.lx, tl.d, true);   // T = X D
