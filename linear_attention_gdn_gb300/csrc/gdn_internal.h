@@ -150,7 +150,7 @@ struct ScanArgs {
 
 // the per-channel-decay preparation of every (chunk, value head)
 struct KdaPrepArgs {
-  CUtensorMap tq, tk;
+  CUtensorMap tq, tk, tg;
   const float* g;             // [T][HV][128] log decay per key channel
   const float* beta;          // [T][HV]
   const int* chunk_tok0;
@@ -240,6 +240,9 @@ gdn_status make_kda_plan(const gdn_problem* p, const int32_t* cu, Plan* P);
 bool device_setup();
 bool aligned16(const void* p);
 bool make_tmap(CUtensorMap* m, const void* base, int64_t T, int heads);
+// FP32 [T][heads][128] (the per-channel log decay g): boxes of 64 tokens x 128 channels of one head,
+// no swizzle, rows past T read as zero
+bool make_tmap_g(CUtensorMap* m, const float* base, int64_t T, int heads);
 gdn_status run_tables(const Plan& P, const gdn_problem* p, const int32_t* cu_dev, uint8_t* ws, void* saved,
                       cudaStream_t s);
 void launch_fwd_scan(const ScanArgs& a, int nchains, cudaStream_t s);

@@ -104,17 +104,14 @@ __global__ void __launch_bounds__(KP_THREADS, 2) kda_prep_kernel(const __grid_co
     mbar_init(&bar_t, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
     unsafe = 0;
-    // the K, Q tiles and the value head's g rows (512 B each, one bulk copy per token) on one barrier
-    mbar_expect_tx(&bar_ld, 32768u + (uint32_t)L * 512u);
+    // the K, Q tiles and the value head's 64 g rows (one TMA box; rows past L are read as zero below)
+    mbar_expect_tx(&bar_ld, 32768u + 32768u);
     tma_load_3d(kq, &a.tk, 0, j, tok0, &bar_ld);
     tma_load_3d(kq + 8192, &a.tq, 0, j, tok0, &bar_ld);
     tma_load_3d(kq + 16384, &a.tk, 64, j, tok0, &bar_ld);
     tma_load_3d(kq + 24576, &a.tq, 64, j, tok0, &bar_ld);
-    const float* gp = a.g + ((size_t)tok0 * a.HV + hv) * D;
-    for (int r = 0; r < L; ++r) bulk_load(Gm + r * D, gp + (size_t)r * a.HV * D, 512u, &bar_ld);
+    tma_load_3d(Gm, &a.tg, 0, hv, tok0, &bar_ld);
   }
-  for (int idx = tid; idx < (CH - L) * 32; idx += KP_THREADS)   // rows past L: zero
-    *reinterpret_cast<float4*>(Gm + (L + (idx >> 5)) * D + 4 * (idx & 31)) = make_float4(0.f, 0.f, 0.f, 0.f);
   if (tid < CH) bs[tid] = tid < L ? a.beta[(size_t)(tok0 + tid) * a.HV + hv] : 0.f;
   __syncthreads();   // the barriers' initialisation is visible before any thread waits on them
   bool landed = __syncthreads_and(mbar_wait(&bar_ld, 0, a.err));
@@ -127,7 +124,7 @@ __global__ void __launch_bounds__(KP_THREADS, 2) kda_prep_kernel(const __grid_co
         ref = run;
         gx[r >> 4][i] = run;
       }
-      run = fmaf(Gm[r * D + i], kUtLog2e, run);
+      run = fmaf(r < L ? Gm[r * D + i] : 0.f, kUtLog2e, run);   // (rows past L: the next document's)
       Gm[r * D + i] = run;
       mx = fmaxf(mx, fabsf(run - ref));
     }
@@ -589,7 +586,8 @@ gdn_status run_kda_prep(const Plan& P, const gdn_problem* p, const void* q, cons
   Tables t = tables_at(P, ws);
   KdaPrepArgs pa;
   memset(&pa, 0, sizeof(pa));
-  if (!make_tmap(&pa.tq, q, P.T, P.H) || !make_tmap(&pa.tk, k, P.T, P.H)) return GDN_ERR_CUDA;
+  if (!make_tmap(&pa.tq, q, P.T, P.H) || !make_tmap(&pa.tk, k, P.T, P.H) || !make_tmap_g(&pa.tg, g, P.T, P.HV))
+    return GDN_ERR_CUDA;
   pa.g = g;
   pa.beta = beta;
   pa.chunk_tok0 = t.chunk_tok0;

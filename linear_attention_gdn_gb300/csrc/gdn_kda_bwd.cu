@@ -39,7 +39,7 @@
 namespace gdn {
 
 struct KdaGradArgs {
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tg;
   const float* g;
   const float* beta;
   const uint8_t* kb;      // [NC][HV][KB_BYTES] (T, M^T)
@@ -240,8 +240,7 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
     const size_t blk = (size_t)c * a.HV + hv;
     if (tid == 0) {   // this value head's tiles
       const uint8_t* kbp = a.kb + blk * KB_BYTES;
-      mbar_expect_tx(&bar_ld, (uint32_t)(2 * STATE_BYTES + 2 * VN_BYTES + 2 * 16384 + 2 * TILE64_BYTES) +
-                                  (uint32_t)L * 512u);
+      mbar_expect_tx(&bar_ld, (uint32_t)(2 * STATE_BYTES + 2 * VN_BYTES + 2 * 16384 + 2 * TILE64_BYTES) + 32768u);
       bulk_load(X + KX_S, a.tape + blk * STATE_BYTES, STATE_BYTES, &bar_ld);
       bulk_load(X + KX_DS, a.dtape + blk * STATE_BYTES, STATE_BYTES, &bar_ld);
       bulk_load(X + KX_VN, a.vn + blk * VN_BYTES, VN_BYTES, &bar_ld);
@@ -252,12 +251,9 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
       tma_load_3d(X + KX_V + 8192, &a.tv, 64, hv, tok0, &bar_ld);
       bulk_load(sm + KG_T, kbp + KB_T, TILE64_BYTES, &bar_ld);
       bulk_load(sm + KG_MT, kbp + KB_MT, TILE64_BYTES, &bar_ld);
-      const float* gp = a.g + ((size_t)tok0 * a.HV + hv) * D;   // g: one 512-byte row per token
-      for (int r = 0; r < L; ++r) bulk_load(Gm + r * D, gp + (size_t)r * a.HV * D, 512u, &bar_ld);
+      tma_load_3d(Gm, &a.tg, 0, hv, tok0, &bar_ld);   // the 64 g rows (rows past L are read as zero below)
     }
     ld_pend = true;
-    for (int idx = tid; idx < (CH - L) * 32; idx += KG_THREADS)   // g rows past L: zero
-      *reinterpret_cast<float4*>(Gm + (L + (idx >> 5)) * D + 4 * (idx & 31)) = make_float4(0.f, 0.f, 0.f, 0.f);
     if (tid < CH) bs[tid] = tid < L ? a.beta[(size_t)(tok0 + tid) * a.HV + hv] : 0.f;
     ok = __syncthreads_and(mbar_wait(&bar_ld, ldph, a.err));
     if (!ok) break;
@@ -268,7 +264,7 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
       float run = 0.f;
       for (int r = 0; r < CH; ++r) {
         if ((r & 15) == 0) gx[r >> 4][i] = run;
-        run = fmaf(Gm[r * D + i], kUtLog2e, run);
+        run = fmaf(r < L ? Gm[r * D + i] : 0.f, kUtLog2e, run);   // (rows past L: the next document's)
         Gm[r * D + i] = run;
       }
       glL[i] = run;
@@ -781,7 +777,7 @@ static gdn_status run_kda_bwd(const Plan& P, const gdn_problem& pr, const void* 
   KdaGradArgs ga;
   memset(&ga, 0, sizeof(ga));
   if (!make_tmap(&ga.tq, q, P.T, P.H) || !make_tmap(&ga.tk, k, P.T, P.H) || !make_tmap(&ga.tv, v, P.T, P.HV) ||
-      !make_tmap(&ga.tdo, dO, P.T, P.HV))
+      !make_tmap(&ga.tdo, dO, P.T, P.HV) || !make_tmap_g(&ga.tg, g, P.T, P.HV))
     return GDN_ERR_CUDA;
   ga.g = g;
   ga.beta = beta;
