@@ -252,6 +252,20 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
       bulk_load(sm + KG_T, kbp + KB_T, TILE64_BYTES, &bar_ld);
       bulk_load(sm + KG_MT, kbp + KB_MT, TILE64_BYTES, &bar_ld);
       tma_load_3d(Gm, &a.tg, 0, hv, tok0, &bar_ld);   // the 64 g rows (rows past L are read as zero below)
+      if (hh + 1 < a.G) {   // the next value head's tiles into L2 while this one is worked on (a hint)
+        const size_t nb = blk + 1;
+        bulk_prefetch(a.tape + nb * STATE_BYTES, STATE_BYTES);
+        bulk_prefetch(a.dtape + nb * STATE_BYTES, STATE_BYTES);
+        bulk_prefetch(a.vn + nb * VN_BYTES, VN_BYTES);
+        bulk_prefetch(a.dvn + nb * VN_BYTES, VN_BYTES);
+        tma_prefetch_3d(&a.tdo, 0, hv + 1, tok0);
+        tma_prefetch_3d(&a.tdo, 64, hv + 1, tok0);
+        tma_prefetch_3d(&a.tv, 0, hv + 1, tok0);
+        tma_prefetch_3d(&a.tv, 64, hv + 1, tok0);
+        bulk_prefetch(a.kb + nb * KB_BYTES + KB_T, TILE64_BYTES);
+        bulk_prefetch(a.kb + nb * KB_BYTES + KB_MT, TILE64_BYTES);
+        tma_prefetch_3d(&a.tg, 0, hv + 1, tok0);
+      }
     }
     ld_pend = true;
     if (tid < CH) bs[tid] = tid < L ? a.beta[(size_t)(tok0 + tid) * a.HV + hv] : 0.f;
