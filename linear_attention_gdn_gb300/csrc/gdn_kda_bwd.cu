@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
   __shared__ __align__(16) float rowdb[KG_WG][CH];   // partial row sums (per warpgroup's columns)
   __shared__ __align__(16) float cum[KG_WG][D];      // per-warpgroup totals of the reverse cumulative sum
   __shared__ __align__(16) float pdiag[CH];    // dP_rr (kept out of the decay-weighted products)
-  __shared__ uint64_t bar_qk, bar_ld, bar_m;
+  __shared__ uint64_t bar_qk, bar_ld, bar_g, bar_m;
   __shared__ uint32_t tslot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = tid >> 7, lt = tid & 127, wq = warp & 3;
   const int c0 = KG_CW * wg;   // this thread's columns (tokens) of a 64-column result
@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
   if (tid == 0) {
     mbar_init(&bar_qk, 1);
     mbar_init(&bar_ld, 1);
+    mbar_init(&bar_g, 1);
     mbar_init(&bar_m, 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
     mbar_expect_tx(&bar_qk, 32768u);
@@ -240,7 +241,11 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
     const size_t blk = (size_t)c * a.HV + hv;
     if (tid == 0) {   // this value head's tiles
       const uint8_t* kbp = a.kb + blk * KB_BYTES;
-      mbar_expect_tx(&bar_ld, (uint32_t)(2 * STATE_BYTES + 2 * VN_BYTES + 2 * 16384 + 2 * TILE64_BYTES) + 32768u);
+      // the 64 g rows first, on their own barrier (rows past L are read as zero below): the decay
+      // cumsum runs while the rest lands
+      mbar_expect_tx(&bar_g, 32768u);
+      tma_load_3d(Gm, &a.tg, 0, hv, tok0, &bar_g);
+      mbar_expect_tx(&bar_ld, (uint32_t)(2 * STATE_BYTES + 2 * VN_BYTES + 2 * 16384 + 2 * TILE64_BYTES));
       bulk_load(X + KX_S, a.tape + blk * STATE_BYTES, STATE_BYTES, &bar_ld);
       bulk_load(X + KX_DS, a.dtape + blk * STATE_BYTES, STATE_BYTES, &bar_ld);
       bulk_load(X + KX_VN, a.vn + blk * VN_BYTES, VN_BYTES, &bar_ld);
@@ -251,7 +256,6 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
       tma_load_3d(X + KX_V + 8192, &a.tv, 64, hv, tok0, &bar_ld);
       bulk_load(sm + KG_T, kbp + KB_T, TILE64_BYTES, &bar_ld);
       bulk_load(sm + KG_MT, kbp + KB_MT, TILE64_BYTES, &bar_ld);
-      tma_load_3d(Gm, &a.tg, 0, hv, tok0, &bar_ld);   // the 64 g rows (rows past L are read as zero below)
       if (hh + 1 < a.G) {   // the next value head's tiles into L2 while this one is worked on (a hint)
         const size_t nb = blk + 1;
         bulk_prefetch(a.tape + nb * STATE_BYTES, STATE_BYTES);
@@ -269,10 +273,8 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
     }
     ld_pend = true;
     if (tid < CH) bs[tid] = tid < L ? a.beta[(size_t)(tok0 + tid) * a.HV + hv] : 0.f;
-    ok = __syncthreads_and(mbar_wait(&bar_ld, ldph, a.err));
+    ok = __syncthreads_and(mbar_wait(&bar_g, ldph, a.err));
     if (!ok) break;
-    ldph ^= 1;
-    ld_pend = false;
     if (tid < 128) {   // channel tid: cumulative decay (log2 units), block entries, block ratios
       const int i = tid;
       float run = 0.f;
@@ -287,6 +289,10 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
 #pragma unroll
         for (int b = 0; b < aa; ++b) fab[kg_pair(aa, b)][i] = exp2f(gx[aa][i] - gx[b][i]);
     }
+    ok = __syncthreads_and(mbar_wait(&bar_ld, ldph, a.err));   // the other tiles
+    if (!ok) break;
+    ldph ^= 1;
+    ld_pend = false;
     if (L < CH) {   // zero the dO, V rows past the document end
       for (int idx = tid; idx < (CH - L) * 32; idx += KG_THREADS) {
         const int t = idx >> 5, tile = (idx >> 4) & 1, c8 = idx & 15;
@@ -580,21 +586,30 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
 #pragma unroll 1
       for (int h = 0; h < KG_NH; ++h) {
         const int aa = (c0 >> 4) + h, cb = c0 + 16 * h;
-        float rm[16], rp[16], z[16];
+        float rm[16], rp[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) rm[e] = rp[e] = 0.f;
-        for (int b = 0; b <= aa; ++b) {
+        for (int b = 0; b <= aa; ++b) {   // Z_b and Zp_b of the block pair: two loads, one wait
           const float f = b == aa ? 1.f : fab[kg_pair(aa, b)][i];
-          tld16c(KGT_Z + kZOff[b] + 16 * (aa - b), z);
+          uint32_t zm[16], zp[16];
+          tmem_ld16_async(taddr(tb, wq * 32, KGT_Z + kZOff[b] + 16 * (aa - b)), zm);
+          tmem_ld16_async(taddr(tb, wq * 32, kZPCol[b] + 16 * (aa - b)), zp);
+          tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) rm[e] = fmaf(f, z[e], rm[e]);
-          tld16c(kZPCol[b] + 16 * (aa - b), z);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) rp[e] = fmaf(f, z[e], rp[e]);
+          for (int e = 0; e < 16; ++e) {
+            rm[e] = fmaf(f, __uint_as_float(zm[e]), rm[e]);
+            rp[e] = fmaf(f, __uint_as_float(zp[e]), rp[e]);
+          }
         }
         float aq[16], ak[16], dg[16];
-        tld16c(KGT_DQ + cb, aq);
-        tld16c(KGT_DK + cb, ak);
+        {
+          uint32_t uq[16], uk[16];
+          tmem_ld16_async(taddr(tb, wq * 32, KGT_DQ + cb), uq);
+          tmem_ld16_async(taddr(tb, wq * 32, KGT_DK + cb), uk);
+          tmem_wait_ld();
+          as_float16(uq, aq);
+          as_float16(uk, ak);
+        }
         tld16c(KGT_DG + cb, dg);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -633,15 +648,31 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
         float cl[16], y[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) cl[e] = 0.f;
-        for (int aa = b; aa < 4; ++aa) {
+        int aa = b;
+        for (; aa + 1 < 4; aa += 2) {   // two Y blocks per wait
+          const float f0 = aa == b ? 1.f : fab[kg_pair(aa, b)][i], f1 = fab[kg_pair(aa + 1, b)][i];
+          uint32_t y0[16], y1[16];
+          tmem_ld16_async(taddr(tb, wq * 32, KGT_Z + kYOff[aa] + cb), y0);
+          tmem_ld16_async(taddr(tb, wq * 32, KGT_Z + kYOff[aa + 1] + cb), y1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) cl[e] = fmaf(f1, __uint_as_float(y1[e]), fmaf(f0, __uint_as_float(y0[e]), cl[e]));
+        }
+        if (aa < 4) {
           const float f = aa == b ? 1.f : fab[kg_pair(aa, b)][i];
           tld16c(KGT_Z + kYOff[aa] + cb, y);
 #pragma unroll
           for (int e = 0; e < 16; ++e) cl[e] = fmaf(f, y[e], cl[e]);
         }
         float ak[16], dg[16];
-        tld16c(KGT_DK + cb, ak);
-        tld16c(KGT_DG + cb, dg);
+        {
+          uint32_t uk[16], ug[16];
+          tmem_ld16_async(taddr(tb, wq * 32, KGT_DK + cb), uk);
+          tmem_ld16_async(taddr(tb, wq * 32, KGT_DG + cb), ug);
+          tmem_wait_ld();
+          as_float16(uk, ak);
+          as_float16(ug, dg);
+        }
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int r = cb + e;
@@ -758,7 +789,10 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
   }
   if (tid == 0 && !ok) {   // error path (bounded waits): nothing may land in or read this CTA's memory
     if (mma_pend) mbar_drain(&bar_m, mph);
-    if (ld_pend) mbar_drain(&bar_ld, ldph);
+    if (ld_pend) {
+      mbar_drain(&bar_g, ldph);
+      mbar_drain(&bar_ld, ldph);
+    }
     if (qk_pend) mbar_drain(&bar_qk, 0);
   }
   tc_fence_before();
