@@ -248,6 +248,19 @@ bool make_tmap_g(CUtensorMap* m, const float* base, int64_t T, int heads) {
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_rows(CUtensorMap* m, const void* base, int64_t T, int C, int rows) {
+  auto fn = encode_fn();
+  if (!fn || C % 256 != 0) return false;
+  cuuint64_t dims[3] = {256, (cuuint64_t)(C / 256), (cuuint64_t)std::max<int64_t>(T, 1)};
+  cuuint64_t strides[2] = {256 * 2, (cuuint64_t)C * 2};
+  cuuint32_t box[3] = {256, 2, (cuuint32_t)rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool device_setup() {
   static std::mutex mu;
   static bool done[128] = {};

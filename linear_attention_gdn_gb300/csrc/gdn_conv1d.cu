@@ -50,6 +50,7 @@ constexpr int CV_SMEM_B = CV_NS * 2 * CV_RSB * CV_ROWB;   // 48 KB
 constexpr int CV_WS_HEAD = 16;                    // the backward workspace opens with the status word
 
 struct ConvArgs {
+  CUtensorMap tx, tdy;   // the backward's row boxes of x and dy (when tma is set)
   const __nv_bfloat16* x;
   const float* w;        // [C][W]
   const float* b;        // [C] or null
@@ -63,6 +64,7 @@ struct ConvArgs {
   float* db;             // [C]
   int64_t T;
   int N, C, W, R;        // R: tokens per range (grid.y ranges)
+  int tma;               // backward: stages land as two TMA boxes (C a multiple of 256), else row copies
 };
 
 __device__ __forceinline__ uint2 ld_raw(const __nv_bfloat16* p) {
@@ -299,7 +301,7 @@ struct BwdState {
 // CTA's channels per row and tensor, the x rows of a stage then its dy rows); every thread reads
 // its 8 bytes of each row from shared memory.
 template <int W>
-__global__ void __launch_bounds__(CV_THREADS) conv_bwd_kernel(const ConvArgs a) {
+__global__ void __launch_bounds__(CV_THREADS) conv_bwd_kernel(const __grid_constant__ ConvArgs a) {
   extern __shared__ __align__(128) uint8_t cv_sm[];
   __shared__ uint64_t full[CV_NS];
   const int cb = blockIdx.x * CV_CH, nchan = min(CV_CH, a.C - cb);
@@ -322,6 +324,12 @@ __global__ void __launch_bounds__(CV_THREADS) conv_bwd_kernel(const ConvArgs a) 
     const int nr = left <= 0 ? 0 : (left < CV_RSB ? (int)left : CV_RSB);
     uint8_t* base = cv_sm + (st % CV_NS) * STAGE;
     uint64_t* bar = &full[st % CV_NS];
+    if (a.tma) {   // one box per tensor: CV_RSB rows of this CTA's 512 channels (past T or C: zero)
+      mbar_expect_tx(bar, (uint32_t)(2 * CV_RSB * CV_ROWB));
+      tma_load_3d(base, &a.tx, 0, 2 * (int)blockIdx.x, (int)r0, bar);
+      tma_load_3d(base + CV_RSB * CV_ROWB, &a.tdy, 0, 2 * (int)blockIdx.x, (int)r0, bar);
+      return;
+    }
     mbar_expect_tx(bar, (uint32_t)(2 * nr * nchan * 2));
     for (int r = 0; r < nr; ++r) {
       bulk_load(base + r * CV_ROWB, a.x + (r0 + r) * a.C + cb, nchan * 2, bar);
@@ -488,6 +496,8 @@ gdn_status gdn_conv1d_bwd(const gdn_conv_problem* p, const void* x, const float*
   a.C = p->C;
   a.W = p->W;
   a.R = CV_RB;
+  a.tma = p->C % 256 == 0 && make_tmap_rows(&a.tx, x, p->T, p->C, CV_RSB) &&
+          make_tmap_rows(&a.tdy, dy, p->T, p->C, CV_RSB);
   const int S = conv_ranges(p->T, CV_RB);
   const dim3 grid((p->C + CV_CH - 1) / CV_CH, S);
   if (!conv_setup()) return GDN_ERR_CUDA;

@@ -243,6 +243,9 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t T, int heads);
 // FP32 [T][heads][128] (the per-channel log decay g): boxes of 64 tokens x 128 channels of one head,
 // no swizzle, rows past T read as zero
 bool make_tmap_g(CUtensorMap* m, const float* base, int64_t T, int heads);
+// BF16 [T][C] with C a multiple of 256, seen as [T][C / 256][256]: boxes of `rows` tokens x 512 channels
+// (two 256-channel halves, so a box lands as `rows` rows of 1 KB), no swizzle, rows past T read as zero
+bool make_tmap_rows(CUtensorMap* m, const void* base, int64_t T, int C, int rows);
 gdn_status run_tables(const Plan& P, const gdn_problem* p, const int32_t* cu_dev, uint8_t* ws, void* saved,
                       cudaStream_t s);
 void launch_fwd_scan(const ScanArgs& a, int nchains, cudaStream_t s);
