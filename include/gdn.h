@@ -237,10 +237,13 @@ gdn_status gdn_conv1d_bwd(const gdn_conv_problem *prob, const void *x, const flo
  * print no formula, and this is the GDN rule above with its scalar decay replaced by a per-channel
  * one).  Conventions as for the GDN entry points, except:
  *   - g and dg are [T][HV][128] FP32: the log decay of each key channel (g <= 0 for a decay);
- *   - prob->saved_form is ignored.  The saved set holds the header, the BF16 state entering every
- *     chunk (32 KiB per chunk and value head), M_seg where a document is split, and the BF16
- *     V_new^T of every chunk (16 KiB per chunk and value head); the backward recomputes the
- *     per-chunk decay products and UT blocks (the pages' replay of w, u and the A matrices);
+ *   - the saved set holds the header, the BF16 state entering every chunk (32 KiB per chunk and
+ *     value head), M_seg where a document is split, and the BF16 V_new^T of every chunk (16 KiB
+ *     per chunk and value head).  With prob->saved_form == GDN_SAVED_FULL (the default) it also
+ *     keeps the forward's per-chunk blocks of decay products and UT tiles (82,944 B per chunk and
+ *     value head: Kd, -W^T, T'', T, Aqk, M^T, Q~, the scalars), which the backward reads; with
+ *     GDN_SAVED_REPLAY the backward recomputes them (the pages' replay of w, u and the A
+ *     matrices).  Both give the same gradients, bit for bit;
  *   - a chunk in which some key channel decays by more than 2^-96 within one 16-token block (a
  *     log decay below -66.5 over 16 tokens) is refused on the device: the error word is set to
  *     GDN_ERR_GATE_RANGE and the outputs are left unwritten.  Below that bound every chunk is

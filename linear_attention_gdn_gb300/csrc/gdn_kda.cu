@@ -533,12 +533,16 @@ void setup_kda_attrs() {
 static size_t kda_align(size_t x, size_t al) { return (x + al - 1) / al * al; }
 
 // The KDA layouts on top of the common plan (tables and segment plan): workspace = tables, the
-// per-chunk blocks, the split-walk states, the forward's own tape and V_new^T when no saved set is
-// given; then the backward's tapes.  Saved set = header, state tape, M_seg, V_new^T.
+// per-chunk blocks (of a forward without a full saved set, and of a replay-form backward), the
+// split-walk states, the forward's own tape and V_new^T when no saved set is given; then the
+// backward's tapes.  Saved set = header, state tape, M_seg, V_new^T and, in the full form
+// (prob->saved_form == GDN_SAVED_FULL, header form 3), the per-chunk blocks; the replay form
+// (header form 2) leaves the blocks out and the backward forms them again.
 gdn_status make_kda_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
   gdn_status st = make_plan(p, cu, P);
   if (st != GDN_OK) return st;
-  P->form = 2;
+  const bool full = p->saved_form == GDN_SAVED_FULL;
+  P->form = full ? 3 : 2;
   const size_t units = (size_t)P->NC * P->HV;
   const size_t st_f32 = (size_t)P->nsplit * P->HV * STATE_F32 * 4;
   size_t off = kda_align(P->o_tables[16], 1024);
@@ -569,8 +573,8 @@ gdn_status make_kda_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
   P->s_tape = SAVED_HEADER;
   P->s_mseg = P->s_tape + units * STATE_BYTES;
   P->s_vn = kda_align(P->s_mseg + st_f32, 1024);
-  P->s_cb = P->s_vn;
-  P->saved_bytes = P->s_vn + units * VN_BYTES;
+  P->s_cb = full ? kda_align(P->s_vn + units * VN_BYTES, 1024) : P->s_vn;
+  P->saved_bytes = full ? P->s_cb + units * KB_BYTES : P->s_vn + units * VN_BYTES;
   return GDN_OK;
 }
 
@@ -582,7 +586,7 @@ void launch_kda_prep(const KdaPrepArgs& a, int NC, cudaStream_t s) {
 }
 
 gdn_status run_kda_prep(const Plan& P, const gdn_problem* p, const void* q, const void* k, const float* g,
-                        const float* beta, uint8_t* ws, cudaStream_t s) {
+                        const float* beta, uint8_t* kb, uint8_t* ws, cudaStream_t s) {
   Tables t = tables_at(P, ws);
   KdaPrepArgs pa;
   memset(&pa, 0, sizeof(pa));
@@ -592,7 +596,7 @@ gdn_status run_kda_prep(const Plan& P, const gdn_problem* p, const void* q, cons
   pa.beta = beta;
   pa.chunk_tok0 = t.chunk_tok0;
   pa.chunk_len = t.chunk_len;
-  pa.kb = ws + P.o_cb;
+  pa.kb = kb;
   pa.H = P.H;
   pa.HV = P.HV;
   pa.G = P.G;
@@ -608,16 +612,18 @@ static gdn_status run_kda_fwd(const Plan& P, const gdn_problem* p, const void* q
   gdn_status st = run_tables(P, p, cu_dev, ws, saved, s);
   if (st != GDN_OK) return st;
   if (P.NC == 0) return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
-  st = run_kda_prep(P, p, q, k, g, beta, ws, s);
+  uint8_t* sv = static_cast<uint8_t*>(saved);
+  // the per-chunk blocks: into the full-form saved set for the backward, else the workspace
+  uint8_t* kb = sv && P.form == 3 ? sv + P.s_cb : ws + P.o_cb;
+  st = run_kda_prep(P, p, q, k, g, beta, kb, ws, s);
   if (st != GDN_OK) return st;
   Tables t = tables_at(P, ws);
-  uint8_t* sv = static_cast<uint8_t*>(saved);
   ScanArgs sa;
   memset(&sa, 0, sizeof(sa));
   if (!make_tmap(&sa.tq, q, P.T, P.H) || !make_tmap(&sa.tk, k, P.T, P.H) || !make_tmap(&sa.tv, v, P.T, P.HV))
     return GDN_ERR_CUDA;
   sa.kda = 1;
-  sa.cb = ws + P.o_cb;
+  sa.cb = kb;
   sa.chunk_tok0 = t.chunk_tok0;
   sa.chunk_len = t.chunk_len;
   sa.seg_c0 = t.seg_c0;
@@ -659,7 +665,7 @@ static gdn_status run_kda_fwd(const Plan& P, const gdn_problem* p, const void* q
   if (!make_tmap(&oa.to, o, P.T, P.HV)) return GDN_ERR_CUDA;
   oa.tape = sa.tape;
   oa.vn = sa.vn;
-  oa.kb = ws + P.o_cb;
+  oa.kb = kb;
   oa.chunk_tok0 = t.chunk_tok0;
   oa.chunk_len = t.chunk_len;
   oa.o = static_cast<__nv_bfloat16*>(o);

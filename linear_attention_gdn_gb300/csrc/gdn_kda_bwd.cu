@@ -805,7 +805,7 @@ void setup_kda_bwd_attrs() {
 }
 
 gdn_status run_kda_prep(const Plan& P, const gdn_problem* p, const void* q, const void* k, const float* g,
-                        const float* beta, uint8_t* ws, cudaStream_t s);
+                        const float* beta, uint8_t* kb, uint8_t* ws, cudaStream_t s);
 
 static gdn_status run_kda_bwd(const Plan& P, const gdn_problem& pr, const void* q, const void* k, const void* v,
                               const float* g, const float* beta, const int32_t* cu_dev, const void* dO,
@@ -815,13 +815,17 @@ static gdn_status run_kda_bwd(const Plan& P, const gdn_problem& pr, const void* 
   if (st != GDN_OK) return st;
   launch_check_saved(P, pr, saved, ws, s);
   if (P.NC == 0) return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
-  // the per-chunk blocks again (the replay of the decay products and UT blocks), then the adjoint walks
-  st = run_kda_prep(P, &pr, q, k, g, beta, ws, s);
-  if (st != GDN_OK) return st;
-  st = run_bwd_walks(P, pr, q, k, dO, ws + P.o_cb, 1, saved, nullptr, nullptr, ws, s);
+  // the per-chunk blocks: the forward's, from a full-form saved set, else formed again (the replay of
+  // the decay products and UT blocks); then the adjoint walks
+  const uint8_t* sv = static_cast<const uint8_t*>(saved);
+  uint8_t* kb = P.form == 3 ? const_cast<uint8_t*>(sv) + P.s_cb : ws + P.o_cb;
+  if (P.form != 3) {
+    st = run_kda_prep(P, &pr, q, k, g, beta, kb, ws, s);
+    if (st != GDN_OK) return st;
+  }
+  st = run_bwd_walks(P, pr, q, k, dO, kb, 1, saved, nullptr, nullptr, ws, s);
   if (st != GDN_OK) return st;
   Tables t = tables_at(P, ws);
-  const uint8_t* sv = static_cast<const uint8_t*>(saved);
   KdaGradArgs ga;
   memset(&ga, 0, sizeof(ga));
   if (!make_tmap(&ga.tq, q, P.T, P.H) || !make_tmap(&ga.tk, k, P.T, P.H) || !make_tmap(&ga.tv, v, P.T, P.HV) ||
@@ -829,7 +833,7 @@ static gdn_status run_kda_bwd(const Plan& P, const gdn_problem& pr, const void* 
     return GDN_ERR_CUDA;
   ga.g = g;
   ga.beta = beta;
-  ga.kb = ws + P.o_cb;
+  ga.kb = kb;
   ga.tape = sv + P.s_tape;
   ga.dtape = ws + P.o_dtape;
   ga.vn = sv + P.s_vn;

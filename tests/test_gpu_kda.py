@@ -54,9 +54,9 @@ def oracle_kda(w, d, with_grad=False, chunk_states=False):
     return out, tape
 
 
-def run_kda_fwd(w, d, save=True):
+def run_kda_fwd(w, d, save=True, saved_form=0):
     import linear_attention_gdn_gb300 as gdn
-    prob = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm, w.segments)
+    prob = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm, w.segments, saved_form=saved_form)
     buf = gdn.Buffers(prob, w.cu_seqlens, fill=255, kda=True)
     o = torch.full((w.T, w.HV, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
     gdn.gdn_kda_fwd(prob, d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_dev"], w.cu_seqlens, o,
@@ -131,9 +131,9 @@ def test_kda_gate_range_refused():
     assert st2 == 0
 
 
-def run_kda_fwd_bwd(w, d):
+def run_kda_fwd_bwd(w, d, saved_form=0):
     import linear_attention_gdn_gb300 as gdn
-    prob, buf, o, st = run_kda_fwd(w, d)
+    prob, buf, o, st = run_kda_fwd(w, d, saved_form=saved_form)
     assert st == 0
     dq = torch.full((w.T, w.H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
     dk = torch.full_like(dq, float("nan"))
@@ -192,6 +192,48 @@ def test_kda_backward_rejects_a_gdn_saved_set():
                     dq, dk, dv, dg, dbeta, ws)
     assert gdn.gdn_device_status(ws) == 4
     assert torch.isnan(dg).all() and torch.isnan(dq.float()).all()
+
+
+@pytest.mark.parametrize("name,w", [KDA_CASES[1], KDA_CASES[3]], ids=[KDA_CASES[1][0], KDA_CASES[3][0]])
+def test_kda_replay_form_matches_full_form(name, w):
+    """The full saved form keeps the forward's per-chunk blocks for the backward; the replay form
+    forms them again in the backward with the same kernel on the same inputs: o and every gradient
+    agree bit for bit (ragged documents; a split document, whose merges read M_seg)."""
+    import linear_attention_gdn_gb300 as gdn
+    d = to_dev(inputs.generate_kda(w, "cpu", with_grad=True))
+    full, st_f = run_kda_fwd_bwd(w, d, saved_form=gdn.SAVED_FULL)
+    rep, st_r = run_kda_fwd_bwd(w, d, saved_form=gdn.SAVED_REPLAY)
+    assert st_f == 0 and st_r == 0
+    for n in full:
+        assert torch.equal(full[n], rep[n]), n
+    pf = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm, w.segments, saved_form=gdn.SAVED_FULL)
+    pr = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm, w.segments, saved_form=gdn.SAVED_REPLAY)
+    assert gdn.gdn_kda_saved_bytes(pf, w.cu_seqlens)[0] > gdn.gdn_kda_saved_bytes(pr, w.cu_seqlens)[0]
+
+
+def test_kda_backward_rejects_the_other_saved_form():
+    """A replay-form saved set given to a full-form backward (and the reverse) is refused on the device
+    with GDN_ERR_SAVED_MISMATCH; no gradient is written."""
+    import linear_attention_gdn_gb300 as gdn
+    w = KDA_CASES[0][1]
+    d = to_dev(inputs.generate_kda(w, "cpu", with_grad=True))
+    for fwd_form, bwd_form in ((gdn.SAVED_REPLAY, gdn.SAVED_FULL), (gdn.SAVED_FULL, gdn.SAVED_REPLAY)):
+        prob_f, buf, o, st = run_kda_fwd(w, d, saved_form=fwd_form)
+        assert st == 0
+        prob_b = gdn.problem(w.T, w.N, w.H, w.HV, w.scale, w.l2norm, w.segments, saved_form=bwd_form)
+        s_b, ws_b = gdn.gdn_kda_saved_bytes(prob_b, w.cu_seqlens)
+        saved = torch.zeros(max(s_b, buf.saved.numel()), dtype=torch.uint8, device="cuda")
+        saved[:buf.saved.numel()].copy_(buf.saved)
+        ws = torch.zeros(ws_b, dtype=torch.uint8, device="cuda")
+        dq = torch.full((w.T, w.H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        dk = torch.full_like(dq, float("nan"))
+        dv = torch.full((w.T, w.HV, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        dg = torch.full((w.T, w.HV, 128), float("nan"), dtype=torch.float32, device="cuda")
+        dbeta = torch.full((w.T, w.HV), float("nan"), dtype=torch.float32, device="cuda")
+        gdn.gdn_kda_bwd(prob_b, d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_dev"], w.cu_seqlens, d["dO"],
+                        saved, dq, dk, dv, dg, dbeta, ws)
+        assert gdn.gdn_device_status(ws) == 4
+        assert torch.isnan(dg).all() and torch.isnan(dq.float()).all()
 
 
 def test_kda_uniform_decay_backward_matches_gdn():

@@ -132,16 +132,18 @@ def test_conv1d_problem_checks_and_workspace():
 
 
 def test_kda_saved_and_workspace_bytes():
-    """The per-channel-decay entry points: saved = header + (BF16 state + BF16 V_new^T) per chunk and
-    value head (the decay products and UT blocks are recomputed); the workspace holds the per-chunk
-    blocks (82,944 B each) and the backward's tapes."""
+    """The per-channel-decay entry points: the full form's saved set = header + (BF16 state + BF16
+    V_new^T + the 82,944-byte block of decay products and UT tiles) per chunk and value head; the
+    replay form leaves the blocks out (the backward forms them again).  The workspace holds the
+    per-chunk blocks and the backward's tapes in either form."""
     p = gdn.problem(320, 2, 2, 4)
     saved, ws = gdn.gdn_kda_saved_bytes(p, [0, 128, 320])
-    assert saved == 4096 + 5 * 4 * (32768 + 16384)
+    assert saved == 4096 + 5 * 4 * (32768 + 16384 + 82944)
     assert ws >= 5 * 4 * (82944 + 32768 + 16384)
-    # saved_form does not change the KDA layout
     p2 = gdn.problem(320, 2, 2, 4, saved_form=gdn.SAVED_REPLAY)
-    assert gdn.gdn_kda_saved_bytes(p2, [0, 128, 320]) == (saved, ws)
+    saved2, ws2 = gdn.gdn_kda_saved_bytes(p2, [0, 128, 320])
+    assert saved2 == 4096 + 5 * 4 * (32768 + 16384)
+    assert ws2 == ws
 
 
 def test_kda_invalid_arguments_refused_before_launch():
