@@ -39,7 +39,7 @@
 namespace gdn {
 
 struct KdaGradArgs {
-  CUtensorMap tq, tk, tv, tdo, tg;
+  CUtensorMap tq, tk, tv, tdo, tg, tdg;
   const float* g;
   const float* beta;
   const uint8_t* kb;      // [NC][HV][KB_BYTES] (T, M^T)
@@ -240,6 +240,7 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
     const int hv = j * a.G + hh;
     const size_t blk = (size_t)c * a.HV + hv;
     if (tid == 0) {   // this value head's tiles
+      bulk_wait_read();   // the last value head's dg copy has read its staging tile
       const uint8_t* kbp = a.kb + blk * KB_BYTES;
       // the 64 g rows first, on their own barrier (rows past L are read as zero below): the decay
       // cumsum runs while the rest lands
@@ -719,10 +720,16 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
         const int cb = c0 + 16 * h;
         float dg[16];
         tld16c(KGT_DG + cb, dg);
+        if (L == CH) {   // staged as FP32 [64 tokens][128] over the dead tiles, then one TMA store
+          float* dgs = reinterpret_cast<float*>(X);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int r = cb + e;
-          if (r < L) a.dg[((size_t)(tok0 + r) * a.HV + hv) * D + i] = dg[e] + add;
+          for (int e = 0; e < 16; ++e) dgs[(cb + e) * D + i] = dg[e] + add;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int r = cb + e;
+            if (r < L) a.dg[((size_t)(tok0 + r) * a.HV + hv) * D + i] = dg[e] + add;
+          }
         }
       }
       if (tid < L) {
@@ -734,9 +741,14 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
         a.dbeta[(size_t)(tok0 + tid) * a.HV + hv] = db;
       }
     }
+    if (L == CH) fence_async_smem();   // the staged dg, for the copy below
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (L == CH && tid == 0) {   // (the next value head's loads wait for it to have read its tile)
+      tma_store_3d(&a.tdg, X, 0, hv, tok0);
+      bulk_commit();
+    }
   }
   if (ok) {  // ---- item end: the L2-norm backward of the group sums dq^, dk^; dq, dk
     const int i = lt;
@@ -787,6 +799,7 @@ __global__ void __launch_bounds__(KG_THREADS, 1) kda_grad_kernel(const __grid_co
       a.dk[((size_t)(tok0 + r) * a.H + j) * D + i] = __float2bfloat16_rn(ok2);
     }
   }
+  if (tid == 0) bulk_wait_all();   // the last dg copy out of shared memory
   if (tid == 0 && !ok) {   // error path (bounded waits): nothing may land in or read this CTA's memory
     if (mma_pend) mbar_drain(&bar_m, mph);
     if (ld_pend) {
@@ -829,7 +842,8 @@ static gdn_status run_kda_bwd(const Plan& P, const gdn_problem& pr, const void* 
   KdaGradArgs ga;
   memset(&ga, 0, sizeof(ga));
   if (!make_tmap(&ga.tq, q, P.T, P.H) || !make_tmap(&ga.tk, k, P.T, P.H) || !make_tmap(&ga.tv, v, P.T, P.HV) ||
-      !make_tmap(&ga.tdo, dO, P.T, P.HV) || !make_tmap_g(&ga.tg, g, P.T, P.HV))
+      !make_tmap(&ga.tdo, dO, P.T, P.HV) || !make_tmap_g(&ga.tg, g, P.T, P.HV) ||
+      !make_tmap_g(&ga.tdg, dg, P.T, P.HV))
     return GDN_ERR_CUDA;
   ga.g = g;
   ga.beta = beta;
