@@ -135,9 +135,9 @@ gdn_status make_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
   P->cu_hash = h;
   // workspace
   size_t off = 256;   // control block (error word)
-  const int counts[17] = {P->N + 1, P->N + 1, P->N + 1, NC, NC, NC, NSEG, NSEG, NSEG, NSEG, NSEG, nsplit,
-                          nsdoc + 1, P->N + 1, NSEG - nsdoc, NSEG - nsdoc, 0};
-  for (int i = 0; i < 17; ++i) {
+  const int counts[19] = {P->N + 1, P->N + 1, P->N + 1, NC, NC, NC, NSEG, NSEG, NSEG, NSEG, NSEG, nsplit,
+                          nsdoc + 1, P->N + 1, NSEG - nsdoc, NSEG - nsdoc, NSEG - nsdoc, NSEG - nsdoc, 0};
+  for (int i = 0; i < 19; ++i) {
     P->o_tables[i] = off;
     off = align_up(off + (size_t)counts[i] * 4, 256);
   }
@@ -288,7 +288,7 @@ static const char* const kKernelNames[K_NUM] = {
     "merge_kernel",       "fwd_scan_kernel",    "check_saved_kernel", "bwd_scan_kernel(walk)",
     "merge_bwd_kernel",   "bwd_scan_kernel",    "grad_kernel",        "passthrough_kernel",
     "conv_fwd_kernel",    "conv_bwd_kernel(+reduce)", "vnew_kernel",      "kda_prep_kernel",
-    "kda_out_kernel",     "kda_grad_kernel"};
+    "kda_out_kernel",     "kda_grad_kernel",    "walk_order_kernel"};
 struct ProfRec {
   int id;
   cudaEvent_t e0, e1;

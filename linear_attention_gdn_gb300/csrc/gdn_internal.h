@@ -76,6 +76,9 @@ struct Tables {
                        //        the transfer walks, from its true start)
   int* bwalk_seg;      // [NSEG - nsdoc] segments whose full reverse walk runs after the backward
                        //        merge: all but the last segment of each split document
+                       // (both in longest-first order: the walks' CTAs take them in list order)
+  int* fwalk_doc;      // [NSEG - nsdoc] the same two lists in segment order, from which the ordered
+  int* bwalk_doc;      //        ones are made
 };
 
 // Hash of one cu_seqlens entry (document d ends at token `end`): murmur3's
@@ -215,7 +218,7 @@ struct Plan {
   int sms;   // SMs of the current device (persistent grids)
   uint32_t cu_hash;
   // workspace offsets (bytes)
-  size_t o_tables[17];
+  size_t o_tables[19];
   size_t o_cb, o_bend, o_sinit, o_mend_ws;
   size_t o_dtape, o_dvn, o_dbend, o_dsinit;   // backward
   size_t o_vnb;                               // backward, replay form: recomputed V_new^T tiles
@@ -227,10 +230,10 @@ struct Plan {
 
 inline Tables tables_at(const Plan& P, uint8_t* ws) {
   Tables t;
-  int** f[16] = {&t.chunk_offsets, &t.seg_offsets, &t.split_offsets, &t.chunk_doc,    &t.chunk_tok0, &t.chunk_len,
+  int** f[18] = {&t.chunk_offsets, &t.seg_offsets, &t.split_offsets, &t.chunk_doc,    &t.chunk_tok0, &t.chunk_len,
                  &t.seg_doc,       &t.seg_c0,      &t.seg_c1,        &t.seg_idx,      &t.seg_split,  &t.split_seg,
-                 &t.sdoc_first,    &t.sdoc_offsets, &t.fwalk_seg,    &t.bwalk_seg};
-  for (int i = 0; i < 16; ++i) *f[i] = reinterpret_cast<int*>(ws + P.o_tables[i]);
+                 &t.sdoc_first,    &t.sdoc_offsets, &t.fwalk_seg,    &t.bwalk_seg,    &t.fwalk_doc,  &t.bwalk_doc};
+  for (int i = 0; i < 18; ++i) *f[i] = reinterpret_cast<int*>(ws + P.o_tables[i]);
   return t;
 }
 

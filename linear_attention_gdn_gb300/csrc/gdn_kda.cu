@@ -545,7 +545,7 @@ gdn_status make_kda_plan(const gdn_problem* p, const int32_t* cu, Plan* P) {
   P->form = full ? 3 : 2;
   const size_t units = (size_t)P->NC * P->HV;
   const size_t st_f32 = (size_t)P->nsplit * P->HV * STATE_F32 * 4;
-  size_t off = kda_align(P->o_tables[16], 1024);
+  size_t off = kda_align(P->o_tables[18], 1024);
   P->o_cb = off;
   off += units * KB_BYTES;
   P->o_bend = off;

@@ -9,6 +9,8 @@
 // from cu_seqlens ("feat(cake_gdn_kcp) ... #8172" page, commit note on the
 // backend's fifth table); their contents are not printed, so these tables are
 // this library's own definition.
+#include <algorithm>
+
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "gdn_prof.h"
@@ -158,10 +160,39 @@ __global__ void __launch_bounds__(256) tables_fill_kernel(TableArgs a) {
     a.t.seg_split[i] = sp;
     // the segments walked in full after the merges: in the forward all but a split document's first
     // segment, in the backward all but its last (those walk from their true start / end with the
-    // transfer walks); both lists keep segment order
+    // transfer walks); both lists in segment order here, longest first after walk_order_kernel
     const int sd = a.t.sdoc_offsets[d];
-    if (!(P > 1 && p == 0)) a.t.fwalk_seg[i - sd - (P > 1 ? 1 : 0)] = i;
-    if (!(P > 1 && p == P - 1)) a.t.bwalk_seg[i - sd] = i;
+    if (!(P > 1 && p == 0)) a.t.fwalk_doc[i - sd - (P > 1 ? 1 : 0)] = i;
+    if (!(P > 1 && p == P - 1)) a.t.bwalk_doc[i - sd] = i;
+  }
+}
+
+// The full walks' segment lists in longest-first order, stable among equal lengths (a walk's length is
+// its chunk count).  With more chains than SMs, the walks' CTAs start in list order: longest first
+// leaves the short chains for the last wave, where segment order can leave a long document's chains
+// to start after the others and end late (the classic longest-processing-time-first rule).
+// blockIdx.y selects the list (0 forward, 1 backward); each thread ranks one entry by counting the
+// entries ahead of it; lists longer than WO_MAX keep segment order.
+constexpr int WO_MAX = 8192;
+__global__ void __launch_bounds__(256) walk_order_kernel(Tables t, int n, const int* err) {
+  __shared__ int len_s[WO_MAX];
+  if (*(volatile const int*)err) return;
+  const int* src = blockIdx.y == 0 ? t.fwalk_doc : t.bwalk_doc;
+  int* dst = blockIdx.y == 0 ? t.fwalk_seg : t.bwalk_seg;
+  if (n > WO_MAX) {
+    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < n; k += gridDim.x * blockDim.x) dst[k] = src[k];
+    return;
+  }
+  for (int k = threadIdx.x; k < n; k += blockDim.x) len_s[k] = t.seg_c1[src[k]] - t.seg_c0[src[k]];
+  __syncthreads();
+  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < n; k += gridDim.x * blockDim.x) {
+    const int lk = len_s[k];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) {
+      const int lj = len_s[j];
+      rank += (lj > lk || (lj == lk && j < k)) ? 1 : 0;
+    }
+    dst[rank] = src[k];
   }
 }
 
@@ -174,6 +205,12 @@ void launch_tables(const TableArgs& a, cudaStream_t s) {
     prof_begin(K_TABLES_FILL, s);
     tables_fill_kernel<<<(n + 255) / 256, 256, 0, s>>>(a);
     prof_end(K_TABLES_FILL, s);
+  }
+  const int nw = a.NSEG - a.nsdoc;
+  if (nw > 0) {
+    prof_begin(K_WALK_ORDER, s);
+    walk_order_kernel<<<dim3((unsigned)std::min((nw + 255) / 256, 64), 2), 256, 0, s>>>(a.t, nw, a.err);
+    prof_end(K_WALK_ORDER, s);
   }
 }
 
