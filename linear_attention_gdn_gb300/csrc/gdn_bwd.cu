@@ -644,9 +644,13 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
   // Consecutive arrivals on each are separated by a wait on a commit the MMA warp makes after
   // consuming the earlier one, so no phase is passed before its waiter saw it.
   // go_kq: the next item's Q, K load went out (the dq / dk accumulator columns are free); kq_bar:
-  // the item's KK^T / QK^T products are in those columns
+  // the item's KK^T / QK^T products are in those columns.
+  // go_cp[3]: the compute warpgroups tell the MMA warp that MB, M4, M5 of a value head have
+  // completed (their regions are dead), for the dv store and the next value head's loads.  Each is
+  // arrived once per value head, and the next value head's arrivals wait for loads the MMA warp
+  // issues after seeing all three.
   __shared__ uint64_t bar_qk, bar_vn, bar_sv, bar_do, bar_dt, bar_ma, mma_bar, go_mma, go_ma, go_kq, kq_bar,
-      done_mma;
+      done_mma, go_cp[3];
   __shared__ uint32_t tslot;
   __shared__ __align__(16) float rq[CH], rk[CH];
   // gates of the current and the next value head (double-buffered)
@@ -656,7 +660,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
   __shared__ float colC[2][4][CH];             // column sums of C (dAqk . Aqk, dA . A) per quarter
   __shared__ float rowC[GK_NWG][CH], rowB[GK_NWG][CH], sdot[GK_THREADS / 32];
   __shared__ float zpart[2], wtot[2];
-  __shared__ float lq[CH], lk[CH];             // per-token L2-norm backward factors
+  __shared__ __align__(16) float lq[CH], lk[CH];   // per-token L2-norm backward factors
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wg = tid >> 7, w4 = warp & 3;
   const int row = w4 * 32 + lane;          // TMEM lane / M = 128 row of this thread
@@ -679,6 +683,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
     mbar_init(&go_kq, 1);
     mbar_init(&kq_bar, 1);
     mbar_init(&done_mma, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&go_cp[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   __syncthreads();
@@ -832,7 +837,9 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
     if (warp == 4) gates(0, j * a.G, tok0, a.chunk_len[c]);
   }
   if (tid >= GK_THREADS) {
-    // ================= MMA warpgroup: its first warp issues MA, MB, M5 and M6 of every value head ====
+    // ================= MMA warpgroup: its first warp issues MA, MB, M5 and M6 of every value head, and
+    // (one lane) the dv store and the next value head's loads, each as soon as the product that last
+    // reads the region has completed: the copies stay off the compute warpgroups' path ====
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(GK_REG_MMA));
     if (warp == GK_THREADS / 32) {
       uint32_t gph = 0, gaph = 0, gkph = 0, qph = 0, hcm = 0;
@@ -883,12 +890,45 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
           for (int ks = 0; ks < 4; ++ks)
             mma_ss_w(tb + GT_A2, desc_k(s_wd, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
           mma_commit_w(&mma_bar);
+          // the value head after this one: the next in the group, else the next item's first
+          const int c = item % a.NC, tok0 = a.chunk_tok0[c], hv = (item / a.NC) * a.G + h;
+          const bool has_next = h + 1 < a.G || nxt < n_items;
+          int nc = c, nhv = hv + 1, ntok0 = tok0;
+          if (h + 1 == a.G && nxt < n_items) {
+            nc = nxt % a.NC;
+            nhv = (nxt / a.NC) * a.G;
+            ntok0 = a.chunk_tok0[nc];
+          }
+          if (!(live = mbar_wait(&go_cp[0], vph, a.err))) break;   // MB done: S, dS', V, scalars dead
+          if (lane == 0) {
+            if (L == CH) {   // dv, staged in the V_new^T region
+              tma_store_3d(&a.tdv, sm + GK_VN, 0, hv, tok0);
+              tma_store_3d(&a.tdv, sm + GK_VN + 8192, 64, hv, tok0);
+              bulk_commit();
+            }
+            if (has_next) issue_sv(nc, nhv, ntok0);
+          }
+          __syncwarp();
+          if (!(live = mbar_wait(&go_cp[1], vph, a.err))) break;   // M4 done: dO (H1, H2), dT dead
+          if (lane == 0 && has_next) {
+            issue_do(nhv, ntok0);
+            issue_dvn(nc, nhv);
+            bulk_wait_read();   // the dv store has read the V_new^T region
+            issue_vn(nc, nhv);
+          }
+          __syncwarp();
           // M5: T^T R1 (= -dA, M = 64)
           if (!go()) break;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             mma_ss_w(tb + GT_A0, desc_mn(s_t, 64, ks), desc_mn(s_r1, 64, ks), idesc(64, 64, 1, 1), ks > 0);
           mma_commit_w(&mma_bar);
+          if (!(live = mbar_wait(&go_cp[2], vph, a.err))) break;   // M5 done: T dead
+          if (lane == 0 && has_next) {   // (the next head recomputed: fewer registers live across M5)
+            const bool in_group = h + 1 < a.G;
+            issue_t(in_group ? c : nxt % a.NC, in_group ? hv + 1 : (nxt / a.NC) * a.G);
+          }
+          __syncwarp();
           // M6: K^T F1 + K^T F2 (+= dk^T), waited for at the end of the item (every later commit
           // of this warp covers it); then the next value head's MA when its chunk is full, each
           // part as soon as its tiles have landed
@@ -900,7 +940,6 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
           for (int ks = 0; ks < 4; ++ks)
             mma_ss_w(tb + GT_DK, desc_mn(s_k, 64, ks), desc_mn(s_f2, 64, ks), idesc(128, 64, 1, 1), 1u);
           if (h + 1 == a.G) mma_commit_w(&mma_bar);
-          const bool has_next = h + 1 < a.G || nxt < n_items;
           const int nL = h + 1 < a.G ? L : (nxt < n_items ? a.chunk_len[nxt % a.NC] : 0);
           pend = has_next && nL == CH;
           if (pend) {
@@ -914,6 +953,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
         }
       }
       mma_commit_w(&done_mma);   // arrives once every MMA this warp issued has completed
+      if (lane == 0) bulk_wait_all();   // the dv stores
     }
     return;
   }
@@ -1133,14 +1173,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
         tmem_wait_st();
       }
       if (!(ok = mma_sync_wait())) break;
-      if (tid == 0) {
-        if (full) {
-          tma_store_3d(&a.tdv, sm + GK_VN, 0, hv, tok0);
-          tma_store_3d(&a.tdv, sm + GK_VN + 8192, 64, hv, tok0);
-          bulk_commit();
-        }
-        if (has_next) issue_sv(nc, nhv, ntok0);   // S, dS', V, scalars are dead from here on
-      }
+      if (tid == 0) mbar_arrive(&go_cp[0]);   // the MMA warp: the dv store, the next S, dS', V, scalars
       // The M = 64 token-pair passes spread each 16 x 16 block over the whole warp:
       // this thread takes rows rb0, rb0 + 8 and columns cbl, cbl + 1, cbl + 8, cbl + 9.
       const int rb0 = w4 * 16 + (lane >> 2), cbl = cb0 + 2 * (lane & 3);
@@ -1264,12 +1297,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
         }
       }
       if (!(ok = mma_sync_wait())) break;
-      if (tid == 0 && has_next) {
-        issue_do(nhv, ntok0);   // the dO region (H1, H2) is dead
-        issue_dvn(nc, nhv);     // and the dV_new^T region (dT)
-        bulk_wait_read();       // the dv store has read the V_new^T region
-        issue_vn(nc, nhv);
-      }
+      if (tid == 0) mbar_arrive(&go_cp[1]);   // the next dO, dV_new^T, V_new^T
       {  // H4: R1 -> shared for M5
         uint32_t u[8];
         tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A5 + cb0), u);
@@ -1301,7 +1329,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
         tmem_wait_st();
       }
       if (!(ok = mma_sync_wait())) break;
-      if (tid == 0 && has_next) issue_t(nc, nhv);   // T is dead
+      if (tid == 0) mbar_arrive(&go_cp[2]);   // the next T
       {  // H5: dA rows -> F1, F2 for M6; dbeta row terms; dA . A -> column sums of C
         uint32_t u[8];
         tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A0 + cb0), u);
@@ -1437,7 +1465,8 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
     tc_fence_before();   // the TMEM reads of DQ / DK precede the next item's table MMAs
     named_bar(GK_BAR, GK_THREADS);
     if (tid == 0 && nxt < n_items) mbar_arrive(&go_kq);
-    if (tid < CH) {      // d|x|/dx . g = (g - x (x . g) / |x|^2) / |x|: the per-token factor (x . g) / |x|^3
+    // d|x|/dx . g = (g - x (x . g) / |x|^2) / |x|: the per-token factor (x . g) / |x|^3
+    if (a.l2norm && tid < CH) {
       float xq = 0.f, xk = 0.f;
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
@@ -1448,21 +1477,34 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
       lq[tid] = xq * nq * nq * nq;
       lk[tid] = xk * nk * nk * nk;
     }
-    named_bar(GK_BAR, GK_THREADS);
+    if (a.l2norm) named_bar(GK_BAR, GK_THREADS);
     {
       const bool full = L == CH;   // full chunk: staged tiles and TMA stores
       uint8_t* sq_tile = sm + GK_WD;   // both regions are dead until the next item's first value head
       uint8_t* sk_tile = sm + GK_KQ;
       __nv_bfloat16* dqp = a.dq + ((size_t)tok0 * a.H + j) * D + row;
       __nv_bfloat16* dkp = a.dk + ((size_t)tok0 * a.H + j) * D + row;
+      if (a.l2norm) {   // this thread's columns' per-token factors, four columns per 16-byte load
+#pragma unroll
+        for (int i = 0; i < GK_CW / 4; ++i) {
+          const float4 rq4 = *reinterpret_cast<const float4*>(rq + cb0 + 4 * i);
+          const float4 lq4 = *reinterpret_cast<const float4*>(lq + cb0 + 4 * i);
+          const float4 rk4 = *reinterpret_cast<const float4*>(rk + cb0 + 4 * i);
+          const float4 lk4 = *reinterpret_cast<const float4*>(lk + cb0 + 4 * i);
+          const float fq[4] = {rq4.x, rq4.y, rq4.z, rq4.w}, gq[4] = {lq4.x, lq4.y, lq4.z, lq4.w};
+          const float fk[4] = {rk4.x, rk4.y, rk4.z, rk4.w}, gk[4] = {lk4.x, lk4.y, lk4.z, lk4.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int e = 4 * i + k;
+            xq[e] = fq[k] * xq[e] - __uint_as_float(qk2[e] << 16) * gq[k];
+            xk[e] = fk[k] * xk[e] - __uint_as_float(qk2[e] & 0xffff0000u) * gk[k];
+          }
+        }
+      }
 #pragma unroll
       for (int e = 0; e < GK_CW; ++e) {
         const int cc = cb0 + e;
-        float outq = xq[e], outk = xk[e];
-        if (a.l2norm) {
-          outq = rq[cc] * xq[e] - __uint_as_float(qk2[e] << 16) * lq[cc];
-          outk = rk[cc] * xk[e] - __uint_as_float(qk2[e] & 0xffff0000u) * lk[cc];
-        }
+        const float outq = xq[e], outk = xk[e];
         if (full) {
           *reinterpret_cast<__nv_bfloat16*>(sq_tile + sw_off(cc, row, 64)) = __float2bfloat16_rn(outq);
           *reinterpret_cast<__nv_bfloat16*>(sk_tile + sw_off(cc, row, 64)) = __float2bfloat16_rn(outk);
