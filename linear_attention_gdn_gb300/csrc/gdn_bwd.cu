@@ -809,16 +809,19 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
       mma_ss_w(tb + GT_A3, desc_mn(s_ds, 128, ks), desc_mn(s_vn, 128, ks), idesc(128, 64, 1, 1), ks > 0);
     }
   };
+  // (bar_ma covers the products the first pass reads; dV_new V^T, read after MB, goes out last and
+  // is covered by MB's commit)
   auto issue_ma2 = [&]() {
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
+    for (int ks = 0; ks < 8; ++ks)
       mma_ss_w(tb + GT_A0, desc_mn(s_s, 128, ks), desc_mn(s_dv, 128, ks), idesc(128, 64, 1, 1), ks > 0);
-      mma_ss_w(tb + GT_A5, desc_mn(s_dv, 128, ks), desc_k(s_v, 64, ks), idesc(64, 64, 1, 0), ks > 0);
-    }
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
       mma_ss_w(tb + GT_A2, desc_k(s_dv, 128, ks), desc_mn(s_t, 64, ks), idesc(128, 64, 0, 1), ks > 0);
     mma_commit_w(&bar_ma);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      mma_ss_w(tb + GT_A5, desc_mn(s_dv, 128, ks), desc_k(s_v, 64, ks), idesc(64, 64, 1, 0), ks > 0);
   };
 
   uint32_t hc = 0;                      // value heads done by this CTA (phase of the per-head loads)
