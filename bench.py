@@ -276,6 +276,41 @@ def replica_rate(world, tokens_per_replica, ms_per_step):
     return world * tokens_per_replica / ms_per_step / 1e3
 
 
+def parse_cpulist(text):
+    """CPU ids of a sysfs cpulist ("0-3,8,10-11")."""
+    cpus = set()
+    for part in text.strip().split(","):
+        if part:
+            a, _, b = part.partition("-")
+            cpus |= set(range(int(a), int(b or a) + 1))
+    return cpus
+
+
+def bind_gpu_local_cpus(dev):
+    """Run this process on the host cores next to the GPU (sysfs local_cpulist of its PCI
+    function), so that the pinned host buffers of the end-to-end pass are allocated on the
+    memory node the GPU's link reaches directly.  A process-local setting (the caller puts the
+    previous set back with os.sched_setaffinity); returns what was done, or why not."""
+    import torch
+    pr = torch.cuda.get_device_properties(dev)
+    ids = [getattr(pr, k, None) for k in ("pci_domain_id", "pci_bus_id", "pci_device_id")]
+    if any(v is None for v in ids):
+        return {"cpus": "unchanged", "why": "no PCI id from the runtime"}
+    path = "/sys/bus/pci/devices/%04x:%02x:%02x.0" % tuple(ids)
+    try:
+        local = parse_cpulist(open(path + "/local_cpulist").read())
+        node = open(path + "/numa_node").read().strip()
+    except OSError:
+        return {"cpus": "unchanged", "why": "no sysfs entry " + path}
+    mine = os.sched_getaffinity(0)
+    use = local & mine
+    if not use:
+        return {"cpus": "unchanged", "why": "no GPU-local core in this process's set", "numa_node": node}
+    if use != mine:
+        os.sched_setaffinity(0, use)
+    return {"cpus": len(use), "of": len(mine), "numa_node": node}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -505,6 +540,8 @@ def run_ours(args, rank, world, local_rank):
         # sets) and step i - 1's results come out on another while step i runs; events order every
         # buffer reuse.
         names_in = ("q", "k", "v", "g", "beta", "dO")
+        cpus_before = os.sched_getaffinity(0)
+        host_binding = bind_gpu_local_cpus(dev)   # before the pinned buffers are allocated
         h_in = {n: x[n].to("cpu").pin_memory() for n in names_in}
         h_cu = torch.from_numpy(w.cu_seqlens).pin_memory()
         d_in = [{n: torch.empty_like(x[n]) for n in names_in} for _ in range(2)]
@@ -564,12 +601,13 @@ def run_ours(args, rank, world, local_rank):
         run_e2e(ke, e0, e1)
         barrier()
         ms_e2e = allmax(max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3) / ke)
+        os.sched_setaffinity(0, cpus_before)
         st = gdn.gdn_device_status(buf.workspace, stream)
         assert st == 0, gdn.gdn_status_string(st)
         e2e = {"value": round(replica_rate(world, w.T, ms_e2e), 3), "unit": UNIT, "h2d_bytes_per_step": int(bi),
                "d2h_bytes_per_step": int(bo), "ms_per_step": round(ms_e2e, 3),
                "overlap": "step i+1's host-to-device and step i-1's device-to-host copies run on two copy streams "
-                          "while step i computes"}
+                          "while step i computes", "host_cpus": host_binding}
 
     if rank != 0:
         return None
