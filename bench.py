@@ -193,10 +193,16 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(["nvidia-smi"] + (["-i", str(self.gpu)] if self.gpu else []) +
                                          [f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200"],
+                                          "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            # nvidia-smi takes a while to start: wait for its first sample (up to 5 s) and keep
+            # only the samples taken from here on, i.e. during the timed region
+            t0 = time.time()
+            while not self.lines and self.proc.poll() is None and time.time() - t0 < 5:
+                time.sleep(0.01)
+            self.lines.clear()
         except Exception:
             self.proc = None
         return self
