@@ -43,7 +43,7 @@ C = 64
 # products of the chunked algorithm, KK^T and QK^T once per q/k head, the O(C^3)
 # inverse not counted; bytes = the method's inputs read once, its outputs
 # written once and the BF16 state saved every 64 tokens written once and read
-# once).  Per full chunk and value head this is the scope table's count:
+# once).  Per full chunk and value head this is the method's count:
 #   fwd  F_f = HV (6 d^2 + 6 C d) + H (4 C d) FLOP / token,
 #        57,728 B / token at (16, 48): q, k, v, g, beta in; o, states out
 #   bwd  F_b = HV (14 d^2 + 24 C d) + H (4 C d) FLOP / token,
@@ -100,7 +100,7 @@ KERNEL_METHOD_TENSORS = {
 
 
 def kernel_bytes(name, w):
-    """Method bytes of one launch of `name` (the scope table's tensors it reads or writes)."""
+    """Method bytes of one launch of `name` (the method's tensors it reads or writes)."""
     m = method_tensors(w)
     return sum(m[t] for t in KERNEL_METHOD_TENSORS.get(name, ()))
 
@@ -528,7 +528,7 @@ def run_ours(args, rank, world, local_rank):
                            "GB_per_s": round(nbytes / (t_c * 1e-3) / 1e9, 1),
                            "Mtokens_per_s": round(replica_rate(world, w.T, t_c), 3)}
         del cx, cdy, cy, cdx
-        # fwd+bwd of the scope table's other full-size workloads (8,192-token document; ~156 log-uniform
+        # fwd+bwd of the other full-size workloads (8,192-token document; ~156 log-uniform
         # documents of 262,144 tokens with L2 off; one 524,288-token document split into segments)
         for widx in (1, 3, 4):
             if widx != args.workload:
@@ -618,10 +618,14 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
     pk = peaks()
+    probe = tensor_probe(gdn, torch, dev, stream)
     kt = {k: v for k, v in kstats.items() if v["timed_launches"] > 0}
     top = max(kt, key=lambda k: kt[k]["total_ms"])
     per_launch_ms = kt[top]["total_ms"] / kt[top]["timed_launches"]
     roof = roofline(top, w, per_launch_ms, pk)
+    k_tflops = kernel_flops(top, w) / (per_launch_ms * 1e-3) / 1e12
+    roof.update({"tensor_frac_of_probe": round(k_tflops / probe["tflops"], 4),
+                 "tensor_frac_of_nominal": round(k_tflops / NOMINAL_BF16_TFLOPS, 4)})
     tot = sum(u["total_ms"] for u in kt.values())
     kernels = {}
     for k, v in kt.items():
@@ -642,14 +646,47 @@ def run_ours(args, rank, world, local_rank):
                    "l2_flush": f"none needed: {in_gb:.1f} GB of inputs per step exceed the 129 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "tflops": round(tflops, 1), "tensor_frac_of_step": round(tflops / pk["bf16_tflops_sustained"], 4),
+        "tensor_frac_of_step_probe": round(tflops / probe["tflops"], 4),
+        "tensor_frac_of_step_nominal": round(tflops / NOMINAL_BF16_TFLOPS, 4), "tensor_probe": probe,
         "step_method_GB_per_s": round(step_gbs, 1), "hbm_frac_of_step": round(step_gbs / pk["hbm_gbs"], 4),
         "roofline": roof, "kernels": kernels, "gpu_launches": n_launch, "clocks": clk.summary(),
         "e2e": e2e, "ops": extra,
     }
 
 
+NOMINAL_BF16_TFLOPS = 2250.0   # the vendor's dense BF16 tensor-core figure for one GB300
+
+
+def tensor_probe(gdn, torch, dev, stream, reps=3, iters=200000):
+    """The library's tensor-pipe probe (one CTA per SM issuing M = 128, N = 256, K = 16 BF16 tcgen05
+    products on operands resident in shared memory): best of `reps` launches, in TFLOP/s, with the SM
+    clocks sampled while it runs."""
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    gdn.gdn_tensor_probe(200, err, stream)   # warm-up (module load, clocks)
+    best = 0.0
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    with ClockSampler(uuid) as clk:
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fl = gdn.gdn_tensor_probe(iters, err, stream)
+            e1.record(stream)
+            e1.synchronize()
+            best = max(best, fl / e0.elapsed_time(e1) / 1e9)
+    assert int(err.item()) == 0, "tensor probe: a bounded wait ran out"
+    return {"tflops": round(best, 1), "nominal_tflops": NOMINAL_BF16_TFLOPS,
+            "what": "tcgen05 BF16 M128 N256 K16 products back to back, operands resident in shared memory, "
+                    "one CTA per SM, FP32 accumulation in TMEM",
+            "iters": iters, "reps": reps, "clocks": clk.summary()}
+
+
 def roofline(kernel, w, launch_ms, pk):
-    """The roofline object of one kernel: method FLOPs and bytes of one launch (the scope table's per-token
+    """The roofline object of one kernel: method FLOPs and bytes of one launch (the method's per-token
     counts over the workload's real chunks) over its measured launch time, against the binding roof (the
     larger of the two time floors at those counts)."""
     fl, by = kernel_flops(kernel, w), kernel_bytes(kernel, w)
@@ -671,7 +708,7 @@ def roofline(kernel, w, launch_ms, pk):
                  "tensor_frac": round(fl / (launch_ms * 1e-3) / 1e12 / pk["bf16_tflops_sustained"], 4),
                  "hbm_frac": round(by / (launch_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
                  "traffic_over_method_bytes": round(traffic / by, 3) if traffic and by else None,
-                 "counting": "method FLOPs / bytes per the scope table's per-token counts (real chunk lengths); "
+                 "counting": "method FLOPs / bytes per the method's per-token counts (real chunk lengths); "
                              "the design's own intermediate tapes are not credited (traffic shows them)"})
     return roof
 

@@ -365,6 +365,21 @@ int gdn_profile_read(gdn_kernel_stat *out, int max_entries);
  */
 int32_t gdn_plan_segment_chunks(const gdn_problem *prob, const int32_t *cu_seqlens_host);
 
+/*
+ * Tensor-pipe probe, for the roofline's own BF16 peak: the benchmark reports
+ * tensor-core fractions against the vendor's dense figure and against the rate
+ * this probe measures with the library's own tcgen05 code.  Launches one CTA per SM of
+ * the current device on `stream`; each issues iters x 4 BF16 tcgen05 products
+ * of M = 128, N = 256, K = 16 (FP32 accumulation in TMEM) on operand tiles
+ * that stay in shared memory, so no memory traffic competes with the tensor
+ * cores.  *flops receives the products' FLOP count (2 M N K each); the caller
+ * times the launch with events on `stream` and reads *dev_err (a device int,
+ * zero on entry) afterwards: nonzero means a bounded wait ran out.
+ * iters: 1 .. 2^20.  Returns GDN_ERR_INVALID_ARG outside that range or for a
+ * null pointer, GDN_ERR_CUDA if the launch fails; nothing is allocated.
+ */
+gdn_status gdn_tensor_probe(int32_t iters, int32_t *dev_err, double *flops, struct CUstream_st *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,7 @@ EXPORTS = ("gdn_saved_bytes", "gdn_fwd", "gdn_bwd", "gdn_ckpt_fwd_bwd", "gdn_sta
            "gdn_device_status", "gdn_plan_segment_chunks", "gdn_chunk_table_offsets", "gdn_profile_enable",
            "gdn_profile_read", "gdn_fwd_noalloc", "gdn_fwd_states", "gdn_bwd_states", "gdn_conv1d_workspace_bytes",
            "gdn_conv1d_fwd", "gdn_conv1d_bwd", "gdn_backward_tape_offsets", "gdn_kda_saved_bytes", "gdn_kda_fwd",
-           "gdn_kda_bwd")
+           "gdn_kda_bwd", "gdn_tensor_probe")
 SAVED_FULL, SAVED_REPLAY = 0, 1   # gdn_problem.saved_form
 
 
@@ -90,6 +90,8 @@ def _load():
     for name in ("gdn_conv1d_workspace_bytes", "gdn_conv1d_fwd", "gdn_conv1d_bwd", "gdn_fwd_states",
                  "gdn_bwd_states"):
         getattr(L, name).restype = ctypes.c_int
+    L.gdn_tensor_probe.argtypes = [ctypes.c_int32, vp, ctypes.POINTER(ctypes.c_double), vp]
+    L.gdn_tensor_probe.restype = ctypes.c_int
     L.gdn_profile_enable.argtypes = [ctypes.c_int]
     L.gdn_profile_enable.restype = None
     L.gdn_profile_read.argtypes = [ctypes.POINTER(gdn_kernel_stat), ctypes.c_int]
@@ -292,6 +294,15 @@ def gdn_profile_read_all() -> dict:
 
 def gdn_device_status(workspace, stream=None) -> int:
     return int(lib.gdn_device_status(_ptr(workspace), _stream(stream)))
+
+
+def gdn_tensor_probe(iters, dev_err, stream=None) -> float:
+    """Launch the tensor-pipe probe (include/gdn.h) on `stream`; dev_err is a zeroed device int32
+    tensor.  Returns the FLOP count of the launch (the caller times it)."""
+    flops = ctypes.c_double(0.0)
+    _check(lib.gdn_tensor_probe(int(iters), _ptr(dev_err), ctypes.byref(flops), _stream(stream)),
+           "gdn_tensor_probe")
+    return flops.value
 
 
 # ---------------------------------------------------------------------------
