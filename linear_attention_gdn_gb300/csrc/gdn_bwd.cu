@@ -1191,7 +1191,8 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
         tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A5 + cb0), u1);   // dV_new V^T
         tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A0 + cb0), u2);   // dW K^T
         tmem_wait_ld();
-        const float qr2[2] = {rq[rb0], rq[rb0 + 8]}, eR2[2] = {eR[rb0], eR[rb0 + 8]};
+        // scale rq of the two rows (the scale folded into the row factor), the row gate factors
+        const float qr2[2] = {a.scale * rq[rb0], a.scale * rq[rb0 + 8]}, eR2[2] = {eR[rb0], eR[rb0 + 8]};
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
           const int c0_ = cbl + 8 * hb;
@@ -1200,10 +1201,11 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
                        gg2 = *reinterpret_cast<const float2*>(gg + c0_), eI2 = *reinterpret_cast<const float2*>(eI + c0_);
           const float rkc[2] = {rk2.x, rk2.y}, bbc[2] = {bb2.x, bb2.y}, eIc[2] = {eI2.x, eI2.y};
           const float bgk[2] = {bb2.x * gg2.x * rk2.x, bb2.y * gg2.y * rk2.y};
+          const float srk[2] = {a.scale * rk2.x, a.scale * rk2.y};
 #pragma unroll
           for (int hr = 0; hr < 2; ++hr) {
             const int r = rb0 + 8 * hr;
-            const float qr = qr2[hr];
+            const float sqr = qr2[hr];
             const float2 qk = *reinterpret_cast<const float2*>(KQ + r * GK_KQLD + c0_);
             const float2 tt = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sm + GK_T + sw_off(r, c0_, 64)));
             float h1[2], h2[2], dt[2];
@@ -1212,12 +1214,12 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
               const int i = hb * 4 + hr * 2 + e, cc = c0_ + e;
               const bool live = cc <= r && r < L;
               const float gam = live ? (sfac ? eR2[hr] * eIc[e] : exp2f(Gb[r] - Gb[cc])) : 0.f;
-              const float dA = live ? a.scale * __uint_as_float(u0[i]) : 0.f;
-              const float cm = dA * gam * qr * rkc[e] * (e ? qk.y : qk.x);
+              const float gd = live ? gam * __uint_as_float(u0[i]) : 0.f;   // gamma (dO V_new^T)
+              h1[e] = srk[e] * gd;
+              h2[e] = sqr * gd;
+              const float cm = h2[e] * (rkc[e] * (e ? qk.y : qk.x));
               rs[hr] += cm;
               cs[hb * 2 + e] += cm;
-              h1[e] = rkc[e] * gam * dA;
-              h2[e] = qr * gam * dA;
               const float v1 = __uint_as_float(u1[i]), v2 = __uint_as_float(u2[i]), tv = e ? tt.y : tt.x;
               dt[e] = fmaf(bgk[e], v2, bbc[e] * v1);
               tb1[hb * 2 + e] = fmaf(tv, v1, tb1[hb * 2 + e]);
@@ -1354,12 +1356,12 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
               const int i = hb * 4 + hr * 2 + e, cc = c0_ + e;
               const bool live = cc < r && r < L;
               const float gam = live ? (sfac ? eR2[hr] * eIc[e] : exp2f(Gb[r] - Gb[cc])) : 0.f;
-              const float dA = live ? -__uint_as_float(u[i]) : 0.f;
+              const float gd = live ? -gam * __uint_as_float(u[i]) : 0.f;   // gamma dA
               const float kk = live ? KQ[cc * GK_KQLD + r] : 0.f;   // KK^T[r][cc], kept above the diagonal
-              const float base = dA * gam * rkr * rkc[e] * kk;      // dA . (A / beta_r)
+              const float base = gd * (rkr * rkc[e]) * kk;          // dA . (A / beta_r)
               rbv[hr] += base;
-              cs[hb * 2 + e] += br * base;
-              const float E = dA * br * gam;
+              cs[hb * 2 + e] = fmaf(br, base, cs[hb * 2 + e]);
+              const float E = br * gd;
               f1[e] = rkc[e] * E;
               f2[e] = rkr * E;
             }
