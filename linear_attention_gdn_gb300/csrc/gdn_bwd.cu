@@ -1088,12 +1088,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
         float w[GK_CW];
         tld2(GT_A0, w, GT_A2, x);
 #pragma unroll
-        for (int q4 = 0; q4 < GK_CW / 8; ++q4) {
-          float t8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) t8[e] = -w[q4 * 8 + e];
-          store_chunk8(sm + GK_WD, row, (cb0 >> 3) + q4, 128, t8);
-        }
+        for (int q4 = 0; q4 < GK_CW / 8; ++q4) store_chunk8(sm + GK_WD, row, (cb0 >> 3) + q4, 128, w + q4 * 8);
       }
       // ---- MB: dW K^T (M = 64), Y^T = dW^T T, issued by the MMA warp
       handoff_to_mma_warp(&go_mma);
@@ -1221,7 +1216,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
               rs[hr] += cm;
               cs[hb * 2 + e] += cm;
               const float v1 = __uint_as_float(u1[i]), v2 = __uint_as_float(u2[i]), tv = e ? tt.y : tt.x;
-              dt[e] = fmaf(bgk[e], v2, bbc[e] * v1);
+              dt[e] = fmaf(-bgk[e], v2, bbc[e] * v1);
               tb1[hb * 2 + e] = fmaf(tv, v1, tb1[hb * 2 + e]);
               tb2[hb * 2 + e] = fmaf(tv, v2, tb2[hb * 2 + e]);
             }
@@ -1269,7 +1264,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
             const int cc = cbl + (k >> 1) * 8 + (k & 1);
             colC[0][w4][cc] = cs[k];
             part[0][w4][cc] = tb1[k];
-            part[3][w4][cc] = rk[cc] * tb2[k];
+            part[3][w4][cc] = rk[cc] * -tb2[k];
           }
         }
         float y[GK_CW], z[GK_CW];
@@ -1325,10 +1320,10 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
         for (int i = 0; i < 4; ++i) {
           const float4 b4 = *reinterpret_cast<const float4*>(bb + cb0 + 4 * i);
           const float4 g4 = *reinterpret_cast<const float4*>(gg + cb0 + 4 * i);
-          ak[4 * i + 0] = fmaf(b4.x * g4.x, yv[4 * i + 0], ak[4 * i + 0]);
-          ak[4 * i + 1] = fmaf(b4.y * g4.y, yv[4 * i + 1], ak[4 * i + 1]);
-          ak[4 * i + 2] = fmaf(b4.z * g4.z, yv[4 * i + 2], ak[4 * i + 2]);
-          ak[4 * i + 3] = fmaf(b4.w * g4.w, yv[4 * i + 3], ak[4 * i + 3]);
+          ak[4 * i + 0] = fmaf(-(b4.x * g4.x), yv[4 * i + 0], ak[4 * i + 0]);
+          ak[4 * i + 1] = fmaf(-(b4.y * g4.y), yv[4 * i + 1], ak[4 * i + 1]);
+          ak[4 * i + 2] = fmaf(-(b4.z * g4.z), yv[4 * i + 2], ak[4 * i + 2]);
+          ak[4 * i + 3] = fmaf(-(b4.w * g4.w), yv[4 * i + 3], ak[4 * i + 3]);
         }
         tmem_st16(taddr(tb, w4 * 32, GT_DK + cb0), ak);
         tmem_wait_st();
