@@ -350,10 +350,21 @@ __global__ void __launch_bounds__(SC_THREADS, 1) fwd_scan_kernel(const __grid_co
         for (int q = 0; q < 4; ++q) {
           uint32_t ps[8], pn[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
+          for (int e = 0; e < 8; e += 2) {
             const int r = q * 16 + 2 * e;
             pn[e] = pack_bf16(vn[r], vn[r + 1]);
-            ps[e] = KDA ? pn[e] : pack_bf16(vn[r] * kd[r], vn[r + 1] * kd[r + 1]);
+            pn[e + 1] = pack_bf16(vn[r + 2], vn[r + 3]);
+            if (KDA) {
+              ps[e] = pn[e];
+              ps[e + 1] = pn[e + 1];
+            } else {
+              const float4 k4 = *reinterpret_cast<const float4*>(kd + r);
+              float t0, t1, t2, t3;
+              mul2v(t0, t1, vn[r], vn[r + 1], k4.x, k4.y);
+              mul2v(t2, t3, vn[r + 2], vn[r + 3], k4.z, k4.w);
+              ps[e] = pack_bf16(t0, t1);
+              ps[e + 1] = pack_bf16(t2, t3);
+            }
           }
           tmem_st8(taddr(tb, wq * 32, TM_AVS + q * 8), ps);
           if (with_o) tmem_st8(taddr(tb, wq * 32, TM_AVN + q * 8), pn);
