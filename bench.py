@@ -485,8 +485,7 @@ def run_ours(args, rank, world, local_rank):
     kstats = gdn.gdn_profile_read_all()
     prof_steps = args.steps + 1
 
-    # (the end-to-end pass runs before the extra timings below: run after them, with their device
-    # buffers still cached, it measured 129 ms per step against 56 ms)
+    # (the end-to-end pass runs right after the main timing, before the extra timings below)
     # end to end through the C ABI with pinned host buffers: every step copies
     # its inputs in and all of its outputs back
     e2e = None
