@@ -621,7 +621,8 @@ __device__ __forceinline__ void store_chunk8(uint8_t* tile, int r, int c8, int R
 // block.  Per value head:
 //   MA  S dV_new^T (= -dW^T), S dO^T, X^T = dV_new^T T, dKd^T = dS' V_new^T,
 //       dO V_new^T (-> dAqk), dV_new V^T                       (44 MMAs)
-//   MB  dW K^T, Y^T = dW^T T
+//   MB  -dW K^T, -Y^T = -dW^T T   (the tile holds S dV_new^T as MA left it: HB and
+//       H4 read the two products with the sign flipped)
 //   M4  R1 = dT T^T, K^T H1 (+= dq^T), Q^T H2 (+= dk^T)
 //   M5  T^T R1 (= -dA)
 //   M6  K^T F1 + K^T F2 (+= dk^T)
@@ -631,7 +632,8 @@ __device__ __forceinline__ void store_chunk8(uint8_t* tile, int r, int c8, int R
 // group reads, hands off, and does its side work (dv, column-scaled dq / dk
 // terms, per-token partial sums) while that group runs.  The next value
 // head's tiles (the next item's first value head after the last one) are
-// requested as soon as the buffers they land in are dead, and its MA is issued
+// requested by one lane of the MMA warp as soon as the buffers they land in are
+// dead (the compute warpgroups arrive on an mbarrier after MB and after M4), and its MA is issued
 // right after M6 (the products of V_new^T, S, dS', dO as soon as those tiles
 // land, then those of dV_new^T and T), so that it runs under the per-token
 // totals (warps 2-3) and the next gate scan (warp 4).  The next item's
@@ -884,7 +886,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
             issue_ma1();
             issue_ma2();
           }
-          // MB: dW K^T (M = 64), Y^T = dW^T T
+          // MB: -dW K^T (M = 64), -Y^T = -dW^T T (the tile holds -dW^T)
           if (!go()) break;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
@@ -1082,7 +1084,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
       const float* gg = gs[gb];
       const float* eR = eGr[gb];
       const float* eI = eGi[gb];
-      // HA: dW^T = -(S dV_new^T) -> shared for MB; X^T kept for the side work
+      // HA: S dV_new^T (= -dW^T) -> shared for MB, unnegated; X^T kept for the side work
       float x[GK_CW];
       {
         float w[GK_CW];
@@ -1090,7 +1092,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
 #pragma unroll
         for (int q4 = 0; q4 < GK_CW / 8; ++q4) store_chunk8(sm + GK_WD, row, (cb0 >> 3) + q4, 128, w + q4 * 8);
       }
-      // ---- MB: dW K^T (M = 64), Y^T = dW^T T, issued by the MMA warp
+      // ---- MB: -dW K^T (M = 64), -Y^T = -dW^T T, issued by the MMA warp
       handoff_to_mma_warp(&go_mma);
       const bool full = L == CH;   // full chunk: dv goes out as a staged tile (TMA store)
       {  // HA side work: dv; the column-scaled terms pg S dO^T into dq^T and dec dKd^T into dk^T (TMEM
@@ -1184,7 +1186,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
         uint32_t u0[8], u1[8], u2[8];
         tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A4 + cb0), u0);   // dO V_new^T
         tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A5 + cb0), u1);   // dV_new V^T
-        tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A0 + cb0), u2);   // dW K^T
+        tmem_ld_m64_async(taddr(tb, w4 * 32, GT_A0 + cb0), u2);   // -dW K^T (sign flipped where used)
         tmem_wait_ld();
         // scale rq of the two rows (the scale folded into the row factor), the row gate factors
         const float qr2[2] = {a.scale * rq[rb0], a.scale * rq[rb0 + 8]}, eR2[2] = {eR[rb0], eR[rb0 + 8]};
@@ -1315,7 +1317,7 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
       handoff_to_mma_warp(&go_mma);
       {  // H4 side work: beta gamma Y^T into dk^T (TMEM: M4 is done, M6 not yet issued)
         float yv[GK_CW], ak[GK_CW];
-        tld2(GT_A2, yv, GT_DK, ak);   // Y^T = dW^T T (rows = dk index)
+        tld2(GT_A2, yv, GT_DK, ak);   // -Y^T = -dW^T T (rows = dk index; sign flipped below)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float4 b4 = *reinterpret_cast<const float4*>(bb + cb0 + 4 * i);
