@@ -605,6 +605,14 @@ __device__ __forceinline__ float colsum16(float (&v)[16], int lane) {
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
+// Error path (bounded): wait for whatever copy may still be landing on `bar`.  Of the two parities
+// one is the phase completed last (no wait), the other the current one: it completes when a copy
+// armed on it lands, else its wait runs out.
+__device__ __forceinline__ void drain_copies(uint64_t* bar) {
+  mbar_drain(bar, 0);
+  mbar_drain(bar, 1);
+}
+
 __device__ __forceinline__ void store_chunk8(uint8_t* tile, int r, int c8, int R, const float* x) {
   uint4 w;
   w.x = pack_bf16(x[0], x[1]);
@@ -959,6 +967,12 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
       }
       mma_commit_w(&done_mma);   // arrives once every MMA this warp issued has completed
       if (lane == 0) bulk_wait_all();   // the dv stores
+      if (!live && lane == 0) {   // error path: the loads this warp issued land before the CTA's memory goes
+        drain_copies(&bar_sv);
+        drain_copies(&bar_do);
+        drain_copies(&bar_vn);
+        drain_copies(&bar_dt);
+      }
     }
     return;
   }
@@ -1531,8 +1545,17 @@ __global__ void __launch_bounds__(GK_LAUNCH, 1) grad_kernel(const __grid_constan
     it_L = nx_L;
   }
   if (tid == 0) bulk_wait_all();
-  // no MMA of the MMA warp may be left in flight (an MA for a value head that never ran included)
-  if (tid == 0) mbar_wait(&done_mma, 0, a.err);
+  if (!ok && tid == 0) {   // error path: the loads this thread issued (Q, K of the next item, the first
+                           // value head's tiles) land before the CTA's memory goes
+    drain_copies(&bar_qk);
+    drain_copies(&bar_vn);
+    drain_copies(&bar_sv);
+    drain_copies(&bar_do);
+    drain_copies(&bar_dt);
+  }
+  // no MMA of the MMA warp may be left in flight (an MA for a value head that never ran included);
+  // on the error path too, whatever the error word says (bounded)
+  if (tid == 0 && !mbar_wait(&done_mma, 0, a.err)) mbar_drain(&done_mma, 0);
   tc_fence_before();
   named_bar(GK_BAR, GK_THREADS);
   if (warp == 0) tmem_dealloc(tb, 512);
