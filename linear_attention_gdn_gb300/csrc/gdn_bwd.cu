@@ -492,7 +492,16 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_kernel(const __grid_co
     }
     if (tid == 0) {
       bulk_wait_all();
-      mbar_wait(&done, 0, a.err);   // no MMA may outlive the TMEM allocation
+      // no MMA may outlive the TMEM allocation, and no tile copy the CTA's shared memory: on the error
+      // path both are waited for whatever the error word says (bounded; a barrier phase nothing
+      // armed just runs out)
+      if (!mbar_wait(&done, 0, a.err)) {
+        mbar_drain(&done, 0);
+        for (int b = 0; b < 2; ++b) {
+          mbar_drain(&full_bar[b], 0);
+          mbar_drain(&full_bar[b], 1);
+        }
+      }
     }
   }
   tc_fence_before();
