@@ -344,7 +344,17 @@ __global__ void __launch_bounds__(CV_THREADS) conv_bwd_kernel(const __grid_const
   bs.init();
   for (int st = 0; st < nst; ++st) {
     if (threadIdx.x == 0 && st + CV_NS - 1 < nst) issue(st + CV_NS - 1);   // into the slot freed last
-    if (!__syncthreads_and(mbar_wait(&full[st % CV_NS], (st / CV_NS) & 1, a.err))) return;
+    if (!__syncthreads_and(mbar_wait(&full[st % CV_NS], (st / CV_NS) & 1, a.err))) {
+      // error path (bounded): the copies still landing in the other slots land before the CTA's memory
+      // goes (of a slot's two phase parities one completed last; the other completes when its copy
+      // lands, else its wait runs out)
+      if (threadIdx.x == 0)
+        for (int i = 0; i < CV_NS; ++i) {
+          mbar_drain(&full[i], 0);
+          mbar_drain(&full[i], 1);
+        }
+      return;
+    }
     const uint8_t* base = cv_sm + (st % CV_NS) * STAGE + threadIdx.x * 8;
     if (on) {
 #pragma unroll
