@@ -508,7 +508,9 @@ def run_ours(args, rank, world, local_rank):
         bi = sum(t.numel() * t.element_size() for t in h_in.values()) + w.cu_seqlens.nbytes
         bo = sum(t.numel() * t.element_size() for t in h_out)
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of set b landed
+        ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of set b landed (fwd+bwd: all but dO)
+        ev_in2 = [torch.cuda.Event() for _ in range(2)]    # fwd+bwd: dO of set b landed
+        ev_fwd = [torch.cuda.Event() for _ in range(2)]    # fwd+bwd: the forward of set b finished
         ev_used = [torch.cuda.Event() for _ in range(2)]   # the step on set b finished
         ev_out = [torch.cuda.Event() for _ in range(2)]    # results of set b copied out
 
@@ -524,6 +526,11 @@ def run_ours(args, rank, world, local_rank):
                 gdn.gdn_ckpt_fwd_bwd(prob, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu, w.cu_seqlens,
                                      xx["dO"], oo, *gr, buf.saved, buf.workspace, stream=stream)
 
+        # fwd+bwd: the forward starts once its own inputs are in (dO follows on the same copy stream)
+        # and o goes out as soon as the forward is done, so the first and last steps of the pass
+        # overlap their copies with compute too
+        split = op == "fwd+bwd"
+
         def run_e2e(K, e_start=None, e_end=None):
             if e_start is not None:
                 e_start.record(s_in)
@@ -534,16 +541,32 @@ def run_ours(args, rank, world, local_rank):
                         s_in.wait_event(ev_used[b])
                     d_cu[b].copy_(h_cu, non_blocking=True)
                     for n in names_in:
-                        d_in[b][n].copy_(h_in[n], non_blocking=True)
+                        if not (split and n == "dO"):
+                            d_in[b][n].copy_(h_in[n], non_blocking=True)
                     ev_in[b].record(s_in)
+                    if split:
+                        d_in[b]["dO"].copy_(h_in["dO"], non_blocking=True)
+                        ev_in2[b].record(s_in)
                 stream.wait_event(ev_in[b])
                 if i >= 2:
                     stream.wait_event(ev_out[b])
-                step_on(b)
+                if split:
+                    xx, cu, (oo, *gr) = d_in[b], d_cu[b], outs[b]
+                    gdn.gdn_fwd(prob, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu, w.cu_seqlens, oo,
+                                buf.saved, buf.workspace, stream=stream)
+                    ev_fwd[b].record(stream)
+                    stream.wait_event(ev_in2[b])
+                    gdn.gdn_bwd(prob, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu, w.cu_seqlens, xx["dO"],
+                                buf.saved, *gr, buf.workspace, stream=stream)
+                else:
+                    step_on(b)
                 ev_used[b].record(stream)
                 with torch.cuda.stream(s_out):
+                    if split:
+                        s_out.wait_event(ev_fwd[b])
+                        h_out[0].copy_(outs[b][0], non_blocking=True)   # o
                     s_out.wait_event(ev_used[b])
-                    for hb, dbuf in zip(h_out, outs[b]):
+                    for hb, dbuf in list(zip(h_out, outs[b]))[1 if split else 0:]:
                         hb.copy_(dbuf, non_blocking=True)
                     ev_out[b].record(s_out)
             if e_end is not None:
@@ -563,7 +586,8 @@ def run_ours(args, rank, world, local_rank):
         e2e = {"value": round(replica_rate(world, w.T, ms_e2e), 3), "unit": UNIT, "h2d_bytes_per_step": int(bi),
                "d2h_bytes_per_step": int(bo), "ms_per_step": round(ms_e2e, 3),
                "overlap": "step i+1's host-to-device and step i-1's device-to-host copies run on two copy streams "
-                          "while step i computes", "host_cpus": host_binding}
+                          "while step i computes; the forward starts once its own inputs are in and o goes out "
+                          "once the forward is done", "host_cpus": host_binding}
 
     extra = {}
     if not args.quick:
