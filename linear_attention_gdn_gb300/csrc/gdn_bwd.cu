@@ -375,8 +375,14 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_kernel(const __grid_co
       // early, else after it
       auto w_hop = [&]() {
         float w[64];
-        tmem_ld32(taddr(tb, warp * 32, BT_DW), w);
-        tmem_ld32(taddr(tb, warp * 32, BT_DW + 32), w + 32);
+        {
+          uint32_t r[4][16];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tmem_ld16_async(taddr(tb, warp * 32, BT_DW + 16 * k), r[k]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) as_float16(r[k], w + 16 * k);
+        }
         uint8_t* wt = sm + BS_W;
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
@@ -404,8 +410,18 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_kernel(const __grid_co
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           float x[32], y[32];
-          tmem_ld32(taddr(tb, warp * 32, BT_DX + h * 32), x);
-          tmem_ld32(taddr(tb, warp * 32, BT_DY + h * 32), y);
+          {
+            uint32_t r[4][16];
+            tmem_ld16_async(taddr(tb, warp * 32, BT_DX + h * 32), r[0]);
+            tmem_ld16_async(taddr(tb, warp * 32, BT_DX + h * 32 + 16), r[1]);
+            tmem_ld16_async(taddr(tb, warp * 32, BT_DY + h * 32), r[2]);
+            tmem_ld16_async(taddr(tb, warp * 32, BT_DY + h * 32 + 16), r[3]);
+            tmem_wait_ld();
+            as_float16(r[0], x);
+            as_float16(r[1], x + 16);
+            as_float16(r[2], y);
+            as_float16(r[3], y + 16);
+          }
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             uint32_t p8[8];
@@ -449,24 +465,36 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_kernel(const __grid_co
       tc_fence_after();
       {
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          float x[32];
-          tmem_ld32(taddr(tb, warp * 32, BT_DS + h * 32), x);
-          if (KDA) {   // column i (key channel) of dS'^T decays by gamma_L[i]
+        for (int h2 = 0; h2 < 2; ++h2) {   // 64 columns per TMEM wait
+          float x64[64];
+          {
+            uint32_t r[4][16];
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              const float4 gv = *reinterpret_cast<const float4*>(glc + h * 32 + e);
-              fma2v(x[e], x[e + 1], gv.x, gv.y, dS[h * 32 + e], dS[h * 32 + e + 1]);
-              fma2v(x[e + 2], x[e + 3], gv.z, gv.w, dS[h * 32 + e + 2], dS[h * 32 + e + 3]);
-              dS[h * 32 + e] = x[e];
-              dS[h * 32 + e + 1] = x[e + 1];
-              dS[h * 32 + e + 2] = x[e + 2];
-              dS[h * 32 + e + 3] = x[e + 3];
+            for (int k = 0; k < 4; ++k) tmem_ld16_async(taddr(tb, warp * 32, BT_DS + h2 * 64 + 16 * k), r[k]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) as_float16(r[k], x64 + 16 * k);
+          }
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int h = 2 * h2 + hh;
+            float* x = x64 + 32 * hh;
+            if (KDA) {   // column i (key channel) of dS'^T decays by gamma_L[i]
+#pragma unroll
+              for (int e = 0; e < 32; e += 4) {
+                const float4 gv = *reinterpret_cast<const float4*>(glc + h * 32 + e);
+                fma2v(x[e], x[e + 1], gv.x, gv.y, dS[h * 32 + e], dS[h * 32 + e + 1]);
+                fma2v(x[e + 2], x[e + 3], gv.z, gv.w, dS[h * 32 + e + 2], dS[h * 32 + e + 3]);
+                dS[h * 32 + e] = x[e];
+                dS[h * 32 + e + 1] = x[e + 1];
+                dS[h * 32 + e + 2] = x[e + 2];
+                dS[h * 32 + e + 3] = x[e + 3];
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; e += 2)
+                fma2_to(dS[h * 32 + e], dS[h * 32 + e + 1], gL, dS[h * 32 + e], dS[h * 32 + e + 1], x[e], x[e + 1]);
             }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; e += 2)
-              fma2_to(dS[h * 32 + e], dS[h * 32 + e + 1], gL, dS[h * 32 + e], dS[h * 32 + e + 1], x[e], x[e + 1]);
           }
         }
         store_row128(ds_tile, tid, dS);
