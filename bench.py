@@ -221,7 +221,7 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -232,13 +232,17 @@ class ClockSampler:
                 mx.append(float(f[2]))
             except ValueError:
                 continue
+            try:
+                pw.append(float(f[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_max": max(pw) if pw else None}
 
 
 # ---------------------------------------------------------------------------
@@ -576,9 +580,10 @@ def run_ours(args, rank, world, local_rank):
         barrier()
         ke = max(3, args.steps)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0 = time.perf_counter()
-        run_e2e(ke, e0, e1)
-        barrier()
+        with ClockSampler(uuid) as clk_e2e:
+            t0 = time.perf_counter()
+            run_e2e(ke, e0, e1)
+            barrier()
         ms_e2e = allmax(max(e0.elapsed_time(e1), (time.perf_counter() - t0) * 1e3) / ke)
         os.sched_setaffinity(0, cpus_before)
         st = gdn.gdn_device_status(buf.workspace, stream)
@@ -587,7 +592,7 @@ def run_ours(args, rank, world, local_rank):
                "d2h_bytes_per_step": int(bo), "ms_per_step": round(ms_e2e, 3),
                "overlap": "step i+1's host-to-device and step i-1's device-to-host copies run on two copy streams "
                           "while step i computes; the forward starts once its own inputs are in and o goes out "
-                          "once the forward is done", "host_cpus": host_binding}
+                          "once the forward is done", "host_cpus": host_binding, "clocks": clk_e2e.summary()}
 
     extra = {}
     if not args.quick:
